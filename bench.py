@@ -1,0 +1,410 @@
+"""Benchmark of the drift-scoring / sparse-refresh step through libpolestar.
+
+A step is one pass of the whole path over one batch of synthetic input:
+spherical k-means (10 warm-started iterations), NVFP4 residuals, centroid
+keys + proxy attention + KL drift, top-k drifting clusters, sparse K/V
+refresh, and the commit over the current block.  Default workload: one
+LLaDA-8B-shaped layer (batch 1, window 1024, d 4096, 32 heads x 128, C 64,
+k 8, commit over 32 x 126464 logits).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl polestar|reference]
+
+Timing: device-side CUDA events on the launching stream, L2 flushed (512 MB
+write) between steps outside the timed events, W >= 3 warm-up steps; for N
+> 1 (torchrun) every rank runs an independent replica, the timed region is
+bracketed by barriers and the slowest rank's time counts.  `--impl
+reference` times the CPU oracle on the same workload (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "drift-refresh steps/s and window tokens/s; achieved HBM GB/s vs ~8 TB/s peak"
+DEFAULT_WORKLOAD = "llada8b_layer_n1024"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "drift_aware_kv_spherical_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 9
+                          for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm)}
+
+
+def op_work(w, npos_mean):
+    """Algorithmic bytes and flops of each op for one window batch."""
+    esz = 4 if w.dtype == "f32" else 2
+    B, N, d, C = w.B, w.N, w.d, w.C
+    H = B * N * d * esz
+    nkv = w.Hkv * w.dh
+    M = npos_mean * B
+    return {
+        "kmeans": ((w.iters + 1) * H, 2.0 * (w.iters + 1) * B * N * C * d),
+        "nvfp4": (H + B * N * d // 2 + B * N * d // 16, 0.0),
+        "proxy_kl": (d * nkv * esz + B * C * d * 4 + B * N * w.Hq * w.dh * esz + 2 * B * N * C * 4,
+                     2.0 * B * C * d * nkv + 2.0 * B * N * w.Hq * C * w.dh),
+        "topk": (B * N * 13, 0.0),
+        "refresh": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
+        "commit": (B * w.P * w.V * 4, 0.0),
+    }
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, timed on this host on the same workload."""
+    import numpy as np
+    import oracle
+    from drift_aware_kv_spherical_gb300 import workloads as wl
+
+    w = wl.BY_NAME[args.workload]
+    L = wl.make_layer(w, 0, "cpu")
+    H0 = L["H"]
+    Wk, Wv = L["Wk"].float().numpy(), L["Wv"].float().numpy()
+    Hs = [H0]
+    for t in range(1, 4):
+        Hs.append(wl.drift_rows(w, Hs[-1], t))
+    Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy() for H in Hs]
+    Hn = [H.float().numpy() for H in Hs]
+    logits = [wl.make_logits(w, t).numpy() for t in range(4)]
+    u = wl.make_uniforms(w).numpy()
+    mu = [oracle.kmeanspp_init(Hn[0][b], w.C, u[b])[0] for b in range(w.B)]
+    A_prev = [None] * w.B
+    chat = [None] * w.B
+    st = dict(s=np.zeros((w.B, w.P), np.float32), n=np.zeros((w.B, w.P), np.int32),
+              p=np.zeros((w.B, w.P), np.float32), u=np.ones((w.B, w.P), np.uint8))
+    role = np.zeros(w.P, np.uint8)
+    params = oracle.CommitParams(w.tau_s, w.alpha, w.ratio, w.mode, 1)
+    Kc = np.zeros((w.N, w.Hkv * w.dh), np.float32)
+
+    def step(t):
+        i = t % 4
+        for b in range(w.B):
+            r = oracle.kmeans_spherical(Hn[i][b], mu[b], w.iters, chat[b])
+            mu[b], chat[b] = r["mu"], r["chat"]
+            oracle.nvfp4_residual(Hn[i][b], r["mu"].astype(np.float32), r["assign"],
+                                  r["rho"].astype(np.float32))
+            Kt = oracle.centroid_keys(r["chat"], Wk)
+            A, D = oracle.proxy_attn_kl(Qs[i][b], Kt, w.Hq, w.Hkv, w.dh, A_prev[b])
+            A_prev[b] = A
+            sel = oracle.topk_drift(D.astype(np.float32), r["assign"], r["counts"], w.k)
+            oracle.refresh_kv(Hn[i][b], sel[2], sel[3], Wk, Wv, Kc, Kc, 0, w.dtype == "bf16")
+            if b == w.B - 1:
+                pass
+            c = oracle.commit_rule(logits[i][b], role, st["u"][b],
+                                   D[w.blk_start:w.blk_start + w.P].astype(np.float32),
+                                   st["s"][b], st["n"][b], st["p"][b], None, params)
+            st["s"][b], st["n"][b], st["p"][b], st["u"][b] = (c["d_sum"], c["d_cnt"],
+                                                              c["d_prev"], c["undecided"])
+
+    for t in range(args.warmup):
+        step(t)
+    t0 = time.perf_counter()
+    for t in range(args.steps):
+        step(args.warmup + t)
+    el = time.perf_counter() - t0
+    sps = args.steps / el
+    cores = _blas_threads()
+    sample = f"full steps of {w.name} (B={w.B}, every stage, fp64 numpy)"
+    line = {"impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": sps, "unit": "steps/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": sps, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "N": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
+            "dh": w.dh, "C": w.C, "iters": w.iters, "k": w.k, "P": w.P, "V": w.V,
+            "layers": 1, "l2": "flushed between steps (512 MB write)"}
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """One or more full oracle steps of the workload on the host cores."""
+    ns = argparse.Namespace(steps=1, warmup=0, workload=w.name, gpus=1)
+    import io
+    import contextlib
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        buf = io.StringIO()
+        with contextlib.redirect_stdout(buf):
+            run_reference(ns)
+        n += 1
+        if time.perf_counter() - t0 > budget_s / 4 or n >= 3:
+            break
+    line = json.loads(buf.getvalue())
+    v = line["value"]
+    return {"value": v, "unit": "steps/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"one full step of {w.name} per sample, fp64 numpy (BLAS threads), "
+                      f"{n} sample(s)"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import torch
+    import torch.distributed as dist
+    from drift_aware_kv_spherical_gb300 import polestar as ps
+    from drift_aware_kv_spherical_gb300 import workloads as wl
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    w = wl.BY_NAME[args.workload]
+    L = wl.make_layer(w, 0, dev)
+    Hs = [L["H"]]
+    for t in range(1, 4):
+        Hs.append(wl.drift_rows(w, Hs[-1], t))
+    Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
+    logits = [wl.make_logits(w, t, dev) for t in range(4)]
+    u = wl.make_uniforms(w, 0, dev)
+    pipe = Pipeline(w, layers=1, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # window build: k-means++ seeding, first distributions
+    pipe.step([Hs[0]], [Qs[0]], [L["Wk"]], [L["Wv"]], logits[0], init_us=[u], first=True)
+    ops = ["kmeans", "nvfp4", "proxy_kl", "topk", "refresh", "commit"]
+
+    def timed_step(t, ev):
+        i = t % 4
+        st = pipe.state[0]
+        cur, prev = st.A[pipe.t % 2], st.A[(pipe.t + 1) % 2]
+        H, Q = Hs[i], Qs[i]
+        ev[0].record(stream)
+        ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
+                               objective=st.obj, ws=pipe.ws[ps.OP_KMEANS])
+        ev[1].record(stream)
+        ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                             ws=pipe.ws[ps.OP_NVFP4])
+        ev[2].record(stream)
+        ps.ps_proxy_attn_kl(Q, st.chat, L["Wk"], prev, cur, st.D, w.Hkv,
+                            ws=pipe.ws[ps.OP_PROXY_KL])
+        ev[3].record(stream)
+        ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
+                         st.npos, st.posmask)
+        ev[4].record(stream)
+        ps.ps_refresh_kv(H, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh)
+        ev[5].record(stream)
+        pipe.commit_step(logits[i])
+        ev[6].record(stream)
+        pipe.t += 1
+
+    def mk():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+
+    for t in range(args.warmup):
+        flush.zero_()
+        timed_step(t, mk())
+    torch.cuda.synchronize()
+    ps.ps_check()
+
+    events = [mk() for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    npos_seen = []
+    for t in range(args.steps):
+        flush.zero_()
+        timed_step(args.warmup + t, events[t])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ps.ps_check()
+    npos_seen.append(int(pipe.state[0].npos.sum()))
+    per_step = [ev[0].elapsed_time(ev[6]) for ev in events]
+    per_op = {op: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, op in enumerate(ops)}
+    total_ms = sum(per_step)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    steps_per_s = world * args.steps / (total_ms / 1000.0)
+
+    # end to end through the public API: inputs from pinned host memory every
+    # step, the step's results read back
+    hH = [H.cpu().pin_memory() for H in Hs]
+    hQ = [Q.cpu().pin_memory() for Q in Qs]
+    hL = [x.cpu().pin_memory() for x in logits]
+    dH, dQ, dL = torch.empty_like(Hs[0]), torch.empty_like(Qs[0]), torch.empty_like(logits[0])
+    out = [torch.empty(pipe.token.shape, dtype=torch.int32).pin_memory(),
+           torch.empty(pipe.conf.shape).pin_memory(),
+           torch.empty(pipe.commit.shape, dtype=torch.uint8).pin_memory(),
+           torch.empty(pipe.state[0].D.shape).pin_memory()]
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for t in range(args.warmup + args.steps):
+        i = t % 4
+        if t >= args.warmup:
+            flush.zero_()
+            e2e_ev[t - args.warmup][0].record(stream)
+        dH.copy_(hH[i], non_blocking=True)
+        dQ.copy_(hQ[i], non_blocking=True)
+        dL.copy_(hL[i], non_blocking=True)
+        pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL)
+        out[0].copy_(pipe.token, non_blocking=True)
+        out[1].copy_(pipe.conf, non_blocking=True)
+        out[2].copy_(pipe.commit, non_blocking=True)
+        out[3].copy_(pipe.state[0].D, non_blocking=True)
+        if t >= args.warmup:
+            e2e_ev[t - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = sum(x.numel() * x.element_size() for x in (hH[0], hQ[0], hL[0]))
+    d2h = sum(x.numel() * x.element_size() for x in out)
+
+    # roofline of the dominant op
+    hbm, tf, src = peaks()
+    work = op_work(w, npos_seen[-1] / w.B)
+    rows = {}
+    for op in ops:
+        ms = statistics.mean(per_op[op])
+        by, fl = work[op]
+        bound = "tensor" if fl / (tf * 1e12) > by / (hbm * 1e9) else "hbm"
+        ach = (fl / (ms * 1e-3) / 1e12) if bound == "tensor" else (by / (ms * 1e-3) / 1e9)
+        peak = tf if bound == "tensor" else hbm
+        rows[op] = {"ms": ms, "bound": bound, "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": ach / peak,
+                    "alg_bytes": by, "alg_flops": fl}
+    top = max(ops, key=lambda o: rows[o]["ms"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("source_hash") == source_hash() and top in tj.get("per_launch_bytes", {}):
+            traffic = tj["per_launch_bytes"][top]
+    r = rows[top]
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "config": workload_config(w),
+        "window_tokens_per_s": steps_per_s * w.B * w.N,
+        "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
+                     "unit": r["unit"], "frac": r["frac"], "traffic": traffic,
+                     "op": top, "peak_source": src},
+        "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
+                for op in ops},
+        "clocks": clk,
+        "gpu_launches": pipe.kernel_launches_per_step() * args.steps,
+        "parallelism": f"replicas x{world}",
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

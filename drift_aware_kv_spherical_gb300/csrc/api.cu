@@ -1,0 +1,245 @@
+// The C ABI of libpolestar: handle management, argument validation,
+// workspace sizing and dispatch to the kernels.  Declarations and the
+// meaning of every argument are in include/polestar.h.
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "ops.h"
+
+using namespace ps;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define PS_REQUIRE(cond) \
+  do {                   \
+    if (!(cond)) return PS_ERR_ARG; \
+  } while (0)
+
+#define PS_PTR(p) PS_REQUIRE((p) != nullptr && aligned16(p))
+#define PS_OPT_PTR(p) PS_REQUIRE((p) == nullptr || aligned16(p))
+// arrays read or written one element at a time only need to exist
+#define PS_NN(p) PS_REQUIRE((p) != nullptr)
+
+ps_status launch_status(cudaError_t e) { return e == cudaSuccess ? PS_OK : PS_ERR_CUDA; }
+
+ps_status check_ws(size_t need, const void* ws, size_t ws_bytes) {
+  if (need == 0) return PS_OK;
+  if (ws == nullptr || ws_bytes < need) return PS_ERR_WORKSPACE;
+  if (!aligned16(ws)) return PS_ERR_ARG;
+  return PS_OK;
+}
+
+bool dtype_ok(int dt) { return dt == PS_F32 || dt == PS_BF16; }
+
+constexpr int kMaxC = 256;
+constexpr int kMaxD = 8192;
+constexpr int kMaxDh = 256;
+
+}  // namespace
+
+extern "C" {
+
+ps_status ps_create(int device, ps_handle* out) {
+  if (out == nullptr) return PS_ERR_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n)
+    return PS_ERR_ARG;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return PS_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return PS_ERR_UNSUPPORTED;
+  if (cudaSetDevice(device) != cudaSuccess) return PS_ERR_CUDA;
+  auto* h = new (std::nothrow) ps_handle_s;
+  if (h == nullptr) return PS_ERR_CUDA;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->status = nullptr;
+  if (cudaMalloc(&h->status, 16) != cudaSuccess ||
+      cudaMemset(h->status, 0, 16) != cudaSuccess) {
+    if (h->status) cudaFree(h->status);
+    delete h;
+    return PS_ERR_CUDA;
+  }
+  *out = h;
+  return PS_OK;
+}
+
+ps_status ps_destroy(ps_handle h) {
+  if (h == nullptr) return PS_ERR_ARG;
+  cudaFree(h->status);
+  delete h;
+  return PS_OK;
+}
+
+ps_status ps_check(ps_handle h, void* stream, int synchronize) {
+  if (h == nullptr) return PS_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (synchronize && cudaStreamSynchronize(s) != cudaSuccess) return PS_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyAsync(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return PS_ERR_CUDA;
+  if (word != 0) {
+    cudaMemsetAsync(h->status, 0, sizeof(int), s);
+    cudaStreamSynchronize(s);
+    return word == PS_ERR_TIMEOUT ? PS_ERR_TIMEOUT : PS_ERR_CUDA;
+  }
+  return PS_OK;
+}
+
+const char* ps_status_string(ps_status s) {
+  switch (s) {
+    case PS_OK: return "ok";
+    case PS_ERR_ARG: return "invalid argument";
+    case PS_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
+    case PS_ERR_WORKSPACE: return "workspace too small";
+    case PS_ERR_CUDA: return "CUDA error";
+    case PS_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
+                          int dh, int k, int P, int V) {
+  (void)k;
+  if (B <= 0) return 0;
+  switch (op) {
+    case PS_OP_KMEANS: return (N > 0 && C > 0) ? kmeans_ws(B, N, d, C) : 0;
+    case PS_OP_NVFP4: return (N > 0 && d > 0) ? nvfp4_ws(B, N, d) : 0;
+    case PS_OP_PROXY_KL:
+      return (N > 0 && C > 0 && Hkv > 0 && dh > 0 && Hq > 0)
+                 ? proxy_ws(B, N, d, C, Hq, Hkv, dh) : 0;
+    case PS_OP_TOPK: return 0;
+    case PS_OP_REFRESH: return 0;
+    case PS_OP_COMMIT: return (P > 0 && V > 0) ? commit_ws(B, P, V) : 0;
+  }
+  return 0;
+}
+
+ps_status ps_kmeans_spherical(ps_handle h, const void* H, int dtype, int B,
+                              int N, int d, int C, int iters, int init_mode,
+                              const double* init_u, float* mu, int32_t* assign,
+                              float* rho, float* chat, int32_t* counts,
+                              float* objective, void* ws, size_t ws_bytes,
+                              void* stream) {
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype));
+  PS_REQUIRE(B >= 0 && iters >= 0 && (init_mode == 0 || init_mode == 1));
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(d > 0 && d % 16 == 0 && d <= kMaxD);
+  PS_REQUIRE(C >= 1 && C <= kMaxC && C <= N);
+  PS_REQUIRE((long)B * N <= (long)INT32_MAX / 2);
+  PS_PTR(H); PS_PTR(mu); PS_NN(assign); PS_NN(rho); PS_PTR(chat); PS_NN(counts);
+  if (init_mode == 1) PS_NN(init_u);
+  PS_REQUIRE(B <= 65535);
+  ps_status st = check_ws(kmeans_ws(B, N, d, C), ws, ws_bytes);
+  if (st != PS_OK) return st;
+  KmeansArgs a{H, dtype, B, N, d, C, iters, init_mode, init_u, mu, assign, rho,
+               chat, counts, objective, ws, h->status, h->num_sms};
+  return launch_status(kmeans_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+ps_status ps_nvfp4_residual(ps_handle h, const void* H, int dtype,
+                            const float* mu, const int32_t* assign,
+                            const float* rho, int B, int N, int d, int C,
+                            uint8_t* codes, uint8_t* scales,
+                            float* tensor_scale, void* ws, size_t ws_bytes,
+                            void* stream) {
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype));
+  PS_REQUIRE(B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && B <= 65535);
+  PS_PTR(H); PS_PTR(codes); PS_NN(scales); PS_NN(tensor_scale);
+  if (mu != nullptr) {
+    PS_PTR(mu); PS_NN(assign); PS_NN(rho);
+    PS_REQUIRE(C >= 1);
+  } else {
+    PS_REQUIRE(dtype == PS_F32 || dtype == PS_BF16);
+    C = 1;
+  }
+  ps_status st = check_ws(nvfp4_ws(B, N, d), ws, ws_bytes);
+  if (st != PS_OK) return st;
+  Nvfp4Args a{H, dtype, mu, assign, rho, B, N, d, C, codes, scales, tensor_scale,
+              ws, h->num_sms};
+  return launch_status(nvfp4_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+ps_status ps_proxy_attn_kl(ps_handle h, const void* Q, const float* chat,
+                           const void* Wk, int dtype, int B, int N, int d,
+                           int C, int Hq, int Hkv, int dh, const float* A_prev,
+                           float* A_cur, float* D, void* ws, size_t ws_bytes,
+                           void* stream) {
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype));
+  PS_REQUIRE(B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && B <= 65535);
+  PS_REQUIRE(C >= 1 && C <= kMaxC);
+  PS_REQUIRE(Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0);
+  PS_REQUIRE(dh > 0 && dh % 16 == 0 && dh <= kMaxDh);
+  PS_PTR(Q); PS_PTR(chat); PS_PTR(Wk); PS_NN(A_cur); PS_NN(D);
+  ps_status st = check_ws(proxy_ws(B, N, d, C, Hq, Hkv, dh), ws, ws_bytes);
+  if (st != PS_OK) return st;
+  ProxyArgs a{Q, chat, Wk, dtype, B, N, d, C, Hq, Hkv, dh, A_prev, A_cur, D, ws,
+              h->num_sms};
+  return launch_status(proxy_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+ps_status ps_topk_drift(ps_handle h, const float* D, const int32_t* assign,
+                        const int32_t* counts, int B, int N, int C, int k,
+                        int32_t* sel, float* sel_score, int32_t* pos,
+                        int32_t* npos, uint8_t* posmask, void* ws,
+                        size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  PS_REQUIRE(h != nullptr && B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && C >= 1 && C <= kMaxC && C <= N && k >= 1 && k <= C);
+  PS_REQUIRE(B <= 65535);
+  PS_NN(D); PS_NN(assign); PS_NN(counts); PS_NN(sel); PS_NN(sel_score);
+  PS_NN(pos); PS_NN(npos);
+  TopkArgs a{D, assign, counts, B, N, C, k, sel, sel_score, pos, npos, posmask};
+  return launch_status(topk_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
+                        const int32_t* pos, const int32_t* npos,
+                        const void* Wk, const void* Wv, int B, int N, int d,
+                        int Hkv, int dh, void* Kcache, void* Vcache,
+                        int Ncache, int cache_off, void* ws, size_t ws_bytes,
+                        void* stream) {
+  (void)ws; (void)ws_bytes;
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype) && B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && Hkv >= 1 && dh > 0 && dh % 16 == 0);
+  PS_REQUIRE(cache_off >= 0 && (long)cache_off + N <= Ncache && B <= 65535);
+  PS_REQUIRE(2L * ceil_div((long)Hkv * dh, 64) <= 65535);
+  PS_PTR(H); PS_NN(pos); PS_NN(npos); PS_PTR(Wk); PS_PTR(Wv);
+  PS_NN(Kcache); PS_NN(Vcache);
+  RefreshArgs a{H, dtype, pos, npos, Wk, Wv, B, N, d, Hkv, dh, Kcache, Vcache,
+                Ncache, cache_off, h->num_sms};
+  return launch_status(refresh_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
+                    const uint8_t* role, uint8_t* undecided,
+                    const float* D_blk, int d_ld, float* d_sum, int32_t* d_cnt,
+                    float* d_prev, const uint8_t* suffix_sel, int sel_ld,
+                    ps_commit_params params, int32_t* token, float* conf,
+                    uint8_t* commit, void* ws, size_t ws_bytes, void* stream) {
+  PS_REQUIRE(h != nullptr && B >= 0 && P >= 0);
+  if (B == 0 || P == 0) return PS_OK;
+  PS_REQUIRE(P <= 1024 && V >= 4 && V % 4 == 0 && (long)B * P <= 65535);
+  PS_REQUIRE(d_ld >= P && (suffix_sel == nullptr || sel_ld >= P));
+  PS_REQUIRE(params.mode >= 0 && params.mode <= 2);
+  PS_REQUIRE(params.ensure_progress == 0 || params.ensure_progress == 1);
+  PS_PTR(logits); PS_NN(role); PS_NN(undecided); PS_NN(D_blk); PS_NN(d_sum);
+  PS_NN(d_cnt); PS_NN(d_prev); PS_NN(token); PS_NN(conf); PS_NN(commit);
+  ps_status st = check_ws(commit_ws(B, P, V), ws, ws_bytes);
+  if (st != PS_OK) return st;
+  CommitArgs a{logits, B, P, V, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
+               suffix_sel, sel_ld, params, token, conf, commit, ws};
+  return launch_status(commit_run(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Shared device/host helpers of libpolestar (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/polestar.h"
+
+struct ps_handle_s {
+  int device;
+  int num_sms;
+  int* status;  // device word: 0 ok, else a PS_ERR_* code set by a kernel
+};
+
+namespace ps {
+
+constexpr int kWarp = 32;
+// SM count the grid and workspace heuristics are sized for (GB300: 152).
+// Workspace sizes depend only on shapes, never on the device queried.
+constexpr int kSmTarget = 152;
+
+// Element loads widened to fp32.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T> struct Store;
+template <> struct Store<float> {
+  __device__ __forceinline__ static void put(float* p, float v) { *p = v; }
+};
+template <> struct Store<__nv_bfloat16> {
+  __device__ __forceinline__ static void put(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Record the first device-side failure of a call in the handle's word.
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__host__ __device__ inline int ceil_div(long a, long b) { return (int)((a + b - 1) / b); }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Carves a caller workspace into 256-byte aligned pieces.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* p) : base((char*)p) {}
+  template <typename T> T* take(size_t count) {
+    off = align_up(off, 256);
+    T* p = base ? (T*)(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+  size_t bytes() const { return align_up(off, 256); }
+};
+
+}  // namespace ps

@@ -1,0 +1,194 @@
+// a2: NVFP4 quantisation of the k-means residuals.
+//
+// [Polestar §2.A, local window & clustering]: residuals of the clustered
+// hidden states are quantised with NVFP4 into compact proxies.  Format:
+// E2M1 elements, one E4M3 scale per 16 consecutive elements, one fp32 scale
+// per window; round-to-nearest-even with saturation, using Blackwell's
+// cvt.rn.satfinite.{e2m1x2,e4m3x2}.f32 conversions.  Every arithmetic step
+// is an IEEE fp32 operation with an explicit rounding (no contraction), so
+// the outputs are bit-exact functions of the inputs.
+//
+//   k_fp4_amax   per-CTA partial max |r| of each window (r recomputed)
+//   k_fp4_quant  tensor scale, block scales and packed codes
+// The residual r = fl(h - fl(rho * mu_a)) is recomputed in the second kernel
+// instead of being stored: re-reading h costs 2 B/element (bf16), storing r
+// would cost 8.
+#include <algorithm>
+#include <cfloat>
+
+#include "ops.h"
+#include "vec.cuh"
+
+namespace ps {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Eight fp32 values -> eight E2M1 codes, element 2j in the low nibble of
+// byte j.  cvt ... e2m1x2 d, a, b puts a in the high nibble, b in the low.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+  uint32_t out;
+  asm("{\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+        "f"(v[6]), "f"(v[7]));
+  return out;
+}
+
+// fp32 -> E4M3 code (low byte of the x2 conversion).
+__device__ __forceinline__ uint32_t e4m3_code(float x) {
+  unsigned short h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.f), "f"(x));
+  return h & 0xFFu;
+}
+
+// Exact value of a non-negative E4M3 code (bias 7, subnormal step 2^-9).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  if (e == 0) return (float)m * 0.001953125f;
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// r[0..15] for block `col` of row `row` of window b.
+template <typename T>
+__device__ __forceinline__ void residual16(const T* __restrict__ H,
+                                           const float* __restrict__ mu,
+                                           const int32_t* __restrict__ assign,
+                                           const float* __restrict__ rho,
+                                           int b, int N, int d, int C, int row,
+                                           int col, float* r) {
+  const T* h = H + ((long)b * N + row) * d + col;
+  constexpr int V = Vec<T>::n;
+#pragma unroll
+  for (int q = 0; q < 16 / V; ++q) load16(h + q * V, r + q * V);
+  if (mu != nullptr) {
+    int a = assign[(long)b * N + row];
+    a = min(max(a, 0), C - 1);
+    const float rh = rho[(long)b * N + row];
+    const float* m = mu + ((long)b * C + a) * d + col;
+    float mv[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) load16(m + 4 * q, mv + 4 * q);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) r[e] = __fsub_rn(r[e], __fmul_rn(rh, mv[e]));
+  }
+}
+
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float r = scratch[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, scratch[w]);
+  __syncthreads();
+  return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
+           const int32_t* __restrict__ assign, const float* __restrict__ rho,
+           int N, int d, int C, float* __restrict__ part) {
+  __shared__ float s_red[kThreads / 32];
+  const int b = blockIdx.y;
+  const int bpr = d / 16;
+  const long nblk = (long)N * bpr;
+  float m = 0.f;
+  for (long blk = (long)blockIdx.x * kThreads + threadIdx.x; blk < nblk;
+       blk += (long)gridDim.x * kThreads) {
+    const int row = (int)(blk / bpr), col = (int)(blk % bpr) * 16;
+    float r[16];
+    residual16(H, mu, assign, rho, b, N, d, C, row, col, r);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r[e]));
+  }
+  m = block_max(m, s_red);
+  if (threadIdx.x == 0) part[(long)b * gridDim.x + blockIdx.x] = m;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_fp4_quant(const T* __restrict__ H, const float* __restrict__ mu,
+            const int32_t* __restrict__ assign, const float* __restrict__ rho,
+            int N, int d, int C, const float* __restrict__ part, int nparts,
+            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+            float* __restrict__ S_out) {
+  __shared__ float s_red[kThreads / 32];
+  const int b = blockIdx.y;
+  float amax = 0.f;
+  for (int p = threadIdx.x; p < nparts; p += kThreads)
+    amax = fmaxf(amax, part[(long)b * nparts + p]);
+  amax = block_max(amax, s_red);
+  const float S = (amax > 0.f && amax <= FLT_MAX)
+                      ? fmaxf(__fdiv_rn(amax, 2688.0f), FLT_MIN) : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) S_out[b] = S;
+  const float six_s = __fmul_rn(6.0f, S);
+  const int bpr = d / 16;
+  const long nblk = (long)N * bpr;
+  for (long blk = (long)blockIdx.x * kThreads + threadIdx.x; blk < nblk;
+       blk += (long)gridDim.x * kThreads) {
+    const int row = (int)(blk / bpr), col = (int)(blk % bpr) * 16;
+    float r[16];
+    residual16(H, mu, assign, rho, b, N, d, C, row, col, r);
+    float bm = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) bm = fmaxf(bm, fabsf(r[e]));
+    const uint32_t sc = e4m3_code(__fdiv_rn(bm, six_s));
+    const float sb = e4m3_value(sc);
+    uint2 q = make_uint2(0u, 0u);
+    if (sb != 0.f) {
+      const float den = __fmul_rn(sb, S);
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fdiv_rn(r[e], den);
+      q.x = e2m1x8(v);
+      q.y = e2m1x8(v + 8);
+    }
+    const long rowbase = (long)b * N + row;
+    *reinterpret_cast<uint2*>(codes + rowbase * (d / 2) + col / 2) = q;
+    scales[rowbase * bpr + col / 16] = (uint8_t)sc;
+  }
+}
+
+int grid_x(int B, int N, int d) {
+  const long nblk = (long)N * (d / 16);
+  const int want = ceil_div(nblk, kThreads);
+  const int cap = std::max(1, 4 * kSmTarget / std::max(B, 1));
+  return std::max(1, std::min(want, cap));
+}
+
+template <typename T>
+cudaError_t run_typed(const Nvfp4Args& a, cudaStream_t s) {
+  const T* H = static_cast<const T*>(a.H);
+  const int gx = grid_x(a.B, a.N, a.d);
+  float* part = Carver(a.ws).take<float>((size_t)a.B * gx);
+  const dim3 grid(gx, a.B);
+  k_fp4_amax<T><<<grid, kThreads, 0, s>>>(H, a.mu, a.assign, a.rho, a.N, a.d,
+                                          a.C, part);
+  k_fp4_quant<T><<<grid, kThreads, 0, s>>>(H, a.mu, a.assign, a.rho, a.N, a.d,
+                                           a.C, part, gx, a.codes, a.scales, a.S);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t nvfp4_ws(int B, int N, int d) {
+  Carver cv(nullptr);
+  cv.take<float>((size_t)B * grid_x(B, N, d));
+  return cv.bytes();
+}
+
+cudaError_t nvfp4_run(const Nvfp4Args& a, cudaStream_t s) {
+  return a.dtype == PS_F32 ? run_typed<float>(a, s)
+                           : run_typed<__nv_bfloat16>(a, s);
+}
+
+}  // namespace ps

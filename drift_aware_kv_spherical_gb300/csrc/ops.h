@@ -1,0 +1,57 @@
+// Internal launchers of libpolestar; api.cu validates arguments and calls
+// these.  Each returns the first CUDA error of its launches.
+#pragma once
+
+#include "common.cuh"
+
+namespace ps {
+
+struct KmeansArgs {
+  const void* H; int dtype; int B, N, d, C, iters, init_mode;
+  const double* init_u;
+  float* mu; int32_t* assign; float* rho; float* chat; int32_t* counts;
+  float* obj; void* ws; int* status; int num_sms;
+};
+size_t kmeans_ws(int B, int N, int d, int C);
+cudaError_t kmeans_run(const KmeansArgs& a, cudaStream_t s);
+
+struct Nvfp4Args {
+  const void* H; int dtype; const float* mu; const int32_t* assign;
+  const float* rho; int B, N, d, C;
+  uint8_t* codes; uint8_t* scales; float* S; void* ws; int num_sms;
+};
+size_t nvfp4_ws(int B, int N, int d);
+cudaError_t nvfp4_run(const Nvfp4Args& a, cudaStream_t s);
+
+struct ProxyArgs {
+  const void* Q; const float* chat; const void* Wk; int dtype;
+  int B, N, d, C, Hq, Hkv, dh;
+  const float* A_prev; float* A_cur; float* D; void* ws; int num_sms;
+};
+size_t proxy_ws(int B, int N, int d, int C, int Hq, int Hkv, int dh);
+cudaError_t proxy_run(const ProxyArgs& a, cudaStream_t s);
+
+struct TopkArgs {
+  const float* D; const int32_t* assign; const int32_t* counts;
+  int B, N, C, k;
+  int32_t* sel; float* sel_score; int32_t* pos; int32_t* npos; uint8_t* posmask;
+};
+cudaError_t topk_run(const TopkArgs& a, cudaStream_t s);
+
+struct RefreshArgs {
+  const void* H; int dtype; const int32_t* pos; const int32_t* npos;
+  const void* Wk; const void* Wv; int B, N, d, Hkv, dh;
+  void* Kc; void* Vc; int Ncache, cache_off; int num_sms;
+};
+cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s);
+
+struct CommitArgs {
+  const float* logits; int B, P, V; const uint8_t* role; uint8_t* undecided;
+  const float* D; int d_ld; float* d_sum; int32_t* d_cnt; float* d_prev;
+  const uint8_t* suffix_sel; int sel_ld; ps_commit_params p;
+  int32_t* token; float* conf; uint8_t* commit; void* ws;
+};
+size_t commit_ws(int B, int P, int V);
+cudaError_t commit_run(const CommitArgs& a, cudaStream_t s);
+
+}  // namespace ps

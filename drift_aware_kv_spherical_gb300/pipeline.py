@@ -1,0 +1,134 @@
+"""One drift-refresh step over all layers of a workload, through libpolestar.
+
+A step runs, for every layer: spherical k-means (warm-started from the
+previous step's centroids, or k-means++ when the window is built), NVFP4
+residuals, proxy attention + KL drift against the previous step's
+distribution, top-k drifting clusters and the sparse K/V refresh; then one
+commit over the current block with the last layer's drift.  All buffers are
+allocated once here (caller-side), so a step allocates nothing and can be
+captured in a CUDA graph.
+"""
+
+import torch
+
+from . import polestar as ps
+from . import workloads as wl
+
+
+class LayerState:
+    def __init__(self, w, device):
+        B, N, C, d = w.B, w.N, w.C, w.d
+        f32 = dict(dtype=torch.float32, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        u8 = dict(dtype=torch.uint8, device=device)
+        dt = wl.torch_dtype(w)
+        self.mu = torch.zeros(B, C, d, **f32)
+        self.chat = torch.zeros(B, C, d, **f32)
+        self.assign = torch.zeros(B, N, **i32)
+        self.rho = torch.zeros(B, N, **f32)
+        self.counts = torch.zeros(B, C, **i32)
+        self.obj = torch.zeros(B, w.iters + 1, **f32)
+        self.codes = torch.zeros(B, N, d // 2, **u8)
+        self.scales = torch.zeros(B, N, d // 16, **u8)
+        self.S = torch.zeros(B, **f32)
+        self.A = [torch.zeros(B, N, C, **f32), torch.zeros(B, N, C, **f32)]
+        self.D = torch.zeros(B, N, **f32)
+        self.sel = torch.zeros(B, w.k, **i32)
+        self.sel_score = torch.zeros(B, w.k, **f32)
+        self.pos = torch.zeros(B, N, **i32)
+        self.npos = torch.zeros(B, **i32)
+        self.posmask = torch.zeros(B, N, **u8)
+        self.Kc = torch.zeros(B, w.Ncache, w.Hkv, w.dh, dtype=dt, device=device)
+        self.Vc = torch.zeros(B, w.Ncache, w.Hkv, w.dh, dtype=dt, device=device)
+
+
+class Pipeline:
+    """Buffers and the per-step call sequence for workload `w`."""
+
+    def __init__(self, w, layers=None, device="cuda"):
+        self.w = w
+        self.layers = w.layers if layers is None else layers
+        self.device = device
+        B, N, d, C = w.B, w.N, w.d, w.C
+        sizes = dict(B=B, N=N, d=d, C=C, Hq=w.Hq, Hkv=w.Hkv, dh=w.dh, k=w.k, P=w.P,
+                     V=w.V)
+        self.ws = {op: ps.workspace(op, device=device, **sizes)
+                   for op in (ps.OP_KMEANS, ps.OP_NVFP4, ps.OP_PROXY_KL, ps.OP_TOPK,
+                              ps.OP_REFRESH, ps.OP_COMMIT)}
+        self.state = [LayerState(w, device) for _ in range(self.layers)]
+        P = w.P
+        self.role = wl.make_roles(w).to(device)
+        self.undecided = torch.ones(B, P, dtype=torch.uint8, device=device)
+        self.d_sum = torch.zeros(B, P, dtype=torch.float32, device=device)
+        self.d_cnt = torch.zeros(B, P, dtype=torch.int32, device=device)
+        self.d_prev = torch.zeros(B, P, dtype=torch.float32, device=device)
+        self.token = torch.zeros(B, P, dtype=torch.int32, device=device)
+        self.conf = torch.zeros(B, P, dtype=torch.float32, device=device)
+        self.commit = torch.zeros(B, P, dtype=torch.uint8, device=device)
+        self.params = ps.CommitParams(w.tau_s, w.alpha, w.ratio, w.mode, 1)
+        self.t = 0
+
+    def reset_block(self):
+        self.undecided.fill_(1)
+        self.d_sum.zero_()
+        self.d_cnt.zero_()
+        self.d_prev.zero_()
+
+    def layer_step(self, l, H, Q, Wk, Wv, init_u=None, first=False, stream=None):
+        w, st = self.w, self.state[l]
+        cur, prev = st.A[self.t % 2], st.A[(self.t + 1) % 2]
+        ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts,
+                               w.iters, init_mode=1 if first else 0, init_u=init_u,
+                               objective=st.obj, ws=self.ws[ps.OP_KMEANS],
+                               stream=stream)
+        ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                             ws=self.ws[ps.OP_NVFP4], stream=stream)
+        ps.ps_proxy_attn_kl(Q, st.chat, Wk, None if first else prev, cur, st.D, w.Hkv,
+                            ws=self.ws[ps.OP_PROXY_KL], stream=stream)
+        ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
+                         st.npos, st.posmask, ws=self.ws[ps.OP_TOPK], stream=stream)
+        ps.ps_refresh_kv(H, st.pos, st.npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
+                         ws=self.ws[ps.OP_REFRESH], stream=stream)
+
+    def commit_step(self, logits, stream=None):
+        w, last = self.w, self.state[-1]
+        D_blk = last.D[:, w.blk_start:]
+        ps.ps_commit(logits, self.role, self.undecided, D_blk, w.N, self.d_sum,
+                     self.d_cnt, self.d_prev, None, w.P, self.params, self.token,
+                     self.conf, self.commit, ws=self.ws[ps.OP_COMMIT], stream=stream)
+
+    def step(self, Hs, Qs, Wks, Wvs, logits, init_us=None, first=False, stream=None):
+        """Hs/Qs/Wks/Wvs: per-layer tensors (lists of length `layers`)."""
+        for l in range(self.layers):
+            self.layer_step(l, Hs[l], Qs[l], Wks[l], Wvs[l],
+                            None if init_us is None else init_us[l], first, stream)
+        self.commit_step(logits, stream)
+        self.t += 1
+
+    def kernel_launches_per_step(self):
+        """Kernels libpolestar enqueues for one step (counted from its launch
+        sequence: k-means 3 per pass + 2, NVFP4 2, proxy 2-4, top-k 1,
+        refresh 1, commit 2)."""
+        w = self.w
+        km = 1 + 3 * (w.iters + 1) - 1 + 1
+        return self.layers * (km + 2 + self._proxy_launches() + 1 + 1) + 2
+
+    def _proxy_launches(self):
+        return _proxy_launch_count(self.w)
+
+
+def _proxy_launch_count(w):
+    # mirrors the split/slice plan of the proxy kernels (k_ckeys [+ reduce]
+    # + k_proxy [+ final])
+    from math import ceil
+    M, nout = w.B * w.C, w.Hkv * w.dh
+    tiles = ceil(M / 64) * ceil(nout / 64)
+    ns = max(1, ceil(2 * 152 / tiles))
+    ns = min(ns, max(1, w.d // 256))
+    klen = ceil(ceil(w.d / ns) / 16) * 16
+    nsplit = ceil(w.d / klen)
+    ptiles = ceil(w.N / 16) * w.B
+    sl = min(max(1, ceil(2 * 152 / ptiles)), w.Hq)
+    hps = ceil(w.Hq / sl)
+    nslice = ceil(w.Hq / hps)
+    return 2 + (nsplit > 1) + (nslice > 1)

@@ -1,0 +1,228 @@
+"""Thin Python binding of libpolestar's C ABI (include/polestar.h).
+
+Argument marshalling only: every function below forwards torch device
+tensors as raw pointers to the function of the same name in libpolestar.so,
+and every step of the computation runs in its CUDA kernels.  There is no CPU
+path: if the library is missing or a call fails, a PolestarError is raised.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpolestar.so")
+
+PS_OK, PS_ERR_ARG, PS_ERR_UNSUPPORTED, PS_ERR_WORKSPACE, PS_ERR_CUDA, PS_ERR_TIMEOUT = range(6)
+PS_F32, PS_BF16 = 0, 1
+OP_KMEANS, OP_NVFP4, OP_PROXY_KL, OP_TOPK, OP_REFRESH, OP_COMMIT = range(6)
+EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string",
+            "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
+            "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit"]
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+class PolestarError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {Library.load().status_string(status)} ({status})")
+
+
+class CommitParams(ctypes.Structure):
+    _fields_ = [("tau_s", ctypes.c_float), ("alpha", ctypes.c_float),
+                ("ratio", ctypes.c_float), ("mode", ctypes.c_int),
+                ("ensure_progress", ctypes.c_int)]
+
+
+_SIGS = {
+    "ps_create": (_i, [_i, ctypes.POINTER(_p)]),
+    "ps_destroy": (_i, [_p]),
+    "ps_check": (_i, [_p, _p, _i]),
+    "ps_status_string": (ctypes.c_char_p, [_i]),
+    "ps_workspace_bytes": (_sz, [_i] * 11),
+    "ps_kmeans_spherical": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
+                                 _p, _p, _p, _p, _p, _sz, _p]),
+    "ps_nvfp4_residual": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p,
+                               _p, _sz, _p]),
+    "ps_proxy_attn_kl": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p,
+                              _p, _p, _p, _sz, _p]),
+    "ps_topk_drift": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p,
+                           _sz, _p]),
+    "ps_refresh_kv": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p,
+                           _i, _i, _p, _sz, _p]),
+    "ps_commit": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _i, _p, _p, _p, _p, _i,
+                       CommitParams, _p, _p, _p, _p, _sz, _p]),
+}
+
+
+class Library:
+    """The loaded libpolestar.so (one per process)."""
+
+    _inst = None
+
+    def __init__(self, path):
+        self.cdll = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(self.cdll, name)
+            fn.restype = res
+            fn.argtypes = args
+        self.path = path
+        self._handles = {}
+
+    @classmethod
+    def load(cls, path=None):
+        if cls._inst is None:
+            path = path or LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is not built; run `python -c 'import __graft_entry__ as g; "
+                    "g.build()'` (libpolestar has no CPU fallback)")
+            cls._inst = cls(path)
+        return cls._inst
+
+    def status_string(self, s):
+        return self.cdll.ps_status_string(s).decode()
+
+    def handle(self, device=None):
+        """A process-wide handle for `device` (created on first use)."""
+        dev = torch.cuda.current_device() if device is None else int(device)
+        if dev not in self._handles:
+            h = _p()
+            st = self.cdll.ps_create(dev, ctypes.byref(h))
+            if st != PS_OK:
+                raise PolestarError(st, "ps_create")
+            self._handles[dev] = h
+        return self._handles[dev]
+
+
+def _lib():
+    return Library.load()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpolestar takes device tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _dtype(t):
+    if t.dtype == torch.float32:
+        return PS_F32
+    if t.dtype == torch.bfloat16:
+        return PS_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _check(st, where):
+    if st != PS_OK:
+        raise PolestarError(st, where)
+
+
+def _ws(ws):
+    return (None, 0) if ws is None else (ws.data_ptr(), ws.numel() * ws.element_size())
+
+
+def ps_workspace_bytes(op, B=0, N=0, d=0, C=0, Hq=0, Hkv=0, dh=0, k=0, P=0, V=0):
+    return int(_lib().cdll.ps_workspace_bytes(op, B, N, d, C, Hq, Hkv, dh, k, P, V))
+
+
+def workspace(op, device=None, **sizes):
+    """A caller-owned workspace tensor large enough for `op` at `sizes`."""
+    n = ps_workspace_bytes(op, **sizes)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def ps_check(synchronize=True, stream=None):
+    lib = _lib()
+    _check(lib.cdll.ps_check(lib.handle(), _stream(stream), int(synchronize)), "ps_check")
+
+
+def ps_kmeans_spherical(H, mu, assign, rho, chat, counts, iters, init_mode=0,
+                        init_u=None, objective=None, ws=None, stream=None):
+    lib = _lib()
+    B, N, d = H.shape
+    C = mu.shape[1]
+    w, wn = _ws(ws)
+    st = lib.cdll.ps_kmeans_spherical(
+        lib.handle(), _ptr(H), _dtype(H), B, N, d, C, iters, init_mode,
+        _ptr(init_u), _ptr(mu), _ptr(assign), _ptr(rho), _ptr(chat), _ptr(counts),
+        _ptr(objective), w, wn, _stream(stream))
+    _check(st, "ps_kmeans_spherical")
+
+
+def ps_nvfp4_residual(H, mu, assign, rho, codes, scales, tensor_scale, ws=None,
+                      stream=None):
+    lib = _lib()
+    B, N, d = H.shape
+    C = mu.shape[1] if mu is not None else 1
+    w, wn = _ws(ws)
+    st = lib.cdll.ps_nvfp4_residual(
+        lib.handle(), _ptr(H), _dtype(H), _ptr(mu), _ptr(assign), _ptr(rho), B, N,
+        d, C, _ptr(codes), _ptr(scales), _ptr(tensor_scale), w, wn, _stream(stream))
+    _check(st, "ps_nvfp4_residual")
+
+
+def ps_proxy_attn_kl(Q, chat, Wk, A_prev, A_cur, D, Hkv, ws=None, stream=None):
+    lib = _lib()
+    B, N, Hq, dh = Q.shape
+    C, d = chat.shape[1], chat.shape[2]
+    w, wn = _ws(ws)
+    st = lib.cdll.ps_proxy_attn_kl(
+        lib.handle(), _ptr(Q), _ptr(chat), _ptr(Wk), _dtype(Q), B, N, d, C, Hq, Hkv,
+        dh, _ptr(A_prev), _ptr(A_cur), _ptr(D), w, wn, _stream(stream))
+    _check(st, "ps_proxy_attn_kl")
+
+
+def ps_topk_drift(D, assign, counts, k, sel, sel_score, pos, npos, posmask=None,
+                  ws=None, stream=None):
+    lib = _lib()
+    B, N = D.shape
+    C = counts.shape[1]
+    w, wn = _ws(ws)
+    st = lib.cdll.ps_topk_drift(
+        lib.handle(), _ptr(D), _ptr(assign), _ptr(counts), B, N, C, k, _ptr(sel),
+        _ptr(sel_score), _ptr(pos), _ptr(npos), _ptr(posmask), w, wn, _stream(stream))
+    _check(st, "ps_topk_drift")
+
+
+def ps_refresh_kv(H, pos, npos, Wk, Wv, Kcache, Vcache, Hkv, dh, cache_off=0,
+                  ws=None, stream=None):
+    lib = _lib()
+    B, N, d = H.shape
+    Ncache = Kcache.shape[1]
+    w, wn = _ws(ws)
+    st = lib.cdll.ps_refresh_kv(
+        lib.handle(), _ptr(H), _dtype(H), _ptr(pos), _ptr(npos), _ptr(Wk), _ptr(Wv),
+        B, N, d, Hkv, dh, _ptr(Kcache), _ptr(Vcache), Ncache, cache_off, w, wn,
+        _stream(stream))
+    _check(st, "ps_refresh_kv")
+
+
+def ps_commit(logits, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
+              suffix_sel, sel_ld, params, token, conf, commit, ws=None,
+              stream=None):
+    lib = _lib()
+    B, P, V = logits.shape
+    w, wn = _ws(ws)
+    if not isinstance(params, CommitParams):
+        params = CommitParams(*params)
+    st = lib.cdll.ps_commit(
+        lib.handle(), _ptr(logits), B, P, V, _ptr(role), _ptr(undecided), _ptr(D_blk),
+        d_ld, _ptr(d_sum), _ptr(d_cnt), _ptr(d_prev), _ptr(suffix_sel), sel_ld, params,
+        _ptr(token), _ptr(conf), _ptr(commit), w, wn, _stream(stream))
+    _check(st, "ps_commit")

@@ -1,0 +1,241 @@
+/*
+ * libpolestar -- the per-step drift-scoring and sparse-refresh path of
+ * Polestar-Cache / Polestar-Commit on one NVIDIA GB300 (sm_103a).
+ *
+ * Method source: "Polestar: Drift-Aware Cache Calibration and Token
+ * Commitment for Efficient Inference of Diffusion LLMs" (gist.science
+ * explainer of arXiv 2607.14107), technical summary, cited below as
+ * [Polestar §x, <paragraph>].
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory   Every array argument is a DEVICE pointer to caller-owned memory,
+ *          row-major, contiguous, last index fastest, 16-byte aligned.
+ *          The library allocates nothing inside an op: scratch comes from the
+ *          caller's workspace `ws` of at least ps_workspace_bytes(op, ...)
+ *          bytes (NULL is fine when that size is 0).  Outputs must not alias
+ *          inputs unless the argument says "in/out".
+ * Streams  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *          default stream).  Calls only enqueue work and return; the results
+ *          are valid once the stream reaches that point.
+ * Errors   Argument errors are detected on the host before anything is
+ *          enqueued and return PS_ERR_ARG (nothing is launched, no output is
+ *          touched).  A launch failure returns PS_ERR_CUDA.  A device-side
+ *          failure (a bounded wait that gave up) sets the handle's status word;
+ *          ps_check() reports it as PS_ERR_TIMEOUT.
+ * Sizes    B >= 0 (B == 0 is a no-op), d % 16 == 0, dh % 16 == 0,
+ *          Hq % Hkv == 0, 1 <= k <= C <= min(N, 1024), V % 4 == 0.
+ * Threads  One handle per concurrently used stream; no C++ exception
+ *          crosses this interface.
+ * State    Step-to-step state (centroids, previous distributions, drift
+ *          history, undecided flags, the KV cache) lives in caller buffers.
+ */
+#ifndef POLESTAR_H
+#define POLESTAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PS_OK = 0,
+  PS_ERR_ARG = 1,          /* bad pointer, size, alignment or dtype       */
+  PS_ERR_UNSUPPORTED = 2,  /* device is not sm_103                         */
+  PS_ERR_WORKSPACE = 3,    /* ws smaller than ps_workspace_bytes()         */
+  PS_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+  PS_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up           */
+} ps_status;
+
+typedef enum { PS_F32 = 0, PS_BF16 = 1 } ps_dtype;
+
+typedef enum {
+  PS_OP_KMEANS = 0, PS_OP_NVFP4 = 1, PS_OP_PROXY_KL = 2,
+  PS_OP_TOPK = 3, PS_OP_REFRESH = 4, PS_OP_COMMIT = 5
+} ps_op;
+
+typedef struct ps_handle_s* ps_handle;
+
+/* Create a handle on `device` (made current).  Allocates the handle's
+ * 16-byte device status word -- the only allocation the library makes.
+ * PS_ERR_UNSUPPORTED unless the device has compute capability 10.3. */
+ps_status ps_create(int device, ps_handle* out);
+ps_status ps_destroy(ps_handle h);
+
+/* Status of device-side work enqueued so far on `stream`.  synchronize != 0
+ * waits for the stream first; otherwise the word is read asynchronously
+ * after a stream sync anyway (the read is ordered on `stream`).  Clears the
+ * word.  Returns PS_OK, PS_ERR_TIMEOUT or PS_ERR_CUDA. */
+ps_status ps_check(ps_handle h, void* stream, int synchronize);
+
+const char* ps_status_string(ps_status s);
+
+/* Workspace bytes `op` needs for these sizes (arguments an op does not use
+ * are ignored).  0 means ws may be NULL. */
+size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
+                          int dh, int k, int P, int V);
+
+/* ---------------------------------------------------------------------------
+ * a1  Spherical k-means of each window's hidden states.
+ * [Polestar §2.A, local window & clustering] -- "clusters the hidden states
+ * in the window with spherical k-means".
+ *
+ * H        [B][N][d]  f32 or bf16 (dtype)      hidden states of the window
+ * mu       [B][C][d]  f32, in/out              centroids: input = warm start
+ *          (init_mode 0, e.g. the previous step's result) or ignored
+ *          (init_mode 1); output = final unit-norm centroids
+ * init_u   [B][C]     f64 in [0,1)             k-means++ draws (init_mode 1;
+ *          NULL for init_mode 0).  First centre = row floor(u0*N); centre r =
+ *          first row whose running sum of w_i = 1 - max cos to the chosen
+ *          centres exceeds u_r * sum(w).
+ * iters    number of centroid updates I >= 0; I+1 assignment passes run.
+ * assign   [B][N] i32 out  final cluster of each row (ties -> lower index)
+ * rho      [B][N] f32 out  <h_i, mu_{assign_i}>
+ * chat     [B][C][d] f32 in/out  mean(rho of members) * mu_c; clusters left
+ *          empty keep the caller's values
+ * counts   [B][C] i32 out  cluster sizes
+ * objective[B][I+1] f32 out (nullable)  sum_i cos(h_i, mu_{a_i}) per pass
+ * Empty clusters keep their centroid.  Rows of zero norm join cluster 0.
+ * ------------------------------------------------------------------------- */
+ps_status ps_kmeans_spherical(ps_handle h, const void* H, int dtype, int B,
+                              int N, int d, int C, int iters, int init_mode,
+                              const double* init_u, float* mu, int32_t* assign,
+                              float* rho, float* chat, int32_t* counts,
+                              float* objective, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a2  NVFP4 quantisation of the k-means residuals.
+ * [Polestar §2.A, local window & clustering] -- "quantises residuals with
+ * NVFP4 to create compact proxy representations".
+ *
+ * r = fl(h - fl(rho_i * mu_{a_i}))  (fp32, two roundings); mu == NULL
+ * quantises H itself (then assign/rho are ignored).
+ * S_b = max(fl(amax_b / 2688), FLT_MIN) for 0 < amax_b < inf, else 1.
+ * Block scale (16 elements along d): E4M3(fl(amax_blk / fl(6 S_b))), RNE,
+ * saturating; element: E2M1(fl(r / fl(s_blk * S_b))), RNE, saturating, or
+ * 0 when s_blk == 0.  Negative values rounding to zero keep their sign.
+ *
+ * codes  [B][N][d/2]  u8 out  element 2j in the low nibble of byte j
+ * scales [B][N][d/16] u8 out  E4M3 block scales
+ * tensor_scale [B]    f32 out S_b
+ * Outputs are bit-exact functions of the inputs.
+ * ------------------------------------------------------------------------- */
+ps_status ps_nvfp4_residual(ps_handle h, const void* H, int dtype,
+                            const float* mu, const int32_t* assign,
+                            const float* rho, int B, int N, int d, int C,
+                            uint8_t* codes, uint8_t* scales,
+                            float* tensor_scale, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a3+a4  Proxy attention on centroid keys and the per-position KL drift.
+ * [Polestar §2.A, sparse updates] -- proxy attention with cluster centroids;
+ * [Polestar §2.A, drift measurement] -- D_i = KL(A_i^(t) || A_i^(t-1)).
+ *
+ * K~[b][c][g] = chat[b][c] . Wk[:, g*dh:(g+1)*dh]            (fp32)
+ * s = q[b][i][h] . K~[b][c][h / (Hq/Hkv)] / sqrt(dh); p = softmax_c(s)
+ * A_cur[b][i][c] = mean over the Hq heads of p
+ * D[b][i] = max(0, sum_c A_cur (ln A_cur - ln max(A_prev, 1e-30))), terms
+ *           with A_cur == 0 skipped; D = 0 when A_prev == NULL.
+ *
+ * Q      [B][N][Hq][dh]  f32 or bf16 (dtype)
+ * chat   [B][C][d]       f32   (from ps_kmeans_spherical)
+ * Wk     [d][Hkv*dh]     dtype
+ * A_prev [B][N][C] f32 or NULL;  A_cur [B][N][C] f32 out;  D [B][N] f32 out
+ * Deterministic: identical inputs give identical bits, so A_prev == A_cur
+ * from an identical call gives D == 0 exactly.
+ * ------------------------------------------------------------------------- */
+ps_status ps_proxy_attn_kl(ps_handle h, const void* Q, const float* chat,
+                           const void* Wk, int dtype, int B, int N, int d,
+                           int C, int Hq, int Hkv, int dh, const float* A_prev,
+                           float* A_cur, float* D, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a5  Top-k most-drifting clusters and the positions they cover.
+ * [Polestar §2.A, sparse updates] -- "identifies the top-k drifting
+ * clusters and runs a sparse forward pass on only these positions".
+ *
+ * score_c = (sum of D_i over members, fp64, ascending i) / n_c, for n_c > 0.
+ * sel       [B][k] i32 out  clusters by score descending, ties -> lower c,
+ *                           padded with -1
+ * sel_score [B][k] f32 out  their scores (fp32 of the fp64 mean), pad -inf
+ * pos       [B][N] i32 out  ascending positions whose cluster is selected,
+ *                           then -1
+ * npos      [B]    i32 out  number of such positions (stays on the device)
+ * posmask   [B][N] u8  out  (nullable) 1 where the position is selected
+ * Bit-exact.
+ * ------------------------------------------------------------------------- */
+ps_status ps_topk_drift(ps_handle h, const float* D, const int32_t* assign,
+                        const int32_t* counts, int B, int N, int C, int k,
+                        int32_t* sel, float* sel_score, int32_t* pos,
+                        int32_t* npos, uint8_t* posmask, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a6  Sparse K/V refresh of the selected positions.
+ * [Polestar §2.A, sparse updates] -- "a sparse forward pass on only these
+ * positions ... refreshes the corresponding KV-cache entries".
+ *
+ * For j < npos[b], p = pos[b][j]:
+ *   Kcache[b][cache_off + p] = round(H[b][p] . Wk), same for V with Wv,
+ *   accumulated in fp32, rounded to the cache dtype (bf16 RNE or f32).
+ * Rows not listed are untouched.  npos is read on the device.
+ * H [B][N][d], Wk/Wv [d][Hkv*dh], Kcache/Vcache [B][Ncache][Hkv][dh], all
+ * of `dtype`.  Requires cache_off + N <= Ncache.
+ * ------------------------------------------------------------------------- */
+ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
+                        const int32_t* pos, const int32_t* npos,
+                        const void* Wk, const void* Wv, int B, int N, int d,
+                        int Hkv, int dh, void* Kcache, void* Vcache,
+                        int Ncache, int cache_off, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a7  Confidence and drift-aware commitment of a block.
+ * [Polestar §2.B, current block commitment] -- commit when the drift delta
+ * exceeds alpha (tau_s - c)^2;  [Polestar §2.B, suffix block commitment] --
+ * suffix tokens commit only with c >= tau_s.
+ *
+ * Per row: token = first arg-max of the logits, conf = 1 / sum exp(l - max).
+ * role[j]: 0 current block, 1 suffix block, 2 inactive.
+ * Current, undecided j:  commit if conf >= tau_s, or (d_cnt >= 1 and)
+ *   mode 0 DELTA_DROP:  d_sum/d_cnt - D > alpha (tau_s - conf)^2
+ *   mode 1 DELTA_RISE:  D - d_sum/d_cnt > alpha (tau_s - conf)^2
+ *   mode 2 RATIO:       D < ratio * d_prev
+ * Suffix, undecided j: commit if suffix_sel[b][j] and conf >= tau_s.
+ * ensure_progress: if no current token commits while some are undecided,
+ *   the undecided current token with the largest conf commits (ties: lower j).
+ * Then every undecided current token sets d_sum = fl32(d_sum + D),
+ *   d_cnt += 1, d_prev = D; committed tokens get undecided = 0.
+ *
+ * logits [B][P][V] f32; role [P] u8; undecided [B][P] u8 in/out;
+ * D_blk: element (b, j) at D_blk[b*d_ld + j] (e.g. the last layer's D with
+ *   d_ld = N, offset to the block); d_sum/d_prev [B][P] f32 in/out,
+ *   d_cnt [B][P] i32 in/out; suffix_sel: element (b, j) at
+ *   suffix_sel[b*sel_ld + j] or NULL (no suffix commits);
+ * token [B][P] i32, conf [B][P] f32, commit [B][P] u8 out.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  float tau_s;
+  float alpha;
+  float ratio;
+  int mode;            /* 0 DELTA_DROP, 1 DELTA_RISE, 2 RATIO */
+  int ensure_progress; /* 0 or 1 */
+} ps_commit_params;
+
+ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
+                    const uint8_t* role, uint8_t* undecided,
+                    const float* D_blk, int d_ld, float* d_sum, int32_t* d_cnt,
+                    float* d_prev, const uint8_t* suffix_sel, int sel_ld,
+                    ps_commit_params params, int32_t* token, float* conf,
+                    uint8_t* commit, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POLESTAR_H */

@@ -64,6 +64,10 @@ def commit_rule(logits, role, undecided, D_blk, d_sum, d_cnt, d_prev,
     Returns dict(token, conf, commit, undecided, d_sum, d_cnt, d_prev,
     margin) where margin[j] is the smallest relative distance of any decision
     input of row j from its threshold (for tie-band accounting)."""
+    # thresholds cross the C ABI as fp32: decide with the same values
+    p = CommitParams(tau_s=float(np.float32(p.tau_s)), alpha=float(np.float32(p.alpha)),
+                     ratio=float(np.float32(p.ratio)), mode=p.mode,
+                     ensure_progress=p.ensure_progress)
     P = len(role)
     token = np.zeros(P, np.int32)
     conf = np.zeros(P)

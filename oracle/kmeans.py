@@ -35,7 +35,7 @@ def normalize_rows(H):
     return out
 
 
-def kmeanspp_init(H, C, u):
+def kmeanspp_init(H, C, u, return_margin=False):
     """k-means++ seeding on the unit sphere.
 
     H: [N][d] hidden states of one window; u: C uniforms in [0, 1) supplied by
@@ -50,7 +50,11 @@ def kmeanspp_init(H, C, u):
       in row order) exceeds u_r * sum(w); if sum(w) == 0 the smallest row not
       yet chosen.
 
-    Returns (mu [C][d] fp64 unit rows, chosen row indices [C]).
+    Returns (mu [C][d] fp64 unit rows, chosen row indices [C]).  With
+    return_margin=True also the smallest distance, relative to sum(w), of any
+    draw u_r * sum(w) from a prefix-sum boundary (a draw that close to a
+    boundary may legitimately pick the neighbouring row under a different
+    summation order).
     """
     Xh = normalize_rows(H)
     N = Xh.shape[0]
@@ -59,14 +63,19 @@ def kmeanspp_init(H, C, u):
     chosen = [first]
     w = np.maximum(0.0, 1.0 - Xh @ Xh[first])
     w[first] = 0.0
+    margin = np.inf
     for r in range(1, C):
         prefix = np.cumsum(w)          # sequential, in row order
         total = prefix[-1]
         pick = -1
         if total > 0:
-            above = np.nonzero(prefix > u[r] * total)[0]
+            target = u[r] * total
+            above = np.nonzero(prefix > target)[0]
             if above.size:
                 pick = int(above[0])
+                lo = prefix[pick - 1] if pick > 0 else 0.0
+                margin = min(margin, (prefix[pick] - target) / total,
+                             (target - lo) / total)
         if pick < 0:
             taken = set(chosen)
             pick = next(i for i in range(N) if i not in taken)
@@ -74,7 +83,8 @@ def kmeanspp_init(H, C, u):
         w = np.minimum(w, np.maximum(0.0, 1.0 - Xh @ Xh[pick]))
         for j in chosen:
             w[j] = 0.0
-    return Xh[chosen].copy(), np.array(chosen, dtype=np.int64)
+    mu, idx = Xh[chosen].copy(), np.array(chosen, dtype=np.int64)
+    return (mu, idx, margin) if return_margin else (mu, idx)
 
 
 def _assign(Xh, mu):
