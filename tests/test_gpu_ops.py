@@ -288,9 +288,10 @@ def test_proxy_kl_of_identical_step_is_exactly_zero():
 
 
 def test_proxy_gqa_and_ragged():
-    # Dream-7B head layout (28 query heads on 4 KV heads), 2 windows of 77 rows
-    w, L, H, Q, chat = _proxy_inputs(2, B=2, N=77)
-    prev = torch.softmax(torch.randn(2, 77, w.C, device="cuda"), dim=2)
+    # Dream-7B head layout (28 query heads on 4 KV heads), 2 windows of 177
+    # rows (ragged against the 16-row tiles)
+    w, L, H, Q, chat = _proxy_inputs(2, B=2, N=177)
+    prev = torch.softmax(torch.randn(2, 177, w.C, device="cuda"), dim=2)
     A, D = run_proxy(Q, chat, L["Wk"], w.Hkv, A_prev=prev)
     oA, oD = _oracle_proxy(w, np_(Q), np_(chat), np_(L["Wk"]), np_(prev))
     assert_close(np_(A), oA, what="A")
