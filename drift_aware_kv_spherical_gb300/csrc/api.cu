@@ -243,3 +243,29 @@ ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
 }
 
 }  // extern "C"
+
+// The same NVFP4 residual quantisation as ps_nvfp4_residual, for callers
+// that cannot allocate device memory: no workspace argument, scratch in a
+// fixed 64 KiB device array inside the library.  See include/polestar.h.
+extern "C" ps_status ps_nvfp4_residual_noalloc(
+    ps_handle h, const void* H, int dtype, const float* mu, const int32_t* assign,
+    const float* rho, int B, int N, int d, int C, uint8_t* codes, uint8_t* scales,
+    float* tensor_scale, void* stream) {
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype));
+  PS_REQUIRE(B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && B <= 65535);
+  PS_PTR(H); PS_PTR(codes); PS_NN(scales); PS_NN(tensor_scale);
+  if (mu != nullptr) {
+    PS_PTR(mu); PS_NN(assign); PS_NN(rho);
+    PS_REQUIRE(C >= 1);
+  } else {
+    C = 1;
+  }
+  if (!nvfp4_static_fits(B, N, d)) return PS_ERR_WORKSPACE;
+  float* scratch = nullptr;
+  if (nvfp4_static_scratch(h->device, &scratch) != cudaSuccess) return PS_ERR_CUDA;
+  Nvfp4Args a{H, dtype, mu, assign, rho, B, N, d, C, codes, scales, tensor_scale,
+              scratch, h->num_sms};
+  return launch_status(nvfp4_run(a, static_cast<cudaStream_t>(stream)));
+}

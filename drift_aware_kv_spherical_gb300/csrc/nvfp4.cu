@@ -15,6 +15,8 @@
 // would cost 8.
 #include <algorithm>
 #include <cfloat>
+#include <mutex>
+#include <unordered_map>
 
 #include "ops.h"
 #include "vec.cuh"
@@ -189,6 +191,55 @@ size_t nvfp4_ws(int B, int N, int d) {
 cudaError_t nvfp4_run(const Nvfp4Args& a, cudaStream_t s) {
   return a.dtype == PS_F32 ? run_typed<float>(a, s)
                            : run_typed<__nv_bfloat16>(a, s);
+}
+
+// ---------------------------------------------------------------------------
+// Variant without a caller workspace, for callers that cannot allocate device
+// memory (for example a host that hands the library only preallocated input
+// and output buffers, or code running where a device allocation is forbidden
+// because it could synchronise the device or fail under a fixed memory
+// budget).  The per-CTA partial maxima live in a fixed file-scope device
+// array instead of the caller's workspace; every GPU that loads the library
+// keeps this array until the process exits.
+namespace {
+
+constexpr int kStaticParts = 16384;  // floats = 64 KiB; fits B <= 16384
+static __device__ __align__(256) float g_nvfp4_static_parts[kStaticParts];
+
+std::mutex g_static_mu;
+std::unordered_map<int, float*> g_static_ptr;  // device id -> array address
+
+}  // namespace
+
+bool nvfp4_static_fits(int B, int N, int d) {
+  return (long)B * grid_x(B, N, d) <= kStaticParts;
+}
+
+// Looks the array's device address up once per device (with that device
+// current, restoring the caller's current device afterwards).  The first
+// call on a device therefore makes runtime calls that must not happen inside
+// a stream capture.
+cudaError_t nvfp4_static_scratch(int device, float** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  auto it = g_static_ptr.find(device);
+  if (it != g_static_ptr.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return e;
+  if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+  float* p = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_nvfp4_static_parts);
+  if (prev != device) {
+    cudaError_t e2 = cudaSetDevice(prev);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return e;
+  g_static_ptr[device] = p;
+  *out = p;
+  return cudaSuccess;
 }
 
 }  // namespace ps

@@ -22,6 +22,9 @@ struct Nvfp4Args {
 };
 size_t nvfp4_ws(int B, int N, int d);
 cudaError_t nvfp4_run(const Nvfp4Args& a, cudaStream_t s);
+// no-workspace variant: a file-scope device array replaces the workspace
+bool nvfp4_static_fits(int B, int N, int d);
+cudaError_t nvfp4_static_scratch(int device, float** out);
 
 struct ProxyArgs {
   const void* Q; const float* chat; const void* Wk; int dtype;

@@ -226,3 +226,19 @@ def ps_commit(logits, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
         d_ld, _ptr(d_sum), _ptr(d_cnt), _ptr(d_prev), _ptr(suffix_sel), sel_ld, params,
         _ptr(token), _ptr(conf), _ptr(commit), w, wn, _stream(stream))
     _check(st, "ps_commit")
+
+
+def ps_nvfp4_residual_noalloc(H, mu, assign, rho, codes, scales, tensor_scale,
+                              stream=None):
+    """ps_nvfp4_residual without a workspace: for callers that cannot
+    allocate device memory; the library's fixed device array holds the
+    scratch (B <= 16384; overlapping calls on one device race)."""
+    lib = _lib()
+    fn = lib.cdll.ps_nvfp4_residual_noalloc
+    fn.restype = _i
+    fn.argtypes = [_p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]
+    B, N, d = H.shape
+    C = mu.shape[1] if mu is not None else 1
+    st = fn(lib.handle(), _ptr(H), _dtype(H), _ptr(mu), _ptr(assign), _ptr(rho), B, N,
+            d, C, _ptr(codes), _ptr(scales), _ptr(tensor_scale), _stream(stream))
+    _check(st, "ps_nvfp4_residual_noalloc")

@@ -234,6 +234,38 @@ ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
                     ps_commit_params params, int32_t* token, float* conf,
                     uint8_t* commit, void* ws, size_t ws_bytes, void* stream);
 
+
+/* ---------------------------------------------------------------------------
+ * NVFP4 residual quantisation without a workspace.
+ * The paper has no counterpart to this call: it exists for callers that
+ * cannot allocate device memory -- e.g. a host application that gives the
+ * library only preallocated inputs and outputs, or code running where a
+ * cudaMalloc is not allowed because it may synchronise the device or break
+ * a fixed memory budget.
+ *
+ * Computes exactly what ps_nvfp4_residual computes (same arguments, same
+ * bit-exact outputs) but takes no `ws`: its scratch (per-CTA partial maxima)
+ * lives in one fixed 64 KiB file-scope device array inside the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Limit: B <= 16384 (the array holds at most max(608, B) partials);
+ * larger B returns PS_ERR_WORKSPACE and launches nothing.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device made current, then the caller's
+ * current device restored); make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array and leaves the last
+ * call's values in it.  Nothing in it has to start at zero (each call writes
+ * every slot it later reads), but calls that overlap on the GPU -- on
+ * different streams, or from different threads -- race on it and must be
+ * serialised by the caller.
+ * ------------------------------------------------------------------------- */
+ps_status ps_nvfp4_residual_noalloc(ps_handle h, const void* H, int dtype,
+                                    const float* mu, const int32_t* assign,
+                                    const float* rho, int B, int N, int d,
+                                    int C, uint8_t* codes, uint8_t* scales,
+                                    float* tensor_scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
