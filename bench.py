@@ -107,6 +107,44 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def graph_kernel_count(g):
+    """Kernel nodes in a captured step (cudaGraphGetNodes through the CUDA
+    runtime that torch loaded); None if the runtime cannot be reached."""
+    import ctypes
+    import torch
+    try:
+        raw = g.raw_cuda_graph()
+    except Exception:
+        return None
+    rt = None
+    cands = ["libcudart.so.13", "libcudart.so.12", "libcudart.so"]
+    base = os.path.dirname(torch.__file__)
+    cands += glob.glob(os.path.join(base, "lib", "libcudart*.so*"))
+    cands += glob.glob(os.path.join(os.path.dirname(base), "nvidia", "cu*", "lib",
+                                    "libcudart.so*"))
+    for name in cands:
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            pass
+    if rt is None:
+        return None
+    n = ctypes.c_size_t(0)
+    if rt.cudaGraphGetNodes(ctypes.c_void_p(raw), None, ctypes.byref(n)) != 0:
+        return None
+    nodes = (ctypes.c_void_p * n.value)()
+    if rt.cudaGraphGetNodes(ctypes.c_void_p(raw), nodes, ctypes.byref(n)) != 0:
+        return None
+    kind = ctypes.c_int(0)
+    count = 0
+    for k in range(n.value):
+        if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[k]), ctypes.byref(kind)) == 0 \
+                and kind.value == 0:          # cudaGraphNodeTypeKernel
+            count += 1
+    return count
+
+
 def op_work(w, npos_mean):
     """Algorithmic bytes and flops of each op for one window batch."""
     esz = 4 if w.dtype == "f32" else 2
@@ -258,65 +296,96 @@ def main():
     logits = [wl.make_logits(w, t, dev) for t in range(4)]
     u = wl.make_uniforms(w, 0, dev)
     pipe = Pipeline(w, layers=1, device=dev)
-    stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # the step reads its inputs from fixed buffers (graph replay needs fixed
+    # addresses); the next step's inputs are copied in outside the timed events
+    dH, dQ, dL = torch.empty_like(Hs[0]), torch.empty_like(Qs[0]), torch.empty_like(logits[0])
+
+    def load(i):
+        dH.copy_(Hs[i % 4])
+        dQ.copy_(Qs[i % 4])
+        dL.copy_(logits[i % 4])
 
     # window build: k-means++ seeding, first distributions
-    pipe.step([Hs[0]], [Qs[0]], [L["Wk"]], [L["Wv"]], logits[0], init_us=[u], first=True)
+    load(0)
+    pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL, init_us=[u], first=True)
     ops = ["kmeans", "nvfp4", "proxy_kl", "topk", "refresh", "commit"]
 
-    def timed_step(t, ev):
-        i = t % 4
+    def op_calls(parity, ev=None):
+        """One step's six calls, A ping-pong selected by parity."""
         st = pipe.state[0]
-        cur, prev = st.A[pipe.t % 2], st.A[(pipe.t + 1) % 2]
-        H, Q = Hs[i], Qs[i]
-        ev[0].record(stream)
-        ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
+        cur, prev = st.A[parity], st.A[1 - parity]
+        rec = (lambda j: ev[j].record()) if ev is not None else (lambda j: None)
+        rec(0)
+        ps.ps_kmeans_spherical(dH, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
                                objective=st.obj, ws=pipe.ws[ps.OP_KMEANS])
-        ev[1].record(stream)
-        ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+        rec(1)
+        ps.ps_nvfp4_residual(dH, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
                              ws=pipe.ws[ps.OP_NVFP4])
-        ev[2].record(stream)
-        ps.ps_proxy_attn_kl(Q, st.chat, L["Wk"], prev, cur, st.D, w.Hkv,
+        rec(2)
+        ps.ps_proxy_attn_kl(dQ, st.chat, L["Wk"], prev, cur, st.D, w.Hkv,
                             ws=pipe.ws[ps.OP_PROXY_KL])
-        ev[3].record(stream)
+        rec(3)
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
                          st.npos, st.posmask)
-        ev[4].record(stream)
-        ps.ps_refresh_kv(H, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh)
-        ev[5].record(stream)
-        pipe.commit_step(logits[i])
-        ev[6].record(stream)
-        pipe.t += 1
+        rec(4)
+        ps.ps_refresh_kv(dH, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh,
+                         ws=pipe.ws[ps.OP_REFRESH])
+        rec(5)
+        pipe.commit_step(dL)
+        rec(6)
 
     def mk():
         return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
 
-    for t in range(args.warmup):
-        flush.zero_()
-        timed_step(t, mk())
+    step_no = 1
+    for t in range(args.warmup):                    # eager warm-up
+        load(step_no)
+        op_calls(step_no % 2)
+        step_no += 1
     torch.cuda.synchronize()
     ps.ps_check()
 
-    events = [mk() for _ in range(args.steps)]
+    # capture one graph per A ping-pong parity
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    for parity in (0, 1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            op_calls(parity)
+        graphs.append(g)
+    launches = graph_kernel_count(graphs[0])
+    if launches is None:                            # runtime not reachable: plan count
+        launches = pipe.kernel_launches_per_step()
+    stream = torch.cuda.current_stream(dev)
+    for t in range(args.warmup):                    # graph warm-up
+        load(step_no)
+        graphs[step_no % 2].replay()
+        step_no += 1
+    torch.cuda.synchronize()
+    ps.ps_check()
+
+    # timed region: K graph replays, L2 flushed and inputs staged between them
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    npos_seen = []
     for t in range(args.steps):
+        load(step_no)
         flush.zero_()
-        timed_step(args.warmup + t, events[t])
+        gev[t][0].record(stream)
+        graphs[step_no % 2].replay()
+        gev[t][1].record(stream)
+        step_no += 1
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ps.ps_check()
-    npos_seen.append(int(pipe.state[0].npos.sum()))
-    per_step = [ev[0].elapsed_time(ev[6]) for ev in events]
-    per_op = {op: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, op in enumerate(ops)}
-    total_ms = sum(per_step)
+    total_ms = sum(a.elapsed_time(b) for a, b in gev)
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -324,12 +393,24 @@ def main():
     ms_step = total_ms / args.steps
     steps_per_s = world * args.steps / (total_ms / 1000.0)
 
+    # per-op breakdown: the same steps eagerly, events between the calls
+    events = [mk() for _ in range(args.steps)]
+    for t in range(args.steps):
+        load(step_no)
+        flush.zero_()
+        op_calls(step_no % 2, events[t])
+        step_no += 1
+    torch.cuda.synchronize()
+    ps.ps_check()
+    npos_seen = [int(pipe.state[0].npos.sum())]
+    per_op = {op: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, op in enumerate(ops)}
+    eager_ms = statistics.mean(ev[0].elapsed_time(ev[6]) for ev in events)
+
     # end to end through the public API: inputs from pinned host memory every
     # step, the step's results read back
     hH = [H.cpu().pin_memory() for H in Hs]
     hQ = [Q.cpu().pin_memory() for Q in Qs]
     hL = [x.cpu().pin_memory() for x in logits]
-    dH, dQ, dL = torch.empty_like(Hs[0]), torch.empty_like(Qs[0]), torch.empty_like(logits[0])
     out = [torch.empty(pipe.token.shape, dtype=torch.int32).pin_memory(),
            torch.empty(pipe.conf.shape).pin_memory(),
            torch.empty(pipe.commit.shape, dtype=torch.uint8).pin_memory(),
@@ -337,20 +418,22 @@ def main():
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     for t in range(args.warmup + args.steps):
-        i = t % 4
-        if t >= args.warmup:
+        i = step_no % 4
+        timed = t >= args.warmup
+        if timed:
             flush.zero_()
             e2e_ev[t - args.warmup][0].record(stream)
         dH.copy_(hH[i], non_blocking=True)
         dQ.copy_(hQ[i], non_blocking=True)
         dL.copy_(hL[i], non_blocking=True)
-        pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL)
+        graphs[step_no % 2].replay()
         out[0].copy_(pipe.token, non_blocking=True)
         out[1].copy_(pipe.conf, non_blocking=True)
         out[2].copy_(pipe.commit, non_blocking=True)
         out[3].copy_(pipe.state[0].D, non_blocking=True)
-        if t >= args.warmup:
+        if timed:
             e2e_ev[t - args.warmup][1].record(stream)
+        step_no += 1
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     if world > 1:
@@ -395,7 +478,9 @@ def main():
         "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
                 for op in ops},
         "clocks": clk,
-        "gpu_launches": pipe.kernel_launches_per_step() * args.steps,
+        "gpu_launches": launches * args.steps,
+        "eager_ms_per_step": eager_ms,
+        "timing": "CUDA-graph replay of the whole step per timed step",
         "parallelism": f"replicas x{world}",
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -113,7 +113,7 @@ size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
       return (N > 0 && C > 0 && Hkv > 0 && dh > 0 && Hq > 0)
                  ? proxy_ws(B, N, d, C, Hq, Hkv, dh) : 0;
     case PS_OP_TOPK: return 0;
-    case PS_OP_REFRESH: return 0;
+    case PS_OP_REFRESH: return (N > 0 && d > 0) ? refresh_ws(B, N, d) : 0;
     case PS_OP_COMMIT: return (P > 0 && V > 0) ? commit_ws(B, P, V) : 0;
   }
   return 0;
@@ -182,7 +182,7 @@ ps_status ps_proxy_attn_kl(ps_handle h, const void* Q, const float* chat,
   ps_status st = check_ws(proxy_ws(B, N, d, C, Hq, Hkv, dh), ws, ws_bytes);
   if (st != PS_OK) return st;
   ProxyArgs a{Q, chat, Wk, dtype, B, N, d, C, Hq, Hkv, dh, A_prev, A_cur, D, ws,
-              h->num_sms};
+              h->num_sms, h->status};
   return launch_status(proxy_run(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -208,7 +208,6 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
                         int Hkv, int dh, void* Kcache, void* Vcache,
                         int Ncache, int cache_off, void* ws, size_t ws_bytes,
                         void* stream) {
-  (void)ws; (void)ws_bytes;
   PS_REQUIRE(h != nullptr && dtype_ok(dtype) && B >= 0);
   if (B == 0) return PS_OK;
   PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && Hkv >= 1 && dh > 0 && dh % 16 == 0);
@@ -216,8 +215,14 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
   PS_REQUIRE(2L * ceil_div((long)Hkv * dh, 64) <= 65535);
   PS_PTR(H); PS_NN(pos); PS_NN(npos); PS_PTR(Wk); PS_PTR(Wv);
   PS_NN(Kcache); PS_NN(Vcache);
+  const bool tc = refresh_tc_ok(dtype, Hkv, dh);
+  if (tc) {
+    PS_PTR(Kcache); PS_PTR(Vcache);
+    ps_status st = check_ws(refresh_ws(B, N, d), ws, ws_bytes);
+    if (st != PS_OK) return st;
+  }
   RefreshArgs a{H, dtype, pos, npos, Wk, Wv, B, N, d, Hkv, dh, Kcache, Vcache,
-                Ncache, cache_off, h->num_sms};
+                Ncache, cache_off, h->num_sms, tc ? ws : nullptr, h->status};
   return launch_status(refresh_run(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -6,15 +6,22 @@
 // sum of unit rows.  Deterministic: every reduction runs in a fixed order.
 //
 // Kernels (one launch each, all on the caller's stream):
-//   k_inv_norm   1/||h_i||                                  (one warp per row)
-//   k_kpp        k-means++ seeding, one CTA per window      (init_mode 1)
-//   k_assign     64-row x 128-centroid dot tiles, arg-max    (per pass)
-//   k_sort       stable counting sort of rows by cluster    (per pass)
-//   k_update     centroid = normalise(sum of member rows)   (passes < I)
-//   k_finalize   C_hat = mean(rho over members) * mu
+//   k_inv_norm      1/||h_i||                                (one warp per row)
+//   k_kpp           k-means++ seeding, one CTA per window    (init_mode 1)
+//   k_split_mu      mu -> (mu_hi, mu_lo) bf16 for the tensor cores
+//   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
+//                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
+//                   d; the last CTA of a tile sums the partials in split
+//                   order and takes the arg-max.  fp32 windows: k_assign on
+//                   CUDA cores.
+//   k_cluster_scan  per (cluster, window): members in ascending row order,
+//                   centroid = normalise(sum of unit rows) (+ bf16 split), or
+//                   on the last pass C_hat = mean(rho) * mu; counts; objective
+#include <algorithm>
 #include <climits>
 
 #include "ops.h"
+#include "tc_gemm.cuh"
 #include "vec.cuh"
 
 namespace ps {
@@ -242,187 +249,326 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
   }
 }
 
-// Stable counting sort of one window's rows by cluster: counts, offsets and
-// the permutation (ascending row order inside each cluster).  Also folds the
-// per-tile objective partials of the pass in tile order.
-__global__ void __launch_bounds__(1024)
-k_sort(const int32_t* __restrict__ assign, int N, int C,
-       int32_t* __restrict__ counts, int32_t* __restrict__ offs,
-       int32_t* __restrict__ perm, const float* __restrict__ objp, int ntile,
-       float* __restrict__ obj, int obj_ld, int pass) {
-  extern __shared__ int sm[];
-  int* cnt = sm;            // C
-  int* base = sm + C;       // C: next write position of each cluster
-  int* wc = sm + 2 * C;     // 32 x C: per-warp counts, then write bases
-  __shared__ int s_scan[32];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t* a = assign + (long)b * N;
-  for (int c = tid; c < C; c += blockDim.x) cnt[c] = 0;
-  __syncthreads();
-  for (int i = tid; i < N; i += blockDim.x) {
-    const int c = a[i];
-    if (c >= 0 && c < C) atomicAdd(&cnt[c], 1);
+// fp32 centroids -> bf16 hi + lo parts (hi = bf16(mu), lo = bf16(mu - hi));
+// also clears the tile counters of the split reduction.
+__global__ void k_split_mu(const float* __restrict__ mu, long n, __nv_bfloat16* __restrict__ hi,
+                           __nv_bfloat16* __restrict__ lo, int* __restrict__ counters,
+                           int ncounters) {
+  const long stride = (long)gridDim.x * blockDim.x;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float x = mu[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
   }
-  __syncthreads();
-  const int v = tid < C ? cnt[tid] : 0;
-  int total;
-  const int ex = block_exclusive_scan<int>(v, s_scan, &total);
-  if (tid < C) {
-    offs[(long)b * (C + 1) + tid] = ex;
-    base[tid] = ex;
-    counts[(long)b * C + tid] = v;
-  }
-  if (tid == 0) offs[(long)b * (C + 1) + C] = total;
-  __syncthreads();
-  const unsigned lt = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < N; c0 += blockDim.x) {
-    for (int e = tid; e < 32 * C; e += blockDim.x) wc[e] = 0;
-    __syncthreads();
-    const int i = c0 + tid;
-    int c = i < N ? a[i] : -1;
-    if (c >= C) c = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, c);
-    const int rank = __popc(peers & lt);
-    if (c >= 0 && rank == 0) wc[warp * C + c] = __popc(peers);
-    __syncthreads();
-    if (tid < C) {
-      int run = base[tid];
-      for (int w = 0; w < 32; ++w) {
-        const int t = wc[w * C + tid];
-        wc[w * C + tid] = run;
-        run += t;
-      }
-      base[tid] = run;
-    }
-    __syncthreads();
-    if (c >= 0) perm[(long)b * N + wc[warp * C + c] + rank] = i;
-    __syncthreads();
-  }
-  if (obj != nullptr && tid == 0) {
-    float s = 0.f;
-    for (int t = 0; t < ntile; ++t) s += objp[(long)b * ntile + t];
-    obj[(long)b * obj_ld + pass] = s;
-  }
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < ncounters; i += stride)
+    counters[i] = 0;
 }
 
-// New centroid of cluster (blockIdx.x, window blockIdx.y): the normalised
-// sum of its members' unit rows, accumulated in ascending row order.
-template <typename T>
+// Epilogue of the tensor-core assignment.  Tile t = (window b, 128-row block
+// mt).  With one d-chunk the arg-max is taken straight from the accumulator;
+// otherwise every chunk stores its partial scores [z][c][row] and the last
+// CTA to finish a tile (tile counter) sums them in chunk order.
+template <int BN>
+struct KmAssignEpi : TcEpiBase {
+  int B, N, C, mtb, nz;
+  float* part;
+  int* counters;
+  const float* inv;
+  int32_t* assign;
+  float* best;
+  float* objp;
+  struct State {
+    float bv;
+    int bi;
+  };
+  __device__ int tiles(int) const { return B * mtb; }
+  __device__ int arow(int t) const { return (t / mtb) * N + (t % mtb) * 128; }
+  __device__ int bcoord(int t, int n0) const { return (t / mtb) * C + n0; }
+  __device__ void consume(int t, int r, int, int z, uint32_t taddr, State& st) const {
+    const int b = t / mtb, i = (t % mtb) * 128 + r;
+    const long ld = (long)B * N;
+    st.bv = -INFINITY;
+    st.bi = INT_MAX;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+      if (nz == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < C && v[j] > st.bv) { st.bv = v[j]; st.bi = c0 + j; }
+      } else if (i < N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < C) part[((long)z * C + c0 + j) * ld + (long)b * N + i] = v[j];
+      }
+    }
+  }
+  __device__ void tile_done(int t, int r, int, int, uint8_t* scratch, State& st) const {
+    const int b = t / mtb, i = (t % mtb) * 128 + r;
+    int* flag = reinterpret_cast<int*>(scratch);
+    float* wsum = reinterpret_cast<float*>(scratch + 16);
+    if (nz > 1) {
+      __threadfence();
+      epi_bar_sync();
+      if (r == 0) flag[0] = (atomicAdd(&counters[t], 1) == nz - 1) ? 1 : 0;
+      epi_bar_sync();
+      const bool last = flag[0] != 0;
+      epi_bar_sync();
+      if (!last) return;
+      __threadfence();
+      st.bv = -INFINITY;
+      st.bi = INT_MAX;
+      if (i < N) {
+        const long ld = (long)B * N;
+        for (int c = 0; c < C; ++c) {
+          float sum = 0.f;
+          for (int zz = 0; zz < nz; ++zz)
+            sum += __ldcg(&part[((long)zz * C + c) * ld + (long)b * N + i]);
+          if (sum > st.bv) { st.bv = sum; st.bi = c; }
+        }
+      }
+      if (r == 0) counters[t] = 0;
+    }
+    float cs = 0.f;
+    if (i < N) {
+      if (st.bi == INT_MAX) { st.bi = 0; st.bv = 0.f; }
+      assign[(long)b * N + i] = st.bi;
+      best[(long)b * N + i] = st.bv;
+      cs = st.bv * inv[(long)b * N + i];
+    }
+    cs = warp_sum(cs);
+    if ((r & 31) == 0) wsum[r >> 5] = cs;
+    epi_bar_sync();
+    if (r == 0) objp[t] = ((wsum[0] + wsum[1]) + wsum[2]) + wsum[3];
+    epi_bar_sync();
+  }
+};
+
+// Per (cluster c, window b): members in ascending row order, 256 rows at a
+// time.  Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the
+// cluster is empty or its sum is zero), plus its bf16 split.  Final pass:
+// C_hat_c = mean(rho over members) * mu_c (kept when empty).  Both write the
+// cluster size; CTA (0, b) folds the pass objective from the tile partials.
+template <typename T, bool FINAL>
 __global__ void __launch_bounds__(256)
-k_update(const T* __restrict__ H, const float* __restrict__ inv, int N, int d,
-         int C, const int32_t* __restrict__ perm, const int32_t* __restrict__ offs,
-         const int32_t* __restrict__ counts, float* __restrict__ mu) {
+k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
+               const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
+               int d, int C, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
+               __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
+               float* __restrict__ chat, const float* __restrict__ objp, int ntile,
+               float* __restrict__ obj, int obj_ld, int pass) {
   constexpr int V = Vec<T>::n;
   constexpr int G = kMaxD / (256 * V);
+  __shared__ int list[256];
+  __shared__ int s_scan[32];
   __shared__ float s_red[8];
   const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int n = counts[(long)b * C + c];
-  if (n == 0) return;
-  const int start = offs[(long)b * (C + 1) + c];
   float u[G][V];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int e = 0; e < V; ++e) u[g][e] = 0.f;
-  for (int m = 0; m < n; ++m) {
-    const int row = perm[(long)b * N + start + m];
-    const float s = inv[(long)b * N + row];
-    const T* h = H + ((long)b * N + row) * d;
+  float rs = 0.f;
+  int n = 0;
+  for (int base = 0; base < N; base += 256) {
+    const int i = base + tid;
+    const int f = (i < N && assign[(long)b * N + i] == c) ? 1 : 0;
+    int tot;
+    const int ex = block_exclusive_scan<int>(f, s_scan, &tot);
+    if (f) list[ex] = i;
+    __syncthreads();
+    if constexpr (FINAL) {
+      if (tid < tot) rs += rho[(long)b * N + list[tid]];
+    } else {
+      for (int m = 0; m < tot; ++m) {
+        const int row = list[m];
+        const float sc = inv[(long)b * N + row];
+        const T* h = H + ((long)b * N + row) * d;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int col = (g * 256 + tid) * V;
+          if (col < d) {
+            float v[V];
+            load16(h + col, v);
+#pragma unroll
+            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc, u[g][e]);
+          }
+        }
+      }
+    }
+    n += tot;
+    __syncthreads();
+  }
+  if (c == 0 && tid == 0 && obj != nullptr) {
+    float so = 0.f;
+    for (int t = 0; t < ntile; ++t) so += objp[(long)b * ntile + t];
+    obj[(long)b * obj_ld + pass] = so;
+  }
+  if (tid == 0) counts[(long)b * C + c] = n;
+  if constexpr (FINAL) {
+    const float tot = block_sum_f32(rs, s_red);
+    if (n == 0) return;
+    const float mean = tot / (float)n;
+    const float* m = mu + ((long)b * C + c) * d;
+    float* o = chat + ((long)b * C + c) * d;
+    for (int k = tid; k < d; k += 256) o[k] = mean * m[k];
+  } else {
+    float ss = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
+    ss = block_sum_f32(ss, s_red);
+    const float nu = sqrtf(ss);
+    if (n == 0 || !(nu > 0.f)) return;
+    const long ro = ((long)b * C + c) * d;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int col = (g * 256 + tid) * V;
       if (col < d) {
-        float v[V];
-        load16(h + col, v);
 #pragma unroll
-        for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], s, u[g][e]);
+        for (int e = 0; e < V; ++e) {
+          const float x = u[g][e] / nu;
+          mu[ro + col + e] = x;
+          if (mu_hi != nullptr) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            mu_hi[ro + col + e] = h;
+            mu_lo[ro + col + e] = __float2bfloat16_rn(x - __bfloat162float(h));
+          }
+        }
       }
-    }
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
-  ss = block_sum_f32(ss, s_red);
-  const float nu = sqrtf(ss);
-  if (!(nu > 0.f)) return;
-  float* out = mu + ((long)b * C + c) * d;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int col = (g * 256 + tid) * V;
-    if (col < d) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) out[col + e] = u[g][e] / nu;
     }
   }
 }
 
-__global__ void __launch_bounds__(256)
-k_finalize(const float* __restrict__ rho, int N, int d, int C,
-           const int32_t* __restrict__ perm, const int32_t* __restrict__ offs,
-           const int32_t* __restrict__ counts, const float* __restrict__ mu,
-           float* __restrict__ chat) {
-  __shared__ float s_red[8];
-  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int n = counts[(long)b * C + c];
-  if (n == 0) return;
-  const int start = offs[(long)b * (C + 1) + c];
-  float s = 0.f;
-  for (int m = tid; m < n; m += blockDim.x)
-    s += rho[(long)b * N + perm[(long)b * N + start + m]];
-  s = block_sum_f32(s, s_red);
-  const float mean = s / (float)n;
-  const float* m = mu + ((long)b * C + c) * d;
-  float* o = chat + ((long)b * C + c) * d;
-  for (int k = tid; k < d; k += blockDim.x) o[k] = mean * m[k];
+struct KmPlan {
+  bool tc;
+  int BN, mtb, nz, kpc, KB;
+  int ntile;  // objective partials per window
+};
+
+int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p *= 2;
+  return p;
+}
+
+KmPlan km_plan(int dtype, int B, int N, int d, int C) {
+  KmPlan p{};
+  p.tc = dtype == PS_BF16 && C <= 256;
+  if (p.tc) {
+    p.BN = pow2_at_least(C);
+    p.mtb = ceil_div(N, 128);
+    p.KB = ceil_div(d, 64);
+    const int tiles = B * p.mtb;
+    int nz = std::min(16, std::max(1, ceil_div(kSmTarget, tiles)));
+    nz = std::min(nz, p.KB);
+    p.kpc = ceil_div(p.KB, nz);
+    p.nz = ceil_div(p.KB, p.kpc);
+    p.ntile = p.mtb;
+  } else {
+    p.ntile = ceil_div(N, kTileRows);
+  }
+  return p;
+}
+
+struct KmWs {
+  float* inv;
+  float* objp;
+  float* w;
+  int8_t* chosen;
+  __nv_bfloat16* mu_hi;
+  __nv_bfloat16* mu_lo;
+  float* part;
+  int* counters;
+};
+
+KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* bytes) {
+  Carver cv(base);
+  KmWs w{};
+  const long BN_ = (long)B * N;
+  w.inv = cv.take<float>(BN_);
+  w.objp = cv.take<float>((size_t)B * p.ntile);
+  w.w = cv.take<float>(BN_);
+  w.chosen = cv.take<int8_t>(BN_);
+  if (p.tc) {
+    w.mu_hi = cv.take<__nv_bfloat16>((size_t)B * C * d);
+    w.mu_lo = cv.take<__nv_bfloat16>((size_t)B * C * d);
+    w.part = p.nz > 1 ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
+    w.counters = cv.take<int>((size_t)B * p.mtb);
+  }
+  if (bytes != nullptr) *bytes = cv.bytes();
+  return w;
+}
+
+template <int BN>
+cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaStream_t s) {
+  TcMaps maps;
+  const long rows = (long)a.B * a.N;
+  if (!make_tmap_bf16_2d(&maps.a[0], a.H, a.d, rows, (uint64_t)a.d * 2, 64, 128) ||
+      !make_tmap_bf16_2d(&maps.b[0], w.mu_hi, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2, 64,
+                         BN) ||
+      !make_tmap_bf16_2d(&maps.b[1], w.mu_lo, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2, 64,
+                         BN))
+    return cudaErrorInvalidValue;
+  maps.a[1] = maps.a[0];
+  TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status};
+  KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.counters, w.inv,
+                      a.assign, a.rho, w.objp};
+  return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
 }
 
 template <typename T>
 cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const T* H = static_cast<const T*>(a.H);
-  const long BN = (long)a.B * a.N;
-  const int ntile = ceil_div(a.N, kTileRows);
-  Carver cv(a.ws);
-  float* inv = cv.take<float>(BN);
-  int32_t* perm = cv.take<int32_t>(BN);
-  int32_t* offs = cv.take<int32_t>((size_t)a.B * (a.C + 1));
-  float* objp = cv.take<float>((size_t)a.B * ntile);
-  float* w = cv.take<float>(BN);
-  int8_t* chosen = cv.take<int8_t>(BN);
+  const long BN_ = (long)a.B * a.N;
+  const KmPlan p = km_plan(a.dtype, a.B, a.N, a.d, a.C);
+  const KmWs w = km_carve(a.ws, p, a.B, a.N, a.d, a.C, nullptr);
 
-  k_inv_norm<T><<<ceil_div(BN * 32, 256), 256, 0, s>>>(H, BN, a.d, inv);
+  k_inv_norm<T><<<ceil_div(BN_ * 32, 256), 256, 0, s>>>(H, BN_, a.d, w.inv);
   if (a.init_mode == 1)
-    k_kpp<T><<<a.B, 1024, a.d * sizeof(float), s>>>(H, inv, a.init_u, a.N, a.d,
-                                                    a.C, a.mu, w, chosen);
-  const size_t sort_smem = (size_t)34 * a.C * sizeof(int);
-  for (int t = 0; t <= a.iters; ++t) {
-    k_assign<T><<<dim3(ntile, a.B), 256, 0, s>>>(H, a.mu, inv, a.N, a.d, a.C,
-                                                 a.assign, a.rho, objp);
-    k_sort<<<a.B, 1024, sort_smem, s>>>(a.assign, a.N, a.C, a.counts, offs,
-                                        perm, objp, ntile, a.obj, a.iters + 1, t);
-    if (t < a.iters)
-      k_update<T><<<dim3(a.C, a.B), 256, 0, s>>>(H, inv, a.N, a.d, a.C, perm,
-                                                  offs, a.counts, a.mu);
+    k_kpp<T><<<a.B, 1024, a.d * sizeof(float), s>>>(H, w.inv, a.init_u, a.N, a.d, a.C, a.mu,
+                                                    w.w, w.chosen);
+  if (p.tc) {
+    const long n = (long)a.B * a.C * a.d;
+    k_split_mu<<<std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s>>>(
+        a.mu, n, w.mu_hi, w.mu_lo, w.counters, a.B * p.mtb);
   }
-  k_finalize<<<dim3(a.C, a.B), 256, 0, s>>>(a.rho, a.N, a.d, a.C, perm, offs,
-                                            a.counts, a.mu, a.chat);
+  for (int t = 0; t <= a.iters; ++t) {
+    cudaError_t e = cudaSuccess;
+    if (p.tc) {
+      switch (p.BN) {
+        case 32: e = assign_tc<32>(a, p, w, s); break;
+        case 64: e = assign_tc<64>(a, p, w, s); break;
+        case 128: e = assign_tc<128>(a, p, w, s); break;
+        default: e = assign_tc<256>(a, p, w, s); break;
+      }
+    } else {
+      k_assign<T><<<dim3(p.ntile, a.B), 256, 0, s>>>(H, a.mu, w.inv, a.N, a.d, a.C,
+                                                     a.assign, a.rho, w.objp);
+    }
+    if (e != cudaSuccess) return e;
+    if (t < a.iters)
+      k_cluster_scan<T, false><<<dim3(a.C, a.B), 256, 0, s>>>(
+          H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, p.tc ? w.mu_hi : nullptr,
+          w.mu_lo, a.counts, a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
+  }
+  k_cluster_scan<T, true><<<dim3(a.C, a.B), 256, 0, s>>>(
+      H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, nullptr, nullptr, a.counts, a.chat,
+      w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t kmeans_ws(int B, int N, int d, int C) {
-  (void)d;
-  Carver cv(nullptr);
-  const long BN = (long)B * N;
-  cv.take<float>(BN);
-  cv.take<int32_t>(BN);
-  cv.take<int32_t>((size_t)B * (C + 1));
-  cv.take<float>((size_t)B * ceil_div(N, kTileRows));
-  cv.take<float>(BN);
-  cv.take<int8_t>(BN);
-  return cv.bytes();
+  // dtype-independent: the larger of the tensor-core and CUDA-core plans
+  size_t tc = 0, simt = 0;
+  km_carve(nullptr, km_plan(PS_BF16, B, N, d, C), B, N, d, C, &tc);
+  km_carve(nullptr, km_plan(PS_F32, B, N, d, C), B, N, d, C, &simt);
+  return std::max(tc, simt);
 }
 
 cudaError_t kmeans_run(const KmeansArgs& a, cudaStream_t s) {

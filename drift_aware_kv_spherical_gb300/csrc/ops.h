@@ -30,6 +30,7 @@ struct ProxyArgs {
   const void* Q; const float* chat; const void* Wk; int dtype;
   int B, N, d, C, Hq, Hkv, dh;
   const float* A_prev; float* A_cur; float* D; void* ws; int num_sms;
+  int* status;
 };
 size_t proxy_ws(int B, int N, int d, int C, int Hq, int Hkv, int dh);
 cudaError_t proxy_run(const ProxyArgs& a, cudaStream_t s);
@@ -45,7 +46,10 @@ struct RefreshArgs {
   const void* H; int dtype; const int32_t* pos; const int32_t* npos;
   const void* Wk; const void* Wv; int B, N, d, Hkv, dh;
   void* Kc; void* Vc; int Ncache, cache_off; int num_sms;
+  void* ws; int* status;
 };
+bool refresh_tc_ok(int dtype, int Hkv, int dh);
+size_t refresh_ws(int B, int N, int d);
 cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s);
 
 struct CommitArgs {

@@ -10,6 +10,15 @@
 //   k_proxy         16 window rows x all C centroids per CTA, a slice of the
 //                   heads per CTA: scores, per-head softmax, head sum
 //   k_proxy_final   sums the head-slice partials, A = sum / Hq, KL
+// bf16 inputs take the tensor-core path instead (C <= 128, dh % 64 == 0):
+//   k_split_f32     C_hat -> bf16 hi + lo
+//   tcgen05 GEMM    K~ = C_hat_hi W_k + C_hat_lo W_k, W_k streamed through
+//                   TMA as MN-major tiles, split over d with a last-CTA
+//                   reduction; written as K~_hi, K~_lo (bf16)
+//   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
+//                   in TMEM, softmax over the C columns in the epilogue,
+//                   head sum in registers; the last head slice of a tile
+//                   sums the slice partials, divides by Hq and takes the KL
 // Every reduction has a fixed order, so identical inputs give identical
 // bits and KL(A || A) is exactly 0.
 #include <algorithm>
@@ -17,6 +26,7 @@
 
 #include "gemm_simt.cuh"
 #include "ops.h"
+#include "tc_gemm.cuh"
 
 namespace ps {
 namespace {
@@ -204,6 +214,290 @@ k_proxy_final(const float* __restrict__ part, int nslice, int B, int N, int C,
   proxy_finish<NJ>(Aacc, Hq, b, i, N, C, A_prev, A_cur, D);
 }
 
+// ------------------------------------------------------------ tensor cores
+__global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* __restrict__ hi,
+                            __nv_bfloat16* __restrict__ lo, int* __restrict__ zero,
+                            int nzero) {
+  const long stride = (long)gridDim.x * blockDim.x;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float v = x[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += stride) zero[i] = 0;
+}
+
+__device__ __forceinline__ void split_store(__nv_bfloat16* hi, __nv_bfloat16* lo, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *hi = h;
+  *lo = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// K~ tile epilogue: rows of B*C centroids, 64 key columns.  One d-chunk:
+// split and store.  Several: store fp32 partials [z][M][nkv]; the last CTA
+// of the (row tile, column tile) sums them in chunk order.
+struct CkeysEpi : TcEpiBase {
+  int M, nkv, nz;
+  float* part;
+  int* counters;   // [row tiles][column tiles]
+  __nv_bfloat16* khi;
+  __nv_bfloat16* klo;
+  struct State {};
+  __device__ int tiles(int) const { return (M + 127) / 128; }
+  __device__ int arow(int t) const { return t * 128; }
+  __device__ int bcoord(int, int n0) const { return n0; }
+  __device__ void consume(int t, int r, int n0, int z, uint32_t taddr, State&) const {
+    const int m = t * 128 + r;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+      if (m >= M) continue;
+      const long o = (long)m * nkv + n0 + c0;
+      if (nz == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) split_store(khi + o + j, klo + o + j, v[j]);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(part + (long)z * M * nkv + o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+    }
+  }
+  __device__ void tile_done(int t, int r, int n0, int, uint8_t* scratch, State&) const {
+    if (nz == 1) return;
+    int* flag = reinterpret_cast<int*>(scratch);
+    int* ctr = counters + (long)t * (nkv / 64) + n0 / 64;
+    __threadfence();
+    epi_bar_sync();
+    if (r == 0) flag[0] = (atomicAdd(ctr, 1) == nz - 1) ? 1 : 0;
+    epi_bar_sync();
+    const bool last = flag[0] != 0;
+    epi_bar_sync();
+    if (!last) return;
+    __threadfence();
+    const int m = t * 128 + r;
+    if (m < M) {
+      for (int c = 0; c < 64; ++c) {
+        const long o = (long)m * nkv + n0 + c;
+        float sum = 0.f;
+        for (int zz = 0; zz < nz; ++zz) sum += __ldcg(part + (long)zz * M * nkv + o);
+        split_store(khi + o, klo + o, sum);
+      }
+    }
+    if (r == 0) *ctr = 0;
+  }
+};
+
+// Proxy epilogue.  Tiles t = ((b * mtb + mt) * Hq + h), taken in blocks of
+// hps heads per CTA.  Per head: softmax of the row's C scores (scaled by
+// 1/sqrt(dh)) added to the row's head sum A (registers).  After the slice's
+// last head: one slice -> A / Hq, KL, store; several -> store the partial,
+// and the last slice CTA of the tile sums the partials in slice order.
+template <int BN>
+struct ProxyEpi : TcEpiBase {
+  static constexpr bool kA3D = true;
+  static constexpr bool kBlocked = true;
+  int B, N, C, Hq, G, dh, mtb, hps, nslice;
+  float scale;
+  const float* A_prev;
+  float* A_cur;
+  float* D;
+  float* part;      // [nslice][B*N][C]
+  int* counters;    // [B*mtb]
+  struct State {
+    float A[BN];
+  };
+  __device__ int tiles(int) const { return B * mtb * Hq; }
+  __device__ int arow(int t) const {
+    const int bm = t / Hq;
+    return (bm / mtb) * N + (bm % mtb) * 128;
+  }
+  __device__ int ahead(int t) const { return t % Hq; }
+  __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
+  __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
+  __device__ void consume(int t, int, int, int, uint32_t taddr, State& st) const {
+    const int h = t % Hq;
+    if (h % hps == 0) {
+#pragma unroll
+      for (int c = 0; c < BN; ++c) st.A[c] = 0.f;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < C) m = fmaxf(m, v[j] * scale);
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < C) sum += expf(v[j] * scale - m);
+    }
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < C) st.A[c0 + j] += expf(v[j] * scale - m) / sum;
+    }
+  }
+  __device__ void finish(int b, int i, const float* Aacc) const {
+    const float hq = (float)Hq;
+    const long row = (long)b * N + i;
+    float kl = 0.f;
+#pragma unroll
+    for (int c = 0; c < BN; ++c) {
+      if (c < C) {
+        const float a = Aacc[c] / hq;
+        A_cur[row * C + c] = a;
+        if (A_prev != nullptr && a > 0.f)
+          kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
+      }
+    }
+    D[row] = A_prev != nullptr ? fmaxf(kl, 0.f) : 0.f;
+  }
+  __device__ void tile_done(int t, int r, int, int, uint8_t* scratch, State& st) const {
+    const int h = t % Hq;
+    if ((h + 1) % hps != 0 && h + 1 != Hq) return;
+    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const bool live = i < N;
+    if (nslice == 1) {
+      if (live) finish(b, i, st.A);
+      return;
+    }
+    const int slice = h / hps;
+    const long ld = (long)B * N;
+    if (live) {
+      float* dst = part + ((long)slice * ld + (long)b * N + i) * C;
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        if (c < C) dst[c] = st.A[c];
+    }
+    int* flag = reinterpret_cast<int*>(scratch);
+    __threadfence();
+    epi_bar_sync();
+    if (r == 0) flag[0] = (atomicAdd(&counters[bm], 1) == nslice - 1) ? 1 : 0;
+    epi_bar_sync();
+    const bool last = flag[0] != 0;
+    epi_bar_sync();
+    if (!last) return;
+    __threadfence();
+    if (live) {
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        float sum = 0.f;
+        if (c < C)
+          for (int sl = 0; sl < nslice; ++sl)
+            sum += __ldcg(part + ((long)sl * ld + (long)b * N + i) * C + c);
+        st.A[c] = sum;
+      }
+      finish(b, i, st.A);
+    }
+    if (r == 0) counters[bm] = 0;
+  }
+};
+
+struct TcPlan {
+  bool ok;
+  int BN, mtb, nslice, hps;             // proxy
+  int ck_mt, ck_nt, ck_nz, ck_kpc, KB;  // centroid keys
+};
+
+TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
+  TcPlan p{};
+  const int nkv = Hkv * dh;
+  p.ok = dtype == PS_BF16 && C <= 128 && dh % 64 == 0 && nkv % 64 == 0;
+  if (!p.ok) return p;
+  p.BN = C <= 32 ? 32 : (C <= 64 ? 64 : 128);
+  p.mtb = ceil_div(N, 128);
+  const int want = std::max(1, ceil_div(kSmTarget, B * p.mtb));
+  p.nslice = 1;
+  for (int sl = std::min(want, Hq); sl >= 1; --sl)
+    if (Hq % sl == 0) { p.nslice = sl; break; }
+  p.hps = Hq / p.nslice;
+  p.KB = ceil_div(d, 64);
+  p.ck_mt = ceil_div(B * C, 128);
+  p.ck_nt = nkv / 64;
+  int nz = std::max(1, std::min(8, ceil_div(kSmTarget, p.ck_mt * p.ck_nt)));
+  nz = std::min(nz, p.KB);
+  p.ck_kpc = ceil_div(p.KB, nz);
+  p.ck_nz = ceil_div(p.KB, p.ck_kpc);
+  return p;
+}
+
+struct TcWs {
+  __nv_bfloat16 *chi, *clo, *khi, *klo;
+  float *kpart, *apart;
+  int* ctr;      // key counters then proxy counters
+  int nctr;
+};
+
+TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, size_t* bytes) {
+  Carver cv(base);
+  TcWs w{};
+  w.chi = cv.take<__nv_bfloat16>((size_t)B * C * d);
+  w.clo = cv.take<__nv_bfloat16>((size_t)B * C * d);
+  w.khi = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
+  w.klo = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
+  w.kpart = p.ck_nz > 1 ? cv.take<float>((size_t)p.ck_nz * B * C * nkv) : nullptr;
+  w.apart = p.nslice > 1 ? cv.take<float>((size_t)p.nslice * B * N * C) : nullptr;
+  w.nctr = p.ck_mt * p.ck_nt + B * p.mtb;
+  w.ctr = cv.take<int>((size_t)w.nctr);
+  if (bytes) *bytes = cv.bytes();
+  return w;
+}
+
+template <int BN>
+cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
+  const int nkv = a.Hkv * a.dh;
+  const TcWs w = tc_carve(a.ws, p, a.B, a.N, a.d, a.C, nkv, nullptr);
+  int* kctr = w.ctr;
+  int* actr = w.ctr + p.ck_mt * p.ck_nt;
+  const long nc = (long)a.B * a.C * a.d;
+  k_split_f32<<<std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s>>>(
+      a.chat, nc, w.chi, w.clo, w.ctr, w.nctr);
+  {
+    TcMaps maps;
+    if (!make_tmap_bf16_2d(&maps.a[0], w.chi, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2,
+                           64, 128) ||
+        !make_tmap_bf16_2d(&maps.a[1], w.clo, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2,
+                           64, 128) ||
+        !make_tmap_bf16_2d(&maps.b[0], a.Wk, nkv, a.d, (uint64_t)nkv * 2, 64, 64))
+      return cudaErrorInvalidValue;
+    maps.b[1] = maps.b[0];
+    TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status};
+    CkeysEpi epi{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, kctr, w.khi, w.klo};
+    cudaError_t e = launch_tc_gemm<64, 2, 1, true>(maps, sh, epi,
+                                                   dim3(p.ck_nt, p.ck_mt, p.ck_nz), s);
+    if (e != cudaSuccess) return e;
+  }
+  TcMaps maps;
+  if (!make_tmap_bf16_3d(&maps.a[0], a.Q, a.dh, a.Hq, (uint64_t)a.B * a.N,
+                         (uint64_t)a.dh * 2, (uint64_t)a.Hq * a.dh * 2, 64, 128) ||
+      !make_tmap_bf16_2d(&maps.b[0], w.khi, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                         BN) ||
+      !make_tmap_bf16_2d(&maps.b[1], w.klo, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                         BN))
+    return cudaErrorInvalidValue;
+  maps.a[1] = maps.a[0];
+  TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status};
+  ProxyEpi<BN> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
+                   (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D,
+                   w.apart, actr};
+  return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb * p.nslice, 1),
+                                         s);
+}
+
 struct Plan {
   int nsplit, klen;   // centroid keys: split of d
   int nslice, hps;    // proxy: head slices
@@ -291,10 +585,22 @@ size_t proxy_ws(int B, int N, int d, int C, int Hq, int Hkv, int dh) {
   cv.take<float>(M * nout);
   if (p.nsplit > 1) cv.take<float>((size_t)p.nsplit * M * nout);
   if (p.nslice > 1) cv.take<float>((size_t)p.nslice * B * N * C);
-  return cv.bytes();
+  size_t simt = cv.bytes(), tcb = 0;
+  // the tensor-core plan applies to bf16 inputs; size for whichever is larger
+  const TcPlan q = tc_plan(PS_BF16, B, N, d, C, Hq, Hkv, dh);
+  if (q.ok) tc_carve(nullptr, q, B, N, d, C, Hkv * dh, &tcb);
+  return std::max(simt, tcb);
 }
 
 cudaError_t proxy_run(const ProxyArgs& a, cudaStream_t s) {
+  const TcPlan p = tc_plan(a.dtype, a.B, a.N, a.d, a.C, a.Hq, a.Hkv, a.dh);
+  if (p.ok) {
+    switch (p.BN) {
+      case 32: return proxy_tc<32>(a, p, s);
+      case 64: return proxy_tc<64>(a, p, s);
+      default: return proxy_tc<128>(a, p, s);
+    }
+  }
   return a.dtype == PS_F32 ? run_typed<float>(a, s)
                            : run_typed<__nv_bfloat16>(a, s);
 }

@@ -1,0 +1,259 @@
+// A warp-specialised tcgen05 GEMM mainloop shared by the dense contractions.
+//
+// CTA = 6 warps: warp 0 issues TMA loads into an S-stage shared-memory ring,
+// warp 1 issues tcgen05.mma (one thread) into a 128 x BN fp32 accumulator
+// in TMEM, warps 2-5 drain the accumulator (each reads the TMEM lane quarter
+// it may access) and hand rows to an op-specific epilogue.  The CTA owns
+// one BN-column tile (blockIdx.x) and walks row tiles t < epi.tiles(M)
+// (strided by gridDim.y, or a contiguous block of them); the epilogue object
+// maps a tile to its TMA coordinates.  blockIdx.z selects a chunk of the K
+// dimension.
+//
+// Operands, all bf16 with a 128-byte swizzle:
+//   A: NA K-major tiles [128 rows][64 k] (NA = 2: a hi/lo split of an fp32
+//      operand, accumulated as A_hi.B + A_lo.B)
+//   B: NB tiles, K-major [BN rows][64 k] or MN-major [64 k][BN cols]
+//      (NB = 2: hi/lo split, A.B_hi + A.B_lo)
+// Every mbarrier wait is bounded (tc::mbar_wait); on a timeout the CTA sets
+// the status word, drains its in-flight copies and MMAs, frees TMEM and
+// returns.
+#pragma once
+
+#include "tc.cuh"
+
+namespace ps {
+
+struct TcMaps {
+  CUtensorMap a[2];
+  CUtensorMap b[2];
+};
+
+struct TcShape {
+  int M;             // rows of A (an upper bound when M_dev is set)
+  const int* M_dev;  // device row count, or nullptr
+  int KB;            // K / 64
+  int kpc;           // 64-wide K blocks per blockIdx.z chunk
+  int* status;
+};
+
+template <int BN, int NA, int NB, bool B_MN>
+struct TcCfg {
+  static constexpr uint32_t kA = 128 * 64 * 2;
+  static constexpr uint32_t kB = BN * 64 * 2;
+  static constexpr uint32_t kStage = NA * kA + NB * kB;
+  static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
+  static constexpr size_t kSmem = 1024 + kStages * kStage + 1024;
+  static constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN, B_MN);
+};
+
+// Epi must provide (device, const unless noted):
+//   static constexpr bool kA3D     A maps are 3-D {k, head, row}
+//   static constexpr bool kBlocked CTA y takes the contiguous tile range
+//                                  [y*ceil(T/gy), ...) instead of striding
+//   int tiles(int M)               number of 128-row tiles
+//   int arow(int t), ahead(t)      A row (and head, 3-D maps) of tile t
+//   int bsel(int t, int n0)        which b map when NB == 1 (else ignored)
+//   int bcoord(int t, int n0)      B column (MN-major) or row (K-major)
+//   int bkoff(int t)               added to the K coordinate of B
+//   struct State                   per-thread epilogue state
+//   void consume(int t, int r, int n0, int z, uint32_t taddr, State&)
+//        row r (0..127) of tile t; taddr = TMEM address of the row's
+//        column 0 (read with tc::tmem_ld32, warp-collective); TMEM is
+//        released after it returns
+//   void tile_done(int t, int r, int n0, int z, uint8_t* scratch, State&)
+//        called by the 128 epilogue threads together after consume; may
+//        synchronise with bar.sync 1, 128; scratch = 512 B of shared memory
+template <int BN, int NA, int NB, bool B_MN, class Epi>
+__global__ void __launch_bounds__(192, 1)
+k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
+  using Cfg = TcCfg<BN, NA, NB, B_MN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* epi_scratch = smem + S * Cfg::kStage + 512;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_empty, 4);
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&maps.a[0]);
+    tc::tma_prefetch(&maps.b[0]);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, BN);
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
+  const int T = epi.tiles(M);
+  int t_begin = blockIdx.y, t_end = T, t_step = gridDim.y;
+  if constexpr (Epi::kBlocked) {
+    const int per = (T + gridDim.y - 1) / gridDim.y;
+    t_begin = blockIdx.y * per;
+    t_end = min(T, t_begin + per);
+    t_step = 1;
+  }
+  const int n0 = blockIdx.x * BN;
+  const int kb0 = blockIdx.z * sh.kpc;
+  const int kb1 = min(sh.KB, kb0 + sh.kpc);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = t_begin; ok && t < t_end; t += t_step) {
+        const int arow = epi.arow(t);
+        const int ahead = epi.ahead(t);
+        const int bkoff = epi.bkoff(t);
+        const int bsel = epi.bsel(t, n0);
+        const int bcol = epi.bcoord(t, n0);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!tc::mbar_wait(empty + s, ph ^ 1, sh.status, abort_flag)) { ok = false; break; }
+          uint8_t* st = smem + s * Cfg::kStage;
+          tc::mbar_expect_tx(full + s, Cfg::kStage);
+#pragma unroll
+          for (int a = 0; a < NA; ++a) {
+            if constexpr (Epi::kA3D)
+              tc::tma_load_3d(st + a * Cfg::kA, &maps.a[a], full + s, kb * 64, ahead, arow);
+            else
+              tc::tma_load_2d(st + a * Cfg::kA, &maps.a[a], full + s, kb * 64, arow);
+          }
+          uint8_t* bs = st + NA * Cfg::kA;
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb) {
+            const CUtensorMap* bm = &maps.b[NB == 1 ? bsel : bb];
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int q = 0; q < BN / 64; ++q)
+                tc::tma_load_2d(bs + bb * Cfg::kB + q * 8192, bm, full + s, bcol + 64 * q,
+                                kb * 64 + bkoff);
+            } else {
+              tc::tma_load_2d(bs + bb * Cfg::kB, bm, full + s, kb * 64 + bkoff, bcol);
+            }
+          }
+          ++it;
+        }
+      }
+      if (!ok) {  // let every copy already issued land before the CTA exits
+        for (int j = it > S ? it - S : 0; j < it; ++j) {
+          const uint64_t t0 = tc::globaltimer();
+          while (!tc::mbar_try_wait(full + j % S, (j / S) & 1) &&
+                 tc::globaltimer() - t0 < tc::kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int t = t_begin; ok && t < t_end; t += t_step, ++tcount) {
+        if (!tc::mbar_wait(acc_empty, (tcount & 1) ^ 1, sh.status, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!tc::mbar_wait(full + s, ph, sh.status, abort_flag)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t a_base = tc::smem_u32(smem + s * Cfg::kStage);
+          const uint32_t b_base = a_base + NA * Cfg::kA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            const uint64_t ad = tc::desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? tc::desc_sw128(b_base + kk * 2048, 8192, 1024)
+                                     : tc::desc_sw128(b_base + kk * 32, 16, 1024);
+            tc::mma_bf16(tmem, ad, bd, Cfg::kIdesc, acc);
+            if constexpr (NA == 2)
+              tc::mma_bf16(tmem, tc::desc_sw128(a_base + Cfg::kA + kk * 32, 16, 1024), bd,
+                           Cfg::kIdesc, 1u);
+            if constexpr (NB == 2) {
+              const uint64_t bd2 =
+                  B_MN ? tc::desc_sw128(b_base + Cfg::kB + kk * 2048, 8192, 1024)
+                       : tc::desc_sw128(b_base + Cfg::kB + kk * 32, 16, 1024);
+              tc::mma_bf16(tmem, ad, bd2, Cfg::kIdesc, 1u);
+            }
+          }
+          tc::mma_commit(empty + s);
+          ++it;
+        }
+        if (!ok) break;
+        tc::mma_commit(acc_full);
+      }
+      if (!ok) {  // wait for the MMAs already issued before TMEM is freed
+        tc::mma_commit(drain);
+        const uint64_t t0 = tc::globaltimer();
+        while (!tc::mbar_try_wait(drain, 0) && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int r = quarter * 32 + lane;
+    typename Epi::State est;
+    int tcount = 0;
+    for (int t = t_begin; t < t_end; t += t_step, ++tcount) {
+      if (!tc::mbar_wait(acc_full, tcount & 1, sh.status, abort_flag)) break;
+      tc::fence_after_sync();
+      epi.consume(t, r, n0, blockIdx.z, tmem + lane_base, est);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty);
+      epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, BN);
+  }
+}
+
+// Plain epilogue base: 2-D maps, strided tiles, no B offset, one b map.
+struct TcEpiBase {
+  static constexpr bool kA3D = false;
+  static constexpr bool kBlocked = false;
+  __device__ int ahead(int) const { return 0; }
+  __device__ int bkoff(int) const { return 0; }
+  __device__ int bsel(int, int) const { return 0; }
+};
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int BN, int NA, int NB, bool B_MN, class Epi>
+cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi, dim3 grid,
+                           cudaStream_t s) {
+  using Cfg = TcCfg<BN, NA, NB, B_MN>;
+  auto kern = k_tc_gemm<BN, NA, NB, B_MN, Epi>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, 192, Cfg::kSmem, s>>>(maps, sh, epi);
+  return cudaGetLastError();
+}
+
+}  // namespace ps

@@ -9,6 +9,7 @@
 
 #include "gemm_simt.cuh"
 #include "ops.h"
+#include "tc_gemm.cuh"
 
 namespace ps {
 namespace {
@@ -131,6 +132,107 @@ k_refresh(const T* __restrict__ H, const int32_t* __restrict__ pos,
   }
 }
 
+// ---- tensor-core path (bf16): gather the selected rows of every window into
+// one compact matrix X [sum_b npos_b][d] (row m remembers b*N + p), then
+// [K | V] = X . [W_k | W_v] on tcgen05 with the weights streamed through TMA
+// as MN-major tiles, and a scatter epilogue into the cache rows.
+
+// One warp per selected row; block (x, b) covers rows 8x .. 8x+7 of window b.
+__global__ void __launch_bounds__(256)
+k_gather_rows(const __nv_bfloat16* __restrict__ H, const int32_t* __restrict__ pos,
+              const int32_t* __restrict__ npos, int B, int N, int d,
+              __nv_bfloat16* __restrict__ X, int32_t* __restrict__ rowinfo,
+              int32_t* __restrict__ M_total) {
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int off = 0, total = 0;
+  for (int bb = 0; bb < B; ++bb) {
+    const int n = min(max(npos[bb], 0), N);
+    if (bb < b) off += n;
+    total += n;
+  }
+  if (b == 0 && blockIdx.x == 0 && threadIdx.x == 0) *M_total = total;
+  const int Mb = min(max(npos[b], 0), N);
+  const int j = blockIdx.x * 8 + warp;
+  if (j >= Mb) return;
+  const int p = pos[(long)b * N + j];
+  const bool valid = p >= 0 && p < N;
+  const uint4* src = reinterpret_cast<const uint4*>(H + ((long)b * N + (valid ? p : 0)) * d);
+  uint4* dst = reinterpret_cast<uint4*>(X + (long)(off + j) * d);
+  for (int c = lane; c < d / 8; c += 32)
+    dst[c] = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  if (lane == 0) rowinfo[off + j] = valid ? b * N + p : -1;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int BN>
+struct RefreshEpi : TcEpiBase {
+  const int32_t* rowinfo;
+  const int32_t* M_total;
+  int N, Ncache, off, nkv;
+  __nv_bfloat16* Kc;
+  __nv_bfloat16* Vc;
+  struct State {};
+  __device__ int tiles(int M) const { return (M + 127) / 128; }
+  __device__ int arow(int t) const { return t * 128; }
+  __device__ int bsel(int, int n0) const { return n0 >= nkv ? 1 : 0; }
+  __device__ int bcoord(int, int n0) const { return n0 >= nkv ? n0 - nkv : n0; }
+  __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
+  __device__ void consume(int t, int rr, int n0, int, uint32_t taddr, State&) const {
+    const int m = t * 128 + rr;
+    const int r = m < *M_total ? rowinfo[m] : -1;
+    const bool is_v = n0 >= nkv;
+    __nv_bfloat16* dst = nullptr;
+    if (r >= 0) {
+      const int b = r / N, p = r % N;
+      dst = (is_v ? Vc : Kc) + ((long)b * Ncache + off + p) * nkv + (is_v ? n0 - nkv : n0);
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);  // warp-collective: every lane loads
+      if (dst == nullptr) continue;
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        uint4 q;
+        q.x = pack_bf16x2(v[c + 0], v[c + 1]);
+        q.y = pack_bf16x2(v[c + 2], v[c + 3]);
+        q.z = pack_bf16x2(v[c + 4], v[c + 5]);
+        q.w = pack_bf16x2(v[c + 6], v[c + 7]);
+        *reinterpret_cast<uint4*>(dst + c0 + c) = q;
+      }
+    }
+  }
+};
+
+template <int BN>
+cudaError_t refresh_tc(const RefreshArgs& a, cudaStream_t s) {
+  const int nkv = a.Hkv * a.dh;
+  const long rows = (long)a.B * a.N;
+  Carver cv(a.ws);
+  __nv_bfloat16* X = cv.take<__nv_bfloat16>((size_t)rows * a.d);
+  int32_t* rowinfo = cv.take<int32_t>((size_t)rows);
+  int32_t* M_total = cv.take<int32_t>(4);
+  k_gather_rows<<<dim3(ceil_div(a.N, 8), a.B), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.H), a.pos, a.npos, a.B, a.N, a.d, X, rowinfo,
+      M_total);
+  TcMaps maps;
+  if (!make_tmap_bf16_2d(&maps.a[0], X, a.d, rows, (uint64_t)a.d * 2, 64, 128) ||
+      !make_tmap_bf16_2d(&maps.b[0], a.Wk, nkv, a.d, (uint64_t)nkv * 2, 64, 64) ||
+      !make_tmap_bf16_2d(&maps.b[1], a.Wv, nkv, a.d, (uint64_t)nkv * 2, 64, 64))
+    return cudaErrorInvalidValue;
+  maps.a[1] = maps.a[0];
+  TcShape sh{(int)rows, M_total, ceil_div(a.d, 64), ceil_div(a.d, 64), a.status};
+  const int ntiles = 2 * nkv / BN;
+  const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(2 * kSmTarget, ntiles)));
+  RefreshEpi<BN> epi{{}, rowinfo, M_total, a.N, a.Ncache, a.cache_off, nkv,
+                     static_cast<__nv_bfloat16*>(a.Kc), static_cast<__nv_bfloat16*>(a.Vc)};
+  return launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(ntiles, gy, 1), s);
+}
+
 template <typename T>
 cudaError_t refresh_typed(const RefreshArgs& a, cudaStream_t s) {
   const int nout = a.Hkv * a.dh;
@@ -150,7 +252,20 @@ cudaError_t topk_run(const TopkArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+bool refresh_tc_ok(int dtype, int Hkv, int dh) {
+  return dtype == PS_BF16 && (Hkv * dh) % 64 == 0;
+}
+
+size_t refresh_ws(int B, int N, int d) {
+  Carver cv(nullptr);
+  cv.take<__nv_bfloat16>((size_t)B * N * d);
+  cv.take<int32_t>((size_t)B * N);
+  cv.take<int32_t>(4);
+  return cv.bytes();
+}
+
 cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s) {
+  if (refresh_tc_ok(a.dtype, a.Hkv, a.dh) && a.ws != nullptr) return refresh_tc<64>(a, s);
   return a.dtype == PS_F32 ? refresh_typed<float>(a, s)
                            : refresh_typed<__nv_bfloat16>(a, s);
 }

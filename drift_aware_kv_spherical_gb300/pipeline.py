@@ -106,29 +106,10 @@ class Pipeline:
         self.t += 1
 
     def kernel_launches_per_step(self):
-        """Kernels libpolestar enqueues for one step (counted from its launch
-        sequence: k-means 3 per pass + 2, NVFP4 2, proxy 2-4, top-k 1,
-        refresh 1, commit 2)."""
+        """Approximate kernel count of one step (bf16 tensor-core plans:
+        k-means 2 + (I+1) + I + 1, NVFP4 2, proxy 3, top-k 1, refresh 2,
+        commit 2); the bench counts the captured graph's nodes instead when
+        it can."""
         w = self.w
-        km = 1 + 3 * (w.iters + 1) - 1 + 1
-        return self.layers * (km + 2 + self._proxy_launches() + 1 + 1) + 2
-
-    def _proxy_launches(self):
-        return _proxy_launch_count(self.w)
-
-
-def _proxy_launch_count(w):
-    # mirrors the split/slice plan of the proxy kernels (k_ckeys [+ reduce]
-    # + k_proxy [+ final])
-    from math import ceil
-    M, nout = w.B * w.C, w.Hkv * w.dh
-    tiles = ceil(M / 64) * ceil(nout / 64)
-    ns = max(1, ceil(2 * 152 / tiles))
-    ns = min(ns, max(1, w.d // 256))
-    klen = ceil(ceil(w.d / ns) / 16) * 16
-    nsplit = ceil(w.d / klen)
-    ptiles = ceil(w.N / 16) * w.B
-    sl = min(max(1, ceil(2 * 152 / ptiles)), w.Hq)
-    hps = ceil(w.Hq / sl)
-    nslice = ceil(w.Hq / hps)
-    return 2 + (nsplit > 1) + (nslice > 1)
+        km = 2 + (w.iters + 1) + w.iters + 1
+        return self.layers * (km + 2 + 3 + 1 + 2) + 2

@@ -129,6 +129,34 @@ def test_kmeans_ragged_and_degenerate():
     assert_close(g1["mu"][0], o1["mu"], what="C=1")
 
 
+@pytest.mark.parametrize("B,N,d,C,iters", [(3, 177, 80, 24, 3), (2, 300, 256, 128, 2),
+                                            (1, 129, 64, 64, 1)])
+def test_kmeans_bf16_ragged(B, N, d, C, iters):
+    """bf16 windows on the tensor-core path: row tiles straddling windows,
+    C not a power of two, a partial 64-wide K block, iters >= 1."""
+    rng = np.random.default_rng(N + C)
+    planted = oracle.normalize_rows(rng.standard_normal((C, d)))
+    z = rng.integers(0, C, (B, N))
+    H = (planted[z] * 4 + rng.normal(0, 0.3, (B, N, d))).astype(np.float32)
+    Ht = torch.from_numpy(H).cuda().to(torch.bfloat16)
+    Hn = np_(Ht)
+    mu0 = np.stack([oracle.normalize_rows(Hn[b][:C]) for b in range(B)]).astype(np.float32)
+    g = run_kmeans(Ht, torch.from_numpy(mu0).cuda(), iters)
+    checked = 0
+    for b in range(B):
+        o = oracle.kmeans_spherical(Hn[b], mu0[b].astype(np.float64), iters)
+        ok = o["margin"][-1] > KM_MARGIN
+        assert np.array_equal(g["assign"][b][ok], o["assign"][ok])
+        if o["margin"].min() > KM_MARGIN:
+            checked += 1
+            assert np.array_equal(g["counts"][b], o["counts"])
+            assert_close(g["mu"][b], o["mu"], what="mu")
+            assert_close(g["rho"][b], o["rho"], what="rho")
+            assert_close(g["chat"][b], o["chat"], what="chat")
+            assert_close(g["obj"][b], o["obj"], what="objective")
+    assert checked >= 1
+
+
 def test_kmeans_empty_cluster_keeps_centroid_and_chat():
     H = np.tile(np.array([[1.0, 0.1] + [0.0] * 14], np.float32), (5, 1))[None]
     far = np.zeros(16, np.float32); far[0] = -1.0
@@ -343,7 +371,7 @@ def _kv_check(g, o, bf16):
     assert np.all(np.abs(g - o) <= tol)
 
 
-@pytest.mark.parametrize("widx", SMALL)
+@pytest.mark.parametrize("widx", [0, 1, 2])
 @pytest.mark.parametrize("off", [0, 5])
 def test_refresh_kv(widx, off):
     w, L = _layer(widx)
@@ -360,7 +388,9 @@ def test_refresh_kv(widx, off):
     Kc0 = torch.randn(B, Ncache, w.Hkv, w.dh, device="cuda").to(dt)
     Vc0 = torch.randn(B, Ncache, w.Hkv, w.dh, device="cuda").to(dt)
     Kc, Vc = Kc0.clone(), Vc0.clone()
-    ps.ps_refresh_kv(H, pos_t, npos_t, L["Wk"], L["Wv"], Kc, Vc, w.Hkv, w.dh, cache_off=off)
+    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=w.d)
+    ps.ps_refresh_kv(H, pos_t, npos_t, L["Wk"], L["Wv"], Kc, Vc, w.Hkv, w.dh, cache_off=off,
+                     ws=ws)
     torch.cuda.synchronize()
     ps.ps_check()
     pos, npos = np_(pos_t), np_(npos_t)
@@ -390,6 +420,40 @@ def test_refresh_empty_selection_leaves_cache():
     ps.ps_refresh_kv(H, pos, npos, W, W, Kc, Vc, 2, 16)
     torch.cuda.synchronize()
     assert torch.equal(Kc, K0) and torch.equal(Vc, K0)
+    # the tensor-core path (K/V width a multiple of 64) with nothing selected
+    W = torch.randn(64, 128, device="cuda").to(torch.bfloat16)
+    Kc = torch.randn(2, 40, 2, 64, device="cuda").to(torch.bfloat16)
+    Vc, K0 = Kc.clone(), Kc.clone()
+    pos = torch.full((2, 40), -1, dtype=torch.int32, device="cuda")
+    npos = torch.zeros(2, dtype=torch.int32, device="cuda")
+    H2 = torch.randn(2, 40, 64, device="cuda").to(torch.bfloat16)
+    ws = ps.workspace(ps.OP_REFRESH, B=2, N=40, d=64)
+    ps.ps_refresh_kv(H2, pos, npos, W, W, Kc, Vc, 2, 64, ws=ws)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    assert torch.equal(Kc, K0) and torch.equal(Vc, K0)
+
+
+def test_refresh_all_rows_ragged_d():
+    """Every row selected, d = 80 (a partial 64-wide K block), 3 windows of
+    150 rows (ragged 128-row tiles): the textbook GEMM, bf16-rounded."""
+    rng = np.random.default_rng(9)
+    B, N, d, Hkv, dh = 3, 150, 80, 2, 64
+    H = torch.from_numpy(rng.standard_normal((B, N, d)).astype(np.float32)).cuda().to(torch.bfloat16)
+    Wk = torch.from_numpy(rng.standard_normal((d, Hkv * dh)).astype(np.float32) * 0.1).cuda().to(torch.bfloat16)
+    Wv = torch.from_numpy(rng.standard_normal((d, Hkv * dh)).astype(np.float32) * 0.1).cuda().to(torch.bfloat16)
+    pos = torch.arange(N, dtype=torch.int32, device="cuda").repeat(B, 1).contiguous()
+    npos = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    Kc = torch.zeros(B, N, Hkv, dh, device="cuda", dtype=torch.bfloat16)
+    Vc = torch.zeros_like(Kc)
+    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=d)
+    ps.ps_refresh_kv(H, pos, npos, Wk, Wv, Kc, Vc, Hkv, dh, ws=ws)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    Hn, Wkn, Wvn = np_(H), np_(Wk), np_(Wv)
+    for b in range(B):
+        _kv_check(np_(Kc[b]).reshape(N, -1), oracle.bf16_round(Hn[b] @ Wkn.astype(np.float64)), True)
+        _kv_check(np_(Vc[b]).reshape(N, -1), oracle.bf16_round(Hn[b] @ Wvn.astype(np.float64)), True)
 
 
 # ---------------------------------------------------------------- commit
