@@ -24,7 +24,8 @@
  *          failure (a bounded wait that gave up) sets the handle's status word;
  *          ps_check() reports it as PS_ERR_TIMEOUT.
  * Sizes    B >= 0 (B == 0 is a no-op), d % 16 == 0, dh % 16 == 0,
- *          Hq % Hkv == 0, 1 <= k <= C <= min(N, 1024), V % 4 == 0.
+ *          Hq % Hkv == 0, 1 <= k <= C <= min(N, 256), d <= 8192,
+ *          dh <= 256, V % 4 == 0, P <= 1024, B * P <= 65535.
  * Threads  One handle per concurrently used stream; no C++ exception
  *          crosses this interface.
  * State    Step-to-step state (centroids, previous distributions, drift
@@ -64,10 +65,11 @@ typedef struct ps_handle_s* ps_handle;
 ps_status ps_create(int device, ps_handle* out);
 ps_status ps_destroy(ps_handle h);
 
-/* Status of device-side work enqueued so far on `stream`.  synchronize != 0
- * waits for the stream first; otherwise the word is read asynchronously
- * after a stream sync anyway (the read is ordered on `stream`).  Clears the
- * word.  Returns PS_OK, PS_ERR_TIMEOUT or PS_ERR_CUDA. */
+/* Status of device-side work enqueued so far on `stream`: reads the
+ * handle's status word after the work on `stream` has finished (the read is
+ * ordered on `stream` and waited for; synchronize != 0 additionally
+ * synchronises the stream first and reports a failed synchronisation).
+ * Clears the word.  Returns PS_OK, PS_ERR_TIMEOUT or PS_ERR_CUDA. */
 ps_status ps_check(ps_handle h, void* stream, int synchronize);
 
 const char* ps_status_string(ps_status s);
@@ -185,7 +187,10 @@ ps_status ps_topk_drift(ps_handle h, const float* D, const int32_t* assign,
  *   accumulated in fp32, rounded to the cache dtype (bf16 RNE or f32).
  * Rows not listed are untouched.  npos is read on the device.
  * H [B][N][d], Wk/Wv [d][Hkv*dh], Kcache/Vcache [B][Ncache][Hkv][dh], all
- * of `dtype`.  Requires cache_off + N <= Ncache.
+ * of `dtype`.  Requires cache_off + N <= Ncache.  bf16 with Hkv*dh a
+ * multiple of 64 runs on the tensor cores and needs the workspace
+ * (ps_workspace_bytes(PS_OP_REFRESH, ...): the gathered rows, B*N*d bf16
+ * at most); the caches must then be 16-byte aligned.
  * ------------------------------------------------------------------------- */
 ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
                         const int32_t* pos, const int32_t* npos,
