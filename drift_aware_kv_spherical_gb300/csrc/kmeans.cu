@@ -11,7 +11,8 @@
 //   k_split_mu      mu -> (mu_hi, mu_lo) bf16 for the tensor cores
 //   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
 //                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
-//                   d; the last CTA of a tile sums the partials in split
+//                   d when the windows give too few row tiles; then
+//                   k_km_argmax (a warp per row) sums the partials in split
 //                   order and takes the arg-max.  fp32 windows: k_assign on
 //                   CUDA cores.
 //   k_cluster_scan  per (cluster, window): members in ascending row order,
@@ -249,11 +250,9 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
   }
 }
 
-// fp32 centroids -> bf16 hi + lo parts (hi = bf16(mu), lo = bf16(mu - hi));
-// also clears the tile counters of the split reduction.
+// fp32 centroids -> bf16 hi + lo parts (hi = bf16(mu), lo = bf16(mu - hi)).
 __global__ void k_split_mu(const float* __restrict__ mu, long n, __nv_bfloat16* __restrict__ hi,
-                           __nv_bfloat16* __restrict__ lo, int* __restrict__ counters,
-                           int ncounters) {
+                           __nv_bfloat16* __restrict__ lo) {
   const long stride = (long)gridDim.x * blockDim.x;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float x = mu[i];
@@ -261,19 +260,16 @@ __global__ void k_split_mu(const float* __restrict__ mu, long n, __nv_bfloat16* 
     hi[i] = h;
     lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
   }
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < ncounters; i += stride)
-    counters[i] = 0;
 }
 
 // Epilogue of the tensor-core assignment.  Tile t = (window b, 128-row block
-// mt).  With one d-chunk the arg-max is taken straight from the accumulator;
-// otherwise every chunk stores its partial scores [z][c][row] and the last
-// CTA to finish a tile (tile counter) sums them in chunk order.
+// mt).  With one d-chunk the arg-max is taken straight from the accumulator
+// and the tile's objective partial is folded here; with several, every chunk
+// stores its partial scores [z][row][c] and k_km_argmax finishes the rows.
 template <int BN>
 struct KmAssignEpi : TcEpiBase {
   int B, N, C, mtb, nz;
   float* part;
-  int* counters;
   const float* inv;
   int32_t* assign;
   float* best;
@@ -287,9 +283,9 @@ struct KmAssignEpi : TcEpiBase {
   __device__ int bcoord(int t, int n0) const { return (t / mtb) * C + n0; }
   __device__ void consume(int t, int r, int, int z, uint32_t taddr, State& st) const {
     const int b = t / mtb, i = (t % mtb) * 128 + r;
-    const long ld = (long)B * N;
     st.bv = -INFINITY;
     st.bi = INT_MAX;
+    float* dst = part + ((long)z * B * N + (long)b * N + i) * C;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       float v[32];
@@ -299,38 +295,23 @@ struct KmAssignEpi : TcEpiBase {
         for (int j = 0; j < 32; ++j)
           if (c0 + j < C && v[j] > st.bv) { st.bv = v[j]; st.bi = c0 + j; }
       } else if (i < N) {
+        if (c0 + 32 <= C && (C & 3) == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < C) part[((long)z * C + c0 + j) * ld + (long)b * N + i] = v[j];
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(dst + c0 + 4 * j) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < C) dst[c0 + j] = v[j];
+        }
       }
     }
   }
   __device__ void tile_done(int t, int r, int, int, uint8_t* scratch, State& st) const {
+    if (nz > 1) return;
     const int b = t / mtb, i = (t % mtb) * 128 + r;
-    int* flag = reinterpret_cast<int*>(scratch);
     float* wsum = reinterpret_cast<float*>(scratch + 16);
-    if (nz > 1) {
-      __threadfence();
-      epi_bar_sync();
-      if (r == 0) flag[0] = (atomicAdd(&counters[t], 1) == nz - 1) ? 1 : 0;
-      epi_bar_sync();
-      const bool last = flag[0] != 0;
-      epi_bar_sync();
-      if (!last) return;
-      __threadfence();
-      st.bv = -INFINITY;
-      st.bi = INT_MAX;
-      if (i < N) {
-        const long ld = (long)B * N;
-        for (int c = 0; c < C; ++c) {
-          float sum = 0.f;
-          for (int zz = 0; zz < nz; ++zz)
-            sum += __ldcg(&part[((long)zz * C + c) * ld + (long)b * N + i]);
-          if (sum > st.bv) { st.bv = sum; st.bi = c; }
-        }
-      }
-      if (r == 0) counters[t] = 0;
-    }
     float cs = 0.f;
     if (i < N) {
       if (st.bi == INT_MAX) { st.bi = 0; st.bv = 0.f; }
@@ -345,6 +326,50 @@ struct KmAssignEpi : TcEpiBase {
     epi_bar_sync();
   }
 };
+
+// Rows of a split assignment: one warp per row sums the nz partial scores of
+// each centroid in chunk order, takes the first arg-max and the cosine;
+// block (x, b) covers rows 8x..8x+7 of window b and stores their objective
+// partial objp[b][x].
+__global__ void __launch_bounds__(256)
+k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
+            const float* __restrict__ inv, int32_t* __restrict__ assign,
+            float* __restrict__ best, float* __restrict__ objp) {
+  __shared__ float s_cos[8];
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  float cs = 0.f;
+  if (i < N) {
+    const long row = (long)b * N + i;
+    const long zs = (long)B * N * C;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int c = lane; c < C; c += 32) {
+      float sum = 0.f;
+      for (int z = 0; z < nz; ++z) sum += __ldcg(part + z * zs + row * C + c);
+      if (sum > bv) { bv = sum; bi = c; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (bi == INT_MAX) { bi = 0; bv = 0.f; }
+    if (lane == 0) {
+      assign[row] = bi;
+      best[row] = bv;
+    }
+    cs = bv * inv[row];
+  }
+  if (lane == 0) s_cos[warp] = cs;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float so = 0.f;
+    for (int w = 0; w < 8; ++w) so += s_cos[w];
+    objp[(long)b * gridDim.x + blockIdx.x] = so;
+  }
+}
 
 // Per (cluster c, window b): members in ascending row order, 256 rows at a
 // time.  Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the
@@ -467,7 +492,7 @@ KmPlan km_plan(int dtype, int B, int N, int d, int C) {
     nz = std::min(nz, p.KB);
     p.kpc = ceil_div(p.KB, nz);
     p.nz = ceil_div(p.KB, p.kpc);
-    p.ntile = p.mtb;
+    p.ntile = p.nz > 1 ? ceil_div(N, 8) : p.mtb;
   } else {
     p.ntile = ceil_div(N, kTileRows);
   }
@@ -482,7 +507,6 @@ struct KmWs {
   __nv_bfloat16* mu_hi;
   __nv_bfloat16* mu_lo;
   float* part;
-  int* counters;
 };
 
 KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* bytes) {
@@ -497,7 +521,6 @@ KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* b
     w.mu_hi = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.mu_lo = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.part = p.nz > 1 ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
-    w.counters = cv.take<int>((size_t)B * p.mtb);
   }
   if (bytes != nullptr) *bytes = cv.bytes();
   return w;
@@ -515,9 +538,14 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaS
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status};
-  KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.counters, w.inv,
-                      a.assign, a.rho, w.objp};
-  return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
+  KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.inv, a.assign, a.rho,
+                      w.objp};
+  cudaError_t e =
+      launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
+  if (e != cudaSuccess || p.nz == 1) return e;
+  k_km_argmax<<<dim3(ceil_div(a.N, 8), a.B), 256, 0, s>>>(w.part, p.nz, a.B, a.N, a.C,
+                                                          w.inv, a.assign, a.rho, w.objp);
+  return cudaGetLastError();
 }
 
 template <typename T>
@@ -533,8 +561,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
                                                     w.w, w.chosen);
   if (p.tc) {
     const long n = (long)a.B * a.C * a.d;
-    k_split_mu<<<std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s>>>(
-        a.mu, n, w.mu_hi, w.mu_lo, w.counters, a.B * p.mtb);
+    k_split_mu<<<std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s>>>(a.mu, n, w.mu_hi,
+                                                                         w.mu_lo);
   }
   for (int t = 0; t <= a.iters; ++t) {
     cudaError_t e = cudaSuccess;

@@ -17,8 +17,8 @@
 //                   reduction; written as K~_hi, K~_lo (bf16)
 //   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
 //                   in TMEM, softmax over the C columns in the epilogue,
-//                   head sum in registers; the last head slice of a tile
-//                   sums the slice partials, divides by Hq and takes the KL
+//                   head sum in registers; with several head slices per
+//                   tile, k_proxy_final sums them, divides by Hq, takes KL
 // Every reduction has a fixed order, so identical inputs give identical
 // bits and KL(A || A) is exactly 0.
 #include <algorithm>
@@ -214,6 +214,10 @@ k_proxy_final(const float* __restrict__ part, int nslice, int B, int N, int C,
   proxy_finish<NJ>(Aacc, Hq, b, i, N, C, A_prev, A_cur, D);
 }
 
+int nj_for(int C);
+
+cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cudaStream_t s);
+
 // ------------------------------------------------------------ tensor cores
 __global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* __restrict__ hi,
                             __nv_bfloat16* __restrict__ lo, int* __restrict__ zero,
@@ -295,7 +299,7 @@ struct CkeysEpi : TcEpiBase {
 // hps heads per CTA.  Per head: softmax of the row's C scores (scaled by
 // 1/sqrt(dh)) added to the row's head sum A (registers).  After the slice's
 // last head: one slice -> A / Hq, KL, store; several -> store the partial,
-// and the last slice CTA of the tile sums the partials in slice order.
+// which k_proxy_final sums in slice order before the KL.
 template <int BN>
 struct ProxyEpi : TcEpiBase {
   static constexpr bool kA3D = true;
@@ -305,8 +309,7 @@ struct ProxyEpi : TcEpiBase {
   const float* A_prev;
   float* A_cur;
   float* D;
-  float* part;      // [nslice][B*N][C]
-  int* counters;    // [B*mtb]
+  float* part;      // [nslice][B*N][C], summed by k_proxy_final
   struct State {
     float A[BN];
   };
@@ -366,7 +369,7 @@ struct ProxyEpi : TcEpiBase {
     }
     D[row] = A_prev != nullptr ? fmaxf(kl, 0.f) : 0.f;
   }
-  __device__ void tile_done(int t, int r, int, int, uint8_t* scratch, State& st) const {
+  __device__ void tile_done(int t, int r, int, int, uint8_t*, State& st) const {
     const int h = t % Hq;
     if ((h + 1) % hps != 0 && h + 1 != Hq) return;
     const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
@@ -383,27 +386,6 @@ struct ProxyEpi : TcEpiBase {
       for (int c = 0; c < BN; ++c)
         if (c < C) dst[c] = st.A[c];
     }
-    int* flag = reinterpret_cast<int*>(scratch);
-    __threadfence();
-    epi_bar_sync();
-    if (r == 0) flag[0] = (atomicAdd(&counters[bm], 1) == nslice - 1) ? 1 : 0;
-    epi_bar_sync();
-    const bool last = flag[0] != 0;
-    epi_bar_sync();
-    if (!last) return;
-    __threadfence();
-    if (live) {
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float sum = 0.f;
-        if (c < C)
-          for (int sl = 0; sl < nslice; ++sl)
-            sum += __ldcg(part + ((long)sl * ld + (long)b * N + i) * C + c);
-        st.A[c] = sum;
-      }
-      finish(b, i, st.A);
-    }
-    if (r == 0) counters[bm] = 0;
   }
 };
 
@@ -451,7 +433,7 @@ TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, 
   w.klo = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
   w.kpart = p.ck_nz > 1 ? cv.take<float>((size_t)p.ck_nz * B * C * nkv) : nullptr;
   w.apart = p.nslice > 1 ? cv.take<float>((size_t)p.nslice * B * N * C) : nullptr;
-  w.nctr = p.ck_mt * p.ck_nt + B * p.mtb;
+  w.nctr = p.ck_mt * p.ck_nt;
   w.ctr = cv.take<int>((size_t)w.nctr);
   if (bytes) *bytes = cv.bytes();
   return w;
@@ -462,7 +444,6 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   const int nkv = a.Hkv * a.dh;
   const TcWs w = tc_carve(a.ws, p, a.B, a.N, a.d, a.C, nkv, nullptr);
   int* kctr = w.ctr;
-  int* actr = w.ctr + p.ck_mt * p.ck_nt;
   const long nc = (long)a.B * a.C * a.d;
   k_split_f32<<<std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s>>>(
       a.chat, nc, w.chi, w.clo, w.ctr, w.nctr);
@@ -493,9 +474,11 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status};
   ProxyEpi<BN> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
                    (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D,
-                   w.apart, actr};
-  return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb * p.nslice, 1),
-                                         s);
+                   w.apart};
+  cudaError_t e = launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi,
+                                                  dim3(1, a.B * p.mtb * p.nslice, 1), s);
+  if (e != cudaSuccess || p.nslice == 1) return e;
+  return launch_final(a, p.nslice, w.apart, s);
 }
 
 struct Plan {
@@ -527,6 +510,18 @@ int nj_for(int C) {
 
 size_t proxy_smem(int dh, int NJ) {
   return sizeof(float) * ((size_t)kRows * (dh + 1) + (size_t)kKc * (16 * NJ + 1));
+}
+
+cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cudaStream_t s) {
+  const dim3 grid(ceil_div(a.N, kRows), a.B);
+  switch (nj_for(a.C)) {
+    case 1: k_proxy_final<1><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 2: k_proxy_final<2><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 4: k_proxy_final<4><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 8: k_proxy_final<8><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    default: k_proxy_final<16><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+  }
+  return cudaGetLastError();
 }
 
 template <typename T, int NJ>
