@@ -393,11 +393,14 @@ def main():
     ms_step = total_ms / args.steps
     steps_per_s = world * args.steps / (total_ms / 1000.0)
 
-    # per-op breakdown: the same steps eagerly, events between the calls
+    # per-op breakdown: the same steps eagerly, events between the calls; a
+    # device-side spin before each step lets the host enqueue the whole step
+    # first, so the events time the kernels and not the host's launch pace
     events = [mk() for _ in range(args.steps)]
     for t in range(args.steps):
         load(step_no)
         flush.zero_()
+        torch.cuda._sleep(4_000_000)
         op_calls(step_no % 2, events[t])
         step_no += 1
     torch.cuda.synchronize()

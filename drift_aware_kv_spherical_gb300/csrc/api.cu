@@ -113,7 +113,8 @@ size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
       return (N > 0 && C > 0 && Hkv > 0 && dh > 0 && Hq > 0)
                  ? proxy_ws(B, N, d, C, Hq, Hkv, dh) : 0;
     case PS_OP_TOPK: return 0;
-    case PS_OP_REFRESH: return (N > 0 && d > 0) ? refresh_ws(B, N, d) : 0;
+    case PS_OP_REFRESH:
+      return (N > 0 && d > 0 && Hkv > 0 && dh > 0) ? refresh_ws(B, N, d, Hkv, dh) : 0;
     case PS_OP_COMMIT: return (P > 0 && V > 0) ? commit_ws(B, P, V) : 0;
   }
   return 0;
@@ -218,7 +219,7 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
   const bool tc = refresh_tc_ok(dtype, Hkv, dh);
   if (tc) {
     PS_PTR(Kcache); PS_PTR(Vcache);
-    ps_status st = check_ws(refresh_ws(B, N, d), ws, ws_bytes);
+    ps_status st = check_ws(refresh_ws(B, N, d, Hkv, dh), ws, ws_bytes);
     if (st != PS_OK) return st;
   }
   RefreshArgs a{H, dtype, pos, npos, Wk, Wv, B, N, d, Hkv, dh, Kcache, Vcache,

@@ -387,6 +387,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   constexpr int V = Vec<T>::n;
   constexpr int G = kMaxD / (256 * V);
   __shared__ int list[256];
+  __shared__ float list_inv[256];
   __shared__ int s_scan[32];
   __shared__ float s_red[8];
   const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
@@ -402,15 +403,37 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     const int f = (i < N && assign[(long)b * N + i] == c) ? 1 : 0;
     int tot;
     const int ex = block_exclusive_scan<int>(f, s_scan, &tot);
-    if (f) list[ex] = i;
+    if (f) {
+      list[ex] = i;
+      if constexpr (!FINAL) list_inv[ex] = inv[(long)b * N + i];
+    }
     __syncthreads();
     if constexpr (FINAL) {
       if (tid < tot) rs += rho[(long)b * N + list[tid]];
     } else {
-      for (int m = 0; m < tot; ++m) {
-        const int row = list[m];
-        const float sc = inv[(long)b * N + row];
-        const T* h = H + ((long)b * N + row) * d;
+      // members in ascending order; four rows' loads in flight at a time
+      int m = 0;
+      for (; m + 4 <= tot; m += 4) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int col = (g * 256 + tid) * V;
+          if (col < d) {
+            float v[4][V];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              load16(H + ((long)b * N + list[m + q]) * d + col, v[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float sc = list_inv[m + q];
+#pragma unroll
+              for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[q][e], sc, u[g][e]);
+            }
+          }
+        }
+      }
+      for (; m < tot; ++m) {
+        const float sc = list_inv[m];
+        const T* h = H + ((long)b * N + list[m]) * d;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const int col = (g * 256 + tid) * V;
@@ -537,7 +560,7 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaS
                          BN))
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
-  TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status};
+  TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status, INT_MAX};
   KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.inv, a.assign, a.rho,
                       w.objp};
   cudaError_t e =

@@ -49,7 +49,7 @@ struct RefreshArgs {
   void* ws; int* status;
 };
 bool refresh_tc_ok(int dtype, int Hkv, int dh);
-size_t refresh_ws(int B, int N, int d);
+size_t refresh_ws(int B, int N, int d, int Hkv, int dh);
 cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s);
 
 struct CommitArgs {

@@ -13,8 +13,8 @@
 // bf16 inputs take the tensor-core path instead (C <= 128, dh % 64 == 0):
 //   k_split_f32     C_hat -> bf16 hi + lo
 //   tcgen05 GEMM    K~ = C_hat_hi W_k + C_hat_lo W_k, W_k streamed through
-//                   TMA as MN-major tiles, split over d with a last-CTA
-//                   reduction; written as K~_hi, K~_lo (bf16)
+//                   TMA as MN-major tiles, split over d for small B*C
+//                   (k_ckeys_finish sums the chunks); kept as K~_hi, K~_lo
 //   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
 //                   in TMEM, softmax over the C columns in the epilogue,
 //                   head sum in registers; with several head slices per
@@ -220,8 +220,7 @@ cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cuda
 
 // ------------------------------------------------------------ tensor cores
 __global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* __restrict__ hi,
-                            __nv_bfloat16* __restrict__ lo, int* __restrict__ zero,
-                            int nzero) {
+                            __nv_bfloat16* __restrict__ lo) {
   const long stride = (long)gridDim.x * blockDim.x;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float v = x[i];
@@ -229,7 +228,6 @@ __global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* 
     hi[i] = h;
     lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += stride) zero[i] = 0;
 }
 
 __device__ __forceinline__ void split_store(__nv_bfloat16* hi, __nv_bfloat16* lo, float v) {
@@ -238,23 +236,24 @@ __device__ __forceinline__ void split_store(__nv_bfloat16* hi, __nv_bfloat16* lo
   *lo = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// K~ tile epilogue: rows of B*C centroids, 64 key columns.  One d-chunk:
-// split and store.  Several: store fp32 partials [z][M][nkv]; the last CTA
-// of the (row tile, column tile) sums them in chunk order.
+// K~ tile epilogue: rows of B*C centroids, BN key columns.  One d-chunk:
+// split and store.  Several: store fp32 partials [z][M][nkv], which
+// k_ckeys_finish sums in chunk order.
+template <int BN>
 struct CkeysEpi : TcEpiBase {
   int M, nkv, nz;
   float* part;
-  int* counters;   // [row tiles][column tiles]
   __nv_bfloat16* khi;
   __nv_bfloat16* klo;
   struct State {};
   __device__ int tiles(int) const { return (M + 127) / 128; }
   __device__ int arow(int t) const { return t * 128; }
   __device__ int bcoord(int, int n0) const { return n0; }
+  __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
   __device__ void consume(int t, int r, int n0, int z, uint32_t taddr, State&) const {
     const int m = t * 128 + r;
 #pragma unroll 1
-    for (int c0 = 0; c0 < 64; c0 += 32) {
+    for (int c0 = 0; c0 < BN; c0 += 32) {
       float v[32];
       tc::tmem_ld32(taddr + c0, v);
       if (m >= M) continue;
@@ -270,30 +269,19 @@ struct CkeysEpi : TcEpiBase {
       }
     }
   }
-  __device__ void tile_done(int t, int r, int n0, int, uint8_t* scratch, State&) const {
-    if (nz == 1) return;
-    int* flag = reinterpret_cast<int*>(scratch);
-    int* ctr = counters + (long)t * (nkv / 64) + n0 / 64;
-    __threadfence();
-    epi_bar_sync();
-    if (r == 0) flag[0] = (atomicAdd(ctr, 1) == nz - 1) ? 1 : 0;
-    epi_bar_sync();
-    const bool last = flag[0] != 0;
-    epi_bar_sync();
-    if (!last) return;
-    __threadfence();
-    const int m = t * 128 + r;
-    if (m < M) {
-      for (int c = 0; c < 64; ++c) {
-        const long o = (long)m * nkv + n0 + c;
-        float sum = 0.f;
-        for (int zz = 0; zz < nz; ++zz) sum += __ldcg(part + (long)zz * M * nkv + o);
-        split_store(khi + o, klo + o, sum);
-      }
-    }
-    if (r == 0) *ctr = 0;
-  }
 };
+
+// K~ = sum of the d-chunk partials (chunk order), stored as bf16 hi + lo.
+__global__ void __launch_bounds__(256)
+k_ckeys_finish(const float* __restrict__ part, int nz, long count,
+               __nv_bfloat16* __restrict__ khi, __nv_bfloat16* __restrict__ klo) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (long)gridDim.x * blockDim.x) {
+    float sum = 0.f;
+    for (int z = 0; z < nz; ++z) sum += __ldcg(part + (long)z * count + i);
+    split_store(khi + i, klo + i, sum);
+  }
+}
 
 // Proxy epilogue.  Tiles t = ((b * mtb + mt) * Hq + h), taken in blocks of
 // hps heads per CTA.  Per head: softmax of the row's C scores (scaled by
@@ -392,7 +380,7 @@ struct ProxyEpi : TcEpiBase {
 struct TcPlan {
   bool ok;
   int BN, mtb, nslice, hps;             // proxy
-  int ck_mt, ck_nt, ck_nz, ck_kpc, KB;  // centroid keys
+  int ck_BN, ck_mt, ck_nt, ck_nz, ck_kpc, KB;  // centroid keys
 };
 
 TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
@@ -408,8 +396,9 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
     if (Hq % sl == 0) { p.nslice = sl; break; }
   p.hps = Hq / p.nslice;
   p.KB = ceil_div(d, 64);
+  p.ck_BN = nkv % 256 == 0 ? 256 : (nkv % 128 == 0 ? 128 : 64);
   p.ck_mt = ceil_div(B * C, 128);
-  p.ck_nt = nkv / 64;
+  p.ck_nt = nkv / p.ck_BN;
   int nz = std::max(1, std::min(8, ceil_div(kSmTarget, p.ck_mt * p.ck_nt)));
   nz = std::min(nz, p.KB);
   p.ck_kpc = ceil_div(p.KB, nz);
@@ -420,8 +409,6 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
 struct TcWs {
   __nv_bfloat16 *chi, *clo, *khi, *klo;
   float *kpart, *apart;
-  int* ctr;      // key counters then proxy counters
-  int nctr;
 };
 
 TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, size_t* bytes) {
@@ -433,8 +420,6 @@ TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, 
   w.klo = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
   w.kpart = p.ck_nz > 1 ? cv.take<float>((size_t)p.ck_nz * B * C * nkv) : nullptr;
   w.apart = p.nslice > 1 ? cv.take<float>((size_t)p.nslice * B * N * C) : nullptr;
-  w.nctr = p.ck_mt * p.ck_nt;
-  w.ctr = cv.take<int>((size_t)w.nctr);
   if (bytes) *bytes = cv.bytes();
   return w;
 }
@@ -443,10 +428,9 @@ template <int BN>
 cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   const int nkv = a.Hkv * a.dh;
   const TcWs w = tc_carve(a.ws, p, a.B, a.N, a.d, a.C, nkv, nullptr);
-  int* kctr = w.ctr;
   const long nc = (long)a.B * a.C * a.d;
-  k_split_f32<<<std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s>>>(
-      a.chat, nc, w.chi, w.clo, w.ctr, w.nctr);
+  k_split_f32<<<std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s>>>(a.chat, nc, w.chi,
+                                                                          w.clo);
   {
     TcMaps maps;
     if (!make_tmap_bf16_2d(&maps.a[0], w.chi, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2,
@@ -456,11 +440,20 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
         !make_tmap_bf16_2d(&maps.b[0], a.Wk, nkv, a.d, (uint64_t)nkv * 2, 64, 64))
       return cudaErrorInvalidValue;
     maps.b[1] = maps.b[0];
-    TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status};
-    CkeysEpi epi{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, kctr, w.khi, w.klo};
-    cudaError_t e = launch_tc_gemm<64, 2, 1, true>(maps, sh, epi,
-                                                   dim3(p.ck_nt, p.ck_mt, p.ck_nz), s);
+    TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status, INT_MAX};
+    const dim3 grid(p.ck_nt, p.ck_mt, p.ck_nz);
+    cudaError_t e;
+    switch (p.ck_BN) {
+      case 256: e = launch_tc_gemm<256, 2, 1, true>(maps, sh, CkeysEpi<256>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
+      case 128: e = launch_tc_gemm<128, 2, 1, true>(maps, sh, CkeysEpi<128>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
+      default: e = launch_tc_gemm<64, 2, 1, true>(maps, sh, CkeysEpi<64>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
+    }
     if (e != cudaSuccess) return e;
+    if (p.ck_nz > 1) {
+      const long count = (long)a.B * a.C * nkv;
+      k_ckeys_finish<<<std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s>>>(
+          w.kpart, p.ck_nz, count, w.khi, w.klo);
+    }
   }
   TcMaps maps;
   if (!make_tmap_bf16_3d(&maps.a[0], a.Q, a.dh, a.Hq, (uint64_t)a.B * a.N,
@@ -471,7 +464,7 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
                          BN))
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
-  TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status};
+  TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status, INT_MAX};
   ProxyEpi<BN> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
                    (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D,
                    w.apart};

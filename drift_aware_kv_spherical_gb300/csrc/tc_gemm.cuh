@@ -34,6 +34,8 @@ struct TcShape {
   int KB;            // K / 64
   int kpc;           // 64-wide K blocks per blockIdx.z chunk
   int* status;
+  int split_max_rows;  // K is split over blockIdx.z only while M <= this;
+                       // above it blockIdx.z == 0 takes the whole K range
 };
 
 template <int BN, int NA, int NB, bool B_MN>
@@ -102,7 +104,8 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   const uint32_t tmem = *tmem_slot;
 
   const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
-  const int T = epi.tiles(M);
+  const bool ksplit = M <= sh.split_max_rows;
+  const int T = (ksplit || blockIdx.z == 0) ? epi.tiles(M) : 0;
   int t_begin = blockIdx.y, t_end = T, t_step = gridDim.y;
   if constexpr (Epi::kBlocked) {
     const int per = (T + gridDim.y - 1) / gridDim.y;
@@ -111,8 +114,8 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     t_step = 1;
   }
   const int n0 = blockIdx.x * BN;
-  const int kb0 = blockIdx.z * sh.kpc;
-  const int kb1 = min(sh.KB, kb0 + sh.kpc);
+  const int kb0 = ksplit ? blockIdx.z * sh.kpc : 0;
+  const int kb1 = ksplit ? min(sh.KB, kb0 + sh.kpc) : sh.KB;
 
   if (warp == 0) {
     if (lane == 0) {

@@ -32,10 +32,13 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
   __shared__ int s_live[1024];
   __shared__ int s_sel[1024];
   __shared__ int s_scan[32];
-  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ double s_sum[1024];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* a = assign + (long)b * N;
   const float* Db = D + (long)b * N;
-  double sum = 0.0;
+  for (int c = tid; c < C; c += blockDim.x) s_sum[c] = 0.0;
+  // warp w owns clusters w, w+32, ...: a ballot over 32 rows at a time finds
+  // the members, which lane 0 adds in ascending row order (fp64)
   for (int base = 0; base < N; base += kStage) {
     const int lim = min(kStage, N - base);
     __syncthreads();
@@ -44,14 +47,25 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
       s_d[e] = Db[base + e];
     }
     __syncthreads();
-    if (tid < C)
-      for (int e = 0; e < lim; ++e)
-        if (s_a[e] == tid) sum += (double)s_d[e];
+    for (int c = warp; c < C; c += 32) {
+      double sum = s_sum[c];
+      for (int e0 = 0; e0 < lim; e0 += 32) {
+        const int e = e0 + lane;
+        unsigned hit = __ballot_sync(0xffffffffu, e < lim && s_a[e] == c);
+        while (hit) {
+          const int j = __ffs(hit) - 1;
+          hit &= hit - 1;
+          sum += (double)s_d[e0 + j];
+        }
+      }
+      if (lane == 0) s_sum[c] = sum;
+    }
   }
+  __syncthreads();
   const int n = tid < C ? counts[(long)b * C + tid] : 0;
   const int live = (tid < C && n > 0) ? 1 : 0;
   s_live[tid] = live;
-  s_score[tid] = live ? sum / (double)n : 0.0;
+  s_score[tid] = live ? s_sum[tid] / (double)n : 0.0;
   const int nlive = __syncthreads_count(live);
   int chosen = 0;
   if (live) {
@@ -168,22 +182,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Column tiles of BN over [K | V]; when the selection is small (few row
+// tiles) the d dimension is split over blockIdx.z and every chunk stores fp32
+// partials [z][m][2*nkv], finished by k_refresh_finish; otherwise the
+// epilogue rounds and scatters directly.
 template <int BN>
 struct RefreshEpi : TcEpiBase {
   const int32_t* rowinfo;
   const int32_t* M_total;
-  int N, Ncache, off, nkv;
+  int N, Ncache, off, nkv, split_max_rows;
   __nv_bfloat16* Kc;
   __nv_bfloat16* Vc;
+  float* part;
   struct State {};
   __device__ int tiles(int M) const { return (M + 127) / 128; }
   __device__ int arow(int t) const { return t * 128; }
   __device__ int bsel(int, int n0) const { return n0 >= nkv ? 1 : 0; }
   __device__ int bcoord(int, int n0) const { return n0 >= nkv ? n0 - nkv : n0; }
   __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
-  __device__ void consume(int t, int rr, int n0, int, uint32_t taddr, State&) const {
+  __device__ void consume(int t, int rr, int n0, int z, uint32_t taddr, State&) const {
+    const int Mt = *M_total;
     const int m = t * 128 + rr;
-    const int r = m < *M_total ? rowinfo[m] : -1;
+    const int r = m < Mt ? rowinfo[m] : -1;
+    if (Mt <= split_max_rows) {
+      float* dst = part + ((long)z * split_max_rows + m) * (2 * nkv) + n0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(taddr + c0, v);  // warp-collective: every lane loads
+        if (m >= Mt) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(dst + c0 + 4 * j) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+      return;
+    }
     const bool is_v = n0 >= nkv;
     __nv_bfloat16* dst = nullptr;
     if (r >= 0) {
@@ -193,7 +227,7 @@ struct RefreshEpi : TcEpiBase {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       float v[32];
-      tc::tmem_ld32(taddr + c0, v);  // warp-collective: every lane loads
+      tc::tmem_ld32(taddr + c0, v);
       if (dst == nullptr) continue;
 #pragma unroll
       for (int c = 0; c < 32; c += 8) {
@@ -208,14 +242,70 @@ struct RefreshEpi : TcEpiBase {
   }
 };
 
+// Sums the d-chunk partials of every selected row in chunk order, rounds to
+// bf16 and scatters into the K or V cache (8 columns per thread).
+__global__ void __launch_bounds__(256)
+k_refresh_finish(const float* __restrict__ part, int nz, const int32_t* __restrict__ M_total,
+                 int split_max_rows, const int32_t* __restrict__ rowinfo, int N, int Ncache,
+                 int off, int nkv, __nv_bfloat16* __restrict__ Kc,
+                 __nv_bfloat16* __restrict__ Vc) {
+  const int M = *M_total;
+  if (M > split_max_rows) return;
+  const int w = 2 * nkv, ncol8 = w / 8;
+  const long total = (long)M * ncol8;
+  for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / ncol8), c = (int)(idx % ncol8) * 8;
+    const int r = rowinfo[m];
+    if (r < 0) continue;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int z = 0; z < nz; ++z) {
+      const float4* src =
+          reinterpret_cast<const float4*>(part + ((long)z * split_max_rows + m) * w + c);
+      const float4 x = __ldcg(src), y = __ldcg(src + 1);
+      acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+      acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+    }
+    const int b = r / N, p = r % N;
+    const bool is_v = c >= nkv;
+    __nv_bfloat16* dst =
+        (is_v ? Vc : Kc) + ((long)b * Ncache + off + p) * nkv + (is_v ? c - nkv : c);
+    uint4 q;
+    q.x = pack_bf16x2(acc[0], acc[1]);
+    q.y = pack_bf16x2(acc[2], acc[3]);
+    q.z = pack_bf16x2(acc[4], acc[5]);
+    q.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(dst) = q;
+  }
+}
+
+struct RefreshPlan {
+  int BN, ntiles, nz, kpc, KB, split_max_rows;
+};
+
+RefreshPlan refresh_plan(int B, int N, int d, int nkv) {
+  RefreshPlan p{};
+  p.BN = nkv % 256 == 0 ? 256 : (nkv % 128 == 0 ? 128 : 64);
+  p.ntiles = 2 * nkv / p.BN;
+  p.KB = ceil_div(d, 64);
+  p.nz = std::min(4, p.KB);
+  p.kpc = ceil_div(p.KB, p.nz);
+  p.nz = ceil_div(p.KB, p.kpc);
+  // split d only while the selected rows give less than a wave of tiles
+  p.split_max_rows = std::min(B * N, 128 * std::max(1, kSmTarget / p.ntiles));
+  if (p.nz == 1) p.split_max_rows = 0;
+  return p;
+}
+
 template <int BN>
-cudaError_t refresh_tc(const RefreshArgs& a, cudaStream_t s) {
+cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t s) {
   const int nkv = a.Hkv * a.dh;
   const long rows = (long)a.B * a.N;
   Carver cv(a.ws);
   __nv_bfloat16* X = cv.take<__nv_bfloat16>((size_t)rows * a.d);
   int32_t* rowinfo = cv.take<int32_t>((size_t)rows);
   int32_t* M_total = cv.take<int32_t>(4);
+  float* part = cv.take<float>((size_t)pl.nz * pl.split_max_rows * 2 * nkv);
   k_gather_rows<<<dim3(ceil_div(a.N, 8), a.B), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(a.H), a.pos, a.npos, a.B, a.N, a.d, X, rowinfo,
       M_total);
@@ -225,12 +315,18 @@ cudaError_t refresh_tc(const RefreshArgs& a, cudaStream_t s) {
       !make_tmap_bf16_2d(&maps.b[1], a.Wv, nkv, a.d, (uint64_t)nkv * 2, 64, 64))
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
-  TcShape sh{(int)rows, M_total, ceil_div(a.d, 64), ceil_div(a.d, 64), a.status};
-  const int ntiles = 2 * nkv / BN;
-  const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(2 * kSmTarget, ntiles)));
+  TcShape sh{(int)rows, M_total, pl.KB, pl.kpc, a.status, pl.split_max_rows};
+  const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(2 * kSmTarget, pl.ntiles)));
   RefreshEpi<BN> epi{{}, rowinfo, M_total, a.N, a.Ncache, a.cache_off, nkv,
-                     static_cast<__nv_bfloat16*>(a.Kc), static_cast<__nv_bfloat16*>(a.Vc)};
-  return launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(ntiles, gy, 1), s);
+                     pl.split_max_rows, static_cast<__nv_bfloat16*>(a.Kc),
+                     static_cast<__nv_bfloat16*>(a.Vc), part};
+  cudaError_t e = launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(pl.ntiles, gy, pl.nz), s);
+  if (e != cudaSuccess || pl.split_max_rows == 0) return e;
+  const long work = (long)pl.split_max_rows * (2 * nkv / 8);
+  k_refresh_finish<<<std::min(ceil_div(work, 256), 4 * kSmTarget), 256, 0, s>>>(
+      part, pl.nz, M_total, pl.split_max_rows, rowinfo, a.N, a.Ncache, a.cache_off, nkv,
+      static_cast<__nv_bfloat16*>(a.Kc), static_cast<__nv_bfloat16*>(a.Vc));
+  return cudaGetLastError();
 }
 
 template <typename T>
@@ -256,16 +352,25 @@ bool refresh_tc_ok(int dtype, int Hkv, int dh) {
   return dtype == PS_BF16 && (Hkv * dh) % 64 == 0;
 }
 
-size_t refresh_ws(int B, int N, int d) {
+size_t refresh_ws(int B, int N, int d, int Hkv, int dh) {
+  const RefreshPlan pl = refresh_plan(B, N, d, Hkv * dh);
   Carver cv(nullptr);
   cv.take<__nv_bfloat16>((size_t)B * N * d);
   cv.take<int32_t>((size_t)B * N);
   cv.take<int32_t>(4);
+  cv.take<float>((size_t)pl.nz * pl.split_max_rows * 2 * Hkv * dh);
   return cv.bytes();
 }
 
 cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s) {
-  if (refresh_tc_ok(a.dtype, a.Hkv, a.dh) && a.ws != nullptr) return refresh_tc<64>(a, s);
+  if (refresh_tc_ok(a.dtype, a.Hkv, a.dh) && a.ws != nullptr) {
+    const RefreshPlan pl = refresh_plan(a.B, a.N, a.d, a.Hkv * a.dh);
+    switch (pl.BN) {
+      case 256: return refresh_tc<256>(a, pl, s);
+      case 128: return refresh_tc<128>(a, pl, s);
+      default: return refresh_tc<64>(a, pl, s);
+    }
+  }
   return a.dtype == PS_F32 ? refresh_typed<float>(a, s)
                            : refresh_typed<__nv_bfloat16>(a, s);
 }

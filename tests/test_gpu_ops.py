@@ -388,7 +388,7 @@ def test_refresh_kv(widx, off):
     Kc0 = torch.randn(B, Ncache, w.Hkv, w.dh, device="cuda").to(dt)
     Vc0 = torch.randn(B, Ncache, w.Hkv, w.dh, device="cuda").to(dt)
     Kc, Vc = Kc0.clone(), Vc0.clone()
-    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=w.d)
+    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=w.d, Hkv=w.Hkv, dh=w.dh)
     ps.ps_refresh_kv(H, pos_t, npos_t, L["Wk"], L["Wv"], Kc, Vc, w.Hkv, w.dh, cache_off=off,
                      ws=ws)
     torch.cuda.synchronize()
@@ -427,7 +427,7 @@ def test_refresh_empty_selection_leaves_cache():
     pos = torch.full((2, 40), -1, dtype=torch.int32, device="cuda")
     npos = torch.zeros(2, dtype=torch.int32, device="cuda")
     H2 = torch.randn(2, 40, 64, device="cuda").to(torch.bfloat16)
-    ws = ps.workspace(ps.OP_REFRESH, B=2, N=40, d=64)
+    ws = ps.workspace(ps.OP_REFRESH, B=2, N=40, d=64, Hkv=2, dh=64)
     ps.ps_refresh_kv(H2, pos, npos, W, W, Kc, Vc, 2, 64, ws=ws)
     torch.cuda.synchronize()
     ps.ps_check()
@@ -446,7 +446,7 @@ def test_refresh_all_rows_ragged_d():
     npos = torch.full((B,), N, dtype=torch.int32, device="cuda")
     Kc = torch.zeros(B, N, Hkv, dh, device="cuda", dtype=torch.bfloat16)
     Vc = torch.zeros_like(Kc)
-    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=d)
+    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=d, Hkv=Hkv, dh=dh)
     ps.ps_refresh_kv(H, pos, npos, Wk, Wv, Kc, Vc, Hkv, dh, ws=ws)
     torch.cuda.synchronize()
     ps.ps_check()
