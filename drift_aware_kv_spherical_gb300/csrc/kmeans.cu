@@ -411,23 +411,31 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     if constexpr (FINAL) {
       if (tid < tot) rs += rho[(long)b * N + list[tid]];
     } else {
-      // members in ascending order; four rows' loads in flight at a time
+      // members in ascending order; the loads of up to kMemb rows are in
+      // flight together (the loop is latency-bound, not bandwidth-bound)
+      constexpr int kMemb = 8;
       int m = 0;
-      for (; m + 4 <= tot; m += 4) {
+      for (; m + kMemb <= tot; m += kMemb) {
+        uint4 raw[kMemb][G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int col = (g * 256 + tid) * V;
-          if (col < d) {
-            float v[4][V];
+        for (int q = 0; q < kMemb; ++q) {
+          const T* h = H + ((long)b * N + list[m + q]) * d;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              load16(H + ((long)b * N + list[m + q]) * d + col, v[q]);
+          for (int g = 0; g < G; ++g) {
+            const int col = (g * 256 + tid) * V;
+            raw[q][g] = col < d ? __ldg(reinterpret_cast<const uint4*>(h + col))
+                                : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float sc = list_inv[m + q];
+        for (int q = 0; q < kMemb; ++q) {
+          const float sc = list_inv[m + q];
 #pragma unroll
-              for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[q][e], sc, u[g][e]);
-            }
+          for (int g = 0; g < G; ++g) {
+            float v[V];
+            unpack16(raw[q][g], v, T{});
+#pragma unroll
+            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc, u[g][e]);
           }
         }
       }
@@ -511,7 +519,7 @@ KmPlan km_plan(int dtype, int B, int N, int d, int C) {
     p.mtb = ceil_div(N, 128);
     p.KB = ceil_div(d, 64);
     const int tiles = B * p.mtb;
-    int nz = std::min(16, std::max(1, ceil_div(kSmTarget, tiles)));
+    int nz = std::min(4, std::max(1, ceil_div(kSmTarget, tiles)));
     nz = std::min(nz, p.KB);
     p.kpc = ceil_div(p.KB, nz);
     p.nz = ceil_div(p.KB, p.kpc);

@@ -28,6 +28,18 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* p, float* out) {
   bf16x2_to_f32(v.w, out[6], out[7]);
 }
 
+// A 16-byte vector already in registers, widened to fp32.
+__device__ __forceinline__ void unpack16(const uint4& r, float* out, float) {
+  out[0] = __uint_as_float(r.x); out[1] = __uint_as_float(r.y);
+  out[2] = __uint_as_float(r.z); out[3] = __uint_as_float(r.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& r, float* out, __nv_bfloat16) {
+  bf16x2_to_f32(r.x, out[0], out[1]);
+  bf16x2_to_f32(r.y, out[2], out[3]);
+  bf16x2_to_f32(r.z, out[4], out[5]);
+  bf16x2_to_f32(r.w, out[6], out[7]);
+}
+
 // Exclusive prefix sum over the threads of a block (blockDim.x % 32 == 0,
 // <= 1024).  `scratch` holds 32 values.  Returns the exclusive prefix and
 // writes the block total to *total.  Contains __syncthreads().
