@@ -457,10 +457,11 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     n += tot;
     __syncthreads();
   }
-  if (c == 0 && tid == 0 && obj != nullptr) {
+  if (c == 0 && obj != nullptr) {  // block-uniform: CTA (0, b) folds the pass objective
     float so = 0.f;
-    for (int t = 0; t < ntile; ++t) so += objp[(long)b * ntile + t];
-    obj[(long)b * obj_ld + pass] = so;
+    for (int t = tid; t < ntile; t += 256) so += objp[(long)b * ntile + t];
+    so = block_sum_f32(so, s_red);
+    if (tid == 0) obj[(long)b * obj_ld + pass] = so;
   }
   if (tid == 0) counts[(long)b * C + c] = n;
   if constexpr (FINAL) {

@@ -1,9 +1,11 @@
 // A warp-specialised tcgen05 GEMM mainloop shared by the dense contractions.
 //
 // CTA = 6 warps: warp 0 issues TMA loads into an S-stage shared-memory ring,
-// warp 1 issues tcgen05.mma (one thread) into a 128 x BN fp32 accumulator
-// in TMEM, warps 2-5 drain the accumulator (each reads the TMEM lane quarter
-// it may access) and hand rows to an op-specific epilogue.  The CTA owns
+// warp 1 issues tcgen05.mma (one thread) into one of two 128 x BN fp32
+// accumulators in TMEM (double-buffered, so the MMAs of the next tile run
+// while the epilogue drains this one), warps 2-5 drain the accumulator (each
+// reads the TMEM lane quarter it may access) and hand rows to an op-specific
+// epilogue.  The CTA owns
 // one BN-column tile (blockIdx.x) and walks row tiles t < epi.tiles(M)
 // (strided by gridDim.y, or a contiguous block of them); the epilogue object
 // maps a tile to its TMA coordinates.  blockIdx.z selects a chunk of the K
@@ -75,34 +77,14 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
   uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + S;      // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* epi_scratch = smem + S * Cfg::kStage + 512;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
-    }
-    tc::mbar_init(acc_full, 1);
-    tc::mbar_init(acc_empty, 4);
-    tc::mbar_init(drain, 1);
-    *abort_flag = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tc::tma_prefetch(&maps.a[0]);
-    tc::tma_prefetch(&maps.b[0]);
-  }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, BN);
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-
+  // tiles of this CTA first: a CTA without work leaves before any set-up
   const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
   const bool ksplit = M <= sh.split_max_rows;
   const int T = (ksplit || blockIdx.z == 0) ? epi.tiles(M) : 0;
@@ -113,6 +95,31 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     t_end = min(T, t_begin + per);
     t_step = 1;
   }
+  if (t_begin >= t_end) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      tc::mbar_init(acc_full + j, 1);
+      tc::mbar_init(acc_empty + j, 4);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&maps.a[0]);
+    tc::tma_prefetch(&maps.b[0]);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * BN);
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
   const int n0 = blockIdx.x * BN;
   const int kb0 = ksplit ? blockIdx.z * sh.kpc : 0;
   const int kb1 = ksplit ? min(sh.KB, kb0 + sh.kpc) : sh.KB;
@@ -170,7 +177,12 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       int it = 0, tcount = 0;
       bool ok = true;
       for (int t = t_begin; ok && t < t_end; t += t_step, ++tcount) {
-        if (!tc::mbar_wait(acc_empty, (tcount & 1) ^ 1, sh.status, abort_flag)) { ok = false; break; }
+        const int buf = tcount & 1;
+        const uint32_t dacc = tmem + buf * BN;
+        if (!tc::mbar_wait(acc_empty + buf, ((tcount >> 1) & 1) ^ 1, sh.status, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc::fence_after_sync();
         for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % S;
@@ -185,22 +197,22 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
             const uint64_t ad = tc::desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::desc_sw128(b_base + kk * 2048, 8192, 1024)
                                      : tc::desc_sw128(b_base + kk * 32, 16, 1024);
-            tc::mma_bf16(tmem, ad, bd, Cfg::kIdesc, acc);
+            tc::mma_bf16(dacc, ad, bd, Cfg::kIdesc, acc);
             if constexpr (NA == 2)
-              tc::mma_bf16(tmem, tc::desc_sw128(a_base + Cfg::kA + kk * 32, 16, 1024), bd,
+              tc::mma_bf16(dacc, tc::desc_sw128(a_base + Cfg::kA + kk * 32, 16, 1024), bd,
                            Cfg::kIdesc, 1u);
             if constexpr (NB == 2) {
               const uint64_t bd2 =
                   B_MN ? tc::desc_sw128(b_base + Cfg::kB + kk * 2048, 8192, 1024)
                        : tc::desc_sw128(b_base + Cfg::kB + kk * 32, 16, 1024);
-              tc::mma_bf16(tmem, ad, bd2, Cfg::kIdesc, 1u);
+              tc::mma_bf16(dacc, ad, bd2, Cfg::kIdesc, 1u);
             }
           }
           tc::mma_commit(empty + s);
           ++it;
         }
         if (!ok) break;
-        tc::mma_commit(acc_full);
+        tc::mma_commit(acc_full + buf);
       }
       if (!ok) {  // wait for the MMAs already issued before TMEM is freed
         tc::mma_commit(drain);
@@ -216,19 +228,20 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     typename Epi::State est;
     int tcount = 0;
     for (int t = t_begin; t < t_end; t += t_step, ++tcount) {
-      if (!tc::mbar_wait(acc_full, tcount & 1, sh.status, abort_flag)) break;
+      const int buf = tcount & 1;
+      if (!tc::mbar_wait(acc_full + buf, (tcount >> 1) & 1, sh.status, abort_flag)) break;
       tc::fence_after_sync();
-      epi.consume(t, r, n0, blockIdx.z, tmem + lane_base, est);
+      epi.consume(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(acc_empty);
+      if (lane == 0) tc::mbar_arrive(acc_empty + buf);
       epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
     }
   }
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, BN);
+    tc::tmem_dealloc(tmem, 2 * BN);
   }
 }
 

@@ -28,7 +28,7 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
        uint8_t* __restrict__ posmask) {
   __shared__ int s_a[kStage];
   __shared__ float s_d[kStage];
-  __shared__ double s_score[1024];
+  __shared__ unsigned long long s_key[1024];
   __shared__ int s_live[1024];
   __shared__ int s_sel[1024];
   __shared__ int s_scan[32];
@@ -65,14 +65,17 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
   const int n = tid < C ? counts[(long)b * C + tid] : 0;
   const int live = (tid < C && n > 0) ? 1 : 0;
   s_live[tid] = live;
-  s_score[tid] = live ? s_sum[tid] / (double)n : 0.0;
+  const double me = live ? s_sum[tid] / (double)n : 0.0;
+  // D >= 0, so every mean is a non-negative double and its bit pattern
+  // orders like its value: rank on integer keys (exact, and cheap here)
+  s_key[tid] = live ? (unsigned long long)__double_as_longlong(me) : 0ull;
   const int nlive = __syncthreads_count(live);
   int chosen = 0;
   if (live) {
-    const double me = s_score[tid];
+    const unsigned long long mk = s_key[tid];
     int rank = 0;
     for (int c = 0; c < C; ++c)
-      if (s_live[c] && (s_score[c] > me || (s_score[c] == me && c < tid))) ++rank;
+      if (s_live[c] && (s_key[c] > mk || (s_key[c] == mk && c < tid))) ++rank;
     if (rank < k) {
       chosen = 1;
       sel[(long)b * k + rank] = tid;
@@ -316,7 +319,7 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   TcShape sh{(int)rows, M_total, pl.KB, pl.kpc, a.status, pl.split_max_rows};
-  const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(2 * kSmTarget, pl.ntiles)));
+  const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(4 * kSmTarget, pl.ntiles)));
   RefreshEpi<BN> epi{{}, rowinfo, M_total, a.N, a.Ncache, a.cache_off, nkv,
                      pl.split_max_rows, static_cast<__nv_bfloat16*>(a.Kc),
                      static_cast<__nv_bfloat16*>(a.Vc), part};
