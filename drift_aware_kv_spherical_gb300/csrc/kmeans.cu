@@ -371,13 +371,21 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
   }
 }
 
-// Per (cluster c, window b): members in ascending row order, 256 rows at a
-// time.  Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the
-// cluster is empty or its sum is zero), plus its bf16 split.  Final pass:
+// Per (cluster c, window b): members in ascending row order.  Each thread
+// owns V consecutive columns (V = 16 bytes of H) times up to kColGroups
+// groups, so a member row costs one 16-byte load per thread, and up to
+// kMemb member rows are loaded together.  Rows are scanned in blocks of 4096:
+// every thread counts the members in its contiguous run of rows, one block
+// scan places them, and the list (row, 1/||h||) sits in shared memory.
+// Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
+// is empty or its sum is zero), plus its bf16 split.  Final pass:
 // C_hat_c = mean(rho over members) * mu_c (kept when empty).  Both write the
 // cluster size; CTA (0, b) folds the pass objective from the tile partials.
+constexpr int kScanRows = 4096;
+constexpr int kColGroups = 2;
+
 template <typename T, bool FINAL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
 k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
                int d, int C, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
@@ -385,69 +393,68 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                float* __restrict__ chat, const float* __restrict__ objp, int ntile,
                float* __restrict__ obj, int obj_ld, int pass) {
   constexpr int V = Vec<T>::n;
-  constexpr int G = kMaxD / (256 * V);
-  __shared__ int list[256];
-  __shared__ float list_inv[256];
+  constexpr int kMemb = 8;
+  __shared__ int list[kScanRows];
+  __shared__ float list_inv[kScanRows];
   __shared__ int s_scan[32];
-  __shared__ float s_red[8];
-  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  float u[G][V];
+  __shared__ float s_red[32];
+  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
+  float u[kColGroups][V];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; g < kColGroups; ++g)
 #pragma unroll
     for (int e = 0; e < V; ++e) u[g][e] = 0.f;
   float rs = 0.f;
   int n = 0;
-  for (int base = 0; base < N; base += 256) {
-    const int i = base + tid;
-    const int f = (i < N && assign[(long)b * N + i] == c) ? 1 : 0;
+  for (int base = 0; base < N; base += kScanRows) {
+    const int len = min(kScanRows, N - base);
+    const int R = (len + nthr - 1) / nthr;  // <= 64
+    const int r0 = base + tid * R;
+    unsigned long long hit = 0ull;
+    int cnt = 0;
+    for (int q = 0; q < R; ++q) {
+      const int i = r0 + q;
+      if (i < base + len && assign[(long)b * N + i] == c) {
+        hit |= 1ull << q;
+        ++cnt;
+      }
+    }
     int tot;
-    const int ex = block_exclusive_scan<int>(f, s_scan, &tot);
-    if (f) {
-      list[ex] = i;
-      if constexpr (!FINAL) list_inv[ex] = inv[(long)b * N + i];
+    int w = block_exclusive_scan<int>(cnt, s_scan, &tot);
+    while (hit) {
+      const int q = __ffsll(hit) - 1;
+      hit &= hit - 1;
+      const int i = r0 + q;
+      list[w] = i;
+      if constexpr (!FINAL) list_inv[w] = inv[(long)b * N + i];
+      ++w;
     }
     __syncthreads();
     if constexpr (FINAL) {
-      if (tid < tot) rs += rho[(long)b * N + list[tid]];
+      for (int m = tid; m < tot; m += nthr) rs += rho[(long)b * N + list[m]];
     } else {
-      // members in ascending order; the loads of up to kMemb rows are in
-      // flight together (the loop is latency-bound, not bandwidth-bound)
-      constexpr int kMemb = 8;
       int m = 0;
-      for (; m + kMemb <= tot; m += kMemb) {
-        uint4 raw[kMemb][G];
+      for (; m < tot; m += kMemb) {
+        const int cnt_m = min(kMemb, tot - m);
+        uint4 raw[kMemb][kColGroups];
 #pragma unroll
         for (int q = 0; q < kMemb; ++q) {
-          const T* h = H + ((long)b * N + list[m + q]) * d;
+          const T* h = H + ((long)b * N + list[m + (q < cnt_m ? q : 0)]) * d;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const int col = (g * 256 + tid) * V;
-            raw[q][g] = col < d ? __ldg(reinterpret_cast<const uint4*>(h + col))
-                                : make_uint4(0u, 0u, 0u, 0u);
+          for (int g = 0; g < kColGroups; ++g) {
+            const int col = (g * nthr + tid) * V;
+            raw[q][g] = (q < cnt_m && col < d)
+                            ? __ldg(reinterpret_cast<const uint4*>(h + col))
+                            : make_uint4(0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
         for (int q = 0; q < kMemb; ++q) {
-          const float sc = list_inv[m + q];
+          const float sc = q < cnt_m ? list_inv[m + q] : 0.f;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
+          for (int g = 0; g < kColGroups; ++g) {
             float v[V];
             unpack16(raw[q][g], v, T{});
-#pragma unroll
-            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc, u[g][e]);
-          }
-        }
-      }
-      for (; m < tot; ++m) {
-        const float sc = list_inv[m];
-        const T* h = H + ((long)b * N + list[m]) * d;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int col = (g * 256 + tid) * V;
-          if (col < d) {
-            float v[V];
-            load16(h + col, v);
 #pragma unroll
             for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc, u[g][e]);
           }
@@ -459,7 +466,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   }
   if (c == 0 && obj != nullptr) {  // block-uniform: CTA (0, b) folds the pass objective
     float so = 0.f;
-    for (int t = tid; t < ntile; t += 256) so += objp[(long)b * ntile + t];
+    for (int t = tid; t < ntile; t += nthr) so += objp[(long)b * ntile + t];
     so = block_sum_f32(so, s_red);
     if (tid == 0) obj[(long)b * obj_ld + pass] = so;
   }
@@ -468,13 +475,13 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     const float tot = block_sum_f32(rs, s_red);
     if (n == 0) return;
     const float mean = tot / (float)n;
-    const float* m = mu + ((long)b * C + c) * d;
+    const float* mc = mu + ((long)b * C + c) * d;
     float* o = chat + ((long)b * C + c) * d;
-    for (int k = tid; k < d; k += 256) o[k] = mean * m[k];
+    for (int k = tid; k < d; k += nthr) o[k] = mean * mc[k];
   } else {
     float ss = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < kColGroups; ++g)
 #pragma unroll
       for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
     ss = block_sum_f32(ss, s_red);
@@ -482,8 +489,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     if (n == 0 || !(nu > 0.f)) return;
     const long ro = ((long)b * C + c) * d;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const int col = (g * 256 + tid) * V;
+    for (int g = 0; g < kColGroups; ++g) {
+      const int col = (g * nthr + tid) * V;
       if (col < d) {
 #pragma unroll
         for (int e = 0; e < V; ++e) {
@@ -498,6 +505,16 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
       }
     }
   }
+}
+
+// Threads of the cluster-scan CTAs: enough for one 16-byte vector per thread
+// across d (kColGroups of them when d needs more than 1024 threads).
+template <typename T>
+int scan_threads(int d) {
+  const int vecs = ceil_div(d, Vec<T>::n);
+  const int want = vecs <= 1024 ? vecs : ceil_div(vecs, kColGroups);
+  // >= 64 threads keeps each thread's run of rows within a 64-bit mask
+  return std::max(64, std::min(1024, ceil_div(want, 32) * 32));
 }
 
 struct KmPlan {
@@ -611,11 +628,11 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     if (e != cudaSuccess) return e;
     if (t < a.iters)
-      k_cluster_scan<T, false><<<dim3(a.C, a.B), 256, 0, s>>>(
+      k_cluster_scan<T, false><<<dim3(a.C, a.B), scan_threads<T>(a.d), 0, s>>>(
           H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, p.tc ? w.mu_hi : nullptr,
           w.mu_lo, a.counts, a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
   }
-  k_cluster_scan<T, true><<<dim3(a.C, a.B), 256, 0, s>>>(
+  k_cluster_scan<T, true><<<dim3(a.C, a.B), scan_threads<T>(a.d), 0, s>>>(
       H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, nullptr, nullptr, a.counts, a.chat,
       w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
   return cudaGetLastError();
