@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kCT)
 k_commit_scan(const float* __restrict__ logits, int V, int nchunk,
               float* __restrict__ pm, int* __restrict__ pidx,
               double* __restrict__ ps) {
+  pdl_prologue();
   __shared__ float s_m[kCT / 32];
   __shared__ int s_i[kCT / 32];
   __shared__ double s_s[kCT / 32];
@@ -91,6 +92,7 @@ k_commit_rule(int P, int nchunk, const float* __restrict__ pm,
               const uint8_t* __restrict__ suffix_sel, int sel_ld,
               ps_commit_params p, int32_t* __restrict__ token,
               float* __restrict__ conf, uint8_t* __restrict__ commit) {
+  pdl_prologue();
   __shared__ double s_c[32];
   __shared__ int s_j[32];
   const int b = blockIdx.x, j = threadIdx.x;
@@ -187,9 +189,9 @@ cudaError_t commit_run(const CommitArgs& a, cudaStream_t s) {
   float* pm = cv.take<float>(rows);
   int* pidx = cv.take<int>(rows);
   double* ps = cv.take<double>(rows);
-  k_commit_scan<<<dim3(nc, a.B * a.P), kCT, 0, s>>>(a.logits, a.V, nc, pm, pidx, ps);
+  launch_pdl(k_commit_scan, dim3(nc, a.B * a.P), kCT, 0, s, a.logits, a.V, nc, pm, pidx, ps);
   const int threads = ((a.P + 31) / 32) * 32;
-  k_commit_rule<<<a.B, threads, 0, s>>>(a.P, nc, pm, pidx, ps, a.role, a.undecided,
+  launch_pdl(k_commit_rule, a.B, threads, 0, s, a.P, nc, pm, pidx, ps, a.role, a.undecided,
                                         a.D, a.d_ld, a.d_sum, a.d_cnt, a.d_prev,
                                         a.suffix_sel, a.sel_ld, a.p, a.token, a.conf,
                                         a.commit);

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/polestar.h"
 
 struct ps_handle_s {
@@ -55,6 +57,32 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 // Record the first device-side failure of a call in the handle's word.
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Programmatic dependent launch.  Every library kernel is launched with
+// launch_pdl, so the next grid on the stream may be scheduled while this one
+// drains; each kernel starts with pdl_prologue(), which waits until the grid
+// before it has finished and its writes are visible (griddepcontrol.wait),
+// then lets the following grid be scheduled.
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __host__ __device__ inline int ceil_div(long a, long b) { return (int)((a + b - 1) / b); }

@@ -7,7 +7,8 @@
 //
 // Kernels (one launch each, all on the caller's stream):
 //   k_inv_norm      1/||h_i||                                (one warp per row)
-//   k_kpp           k-means++ seeding, one CTA per window    (init_mode 1)
+//   k_kpp_pick      k-means++ centre r, one CTA per window   (init_mode 1)
+//   k_kpp_weights   weights against centre r, warp per row   (C - 1 rounds)
 //   k_split_mu      mu -> (mu_hi, mu_lo) bf16 for the tensor cores
 //   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
 //                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
@@ -36,6 +37,7 @@ constexpr int kMaxD = 8192;
 template <typename T>
 __global__ void k_inv_norm(const T* __restrict__ H, long rows, int d,
                            float* __restrict__ inv) {
+  pdl_prologue();
   constexpr int V = Vec<T>::n;
   const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -52,75 +54,90 @@ __global__ void k_inv_norm(const T* __restrict__ H, long rows, int d,
   if (lane == 0) inv[row] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
 }
 
-// k-means++ on the sphere: one CTA of 1024 threads per window.  Weights
-// w_i = 1 - max cos to the chosen centres (0 for chosen rows); centre r is
-// the first row whose running sum of w (fp64) exceeds u_r * sum(w).
+// k-means++ on the sphere, one round r at a time: k_kpp_pick chooses centre
+// r (one CTA per window), then k_kpp_weights lowers every row's weight to
+// w_i = min(w_i, max(0, 1 - cos(h_i, centre r))) (0 for chosen rows) over the
+// whole grid.  Centre 0 is row floor(u_0 N); centre r >= 1 is the first row
+// whose running sum of w (fp64, row order) exceeds u_r * sum(w), or the first
+// row not yet chosen when every weight is 0.
 template <typename T>
 __global__ void __launch_bounds__(1024)
-k_kpp(const T* __restrict__ H, const float* __restrict__ inv_all,
-      const double* __restrict__ U, int N, int d, int C, float* __restrict__ mu,
-      float* __restrict__ w_all, int8_t* __restrict__ chosen_all) {
-  extern __shared__ float smu[];  // d floats: the newest centre
+k_kpp_pick(const T* __restrict__ H, const float* __restrict__ inv_all,
+           const double* __restrict__ U, int N, int d, int C, int r, float* __restrict__ mu,
+           const float* __restrict__ w_all, int8_t* __restrict__ chosen_all) {
   __shared__ double s_scan[32];
   __shared__ int s_min[32];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, tid = threadIdx.x;
   const T* Hb = H + (long)b * N * d;
   const float* inv = inv_all + (long)b * N;
-  float* w = w_all + (long)b * N;
+  const float* w = w_all + (long)b * N;
   int8_t* chosen = chosen_all + (long)b * N;
-  float* mub = mu + (long)b * C * d;
   const double* u = U + (long)b * C;
-  for (int i = tid; i < N; i += blockDim.x) chosen[i] = 0;
-  __syncthreads();
-  const int chunk = (N + blockDim.x - 1) / blockDim.x;
-  for (int r = 0; r < C; ++r) {
-    int pick = INT_MAX;
-    if (r == 0) {
-      pick = min(max((int)floor(u[0] * (double)N), 0), N - 1);
-    } else {
-      const int lo = tid * chunk, hi = min(N, lo + chunk);
-      double s = 0.0;
-      for (int i = lo; i < hi; ++i) s += (double)w[i];
-      double total;
-      double base = block_exclusive_scan<double>(s, s_scan, &total);
-      int cand = INT_MAX;
-      if (total > 0.0) {
-        const double target = u[r] * total;
-        double run = base;
-        for (int i = lo; i < hi; ++i) {
-          run += (double)w[i];
-          if (run > target) { cand = i; break; }
-        }
+  if (r == 0) {
+    for (int i = tid; i < N; i += blockDim.x) chosen[i] = 0;
+    __syncthreads();
+  }
+  int pick;
+  if (r == 0) {
+    pick = min(max((int)floor(u[0] * (double)N), 0), N - 1);
+  } else {
+    const int chunk = (N + blockDim.x - 1) / blockDim.x;
+    const int lo = tid * chunk, hi = min(N, lo + chunk);
+    double sum = 0.0;
+    for (int i = lo; i < hi; ++i) sum += (double)w[i];
+    double total;
+    const double base = block_exclusive_scan<double>(sum, s_scan, &total);
+    int cand = INT_MAX;
+    if (total > 0.0) {
+      const double target = u[r] * total;
+      double run = base;
+      for (int i = lo; i < hi; ++i) {
+        run += (double)w[i];
+        if (run > target) { cand = i; break; }
       }
+    }
+    pick = block_min_int(cand, s_min);
+    if (pick == INT_MAX) {  // no weight left: first row not yet chosen
+      cand = INT_MAX;
+      for (int i = tid; i < N; i += blockDim.x)
+        if (!chosen[i]) { cand = i; break; }
       pick = block_min_int(cand, s_min);
-      if (pick == INT_MAX) {  // no weight left: first row not yet chosen
-        cand = INT_MAX;
-        for (int i = tid; i < N; i += blockDim.x)
-          if (!chosen[i]) { cand = i; break; }
-        pick = block_min_int(cand, s_min);
-        if (pick == INT_MAX) pick = 0;
-      }
+      if (pick == INT_MAX) pick = 0;
     }
-    __syncthreads();
-    if (tid == 0) chosen[pick] = 1;
-    const float ip = inv[pick];
-    for (int k = tid; k < d; k += blockDim.x) {
-      const float v = to_f32(Hb[(long)pick * d + k]) * ip;
-      smu[k] = v;
-      mub[(long)r * d + k] = v;
-    }
-    __syncthreads();
-    for (int row = warp; row < N; row += blockDim.x >> 5) {
-      const T* h = Hb + (long)row * d;
-      float dot = 0.f;
-      for (int k = lane; k < d; k += 32) dot = fmaf(to_f32(h[k]), smu[k], dot);
-      dot = warp_sum(dot);
-      if (lane == 0) {
-        const float cw = chosen[row] ? 0.f : fmaxf(0.f, 1.f - dot * inv[row]);
-        w[row] = (r == 0) ? cw : fminf(w[row], cw);
-      }
-    }
-    __syncthreads();
+  }
+  __syncthreads();
+  if (tid == 0) chosen[pick] = 1;
+  const float ip = inv[pick];
+  float* mur = mu + ((long)b * C + r) * d;
+  for (int k = tid; k < d; k += blockDim.x) mur[k] = to_f32(Hb[(long)pick * d + k]) * ip;
+}
+
+// One warp per row: cosine with centre r, weight update.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_kpp_weights(const T* __restrict__ H, const float* __restrict__ inv, int B, int N, int d,
+              int C, int r, const float* __restrict__ mu, float* __restrict__ w,
+              const int8_t* __restrict__ chosen) {
+  constexpr int V = Vec<T>::n;
+  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= (long)B * N) return;
+  const int b = (int)(row / N);
+  const T* h = H + row * d;
+  const float* m = mu + ((long)b * C + r) * d;
+  float dot = 0.f;
+  for (int k = lane * V; k < d; k += 32 * V) {
+    float hv[V], mv[V];
+    load16(h + k, hv);
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) load16(m + k + 4 * q, mv + 4 * q);
+#pragma unroll
+    for (int e = 0; e < V; ++e) dot = fmaf(hv[e], mv[e], dot);
+  }
+  dot = warp_sum(dot);
+  if (lane == 0) {
+    const float cw = chosen[row] ? 0.f : fmaxf(0.f, 1.f - dot * inv[row]);
+    w[row] = (r == 0) ? cw : fminf(w[row], cw);
   }
 }
 
@@ -132,6 +149,7 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
          const float* __restrict__ inv, int N, int d, int C,
          int32_t* __restrict__ assign, float* __restrict__ best_dot,
          float* __restrict__ objp) {
+  pdl_prologue();
   __shared__ __align__(16) float Hs[kTileK][kTileRows];
   __shared__ __align__(16) float Ms[kTileK][kTileC];
   __shared__ float s_red[8];
@@ -253,6 +271,7 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
 // fp32 centroids -> bf16 hi + lo parts (hi = bf16(mu), lo = bf16(mu - hi)).
 __global__ void k_split_mu(const float* __restrict__ mu, long n, __nv_bfloat16* __restrict__ hi,
                            __nv_bfloat16* __restrict__ lo) {
+  pdl_prologue();
   const long stride = (long)gridDim.x * blockDim.x;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float x = mu[i];
@@ -335,6 +354,7 @@ __global__ void __launch_bounds__(256)
 k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
             const float* __restrict__ inv, int32_t* __restrict__ assign,
             float* __restrict__ best, float* __restrict__ objp) {
+  pdl_prologue();
   __shared__ float s_cos[8];
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
@@ -392,6 +412,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
                float* __restrict__ chat, const float* __restrict__ objp, int ntile,
                float* __restrict__ obj, int obj_ld, int pass) {
+  pdl_prologue();
   constexpr int V = Vec<T>::n;
   constexpr int kMemb = 8;
   __shared__ int list[kScanRows];
@@ -592,7 +613,7 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaS
   cudaError_t e =
       launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
   if (e != cudaSuccess || p.nz == 1) return e;
-  k_km_argmax<<<dim3(ceil_div(a.N, 8), a.B), 256, 0, s>>>(w.part, p.nz, a.B, a.N, a.C,
+  launch_pdl(k_km_argmax, dim3(ceil_div(a.N, 8), a.B), 256, 0, s, w.part, p.nz, a.B, a.N, a.C,
                                                           w.inv, a.assign, a.rho, w.objp);
   return cudaGetLastError();
 }
@@ -604,13 +625,19 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const KmPlan p = km_plan(a.dtype, a.B, a.N, a.d, a.C);
   const KmWs w = km_carve(a.ws, p, a.B, a.N, a.d, a.C, nullptr);
 
-  k_inv_norm<T><<<ceil_div(BN_ * 32, 256), 256, 0, s>>>(H, BN_, a.d, w.inv);
-  if (a.init_mode == 1)
-    k_kpp<T><<<a.B, 1024, a.d * sizeof(float), s>>>(H, w.inv, a.init_u, a.N, a.d, a.C, a.mu,
-                                                    w.w, w.chosen);
+  launch_pdl(k_inv_norm<T>, ceil_div(BN_ * 32, 256), 256, 0, s, H, BN_, a.d, w.inv);
+  if (a.init_mode == 1) {
+    for (int r = 0; r < a.C; ++r) {
+      launch_pdl(k_kpp_pick<T>, a.B, 1024, 0, s, H, w.inv, a.init_u, a.N, a.d, a.C, r, a.mu,
+                 w.w, w.chosen);
+      if (r + 1 < a.C)
+        launch_pdl(k_kpp_weights<T>, ceil_div(BN_ * 32, 256), 256, 0, s, H, w.inv, a.B, a.N,
+                   a.d, a.C, r, a.mu, w.w, w.chosen);
+    }
+  }
   if (p.tc) {
     const long n = (long)a.B * a.C * a.d;
-    k_split_mu<<<std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s>>>(a.mu, n, w.mu_hi,
+    launch_pdl(k_split_mu, std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s, a.mu, n, w.mu_hi,
                                                                          w.mu_lo);
   }
   for (int t = 0; t <= a.iters; ++t) {
@@ -623,16 +650,16 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
         default: e = assign_tc<256>(a, p, w, s); break;
       }
     } else {
-      k_assign<T><<<dim3(p.ntile, a.B), 256, 0, s>>>(H, a.mu, w.inv, a.N, a.d, a.C,
+      launch_pdl(k_assign<T>, dim3(p.ntile, a.B), 256, 0, s, H, a.mu, w.inv, a.N, a.d, a.C,
                                                      a.assign, a.rho, w.objp);
     }
     if (e != cudaSuccess) return e;
     if (t < a.iters)
-      k_cluster_scan<T, false><<<dim3(a.C, a.B), scan_threads<T>(a.d), 0, s>>>(
+      launch_pdl(k_cluster_scan<T, false>, dim3(a.C, a.B), scan_threads<T>(a.d), 0, s, 
           H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, p.tc ? w.mu_hi : nullptr,
           w.mu_lo, a.counts, a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
   }
-  k_cluster_scan<T, true><<<dim3(a.C, a.B), scan_threads<T>(a.d), 0, s>>>(
+  launch_pdl(k_cluster_scan<T, true>, dim3(a.C, a.B), scan_threads<T>(a.d), 0, s, 
       H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, nullptr, nullptr, a.counts, a.chat,
       w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
   return cudaGetLastError();

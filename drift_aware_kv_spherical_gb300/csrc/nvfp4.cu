@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads)
 k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
            const int32_t* __restrict__ assign, const float* __restrict__ rho,
            int N, int d, int C, float* __restrict__ part) {
+  pdl_prologue();
   __shared__ float s_red[kThreads / 32];
   const int b = blockIdx.y;
   const int bpr = d / 16;
@@ -123,6 +124,7 @@ k_fp4_quant(const T* __restrict__ H, const float* __restrict__ mu,
             int N, int d, int C, const float* __restrict__ part, int nparts,
             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
             float* __restrict__ S_out) {
+  pdl_prologue();
   __shared__ float s_red[kThreads / 32];
   const int b = blockIdx.y;
   float amax = 0.f;
@@ -173,9 +175,9 @@ cudaError_t run_typed(const Nvfp4Args& a, cudaStream_t s) {
   const int gx = grid_x(a.B, a.N, a.d);
   float* part = Carver(a.ws).take<float>((size_t)a.B * gx);
   const dim3 grid(gx, a.B);
-  k_fp4_amax<T><<<grid, kThreads, 0, s>>>(H, a.mu, a.assign, a.rho, a.N, a.d,
+  launch_pdl(k_fp4_amax<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.N, a.d,
                                           a.C, part);
-  k_fp4_quant<T><<<grid, kThreads, 0, s>>>(H, a.mu, a.assign, a.rho, a.N, a.d,
+  launch_pdl(k_fp4_quant<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.N, a.d,
                                            a.C, part, gx, a.codes, a.scales, a.S);
   return cudaGetLastError();
 }

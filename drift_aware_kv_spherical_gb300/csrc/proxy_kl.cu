@@ -38,6 +38,7 @@ template <typename TW>
 __global__ void __launch_bounds__(256)
 k_ckeys(const float* __restrict__ chat, const TW* __restrict__ Wk, int M,
         int nout, int d, int klen, float* __restrict__ out) {
+  pdl_prologue();
   __shared__ __align__(16) SimtSmem sm;
   __shared__ long arow[kSimtM];
   const int tid = threadIdx.x;
@@ -60,6 +61,7 @@ k_ckeys(const float* __restrict__ chat, const TW* __restrict__ Wk, int M,
 
 __global__ void k_split_reduce(const float* __restrict__ part, int nsplit,
                                long count, float* __restrict__ out) {
+  pdl_prologue();
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
        i += (long)gridDim.x * blockDim.x) {
     float s = part[i];
@@ -113,6 +115,7 @@ k_proxy(const T* __restrict__ Q, const float* __restrict__ Kt, int N, int C,
         int Hq, int Hkv, int dh, int hps, float scale,
         const float* __restrict__ A_prev, float* __restrict__ A_cur,
         float* __restrict__ D, float* __restrict__ part) {
+  pdl_prologue();
   extern __shared__ float smem[];
   constexpr int Cp = 16 * NJ;
   constexpr int V = Vec<T>::n;
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(256)
 k_proxy_final(const float* __restrict__ part, int nslice, int B, int N, int C,
               int Hq, const float* __restrict__ A_prev, float* __restrict__ A_cur,
               float* __restrict__ D) {
+  pdl_prologue();
   const int b = blockIdx.y, tid = threadIdx.x, r = tid >> 4, l = tid & 15;
   const int i = blockIdx.x * kRows + r;
   float Aacc[NJ];
@@ -221,6 +225,7 @@ cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cuda
 // ------------------------------------------------------------ tensor cores
 __global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* __restrict__ hi,
                             __nv_bfloat16* __restrict__ lo) {
+  pdl_prologue();
   const long stride = (long)gridDim.x * blockDim.x;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float v = x[i];
@@ -275,6 +280,7 @@ struct CkeysEpi : TcEpiBase {
 __global__ void __launch_bounds__(256)
 k_ckeys_finish(const float* __restrict__ part, int nz, long count,
                __nv_bfloat16* __restrict__ khi, __nv_bfloat16* __restrict__ klo) {
+  pdl_prologue();
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
        i += (long)gridDim.x * blockDim.x) {
     float sum = 0.f;
@@ -429,7 +435,7 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   const int nkv = a.Hkv * a.dh;
   const TcWs w = tc_carve(a.ws, p, a.B, a.N, a.d, a.C, nkv, nullptr);
   const long nc = (long)a.B * a.C * a.d;
-  k_split_f32<<<std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s>>>(a.chat, nc, w.chi,
+  launch_pdl(k_split_f32, std::min(ceil_div(nc, 256), 4 * kSmTarget), 256, 0, s, a.chat, nc, w.chi,
                                                                           w.clo);
   {
     TcMaps maps;
@@ -451,7 +457,7 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (p.ck_nz > 1) {
       const long count = (long)a.B * a.C * nkv;
-      k_ckeys_finish<<<std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s>>>(
+      launch_pdl(k_ckeys_finish, std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s, 
           w.kpart, p.ck_nz, count, w.khi, w.klo);
     }
   }
@@ -508,11 +514,11 @@ size_t proxy_smem(int dh, int NJ) {
 cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cudaStream_t s) {
   const dim3 grid(ceil_div(a.N, kRows), a.B);
   switch (nj_for(a.C)) {
-    case 1: k_proxy_final<1><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 2: k_proxy_final<2><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 4: k_proxy_final<4><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 8: k_proxy_final<8><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    default: k_proxy_final<16><<<grid, 256, 0, s>>>(part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 1: launch_pdl(k_proxy_final<1>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 2: launch_pdl(k_proxy_final<2>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 4: launch_pdl(k_proxy_final<4>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    case 8: launch_pdl(k_proxy_final<8>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
+    default: launch_pdl(k_proxy_final<16>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
   }
   return cudaGetLastError();
 }
@@ -529,11 +535,11 @@ cudaError_t launch_proxy(const ProxyArgs& a, const Plan& p, const float* Kt,
   }
   const float scale = (float)(1.0 / std::sqrt((double)a.dh));
   const dim3 grid(ceil_div(a.N, kRows), a.B, p.nslice);
-  k_proxy<T, NJ><<<grid, 256, smem, s>>>(
+  launch_pdl(k_proxy<T, NJ>, grid, 256, smem, s, 
       static_cast<const T*>(a.Q), Kt, a.N, a.C, a.Hq, a.Hkv, a.dh, p.hps, scale,
       a.A_prev, a.A_cur, a.D, p.nslice > 1 ? part : nullptr);
   if (p.nslice > 1)
-    k_proxy_final<NJ><<<dim3(ceil_div(a.N, kRows), a.B), 256, 0, s>>>(
+    launch_pdl(k_proxy_final<NJ>, dim3(ceil_div(a.N, kRows), a.B), 256, 0, s, 
         part, p.nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D);
   return cudaGetLastError();
 }
@@ -548,11 +554,11 @@ cudaError_t run_typed(const ProxyArgs& a, cudaStream_t s) {
   float* apart = p.nslice > 1 ? cv.take<float>((size_t)p.nslice * a.B * a.N * a.C) : nullptr;
 
   const dim3 g1(ceil_div(nout, kSimtN), ceil_div(M, kSimtM), p.nsplit);
-  k_ckeys<T><<<g1, 256, 0, s>>>(a.chat, static_cast<const T*>(a.Wk), M, nout,
+  launch_pdl(k_ckeys<T>, g1, 256, 0, s, a.chat, static_cast<const T*>(a.Wk), M, nout,
                                 a.d, p.klen, p.nsplit > 1 ? kpart : Kt);
   if (p.nsplit > 1) {
     const long count = (long)M * nout;
-    k_split_reduce<<<std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s>>>(
+    launch_pdl(k_split_reduce, std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s, 
         kpart, p.nsplit, count, Kt);
   }
   switch (nj_for(a.C)) {

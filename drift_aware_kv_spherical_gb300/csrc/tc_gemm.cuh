@@ -70,6 +70,7 @@ struct TcCfg {
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __global__ void __launch_bounds__(192, 1)
 k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
+  pdl_prologue();
   using Cfg = TcCfg<BN, NA, NB, B_MN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -268,7 +269,7 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, 192, Cfg::kSmem, s>>>(maps, sh, epi);
+  launch_pdl(kern, grid, 192, Cfg::kSmem, s, maps, sh, epi);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
        int32_t* __restrict__ sel, float* __restrict__ sel_score,
        int32_t* __restrict__ pos, int32_t* __restrict__ npos,
        uint8_t* __restrict__ posmask) {
+  pdl_prologue();
   __shared__ int s_a[kStage];
   __shared__ float s_d[kStage];
   __shared__ unsigned long long s_key[1024];
@@ -112,6 +113,7 @@ k_refresh(const T* __restrict__ H, const int32_t* __restrict__ pos,
           const int32_t* __restrict__ npos, const T* __restrict__ Wk,
           const T* __restrict__ Wv, int N, int d, int nout, T* __restrict__ Kc,
           T* __restrict__ Vc, int Ncache, int off) {
+  pdl_prologue();
   __shared__ __align__(16) SimtSmem sm;
   __shared__ long arow[kSimtM];
   __shared__ int prow[kSimtM];
@@ -160,6 +162,7 @@ k_gather_rows(const __nv_bfloat16* __restrict__ H, const int32_t* __restrict__ p
               const int32_t* __restrict__ npos, int B, int N, int d,
               __nv_bfloat16* __restrict__ X, int32_t* __restrict__ rowinfo,
               int32_t* __restrict__ M_total) {
+  pdl_prologue();
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int off = 0, total = 0;
   for (int bb = 0; bb < B; ++bb) {
@@ -252,6 +255,7 @@ k_refresh_finish(const float* __restrict__ part, int nz, const int32_t* __restri
                  int split_max_rows, const int32_t* __restrict__ rowinfo, int N, int Ncache,
                  int off, int nkv, __nv_bfloat16* __restrict__ Kc,
                  __nv_bfloat16* __restrict__ Vc) {
+  pdl_prologue();
   const int M = *M_total;
   if (M > split_max_rows) return;
   const int w = 2 * nkv, ncol8 = w / 8;
@@ -309,7 +313,7 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
   int32_t* rowinfo = cv.take<int32_t>((size_t)rows);
   int32_t* M_total = cv.take<int32_t>(4);
   float* part = cv.take<float>((size_t)pl.nz * pl.split_max_rows * 2 * nkv);
-  k_gather_rows<<<dim3(ceil_div(a.N, 8), a.B), 256, 0, s>>>(
+  launch_pdl(k_gather_rows, dim3(ceil_div(a.N, 8), a.B), 256, 0, s, 
       static_cast<const __nv_bfloat16*>(a.H), a.pos, a.npos, a.B, a.N, a.d, X, rowinfo,
       M_total);
   TcMaps maps;
@@ -326,7 +330,7 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
   cudaError_t e = launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(pl.ntiles, gy, pl.nz), s);
   if (e != cudaSuccess || pl.split_max_rows == 0) return e;
   const long work = (long)pl.split_max_rows * (2 * nkv / 8);
-  k_refresh_finish<<<std::min(ceil_div(work, 256), 4 * kSmTarget), 256, 0, s>>>(
+  launch_pdl(k_refresh_finish, std::min(ceil_div(work, 256), 4 * kSmTarget), 256, 0, s, 
       part, pl.nz, M_total, pl.split_max_rows, rowinfo, a.N, a.Ncache, a.cache_off, nkv,
       static_cast<__nv_bfloat16*>(a.Kc), static_cast<__nv_bfloat16*>(a.Vc));
   return cudaGetLastError();
@@ -336,7 +340,7 @@ template <typename T>
 cudaError_t refresh_typed(const RefreshArgs& a, cudaStream_t s) {
   const int nout = a.Hkv * a.dh;
   const dim3 grid(std::min(ceil_div(a.N, kSimtM), 8), 2 * ceil_div(nout, kSimtN), a.B);
-  k_refresh<T><<<grid, 256, 0, s>>>(
+  launch_pdl(k_refresh<T>, grid, 256, 0, s, 
       static_cast<const T*>(a.H), a.pos, a.npos, static_cast<const T*>(a.Wk),
       static_cast<const T*>(a.Wv), a.N, a.d, nout, static_cast<T*>(a.Kc),
       static_cast<T*>(a.Vc), a.Ncache, a.cache_off);
@@ -346,7 +350,7 @@ cudaError_t refresh_typed(const RefreshArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t topk_run(const TopkArgs& a, cudaStream_t s) {
-  k_topk<<<a.B, 1024, 0, s>>>(a.D, a.assign, a.counts, a.N, a.C, a.k, a.sel,
+  launch_pdl(k_topk, a.B, 1024, 0, s, a.D, a.assign, a.counts, a.N, a.C, a.k, a.sel,
                               a.sel_score, a.pos, a.npos, a.posmask);
   return cudaGetLastError();
 }
