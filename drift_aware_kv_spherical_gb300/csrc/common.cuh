@@ -59,11 +59,14 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// Programmatic dependent launch.  Every library kernel is launched with
-// launch_pdl, so the next grid on the stream may be scheduled while this one
-// drains; each kernel starts with pdl_prologue(), which waits until the grid
-// before it has finished and its writes are visible (griddepcontrol.wait),
-// then lets the following grid be scheduled.
+// Kernel launches.  launch_pdl launches through cudaLaunchKernelEx; with
+// kUsePdl it asks for programmatic dependent launch (the next grid may be
+// scheduled while this one drains).  Every kernel starts with pdl_prologue(),
+// which waits for the previous grid's writes when such a dependency exists
+// (griddepcontrol.wait; a no-op otherwise) and releases the next grid.
+// Measured in the bench's CUDA-graph replay on GB300, programmatic launch
+// made the step slower (0.51 vs 0.43 ms), so it is off.
+constexpr bool kUsePdl = false;
 __device__ __forceinline__ void pdl_prologue() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -79,7 +82,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = kUsePdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
