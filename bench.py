@@ -107,6 +107,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def world_max(x, dev):
+    """Max of a per-rank number over all ranks (the identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_steps_per_s(world, steps, max_total_ms):
+    """Whole-job throughput: every rank ran `steps` steps; the slowest rank's
+    time counts."""
+    return world * steps / (max_total_ms / 1000.0)
+
+
 def graph_kernel_count(g):
     """Kernel nodes in a captured step (cudaGraphGetNodes through the CUDA
     runtime that torch loaded); None if the runtime cannot be reached."""
@@ -385,13 +402,9 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     ps.ps_check()
-    total_ms = sum(a.elapsed_time(b) for a, b in gev)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = world_max(sum(a.elapsed_time(b) for a, b in gev), dev)
     ms_step = total_ms / args.steps
-    steps_per_s = world * args.steps / (total_ms / 1000.0)
+    steps_per_s = aggregate_steps_per_s(world, args.steps, total_ms)
 
     # per-op breakdown: the same steps eagerly, events between the calls; a
     # device-side spin before each step lets the host enqueue the whole step
@@ -438,11 +451,7 @@ def main():
             e2e_ev[t - args.warmup][1].record(stream)
         step_no += 1
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = world_max(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
     h2d = sum(x.numel() * x.element_size() for x in (hH[0], hQ[0], hL[0]))
     d2h = sum(x.numel() * x.element_size() for x in out)
 
@@ -473,7 +482,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic", "config": workload_config(w),
         "window_tokens_per_s": steps_per_s * w.B * w.N,
-        "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "steps/s",
+        "e2e": {"value": aggregate_steps_per_s(world, args.steps, e2e_ms), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
                      "unit": r["unit"], "frac": r["frac"], "traffic": traffic,

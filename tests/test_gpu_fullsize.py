@@ -32,9 +32,7 @@ def _one_layer(widx, B=None):
 def _run_step(w, L, Q, B, first_u, steps=2):
     """Build the window (k-means++), then `steps - 1` warm-started steps on
     drifted hidden states; returns the pipeline and the per-step inputs."""
-    pipe = Pipeline(w, layers=1)
-    if B != w.B:
-        pipe = Pipeline(_with_batch(w, B), layers=1)
+    pipe = Pipeline(w if B == w.B else _with_batch(w, B), layers=1)
     Hs, Qs = [L["H"]], [Q]
     for t in range(1, steps):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
