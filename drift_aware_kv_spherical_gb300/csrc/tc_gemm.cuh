@@ -21,6 +21,8 @@
 // returns.
 #pragma once
 
+#include <cstdlib>
+
 #include "tc.cuh"
 
 namespace ps {
@@ -38,6 +40,9 @@ struct TcShape {
   int* status;
   int split_max_rows;  // K is split over blockIdx.z only while M <= this;
                        // above it blockIdx.z == 0 takes the whole K range
+  int starve_loads;    // test hook: the producer issues no copies, so the
+                       // MMA thread's bounded wait must give up (set only
+                       // when PS_TEST_STARVE_TMA is in the environment)
 };
 
 template <int BN, int NA, int NB, bool B_MN>
@@ -126,7 +131,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   const int kb1 = ksplit ? min(sh.KB, kb0 + sh.kpc) : sh.KB;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !sh.starve_loads) {
       int it = 0;
       bool ok = true;
       for (int t = t_begin; ok && t < t_end; t += t_step) {
@@ -269,7 +274,9 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  launch_pdl(kern, grid, 192, Cfg::kSmem, s, maps, sh, epi);
+  TcShape shape = sh;
+  shape.starve_loads = std::getenv("PS_TEST_STARVE_TMA") != nullptr ? 1 : 0;
+  launch_pdl(kern, grid, 192, Cfg::kSmem, s, maps, shape, epi);
   return cudaGetLastError();
 }
 
