@@ -109,7 +109,9 @@ k_commit_rule(int P, int nchunk, const float* __restrict__ pm,
     for (int q = 0; q < nchunk; ++q) {
       const float mq = pm[row * nchunk + q];
       if (mq == M && tok == INT_MAX) tok = pidx[row * nchunk + q];
-      s += ps[row * nchunk + q] * exp((double)mq - (double)M);
+      // chunk rescale in fp32 (mq <= M; expf is within 2 ulp) -- fp64 exp is
+      // a long software sequence here
+      s += ps[row * nchunk + q] * (double)expf(mq - M);
     }
     c = 1.0 / s;
   }

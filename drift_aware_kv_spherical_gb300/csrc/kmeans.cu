@@ -558,7 +558,7 @@ KmPlan km_plan(int dtype, int B, int N, int d, int C) {
     p.mtb = ceil_div(N, 128);
     p.KB = ceil_div(d, 64);
     const int tiles = B * p.mtb;
-    int nz = std::min(4, std::max(1, ceil_div(kSmTarget, tiles)));
+    int nz = std::min(8, std::max(1, ceil_div(kSmTarget, tiles)));
     nz = std::min(nz, p.KB);
     p.kpc = ceil_div(p.KB, nz);
     p.nz = ceil_div(p.KB, p.kpc);

@@ -321,32 +321,59 @@ struct ProxyEpi : TcEpiBase {
 #pragma unroll
       for (int c = 0; c < BN; ++c) st.A[c] = 0.f;
     }
+    // softmax with one reciprocal; __expf's error (a few ulp for arguments
+    // <= 0) is far inside the 1e-4 tolerance.  BN <= 64: the scores stay in
+    // registers; BN = 128: TMEM is read again instead (registers would spill)
+    if constexpr (BN > 64) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < C) m = fmaxf(m, v[j] * scale);
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < C) sum += __expf(v[j] * scale - m);
+      }
+      const float rs = 1.0f / sum;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < C) st.A[c0 + j] = fmaf(__expf(v[j] * scale - m), rs, st.A[c0 + j]);
+      }
+      return;
+    }
+    float e[BN];
     float m = -INFINITY;
 #pragma unroll
     for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tc::tmem_ld32(taddr + c0, v);
+      tc::tmem_ld32(taddr + c0, e + c0);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < C) m = fmaxf(m, v[j] * scale);
+      for (int j = 0; j < 32; ++j) {
+        e[c0 + j] = (c0 + j < C) ? e[c0 + j] * scale : -INFINITY;
+        m = fmaxf(m, e[c0 + j]);
+      }
     }
     float sum = 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tc::tmem_ld32(taddr + c0, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < C) sum += expf(v[j] * scale - m);
+    for (int c = 0; c < BN; ++c) {
+      e[c] = (c < C) ? __expf(e[c] - m) : 0.f;
+      sum += e[c];
     }
+    const float rs = 1.0f / sum;
 #pragma unroll
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tc::tmem_ld32(taddr + c0, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < C) st.A[c0 + j] += expf(v[j] * scale - m) / sum;
-    }
+    for (int c = 0; c < BN; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
   }
   __device__ void finish(int b, int i, const float* Aacc) const {
     const float hq = (float)Hq;
