@@ -16,9 +16,11 @@
 //                   k_km_argmax (a warp per row) sums the partials in split
 //                   order and takes the arg-max.  fp32 windows: k_assign on
 //                   CUDA cores.
-//   k_cluster_scan  per (cluster, window): members in ascending row order,
-//                   centroid = normalise(sum of unit rows) (+ bf16 split), or
-//                   on the last pass C_hat = mean(rho) * mu; counts; objective
+//   k_cluster_scan  per (cluster, window, column slice), the slices of one
+//                   cluster forming a thread-block cluster: members in
+//                   ascending row order, centroid = normalise(sum of unit
+//                   rows) (+ bf16 split), or on the last pass C_hat =
+//                   mean(rho) * mu; counts; objective
 #include <algorithm>
 #include <climits>
 
@@ -391,24 +393,45 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
   }
 }
 
-// Per (cluster c, window b): members in ascending row order.  Each thread
-// owns V consecutive columns (V = 16 bytes of H) times up to kColGroups
-// groups, so a member row costs one 16-byte load per thread, and up to
-// kMemb member rows are loaded together.  Rows are scanned in blocks of 4096:
-// every thread counts the members in its contiguous run of rows, one block
-// scan places them, and the list (row, 1/||h||) sits in shared memory.
+// Per (cluster c, window b, column slice z): members in ascending row order.
+// The d columns are cut into S slices of W columns (a multiple of 16); the S
+// CTAs of one (c, b) form a thread-block cluster along z.  Each thread owns
+// V consecutive columns (V = 16 bytes of H) of its slice, times up to
+// kColGroups groups, so a member row costs one 16-byte load per thread, and
+// up to kMemb member rows are loaded together.  Rows are scanned in blocks
+// of 4096: every thread counts the members in its contiguous run of rows, one
+// block scan places them, and the list (row, 1/||h||) sits in shared memory.
 // Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
-// is empty or its sum is zero), plus its bf16 split.  Final pass:
-// C_hat_c = mean(rho over members) * mu_c (kept when empty).  Both write the
-// cluster size; CTA (0, b) folds the pass objective from the tile partials.
+// is empty or its sum is zero), plus its bf16 split; the squared norm is the
+// sum of the slices' partials, read from each CTA's shared memory across the
+// cluster in rank order, so every slice divides by the same number.  Final
+// pass: C_hat_c = mean(rho over members) * mu_c (kept when empty).  Slice 0
+// writes the cluster size; CTA (0, b, 0) folds the pass objective from the
+// tile partials.
 constexpr int kScanRows = 4096;
 constexpr int kColGroups = 2;
+constexpr int kMaxSlices = 8;
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Reads a float at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, int rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 template <typename T, bool FINAL>
 __global__ void __launch_bounds__(1024)
 k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
-               int d, int C, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
+               int d, int C, int W, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
                __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
                float* __restrict__ chat, const float* __restrict__ objp, int ntile,
                float* __restrict__ obj, int obj_ld, int pass) {
@@ -419,7 +442,10 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   __shared__ float list_inv[kScanRows];
   __shared__ int s_scan[32];
   __shared__ float s_red[32];
-  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
+  __shared__ float s_ss;
+  const int c = blockIdx.x, b = blockIdx.y, z = blockIdx.z, S = gridDim.z;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int col0 = z * W, col1 = min(d, col0 + W);
   float u[kColGroups][V];
 #pragma unroll
   for (int g = 0; g < kColGroups; ++g)
@@ -454,8 +480,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     if constexpr (FINAL) {
       for (int m = tid; m < tot; m += nthr) rs += rho[(long)b * N + list[m]];
     } else {
-      int m = 0;
-      for (; m < tot; m += kMemb) {
+      for (int m = 0; m < tot; m += kMemb) {
         const int cnt_m = min(kMemb, tot - m);
         uint4 raw[kMemb][kColGroups];
 #pragma unroll
@@ -463,8 +488,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
           const T* h = H + ((long)b * N + list[m + (q < cnt_m ? q : 0)]) * d;
 #pragma unroll
           for (int g = 0; g < kColGroups; ++g) {
-            const int col = (g * nthr + tid) * V;
-            raw[q][g] = (q < cnt_m && col < d)
+            const int col = col0 + (g * nthr + tid) * V;
+            raw[q][g] = (q < cnt_m && col < col1)
                             ? __ldg(reinterpret_cast<const uint4*>(h + col))
                             : make_uint4(0u, 0u, 0u, 0u);
           }
@@ -485,20 +510,20 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     n += tot;
     __syncthreads();
   }
-  if (c == 0 && obj != nullptr) {  // block-uniform: CTA (0, b) folds the pass objective
+  if (c == 0 && z == 0 && obj != nullptr) {  // block-uniform: folds the pass objective
     float so = 0.f;
     for (int t = tid; t < ntile; t += nthr) so += objp[(long)b * ntile + t];
     so = block_sum_f32(so, s_red);
     if (tid == 0) obj[(long)b * obj_ld + pass] = so;
   }
-  if (tid == 0) counts[(long)b * C + c] = n;
+  if (z == 0 && tid == 0) counts[(long)b * C + c] = n;
   if constexpr (FINAL) {
     const float tot = block_sum_f32(rs, s_red);
     if (n == 0) return;
     const float mean = tot / (float)n;
     const float* mc = mu + ((long)b * C + c) * d;
     float* o = chat + ((long)b * C + c) * d;
-    for (int k = tid; k < d; k += nthr) o[k] = mean * mc[k];
+    for (int k = col0 + tid; k < col1; k += nthr) o[k] = mean * mc[k];
   } else {
     float ss = 0.f;
 #pragma unroll
@@ -506,13 +531,25 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
 #pragma unroll
       for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
     ss = block_sum_f32(ss, s_red);
+    if (S > 1) {  // every CTA of the cluster reaches both barriers
+      if (tid == 0) s_ss = ss;
+      cluster_barrier();
+      if (tid == 0) {
+        float t = 0.f;
+        for (int r = 0; r < S; ++r) t += ld_cluster_f32(&s_ss, r);
+        s_red[0] = t;
+      }
+      cluster_barrier();  // no CTA leaves while another still reads its s_ss
+      __syncthreads();
+      ss = s_red[0];
+    }
     const float nu = sqrtf(ss);
     if (n == 0 || !(nu > 0.f)) return;
     const long ro = ((long)b * C + c) * d;
 #pragma unroll
     for (int g = 0; g < kColGroups; ++g) {
-      const int col = (g * nthr + tid) * V;
-      if (col < d) {
+      const int col = col0 + (g * nthr + tid) * V;
+      if (col < col1) {
 #pragma unroll
         for (int e = 0; e < V; ++e) {
           const float x = u[g][e] / nu;
@@ -528,14 +565,42 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   }
 }
 
-// Threads of the cluster-scan CTAs: enough for one 16-byte vector per thread
-// across d (kColGroups of them when d needs more than 1024 threads).
+// Column slices of the cluster scan: enough (<= 8, a power of two) that the
+// C x B x S CTAs fill the SMs, while a slice keeps >= 2 warps of 16-byte
+// vectors.  W = slice width, a multiple of 16 columns.
+struct ScanPlan {
+  int S, W, threads;
+};
+
 template <typename T>
-int scan_threads(int d) {
-  const int vecs = ceil_div(d, Vec<T>::n);
+ScanPlan scan_plan(int B, int d, int C) {
+  constexpr int V = Vec<T>::n;
+  ScanPlan p{1, d, 0};
+  while (p.S < kMaxSlices && (long)C * B * p.S < kSmTarget && d / (2 * p.S) >= 64 * V) p.S *= 2;
+  p.W = ceil_div(ceil_div(d, p.S), 16) * 16;
+  const int vecs = ceil_div(p.W, V);
   const int want = vecs <= 1024 ? vecs : ceil_div(vecs, kColGroups);
   // >= 64 threads keeps each thread's run of rows within a 64-bit mask
-  return std::max(64, std::min(1024, ceil_div(want, 32) * 32));
+  p.threads = std::max(64, std::min(1024, ceil_div(want, 32) * 32));
+  return p;
+}
+
+template <typename T, bool FINAL, typename... Args>
+cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, B, p.S);
+  cfg.blockDim = dim3(p.threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kUsePdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = p.S;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL>, std::forward<Args>(args)...);
 }
 
 struct KmPlan {
@@ -624,6 +689,7 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const long BN_ = (long)a.B * a.N;
   const KmPlan p = km_plan(a.dtype, a.B, a.N, a.d, a.C);
   const KmWs w = km_carve(a.ws, p, a.B, a.N, a.d, a.C, nullptr);
+  const ScanPlan sp = scan_plan<T>(a.B, a.d, a.C);
 
   launch_pdl(k_inv_norm<T>, ceil_div(BN_ * 32, 256), 256, 0, s, H, BN_, a.d, w.inv);
   if (a.init_mode == 1) {
@@ -655,14 +721,15 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     if (e != cudaSuccess) return e;
     if (t < a.iters)
-      launch_pdl(k_cluster_scan<T, false>, dim3(a.C, a.B), scan_threads<T>(a.d), 0, s, 
-          H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, p.tc ? w.mu_hi : nullptr,
-          w.mu_lo, a.counts, a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
+      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
+                                sp.W, a.mu, p.tc ? w.mu_hi : nullptr, w.mu_lo, a.counts,
+                                a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
+    if (e != cudaSuccess) return e;
   }
-  launch_pdl(k_cluster_scan<T, true>, dim3(a.C, a.B), scan_threads<T>(a.d), 0, s, 
-      H, w.inv, a.assign, a.rho, a.N, a.d, a.C, a.mu, nullptr, nullptr, a.counts, a.chat,
-      w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
-  return cudaGetLastError();
+  cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
+                                       a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
+                                       w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -14,12 +14,34 @@
 namespace ps {
 namespace {
 
-constexpr int kStage = 2048;
+// Splits a non-negative finite fp32 x into x = m * 2^e (m < 2^24 an integer,
+// e >= -149); returns false for a negative, infinite or NaN x.
+__device__ __forceinline__ bool f32_mant_exp(float x, uint32_t* m, int* e) {
+  const uint32_t u = __float_as_uint(x) & 0x7fffffffu;  // -0.0 reads as +0.0
+  if (x < 0.f || u >= 0x7f800000u) return false;
+  const uint32_t ef = u >> 23;
+  *m = ef ? ((u & 0x7fffffu) | 0x800000u) : u;
+  *e = ef ? (int)ef - 150 : -149;
+  return true;
+}
 
-// One CTA of 1024 threads per window.  Thread c owns cluster c: its drift
-// sum runs in fp64 over members in ascending position order; its rank is the
-// number of clusters that beat it (higher mean, or equal mean and lower
-// index).  Positions are compacted with a block scan, ascending.
+// One CTA of 1024 threads per window; C <= 1024.  Thread c owns cluster c.
+//
+// Drift sum of a cluster: fp64, one member at a time in ascending position
+// order.  This sequence is reproduced exactly without per-member fp64 work
+// (fp64 issues at a small fraction of the fp32 rate on this part): every
+// member value is m * 2^e with m < 2^24, so every partial sum is an integer
+// multiple of 2^emin (emin = the smallest member exponent).  When the exact
+// integer total S = sum of m << (e - emin) stays below 2^53, every partial
+// sum has a 53-bit significand and no fp64 addition rounds, so the
+// sequential fp64 sum equals S * 2^emin.  S is order-free, so the members are
+// folded with shared-memory integer atomics.  A cluster outside that range
+// (a term or the total at or above 2^53, a negative or non-finite value)
+// takes the sequential fp64 loop itself, one warp per such cluster.
+//
+// Rank of a cluster = the number of clusters that beat it (higher mean, or
+// equal mean and lower index).  Positions are compacted with a block scan,
+// ascending.
 __global__ void __launch_bounds__(1024)
 k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
        const int32_t* __restrict__ counts, int N, int C, int k,
@@ -27,40 +49,74 @@ k_topk(const float* __restrict__ D, const int32_t* __restrict__ assign,
        int32_t* __restrict__ pos, int32_t* __restrict__ npos,
        uint8_t* __restrict__ posmask) {
   pdl_prologue();
-  __shared__ int s_a[kStage];
-  __shared__ float s_d[kStage];
-  __shared__ unsigned long long s_key[1024];
-  __shared__ int s_live[1024];
+  __shared__ unsigned long long s_key[1024];  // integer sum, then rank key
+  __shared__ int s_emin[1024];
+  __shared__ int s_live[1024];  // fallback flag, then liveness
   __shared__ int s_sel[1024];
   __shared__ int s_scan[32];
   __shared__ double s_sum[1024];
+  __shared__ int s_nfall;
+  __shared__ int s_fall[1024];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* a = assign + (long)b * N;
   const float* Db = D + (long)b * N;
-  for (int c = tid; c < C; c += blockDim.x) s_sum[c] = 0.0;
-  // warp w owns clusters w, w+32, ...: a ballot over 32 rows at a time finds
-  // the members, which lane 0 adds in ascending row order (fp64)
-  for (int base = 0; base < N; base += kStage) {
-    const int lim = min(kStage, N - base);
-    __syncthreads();
-    for (int e = tid; e < lim; e += blockDim.x) {
-      s_a[e] = a[base + e];
-      s_d[e] = Db[base + e];
+  s_key[tid] = 0ull;
+  s_emin[tid] = INT_MAX;
+  s_live[tid] = 0;
+  if (tid == 0) s_nfall = 0;
+  __syncthreads();
+  for (int i = tid; i < N; i += blockDim.x) {  // smallest exponent per cluster
+    const int c = a[i];
+    uint32_t m;
+    int e;
+    if (c < 0 || c >= C) continue;
+    if (!f32_mant_exp(Db[i], &m, &e)) s_live[c] = 1;
+    else if (m != 0u) atomicMin(&s_emin[c], e);
+  }
+  __syncthreads();
+  for (int i = tid; i < N; i += blockDim.x) {  // exact integer totals
+    const int c = a[i];
+    uint32_t m;
+    int e;
+    if (c < 0 || c >= C || !f32_mant_exp(Db[i], &m, &e) || m == 0u) continue;
+    const int sh = e - s_emin[c];
+    if (sh > 29) {  // m << sh could reach 2^53
+      s_live[c] = 1;
+      continue;
     }
-    __syncthreads();
-    for (int c = warp; c < C; c += 32) {
-      double sum = s_sum[c];
-      for (int e0 = 0; e0 < lim; e0 += 32) {
-        const int e = e0 + lane;
-        unsigned hit = __ballot_sync(0xffffffffu, e < lim && s_a[e] == c);
-        while (hit) {
-          const int j = __ffs(hit) - 1;
-          hit &= hit - 1;
-          sum += (double)s_d[e0 + j];
-        }
+    const unsigned long long t = (unsigned long long)m << sh;
+    const unsigned long long old = atomicAdd(&s_key[c], t);
+    if (old + t < old) s_live[c] = 1;  // wrapped: the total is far above 2^53
+  }
+  __syncthreads();
+  if (tid < C) {
+    const unsigned long long S = s_key[tid];
+    if (s_live[tid] || S >= (1ull << 53)) {
+      s_fall[atomicAdd(&s_nfall, 1)] = tid;
+    } else {
+      // S * 2^emin, exact: S < 2^53 converts exactly and 2^emin (emin >=
+      // -149) is a normal fp64 power of two, built from its exponent bits
+      s_sum[tid] = S == 0ull ? 0.0
+                             : (double)S * __longlong_as_double(
+                                               (long long)(s_emin[tid] + 1023) << 52);
+    }
+  }
+  __syncthreads();
+  for (int f = warp; f < s_nfall; f += 32) {  // the sequential fp64 sum itself
+    const int c = s_fall[f];
+    double sum = 0.0;
+    for (int e0 = 0; e0 < N; e0 += 32) {
+      const int e = e0 + lane;
+      const bool mine = e < N && a[e] == c;
+      const float dv = mine ? Db[e] : 0.f;
+      unsigned hit = __ballot_sync(0xffffffffu, mine);
+      while (hit) {
+        const int j = __ffs(hit) - 1;
+        hit &= hit - 1;
+        sum += (double)__shfl_sync(0xffffffffu, dv, j);
       }
-      if (lane == 0) s_sum[c] = sum;
     }
+    if (lane == 0) s_sum[c] = sum;
   }
   __syncthreads();
   const int n = tid < C ? counts[(long)b * C + tid] : 0;

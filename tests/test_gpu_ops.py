@@ -129,16 +129,23 @@ def test_kmeans_ragged_and_degenerate():
     assert_close(g1["mu"][0], o1["mu"], what="C=1")
 
 
-@pytest.mark.parametrize("B,N,d,C,iters", [(3, 177, 80, 24, 3), (2, 300, 256, 128, 2),
-                                            (1, 129, 64, 64, 1)])
-def test_kmeans_bf16_ragged(B, N, d, C, iters):
+@pytest.mark.parametrize("B,N,d,C,iters,dt", [(3, 177, 80, 24, 3, "bf16"),
+                                               (2, 300, 256, 128, 2, "bf16"),
+                                               (1, 129, 64, 64, 1, "bf16"),
+                                               (1, 301, 1552, 20, 2, "bf16"),
+                                               (1, 200, 1040, 5, 2, "f32")])
+def test_kmeans_ragged_tiles(B, N, d, C, iters, dt):
     """bf16 windows on the tensor-core path: row tiles straddling windows,
-    C not a power of two, a partial 64-wide K block, iters >= 1."""
+    C not a power of two, a partial 64-wide K block, iters >= 1.  The last
+    two cases give few (cluster, window) pairs, so the centroid update splits
+    d into 2 (bf16) and 4 (f32) column slices, the last one shorter."""
     rng = np.random.default_rng(N + C)
     planted = oracle.normalize_rows(rng.standard_normal((C, d)))
     z = rng.integers(0, C, (B, N))
     H = (planted[z] * 4 + rng.normal(0, 0.3, (B, N, d))).astype(np.float32)
-    Ht = torch.from_numpy(H).cuda().to(torch.bfloat16)
+    Ht = torch.from_numpy(H).cuda()
+    if dt == "bf16":
+        Ht = Ht.to(torch.bfloat16)
     Hn = np_(Ht)
     mu0 = np.stack([oracle.normalize_rows(Hn[b][:C]) for b in range(B)]).astype(np.float32)
     g = run_kmeans(Ht, torch.from_numpy(mu0).cuda(), iters)
@@ -340,9 +347,14 @@ def _oracle_topk(Dn, an, cn, k):
     return [oracle.topk_drift(Dn[b], an[b], cn[b], k) for b in range(Dn.shape[0])]
 
 
-@pytest.mark.parametrize("case", ["random", "zeros", "k_eq_c", "empty_clusters"])
+@pytest.mark.parametrize("case", ["random", "zeros", "k_eq_c", "empty_clusters",
+                                  "wide_range", "big_total", "ties", "denormal"])
 def test_topk_drift(case):
-    rng = np.random.default_rng(hash(case) % 1000)
+    """The kernel forms most cluster sums as exact integer totals and runs the
+    sequential fp64 sum only where that could differ; the last four cases put
+    clusters on both sides of that line (members 2^-60 apart, a total of
+    2^53 units of the smallest member, equal means, subnormal drifts)."""
+    rng = np.random.default_rng(sum(map(ord, case)))
     B, N, C, k = 3, 1000, 64, 8
     a = rng.integers(0, C, (B, N)).astype(np.int32)
     if case == "empty_clusters":
@@ -352,6 +364,19 @@ def test_topk_drift(case):
         D[:] = 0
     if case == "k_eq_c":
         k = C
+    if case == "wide_range":                       # every 7th row tiny
+        D[:, ::7] = (D[:, ::7] * 2.0 ** -60).astype(np.float32)
+    if case == "big_total":                        # 1.0 and 2^-29 in one cluster
+        for b in range(B):
+            rows = np.nonzero(a[b] == 5)[0]
+            D[b, rows] = 1.0
+            D[b, rows[0]] = np.float32(2.0 ** -29)
+    if case == "ties":                             # equal means in many clusters
+        D = (np.round(D * 1e3) / 1e3).astype(np.float32)
+        D[:, :] = np.float32(0.25) * (a % 3 == 0) + D * (a % 3 != 0)
+    if case == "denormal":
+        D = (D * np.float32(1e-36)).astype(np.float32)
+        D[:, ::3] = np.float32(1e-45) * rng.integers(0, 50, (B, (N + 2) // 3))
     counts = np.stack([np.bincount(a[b], minlength=C) for b in range(B)]).astype(np.int32)
     sel, sc, pos, npos, mask, _, _ = run_topk(torch.from_numpy(D).cuda(),
                                               torch.from_numpy(a).cuda(),
