@@ -12,10 +12,12 @@
 //   k_split_mu      mu -> (mu_hi, mu_lo) bf16 for the tensor cores
 //   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
 //                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
-//                   d when the windows give too few row tiles; then
-//                   k_km_argmax (a warp per row) sums the partials in split
-//                   order and takes the arg-max.  fp32 windows: k_assign on
-//                   CUDA cores.
+//                   d when the windows give too few row tiles.  The d-chunks
+//                   of a tile form a thread-block cluster (C <= 128) and sum
+//                   their scores in chunk order through distributed shared
+//                   memory, a warp per row taking the arg-max; for C > 128
+//                   the chunks go through global memory to k_km_argmax.
+//                   fp32 windows: k_assign on CUDA cores.
 //   k_cluster_scan  per (cluster, window, column slice), the slices of one
 //                   cluster forming a thread-block cluster: members in
 //                   ascending row order, centroid = normalise(sum of unit
@@ -34,7 +36,6 @@ namespace {
 constexpr int kTileRows = 64;    // rows per assignment tile
 constexpr int kTileC = 128;      // centroids per chunk of an assignment tile
 constexpr int kTileK = 32;       // d per shared-memory stage
-constexpr int kMaxD = 8192;
 
 template <typename T>
 __global__ void k_inv_norm(const T* __restrict__ H, long rows, int d,
@@ -348,6 +349,86 @@ struct KmAssignEpi : TcEpiBase {
   }
 };
 
+// Split assignment inside one thread-block cluster (nz <= 8 d-chunks, C <=
+// 128): each CTA leaves its chunk's 128 x C scores in shared memory; CTA z
+// then takes rows [128 z / nz, 128 (z+1) / nz) of the tile, one warp per row:
+// sums the nz chunks' scores of each centroid in chunk order, takes the first
+// arg-max and the cosine, and stores the objective partial of its rows as
+// objp[t * nz + z].
+template <int BN>
+struct KmAssignClusterEpi : TcEpiBase {
+  static constexpr bool kClusterReduce = true;
+  static constexpr uint32_t kLd = BN + 4;
+  int B, N, C, mtb;
+  const float* inv;
+  int32_t* assign;
+  float* best;
+  float* objp;
+  struct State {};
+  __device__ int tiles(int) const { return B * mtb; }
+  __device__ int arow(int t) const { return (t / mtb) * N + (t % mtb) * 128; }
+  __device__ int bcoord(int t, int n0) const { return (t / mtb) * C + n0; }
+  __device__ void consume_red(int, int, int, int, uint32_t taddr, State&,
+                              float* red_row) const {
+    if (red_row == nullptr) return;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(red_row + c0 + 4 * j) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+  __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
+    const int t = blockIdx.y, b = t / mtb, mt = t % mtb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    float* cosv = reinterpret_cast<float*>(scratch);  // [128]
+    uint32_t base[8];
+    const uint32_t local = tc::smem_u32(red);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
+    for (int r = r0 + warp; r < r1; r += nwarps) {
+      const int i = mt * 128 + r;
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      for (int c = lane; c < C; c += 32) {
+        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nz) sum += tc::ld_dsmem_f32(base[q] + off);
+        if (sum > bv) { bv = sum; bi = c; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (bi == INT_MAX) { bi = 0; bv = 0.f; }
+      if (lane == 0) {
+        float cs = 0.f;
+        if (i < N) {
+          const long row = (long)b * N + i;
+          assign[row] = bi;
+          best[row] = bv;
+          cs = bv * inv[row];
+        }
+        cosv[r - r0] = cs;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float so = 0.f;
+      for (int j = 0; j < r1 - r0; ++j) so += cosv[j];
+      objp[(long)t * nz + z] = so;
+    }
+  }
+};
+
 // Rows of a split assignment: one warp per row sums the nz partial scores of
 // each centroid in chunk order, takes the first arg-max and the cosine;
 // block (x, b) covers rows 8x..8x+7 of window b and stores their objective
@@ -396,11 +477,13 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
 // Per (cluster c, window b, column slice z): members in ascending row order.
 // The d columns are cut into S slices of W columns (a multiple of 16); the S
 // CTAs of one (c, b) form a thread-block cluster along z.  Each thread owns
-// V consecutive columns (V = 16 bytes of H) of its slice, times up to
-// kColGroups groups, so a member row costs one 16-byte load per thread, and
-// up to kMemb member rows are loaded together.  Rows are scanned in blocks
-// of 4096: every thread counts the members in its contiguous run of rows, one
-// block scan places them, and the list (row, 1/||h||) sits in shared memory.
+// V consecutive columns (V = 16 bytes of H) of its slice, times G (1 or 2)
+// groups, so a member row costs one 16-byte load per thread, and up to
+// 16 / G member rows are loaded together.  Rows are scanned in blocks of
+// 4096: the block's assignments are staged in shared memory with 16-byte
+// loads, every thread counts the members in its contiguous run of rows, one
+// block scan places them, and the list (row, 1/||h||) sits in shared memory
+// (over the staged assignments, which are all read before the scan).
 // Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
 // is empty or its sum is zero), plus its bf16 split; the squared norm is the
 // sum of the slices' partials, read from each CTA's shared memory across the
@@ -409,25 +492,10 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
 // writes the cluster size; CTA (0, b, 0) folds the pass objective from the
 // tile partials.
 constexpr int kScanRows = 4096;
-constexpr int kColGroups = 2;
+constexpr int kMaxColGroups = 2;
 constexpr int kMaxSlices = 8;
 
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Reads a float at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster_f32(const float* local, int rank) {
-  uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
-template <typename T, bool FINAL>
+template <typename T, bool FINAL, int G>
 __global__ void __launch_bounds__(1024)
 k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
@@ -437,8 +505,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                float* __restrict__ obj, int obj_ld, int pass) {
   pdl_prologue();
   constexpr int V = Vec<T>::n;
-  constexpr int kMemb = 8;
-  __shared__ int list[kScanRows];
+  constexpr int kMemb = 16 / G;
+  __shared__ __align__(16) int list[kScanRows];  // staged assignments, then members
   __shared__ float list_inv[kScanRows];
   __shared__ int s_scan[32];
   __shared__ float s_red[32];
@@ -446,26 +514,36 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   const int c = blockIdx.x, b = blockIdx.y, z = blockIdx.z, S = gridDim.z;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int col0 = z * W, col1 = min(d, col0 + W);
-  float u[kColGroups][V];
+  float u[G][V];
 #pragma unroll
-  for (int g = 0; g < kColGroups; ++g)
+  for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int e = 0; e < V; ++e) u[g][e] = 0.f;
   float rs = 0.f;
   int n = 0;
   for (int base = 0; base < N; base += kScanRows) {
     const int len = min(kScanRows, N - base);
+    const int32_t* ab = assign + (long)b * N + base;
+    if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
+      const int n4 = len >> 2;
+      for (int j = tid; j < n4; j += nthr)
+        reinterpret_cast<int4*>(list)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
+      for (int j = (n4 << 2) + tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+    } else {
+      for (int j = tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+    }
+    __syncthreads();
     const int R = (len + nthr - 1) / nthr;  // <= 64
-    const int r0 = base + tid * R;
+    const int q0 = tid * R;
     unsigned long long hit = 0ull;
     int cnt = 0;
     for (int q = 0; q < R; ++q) {
-      const int i = r0 + q;
-      if (i < base + len && assign[(long)b * N + i] == c) {
+      if (q0 + q < len && list[q0 + q] == c) {
         hit |= 1ull << q;
         ++cnt;
       }
     }
+    const int r0 = base + q0;
     int tot;
     int w = block_exclusive_scan<int>(cnt, s_scan, &tot);
     while (hit) {
@@ -482,12 +560,12 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     } else {
       for (int m = 0; m < tot; m += kMemb) {
         const int cnt_m = min(kMemb, tot - m);
-        uint4 raw[kMemb][kColGroups];
+        uint4 raw[kMemb][G];
 #pragma unroll
         for (int q = 0; q < kMemb; ++q) {
           const T* h = H + ((long)b * N + list[m + (q < cnt_m ? q : 0)]) * d;
 #pragma unroll
-          for (int g = 0; g < kColGroups; ++g) {
+          for (int g = 0; g < G; ++g) {
             const int col = col0 + (g * nthr + tid) * V;
             raw[q][g] = (q < cnt_m && col < col1)
                             ? __ldg(reinterpret_cast<const uint4*>(h + col))
@@ -498,7 +576,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
         for (int q = 0; q < kMemb; ++q) {
           const float sc = q < cnt_m ? list_inv[m + q] : 0.f;
 #pragma unroll
-          for (int g = 0; g < kColGroups; ++g) {
+          for (int g = 0; g < G; ++g) {
             float v[V];
             unpack16(raw[q][g], v, T{});
 #pragma unroll
@@ -527,19 +605,20 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   } else {
     float ss = 0.f;
 #pragma unroll
-    for (int g = 0; g < kColGroups; ++g)
+    for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
     ss = block_sum_f32(ss, s_red);
     if (S > 1) {  // every CTA of the cluster reaches both barriers
       if (tid == 0) s_ss = ss;
-      cluster_barrier();
+      tc::cluster_sync_all();
       if (tid == 0) {
+        const uint32_t a = tc::smem_u32(&s_ss);
         float t = 0.f;
-        for (int r = 0; r < S; ++r) t += ld_cluster_f32(&s_ss, r);
+        for (int r = 0; r < S; ++r) t += tc::ld_dsmem_f32(tc::cluster_map(a, r));
         s_red[0] = t;
       }
-      cluster_barrier();  // no CTA leaves while another still reads its s_ss
+      tc::cluster_sync_all();  // no CTA leaves while another still reads its s_ss
       __syncthreads();
       ss = s_red[0];
     }
@@ -547,7 +626,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     if (n == 0 || !(nu > 0.f)) return;
     const long ro = ((long)b * C + c) * d;
 #pragma unroll
-    for (int g = 0; g < kColGroups; ++g) {
+    for (int g = 0; g < G; ++g) {
       const int col = col0 + (g * nthr + tid) * V;
       if (col < col1) {
 #pragma unroll
@@ -569,17 +648,18 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
 // C x B x S CTAs fill the SMs, while a slice keeps >= 2 warps of 16-byte
 // vectors.  W = slice width, a multiple of 16 columns.
 struct ScanPlan {
-  int S, W, threads;
+  int S, W, threads, G;
 };
 
 template <typename T>
 ScanPlan scan_plan(int B, int d, int C) {
   constexpr int V = Vec<T>::n;
-  ScanPlan p{1, d, 0};
+  ScanPlan p{1, d, 0, 1};
   while (p.S < kMaxSlices && (long)C * B * p.S < kSmTarget && d / (2 * p.S) >= 64 * V) p.S *= 2;
   p.W = ceil_div(ceil_div(d, p.S), 16) * 16;
   const int vecs = ceil_div(p.W, V);
-  const int want = vecs <= 1024 ? vecs : ceil_div(vecs, kColGroups);
+  p.G = vecs <= 1024 ? 1 : kMaxColGroups;
+  const int want = ceil_div(vecs, p.G);
   // >= 64 threads keeps each thread's run of rows within a 64-bit mask
   p.threads = std::max(64, std::min(1024, ceil_div(want, 32) * 32));
   return p;
@@ -600,11 +680,15 @@ cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&.
   attr[1].val.clusterDim.z = p.S;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL>, std::forward<Args>(args)...);
+  return p.G == 1
+             ? cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL, 1>, std::forward<Args>(args)...)
+             : cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL, kMaxColGroups>,
+                                  std::forward<Args>(args)...);
 }
 
 struct KmPlan {
   bool tc;
+  bool cluster;  // d-chunks reduced inside a thread-block cluster
   int BN, mtb, nz, kpc, KB;
   int ntile;  // objective partials per window
 };
@@ -627,7 +711,8 @@ KmPlan km_plan(int dtype, int B, int N, int d, int C) {
     nz = std::min(nz, p.KB);
     p.kpc = ceil_div(p.KB, nz);
     p.nz = ceil_div(p.KB, p.kpc);
-    p.ntile = p.nz > 1 ? ceil_div(N, 8) : p.mtb;
+    p.cluster = p.nz > 1 && p.BN <= 128;
+    p.ntile = p.nz == 1 ? p.mtb : (p.cluster ? p.mtb * p.nz : ceil_div(N, 8));
   } else {
     p.ntile = ceil_div(N, kTileRows);
   }
@@ -655,7 +740,7 @@ KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* b
   if (p.tc) {
     w.mu_hi = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.mu_lo = cv.take<__nv_bfloat16>((size_t)B * C * d);
-    w.part = p.nz > 1 ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
+    w.part = p.nz > 1 && !p.cluster ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
   }
   if (bytes != nullptr) *bytes = cv.bytes();
   return w;
@@ -673,6 +758,12 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaS
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status, INT_MAX};
+  if constexpr (BN <= 128) {
+    if (p.cluster) {
+      KmAssignClusterEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, w.inv, a.assign, a.rho, w.objp};
+      return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
+    }
+  }
   KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.inv, a.assign, a.rho,
                       w.objp};
   cudaError_t e =

@@ -17,8 +17,10 @@
 //                   (k_ckeys_finish sums the chunks); kept as K~_hi, K~_lo
 //   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
 //                   in TMEM, softmax over the C columns in the epilogue,
-//                   head sum in registers; with several head slices per
-//                   tile, k_proxy_final sums them, divides by Hq, takes KL
+//                   head sum in registers; the head slices of a row tile
+//                   (<= 8) form a thread-block cluster that sums them in
+//                   slice order through distributed shared memory, divides
+//                   by Hq and takes KL
 // Every reduction has a fixed order, so identical inputs give identical
 // bits and KL(A || A) is exactly 0.
 #include <algorithm>
@@ -220,8 +222,6 @@ k_proxy_final(const float* __restrict__ part, int nslice, int B, int N, int C,
 
 int nj_for(int C);
 
-cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cudaStream_t s);
-
 // ------------------------------------------------------------ tensor cores
 __global__ void k_split_f32(const float* __restrict__ x, long n, __nv_bfloat16* __restrict__ hi,
                             __nv_bfloat16* __restrict__ lo) {
@@ -410,6 +410,64 @@ struct ProxyEpi : TcEpiBase {
   }
 };
 
+// Head slices of one row tile inside one thread-block cluster: CTA z runs
+// heads [z hps, (z+1) hps) of row tile blockIdx.y and leaves its head sum in
+// shared memory; then CTA z finishes rows [128 z / Z, 128 (z+1) / Z), one
+// warp per row: the slices' sums in slice order, A = sum / Hq, KL.
+template <int BN>
+struct ProxyClusterEpi : ProxyEpi<BN> {
+  static constexpr bool kBlocked = false;
+  static constexpr bool kClusterReduce = true;
+  static constexpr bool kZSplitsK = false;
+  static constexpr uint32_t kLd = BN + 4;
+  using State = typename ProxyEpi<BN>::State;
+  __device__ bool tile_range(int, int* tb, int* te, int* ts) const {
+    *tb = blockIdx.y * this->Hq + blockIdx.z * this->hps;
+    *te = *tb + this->hps;
+    *ts = 1;
+    return true;
+  }
+  __device__ void consume_red(int t, int r, int n0, int z, uint32_t taddr, State& st,
+                              float* red_row) const {
+    this->consume(t, r, n0, z, taddr, st);
+    if (red_row == nullptr) return;
+#pragma unroll
+    for (int c = 0; c < BN; c += 4)
+      *reinterpret_cast<float4*>(red_row + c) =
+          make_float4(st.A[c], st.A[c + 1], st.A[c + 2], st.A[c + 3]);
+  }
+  __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
+    const int bm = blockIdx.y, b = bm / this->mtb, mt = bm % this->mtb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    const int C = this->C, N = this->N;
+    const float hq = (float)this->Hq;
+    uint32_t base[8];
+    const uint32_t local = tc::smem_u32(red);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
+    for (int r = r0 + warp; r < r1; r += nwarps) {
+      const int i = mt * 128 + r;
+      if (i >= N) continue;  // warp-uniform
+      const long row = (long)b * N + i;
+      float kl = 0.f;
+      for (int c = lane; c < C; c += 32) {
+        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nz) sum += tc::ld_dsmem_f32(base[q] + off);
+        const float a = sum / hq;
+        this->A_cur[row * C + c] = a;
+        if (this->A_prev != nullptr && a > 0.f)
+          kl += a * logf(a / fmaxf(this->A_prev[row * C + c], 1e-30f));
+      }
+      kl = warp_sum(kl);
+      if (lane == 0) this->D[row] = this->A_prev != nullptr ? fmaxf(kl, 0.f) : 0.f;
+    }
+  }
+};
+
 struct TcPlan {
   bool ok;
   int BN, mtb, nslice, hps;             // proxy
@@ -423,7 +481,8 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
   if (!p.ok) return p;
   p.BN = C <= 32 ? 32 : (C <= 64 ? 64 : 128);
   p.mtb = ceil_div(N, 128);
-  const int want = std::max(1, ceil_div(kSmTarget, B * p.mtb));
+  // head slices of a row tile share one thread-block cluster: <= 8
+  const int want = std::min(8, std::max(1, ceil_div(kSmTarget, B * p.mtb)));
   p.nslice = 1;
   for (int sl = std::min(want, Hq); sl >= 1; --sl)
     if (Hq % sl == 0) { p.nslice = sl; break; }
@@ -441,7 +500,7 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
 
 struct TcWs {
   __nv_bfloat16 *chi, *clo, *khi, *klo;
-  float *kpart, *apart;
+  float* kpart;
 };
 
 TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, size_t* bytes) {
@@ -452,7 +511,6 @@ TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, 
   w.khi = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
   w.klo = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
   w.kpart = p.ck_nz > 1 ? cv.take<float>((size_t)p.ck_nz * B * C * nkv) : nullptr;
-  w.apart = p.nslice > 1 ? cv.take<float>((size_t)p.nslice * B * N * C) : nullptr;
   if (bytes) *bytes = cv.bytes();
   return w;
 }
@@ -500,11 +558,11 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status, INT_MAX};
   ProxyEpi<BN> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
                    (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D,
-                   w.apart};
-  cudaError_t e = launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi,
-                                                  dim3(1, a.B * p.mtb * p.nslice, 1), s);
-  if (e != cudaSuccess || p.nslice == 1) return e;
-  return launch_final(a, p.nslice, w.apart, s);
+                   nullptr};
+  if (p.nslice == 1)
+    return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, 1), s);
+  ProxyClusterEpi<BN> cepi{epi};
+  return launch_tc_gemm<BN, 1, 2, false>(maps, sh, cepi, dim3(1, a.B * p.mtb, p.nslice), s);
 }
 
 struct Plan {
@@ -536,18 +594,6 @@ int nj_for(int C) {
 
 size_t proxy_smem(int dh, int NJ) {
   return sizeof(float) * ((size_t)kRows * (dh + 1) + (size_t)kKc * (16 * NJ + 1));
-}
-
-cudaError_t launch_final(const ProxyArgs& a, int nslice, const float* part, cudaStream_t s) {
-  const dim3 grid(ceil_div(a.N, kRows), a.B);
-  switch (nj_for(a.C)) {
-    case 1: launch_pdl(k_proxy_final<1>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 2: launch_pdl(k_proxy_final<2>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 4: launch_pdl(k_proxy_final<4>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    case 8: launch_pdl(k_proxy_final<8>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-    default: launch_pdl(k_proxy_final<16>, grid, 256, 0, s, part, nslice, a.B, a.N, a.C, a.Hq, a.A_prev, a.A_cur, a.D); break;
-  }
-  return cudaGetLastError();
 }
 
 template <typename T, int NJ>

@@ -19,6 +19,14 @@
 // Every mbarrier wait is bounded (tc::mbar_wait); on a timeout the CTA sets
 // the status word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
+//
+// Cluster reduction (Epi::kClusterReduce): the gridDim.z CTAs that share a
+// row tile (chunks of K, or slices of another summed dimension) form one
+// thread-block cluster (<= 8 CTAs).  Each CTA leaves its 128 x BN fp32
+// result in its own shared memory (over the stage ring, idle by then); after
+// a cluster barrier, CTA z finishes rows [128 z / Z, 128 (z+1) / Z) reading
+// every rank's rows through distributed shared memory in rank order, so the
+// sum is deterministic and no partial goes through global memory.
 #pragma once
 
 #include <cstdlib>
@@ -52,6 +60,7 @@ struct TcCfg {
   static constexpr uint32_t kStage = NA * kA + NB * kB;
   static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
   static constexpr size_t kSmem = 1024 + kStages * kStage + 1024;
+  static constexpr uint32_t kRedLd = BN + 4;  // row stride (floats) of a cluster result
   static constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN, B_MN);
 };
 
@@ -72,6 +81,16 @@ struct TcCfg {
 //   void tile_done(int t, int r, int n0, int z, uint8_t* scratch, State&)
 //        called by the 128 epilogue threads together after consume; may
 //        synchronise with bar.sync 1, 128; scratch = 512 B of shared memory
+//   static constexpr bool kZSplitsK  blockIdx.z chunks K (else z is the
+//        epilogue's own and every CTA takes the whole K range)
+//   bool tile_range(int T, int* begin, int* end, int* step)  optional
+//        override of the CTA's tile walk (returns true when it applies)
+// and with kClusterReduce (instead of consume / tile_done):
+//   void consume_red(t, r, n0, z, taddr, State&, float* red_row)
+//        red_row = this row's slot in the CTA's result (kRedLd floats), or
+//        nullptr before the CTA's last tile
+//   void reduce(const float* red, int z, int Z, uint8_t* scratch)
+//        called by all 192 threads between two cluster barriers
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __global__ void __launch_bounds__(192, 1)
 k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
@@ -91,9 +110,10 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   uint8_t* epi_scratch = smem + S * Cfg::kStage + 512;
 
   // tiles of this CTA first: a CTA without work leaves before any set-up
+  // (never in a cluster, whose barriers every CTA joins)
   const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
-  const bool ksplit = M <= sh.split_max_rows;
-  const int T = (ksplit || blockIdx.z == 0) ? epi.tiles(M) : 0;
+  const bool ksplit = Epi::kZSplitsK && M <= sh.split_max_rows;
+  const int T = (ksplit || blockIdx.z == 0 || !Epi::kZSplitsK) ? epi.tiles(M) : 0;
   int t_begin = blockIdx.y, t_end = T, t_step = gridDim.y;
   if constexpr (Epi::kBlocked) {
     const int per = (T + gridDim.y - 1) / gridDim.y;
@@ -101,7 +121,8 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     t_end = min(T, t_begin + per);
     t_step = 1;
   }
-  if (t_begin >= t_end) return;
+  epi.tile_range(T, &t_begin, &t_end, &t_step);
+  if (!Epi::kClusterReduce && t_begin >= t_end) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -237,14 +258,28 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       const int buf = tcount & 1;
       if (!tc::mbar_wait(acc_full + buf, (tcount >> 1) & 1, sh.status, abort_flag)) break;
       tc::fence_after_sync();
-      epi.consume(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est);
+      if constexpr (Epi::kClusterReduce) {
+        // the stage ring is idle once the CTA's last accumulator is full
+        float* red_row = t + t_step >= t_end
+                             ? reinterpret_cast<float*>(smem) + r * Cfg::kRedLd
+                             : nullptr;
+        epi.consume_red(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est, red_row);
+      } else {
+        epi.consume(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est);
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(acc_empty + buf);
-      epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
+      if constexpr (!Epi::kClusterReduce) epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
     }
   }
   __syncthreads();
+  if constexpr (Epi::kClusterReduce) {
+    static_assert(128 * Cfg::kRedLd * 4 <= Cfg::kStages * Cfg::kStage, "cluster result > ring");
+    tc::cluster_sync_all();
+    epi.reduce(reinterpret_cast<const float*>(smem), blockIdx.z, gridDim.z, epi_scratch);
+    tc::cluster_sync_all();  // no CTA leaves while another still reads its result
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 2 * BN);
@@ -255,6 +290,9 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
 struct TcEpiBase {
   static constexpr bool kA3D = false;
   static constexpr bool kBlocked = false;
+  static constexpr bool kClusterReduce = false;
+  static constexpr bool kZSplitsK = true;
+  __device__ bool tile_range(int, int*, int*, int*) const { return false; }
   __device__ int ahead(int) const { return 0; }
   __device__ int bkoff(int) const { return 0; }
   __device__ int bsel(int, int) const { return 0; }
@@ -276,6 +314,24 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
   }
   TcShape shape = sh;
   shape.starve_loads = std::getenv("PS_TEST_STARVE_TMA") != nullptr ? 1 : 0;
+  if constexpr (Epi::kClusterReduce) {
+    if (grid.z < 1 || grid.z > 8) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = kUsePdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = grid.z;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, maps, shape, epi);
+  }
   launch_pdl(kern, grid, 192, Cfg::kSmem, s, maps, shape, epi);
   return cudaGetLastError();
 }

@@ -6,6 +6,7 @@ the path's criteria: integer outputs bit-exact, k-means assignments exact
 where the oracle's top-2 margin exceeds 1e-5, fp32 outputs within 1e-4
 relative / 1e-6 absolute, bf16 K/V within 2e-2 relative.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -133,12 +134,15 @@ def test_kmeans_ragged_and_degenerate():
                                                (2, 300, 256, 128, 2, "bf16"),
                                                (1, 129, 64, 64, 1, "bf16"),
                                                (1, 301, 1552, 20, 2, "bf16"),
+                                               (1, 333, 320, 150, 2, "bf16"),
                                                (1, 200, 1040, 5, 2, "f32")])
 def test_kmeans_ragged_tiles(B, N, d, C, iters, dt):
     """bf16 windows on the tensor-core path: row tiles straddling windows,
-    C not a power of two, a partial 64-wide K block, iters >= 1.  The last
-    two cases give few (cluster, window) pairs, so the centroid update splits
-    d into 2 (bf16) and 4 (f32) column slices, the last one shorter."""
+    C not a power of two, a partial 64-wide K block, iters >= 1; d-chunks
+    reduced in a thread-block cluster (2 and 4 chunks) and, for C = 150 > 128,
+    through global memory (5 chunks).  The 1552- and 1040-column cases give few
+    (cluster, window) pairs, so the centroid update splits d into 2 (bf16) and
+    4 (f32) column slices, the last one shorter."""
     rng = np.random.default_rng(N + C)
     planted = oracle.normalize_rows(rng.standard_normal((C, d)))
     z = rng.integers(0, C, (B, N))
@@ -329,6 +333,24 @@ def test_proxy_gqa_and_ragged():
     prev = torch.softmax(torch.randn(2, 177, w.C, device="cuda"), dim=2)
     A, D = run_proxy(Q, chat, L["Wk"], w.Hkv, A_prev=prev)
     oA, oD = _oracle_proxy(w, np_(Q), np_(chat), np_(L["Wk"]), np_(prev))
+    assert_close(np_(A), oA, what="A")
+    assert_close(np_(D), oD, what="D")
+
+
+def test_proxy_one_head_slice_many_windows():
+    """160 windows of 70 rows give 160 row tiles, so every tile keeps all its
+    heads in one CTA (no head-slice cluster); bf16, GQA 4 on 2."""
+    rng = np.random.default_rng(11)
+    B, N, Hq, Hkv, dh, C, d = 160, 70, 4, 2, 64, 40, 128
+    Q = torch.from_numpy(rng.standard_normal((B, N, Hq, dh)).astype(np.float32))
+    Q = Q.to(torch.bfloat16).cuda()
+    chat = torch.from_numpy(rng.standard_normal((B, C, d)).astype(np.float32)).cuda()
+    Wk = torch.from_numpy((rng.standard_normal((d, Hkv * dh)) * 0.1).astype(np.float32))
+    Wk = Wk.to(torch.bfloat16).cuda()
+    prev = torch.softmax(torch.randn(B, N, C, device="cuda"), dim=2)
+    A, D = run_proxy(Q, chat, Wk, Hkv, A_prev=prev)
+    w = dataclasses.replace(wl.WORKLOADS[0], Hq=Hq, Hkv=Hkv, dh=dh)
+    oA, oD = _oracle_proxy(w, np_(Q), np_(chat), np_(Wk), np_(prev))
     assert_close(np_(A), oA, what="A")
     assert_close(np_(D), oD, what="D")
 
