@@ -60,15 +60,21 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 }
 
 // Kernel launches.  launch_pdl launches through cudaLaunchKernelEx; with
-// kUsePdl it asks for programmatic dependent launch (the next grid may be
-// scheduled while this one drains).  Every kernel starts with pdl_prologue(),
-// which waits for the previous grid's writes when such a dependency exists
-// (griddepcontrol.wait; a no-op otherwise) and releases the next grid.
-// Measured in the bench's CUDA-graph replay on GB300, programmatic launch
-// made the step slower (0.51 vs 0.43 ms), so it is off.
+// kUsePdl it asks for programmatic dependent launch.  Every kernel starts
+// with pdl_prologue() (griddepcontrol.wait: waits for the previous grid's
+// completion and writes when such a dependency exists, a no-op otherwise)
+// before its first read of an earlier kernel's output.  The next grid may be
+// scheduled once every CTA of this one has called pdl_trigger() or exited;
+// the long kernels call it after their main work, so the next grid's
+// set-up overlaps only this grid's tail.  Measured in the bench's CUDA-graph
+// replay on GB300, programmatic launch made the step slower both with the
+// trigger at every kernel's start (0.51 vs 0.43 ms) and with it after the
+// main work (0.346 vs 0.341 ms), so it is off.
 constexpr bool kUsePdl = false;
 __device__ __forceinline__ void pdl_prologue() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 

@@ -482,8 +482,9 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
 // 16 / G member rows are loaded together.  Rows are scanned in blocks of
 // 4096: the block's assignments are staged in shared memory with 16-byte
 // loads, every thread counts the members in its contiguous run of rows, one
-// block scan places them, and the list (row, 1/||h||) sits in shared memory
-// (over the staged assignments, which are all read before the scan).
+// block scan places them, and the member list sits in shared memory (over the
+// staged assignments, which are all read before the scan); 1/||h|| of a
+// member is loaded with its row.
 // Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
 // is empty or its sum is zero), plus its bf16 split; the squared norm is the
 // sum of the slices' partials, read from each CTA's shared memory across the
@@ -507,7 +508,6 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   constexpr int V = Vec<T>::n;
   constexpr int kMemb = 16 / G;
   __shared__ __align__(16) int list[kScanRows];  // staged assignments, then members
-  __shared__ float list_inv[kScanRows];
   __shared__ int s_scan[32];
   __shared__ float s_red[32];
   __shared__ float s_ss;
@@ -551,7 +551,6 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
       hit &= hit - 1;
       const int i = r0 + q;
       list[w] = i;
-      if constexpr (!FINAL) list_inv[w] = inv[(long)b * N + i];
       ++w;
     }
     __syncthreads();
@@ -561,9 +560,12 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
       for (int m = 0; m < tot; m += kMemb) {
         const int cnt_m = min(kMemb, tot - m);
         uint4 raw[kMemb][G];
+        float sc[kMemb];
 #pragma unroll
         for (int q = 0; q < kMemb; ++q) {
-          const T* h = H + ((long)b * N + list[m + (q < cnt_m ? q : 0)]) * d;
+          const long row = (long)b * N + list[m + (q < cnt_m ? q : 0)];
+          sc[q] = q < cnt_m ? __ldg(inv + row) : 0.f;
+          const T* h = H + row * d;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const int col = col0 + (g * nthr + tid) * V;
@@ -574,13 +576,12 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
         }
 #pragma unroll
         for (int q = 0; q < kMemb; ++q) {
-          const float sc = q < cnt_m ? list_inv[m + q] : 0.f;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             float v[V];
             unpack16(raw[q][g], v, T{});
 #pragma unroll
-            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc, u[g][e]);
+            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc[q], u[g][e]);
           }
         }
       }
@@ -588,6 +589,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     n += tot;
     __syncthreads();
   }
+  pdl_trigger();
   if (c == 0 && z == 0 && obj != nullptr) {  // block-uniform: folds the pass objective
     float so = 0.f;
     for (int t = tid; t < ntile; t += nthr) so += objp[(long)b * ntile + t];
@@ -709,6 +711,8 @@ KmPlan km_plan(int dtype, int B, int N, int d, int C) {
     const int tiles = B * p.mtb;
     int nz = std::min(8, std::max(1, ceil_div(kSmTarget, tiles)));
     nz = std::min(nz, p.KB);
+    // the d-chunks of a tile share a cluster: keep the clusters in one wave
+    while (nz > 1 && p.BN <= 128 && tiles > tc_cluster_capacity(nz)) --nz;
     p.kpc = ceil_div(p.KB, nz);
     p.nz = ceil_div(p.KB, p.kpc);
     p.cluster = p.nz > 1 && p.BN <= 128;

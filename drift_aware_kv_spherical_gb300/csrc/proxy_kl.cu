@@ -13,8 +13,10 @@
 // bf16 inputs take the tensor-core path instead (C <= 128, dh % 64 == 0):
 //   k_split_f32     C_hat -> bf16 hi + lo
 //   tcgen05 GEMM    K~ = C_hat_hi W_k + C_hat_lo W_k, W_k streamed through
-//                   TMA as MN-major tiles, split over d for small B*C
-//                   (k_ckeys_finish sums the chunks); kept as K~_hi, K~_lo
+//                   TMA as MN-major tiles, split over d for small B*C (the
+//                   chunks of a tile form a thread-block cluster and sum in
+//                   chunk order through distributed shared memory); kept as
+//                   K~_hi, K~_lo
 //   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
 //                   in TMEM, softmax over the C columns in the epilogue,
 //                   head sum in registers; the head slices of a row tile
@@ -241,13 +243,11 @@ __device__ __forceinline__ void split_store(__nv_bfloat16* hi, __nv_bfloat16* lo
   *lo = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// K~ tile epilogue: rows of B*C centroids, BN key columns.  One d-chunk:
-// split and store.  Several: store fp32 partials [z][M][nkv], which
-// k_ckeys_finish sums in chunk order.
+// K~ tile epilogue: rows of B*C centroids, BN key columns, one d-chunk:
+// split and store (several chunks: CkeysClusterEpi).
 template <int BN>
 struct CkeysEpi : TcEpiBase {
-  int M, nkv, nz;
-  float* part;
+  int M, nkv;
   __nv_bfloat16* khi;
   __nv_bfloat16* klo;
   struct State {};
@@ -255,7 +255,7 @@ struct CkeysEpi : TcEpiBase {
   __device__ int arow(int t) const { return t * 128; }
   __device__ int bcoord(int, int n0) const { return n0; }
   __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
-  __device__ void consume(int t, int r, int n0, int z, uint32_t taddr, State&) const {
+  __device__ void consume(int t, int r, int n0, int, uint32_t taddr, State&) const {
     const int m = t * 128 + r;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -263,31 +263,64 @@ struct CkeysEpi : TcEpiBase {
       tc::tmem_ld32(taddr + c0, v);
       if (m >= M) continue;
       const long o = (long)m * nkv + n0 + c0;
-      if (nz == 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) split_store(khi + o + j, klo + o + j, v[j]);
-      } else {
-        float4* dst = reinterpret_cast<float4*>(part + (long)z * M * nkv + o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      }
+      for (int j = 0; j < 32; ++j) split_store(khi + o + j, klo + o + j, v[j]);
     }
   }
 };
 
-// K~ = sum of the d-chunk partials (chunk order), stored as bf16 hi + lo.
-__global__ void __launch_bounds__(256)
-k_ckeys_finish(const float* __restrict__ part, int nz, long count,
-               __nv_bfloat16* __restrict__ khi, __nv_bfloat16* __restrict__ klo) {
-  pdl_prologue();
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
-       i += (long)gridDim.x * blockDim.x) {
-    float sum = 0.f;
-    for (int z = 0; z < nz; ++z) sum += __ldcg(part + (long)z * count + i);
-    split_store(khi + i, klo + i, sum);
+// K~ with its d-chunks in one thread-block cluster: each chunk's 128 x BN
+// tile stays in shared memory; CTA z sums rows [128 z / nz, 128 (z+1) / nz)
+// over the chunks in chunk order (a warp per row, 4 columns per lane) and
+// stores them split into bf16 hi + lo.
+template <int BN>
+struct CkeysClusterEpi : CkeysEpi<BN> {
+  static constexpr bool kClusterReduce = true;
+  static constexpr uint32_t kLd = BN + 4;
+  using State = typename CkeysEpi<BN>::State;
+  __device__ void consume_red(int, int, int, int, uint32_t taddr, State&,
+                              float* red_row) const {
+    if (red_row == nullptr) return;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(red_row + c0 + 4 * j) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
   }
-}
+  __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
+    const int t = blockIdx.y, n0 = blockIdx.x * BN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    uint32_t base[8];
+    const uint32_t local = tc::smem_u32(red);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
+    for (int r = r0 + warp; r < r1; r += nwarps) {
+      const int m = t * 128 + r;
+      if (m >= this->M) continue;  // warp-uniform
+#pragma unroll
+      for (int c = lane * 4; c < BN; c += 128) {
+        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nz) {
+            const float4 x = tc::ld_dsmem_v4(base[q] + off);
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+          }
+        const long o = (long)m * this->nkv + n0 + c;
+        split_store(this->khi + o, this->klo + o, acc.x);
+        split_store(this->khi + o + 1, this->klo + o + 1, acc.y);
+        split_store(this->khi + o + 2, this->klo + o + 2, acc.z);
+        split_store(this->khi + o + 3, this->klo + o + 3, acc.w);
+      }
+    }
+  }
+};
 
 // Proxy epilogue.  Tiles t = ((b * mtb + mt) * Hq + h), taken in blocks of
 // hps heads per CTA.  Per head: softmax of the row's C scores (scaled by
@@ -488,19 +521,35 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
     if (Hq % sl == 0) { p.nslice = sl; break; }
   p.hps = Hq / p.nslice;
   p.KB = ceil_div(d, 64);
-  p.ck_BN = nkv % 256 == 0 ? 256 : (nkv % 128 == 0 ? 128 : 64);
+  // centroid keys: column tile BN and d split Z by a simple cost, waves x
+  // bytes one CTA streams; a split's Z CTAs form a cluster, and the clusters
+  // the GPU holds at once are counted by GPC (tc_cluster_capacity)
   p.ck_mt = ceil_div(B * C, 128);
-  p.ck_nt = nkv / p.ck_BN;
-  int nz = std::max(1, std::min(8, ceil_div(kSmTarget, p.ck_mt * p.ck_nt)));
-  nz = std::min(nz, p.KB);
-  p.ck_kpc = ceil_div(p.KB, nz);
-  p.ck_nz = ceil_div(p.KB, p.ck_kpc);
+  double best = 0.0;
+  for (int bn : {256, 128, 64}) {
+    if (nkv % bn != 0) continue;
+    const int nt = nkv / bn, groups = p.ck_mt * nt;
+    for (int z = 1; z <= std::min(8, p.KB); ++z) {
+      const int kpc = ceil_div(p.KB, z);
+      if (ceil_div(p.KB, kpc) != z) continue;  // every chunk non-empty
+      const int cap = z == 1 ? kSmTarget : tc_cluster_capacity(z);
+      if (cap <= 0) continue;
+      const double waves = ceil_div(groups, cap);
+      const double cost = waves * kpc * (2.0 * 128 * 64 * 2 + (double)bn * 64 * 2);
+      if (best == 0.0 || cost < best) {
+        best = cost;
+        p.ck_BN = bn;
+        p.ck_nt = nt;
+        p.ck_kpc = kpc;
+        p.ck_nz = z;
+      }
+    }
+  }
   return p;
 }
 
 struct TcWs {
   __nv_bfloat16 *chi, *clo, *khi, *klo;
-  float* kpart;
 };
 
 TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, size_t* bytes) {
@@ -510,7 +559,6 @@ TcWs tc_carve(void* base, const TcPlan& p, int B, int N, int d, int C, int nkv, 
   w.clo = cv.take<__nv_bfloat16>((size_t)B * C * d);
   w.khi = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
   w.klo = cv.take<__nv_bfloat16>((size_t)B * C * nkv);
-  w.kpart = p.ck_nz > 1 ? cv.take<float>((size_t)p.ck_nz * B * C * nkv) : nullptr;
   if (bytes) *bytes = cv.bytes();
   return w;
 }
@@ -533,18 +581,22 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
     maps.b[1] = maps.b[0];
     TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status, INT_MAX};
     const dim3 grid(p.ck_nt, p.ck_mt, p.ck_nz);
+    const int M = a.B * a.C;
     cudaError_t e;
-    switch (p.ck_BN) {
-      case 256: e = launch_tc_gemm<256, 2, 1, true>(maps, sh, CkeysEpi<256>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
-      case 128: e = launch_tc_gemm<128, 2, 1, true>(maps, sh, CkeysEpi<128>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
-      default: e = launch_tc_gemm<64, 2, 1, true>(maps, sh, CkeysEpi<64>{{}, a.B * a.C, nkv, p.ck_nz, w.kpart, w.khi, w.klo}, grid, s); break;
+    if (p.ck_nz > 1) {  // d-chunks summed inside a thread-block cluster
+      switch (p.ck_BN) {
+        case 256: e = launch_tc_gemm<256, 2, 1, true>(maps, sh, CkeysClusterEpi<256>{{{}, M, nkv, w.khi, w.klo}}, grid, s); break;
+        case 128: e = launch_tc_gemm<128, 2, 1, true>(maps, sh, CkeysClusterEpi<128>{{{}, M, nkv, w.khi, w.klo}}, grid, s); break;
+        default: e = launch_tc_gemm<64, 2, 1, true>(maps, sh, CkeysClusterEpi<64>{{{}, M, nkv, w.khi, w.klo}}, grid, s); break;
+      }
+    } else {
+      switch (p.ck_BN) {
+        case 256: e = launch_tc_gemm<256, 2, 1, true>(maps, sh, CkeysEpi<256>{{}, M, nkv, w.khi, w.klo}, grid, s); break;
+        case 128: e = launch_tc_gemm<128, 2, 1, true>(maps, sh, CkeysEpi<128>{{}, M, nkv, w.khi, w.klo}, grid, s); break;
+        default: e = launch_tc_gemm<64, 2, 1, true>(maps, sh, CkeysEpi<64>{{}, M, nkv, w.khi, w.klo}, grid, s); break;
+      }
     }
     if (e != cudaSuccess) return e;
-    if (p.ck_nz > 1) {
-      const long count = (long)a.B * a.C * nkv;
-      launch_pdl(k_ckeys_finish, std::min(ceil_div(count, 256), 4 * kSmTarget), 256, 0, s, 
-          w.kpart, p.ck_nz, count, w.khi, w.klo);
-    }
   }
   TcMaps maps;
   if (!make_tmap_bf16_3d(&maps.a[0], a.Q, a.dh, a.Hq, (uint64_t)a.B * a.N,

@@ -191,6 +191,15 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 }  // namespace tc
 
 // Host: a 2-D bf16 TMA descriptor with a 128-byte swizzle; inner = elements
@@ -202,5 +211,12 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
                        uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
                        uint32_t box_inner, uint32_t box_outer);
+
+// Thread-block clusters of z CTAs (1 <= z <= 8) of a tensor-core GEMM shape
+// (192 threads, ~200 KB of shared memory, so one CTA per SM) that the GPU
+// holds at once: SMs are grouped in GPCs and a cluster stays inside one, so
+// this is below 152 / z for z > 2 (on GB300: 36 for z = 4, 15 for z = 8).
+// Queried once per z and device; 0 when the query fails.
+int tc_cluster_capacity(int z);
 
 }  // namespace ps

@@ -94,7 +94,6 @@ struct TcCfg {
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __global__ void __launch_bounds__(192, 1)
 k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
-  pdl_prologue();
   using Cfg = TcCfg<BN, NA, NB, B_MN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -109,11 +108,16 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* epi_scratch = smem + S * Cfg::kStage + 512;
 
-  // tiles of this CTA first: a CTA without work leaves before any set-up
-  // (never in a cluster, whose barriers every CTA joins)
+  // tiles of this CTA first: a CTA without work leaves before any set-up.
+  // In a cluster, whose barriers every CTA joins, only whole clusters leave:
+  // those whose row-tile slot is empty whatever the K split (a K chunk
+  // z > 0 left without tiles because K is not split still joins).
+  static_assert(!(Epi::kClusterReduce && Epi::kBlocked), "cluster tiles are strided");
+  if (sh.M_dev != nullptr) pdl_prologue();  // the row count is an earlier kernel's output
   const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
   const bool ksplit = Epi::kZSplitsK && M <= sh.split_max_rows;
-  const int T = (ksplit || blockIdx.z == 0 || !Epi::kZSplitsK) ? epi.tiles(M) : 0;
+  const int T_all = epi.tiles(M);
+  const int T = (ksplit || blockIdx.z == 0 || !Epi::kZSplitsK) ? T_all : 0;
   int t_begin = blockIdx.y, t_end = T, t_step = gridDim.y;
   if constexpr (Epi::kBlocked) {
     const int per = (T + gridDim.y - 1) / gridDim.y;
@@ -122,7 +126,13 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     t_step = 1;
   }
   epi.tile_range(T, &t_begin, &t_end, &t_step);
-  if (!Epi::kClusterReduce && t_begin >= t_end) return;
+  if constexpr (Epi::kClusterReduce) {
+    int b0 = blockIdx.y, e0 = T_all, s0 = gridDim.y;
+    epi.tile_range(T_all, &b0, &e0, &s0);
+    if (b0 >= e0) return;
+  } else {
+    if (t_begin >= t_end) return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -146,6 +156,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  pdl_prologue();  // set-up above overlaps the previous grid's tail
 
   const int n0 = blockIdx.x * BN;
   const int kb0 = ksplit ? blockIdx.z * sh.kpc : 0;
@@ -274,6 +285,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     }
   }
   __syncthreads();
+  pdl_trigger();
   if constexpr (Epi::kClusterReduce) {
     static_assert(128 * Cfg::kRedLd * 4 <= Cfg::kStages * Cfg::kStage, "cluster result > ring");
     tc::cluster_sync_all();

@@ -21,7 +21,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+// Never launched: stands for the tensor-core GEMMs' resource shape in the
+// cluster-occupancy query.
+__global__ void __launch_bounds__(192, 1) k_cluster_shape(int*) {}
+
 }  // namespace
+
+int tc_cluster_capacity(int z) {
+  if (z < 1 || z > 8) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  static int cache[64][9] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][z] == 0) {
+    const int smem = 200 * 1024;
+    if (cudaFuncSetAttribute(k_cluster_shape, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, z);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = z;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_cluster_shape, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev][z] = n;
+  }
+  return cache[dev][z];
+}
 
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {

@@ -244,10 +244,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Column tiles of BN over [K | V]; when the selection is small (few row
-// tiles) the d dimension is split over blockIdx.z and every chunk stores fp32
-// partials [z][m][2*nkv], finished by k_refresh_finish; otherwise the
-// epilogue rounds and scatters directly.
+// Column tiles of BN over [K | V]; the epilogue rounds to bf16 and scatters
+// each selected row into the K or V cache (a split d: RefreshClusterEpi).
 template <int BN>
 struct RefreshEpi : TcEpiBase {
   const int32_t* rowinfo;
@@ -255,31 +253,16 @@ struct RefreshEpi : TcEpiBase {
   int N, Ncache, off, nkv, split_max_rows;
   __nv_bfloat16* Kc;
   __nv_bfloat16* Vc;
-  float* part;
   struct State {};
   __device__ int tiles(int M) const { return (M + 127) / 128; }
   __device__ int arow(int t) const { return t * 128; }
   __device__ int bsel(int, int n0) const { return n0 >= nkv ? 1 : 0; }
   __device__ int bcoord(int, int n0) const { return n0 >= nkv ? n0 - nkv : n0; }
   __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
-  __device__ void consume(int t, int rr, int n0, int z, uint32_t taddr, State&) const {
+  __device__ void consume(int t, int rr, int n0, int, uint32_t taddr, State&) const {
     const int Mt = *M_total;
     const int m = t * 128 + rr;
     const int r = m < Mt ? rowinfo[m] : -1;
-    if (Mt <= split_max_rows) {
-      float* dst = part + ((long)z * split_max_rows + m) * (2 * nkv) + n0;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(taddr + c0, v);  // warp-collective: every lane loads
-        if (m >= Mt) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(dst + c0 + 4 * j) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      }
-      return;
-    }
     const bool is_v = n0 >= nkv;
     __nv_bfloat16* dst = nullptr;
     if (r >= 0) {
@@ -304,43 +287,75 @@ struct RefreshEpi : TcEpiBase {
   }
 };
 
-// Sums the d-chunk partials of every selected row in chunk order, rounds to
-// bf16 and scatters into the K or V cache (8 columns per thread).
-__global__ void __launch_bounds__(256)
-k_refresh_finish(const float* __restrict__ part, int nz, const int32_t* __restrict__ M_total,
-                 int split_max_rows, const int32_t* __restrict__ rowinfo, int N, int Ncache,
-                 int off, int nkv, __nv_bfloat16* __restrict__ Kc,
-                 __nv_bfloat16* __restrict__ Vc) {
-  pdl_prologue();
-  const int M = *M_total;
-  if (M > split_max_rows) return;
-  const int w = 2 * nkv, ncol8 = w / 8;
-  const long total = (long)M * ncol8;
-  for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long)gridDim.x * blockDim.x) {
-    const int m = (int)(idx / ncol8), c = (int)(idx % ncol8) * 8;
-    const int r = rowinfo[m];
-    if (r < 0) continue;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int z = 0; z < nz; ++z) {
-      const float4* src =
-          reinterpret_cast<const float4*>(part + ((long)z * split_max_rows + m) * w + c);
-      const float4 x = __ldcg(src), y = __ldcg(src + 1);
-      acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
-      acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+// The d-chunks of a column tile in one thread-block cluster.  While the
+// selection is small (split) each chunk's 128 x BN tile stays in shared
+// memory and CTA z sums rows [128 z / nz, 128 (z+1) / nz) over the chunks in
+// chunk order, a warp per row and 8 columns per lane, rounds to bf16 and
+// scatters the row into the K or V cache.  Otherwise chunk 0 takes the whole
+// d range and scatters straight from TMEM, the other chunks idle.
+template <int BN>
+struct RefreshClusterEpi : RefreshEpi<BN> {
+  static constexpr bool kClusterReduce = true;
+  static constexpr uint32_t kLd = BN + 4;
+  using State = typename RefreshEpi<BN>::State;
+  __device__ void consume_red(int t, int rr, int n0, int z, uint32_t taddr, State& st,
+                              float* red_row) const {
+    if (*this->M_total > this->split_max_rows) {
+      this->consume(t, rr, n0, z, taddr, st);
+      return;
     }
-    const int b = r / N, p = r % N;
-    const bool is_v = c >= nkv;
-    __nv_bfloat16* dst =
-        (is_v ? Vc : Kc) + ((long)b * Ncache + off + p) * nkv + (is_v ? c - nkv : c);
-    uint4 q;
-    q.x = pack_bf16x2(acc[0], acc[1]);
-    q.y = pack_bf16x2(acc[2], acc[3]);
-    q.z = pack_bf16x2(acc[4], acc[5]);
-    q.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(dst) = q;
+    if (red_row == nullptr) return;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(red_row + c0 + 4 * j) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
   }
-}
+  __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
+    const int Mt = *this->M_total;
+    if (Mt > this->split_max_rows) return;
+    const int t = blockIdx.y, n0 = blockIdx.x * BN, nkv = this->nkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    const bool is_v = n0 >= nkv;
+    uint32_t base[8];
+    const uint32_t local = tc::smem_u32(red);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
+    for (int r = r0 + warp; r < r1; r += nwarps) {
+      const int m = t * 128 + r;
+      const int ri = m < Mt ? this->rowinfo[m] : -1;
+      if (ri < 0) continue;  // warp-uniform
+      const int b = ri / this->N, p = ri % this->N;
+      __nv_bfloat16* dst = (is_v ? this->Vc : this->Kc) +
+                           ((long)b * this->Ncache + this->off + p) * nkv +
+                           (is_v ? n0 - nkv : n0);
+#pragma unroll
+      for (int c = lane * 8; c < BN; c += 256) {
+        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nz) {
+            const float4 x = tc::ld_dsmem_v4(base[q] + off);
+            const float4 y = tc::ld_dsmem_v4(base[q] + off + 16);
+            a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+            a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+          }
+        uint4 o;
+        o.x = pack_bf16x2(a[0], a[1]);
+        o.y = pack_bf16x2(a[2], a[3]);
+        o.z = pack_bf16x2(a[4], a[5]);
+        o.w = pack_bf16x2(a[6], a[7]);
+        *reinterpret_cast<uint4*>(dst + c) = o;
+      }
+    }
+  }
+};
 
 struct RefreshPlan {
   int BN, ntiles, nz, kpc, KB, split_max_rows;
@@ -354,7 +369,8 @@ RefreshPlan refresh_plan(int B, int N, int d, int nkv) {
   p.nz = std::min(4, p.KB);
   p.kpc = ceil_div(p.KB, p.nz);
   p.nz = ceil_div(p.KB, p.kpc);
-  // split d only while the selected rows give less than a wave of tiles
+  // split d only while the selected rows give less than a wave of tiles; the
+  // grid's y extent (>= this many row tiles) then gives each CTA one tile
   p.split_max_rows = std::min(B * N, 128 * std::max(1, kSmTarget / p.ntiles));
   if (p.nz == 1) p.split_max_rows = 0;
   return p;
@@ -368,7 +384,6 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
   __nv_bfloat16* X = cv.take<__nv_bfloat16>((size_t)rows * a.d);
   int32_t* rowinfo = cv.take<int32_t>((size_t)rows);
   int32_t* M_total = cv.take<int32_t>(4);
-  float* part = cv.take<float>((size_t)pl.nz * pl.split_max_rows * 2 * nkv);
   launch_pdl(k_gather_rows, dim3(ceil_div(a.N, 8), a.B), 256, 0, s, 
       static_cast<const __nv_bfloat16*>(a.H), a.pos, a.npos, a.B, a.N, a.d, X, rowinfo,
       M_total);
@@ -382,14 +397,11 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
   const int gy = std::max(1, std::min(ceil_div(rows, 128), ceil_div(4 * kSmTarget, pl.ntiles)));
   RefreshEpi<BN> epi{{}, rowinfo, M_total, a.N, a.Ncache, a.cache_off, nkv,
                      pl.split_max_rows, static_cast<__nv_bfloat16*>(a.Kc),
-                     static_cast<__nv_bfloat16*>(a.Vc), part};
-  cudaError_t e = launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(pl.ntiles, gy, pl.nz), s);
-  if (e != cudaSuccess || pl.split_max_rows == 0) return e;
-  const long work = (long)pl.split_max_rows * (2 * nkv / 8);
-  launch_pdl(k_refresh_finish, std::min(ceil_div(work, 256), 4 * kSmTarget), 256, 0, s, 
-      part, pl.nz, M_total, pl.split_max_rows, rowinfo, a.N, a.Ncache, a.cache_off, nkv,
-      static_cast<__nv_bfloat16*>(a.Kc), static_cast<__nv_bfloat16*>(a.Vc));
-  return cudaGetLastError();
+                     static_cast<__nv_bfloat16*>(a.Vc)};
+  if (pl.nz == 1)
+    return launch_tc_gemm<BN, 1, 1, true>(maps, sh, epi, dim3(pl.ntiles, gy, 1), s);
+  return launch_tc_gemm<BN, 1, 1, true>(maps, sh, RefreshClusterEpi<BN>{epi},
+                                        dim3(pl.ntiles, gy, pl.nz), s);
 }
 
 template <typename T>
@@ -415,13 +427,11 @@ bool refresh_tc_ok(int dtype, int Hkv, int dh) {
   return dtype == PS_BF16 && (Hkv * dh) % 64 == 0;
 }
 
-size_t refresh_ws(int B, int N, int d, int Hkv, int dh) {
-  const RefreshPlan pl = refresh_plan(B, N, d, Hkv * dh);
+size_t refresh_ws(int B, int N, int d, int, int) {
   Carver cv(nullptr);
   cv.take<__nv_bfloat16>((size_t)B * N * d);
   cv.take<int32_t>((size_t)B * N);
   cv.take<int32_t>(4);
-  cv.take<float>((size_t)pl.nz * pl.split_max_rows * 2 * Hkv * dh);
   return cv.bytes();
 }
 

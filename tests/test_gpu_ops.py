@@ -503,6 +503,28 @@ def test_refresh_all_rows_ragged_d():
         _kv_check(np_(Vc[b]).reshape(N, -1), oracle.bf16_round(Hn[b] @ Wvn.astype(np.float64)), True)
 
 
+def test_refresh_many_rows_unsplit():
+    """1000 of 1000 rows selected against a 2 x 4096-wide [K | V]: more rows
+    than the d split takes (512 here), so chunk 0 of each cluster runs the
+    whole d range and scatters from TMEM while the other chunk idles."""
+    rng = np.random.default_rng(10)
+    B, N, d, Hkv, dh = 1, 1000, 128, 32, 128
+    H = torch.from_numpy(rng.standard_normal((B, N, d)).astype(np.float32)).cuda().to(torch.bfloat16)
+    Wk = torch.from_numpy(rng.standard_normal((d, Hkv * dh)).astype(np.float32) * 0.1).cuda().to(torch.bfloat16)
+    Wv = torch.from_numpy(rng.standard_normal((d, Hkv * dh)).astype(np.float32) * 0.1).cuda().to(torch.bfloat16)
+    pos = torch.from_numpy(rng.permutation(N).astype(np.int32))[None].cuda().contiguous()
+    npos = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    Kc = torch.zeros(B, N, Hkv, dh, device="cuda", dtype=torch.bfloat16)
+    Vc = torch.zeros_like(Kc)
+    ws = ps.workspace(ps.OP_REFRESH, B=B, N=N, d=d, Hkv=Hkv, dh=dh)
+    ps.ps_refresh_kv(H, pos, npos, Wk, Wv, Kc, Vc, Hkv, dh, ws=ws)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    Hn, Wkn, Wvn = np_(H), np_(Wk), np_(Wv)
+    _kv_check(np_(Kc[0]).reshape(N, -1), oracle.bf16_round(Hn[0] @ Wkn.astype(np.float64)), True)
+    _kv_check(np_(Vc[0]).reshape(N, -1), oracle.bf16_round(Hn[0] @ Wvn.astype(np.float64)), True)
+
+
 # ---------------------------------------------------------------- commit
 def _commit_case(widx, mode, suffix, B=None, seed=0):
     w = wl.WORKLOADS[widx]
