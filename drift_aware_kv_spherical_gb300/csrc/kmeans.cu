@@ -384,23 +384,35 @@ struct KmAssignClusterEpi : TcEpiBase {
   __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
     const int t = blockIdx.y, b = t / mtb, mt = t % mtb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
-    float* cosv = reinterpret_cast<float*>(scratch);  // [128]
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;  // <= 64 rows (nz >= 2)
+    float* s_inv = reinterpret_cast<float*>(scratch);       // [64]
+    float* cosv = s_inv + 64;                               // [64]
+    for (int j = threadIdx.x; j < r1 - r0; j += blockDim.x) {
+      const int i = mt * 128 + r0 + j;
+      s_inv[j] = i < N ? inv[(long)b * N + i] : 0.f;
+    }
+    __syncthreads();
     uint32_t base[8];
     const uint32_t local = tc::smem_u32(red);
 #pragma unroll
     for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
     for (int r = r0 + warp; r < r1; r += nwarps) {
       const int i = mt * 128 + r;
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int c = lane; c < C; c += 32) {
-        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
-        float sum = 0.f;
+      float sum[BN / 32];
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) {  // every load of the row issued together
+        const uint32_t off = (uint32_t)(r * kLd + lane + 32 * j) * 4u;
+        sum[j] = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          if (q < nz) sum += tc::ld_dsmem_f32(base[q] + off);
-        if (sum > bv) { bv = sum; bi = c; }
+          if (q < nz) sum[j] += tc::ld_dsmem_f32(base[q] + off);
+      }
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) {
+        const int c = lane + 32 * j;
+        if (c < C && sum[j] > bv) { bv = sum[j]; bi = c; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -415,11 +427,12 @@ struct KmAssignClusterEpi : TcEpiBase {
           const long row = (long)b * N + i;
           assign[row] = bi;
           best[row] = bv;
-          cs = bv * inv[row];
+          cs = bv * s_inv[r - r0];
         }
         cosv[r - r0] = cs;
       }
     }
+    tc::cluster_arrive();
     __syncthreads();
     if (threadIdx.x == 0) {
       float so = 0.f;
@@ -611,21 +624,30 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
 #pragma unroll
       for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
     ss = block_sum_f32(ss, s_red);
-    if (S > 1) {  // every CTA of the cluster reaches both barriers
+    if (S > 1) {  // every CTA of the cluster reaches the barrier and the wait below
       if (tid == 0) s_ss = ss;
       tc::cluster_sync_all();
       if (tid == 0) {
         const uint32_t a = tc::smem_u32(&s_ss);
+        float part[kMaxSlices];
+#pragma unroll
+        for (int r = 0; r < kMaxSlices; ++r)
+          part[r] = r < S ? tc::ld_dsmem_f32(tc::cluster_map(a, r)) : 0.f;
         float t = 0.f;
-        for (int r = 0; r < S; ++r) t += tc::ld_dsmem_f32(tc::cluster_map(a, r));
+#pragma unroll
+        for (int r = 0; r < kMaxSlices; ++r)
+          if (r < S) t += part[r];
         s_red[0] = t;
       }
-      tc::cluster_sync_all();  // no CTA leaves while another still reads its s_ss
+      tc::cluster_arrive();
       __syncthreads();
       ss = s_red[0];
     }
     const float nu = sqrtf(ss);
-    if (n == 0 || !(nu > 0.f)) return;
+    if (n == 0 || !(nu > 0.f)) {
+      if (S > 1) tc::cluster_wait();
+      return;
+    }
     const long ro = ((long)b * C + c) * d;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -643,6 +665,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
         }
       }
     }
+    // no CTA leaves while another still reads its s_ss
+    if (S > 1) tc::cluster_wait();
   }
 }
 

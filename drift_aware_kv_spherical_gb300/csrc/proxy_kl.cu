@@ -319,6 +319,7 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
         split_store(this->khi + o + 3, this->klo + o + 3, acc.w);
       }
     }
+    tc::cluster_arrive();
   }
 };
 
@@ -474,30 +475,47 @@ struct ProxyClusterEpi : ProxyEpi<BN> {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
     const int C = this->C, N = this->N;
+    const int i0 = mt * 128 + r0, nrow = max(0, min(r1, N - mt * 128) - r0);
+    const long row0 = (long)b * N + i0;
     const float hq = (float)this->Hq;
+    // the previous distributions of this CTA's rows, staged in one pass (the
+    // shared memory past the cluster-read result is this CTA's own)
+    float* s_prev = const_cast<float*>(red) + 128 * kLd;
+    const bool prev = this->A_prev != nullptr;
+    if (prev)
+      for (int j = threadIdx.x; j < nrow * C; j += blockDim.x)
+        s_prev[j] = __ldg(this->A_prev + row0 * C + j);
+    __syncthreads();
     uint32_t base[8];
     const uint32_t local = tc::smem_u32(red);
 #pragma unroll
     for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
-    for (int r = r0 + warp; r < r1; r += nwarps) {
-      const int i = mt * 128 + r;
-      if (i >= N) continue;  // warp-uniform
-      const long row = (long)b * N + i;
-      float kl = 0.f;
-      for (int c = lane; c < C; c += 32) {
-        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
-        float sum = 0.f;
+    for (int r = r0 + warp; r < r0 + nrow; r += nwarps) {
+      float sum[BN / 32];
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) {  // every load of the row issued together
+        const uint32_t off = (uint32_t)(r * kLd + lane + 32 * j) * 4u;
+        sum[j] = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          if (q < nz) sum += tc::ld_dsmem_f32(base[q] + off);
-        const float a = sum / hq;
-        this->A_cur[row * C + c] = a;
-        if (this->A_prev != nullptr && a > 0.f)
-          kl += a * logf(a / fmaxf(this->A_prev[row * C + c], 1e-30f));
+          if (q < nz) sum[j] += tc::ld_dsmem_f32(base[q] + off);
+      }
+      const long row = row0 + (r - r0);
+      float kl = 0.f;
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) {
+        const int c = lane + 32 * j;
+        if (c < C) {
+          const float a = sum[j] / hq;
+          this->A_cur[row * C + c] = a;
+          if (prev && a > 0.f)
+            kl += a * logf(a / fmaxf(s_prev[(r - r0) * C + c], 1e-30f));
+        }
       }
       kl = warp_sum(kl);
-      if (lane == 0) this->D[row] = this->A_prev != nullptr ? fmaxf(kl, 0.f) : 0.f;
+      if (lane == 0) this->D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
     }
+    tc::cluster_arrive();
   }
 };
 

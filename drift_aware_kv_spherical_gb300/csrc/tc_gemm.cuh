@@ -90,7 +90,9 @@ struct TcCfg {
 //        red_row = this row's slot in the CTA's result (kRedLd floats), or
 //        nullptr before the CTA's last tile
 //   void reduce(const float* red, int z, int Z, uint8_t* scratch)
-//        called by all 192 threads between two cluster barriers
+//        called by all 192 threads after a cluster barrier; must call
+//        tc::cluster_arrive() exactly once, uniformly, after its last read
+//        of another CTA's shared memory (the CTA waits before leaving)
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __global__ void __launch_bounds__(192, 1)
 k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
@@ -290,12 +292,13 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     static_assert(128 * Cfg::kRedLd * 4 <= Cfg::kStages * Cfg::kStage, "cluster result > ring");
     tc::cluster_sync_all();
     epi.reduce(reinterpret_cast<const float*>(smem), blockIdx.z, gridDim.z, epi_scratch);
-    tc::cluster_sync_all();  // no CTA leaves while another still reads its result
   }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 2 * BN);
   }
+  // no CTA leaves while another still reads its result
+  if constexpr (Epi::kClusterReduce) tc::cluster_wait();
 }
 
 // Plain epilogue base: 2-D maps, strided tiles, no B offset, one b map.
