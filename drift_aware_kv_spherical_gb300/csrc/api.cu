@@ -1,6 +1,7 @@
 // The C ABI of libpolestar: handle management, argument validation,
 // workspace sizing and dispatch to the kernels.  Declarations and the
 // meaning of every argument are in include/polestar.h.
+#include <cstdio>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -23,7 +24,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // arrays read or written one element at a time only need to exist
 #define PS_NN(p) PS_REQUIRE((p) != nullptr)
 
-ps_status launch_status(cudaError_t e) { return e == cudaSuccess ? PS_OK : PS_ERR_CUDA; }
+thread_local char g_last_cuda_error[192] = "";
+
+ps_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return PS_OK;
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return PS_ERR_CUDA;
+}
 
 ps_status check_ws(size_t need, const void* ws, size_t ws_bytes) {
   if (need == 0) return PS_OK;
@@ -49,19 +57,22 @@ ps_status ps_create(int device, ps_handle* out) {
   if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n)
     return PS_ERR_ARG;
   cudaDeviceProp prop;
-  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return PS_ERR_CUDA;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return launch_status(e);
   if (!(prop.major == 10 && prop.minor == 3)) return PS_ERR_UNSUPPORTED;
-  if (cudaSetDevice(device) != cudaSuccess) return PS_ERR_CUDA;
+  e = cudaSetDevice(device);
+  if (e != cudaSuccess) return launch_status(e);
   auto* h = new (std::nothrow) ps_handle_s;
   if (h == nullptr) return PS_ERR_CUDA;
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
   h->status = nullptr;
-  if (cudaMalloc(&h->status, 16) != cudaSuccess ||
-      cudaMemset(h->status, 0, 16) != cudaSuccess) {
+  e = cudaMalloc(&h->status, 16);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
+  if (e != cudaSuccess) {
     if (h->status) cudaFree(h->status);
     delete h;
-    return PS_ERR_CUDA;
+    return launch_status(e);
   }
   *out = h;
   return PS_OK;
@@ -77,11 +88,12 @@ ps_status ps_destroy(ps_handle h) {
 ps_status ps_check(ps_handle h, void* stream, int synchronize) {
   if (h == nullptr) return PS_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (synchronize && cudaStreamSynchronize(s) != cudaSuccess) return PS_ERR_CUDA;
+  cudaError_t e = synchronize ? cudaStreamSynchronize(s) : cudaSuccess;
+  if (e != cudaSuccess) return launch_status(e);
   int word = 0;
-  if (cudaMemcpyAsync(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return PS_ERR_CUDA;
+  e = cudaMemcpyAsync(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return launch_status(e);
   if (word != 0) {
     cudaMemsetAsync(h->status, 0, sizeof(int), s);
     cudaStreamSynchronize(s);
@@ -101,6 +113,8 @@ const char* ps_status_string(ps_status s) {
   }
   return "unknown status";
 }
+
+const char* ps_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
                           int dh, int k, int P, int V) {

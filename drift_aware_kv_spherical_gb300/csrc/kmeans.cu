@@ -391,28 +391,22 @@ struct KmAssignClusterEpi : TcEpiBase {
       const int i = mt * 128 + r0 + j;
       s_inv[j] = i < N ? inv[(long)b * N + i] : 0.f;
     }
+    // the summed scores replace this CTA's own rows [r0, r1), which only it reads
+    float* own = const_cast<float*>(red);
+    cluster_rows_sum(red, kLd, r0, r1, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
+      *reinterpret_cast<float4*>(own + r * kLd + c) = v;
+    });
+    tc::cluster_arrive();
     __syncthreads();
-    uint32_t base[8];
-    const uint32_t local = tc::smem_u32(red);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
     for (int r = r0 + warp; r < r1; r += nwarps) {
       const int i = mt * 128 + r;
-      float sum[BN / 32];
-#pragma unroll
-      for (int j = 0; j < BN / 32; ++j) {  // every load of the row issued together
-        const uint32_t off = (uint32_t)(r * kLd + lane + 32 * j) * 4u;
-        sum[j] = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < nz) sum[j] += tc::ld_dsmem_f32(base[q] + off);
-      }
       float bv = -INFINITY;
       int bi = INT_MAX;
 #pragma unroll
       for (int j = 0; j < BN / 32; ++j) {
         const int c = lane + 32 * j;
-        if (c < C && sum[j] > bv) { bv = sum[j]; bi = c; }
+        const float v = own[r * kLd + c];
+        if (c < C && v > bv) { bv = v; bi = c; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -432,7 +426,6 @@ struct KmAssignClusterEpi : TcEpiBase {
         cosv[r - r0] = cs;
       }
     }
-    tc::cluster_arrive();
     __syncthreads();
     if (threadIdx.x == 0) {
       float so = 0.f;
@@ -652,15 +645,29 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int col = col0 + (g * nthr + tid) * V;
-      if (col < col1) {
+      if (col < col1) {  // V consecutive columns: 16-byte fp32 stores, 8- or 16-byte bf16
+        float x[V];
+        uint32_t hi[V / 2], lo[V / 2];
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float x = u[g][e] / nu;
-          mu[ro + col + e] = x;
-          if (mu_hi != nullptr) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(x);
-            mu_hi[ro + col + e] = h;
-            mu_lo[ro + col + e] = __float2bfloat16_rn(x - __bfloat162float(h));
+        for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
+#pragma unroll
+        for (int e = 0; e < V; e += 2) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(x[e] - hf.x, x[e + 1] - hf.y);
+          hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        float4* mo = reinterpret_cast<float4*>(mu + ro + col);
+#pragma unroll
+        for (int e = 0; e < V; e += 4) mo[e / 4] = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+        if (mu_hi != nullptr) {
+          if constexpr (V == 8) {
+            *reinterpret_cast<uint4*>(mu_hi + ro + col) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(mu_lo + ro + col) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          } else {
+            *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
+            *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
           }
         }
       }

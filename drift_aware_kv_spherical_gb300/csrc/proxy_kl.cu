@@ -293,32 +293,14 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
   }
   __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
     const int t = blockIdx.y, n0 = blockIdx.x * BN;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
-    uint32_t base[8];
-    const uint32_t local = tc::smem_u32(red);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
-    for (int r = r0 + warp; r < r1; r += nwarps) {
-      const int m = t * 128 + r;
-      if (m >= this->M) continue;  // warp-uniform
-#pragma unroll
-      for (int c = lane * 4; c < BN; c += 128) {
-        const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < nz) {
-            const float4 x = tc::ld_dsmem_v4(base[q] + off);
-            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
-          }
-        const long o = (long)m * this->nkv + n0 + c;
-        split_store(this->khi + o, this->klo + o, acc.x);
-        split_store(this->khi + o + 1, this->klo + o + 1, acc.y);
-        split_store(this->khi + o + 2, this->klo + o + 2, acc.z);
-        split_store(this->khi + o + 3, this->klo + o + 3, acc.w);
-      }
-    }
+    const int r0 = z * 128 / nz, r1 = min((z + 1) * 128 / nz, this->M - t * 128);
+    cluster_rows_sum(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
+      const long o = (long)(t * 128 + r) * this->nkv + n0 + c;
+      split_store(this->khi + o, this->klo + o, v.x);
+      split_store(this->khi + o + 1, this->klo + o + 1, v.y);
+      split_store(this->khi + o + 2, this->klo + o + 2, v.z);
+      split_store(this->khi + o + 3, this->klo + o + 3, v.w);
+    });
     tc::cluster_arrive();
   }
 };
@@ -485,28 +467,21 @@ struct ProxyClusterEpi : ProxyEpi<BN> {
     if (prev)
       for (int j = threadIdx.x; j < nrow * C; j += blockDim.x)
         s_prev[j] = __ldg(this->A_prev + row0 * C + j);
+    // head-slice sums replace this CTA's own rows, which only it reads
+    float* own = const_cast<float*>(red);
+    cluster_rows_sum(red, kLd, r0, r0 + nrow, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
+      *reinterpret_cast<float4*>(own + r * kLd + c) = v;
+    });
+    tc::cluster_arrive();
     __syncthreads();
-    uint32_t base[8];
-    const uint32_t local = tc::smem_u32(red);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
     for (int r = r0 + warp; r < r0 + nrow; r += nwarps) {
-      float sum[BN / 32];
-#pragma unroll
-      for (int j = 0; j < BN / 32; ++j) {  // every load of the row issued together
-        const uint32_t off = (uint32_t)(r * kLd + lane + 32 * j) * 4u;
-        sum[j] = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < nz) sum[j] += tc::ld_dsmem_f32(base[q] + off);
-      }
       const long row = row0 + (r - r0);
       float kl = 0.f;
 #pragma unroll
       for (int j = 0; j < BN / 32; ++j) {
         const int c = lane + 32 * j;
         if (c < C) {
-          const float a = sum[j] / hq;
+          const float a = own[r * kLd + c] / hq;
           this->A_cur[row * C + c] = a;
           if (prev && a > 0.f)
             kl += a * logf(a / fmaxf(s_prev[(r - r0) * C + c], 1e-30f));
@@ -515,7 +490,6 @@ struct ProxyClusterEpi : ProxyEpi<BN> {
       kl = warp_sum(kl);
       if (lane == 0) this->D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
     }
-    tc::cluster_arrive();
   }
 };
 

@@ -319,7 +319,6 @@ struct RefreshClusterEpi : RefreshEpi<BN> {
     const int Mt = *this->M_total;
     if (Mt <= this->split_max_rows) {
       const int t = blockIdx.y, n0 = blockIdx.x * BN, nkv = this->nkv;
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
       const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;  // <= 64 rows (nz >= 2)
       const bool is_v = n0 >= nkv;
       int* s_ri = reinterpret_cast<int*>(scratch);  // [64] destination rows, one pass
@@ -328,37 +327,15 @@ struct RefreshClusterEpi : RefreshEpi<BN> {
         s_ri[j] = m < Mt ? this->rowinfo[m] : -1;
       }
       __syncthreads();
-      uint32_t base[8];
-      const uint32_t local = tc::smem_u32(red);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) base[q] = q < nz ? tc::cluster_map(local, q) : 0u;
-      for (int r = r0 + warp; r < r1; r += nwarps) {
+      __nv_bfloat16* cache = is_v ? this->Vc : this->Kc;
+      const int coff = is_v ? n0 - nkv : n0;
+      cluster_rows_sum(red, kLd, r0, r1, BN, nz, [&](int r, int c, float4 v) {
         const int ri = s_ri[r - r0];
-        if (ri < 0) continue;  // warp-uniform
+        if (ri < 0) return;
         const int b = ri / this->N, p = ri % this->N;
-        __nv_bfloat16* dst = (is_v ? this->Vc : this->Kc) +
-                             ((long)b * this->Ncache + this->off + p) * nkv +
-                             (is_v ? n0 - nkv : n0);
-#pragma unroll
-        for (int c = lane * 8; c < BN; c += 256) {
-          const uint32_t off = (uint32_t)(r * kLd + c) * 4u;
-          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (q < nz) {
-              const float4 x = tc::ld_dsmem_v4(base[q] + off);
-              const float4 y = tc::ld_dsmem_v4(base[q] + off + 16);
-              a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
-              a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
-            }
-          uint4 o;
-          o.x = pack_bf16x2(a[0], a[1]);
-          o.y = pack_bf16x2(a[2], a[3]);
-          o.z = pack_bf16x2(a[4], a[5]);
-          o.w = pack_bf16x2(a[6], a[7]);
-          *reinterpret_cast<uint4*>(dst + c) = o;
-        }
-      }
+        *reinterpret_cast<uint2*>(cache + ((long)b * this->Ncache + this->off + p) * nkv + coff +
+                                  c) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      });
     }
     tc::cluster_arrive();
   }

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libpolestar.so")
 PS_OK, PS_ERR_ARG, PS_ERR_UNSUPPORTED, PS_ERR_WORKSPACE, PS_ERR_CUDA, PS_ERR_TIMEOUT = range(6)
 PS_F32, PS_BF16 = 0, 1
 OP_KMEANS, OP_NVFP4, OP_PROXY_KL, OP_TOPK, OP_REFRESH, OP_COMMIT = range(6)
-EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string",
+EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_cuda_error",
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
             "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit"]
 
@@ -29,7 +29,11 @@ _sz = ctypes.c_size_t
 class PolestarError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
-        super().__init__(f"{where}: {Library.load().status_string(status)} ({status})")
+        lib = Library.load()
+        msg = f"{where}: {lib.status_string(status)} ({status})"
+        if status == PS_ERR_CUDA:
+            msg += f" [{lib.cdll.ps_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 class CommitParams(ctypes.Structure):
@@ -43,6 +47,7 @@ _SIGS = {
     "ps_destroy": (_i, [_p]),
     "ps_check": (_i, [_p, _p, _i]),
     "ps_status_string": (ctypes.c_char_p, [_i]),
+    "ps_last_cuda_error": (ctypes.c_char_p, []),
     "ps_workspace_bytes": (_sz, [_i] * 11),
     "ps_kmeans_spherical": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                                  _p, _p, _p, _p, _p, _sz, _p]),

@@ -74,6 +74,12 @@ ps_status ps_check(ps_handle h, void* stream, int synchronize);
 
 const char* ps_status_string(ps_status s);
 
+/* The CUDA runtime error behind the calling thread's most recent
+ * PS_ERR_CUDA ("cudaErrorName: description"), or "" if there was none.  The
+ * text lives in thread-local storage owned by the library and stays valid
+ * until the thread's next call that fails with PS_ERR_CUDA. */
+const char* ps_last_cuda_error(void);
+
 /* Workspace bytes `op` needs for these sizes (arguments an op does not use
  * are ignored).  0 means ws may be NULL. */
 size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
