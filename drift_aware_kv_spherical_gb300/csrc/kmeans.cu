@@ -393,7 +393,7 @@ struct KmAssignClusterEpi : TcEpiBase {
     }
     // the summed scores replace this CTA's own rows [r0, r1), which only it reads
     float* own = const_cast<float*>(red);
-    cluster_rows_sum(red, kLd, r0, r1, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
+    cluster_rows_sum<8>(red, kLd, r0, r1, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
       *reinterpret_cast<float4*>(own + r * kLd + c) = v;
     });
     tc::cluster_arrive();

@@ -294,7 +294,7 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
   __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
     const int t = blockIdx.y, n0 = blockIdx.x * BN;
     const int r0 = z * 128 / nz, r1 = min((z + 1) * 128 / nz, this->M - t * 128);
-    cluster_rows_sum(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
+    cluster_rows_sum<8>(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
       const long o = (long)(t * 128 + r) * this->nkv + n0 + c;
       split_store(this->khi + o, this->klo + o, v.x);
       split_store(this->khi + o + 1, this->klo + o + 1, v.y);
@@ -337,59 +337,71 @@ struct ProxyEpi : TcEpiBase {
 #pragma unroll
       for (int c = 0; c < BN; ++c) st.A[c] = 0.f;
     }
-    // softmax with one reciprocal; __expf's error (a few ulp for arguments
-    // <= 0) is far inside the 1e-4 tolerance.  BN <= 64: the scores stay in
-    // registers; BN = 128: TMEM is read again instead (registers would spill)
-    if constexpr (BN > 64) {
-      float m = -INFINITY;
+    // softmax with one reciprocal, in base 2: the scores are scaled by
+    // log2(e) / sqrt(dh) once, so each term is one exp2 (a few ulp, far
+    // inside the 1e-4 tolerance).  TMEM columns are loaded 64 at a time with
+    // one wait; the max and the sum run as four interleaved partials.
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float sl = scale * kLog2e;
+    if constexpr (BN > 64) {  // scores re-read from TMEM (registers would spill)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(taddr + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t r[64];
+        tc::tmem_ld32_nowait(taddr + c0, r);
+        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < C) m = fmaxf(m, v[j] * scale);
+        for (int j = 0; j < 64; ++j)
+          if (c0 + j < C) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[j]) * sl);
       }
-      float sum = 0.f;
+      const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(taddr + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t r[64];
+        tc::tmem_ld32_nowait(taddr + c0, r);
+        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < C) sum += __expf(v[j] * scale - m);
+        for (int j = 0; j < 64; ++j)
+          if (c0 + j < C) s4[j & 3] += exp2f(fmaf(__uint_as_float(r[j]), sl, -m));
       }
-      const float rs = 1.0f / sum;
+      const float rs = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(taddr + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t r[64];
+        tc::tmem_ld32_nowait(taddr + c0, r);
+        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < C) st.A[c0 + j] = fmaf(__expf(v[j] * scale - m), rs, st.A[c0 + j]);
+        for (int j = 0; j < 64; ++j)
+          if (c0 + j < C)
+            st.A[c0 + j] = fmaf(exp2f(fmaf(__uint_as_float(r[j]), sl, -m)), rs, st.A[c0 + j]);
       }
-      return;
+    } else {
+      uint32_t r[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) tc::tmem_ld32_nowait(taddr + c0, r + c0);
+      tc::tmem_wait_ld();
+      float e[BN];
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        e[c] = c < C ? __uint_as_float(r[c]) * sl : -INFINITY;
+        m4[c & 3] = fmaxf(m4[c & 3], e[c]);
+      }
+      const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        e[c] = c < C ? exp2f(e[c] - m) : 0.f;
+        s4[c & 3] += e[c];
+      }
+      const float rs = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+#pragma unroll
+      for (int c = 0; c < BN; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
     }
-    float e[BN];
-    float m = -INFINITY;
-#pragma unroll
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      tc::tmem_ld32(taddr + c0, e + c0);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        e[c0 + j] = (c0 + j < C) ? e[c0 + j] * scale : -INFINITY;
-        m = fmaxf(m, e[c0 + j]);
-      }
-    }
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      e[c] = (c < C) ? __expf(e[c] - m) : 0.f;
-      sum += e[c];
-    }
-    const float rs = 1.0f / sum;
-#pragma unroll
-    for (int c = 0; c < BN; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
   }
   __device__ void finish(int b, int i, const float* Aacc) const {
     const float hq = (float)Hq;
@@ -469,7 +481,7 @@ struct ProxyClusterEpi : ProxyEpi<BN> {
         s_prev[j] = __ldg(this->A_prev + row0 * C + j);
     // head-slice sums replace this CTA's own rows, which only it reads
     float* own = const_cast<float*>(red);
-    cluster_rows_sum(red, kLd, r0, r0 + nrow, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
+    cluster_rows_sum<8>(red, kLd, r0, r0 + nrow, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
       *reinterpret_cast<float4*>(own + r * kLd + c) = v;
     });
     tc::cluster_arrive();

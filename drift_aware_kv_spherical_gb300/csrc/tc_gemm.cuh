@@ -315,35 +315,49 @@ struct TcEpiBase {
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Rows [r0, r1) of the cluster's Z results (row stride ld floats, at `red` in
-// every CTA's shared memory), summed in rank order four columns at a time by
-// all threads of the CTA; every rank's load of an item is issued before any
-// is used.  f(r, c, sum) takes columns c..c+3 of row r.  ncol: a multiple of 4.
-template <class F>
+// Rows [r0, r1) of the cluster's Z (<= ZMAX) results (row stride ld floats,
+// at `red` in every CTA's shared memory), summed in rank order four columns
+// at a time by all threads of the CTA; each thread issues the loads of a
+// batch of items (every rank) before using any.  f(r, c, sum) takes columns
+// c..c+3 of row r.  ncol: a multiple of 4.
+template <int ZMAX, class F>
 __device__ __forceinline__ void cluster_rows_sum(const float* red, uint32_t ld, int r0, int r1,
                                                  int ncol, int Z, F&& f) {
-  uint32_t base[8];
+  constexpr int kBatch = 16 / ZMAX > 1 ? 16 / ZMAX : 1;
+  uint32_t base[ZMAX];
   const uint32_t local = tc::smem_u32(red);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) base[q] = q < Z ? tc::cluster_map(local, q) : 0u;
-  const int c4n = ncol / 4, items = (r1 - r0) * c4n;
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int r = r0 + it / c4n, c = (it % c4n) * 4;
-    const uint32_t off = (uint32_t)(r * ld + c) * 4u;
-    float4 x[8];
+  for (int q = 0; q < ZMAX; ++q) base[q] = q < Z ? tc::cluster_map(local, q) : 0u;
+  const int c4n = ncol / 4, items = (r1 - r0) * c4n, nthr = blockDim.x;
+  for (int it0 = threadIdx.x; it0 < items; it0 += kBatch * nthr) {
+    float4 x[kBatch][ZMAX];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q < Z) x[q] = tc::ld_dsmem_v4(base[q] + off);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kBatch; ++k) {
+      const int it = it0 + k * nthr;
+      if (it < items) {
+        const int r = r0 + it / c4n, c = (it % c4n) * 4;
+        const uint32_t off = (uint32_t)(r * ld + c) * 4u;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q < Z) {
-        acc.x += x[q].x;
-        acc.y += x[q].y;
-        acc.z += x[q].z;
-        acc.w += x[q].w;
+        for (int q = 0; q < ZMAX; ++q)
+          if (q < Z) x[k][q] = tc::ld_dsmem_v4(base[q] + off);
       }
-    f(r, c, acc);
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int it = it0 + k * nthr;
+      if (it < items) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < ZMAX; ++q)
+          if (q < Z) {
+            acc.x += x[k][q].x;
+            acc.y += x[k][q].y;
+            acc.z += x[k][q].z;
+            acc.w += x[k][q].w;
+          }
+        f(r0 + it / c4n, (it % c4n) * 4, acc);
+      }
+    }
   }
 }
 

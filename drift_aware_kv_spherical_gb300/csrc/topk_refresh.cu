@@ -329,7 +329,7 @@ struct RefreshClusterEpi : RefreshEpi<BN> {
       __syncthreads();
       __nv_bfloat16* cache = is_v ? this->Vc : this->Kc;
       const int coff = is_v ? n0 - nkv : n0;
-      cluster_rows_sum(red, kLd, r0, r1, BN, nz, [&](int r, int c, float4 v) {
+      cluster_rows_sum<4>(red, kLd, r0, r1, BN, nz, [&](int r, int c, float4 v) {
         const int ri = s_ri[r - r0];
         if (ri < 0) return;
         const int b = ri / this->N, p = ri % this->N;
