@@ -307,11 +307,15 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
 
 // Proxy epilogue.  Tiles t = ((b * mtb + mt) * Hq + h), taken in blocks of
 // hps heads per CTA.  Per head: softmax of the row's C scores (scaled by
-// 1/sqrt(dh)) added to the row's head sum A (registers).  After the slice's
-// last head: one slice -> A / Hq, KL, store; several -> store the partial,
-// which k_proxy_final sums in slice order before the KL.
-template <int BN>
+// 1/sqrt(dh)) added to the row's head sum A (registers).  With P > 1 the P
+// epilogue warps of a TMEM lane quarter each take W = BN / P columns of the
+// row and combine their partial max and sum through shared memory (scratch:
+// two head slots of [max | sum][128 rows][P], then KL partials [128][P]).
+// After the slice's last head (one slice per tile): A / Hq, KL, store.
+template <int BN, int P>
 struct ProxyEpi : TcEpiBase {
+  static constexpr int kEpiWarps = 4 * P;
+  static constexpr int W = BN / P;  // columns per thread
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   int B, N, C, Hq, G, dh, mtb, hps, nslice;
@@ -319,9 +323,8 @@ struct ProxyEpi : TcEpiBase {
   const float* A_prev;
   float* A_cur;
   float* D;
-  float* part;      // [nslice][B*N][C], summed by k_proxy_final
   struct State {
-    float A[BN];
+    float A[W];
   };
   __device__ int tiles(int) const { return B * mtb * Hq; }
   __device__ int arow(int t) const {
@@ -331,110 +334,147 @@ struct ProxyEpi : TcEpiBase {
   __device__ int ahead(int t) const { return t % Hq; }
   __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
   __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
-  __device__ void consume(int t, int, int, int, uint32_t taddr, State& st) const {
+
+  // One head.  Softmax with one reciprocal, in base 2: the scores are scaled
+  // by log2(e) / sqrt(dh) once, so each term is one exp2 (a few ulp, far
+  // inside the 1e-4 tolerance).  TMEM columns are loaded with one wait; the
+  // max and the sum run as four interleaved partials.
+  __device__ void head(int t, int r, int part, uint32_t taddr, float* xs, State& st) const {
     const int h = t % Hq;
     if (h % hps == 0) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) st.A[c] = 0.f;
+      for (int c = 0; c < W; ++c) st.A[c] = 0.f;
     }
-    // softmax with one reciprocal, in base 2: the scores are scaled by
-    // log2(e) / sqrt(dh) once, so each term is one exp2 (a few ulp, far
-    // inside the 1e-4 tolerance).  TMEM columns are loaded 64 at a time with
-    // one wait; the max and the sum run as four interleaved partials.
     constexpr float kLog2e = 1.4426950408889634f;
     const float sl = scale * kLog2e;
-    if constexpr (BN > 64) {  // scores re-read from TMEM (registers would spill)
+    const int c0 = part * W;
+    const uint32_t ta = taddr + c0;
+    if constexpr (W > 64) {  // scores re-read from TMEM (registers would spill)
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        uint32_t r[64];
-        tc::tmem_ld32_nowait(taddr + c0, r);
-        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+      for (int k0 = 0; k0 < W; k0 += 64) {
+        uint32_t raw[64];
+        tc::tmem_ld32_nowait(ta + k0, raw);
+        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-          if (c0 + j < C) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[j]) * sl);
+          if (c0 + k0 + j < C) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(raw[j]) * sl);
       }
       const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        uint32_t r[64];
-        tc::tmem_ld32_nowait(taddr + c0, r);
-        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+      for (int k0 = 0; k0 < W; k0 += 64) {
+        uint32_t raw[64];
+        tc::tmem_ld32_nowait(ta + k0, raw);
+        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-          if (c0 + j < C) s4[j & 3] += exp2f(fmaf(__uint_as_float(r[j]), sl, -m));
+          if (c0 + k0 + j < C) s4[j & 3] += exp2f(fmaf(__uint_as_float(raw[j]), sl, -m));
       }
       const float rs = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        uint32_t r[64];
-        tc::tmem_ld32_nowait(taddr + c0, r);
-        tc::tmem_ld32_nowait(taddr + c0 + 32, r + 32);
+      for (int k0 = 0; k0 < W; k0 += 64) {
+        uint32_t raw[64];
+        tc::tmem_ld32_nowait(ta + k0, raw);
+        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-          if (c0 + j < C)
-            st.A[c0 + j] = fmaf(exp2f(fmaf(__uint_as_float(r[j]), sl, -m)), rs, st.A[c0 + j]);
+          if (c0 + k0 + j < C)
+            st.A[k0 + j] =
+                fmaf(exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)), rs, st.A[k0 + j]);
       }
     } else {
-      uint32_t r[BN];
+      uint32_t raw[W];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) tc::tmem_ld32_nowait(taddr + c0, r + c0);
+      for (int k0 = 0; k0 < W; k0 += 32) tc::tmem_ld32_nowait(ta + k0, raw + k0);
       tc::tmem_wait_ld();
-      float e[BN];
+      float e[W];
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        e[c] = c < C ? __uint_as_float(r[c]) * sl : -INFINITY;
+      for (int c = 0; c < W; ++c) {
+        e[c] = c0 + c < C ? __uint_as_float(raw[c]) * sl : -INFINITY;
         m4[c & 3] = fmaxf(m4[c & 3], e[c]);
       }
-      const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float* mx = xs + (h & 1) * (2 * 128 * P);
+      if constexpr (P > 1) {
+        mx[r * P + part] = m;
+        epi_bar_sync_n<128 * P>();
+        m = mx[r * P];
+#pragma unroll
+        for (int q = 1; q < P; ++q) m = fmaxf(m, mx[r * P + q]);
+      }
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        e[c] = c < C ? exp2f(e[c] - m) : 0.f;
+      for (int c = 0; c < W; ++c) {
+        e[c] = c0 + c < C ? exp2f(e[c] - m) : 0.f;
         s4[c & 3] += e[c];
       }
-      const float rs = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      if constexpr (P > 1) {
+        float* sm = mx + 128 * P;
+        sm[r * P + part] = sum;
+        epi_bar_sync_n<128 * P>();
+        sum = sm[r * P];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
+        for (int q = 1; q < P; ++q) sum += sm[r * P + q];
+      }
+      const float rs = 1.0f / sum;
+#pragma unroll
+      for (int c = 0; c < W; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
     }
   }
-  __device__ void finish(int b, int i, const float* Aacc) const {
-    const float hq = (float)Hq;
+  // After the slice's last head: A / Hq, the KL terms of this thread's
+  // columns, the row's KL from the P partials (part order).
+  __device__ void finish(int t, int r, int part, float* xs, const State& st) const {
+    const int h = t % Hq;
+    if ((h + 1) % hps != 0 && h + 1 != Hq) return;  // tile-uniform
+    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const bool live = i < N, prev = A_prev != nullptr;
     const long row = (long)b * N + i;
+    const float hq = (float)Hq;
+    const int c0 = part * W;
     float kl = 0.f;
+    if (live) {
 #pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      if (c < C) {
-        const float a = Aacc[c] / hq;
-        A_cur[row * C + c] = a;
-        if (A_prev != nullptr && a > 0.f)
-          kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
+      for (int c = 0; c < W; ++c) {
+        if (c0 + c < C) {
+          const float a = st.A[c] / hq;
+          A_cur[row * C + c0 + c] = a;
+          if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c0 + c], 1e-30f));
+        }
       }
     }
-    D[row] = A_prev != nullptr ? fmaxf(kl, 0.f) : 0.f;
+    if constexpr (P > 1) {
+      float* zs = xs + 4 * 128 * P;
+      zs[r * P + part] = kl;
+      epi_bar_sync_n<128 * P>();
+      if (part == 0 && live) {
+        float sum = zs[r * P];
+#pragma unroll
+        for (int q = 1; q < P; ++q) sum += zs[r * P + q];
+        D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
+      }
+    } else if (live) {
+      D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+    }
+  }
+  __device__ void consume(int t, int r, int, int, uint32_t taddr, State& st) const {
+    head(t, r, 0, taddr, nullptr, st);
+  }
+  __device__ void consume_part(int t, int r, int part, int, int, uint32_t taddr,
+                               uint8_t* scratch, State& st) const {
+    head(t, r, part, taddr, reinterpret_cast<float*>(scratch), st);
   }
   __device__ void tile_done(int t, int r, int, int, uint8_t*, State& st) const {
-    const int h = t % Hq;
-    if ((h + 1) % hps != 0 && h + 1 != Hq) return;
-    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
-    const bool live = i < N;
-    if (nslice == 1) {
-      if (live) finish(b, i, st.A);
-      return;
-    }
-    const int slice = h / hps;
-    const long ld = (long)B * N;
-    if (live) {
-      float* dst = part + ((long)slice * ld + (long)b * N + i) * C;
-#pragma unroll
-      for (int c = 0; c < BN; ++c)
-        if (c < C) dst[c] = st.A[c];
-    }
+    finish(t, r, 0, nullptr, st);
+  }
+  __device__ void tile_done_part(int t, int r, int part, int, int, uint8_t* scratch,
+                                 State& st) const {
+    finish(t, r, part, reinterpret_cast<float*>(scratch), st);
   }
 };
 
@@ -442,27 +482,36 @@ struct ProxyEpi : TcEpiBase {
 // heads [z hps, (z+1) hps) of row tile blockIdx.y and leaves its head sum in
 // shared memory; then CTA z finishes rows [128 z / Z, 128 (z+1) / Z), one
 // warp per row: the slices' sums in slice order, A = sum / Hq, KL.
-template <int BN>
-struct ProxyClusterEpi : ProxyEpi<BN> {
+template <int BN, int P>
+struct ProxyClusterEpi : ProxyEpi<BN, P> {
+  using Base = ProxyEpi<BN, P>;
   static constexpr bool kBlocked = false;
   static constexpr bool kClusterReduce = true;
   static constexpr bool kZSplitsK = false;
   static constexpr uint32_t kLd = BN + 4;
-  using State = typename ProxyEpi<BN>::State;
+  using State = typename Base::State;
   __device__ bool tile_range(int, int* tb, int* te, int* ts) const {
     *tb = blockIdx.y * this->Hq + blockIdx.z * this->hps;
     *te = *tb + this->hps;
     *ts = 1;
     return true;
   }
-  __device__ void consume_red(int t, int r, int n0, int z, uint32_t taddr, State& st,
-                              float* red_row) const {
-    this->consume(t, r, n0, z, taddr, st);
+  __device__ void stash(int part, const State& st, float* red_row) const {
     if (red_row == nullptr) return;
 #pragma unroll
-    for (int c = 0; c < BN; c += 4)
-      *reinterpret_cast<float4*>(red_row + c) =
+    for (int c = 0; c < Base::W; c += 4)
+      *reinterpret_cast<float4*>(red_row + part * Base::W + c) =
           make_float4(st.A[c], st.A[c + 1], st.A[c + 2], st.A[c + 3]);
+  }
+  __device__ void consume_red(int t, int r, int, int, uint32_t taddr, State& st,
+                              float* red_row) const {
+    this->head(t, r, 0, taddr, nullptr, st);
+    stash(0, st, red_row);
+  }
+  __device__ void consume_red_part(int t, int r, int part, int, int, uint32_t taddr,
+                                   uint8_t* scratch, State& st, float* red_row) const {
+    this->head(t, r, part, taddr, reinterpret_cast<float*>(scratch), st);
+    stash(part, st, red_row);
   }
   __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
     const int bm = blockIdx.y, b = bm / this->mtb, mt = bm % this->mtb;
@@ -472,13 +521,25 @@ struct ProxyClusterEpi : ProxyEpi<BN> {
     const int i0 = mt * 128 + r0, nrow = max(0, min(r1, N - mt * 128) - r0);
     const long row0 = (long)b * N + i0;
     const float hq = (float)this->Hq;
-    // the previous distributions of this CTA's rows, staged in one pass (the
-    // shared memory past the cluster-read result is this CTA's own)
+    // the previous distributions of this CTA's rows (one contiguous block),
+    // staged in one pass with 16-byte loads; the shared memory past the
+    // cluster-read result is this CTA's own
     float* s_prev = const_cast<float*>(red) + 128 * kLd;
     const bool prev = this->A_prev != nullptr;
-    if (prev)
-      for (int j = threadIdx.x; j < nrow * C; j += blockDim.x)
-        s_prev[j] = __ldg(this->A_prev + row0 * C + j);
+    if (prev) {
+      const float* src = this->A_prev + row0 * C;
+      const int n = nrow * C;
+      if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const int n4 = n >> 2;
+#pragma unroll 4
+        for (int j = threadIdx.x; j < n4; j += blockDim.x)
+          reinterpret_cast<float4*>(s_prev)[j] = __ldg(reinterpret_cast<const float4*>(src) + j);
+        for (int j = (n4 << 2) + threadIdx.x; j < n; j += blockDim.x) s_prev[j] = __ldg(src + j);
+      } else {
+#pragma unroll 4
+        for (int j = threadIdx.x; j < n; j += blockDim.x) s_prev[j] = __ldg(src + j);
+      }
+    }
     // head-slice sums replace this CTA's own rows, which only it reads
     float* own = const_cast<float*>(red);
     cluster_rows_sum<8>(red, kLd, r0, r0 + nrow, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
@@ -612,12 +673,13 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status, INT_MAX};
-  ProxyEpi<BN> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
-                   (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D,
-                   nullptr};
+  // columns of a row split over P epilogue warps per lane quarter (BN / P <= 64)
+  constexpr int P = BN > 64 ? BN / 64 : 1;
+  ProxyEpi<BN, P> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
+                      (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D};
   if (p.nslice == 1)
     return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, 1), s);
-  ProxyClusterEpi<BN> cepi{epi};
+  ProxyClusterEpi<BN, P> cepi{epi};
   return launch_tc_gemm<BN, 1, 2, false>(maps, sh, cepi, dim3(1, a.B * p.mtb, p.nslice), s);
 }
 

@@ -1,11 +1,12 @@
 // A warp-specialised tcgen05 GEMM mainloop shared by the dense contractions.
 //
-// CTA = 6 warps: warp 0 issues TMA loads into an S-stage shared-memory ring,
-// warp 1 issues tcgen05.mma (one thread) into one of two 128 x BN fp32
+// CTA = 2 + E warps: warp 0 issues TMA loads into an S-stage shared-memory
+// ring, warp 1 issues tcgen05.mma (one thread) into one of two 128 x BN fp32
 // accumulators in TMEM (double-buffered, so the MMAs of the next tile run
-// while the epilogue drains this one), warps 2-5 drain the accumulator (each
-// reads the TMEM lane quarter it may access) and hand rows to an op-specific
-// epilogue.  The CTA owns
+// while the epilogue drains this one), and the E = Epi::kEpiWarps (4, 8 or
+// 16) warps from 2 on drain the accumulator and hand rows to an op-specific
+// epilogue: warp w reads the TMEM lane quarter w % 4 it may access, and with
+// E > 4 the E / 4 warps of a quarter split the BN columns between them.  The CTA owns
 // one BN-column tile (blockIdx.x) and walks row tiles t < epi.tiles(M)
 // (strided by gridDim.y, or a contiguous block of them); the epilogue object
 // maps a tile to its TMA coordinates.  blockIdx.z selects a chunk of the K
@@ -59,7 +60,8 @@ struct TcCfg {
   static constexpr uint32_t kB = BN * 64 * 2;
   static constexpr uint32_t kStage = NA * kA + NB * kB;
   static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
-  static constexpr size_t kSmem = 1024 + kStages * kStage + 1024;
+  static constexpr uint32_t kScratch = 16384;  // epilogue scratch after the barriers
+  static constexpr size_t kSmem = 1024 + kStages * kStage + 512 + kScratch;
   static constexpr uint32_t kRedLd = BN + 4;  // row stride (floats) of a cluster result
   static constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN, B_MN);
 };
@@ -80,7 +82,12 @@ struct TcCfg {
 //        released after it returns
 //   void tile_done(int t, int r, int n0, int z, uint8_t* scratch, State&)
 //        called by the 128 epilogue threads together after consume; may
-//        synchronise with bar.sync 1, 128; scratch = 512 B of shared memory
+//        synchronise with epi_bar_sync(); scratch = 16 KB of shared memory
+//   static constexpr int kEpiWarps  4 (default), 8 or 16; above 4 the
+//        engine calls consume_part / tile_done_part / consume_red_part, which
+//        also take the thread's column part (0 .. kEpiWarps / 4 - 1) and the
+//        scratch, and may synchronise the epilogue warps with
+//        epi_bar_sync_n<32 * kEpiWarps>()
 //   static constexpr bool kZSplitsK  blockIdx.z chunks K (else z is the
 //        epilogue's own and every CTA takes the whole K range)
 //   bool tile_range(int T, int* begin, int* end, int* step)  optional
@@ -90,11 +97,11 @@ struct TcCfg {
 //        red_row = this row's slot in the CTA's result (kRedLd floats), or
 //        nullptr before the CTA's last tile
 //   void reduce(const float* red, int z, int Z, uint8_t* scratch)
-//        called by all 192 threads after a cluster barrier; must call
+//        called by every thread of the CTA after a cluster barrier; must call
 //        tc::cluster_arrive() exactly once, uniformly, after its last read
 //        of another CTA's shared memory (the CTA waits before leaving)
 template <int BN, int NA, int NB, bool B_MN, class Epi>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * Epi::kEpiWarps, 1)
 k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
   using Cfg = TcCfg<BN, NA, NB, B_MN>;
   constexpr int S = Cfg::kStages;
@@ -144,7 +151,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     }
     for (int j = 0; j < 2; ++j) {
       tc::mbar_init(acc_full + j, 1);
-      tc::mbar_init(acc_empty + j, 4);
+      tc::mbar_init(acc_empty + j, Epi::kEpiWarps);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -262,7 +269,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       }
     }
   } else {
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, part = (warp - 2) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int r = quarter * 32 + lane;
     typename Epi::State est;
@@ -276,14 +283,26 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
         float* red_row = t + t_step >= t_end
                              ? reinterpret_cast<float*>(smem) + r * Cfg::kRedLd
                              : nullptr;
-        epi.consume_red(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est, red_row);
+        if constexpr (Epi::kEpiWarps > 4)
+          epi.consume_red_part(t, r, part, n0, blockIdx.z, tmem + buf * BN + lane_base,
+                               epi_scratch, est, red_row);
+        else
+          epi.consume_red(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est, red_row);
+      } else if constexpr (Epi::kEpiWarps > 4) {
+        epi.consume_part(t, r, part, n0, blockIdx.z, tmem + buf * BN + lane_base, epi_scratch,
+                         est);
       } else {
         epi.consume(t, r, n0, blockIdx.z, tmem + buf * BN + lane_base, est);
       }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(acc_empty + buf);
-      if constexpr (!Epi::kClusterReduce) epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
+      if constexpr (!Epi::kClusterReduce) {
+        if constexpr (Epi::kEpiWarps > 4)
+          epi.tile_done_part(t, r, part, n0, blockIdx.z, epi_scratch, est);
+        else
+          epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
+      }
     }
   }
   __syncthreads();
@@ -303,6 +322,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
 
 // Plain epilogue base: 2-D maps, strided tiles, no B offset, one b map.
 struct TcEpiBase {
+  static constexpr int kEpiWarps = 4;
   static constexpr bool kA3D = false;
   static constexpr bool kBlocked = false;
   static constexpr bool kClusterReduce = false;
@@ -314,6 +334,11 @@ struct TcEpiBase {
 };
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The epilogue warps only (NT = 32 x their number).
+template <int NT>
+__device__ __forceinline__ void epi_bar_sync_n() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
 // Rows [r0, r1) of the cluster's Z (<= ZMAX) results (row stride ld floats,
 // at `red` in every CTA's shared memory), summed in rank order four columns
@@ -379,7 +404,7 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
     if (grid.z < 1 || grid.z > 8) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(64 + 32 * Epi::kEpiWarps);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -393,7 +418,7 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, maps, shape, epi);
   }
-  launch_pdl(kern, grid, 192, Cfg::kSmem, s, maps, shape, epi);
+  launch_pdl(kern, grid, 64 + 32 * Epi::kEpiWarps, Cfg::kSmem, s, maps, shape, epi);
   return cudaGetLastError();
 }
 
