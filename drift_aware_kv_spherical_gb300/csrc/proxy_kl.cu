@@ -10,7 +10,7 @@
 //   k_proxy         16 window rows x all C centroids per CTA, a slice of the
 //                   heads per CTA: scores, per-head softmax, head sum
 //   k_proxy_final   sums the head-slice partials, A = sum / Hq, KL
-// bf16 inputs take the tensor-core path instead (C <= 128, dh % 64 == 0):
+// bf16 inputs take the tensor-core path instead (C <= 256, dh % 64 == 0):
 //   k_split_f32     C_hat -> bf16 hi + lo
 //   tcgen05 GEMM    K~ = C_hat_hi W_k + C_hat_lo W_k, W_k streamed through
 //                   TMA as MN-major tiles, split over d for small B*C (the
@@ -18,8 +18,9 @@
 //                   chunk order through distributed shared memory); kept as
 //                   K~_hi, K~_lo
 //   tcgen05 GEMM    per (window, 128 rows, head slice): S = q K~_hi + q K~_lo
-//                   in TMEM, softmax over the C columns in the epilogue,
-//                   head sum in registers; the head slices of a row tile
+//                   in TMEM, softmax over the C columns in the epilogue (a
+//                   row's columns split over 1, 2 or 4 epilogue warps), head
+//                   sum in registers; the head slices of a row tile
 //                   (<= 8) form a thread-block cluster that sums them in
 //                   slice order through distributed shared memory, divides
 //                   by Hq and takes KL
@@ -316,6 +317,9 @@ template <int BN, int P>
 struct ProxyEpi : TcEpiBase {
   static constexpr int kEpiWarps = 4 * P;
   static constexpr int W = BN / P;  // columns per thread
+  // scores kept in registers only while they fit: above 64 columns, or with
+  // 16 epilogue warps (576 threads, <= 113 registers each), TMEM is re-read
+  static constexpr bool kReread = W > 64 || P >= 4;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   int B, N, C, Hq, G, dh, mtb, hps, nslice;
@@ -349,39 +353,57 @@ struct ProxyEpi : TcEpiBase {
     const float sl = scale * kLog2e;
     const int c0 = part * W;
     const uint32_t ta = taddr + c0;
-    if constexpr (W > 64) {  // scores re-read from TMEM (registers would spill)
+    if constexpr (kReread) {  // scores re-read from TMEM in K-column chunks
+      constexpr int K = W > 64 ? 64 : 32;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k0 = 0; k0 < W; k0 += 64) {
-        uint32_t raw[64];
-        tc::tmem_ld32_nowait(ta + k0, raw);
-        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
+      for (int k0 = 0; k0 < W; k0 += K) {
+        uint32_t raw[K];
+#pragma unroll
+        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < K; ++j)
           if (c0 + k0 + j < C) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(raw[j]) * sl);
       }
-      const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float* mx = xs + (h & 1) * (2 * 128 * P);
+      if constexpr (P > 1) {
+        mx[r * P + part] = m;
+        epi_bar_sync_n<128 * P>();
+        m = mx[r * P];
+#pragma unroll
+        for (int q = 1; q < P; ++q) m = fmaxf(m, mx[r * P + q]);
+      }
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k0 = 0; k0 < W; k0 += 64) {
-        uint32_t raw[64];
-        tc::tmem_ld32_nowait(ta + k0, raw);
-        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
+      for (int k0 = 0; k0 < W; k0 += K) {
+        uint32_t raw[K];
+#pragma unroll
+        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < K; ++j)
           if (c0 + k0 + j < C) s4[j & 3] += exp2f(fmaf(__uint_as_float(raw[j]), sl, -m));
       }
-      const float rs = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      if constexpr (P > 1) {
+        float* sm = mx + 128 * P;
+        sm[r * P + part] = sum;
+        epi_bar_sync_n<128 * P>();
+        sum = sm[r * P];
 #pragma unroll
-      for (int k0 = 0; k0 < W; k0 += 64) {
-        uint32_t raw[64];
-        tc::tmem_ld32_nowait(ta + k0, raw);
-        tc::tmem_ld32_nowait(ta + k0 + 32, raw + 32);
+        for (int q = 1; q < P; ++q) sum += sm[r * P + q];
+      }
+      const float rs = 1.0f / sum;
+#pragma unroll
+      for (int k0 = 0; k0 < W; k0 += K) {
+        uint32_t raw[K];
+#pragma unroll
+        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < K; ++j)
           if (c0 + k0 + j < C)
             st.A[k0 + j] =
                 fmaf(exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)), rs, st.A[k0 + j]);
@@ -526,7 +548,10 @@ struct ProxyClusterEpi : ProxyEpi<BN, P> {
     // cluster-read result is this CTA's own
     float* s_prev = const_cast<float*>(red) + 128 * kLd;
     const bool prev = this->A_prev != nullptr;
-    if (prev) {
+    using Cfg = TcCfg<BN, 1, 2, false>;
+    // staged when it fits in the ring past the result, else read in place
+    const bool staged = (128 * kLd + nrow * C) * 4 <= Cfg::kStages * Cfg::kStage;
+    if (prev && staged) {
       const float* src = this->A_prev + row0 * C;
       const int n = nrow * C;
       if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
@@ -556,8 +581,10 @@ struct ProxyClusterEpi : ProxyEpi<BN, P> {
         if (c < C) {
           const float a = own[r * kLd + c] / hq;
           this->A_cur[row * C + c] = a;
-          if (prev && a > 0.f)
-            kl += a * logf(a / fmaxf(s_prev[(r - r0) * C + c], 1e-30f));
+          if (prev && a > 0.f) {
+            const float ap = staged ? s_prev[(r - r0) * C + c] : this->A_prev[row * C + c];
+            kl += a * logf(a / fmaxf(ap, 1e-30f));
+          }
         }
       }
       kl = warp_sum(kl);
@@ -575,9 +602,9 @@ struct TcPlan {
 TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
   TcPlan p{};
   const int nkv = Hkv * dh;
-  p.ok = dtype == PS_BF16 && C <= 128 && dh % 64 == 0 && nkv % 64 == 0;
+  p.ok = dtype == PS_BF16 && C <= 256 && dh % 64 == 0 && nkv % 64 == 0;
   if (!p.ok) return p;
-  p.BN = C <= 32 ? 32 : (C <= 64 ? 64 : 128);
+  p.BN = C <= 32 ? 32 : (C <= 64 ? 64 : (C <= 128 ? 128 : 256));
   p.mtb = ceil_div(N, 128);
   // head slices of a row tile share one thread-block cluster: <= 8
   const int want = std::min(8, std::max(1, ceil_div(kSmTarget, B * p.mtb)));
@@ -783,7 +810,8 @@ cudaError_t proxy_run(const ProxyArgs& a, cudaStream_t s) {
     switch (p.BN) {
       case 32: return proxy_tc<32>(a, p, s);
       case 64: return proxy_tc<64>(a, p, s);
-      default: return proxy_tc<128>(a, p, s);
+      case 128: return proxy_tc<128>(a, p, s);
+      default: return proxy_tc<256>(a, p, s);
     }
   }
   return a.dtype == PS_F32 ? run_typed<float>(a, s)

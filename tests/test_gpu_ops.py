@@ -355,6 +355,28 @@ def test_proxy_one_head_slice_many_windows():
     assert_close(np_(D), oD, what="D")
 
 
+@pytest.mark.parametrize("B,N,Hq,Hkv,C", [(2, 150, 8, 2, 200), (2, 150, 2, 2, 256),
+                                          (160, 70, 4, 2, 160), (3, 200, 6, 3, 100)])
+def test_proxy_wide_c(B, N, Hq, Hkv, C):
+    """C above 128 on the tensor cores: a row's columns split over four
+    epilogue warps (C = 100: two), with 8 and 2 head slices in a cluster (the
+    2-slice case reads the previous distributions in place: they do not fit
+    the shared memory left over) and with one slice per tile (160 windows)."""
+    rng = np.random.default_rng(B * 1000 + C)
+    dh, d = 64, 128
+    Q = torch.from_numpy(rng.standard_normal((B, N, Hq, dh)).astype(np.float32))
+    Q = Q.to(torch.bfloat16).cuda()
+    chat = torch.from_numpy(rng.standard_normal((B, C, d)).astype(np.float32)).cuda()
+    Wk = torch.from_numpy((rng.standard_normal((d, Hkv * dh)) * 0.1).astype(np.float32))
+    Wk = Wk.to(torch.bfloat16).cuda()
+    prev = torch.softmax(torch.randn(B, N, C, device="cuda"), dim=2)
+    A, D = run_proxy(Q, chat, Wk, Hkv, A_prev=prev)
+    w = dataclasses.replace(wl.WORKLOADS[0], Hq=Hq, Hkv=Hkv, dh=dh)
+    oA, oD = _oracle_proxy(w, np_(Q), np_(chat), np_(Wk), np_(prev))
+    assert_close(np_(A), oA, what="A")
+    assert_close(np_(D), oD, what="D")
+
+
 def test_proxy_single_cluster():
     rng = np.random.default_rng(0)
     Q = torch.from_numpy(rng.standard_normal((1, 9, 2, 16)).astype(np.float32)).cuda()
