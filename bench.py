@@ -180,6 +180,78 @@ def op_work(w, npos_mean):
     }
 
 
+# kernel trace names (the library's kernels, as the CUDA runtime names them)
+# -> what they compute
+KERNEL_KEYS = [("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
+               ("k_inv_norm", "kmeans_inv_norm"), ("k_split_mu", "kmeans_split_mu"),
+               ("k_kpp_", "kmeans_seeding"), ("k_assign", "kmeans_assign"),
+               ("k_fp4_amax", "nvfp4_amax"), ("k_fp4_quant", "nvfp4_quant"),
+               ("Ckeys", "centroid_keys"), ("k_ckeys", "centroid_keys"),
+               ("k_split_f32", "proxy_split"), ("Proxy", "proxy_attn"),
+               ("k_proxy", "proxy_attn"), ("k_topk", "topk"), ("k_gather_rows", "refresh_gather"),
+               ("Refresh", "refresh_gemm"), ("k_refresh", "refresh_gemm"),
+               ("k_commit_scan", "commit_scan"), ("k_commit_rule", "commit_rule")]
+
+
+def kernel_key(name):
+    if "k_cluster_scan" in name:
+        return "kmeans_final" if "Lb1E" in name else "kmeans_update"
+    for pat, key in KERNEL_KEYS:
+        if pat in name:
+            return key
+    return name[:48]
+
+
+def kernel_work(key, w, npos_mean):
+    """Algorithmic bytes and flops of one launch of a kernel, or None."""
+    esz = 4 if w.dtype == "f32" else 2
+    B, N, d, C = w.B, w.N, w.d, w.C
+    nkv = w.Hkv * w.dh
+    H = B * N * d * esz
+    M = npos_mean * B
+    return {
+        "kmeans_assign": (H + B * C * d * 4, 2.0 * B * N * C * d),
+        "kmeans_update": (H + B * C * d * 4, 0.0),
+        "kmeans_final": (B * N * 4 + 2 * B * C * d * 4, 0.0),
+        "nvfp4_amax": (H, 0.0),
+        "nvfp4_quant": (H + B * N * d // 2 + B * N * d // 16, 0.0),
+        "centroid_keys": (d * nkv * esz + B * C * d * 4, 2.0 * B * C * d * nkv),
+        "proxy_attn": (B * N * w.Hq * w.dh * esz + 2 * B * N * C * 4,
+                       2.0 * B * N * w.Hq * C * w.dh),
+        "topk": (B * N * 13, 0.0),
+        "refresh_gather": (2 * M * d * esz, 0.0),
+        "refresh_gemm": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
+        "commit_scan": (B * w.P * w.V * 4, 0.0),
+    }.get(key)
+
+
+def kernel_rooflines(records, nsteps, w, npos_mean, hbm, tf):
+    """Per kernel: launches and time per step, average launch time and its
+    algorithmic roofline fraction."""
+    agg = {}
+    for name, ms in records:
+        k = kernel_key(name)
+        a = agg.setdefault(k, [0, 0.0])
+        a[0] += 1
+        a[1] += ms
+    out = {}
+    for k, (n, ms) in agg.items():
+        row = {"launches_per_step": n / nsteps, "us_per_step": 1e3 * ms / nsteps,
+               "us_per_launch": 1e3 * ms / n}
+        work = kernel_work(k, w, npos_mean)
+        if work is not None:
+            by, fl = work
+            sec = ms / n * 1e-3
+            tensor = fl / (tf * 1e12) > by / (hbm * 1e9)
+            ach = fl / sec / 1e12 if tensor else by / sec / 1e9
+            row.update({"bound": "tensor" if tensor else "hbm", "achieved": ach,
+                        "peak": tf if tensor else hbm, "unit": "TFLOP/s" if tensor else "GB/s",
+                        "frac": ach / (tf if tensor else hbm), "alg_bytes": by,
+                        "alg_flops": fl})
+        out[k] = {kk: (round(v, 6) if isinstance(v, float) else v) for kk, v in row.items()}
+    return out
+
+
 def run_reference(args):
     """The CPU oracle, as it stands, timed on this host on the same workload."""
     import numpy as np
@@ -422,6 +494,21 @@ def main():
     per_op = {op: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, op in enumerate(ops)}
     eager_ms = statistics.mean(ev[0].elapsed_time(ev[6]) for ev in events)
 
+    # per kernel: the library's own trace (CUDA events around each of its
+    # launches, on the launching stream) over a few more eager steps
+    ntrace = min(3, args.steps)
+    ps.ps_trace_enable(True)
+    for t in range(ntrace):
+        load(step_no)
+        flush.zero_()
+        torch.cuda._sleep(4_000_000)
+        op_calls(step_no % 2)
+        step_no += 1
+    torch.cuda.synchronize()
+    trace = ps.ps_trace_records()
+    ps.ps_trace_enable(False)
+    ps.ps_check()
+
     # end to end through the public API: inputs from pinned host memory every
     # step, the step's results read back
     hH = [H.cpu().pin_memory() for H in Hs]
@@ -468,14 +555,18 @@ def main():
         rows[op] = {"ms": ms, "bound": bound, "achieved": ach, "peak": peak,
                     "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": ach / peak,
                     "alg_bytes": by, "alg_flops": fl}
-    top = max(ops, key=lambda o: rows[o]["ms"])
+    kernels = kernel_rooflines(trace, ntrace, w, npos_seen[-1] / w.B, hbm, tf)
+    # the dominant kernel: most device time per step among those with a
+    # stated algorithmic workload
+    top = max((k for k in kernels if "frac" in kernels[k]),
+              key=lambda k: kernels[k]["us_per_step"])
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         tj = json.load(open(tpath))
         if tj.get("source_hash") == source_hash() and top in tj.get("per_launch_bytes", {}):
             traffic = tj["per_launch_bytes"][top]
-    r = rows[top]
+    r = kernels[top]
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -486,7 +577,11 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
                      "unit": r["unit"], "frac": r["frac"], "traffic": traffic,
-                     "op": top, "peak_source": src},
+                     "kernel": top, "us_per_launch": r["us_per_launch"],
+                     "launches_per_step": r["launches_per_step"],
+                     "alg_bytes_per_launch": r["alg_bytes"],
+                     "alg_flops_per_launch": r["alg_flops"], "peak_source": src},
+        "kernels": kernels,
         "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
                 for op in ops},
         "clocks": clk,

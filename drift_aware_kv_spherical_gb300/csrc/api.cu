@@ -5,8 +5,46 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "ops.h"
+
+namespace ps {
+
+struct TraceRec {
+  const void* kernel;
+  cudaEvent_t a, b;
+};
+struct TraceSink {
+  std::vector<TraceRec> recs;
+  cudaEvent_t pending = nullptr;
+};
+
+// The calling thread's sink while it runs a ps_* call on a tracing handle.
+thread_local TraceSink* g_trace = nullptr;
+
+void trace_begin(cudaStream_t s) {
+  if (g_trace == nullptr) return;
+  cudaEvent_t a;
+  if (cudaEventCreate(&a) != cudaSuccess) return;
+  cudaEventRecord(a, s);
+  g_trace->pending = a;
+}
+
+void trace_end(cudaStream_t s, const void* kernel) {
+  if (g_trace == nullptr || g_trace->pending == nullptr) return;
+  cudaEvent_t b;
+  if (cudaEventCreate(&b) != cudaSuccess) {
+    cudaEventDestroy(g_trace->pending);
+    g_trace->pending = nullptr;
+    return;
+  }
+  cudaEventRecord(b, s);
+  g_trace->recs.push_back({kernel, g_trace->pending, b});
+  g_trace->pending = nullptr;
+}
+
+}  // namespace ps
 
 using namespace ps;
 
@@ -42,6 +80,20 @@ ps_status check_ws(size_t need, const void* ws, size_t ws_bytes) {
 
 bool dtype_ok(int dt) { return dt == PS_F32 || dt == PS_BF16; }
 
+// Sets the calling thread's trace sink for the duration of one ps_* call.
+struct TraceScope {
+  explicit TraceScope(ps_handle h) { g_trace = h != nullptr ? h->trace : nullptr; }
+  ~TraceScope() { g_trace = nullptr; }
+};
+
+void trace_clear(TraceSink* t) {
+  for (auto& r : t->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  t->recs.clear();
+}
+
 constexpr int kMaxC = 256;
 constexpr int kMaxD = 8192;
 constexpr int kMaxDh = 256;
@@ -67,6 +119,7 @@ ps_status ps_create(int device, ps_handle* out) {
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
   h->status = nullptr;
+  h->trace = nullptr;
   e = cudaMalloc(&h->status, 16);
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
   if (e != cudaSuccess) {
@@ -80,6 +133,10 @@ ps_status ps_create(int device, ps_handle* out) {
 
 ps_status ps_destroy(ps_handle h) {
   if (h == nullptr) return PS_ERR_ARG;
+  if (h->trace != nullptr) {
+    trace_clear(h->trace);
+    delete h->trace;
+  }
   cudaFree(h->status);
   delete h;
   return PS_OK;
@@ -116,6 +173,35 @@ const char* ps_status_string(ps_status s) {
 
 const char* ps_last_cuda_error(void) { return g_last_cuda_error; }
 
+ps_status ps_trace_enable(ps_handle h, int enable) {
+  if (h == nullptr) return PS_ERR_ARG;
+  if (h->trace != nullptr) {
+    trace_clear(h->trace);
+    delete h->trace;
+    h->trace = nullptr;
+  }
+  if (enable) {
+    h->trace = new (std::nothrow) TraceSink;
+    if (h->trace == nullptr) return PS_ERR_CUDA;
+  }
+  return PS_OK;
+}
+
+int ps_trace_count(ps_handle h) {
+  return h != nullptr && h->trace != nullptr ? static_cast<int>(h->trace->recs.size()) : 0;
+}
+
+ps_status ps_trace_get(ps_handle h, int i, const char** name, float* ms) {
+  if (h == nullptr || h->trace == nullptr || name == nullptr || ms == nullptr || i < 0 ||
+      i >= static_cast<int>(h->trace->recs.size()))
+    return PS_ERR_ARG;
+  const TraceRec& r = h->trace->recs[i];
+  cudaError_t e = cudaEventSynchronize(r.b);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, r.a, r.b);
+  if (e == cudaSuccess) e = cudaFuncGetName(name, r.kernel);
+  return launch_status(e);
+}
+
 size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
                           int dh, int k, int P, int V) {
   (void)k;
@@ -140,6 +226,7 @@ ps_status ps_kmeans_spherical(ps_handle h, const void* H, int dtype, int B,
                               float* rho, float* chat, int32_t* counts,
                               float* objective, void* ws, size_t ws_bytes,
                               void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && dtype_ok(dtype));
   PS_REQUIRE(B >= 0 && iters >= 0 && (init_mode == 0 || init_mode == 1));
   if (B == 0) return PS_OK;
@@ -162,6 +249,7 @@ ps_status ps_nvfp4_residual(ps_handle h, const void* H, int dtype,
                             uint8_t* codes, uint8_t* scales,
                             float* tensor_scale, void* ws, size_t ws_bytes,
                             void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && dtype_ok(dtype));
   PS_REQUIRE(B >= 0);
   if (B == 0) return PS_OK;
@@ -186,6 +274,7 @@ ps_status ps_proxy_attn_kl(ps_handle h, const void* Q, const float* chat,
                            int C, int Hq, int Hkv, int dh, const float* A_prev,
                            float* A_cur, float* D, void* ws, size_t ws_bytes,
                            void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && dtype_ok(dtype));
   PS_REQUIRE(B >= 0);
   if (B == 0) return PS_OK;
@@ -206,6 +295,7 @@ ps_status ps_topk_drift(ps_handle h, const float* D, const int32_t* assign,
                         int32_t* sel, float* sel_score, int32_t* pos,
                         int32_t* npos, uint8_t* posmask, void* ws,
                         size_t ws_bytes, void* stream) {
+  TraceScope trace_scope(h);
   (void)ws; (void)ws_bytes;
   PS_REQUIRE(h != nullptr && B >= 0);
   if (B == 0) return PS_OK;
@@ -223,6 +313,7 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
                         int Hkv, int dh, void* Kcache, void* Vcache,
                         int Ncache, int cache_off, void* ws, size_t ws_bytes,
                         void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && dtype_ok(dtype) && B >= 0);
   if (B == 0) return PS_OK;
   PS_REQUIRE(N >= 1 && d > 0 && d % 16 == 0 && Hkv >= 1 && dh > 0 && dh % 16 == 0);
@@ -247,6 +338,7 @@ ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
                     float* d_prev, const uint8_t* suffix_sel, int sel_ld,
                     ps_commit_params params, int32_t* token, float* conf,
                     uint8_t* commit, void* ws, size_t ws_bytes, void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && B >= 0 && P >= 0);
   if (B == 0 || P == 0) return PS_OK;
   PS_REQUIRE(P <= 1024 && V >= 4 && V % 4 == 0 && (long)B * P <= 65535);
@@ -271,6 +363,7 @@ extern "C" ps_status ps_nvfp4_residual_noalloc(
     ps_handle h, const void* H, int dtype, const float* mu, const int32_t* assign,
     const float* rho, int B, int N, int d, int C, uint8_t* codes, uint8_t* scales,
     float* tensor_scale, void* stream) {
+  TraceScope trace_scope(h);
   PS_REQUIRE(h != nullptr && dtype_ok(dtype));
   PS_REQUIRE(B >= 0);
   if (B == 0) return PS_OK;

@@ -9,10 +9,15 @@
 
 #include "../../include/polestar.h"
 
+namespace ps {
+struct TraceSink;
+}
+
 struct ps_handle_s {
   int device;
   int num_sms;
   int* status;  // device word: 0 ok, else a PS_ERR_* code set by a kernel
+  ps::TraceSink* trace;  // non-null while ps_trace_enable is on
 };
 
 namespace ps {
@@ -78,6 +83,21 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Kernel trace (ps_trace_enable): while the calling thread runs a ps_* call
+// on a handle with tracing on, every launch below is bracketed by two CUDA
+// events on its stream.  Defined in api.cu.
+void trace_begin(cudaStream_t s);
+void trace_end(cudaStream_t s, const void* kernel);
+
+// Every kernel of the library is launched here.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(const cudaLaunchConfig_t& cfg, void (*kernel)(KArgs...), Args&&... args) {
+  trace_begin(cfg.stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  trace_end(cfg.stream, reinterpret_cast<const void*>(kernel));
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
@@ -91,7 +111,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = kUsePdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return launch_ex(cfg, kernel, std::forward<Args>(args)...);
 }
 
 __host__ __device__ inline int ceil_div(long a, long b) { return (int)((a + b - 1) / b); }

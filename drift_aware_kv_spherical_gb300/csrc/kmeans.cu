@@ -713,10 +713,9 @@ cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&.
   attr[1].val.clusterDim.z = p.S;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return p.G == 1
-             ? cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL, 1>, std::forward<Args>(args)...)
-             : cudaLaunchKernelEx(&cfg, k_cluster_scan<T, FINAL, kMaxColGroups>,
-                                  std::forward<Args>(args)...);
+  return p.G == 1 ? launch_ex(cfg, k_cluster_scan<T, FINAL, 1>, std::forward<Args>(args)...)
+                  : launch_ex(cfg, k_cluster_scan<T, FINAL, kMaxColGroups>,
+                              std::forward<Args>(args)...);
 }
 
 struct KmPlan {

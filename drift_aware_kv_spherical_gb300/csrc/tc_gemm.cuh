@@ -416,7 +416,7 @@ cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi
     attr[1].val.clusterDim.z = grid.z;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, maps, shape, epi);
+    return launch_ex(cfg, kern, maps, shape, epi);
   }
   launch_pdl(kern, grid, 64 + 32 * Epi::kEpiWarps, Cfg::kSmem, s, maps, shape, epi);
   return cudaGetLastError();

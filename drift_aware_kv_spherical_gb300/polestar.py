@@ -18,6 +18,7 @@ PS_OK, PS_ERR_ARG, PS_ERR_UNSUPPORTED, PS_ERR_WORKSPACE, PS_ERR_CUDA, PS_ERR_TIM
 PS_F32, PS_BF16 = 0, 1
 OP_KMEANS, OP_NVFP4, OP_PROXY_KL, OP_TOPK, OP_REFRESH, OP_COMMIT = range(6)
 EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_cuda_error",
+            "ps_trace_enable", "ps_trace_count", "ps_trace_get",
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
             "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit"]
 
@@ -48,6 +49,10 @@ _SIGS = {
     "ps_check": (_i, [_p, _p, _i]),
     "ps_status_string": (ctypes.c_char_p, [_i]),
     "ps_last_cuda_error": (ctypes.c_char_p, []),
+    "ps_trace_enable": (_i, [_p, _i]),
+    "ps_trace_count": (_i, [_p]),
+    "ps_trace_get": (_i, [_p, _i, ctypes.POINTER(ctypes.c_char_p),
+                          ctypes.POINTER(ctypes.c_float)]),
     "ps_workspace_bytes": (_sz, [_i] * 11),
     "ps_kmeans_spherical": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                                  _p, _p, _p, _p, _p, _sz, _p]),
@@ -247,3 +252,23 @@ def ps_nvfp4_residual_noalloc(H, mu, assign, rho, codes, scales, tensor_scale,
     st = fn(lib.handle(), _ptr(H), _dtype(H), _ptr(mu), _ptr(assign), _ptr(rho), B, N,
             d, C, _ptr(codes), _ptr(scales), _ptr(tensor_scale), _stream(stream))
     _check(st, "ps_nvfp4_residual_noalloc")
+
+
+def ps_trace_enable(enable=True):
+    """Start (clearing earlier records) or stop the library's kernel trace."""
+    lib = _lib()
+    _check(lib.cdll.ps_trace_enable(lib.handle(), int(bool(enable))), "ps_trace_enable")
+
+
+def ps_trace_records():
+    """[(kernel name, ms)] for every kernel launched since tracing was enabled,
+    in launch order (waits for them to finish)."""
+    lib = _lib()
+    out = []
+    for i in range(lib.cdll.ps_trace_count(lib.handle())):
+        name = ctypes.c_char_p()
+        ms = ctypes.c_float()
+        _check(lib.cdll.ps_trace_get(lib.handle(), i, ctypes.byref(name), ctypes.byref(ms)),
+               "ps_trace_get")
+        out.append((name.value.decode(), ms.value))
+    return out

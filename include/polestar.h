@@ -80,6 +80,22 @@ const char* ps_status_string(ps_status s);
  * until the thread's next call that fails with PS_ERR_CUDA. */
 const char* ps_last_cuda_error(void);
 
+/* Kernel trace, for diagnostics (no counterpart in the paper).  While it is
+ * enabled on a handle, every kernel a ps_* call on that handle launches is
+ * bracketed by two CUDA events on the call's stream, kept in host memory the
+ * handle owns.  Enabling (enable != 0) or disabling discards earlier
+ * records.  Not for calls made while the stream is captured into a CUDA
+ * graph.  PS_ERR_ARG for a NULL handle. */
+ps_status ps_trace_enable(ps_handle h, int enable);
+/* Number of kernels recorded since tracing was enabled (0 when it is off). */
+int ps_trace_count(ps_handle h);
+/* Record i (0-based, in launch order): the kernel's name and its duration in
+ * milliseconds; waits for the kernel to finish.  The name is owned by the
+ * CUDA runtime and stays valid while the library is loaded.  PS_ERR_ARG for
+ * an index out of range or NULL outputs, PS_ERR_CUDA if an event query
+ * fails. */
+ps_status ps_trace_get(ps_handle h, int i, const char** name, float* ms);
+
 /* Workspace bytes `op` needs for these sizes (arguments an op does not use
  * are ignored).  0 means ws may be NULL. */
 size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,

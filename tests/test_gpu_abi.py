@@ -82,3 +82,28 @@ def test_topk_and_commit_reject_bad_k_and_mode(lib):
 def test_check_reports_ok_after_work(lib):
     cd, h = _lib_handle(lib)
     assert cd.ps_check(h, torch.cuda.current_stream().cuda_stream, 1) == ps.PS_OK
+
+
+def test_kernel_trace_records_every_launch(lib):
+    """The diagnostic trace brackets each launch of a call with events: a
+    k-means call with I passes on the tensor-core path records its launches
+    in order with positive durations; disabling clears the records."""
+    H = torch.randn(1, 300, 256, device="cuda").to(torch.bfloat16)
+    mu = torch.nn.functional.normalize(torch.randn(1, 24, 256, device="cuda"), dim=2)
+    a = torch.zeros(1, 300, dtype=torch.int32, device="cuda")
+    rho = torch.zeros(1, 300, device="cuda")
+    chat = torch.zeros(1, 24, 256, device="cuda")
+    n = torch.zeros(1, 24, dtype=torch.int32, device="cuda")
+    ws = ps.workspace(ps.OP_KMEANS, B=1, N=300, d=256, C=24)
+    ps.ps_trace_enable(True)
+    ps.ps_kmeans_spherical(H, mu, a, rho, chat, n, 3, ws=ws)
+    rec = ps.ps_trace_records()
+    ps.ps_check()
+    names = [r[0] for r in rec]
+    assert sum("k_tc_gemm" in x for x in names) == 4             # I + 1 assignment passes
+    assert sum("k_cluster_scan" in x for x in names) == 4        # 3 updates + the final pass
+    assert all(ms > 0 for _, ms in rec)
+    ps.ps_trace_enable(False)
+    assert lib.cdll.ps_trace_count(lib.handle()) == 0
+    ps.ps_kmeans_spherical(H, mu, a, rho, chat, n, 3, ws=ws)     # untraced calls record nothing
+    assert lib.cdll.ps_trace_count(lib.handle()) == 0
