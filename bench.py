@@ -435,13 +435,24 @@ def main():
     torch.cuda.synchronize()
     ps.ps_check()
 
-    # capture one graph per A ping-pong parity
+    # capture one graph per A ping-pong parity: the pipeline's step with the
+    # ops off the critical path (NVFP4, commit) on side streams
+    def concurrent_step(parity):
+        pipe.t = parity          # A[parity] is this step's distribution
+        pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL, concurrent=True)
+
+    for t in range(2):           # side streams warmed up eagerly
+        load(step_no)
+        concurrent_step(step_no % 2)
+        step_no += 1
+    torch.cuda.synchronize()
+    ps.ps_check()
     graphs = []
     cap = torch.cuda.Stream(dev)
     for parity in (0, 1):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
-            op_calls(parity)
+            concurrent_step(parity)
         graphs.append(g)
     launches = graph_kernel_count(graphs[0])
     if launches is None:                            # runtime not reachable: plan count

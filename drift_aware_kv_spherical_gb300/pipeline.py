@@ -67,6 +67,14 @@ class Pipeline:
         self.commit = torch.zeros(B, P, dtype=torch.uint8, device=device)
         self.params = ps.CommitParams(w.tau_s, w.alpha, w.ratio, w.mode, 1)
         self.t = 0
+        self._side = None
+        self._after_proxy = None
+
+    def side_streams(self):
+        """Two streams for the ops off the critical path (NVFP4, commit)."""
+        if self._side is None:
+            self._side = [torch.cuda.Stream(self.device), torch.cuda.Stream(self.device)]
+        return self._side
 
     def reset_block(self):
         self.undecided.fill_(1)
@@ -74,17 +82,31 @@ class Pipeline:
         self.d_cnt.zero_()
         self.d_prev.zero_()
 
-    def layer_step(self, l, H, Q, Wk, Wv, init_u=None, first=False, stream=None):
+    def layer_step(self, l, H, Q, Wk, Wv, init_u=None, first=False, stream=None,
+                   concurrent=False, joins=None):
+        """One layer.  concurrent: the NVFP4 residuals run on a side stream
+        (they depend on k-means only), and the event that ends them is
+        appended to `joins` for the caller to wait on."""
         w, st = self.w, self.state[l]
         cur, prev = st.A[self.t % 2], st.A[(self.t + 1) % 2]
         ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts,
                                w.iters, init_mode=1 if first else 0, init_u=init_u,
                                objective=st.obj, ws=self.ws[ps.OP_KMEANS],
                                stream=stream)
-        ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
-                             ws=self.ws[ps.OP_NVFP4], stream=stream)
+        if concurrent:
+            main = stream if stream is not None else torch.cuda.current_stream(self.device)
+            side = self.side_streams()[0]
+            side.wait_event(main.record_event())
+            ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                                 ws=self.ws[ps.OP_NVFP4], stream=side)
+            joins.append(side.record_event())
+        else:
+            ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                                 ws=self.ws[ps.OP_NVFP4], stream=stream)
         ps.ps_proxy_attn_kl(Q, st.chat, Wk, None if first else prev, cur, st.D, w.Hkv,
                             ws=self.ws[ps.OP_PROXY_KL], stream=stream)
+        if concurrent:  # the drift is final here: the commit may start
+            self._after_proxy = main.record_event()
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
                          st.npos, st.posmask, ws=self.ws[ps.OP_TOPK], stream=stream)
         ps.ps_refresh_kv(H, st.pos, st.npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
@@ -97,12 +119,29 @@ class Pipeline:
                      self.d_cnt, self.d_prev, None, w.P, self.params, self.token,
                      self.conf, self.commit, ws=self.ws[ps.OP_COMMIT], stream=stream)
 
-    def step(self, Hs, Qs, Wks, Wvs, logits, init_us=None, first=False, stream=None):
-        """Hs/Qs/Wks/Wvs: per-layer tensors (lists of length `layers`)."""
+    def step(self, Hs, Qs, Wks, Wvs, logits, init_us=None, first=False, stream=None,
+             concurrent=False):
+        """Hs/Qs/Wks/Wvs: per-layer tensors (lists of length `layers`).
+
+        concurrent: the ops off the critical path (each layer's NVFP4
+        residuals, the commit after the last layer's proxy) run on side
+        streams joined back into `stream` before the step ends; the results
+        are the same."""
+        joins = []
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
         for l in range(self.layers):
             self.layer_step(l, Hs[l], Qs[l], Wks[l], Wvs[l],
-                            None if init_us is None else init_us[l], first, stream)
-        self.commit_step(logits, stream)
+                            None if init_us is None else init_us[l], first, stream,
+                            concurrent, joins)
+        if concurrent:  # needs the last layer's drift only: overlaps its top-k and refresh
+            side = self.side_streams()[1]
+            side.wait_event(self._after_proxy)
+            self.commit_step(logits, side)
+            joins.append(side.record_event())
+            for ev in joins:
+                main.wait_event(ev)
+        else:
+            self.commit_step(logits, stream)
         self.t += 1
 
     def kernel_launches_per_step(self):

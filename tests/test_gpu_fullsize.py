@@ -138,3 +138,28 @@ def test_loop_and_stress_layers_sampled(widx, B, sample):
         assert np.all((npos > 0) & (npos <= w.N))
     for b in sample:
         _check_window(w, L, Hs[1], Qs[1], snaps[1], b)
+
+
+def test_concurrent_step_matches_sequential():
+    """The step with NVFP4 and the commit on side streams (as the bench
+    captures it) gives bit-identical outputs to the single-stream step."""
+    w, L, Q = _one_layer(1)
+    u = wl.make_uniforms(w, 0, "cuda")
+    logits = wl.make_logits(w, 0, "cuda")
+    H1 = wl.drift_rows(w, L["H"], 1)
+    Q1 = wl.make_queries(w, H1, L["Wq"])
+    outs = []
+    for concurrent in (False, True):
+        pipe = Pipeline(w, layers=1)
+        pipe.step([L["H"]], [Q], [L["Wk"]], [L["Wv"]], logits, init_us=[u], first=True,
+                  concurrent=concurrent)
+        pipe.step([H1], [Q1], [L["Wk"]], [L["Wv"]], logits, concurrent=concurrent)
+        torch.cuda.synchronize()
+        ps.ps_check()
+        st = pipe.state[0]
+        outs.append([x.clone() for x in (st.mu, st.assign, st.chat, st.codes, st.scales, st.S,
+                                         st.A[0], st.A[1], st.D, st.pos, st.npos, st.Kc,
+                                         st.Vc, pipe.token, pipe.conf, pipe.commit,
+                                         pipe.undecided, pipe.d_sum, pipe.d_cnt)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
