@@ -183,7 +183,7 @@ def op_work(w, npos_mean):
 # kernel trace names (the library's kernels, as the CUDA runtime names them)
 # -> what they compute
 KERNEL_KEYS = [("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
-               ("k_inv_norm", "kmeans_inv_norm"), ("k_split_mu", "kmeans_split_mu"),
+               ("k_km_prep", "kmeans_prep"),
                ("k_kpp_", "kmeans_seeding"), ("k_assign", "kmeans_assign"),
                ("k_fp4_amax", "nvfp4_amax"), ("k_fp4_quant", "nvfp4_quant"),
                ("Ckeys", "centroid_keys"), ("k_ckeys", "centroid_keys"),

@@ -6,10 +6,10 @@
 // sum of unit rows.  Deterministic: every reduction runs in a fixed order.
 //
 // Kernels (one launch each, all on the caller's stream):
-//   k_inv_norm      1/||h_i||                                (one warp per row)
+//   k_km_prep       1/||h_i|| (one warp per row) and the bf16 split of mu
+//                   for the tensor cores, one launch
 //   k_kpp_pick      k-means++ centre r, one CTA per window   (init_mode 1)
 //   k_kpp_weights   weights against centre r, warp per row   (C - 1 rounds)
-//   k_split_mu      mu -> (mu_hi, mu_lo) bf16 for the tensor cores
 //   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
 //                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
 //                   d when the windows give too few row tiles.  The d-chunks
@@ -37,25 +37,6 @@ constexpr int kTileRows = 64;    // rows per assignment tile
 constexpr int kTileC = 128;      // centroids per chunk of an assignment tile
 constexpr int kTileK = 32;       // d per shared-memory stage
 
-template <typename T>
-__global__ void k_inv_norm(const T* __restrict__ H, long rows, int d,
-                           float* __restrict__ inv) {
-  pdl_prologue();
-  constexpr int V = Vec<T>::n;
-  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const T* h = H + row * d;
-  float ss = 0.f;
-  for (int k = lane * V; k < d; k += 32 * V) {
-    float v[V];
-    load16(h + k, v);
-#pragma unroll
-    for (int e = 0; e < V; ++e) ss = fmaf(v[e], v[e], ss);
-  }
-  ss = warp_sum(ss);
-  if (lane == 0) inv[row] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
-}
 
 // k-means++ on the sphere, one round r at a time: k_kpp_pick chooses centre
 // r (one CTA per window), then k_kpp_weights lowers every row's weight to
@@ -271,16 +252,48 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
   }
 }
 
-// fp32 centroids -> bf16 hi + lo parts (hi = bf16(mu), lo = bf16(mu - hi)).
-__global__ void k_split_mu(const float* __restrict__ mu, long n, __nv_bfloat16* __restrict__ hi,
-                           __nv_bfloat16* __restrict__ lo) {
+// Set-up of a call, in one launch: blocks [0, inv_blocks) take 1/||h_i||
+// for 8 rows each (a warp per row, its 16-byte loads unrolled four deep);
+// the rest split mu (fp32) into bf16 hi + lo parts (hi = bf16(mu), lo =
+// bf16(mu - hi)), four values per thread.  Either part may be empty.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, int inv_blocks,
+          const float* __restrict__ mu, long n_mu, __nv_bfloat16* __restrict__ hi,
+          __nv_bfloat16* __restrict__ lo) {
   pdl_prologue();
-  const long stride = (long)gridDim.x * blockDim.x;
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const float x = mu[i];
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi[i] = h;
-    lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+  if ((int)blockIdx.x < inv_blocks) {
+    constexpr int V = Vec<T>::n;
+    const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const T* h = H + row * d;
+    float ss = 0.f;
+#pragma unroll 4
+    for (int k = lane * V; k < d; k += 32 * V) {
+      float v[V];
+      load16(h + k, v);
+#pragma unroll
+      for (int e = 0; e < V; ++e) ss = fmaf(v[e], v[e], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) inv[row] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    return;
+  }
+  const long n4 = n_mu >> 2;  // n_mu = B * C * d, a multiple of 16
+  const long stride = (long)(gridDim.x - inv_blocks) * blockDim.x;
+  for (long i = (long)(blockIdx.x - inv_blocks) * blockDim.x + threadIdx.x; i < n4;
+       i += stride) {
+    const float4 x = reinterpret_cast<const float4*>(mu)[i];
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
+    reinterpret_cast<uint2*>(hi)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                 *reinterpret_cast<const uint32_t*>(&h1));
+    reinterpret_cast<uint2*>(lo)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
+                                                 *reinterpret_cast<const uint32_t*>(&l1));
   }
 }
 
@@ -816,8 +829,15 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const KmWs w = km_carve(a.ws, p, a.B, a.N, a.d, a.C, nullptr);
   const ScanPlan sp = scan_plan<T>(a.B, a.d, a.C);
 
-  launch_pdl(k_inv_norm<T>, ceil_div(BN_ * 32, 256), 256, 0, s, H, BN_, a.d, w.inv);
-  if (a.init_mode == 1) {
+  // 1/||h|| and (tensor cores) the split of the given centroids in one
+  // launch; with k-means++ seeding the split waits for the seeds
+  const int inv_blocks = ceil_div(BN_ * 32, 256);
+  const long n_mu = p.tc ? (long)a.B * a.C * a.d : 0;
+  const int split_blocks = n_mu > 0 ? std::min(ceil_div(n_mu / 4, 256), 2 * kSmTarget) : 0;
+  const bool seeding = a.init_mode == 1;
+  launch_pdl(k_km_prep<T>, inv_blocks + (seeding ? 0 : split_blocks), 256, 0, s, H, BN_, a.d,
+             w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, w.mu_hi, w.mu_lo);
+  if (seeding) {
     for (int r = 0; r < a.C; ++r) {
       launch_pdl(k_kpp_pick<T>, a.B, 1024, 0, s, H, w.inv, a.init_u, a.N, a.d, a.C, r, a.mu,
                  w.w, w.chosen);
@@ -825,11 +845,9 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
         launch_pdl(k_kpp_weights<T>, ceil_div(BN_ * 32, 256), 256, 0, s, H, w.inv, a.B, a.N,
                    a.d, a.C, r, a.mu, w.w, w.chosen);
     }
-  }
-  if (p.tc) {
-    const long n = (long)a.B * a.C * a.d;
-    launch_pdl(k_split_mu, std::min(ceil_div(n, 256), 4 * kSmTarget), 256, 0, s, a.mu, n, w.mu_hi,
-                                                                         w.mu_lo);
+    if (split_blocks > 0)
+      launch_pdl(k_km_prep<T>, split_blocks, 256, 0, s, H, 0L, a.d, w.inv, 0, a.mu, n_mu,
+                 w.mu_hi, w.mu_lo);
   }
   for (int t = 0; t <= a.iters; ++t) {
     cudaError_t e = cudaSuccess;
