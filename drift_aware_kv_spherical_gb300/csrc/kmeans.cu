@@ -309,6 +309,7 @@ struct KmAssignEpi : TcEpiBase {
   int32_t* assign;
   float* best;
   float* objp;
+  float* scores;  // nullable: [B][N][C] cosines of the pass
   struct State {
     float bv;
     int bi;
@@ -321,6 +322,8 @@ struct KmAssignEpi : TcEpiBase {
     st.bv = -INFINITY;
     st.bi = INT_MAX;
     float* dst = part + ((long)z * B * N + (long)b * N + i) * C;
+    const bool keep = nz == 1 && scores != nullptr && i < N;
+    const float iv = keep ? inv[(long)b * N + i] : 0.f;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       float v[32];
@@ -329,6 +332,12 @@ struct KmAssignEpi : TcEpiBase {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (c0 + j < C && v[j] > st.bv) { st.bv = v[j]; st.bi = c0 + j; }
+        if (keep) {
+          float* so = scores + ((long)b * N + i) * C;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < C) so[c0 + j] = v[j] * iv;
+        }
       } else if (i < N) {
         if (c0 + 32 <= C && (C & 3) == 0) {
 #pragma unroll
@@ -377,6 +386,7 @@ struct KmAssignClusterEpi : TcEpiBase {
   int32_t* assign;
   float* best;
   float* objp;
+  float* scores;  // nullable: [B][N][C] cosines of the pass
   struct State {};
   __device__ int tiles(int) const { return B * mtb; }
   __device__ int arow(int t) const { return (t / mtb) * N + (t % mtb) * 128; }
@@ -420,6 +430,8 @@ struct KmAssignClusterEpi : TcEpiBase {
         const int c = lane + 32 * j;
         const float v = own[r * kLd + c];
         if (c < C && v > bv) { bv = v; bi = c; }
+        if (scores != nullptr && c < C && i < N)
+          scores[((long)b * N + i) * C + c] = v * s_inv[r - r0];
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -455,7 +467,7 @@ struct KmAssignClusterEpi : TcEpiBase {
 __global__ void __launch_bounds__(256)
 k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
             const float* __restrict__ inv, int32_t* __restrict__ assign,
-            float* __restrict__ best, float* __restrict__ objp) {
+            float* __restrict__ best, float* __restrict__ objp, float* __restrict__ scores) {
   pdl_prologue();
   __shared__ float s_cos[8];
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -470,6 +482,7 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
       float sum = 0.f;
       for (int z = 0; z < nz; ++z) sum += __ldcg(part + z * zs + row * C + c);
       if (sum > bv) { bv = sum; bi = c; }
+      if (scores != nullptr) scores[row * C + c] = sum * inv[row];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -731,6 +744,13 @@ cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&.
                               std::forward<Args>(args)...);
 }
 
+// PS_KMEANS_LLOYD set in the environment keeps every pass in the Lloyd form
+// (centroid update + tensor-core assignment), for comparing the two forms.
+bool kmeans_lloyd_forced() {
+  static const bool forced = std::getenv("PS_KMEANS_LLOYD") != nullptr;
+  return forced;
+}
+
 struct KmPlan {
   bool tc;
   bool cluster;  // d-chunks reduced inside a thread-block cluster
@@ -774,9 +794,13 @@ struct KmWs {
   __nv_bfloat16* mu_hi;
   __nv_bfloat16* mu_lo;
   float* part;
+  float* L;        // Gram form: [B][N][C] cosines carried for kept centroids
+  int16_t* qhi;    // Gram form: fixed-point Gram matrices, high and low parts
+  uint8_t* qlo;
 };
 
-KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* bytes) {
+KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int d, int C,
+              size_t* bytes) {
   Carver cv(base);
   KmWs w{};
   const long BN_ = (long)B * N;
@@ -789,12 +813,19 @@ KmWs km_carve(void* base, const KmPlan& p, int B, int N, int d, int C, size_t* b
     w.mu_lo = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.part = p.nz > 1 && !p.cluster ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
   }
+  if (g.ok) {
+    const size_t q = (size_t)B * g.Z * N * g.R;
+    w.L = cv.take<float>((size_t)BN_ * C);
+    w.qhi = cv.take<int16_t>(q);
+    w.qlo = cv.take<uint8_t>(q);
+  }
   if (bytes != nullptr) *bytes = cv.bytes();
   return w;
 }
 
 template <int BN>
-cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaStream_t s) {
+cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, float* scores,
+                      cudaStream_t s) {
   TcMaps maps;
   const long rows = (long)a.B * a.N;
   if (!make_tmap_bf16_2d(&maps.a[0], a.H, a.d, rows, (uint64_t)a.d * 2, 64, 128) ||
@@ -807,17 +838,18 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, cudaS
   TcShape sh{(int)rows, nullptr, p.KB, p.kpc, a.status, INT_MAX};
   if constexpr (BN <= 128) {
     if (p.cluster) {
-      KmAssignClusterEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, w.inv, a.assign, a.rho, w.objp};
+      KmAssignClusterEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, w.inv, a.assign, a.rho, w.objp,
+                                 scores};
       return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
     }
   }
   KmAssignEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, p.nz, w.part, w.inv, a.assign, a.rho,
-                      w.objp};
+                      w.objp, scores};
   cudaError_t e =
       launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, p.nz), s);
   if (e != cudaSuccess || p.nz == 1) return e;
   launch_pdl(k_km_argmax, dim3(ceil_div(a.N, 8), a.B), 256, 0, s, w.part, p.nz, a.B, a.N, a.C,
-                                                          w.inv, a.assign, a.rho, w.objp);
+                                                          w.inv, a.assign, a.rho, w.objp, scores);
   return cudaGetLastError();
 }
 
@@ -826,7 +858,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const T* H = static_cast<const T*>(a.H);
   const long BN_ = (long)a.B * a.N;
   const KmPlan p = km_plan(a.dtype, a.B, a.N, a.d, a.C);
-  const KmWs w = km_carve(a.ws, p, a.B, a.N, a.d, a.C, nullptr);
+  const GramPlan g = gram_plan(a.dtype, a.B, a.N, a.d, a.C);
+  const KmWs w = km_carve(a.ws, p, g, a.B, a.N, a.d, a.C, nullptr);
   const ScanPlan sp = scan_plan<T>(a.B, a.d, a.C);
 
   // 1/||h|| and (tensor cores) the split of the given centroids in one
@@ -849,15 +882,40 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
       launch_pdl(k_km_prep<T>, split_blocks, 256, 0, s, H, 0L, a.d, w.inv, 0, a.mu, n_mu,
                  w.mu_hi, w.mu_lo);
   }
+  auto assign_pass = [&](float* scores) {
+    switch (p.BN) {
+      case 32: return assign_tc<32>(a, p, w, scores, s);
+      case 64: return assign_tc<64>(a, p, w, scores, s);
+      case 128: return assign_tc<128>(a, p, w, scores, s);
+      default: return assign_tc<256>(a, p, w, scores, s);
+    }
+  };
+  // Gram form: pass 0 against the given centroids (its cosines seed the
+  // carried columns), passes 1..I-1 on the Gram matrices, then the last
+  // centroid update and pass I exactly as below
+  if (p.tc && g.ok && a.iters >= 2 && !kmeans_lloyd_forced() && gram_launchable(g)) {
+    cudaError_t e = assign_pass(w.L);
+    if (e == cudaSuccess)
+      e = gram_build(g, static_cast<const __nv_bfloat16*>(a.H), w.inv, a.B, a.N, a.d, w.qhi,
+                     w.qlo, a.status, s);
+    if (e == cudaSuccess)
+      e = gram_iterate(g, w.qhi, w.qlo, a.B, a.N, a.C, a.iters - 1, a.assign, w.L, w.objp,
+                       p.ntile, a.obj, a.iters + 1, a.status, s);
+    if (e == cudaSuccess)
+      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C, sp.W,
+                                a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp, p.ntile,
+                                nullptr, a.iters + 1, a.iters - 1);
+    if (e == cudaSuccess) e = assign_pass(nullptr);
+    if (e == cudaSuccess)
+      e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C, sp.W,
+                               a.mu, nullptr, nullptr, a.counts, a.chat, w.objp, p.ntile, a.obj,
+                               a.iters + 1, a.iters);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   for (int t = 0; t <= a.iters; ++t) {
     cudaError_t e = cudaSuccess;
     if (p.tc) {
-      switch (p.BN) {
-        case 32: e = assign_tc<32>(a, p, w, s); break;
-        case 64: e = assign_tc<64>(a, p, w, s); break;
-        case 128: e = assign_tc<128>(a, p, w, s); break;
-        default: e = assign_tc<256>(a, p, w, s); break;
-      }
+      e = assign_pass(nullptr);
     } else {
       launch_pdl(k_assign<T>, dim3(p.ntile, a.B), 256, 0, s, H, a.mu, w.inv, a.N, a.d, a.C,
                                                      a.assign, a.rho, w.objp);
@@ -880,8 +938,9 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
 size_t kmeans_ws(int B, int N, int d, int C) {
   // dtype-independent: the larger of the tensor-core and CUDA-core plans
   size_t tc = 0, simt = 0;
-  km_carve(nullptr, km_plan(PS_BF16, B, N, d, C), B, N, d, C, &tc);
-  km_carve(nullptr, km_plan(PS_F32, B, N, d, C), B, N, d, C, &simt);
+  km_carve(nullptr, km_plan(PS_BF16, B, N, d, C), gram_plan(PS_BF16, B, N, d, C), B, N, d, C,
+           &tc);
+  km_carve(nullptr, km_plan(PS_F32, B, N, d, C), GramPlan{}, B, N, d, C, &simt);
   return std::max(tc, simt);
 }
 

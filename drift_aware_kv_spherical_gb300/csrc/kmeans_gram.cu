@@ -1,0 +1,629 @@
+// a1, Gram form: the k-means passes between the first and the last
+// assignment, run on the windows' cosine Gram matrices.
+//
+// [Polestar §2.A, local window & clustering] clusters a window with spherical
+// k-means: mu_c = u_c / ||u_c|| with u_c the sum of the member rows' unit
+// vectors x_j, and each row joins the centroid of largest cosine.  Since
+//   cos(x_i, mu_c) = sum_{j in c} <x_i, x_j> / sqrt(sum_{j,l in c} <x_j, x_l>),
+// a pass needs only the Gram matrix K = X X^T and the current labels: no
+// centroid is formed and H is not read again.  For a window of N <= 1024 rows
+// the whole of K fits in the shared memory of one thread-block cluster, so
+// the passes run back to back inside one launch.
+//
+//   k_tc_gemm<GramClusterEpi>  K = X X^T on the tensor cores (bf16 H, fp32
+//        accumulation, upper-triangle tiles, K split over a cluster), each
+//        entry scaled by 1/(||h_i|| ||h_j||) and stored as a 24-bit fixed-point
+//        integer q = rint(K * 2^20) in two planes (int16 high part, u8 low
+//        byte), laid out so that CTA z of the iteration kernel finds the
+//        columns of its rows as one contiguous slab.
+//   k_km_gram  one cluster of Z (<= 16) CTAs per window; CTA z holds rows
+//        [zR, zR + R) of K (its slab, loaded once) and runs every pass:
+//        counting-sort the labels, S[i][c] = sum_{j in c} q_ij (exact integer
+//        sums), n_c = sum_{i in c} S[i][c] (int64, summed over the cluster
+//        through distributed shared memory), cos = S / sqrt(n_c), arg-max,
+//        and the new labels pushed to every CTA of the cluster.
+//
+// Integer sums make every reduction exact, hence independent of order.  The
+// fixed-point step (2^-20) bounds a cosine's error by about |c| 2^-21 /
+// ||u_c||, a few 1e-7 for the clusters of these windows; ties between
+// centroids closer than that may resolve differently from an fp64 Lloyd pass.
+// A cluster left empty (or with a zero sum) keeps its centroid, so its column
+// of cosines is carried over from the pass that last set it (kept in global
+// memory, seeded by the first assignment pass against the given centroids).
+#include <climits>
+#include <mutex>
+
+#include "ops.h"
+#include "tc_gemm.cuh"
+#include "vec.cuh"
+
+namespace ps {
+namespace {
+
+constexpr int kGramThreads = 512;
+constexpr int kGramMaxZ = 16;
+constexpr float kGramScale = 1048576.f;  // 2^20 units per unit cosine
+
+// q of rows 2l and 2l + 1 from their packed high parts (two int16) and low bytes
+__device__ __forceinline__ int q_lo(uint32_t h, uint32_t l) {
+  return static_cast<int>(static_cast<int16_t>(h & 0xffffu)) * 256 + static_cast<int>(l & 0xffu);
+}
+__device__ __forceinline__ int q_hi(uint32_t h, uint32_t l) {
+  return static_cast<int>(static_cast<int16_t>(h >> 16)) * 256 + static_cast<int>((l >> 8) & 0xffu);
+}
+
+__device__ __forceinline__ int gram_quant(float k) {
+  const int q = __float2int_rn(k * kGramScale);
+  return min(max(q, -8388607), 8388607);
+}
+
+// Tile t of the Gram GEMM = (window b, row block mt <= column block nt), the
+// upper triangle of the window's 128 x 128 blocks in row-major order.
+struct GramClusterEpi : TcEpiBase {
+  static constexpr bool kClusterReduce = true;
+  static constexpr uint32_t kLd = 128 + 4;
+  int B, N, mtb, T, R, Z;
+  const float* inv;
+  int16_t* qhi;
+  uint8_t* qlo;
+  struct State {};
+  __device__ void tile_of(int t, int& b, int& mt, int& nt) const {
+    b = t / T;
+    int u = t % T;
+    mt = 0;
+    while (u >= mtb - mt) {
+      u -= mtb - mt;
+      ++mt;
+    }
+    nt = mt + u;
+  }
+  __device__ int tiles(int) const { return B * T; }
+  __device__ int arow(int t) const {
+    int b, mt, nt;
+    tile_of(t, b, mt, nt);
+    return b * N + mt * 128;
+  }
+  __device__ int bcoord(int t, int) const {
+    int b, mt, nt;
+    tile_of(t, b, mt, nt);
+    return b * N + nt * 128;
+  }
+  __device__ void consume_red(int, int, int, int, uint32_t taddr, State&,
+                              float* red_row) const {
+    if (red_row == nullptr) return;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(red_row + c0 + 4 * j) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+  // element (row i, column j) sits at slab offset off(i) + j R, with
+  // off(i) = ((b Z + i / R) N) R + i % R; eight consecutive rows from a
+  // multiple of 8 (or eight consecutive columns) share one R-row block, since
+  // R is a multiple of 16, so their high parts are one 16-byte store and
+  // their low bytes one 8-byte store
+  __device__ long long slab_off(int b, int i) const {
+    return ((long long)b * Z + i / R) * N * R + i % R;
+  }
+  __device__ void put(long long off, int q) const {
+    qhi[off] = static_cast<int16_t>(q >> 8);
+    qlo[off] = static_cast<uint8_t>(q & 255);
+  }
+  __device__ void put8(long long off, const int* q) const {
+    uint32_t h[4], l[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      h[e] = (static_cast<uint32_t>(q[2 * e] >> 8) & 0xffffu) |
+             (static_cast<uint32_t>(q[2 * e + 1] >> 8) << 16);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) l[e / 4] |= static_cast<uint32_t>(q[e] & 255) << (8 * (e & 3));
+    *reinterpret_cast<uint4*>(qhi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint2*>(qlo + off) = make_uint2(l[0], l[1]);
+  }
+  __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
+    const int t = blockIdx.y;
+    int b, mt, nt;
+    tile_of(t, b, mt, nt);
+    // rows [r0, r1) of the tile, cut at multiples of 8 (the 16-byte stores
+    // below take eight rows from a multiple of 8); nz <= 8 leaves nr >= 8
+    const int r0 = (z * 128 / nz) & ~7, r1 = z + 1 == nz ? 128 : ((z + 1) * 128 / nz) & ~7;
+    const int nr = r1 - r0;
+    float* s_ir = reinterpret_cast<float*>(scratch);  // [128] 1/||h|| of the rows
+    float* s_ic = s_ir + 128;                         // [128] and of the columns
+    long long* s_ro = reinterpret_cast<long long*>(s_ic + 128);  // [128] off(i) of the rows
+    long long* s_co = s_ro + 128;                                // [128] off(j) of the columns
+    for (int k = threadIdx.x; k < 128; k += blockDim.x) {
+      const int i = mt * 128 + k, j = nt * 128 + k;
+      s_ir[k] = i < N ? inv[(long)b * N + i] : 0.f;
+      s_ic[k] = j < N ? inv[(long)b * N + j] : 0.f;
+      s_ro[k] = slab_off(b, i);
+      s_co[k] = slab_off(b, j);
+    }
+    __syncthreads();
+    // the quantised sums replace this CTA's own rows [r0, r1), which only it reads
+    int* own = reinterpret_cast<int*>(const_cast<float*>(red));
+    auto quant = [&](int r, int c, float4 v) {
+      const float ir = s_ir[r];
+      const int4 q = make_int4(gram_quant(v.x * ir * s_ic[c]), gram_quant(v.y * ir * s_ic[c + 1]),
+                               gram_quant(v.z * ir * s_ic[c + 2]),
+                               gram_quant(v.w * ir * s_ic[c + 3]));
+      *reinterpret_cast<int4*>(own + r * kLd + c) = q;
+    };
+    if (nz <= 4)
+      cluster_rows_sum<4>(red, kLd, r0, r1, 128, nz, quant);
+    else
+      cluster_rows_sum<8>(red, kLd, r0, r1, 128, nz, quant);
+    tc::cluster_arrive();
+    __syncthreads();
+    // K(i, j): eight rows of one column per item
+    const int nu = nr / 8;
+    for (int it = threadIdx.x; it < 128 * nu; it += blockDim.x) {
+      const int c = it / nu, rb = r0 + 8 * (it % nu);
+      const int i0 = mt * 128 + rb, j = nt * 128 + c;
+      if (j >= N || i0 >= N) continue;
+      int q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = own[(rb + e) * kLd + c];
+      if (i0 + 8 <= N) {
+        put8(s_ro[rb] + (long long)j * R, q);
+      } else {
+        for (int e = 0; e < 8 && i0 + e < N; ++e) put(s_ro[rb + e] + (long long)j * R, q[e]);
+      }
+    }
+    if (mt != nt) {  // K(j, i) = K(i, j) for the lower triangle: eight columns of one row
+      for (int it = threadIdx.x; it < nr * 16; it += blockDim.x) {
+        const int r = r0 + it / 16, cb = 8 * (it % 16);
+        const int i = mt * 128 + r, j0 = nt * 128 + cb;
+        if (i >= N || j0 >= N) continue;
+        int q[8];
+        const int4 qa = *reinterpret_cast<const int4*>(own + r * kLd + cb);
+        const int4 qb = *reinterpret_cast<const int4*>(own + r * kLd + cb + 4);
+        q[0] = qa.x; q[1] = qa.y; q[2] = qa.z; q[3] = qa.w;
+        q[4] = qb.x; q[5] = qb.y; q[6] = qb.z; q[7] = qb.w;
+        if (j0 + 8 <= N) {
+          put8(s_co[cb] + (long long)i * R, q);
+        } else {
+          for (int e = 0; e < 8 && j0 + e < N; ++e) put(s_co[cb + e] + (long long)i * R, q[e]);
+        }
+      }
+    }
+  }
+};
+
+// Shared-memory layout of k_km_gram (16-byte aligned pieces).
+struct GramSmem {
+  uint32_t hi, lo, S, slot, npart, lab, prev, perm, chg, nchg, off, cur, hist, invn, keep,
+      newlab, best, objp, red, bar, abort, total;
+};
+
+__host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
+
+__host__ __device__ inline GramSmem gram_smem(int N, int C, int R, int Z) {
+  GramSmem o{};
+  uint32_t p = 0;
+  o.hi = p;     p = al16(p + (uint32_t)N * R * 2);
+  o.lo = p;     p = al16(p + (uint32_t)N * R);
+  o.S = p;      p = al16(p + (uint32_t)R * (C + 1) * 4);
+  o.slot = p;   p = al16(p + (uint32_t)Z * C * 8);
+  o.npart = p;  p = al16(p + (uint32_t)C * 8);
+  o.lab = p;    p = al16(p + (uint32_t)Z * R);
+  o.prev = p;   p = al16(p + (uint32_t)N);
+  o.perm = p;   p = al16(p + (uint32_t)N * 2);
+  o.chg = p;    p = al16(p + (uint32_t)N * 2);
+  o.nchg = p;   p = al16(p + 4);
+  o.off = p;    p = al16(p + (uint32_t)(C + 1) * 4);
+  o.cur = p;    p = al16(p + (uint32_t)C * 4);
+  o.hist = p;   p = al16(p + (uint32_t)C * 4);
+  o.invn = p;   p = al16(p + (uint32_t)C * 4);
+  o.keep = p;   p = al16(p + (uint32_t)C);
+  o.newlab = p; p = al16(p + (uint32_t)R);
+  o.best = p;   p = al16(p + (uint32_t)R * 4);
+  o.objp = p;   p = al16(p + (uint32_t)Z * 4);
+  o.red = p;    p = al16(p + 32 * 4);
+  o.bar = p;    p = al16(p + 8);
+  o.abort = p;  p = al16(p + 4);
+  o.total = p;
+  return o;
+}
+
+// One cluster of Z CTAs per window (blockIdx.y); CTA z = blockIdx.x owns rows
+// [z R, z R + R).  Passes 1..passes; on entry assign holds the labels of pass
+// 0 and L[b][i][c] the cosines against the given centroids; on exit assign
+// holds the labels of the last pass, obj[b][0..passes] the objectives (pass 0
+// folded from the first assignment's partials objp0).
+__global__ void __launch_bounds__(kGramThreads, 1)
+k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int N, int C,
+          int R, int passes, int32_t* __restrict__ assign, float* __restrict__ L,
+          const float* __restrict__ objp0, int ntile0, float* __restrict__ obj, int obj_ld,
+          int* status) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int Z = gridDim.x, z = blockIdx.x, b = blockIdx.y;
+  const GramSmem o = gram_smem(N, C, R, Z);
+  const int16_t* s_hi = reinterpret_cast<const int16_t*>(sm + o.hi);
+  const uint8_t* s_lo = sm + o.lo;
+  int* s_S = reinterpret_cast<int*>(sm + o.S);
+  long long* s_slot = reinterpret_cast<long long*>(sm + o.slot);
+  long long* s_npart = reinterpret_cast<long long*>(sm + o.npart);
+  uint8_t* s_lab = sm + o.lab;
+  uint8_t* s_prev = sm + o.prev;
+  uint16_t* s_perm = reinterpret_cast<uint16_t*>(sm + o.perm);
+  uint16_t* s_chg = reinterpret_cast<uint16_t*>(sm + o.chg);
+  int* s_nchg = reinterpret_cast<int*>(sm + o.nchg);
+  int* s_off = reinterpret_cast<int*>(sm + o.off);
+  int* s_cur = reinterpret_cast<int*>(sm + o.cur);
+  int* s_hist = reinterpret_cast<int*>(sm + o.hist);
+  float* s_invn = reinterpret_cast<float*>(sm + o.invn);
+  uint8_t* s_keep = sm + o.keep;
+  uint8_t* s_newlab = sm + o.newlab;
+  float* s_best = reinterpret_cast<float*>(sm + o.best);
+  float* s_objp = reinterpret_cast<float*>(sm + o.objp);
+  float* s_red = reinterpret_cast<float*>(sm + o.red);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + o.bar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + o.abort);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = kGramThreads / 32;
+  const int row0 = z * R, nrow = min(R, N - row0);
+  const int ldS = C + 1;
+
+  const size_t slab = (size_t)N * R;
+  if (tid == 0) {
+    *abort_flag = 0;
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint8_t* gh = reinterpret_cast<const uint8_t*>(qhi + ((size_t)b * Z + z) * slab);
+    const uint8_t* gl = qlo + ((size_t)b * Z + z) * slab;
+    tc::mbar_expect_tx(bar, static_cast<uint32_t>(slab * 3));
+    for (size_t k = 0; k < slab * 2; k += 32768)
+      tc::bulk_load(sm + o.hi + k, gh + k, static_cast<uint32_t>(min((size_t)32768, slab * 2 - k)),
+                    bar);
+    for (size_t k = 0; k < slab; k += 32768)
+      tc::bulk_load(sm + o.lo + k, gl + k, static_cast<uint32_t>(min((size_t)32768, slab - k)),
+                    bar);
+  }
+  for (int j = tid; j < N; j += kGramThreads)
+    s_lab[j] = static_cast<uint8_t>(assign[(size_t)b * N + j]);
+  if (obj != nullptr && z == 0) {  // block-uniform: the objective of pass 0
+    float so = 0.f;
+    for (int t = tid; t < ntile0; t += kGramThreads) so += objp0[(size_t)b * ntile0 + t];
+    so = block_sum_f32(so, s_red);
+    if (tid == 0) obj[(size_t)b * obj_ld] = so;
+  }
+  // every thread observes the slab's arrival (a timeout leaves the status set
+  // and the passes run on whatever landed; the copies are awaited before exit)
+  tc::mbar_wait(bar, 0, status, abort_flag);
+
+  float last_obj = 0.f;  // CTA 0, thread 0: the latest pass objective
+  for (int p = 1; p <= passes; ++p) {
+    int M = 0;  // labels changed since S was formed (pass 1: all, from scratch)
+    if (p == 1) {
+      // counting sort of the labels: s_perm lists rows cluster by cluster
+      for (int k = tid; k < R * ldS; k += kGramThreads) s_S[k] = 0;
+      for (int c = tid; c < C; c += kGramThreads) s_hist[c] = 0;
+      __syncthreads();
+      for (int j = tid; j < N; j += kGramThreads) atomicAdd(&s_hist[s_lab[j]], 1);
+      __syncthreads();
+      if (warp == 0) {  // C <= 256: a lane scans 8 consecutive bins
+        int v[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = lane * 8 + k;
+          v[k] = c < C ? s_hist[c] : 0;
+          sum += v[k];
+        }
+        int inc = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, inc, d);
+          if (lane >= d) inc += x;
+        }
+        int run = inc - sum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = lane * 8 + k;
+          if (c < C) {
+            s_off[c] = run;
+            s_cur[c] = run;
+          }
+          run += v[k];
+        }
+        if (lane == 31) s_off[C] = inc;
+      }
+      __syncthreads();
+      for (int j = tid; j < N; j += kGramThreads) {
+        const int at = atomicAdd(&s_cur[s_lab[j]], 1);
+        s_perm[at] = static_cast<uint16_t>(j);
+        s_prev[j] = s_lab[j];
+      }
+      __syncthreads();
+
+      // S[r][c] = sum over members j of c of q(row0 + r, j).  Warp w takes
+      // positions [w N / 16, (w+1) N / 16) of the sorted list, lane l rows 2l
+      // and 2l + 1; a segment's sums go to S with one integer atomic per row.
+      const int p0 = warp * N / nwarps, p1 = (warp + 1) * N / nwarps;
+      const int r2 = 2 * lane;
+      const bool act = r2 < R;
+      int pp = p0;
+      if (pp < p1) {
+        int c = s_lab[s_perm[pp]];
+        while (true) {
+          const int e = min(s_off[c + 1], p1);
+          if (act) {
+            int a0 = 0, a1 = 0;
+            for (; pp + 4 <= e; pp += 4) {
+              uint32_t h[4], l[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = s_perm[pp + u];
+                h[u] = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
+                l[u] = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                a0 += q_lo(h[u], l[u]);
+                a1 += q_hi(h[u], l[u]);
+              }
+            }
+            for (; pp < e; ++pp) {
+              const int j = s_perm[pp];
+              const uint32_t h = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
+              const uint32_t l = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
+              a0 += q_lo(h, l);
+              a1 += q_hi(h, l);
+            }
+            atomicAdd(&s_S[r2 * ldS + c], a0);
+            atomicAdd(&s_S[(r2 + 1) * ldS + c], a1);
+          } else {
+            pp = e;
+          }
+          if (pp >= p1) break;
+          c = s_lab[s_perm[pp]];
+        }
+      }
+      M = N;
+    } else {
+      // rows whose label changed in the last pass move their column of q
+      // from the old cluster's sums to the new one's (integer, so S stays
+      // equal to the sums formed from scratch)
+      if (tid == 0) *s_nchg = 0;
+      __syncthreads();
+      for (int j = tid; j < N; j += kGramThreads)
+        if (s_lab[j] != s_prev[j]) s_chg[atomicAdd(s_nchg, 1)] = static_cast<uint16_t>(j);
+      __syncthreads();
+      M = *s_nchg;
+      if (M > 0) {  // cluster-uniform: every CTA holds the same labels
+        const int half = R / 2;
+        for (int it = tid; it < M * half; it += kGramThreads) {
+          const int k = it / half, r2 = 2 * (it % half);
+          const int j = s_chg[k];
+          const int co = s_prev[j], cn = s_lab[j];
+          const uint32_t h = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
+          const uint32_t l = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
+          const int v0 = q_lo(h, l), v1 = q_hi(h, l);
+          atomicAdd(&s_S[r2 * ldS + co], -v0);
+          atomicAdd(&s_S[r2 * ldS + cn], v0);
+          atomicAdd(&s_S[(r2 + 1) * ldS + co], -v1);
+          atomicAdd(&s_S[(r2 + 1) * ldS + cn], v1);
+        }
+        for (int k = tid; k < M; k += kGramThreads) {
+          const int j = s_chg[k];
+          atomicSub(&s_hist[s_prev[j]], 1);
+          atomicAdd(&s_hist[s_lab[j]], 1);
+        }
+        __syncthreads();
+        for (int k = tid; k < M; k += kGramThreads) s_prev[s_chg[k]] = s_lab[s_chg[k]];
+      }
+    }
+
+    if (M > 0) {
+      // ||u_c||^2 partial of this CTA's rows, pushed into slot z of every CTA
+      for (int c = tid; c < C; c += kGramThreads) s_npart[c] = 0;
+      __syncthreads();
+      for (int r = tid; r < nrow; r += kGramThreads) {
+        const int c = s_lab[row0 + r];
+        atomicAdd(reinterpret_cast<unsigned long long*>(&s_npart[c]),
+                  static_cast<unsigned long long>(static_cast<long long>(s_S[r * ldS + c])));
+      }
+      __syncthreads();
+      const uint32_t base = tc::smem_u32(s_slot + (size_t)z * C);
+      for (int k = tid; k < Z * C; k += kGramThreads) {
+        const int q = k / C, c = k % C;
+        tc::st_dsmem_u64(tc::cluster_map(base + 8u * c, q),
+                         static_cast<unsigned long long>(s_npart[c]));
+      }
+      tc::cluster_sync_all();
+      // 1 / ||u_c|| (2^-10 folds the fixed-point scale of S and of n_c)
+      for (int c = tid; c < C; c += kGramThreads) {
+        long long n = 0;
+        for (int q = 0; q < Z; ++q) n += s_slot[q * C + c];
+        const bool keep = s_hist[c] == 0 || n <= 0;
+        s_keep[c] = keep ? 1 : 0;
+        s_invn[c] = keep ? 0.f : 0.0009765625f / sqrtf(static_cast<float>(n));
+      }
+      __syncthreads();
+    }
+    // (M == 0: S, the counts and the norms are those of the last pass)
+
+    // cosines and arg-max (first maximum): 8 threads per row, thread `sub`
+    // taking clusters sub, sub + 8, ...; a kept cluster's column comes from
+    // L, the others refresh it
+    {
+      const int r = tid >> 3, sub = tid & 7;
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      if (r < R) {
+        const bool valid = r < nrow;
+        float* Lrow = L + ((size_t)b * N + (valid ? row0 + r : 0)) * C;
+        for (int c = sub; c < C; c += 8) {
+          float v;
+          if (s_keep[c]) {
+            v = valid ? Lrow[c] : 0.f;
+          } else {
+            v = static_cast<float>(s_S[r * ldS + c]) * s_invn[c];
+            if (valid && M > 0) Lrow[c] = v;
+          }
+          if (v > bv) {
+            bv = v;
+            bi = c;
+          }
+        }
+      }
+#pragma unroll
+      for (int d = 1; d < 8; d <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (sub == 0 && r < R) {
+        if (bi == INT_MAX) {
+          bi = 0;
+          bv = 0.f;
+        }
+        s_newlab[r] = static_cast<uint8_t>(bi);
+        s_best[r] = r < nrow ? bv : 0.f;
+      }
+    }
+    __syncthreads();
+
+    if (M > 0) {
+      // the pass objective's partial to CTA 0, the new labels to every CTA
+      if (obj != nullptr && warp == 0) {
+        float so = 0.f;
+        for (int r = lane; r < R; r += 32) so += s_best[r];
+        so = warp_sum(so);
+        if (lane == 0) tc::st_dsmem_f32(tc::cluster_map(tc::smem_u32(s_objp + z), 0), so);
+      }
+      const int words = R / 4;
+      for (int k = tid; k < Z * words; k += kGramThreads) {
+        const int q = k / words, w = k % words;
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(s_newlab + 4 * w);
+        tc::st_dsmem_u32(tc::cluster_map(tc::smem_u32(s_lab + row0 + 4 * w), q), v);
+      }
+      tc::cluster_sync_all();
+      if (obj != nullptr && z == 0 && tid == 0) {
+        float so = 0.f;
+        for (int q = 0; q < Z; ++q) so += s_objp[q];
+        last_obj = so;
+      }
+    }
+    // (M == 0: the same inputs gave the same labels and objective)
+    if (obj != nullptr && z == 0 && tid == 0) obj[(size_t)b * obj_ld + p] = last_obj;
+  }
+  for (int r = tid; r < nrow; r += kGramThreads)
+    assign[(size_t)b * N + row0 + r] = s_lab[row0 + r];
+  if (tid == 0 && *abort_flag) {  // copies still in flight must land before the CTA leaves
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, 0) && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
+    }
+  }
+}
+
+// Clusters of z CTAs of k_km_gram (smem bytes each) the GPU holds at once;
+// 0 when the shape cannot launch.  Cached per device and shape.
+int gram_capacity(int z, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static int c_dev = -1, c_z = 0;
+  static size_t c_smem = 0;
+  static int c_val = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev == c_dev && z == c_z && smem == c_smem) return c_val;
+  int n = 0;
+  if (cudaFuncSetAttribute(k_km_gram, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) == cudaSuccess &&
+      cudaFuncSetAttribute(k_km_gram, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(z, 1, 1);
+    cfg.blockDim = dim3(kGramThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = z;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, k_km_gram, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  c_dev = dev;
+  c_z = z;
+  c_smem = smem;
+  c_val = n;
+  return n;
+}
+
+}  // namespace
+
+GramPlan gram_plan(int dtype, int B, int N, int d, int C) {
+  GramPlan g{};
+  if (dtype != PS_BF16 || B < 1 || N < 2 || N > 1024 || C < 1 || C > 256 || d < 64) return g;
+  g.R = ceil_div(ceil_div(N, kGramMaxZ), 16) * 16;
+  g.Z = ceil_div(N, g.R);
+  g.smem = gram_smem(N, C, g.R, g.Z).total;
+  if (g.smem > 227 * 1024) return g;
+  g.mtb = ceil_div(N, 128);
+  g.T = g.mtb * (g.mtb + 1) / 2;
+  g.KB = ceil_div(d, 64);
+  const int tiles = B * g.T;
+  g.nz = 1;
+  for (int z = 8; z >= 2; z /= 2)
+    if (z <= g.KB && (long)tiles * z <= kSmTarget && tiles <= tc_cluster_capacity(z)) {
+      g.nz = z;
+      break;
+    }
+  g.kpc = ceil_div(g.KB, g.nz);
+  g.nz = ceil_div(g.KB, g.kpc);
+  g.ok = true;
+  return g;
+}
+
+bool gram_launchable(const GramPlan& g) {
+  return g.ok && gram_capacity(g.Z, g.smem) >= 1;
+}
+
+cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
+                       int N, int d, int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s) {
+  TcMaps maps;
+  if (!make_tmap_bf16_2d(&maps.a[0], H, d, (uint64_t)B * N, (uint64_t)d * 2, 64, 128))
+    return cudaErrorInvalidValue;
+  maps.a[1] = maps.a[0];
+  maps.b[0] = maps.a[0];
+  maps.b[1] = maps.a[0];
+  TcShape sh{B * N, nullptr, g.KB, g.kpc, status, INT_MAX};
+  GramClusterEpi epi{{}, B, N, g.mtb, g.T, g.R, g.Z, inv, qhi, qlo};
+  return launch_tc_gemm<128, 1, 1, false>(maps, sh, epi, dim3(1, B * g.T, g.nz), s);
+}
+
+cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,
+                         int C, int passes, int32_t* assign, float* L, const float* objp0,
+                         int ntile0, float* obj, int obj_ld, int* status, cudaStream_t s) {
+  if (gram_capacity(g.Z, g.smem) < 1) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.Z, B, 1);
+  cfg.blockDim = dim3(kGramThreads);
+  cfg.dynamicSmemBytes = g.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.Z;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_ex(cfg, k_km_gram, qhi, qlo, N, C, g.R, passes, assign, L, objp0, ntile0, obj,
+                   obj_ld, status);
+}
+
+}  // namespace ps

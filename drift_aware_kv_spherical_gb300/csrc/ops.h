@@ -15,6 +15,25 @@ struct KmeansArgs {
 size_t kmeans_ws(int B, int N, int d, int C);
 cudaError_t kmeans_run(const KmeansArgs& a, cudaStream_t s);
 
+// k-means passes in Gram form (kmeans_gram.cu): bf16 windows of N <= 1024
+// rows whose cosine Gram matrix fits one thread-block cluster's shared memory.
+struct GramPlan {
+  bool ok;
+  int R, Z;      // rows per CTA, CTAs per window of the pass kernel
+  size_t smem;   // its shared memory per CTA
+  int mtb, T;    // 128-row blocks, upper-triangle tiles per window
+  int KB, kpc, nz;  // the Gram GEMM's K blocks and split
+};
+GramPlan gram_plan(int dtype, int B, int N, int d, int C);
+bool gram_launchable(const GramPlan& g);
+// K = X X^T of every window in 24-bit fixed point (qhi/qlo: B * Z * N * R each)
+cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
+                       int N, int d, int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s);
+// passes 1..passes from the labels in assign and the cosines L of pass 0
+cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,
+                         int C, int passes, int32_t* assign, float* L, const float* objp0,
+                         int ntile0, float* obj, int obj_ld, int* status, cudaStream_t s);
+
 struct Nvfp4Args {
   const void* H; int dtype; const float* mu; const int32_t* assign;
   const float* rho; int B, N, d, C;

@@ -328,6 +328,9 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       }
     }
   }
+  // lanes 1..31 of the TMA and MMA warps wait for their lane 0 here, so each
+  // warp reaches the CTA barrier converged (the barrier is warp-aligned)
+  __syncwarp();
   __syncthreads();
   pdl_trigger();
   if constexpr (Epi::kClusterReduce) {

@@ -86,8 +86,9 @@ def test_check_reports_ok_after_work(lib):
 
 def test_kernel_trace_records_every_launch(lib):
     """The diagnostic trace brackets each launch of a call with events: a
-    k-means call with I passes on the tensor-core path records its launches
-    in order with positive durations; disabling clears the records."""
+    k-means call with I = 3 on the tensor-core path (Gram form) records its
+    launches in order with positive durations; disabling clears the
+    records."""
     H = torch.randn(1, 300, 256, device="cuda").to(torch.bfloat16)
     mu = torch.nn.functional.normalize(torch.randn(1, 24, 256, device="cuda"), dim=2)
     a = torch.zeros(1, 300, dtype=torch.int32, device="cuda")
@@ -100,8 +101,11 @@ def test_kernel_trace_records_every_launch(lib):
     rec = ps.ps_trace_records()
     ps.ps_check()
     names = [r[0] for r in rec]
-    assert sum("k_tc_gemm" in x for x in names) == 4             # I + 1 assignment passes
-    assert sum("k_cluster_scan" in x for x in names) == 4        # 3 updates + the final pass
+    assert len(names) == 7
+    assert "k_km_prep" in names[0]
+    assert sum("k_tc_gemm" in x for x in names) == 3             # passes 0 and I, the Gram GEMM
+    assert sum("k_km_gram" in x for x in names) == 1             # passes 1 .. I-1
+    assert sum("k_cluster_scan" in x for x in names) == 2        # last update + the final pass
     assert all(ms > 0 for _, ms in rec)
     ps.ps_trace_enable(False)
     assert lib.cdll.ps_trace_count(lib.handle()) == 0
