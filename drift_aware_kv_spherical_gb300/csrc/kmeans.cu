@@ -535,7 +535,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                int d, int C, int W, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
                __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
                float* __restrict__ chat, const float* __restrict__ objp, int ntile,
-               float* __restrict__ obj, int obj_ld, int pass) {
+               float* __restrict__ obj, int obj_ld, int pass,
+               const int32_t* __restrict__ assign_fin) {
   pdl_prologue();
   constexpr int V = Vec<T>::n;
   constexpr int kMemb = 16 / G;
@@ -628,7 +629,21 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     so = block_sum_f32(so, s_red);
     if (tid == 0) obj[(long)b * obj_ld + pass] = so;
   }
-  if (z == 0 && tid == 0) counts[(long)b * C + c] = n;
+  // fused last update + final pass: the final labels' members give the
+  // count and the mean rho of C_hat
+  int n_fin = n;
+  float rs_fin = 0.f;
+  if (!FINAL && assign_fin != nullptr) {  // block-uniform
+    int cnt = 0;
+    for (int i = tid; i < N; i += nthr)
+      if (__ldg(assign_fin + (long)b * N + i) == c) {
+        rs_fin += rho[(long)b * N + i];
+        ++cnt;
+      }
+    block_exclusive_scan<int>(cnt, s_scan, &n_fin);
+    rs_fin = block_sum_f32(rs_fin, s_red);
+  }
+  if (z == 0 && tid == 0) counts[(long)b * C + c] = n_fin;
   if constexpr (FINAL) {
     const float tot = block_sum_f32(rs, s_red);
     if (n == 0) return;
@@ -663,38 +678,52 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
       ss = s_red[0];
     }
     const float nu = sqrtf(ss);
-    if (n == 0 || !(nu > 0.f)) {
-      if (S > 1) tc::cluster_wait();
-      return;
-    }
+    const bool formed = n > 0 && nu > 0.f;  // else the centroid is kept
     const long ro = ((long)b * C + c) * d;
+    const float mean = (assign_fin != nullptr && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int col = col0 + (g * nthr + tid) * V;
       if (col < col1) {  // V consecutive columns: 16-byte fp32 stores, 8- or 16-byte bf16
         float x[V];
-        uint32_t hi[V / 2], lo[V / 2];
+        if (formed) {
 #pragma unroll
-        for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
+          for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
+          float4* mo = reinterpret_cast<float4*>(mu + ro + col);
 #pragma unroll
-        for (int e = 0; e < V; e += 2) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
-          const float2 hf = __bfloat1622float2(h);
-          const __nv_bfloat162 l = __floats2bfloat162_rn(x[e] - hf.x, x[e + 1] - hf.y);
-          hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
-          lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
-        }
-        float4* mo = reinterpret_cast<float4*>(mu + ro + col);
+          for (int e = 0; e < V; e += 4)
+            mo[e / 4] = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+          if (mu_hi != nullptr) {
+            uint32_t hi[V / 2], lo[V / 2];
 #pragma unroll
-        for (int e = 0; e < V; e += 4) mo[e / 4] = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-        if (mu_hi != nullptr) {
-          if constexpr (V == 8) {
-            *reinterpret_cast<uint4*>(mu_hi + ro + col) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(mu_lo + ro + col) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          } else {
-            *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
-            *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
+            for (int e = 0; e < V; e += 2) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
+              const float2 hf = __bfloat1622float2(h);
+              const __nv_bfloat162 l = __floats2bfloat162_rn(x[e] - hf.x, x[e + 1] - hf.y);
+              hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+              lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            if constexpr (V == 8) {
+              *reinterpret_cast<uint4*>(mu_hi + ro + col) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(mu_lo + ro + col) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            } else {
+              *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
+              *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
+            }
           }
+        } else if (assign_fin != nullptr && n_fin > 0) {
+          const float4* mi = reinterpret_cast<const float4*>(mu + ro + col);
+#pragma unroll
+          for (int e = 0; e < V; e += 4) {
+            const float4 m4 = mi[e / 4];
+            x[e] = m4.x; x[e + 1] = m4.y; x[e + 2] = m4.z; x[e + 3] = m4.w;
+          }
+        }
+        if (assign_fin != nullptr && n_fin > 0) {
+          float4* co = reinterpret_cast<float4*>(chat + ro + col);
+#pragma unroll
+          for (int e = 0; e < V; e += 4)
+            co[e / 4] = make_float4(mean * x[e], mean * x[e + 1], mean * x[e + 2], mean * x[e + 3]);
         }
       }
     }
@@ -795,6 +824,7 @@ struct KmWs {
   __nv_bfloat16* mu_lo;
   float* part;
   float* L;        // Gram form: [B][N][C] cosines carried for kept centroids
+  int32_t* prev;   // Gram form: labels of pass I - 1
   int16_t* qhi;    // Gram form: fixed-point Gram matrices, high and low parts
   uint8_t* qlo;
 };
@@ -816,6 +846,7 @@ KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int 
   if (g.ok) {
     const size_t q = (size_t)B * g.Z * N * g.R;
     w.L = cv.take<float>((size_t)BN_ * C);
+    w.prev = cv.take<int32_t>((size_t)BN_);
     w.qhi = cv.take<int16_t>(q);
     w.qlo = cv.take<uint8_t>(q);
   }
@@ -891,25 +922,20 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
   };
   // Gram form: pass 0 against the given centroids (its cosines seed the
-  // carried columns), passes 1..I-1 on the Gram matrices, then the last
-  // centroid update and pass I exactly as below
+  // carried columns), passes 1..I on the Gram matrices, then one scan that
+  // forms mu^(I) from the labels of pass I - 1 and C_hat from those of pass I
   if (p.tc && g.ok && a.iters >= 2 && !kmeans_lloyd_forced() && gram_launchable(g)) {
+    const auto* Hb = static_cast<const __nv_bfloat16*>(a.H);
     cudaError_t e = assign_pass(w.L);
     if (e == cudaSuccess)
-      e = gram_build(g, static_cast<const __nv_bfloat16*>(a.H), w.inv, a.B, a.N, a.d, w.qhi,
-                     w.qlo, a.status, s);
+      e = gram_build(g, Hb, w.inv, a.B, a.N, a.d, w.qhi, w.qlo, a.status, s);
     if (e == cudaSuccess)
-      e = gram_iterate(g, w.qhi, w.qlo, a.B, a.N, a.C, a.iters - 1, a.assign, w.L, w.objp,
-                       p.ntile, a.obj, a.iters + 1, a.status, s);
+      e = gram_iterate(g, w.qhi, w.qlo, a.B, a.N, a.C, a.iters, Hb, a.d, w.inv, a.mu, a.assign,
+                       w.prev, a.rho, w.L, w.objp, p.ntile, a.obj, a.iters + 1, a.status, s);
     if (e == cudaSuccess)
-      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C, sp.W,
-                                a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp, p.ntile,
-                                nullptr, a.iters + 1, a.iters - 1);
-    if (e == cudaSuccess) e = assign_pass(nullptr);
-    if (e == cudaSuccess)
-      e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C, sp.W,
-                               a.mu, nullptr, nullptr, a.counts, a.chat, w.objp, p.ntile, a.obj,
-                               a.iters + 1, a.iters);
+      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C, sp.W,
+                                a.mu, nullptr, nullptr, a.counts, a.chat, w.objp, p.ntile,
+                                nullptr, a.iters + 1, a.iters, a.assign);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   for (int t = 0; t <= a.iters; ++t) {
@@ -924,12 +950,14 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     if (t < a.iters)
       e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
                                 sp.W, a.mu, p.tc ? w.mu_hi : nullptr, w.mu_lo, a.counts,
-                                a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t);
+                                a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t,
+                                static_cast<const int32_t*>(nullptr));
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
                                        a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
-                                       w.objp, p.ntile, a.obj, a.iters + 1, a.iters);
+                                       w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
+                                       static_cast<const int32_t*>(nullptr));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

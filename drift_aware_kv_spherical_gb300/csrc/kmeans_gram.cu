@@ -197,7 +197,7 @@ struct GramClusterEpi : TcEpiBase {
 // Shared-memory layout of k_km_gram (16-byte aligned pieces).
 struct GramSmem {
   uint32_t hi, lo, S, slot, npart, lab, prev, perm, chg, nchg, off, cur, hist, invn, keep,
-      newlab, best, objp, red, bar, abort, total;
+      formed, newlab, best, objp, red, bar, abort, total;
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -220,6 +220,7 @@ __host__ __device__ inline GramSmem gram_smem(int N, int C, int R, int Z) {
   o.hist = p;   p = al16(p + (uint32_t)C * 4);
   o.invn = p;   p = al16(p + (uint32_t)C * 4);
   o.keep = p;   p = al16(p + (uint32_t)C);
+  o.formed = p; p = al16(p + (uint32_t)C);
   o.newlab = p; p = al16(p + (uint32_t)R);
   o.best = p;   p = al16(p + (uint32_t)R * 4);
   o.objp = p;   p = al16(p + (uint32_t)Z * 4);
@@ -230,14 +231,73 @@ __host__ __device__ inline GramSmem gram_smem(int N, int C, int R, int Z) {
   return o;
 }
 
+// mu[b][c] = normalise(sum over rows j with lab[j] == c of h_j / ||h_j||),
+// by every thread of the CTA: thread t owns columns 8t.. of each 4096-column
+// block (d <= kGramMaxD), members in ascending row order.  Kept as is when
+// the sum is zero.
+constexpr int kGramMaxD = 4 * kGramThreads * 8;
+__device__ void materialise(const __nv_bfloat16* __restrict__ H, int d,
+                            const float* __restrict__ inv, float* __restrict__ mu, int b, int N,
+                            int C, int c, const uint8_t* lab, float* s_red) {
+  constexpr int kChunks = kGramMaxD / (kGramThreads * 8);
+  float u[kChunks][8];
+#pragma unroll
+  for (int q = 0; q < kChunks; ++q)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u[q][e] = 0.f;
+  for (int j = 0; j < N; ++j) {
+    if (lab[j] != c) continue;
+    const float sc = inv[(size_t)b * N + j];
+    const __nv_bfloat16* h = H + ((size_t)b * N + j) * d;
+#pragma unroll
+    for (int q = 0; q < kChunks; ++q) {
+      const int col = (q * kGramThreads + threadIdx.x) * 8;
+      if (col < d) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(h + col);
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(p2[e]);
+          u[q][2 * e] = fmaf(f.x, sc, u[q][2 * e]);
+          u[q][2 * e + 1] = fmaf(f.y, sc, u[q][2 * e + 1]);
+        }
+      }
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < kChunks; ++q)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(u[q][e], u[q][e], ss);
+  ss = block_sum_f32(ss, s_red);
+  const float nu = sqrtf(ss);
+  if (!(nu > 0.f)) return;
+  float* m = mu + ((size_t)b * C + c) * d;
+#pragma unroll
+  for (int q = 0; q < kChunks; ++q) {
+    const int col = (q * kGramThreads + threadIdx.x) * 8;
+    if (col < d) {
+      reinterpret_cast<float4*>(m + col)[0] =
+          make_float4(u[q][0] / nu, u[q][1] / nu, u[q][2] / nu, u[q][3] / nu);
+      reinterpret_cast<float4*>(m + col)[1] =
+          make_float4(u[q][4] / nu, u[q][5] / nu, u[q][6] / nu, u[q][7] / nu);
+    }
+  }
+}
+
 // One cluster of Z CTAs per window (blockIdx.y); CTA z = blockIdx.x owns rows
 // [z R, z R + R).  Passes 1..passes; on entry assign holds the labels of pass
 // 0 and L[b][i][c] the cosines against the given centroids; on exit assign
-// holds the labels of the last pass, obj[b][0..passes] the objectives (pass 0
-// folded from the first assignment's partials objp0).
+// holds the labels of the last pass, prev those of the pass before, rho the
+// last pass's <h_i, mu_{a_i}>, obj[b][0..passes] the objectives (pass 0
+// folded from the first assignment's partials objp0), and mu the centroids
+// that stopped being formed at some pass (the others are formed afterwards
+// from prev, by the last update).
 __global__ void __launch_bounds__(kGramThreads, 1)
 k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int N, int C,
-          int R, int passes, int32_t* __restrict__ assign, float* __restrict__ L,
+          int R, int passes, const __nv_bfloat16* __restrict__ H, int d,
+          const float* __restrict__ inv, float* __restrict__ mu, int32_t* __restrict__ assign,
+          int32_t* __restrict__ prev, float* __restrict__ rho, float* __restrict__ L,
           const float* __restrict__ objp0, int ntile0, float* __restrict__ obj, int obj_ld,
           int* status) {
   extern __shared__ __align__(16) uint8_t sm[];
@@ -258,6 +318,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
   int* s_hist = reinterpret_cast<int*>(sm + o.hist);
   float* s_invn = reinterpret_cast<float*>(sm + o.invn);
   uint8_t* s_keep = sm + o.keep;
+  uint8_t* s_formed = sm + o.formed;
   uint8_t* s_newlab = sm + o.newlab;
   float* s_best = reinterpret_cast<float*>(sm + o.best);
   float* s_objp = reinterpret_cast<float*>(sm + o.objp);
@@ -289,6 +350,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
   }
   for (int j = tid; j < N; j += kGramThreads)
     s_lab[j] = static_cast<uint8_t>(assign[(size_t)b * N + j]);
+  for (int c = tid; c < C; c += kGramThreads) s_formed[c] = 0;  // pass 0 used the given centroids
   if (obj != nullptr && z == 0) {  // block-uniform: the objective of pass 0
     float so = 0.f;
     for (int t = tid; t < ntile0; t += kGramThreads) so += objp0[(size_t)b * ntile0 + t];
@@ -416,8 +478,8 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
           atomicSub(&s_hist[s_prev[j]], 1);
           atomicAdd(&s_hist[s_lab[j]], 1);
         }
-        __syncthreads();
-        for (int k = tid; k < M; k += kGramThreads) s_prev[s_chg[k]] = s_lab[s_chg[k]];
+        // s_prev keeps the labels of the pass before until the centroids
+        // that stop being formed have been materialised below
       }
     }
 
@@ -446,6 +508,18 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
         s_keep[c] = keep ? 1 : 0;
         s_invn[c] = keep ? 0.f : 0.0009765625f / sqrtf(static_cast<float>(n));
       }
+      __syncthreads();
+      // a centroid formed in the last pass but kept from this one stays as
+      // it was: normalise(sum of the unit rows labelled c in s_prev), formed
+      // here from H (CTA c mod Z) so that the last update can keep it
+      for (int c = z; c < C; c += Z) {
+        if (!(s_keep[c] && s_formed[c])) continue;  // CTA-uniform
+        materialise(H, d, inv, mu, b, N, C, c, s_prev, s_red);
+      }
+      __syncthreads();
+      for (int c = tid; c < C; c += kGramThreads) s_formed[c] = s_keep[c] ? 0 : 1;
+      if (p > 1)
+        for (int k = tid; k < M; k += kGramThreads) s_prev[s_chg[k]] = s_lab[s_chg[k]];
       __syncthreads();
     }
     // (M == 0: S, the counts and the norms are those of the last pass)
@@ -518,8 +592,13 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
     // (M == 0: the same inputs gave the same labels and objective)
     if (obj != nullptr && z == 0 && tid == 0) obj[(size_t)b * obj_ld + p] = last_obj;
   }
-  for (int r = tid; r < nrow; r += kGramThreads)
-    assign[(size_t)b * N + row0 + r] = s_lab[row0 + r];
+  for (int r = tid; r < nrow; r += kGramThreads) {
+    const size_t i = (size_t)b * N + row0 + r;
+    assign[i] = s_lab[row0 + r];
+    prev[i] = s_prev[row0 + r];
+    const float iv = inv[i];
+    rho[i] = iv > 0.f ? s_best[r] / iv : 0.f;  // <h, mu> = ||h|| cos
+  }
   if (tid == 0 && *abort_flag) {  // copies still in flight must land before the CTA leaves
     const uint64_t t0 = tc::globaltimer();
     while (!tc::mbar_try_wait(bar, 0) && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
@@ -568,7 +647,9 @@ int gram_capacity(int z, size_t smem) {
 
 GramPlan gram_plan(int dtype, int B, int N, int d, int C) {
   GramPlan g{};
-  if (dtype != PS_BF16 || B < 1 || N < 2 || N > 1024 || C < 1 || C > 256 || d < 64) return g;
+  if (dtype != PS_BF16 || B < 1 || N < 2 || N > 1024 || C < 1 || C > 256 || d < 64 ||
+      d > kGramMaxD || d % 8 != 0)
+    return g;
   g.R = ceil_div(ceil_div(N, kGramMaxZ), 16) * 16;
   g.Z = ceil_div(N, g.R);
   g.smem = gram_smem(N, C, g.R, g.Z).total;
@@ -607,8 +688,10 @@ cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* i
 }
 
 cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,
-                         int C, int passes, int32_t* assign, float* L, const float* objp0,
-                         int ntile0, float* obj, int obj_ld, int* status, cudaStream_t s) {
+                         int C, int passes, const __nv_bfloat16* H, int d, const float* inv,
+                         float* mu, int32_t* assign, int32_t* prev, float* rho, float* L,
+                         const float* objp0, int ntile0, float* obj, int obj_ld, int* status,
+                         cudaStream_t s) {
   if (gram_capacity(g.Z, g.smem) < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.Z, B, 1);
@@ -622,8 +705,8 @@ cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* q
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launch_ex(cfg, k_km_gram, qhi, qlo, N, C, g.R, passes, assign, L, objp0, ntile0, obj,
-                   obj_ld, status);
+  return launch_ex(cfg, k_km_gram, qhi, qlo, N, C, g.R, passes, H, d, inv, mu, assign, prev, rho,
+                   L, objp0, ntile0, obj, obj_ld, status);
 }
 
 }  // namespace ps

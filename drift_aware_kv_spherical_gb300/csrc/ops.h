@@ -29,10 +29,14 @@ bool gram_launchable(const GramPlan& g);
 // K = X X^T of every window in 24-bit fixed point (qhi/qlo: B * Z * N * R each)
 cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
                        int N, int d, int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s);
-// passes 1..passes from the labels in assign and the cosines L of pass 0
+// passes 1..passes from the labels in assign and the cosines L of pass 0;
+// leaves the last pass's labels in assign, the pass before's in prev, rho,
+// the objectives, and in mu the centroids that stopped being formed
 cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,
-                         int C, int passes, int32_t* assign, float* L, const float* objp0,
-                         int ntile0, float* obj, int obj_ld, int* status, cudaStream_t s);
+                         int C, int passes, const __nv_bfloat16* H, int d, const float* inv,
+                         float* mu, int32_t* assign, int32_t* prev, float* rho, float* L,
+                         const float* objp0, int ntile0, float* obj, int obj_ld, int* status,
+                         cudaStream_t s);
 
 struct Nvfp4Args {
   const void* H; int dtype; const float* mu; const int32_t* assign;
