@@ -404,19 +404,26 @@ struct KmAssignClusterEpi : TcEpiBase {
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   }
+  // scratch: 1/||h|| of this CTA's rows of the tile
+  __device__ void prefetch(uint8_t* scratch, int k, int n) const {
+    const int t = blockIdx.y, b = t / mtb, mt = t % mtb;
+    const int z = blockIdx.z, nz = gridDim.z;
+    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    float* s_inv = reinterpret_cast<float*>(scratch);
+    for (int j = k; j < r1 - r0; j += n) {
+      const int i = mt * 128 + r0 + j;
+      s_inv[j] = i < N ? inv[(long)b * N + i] : 0.f;
+    }
+  }
   __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
     const int t = blockIdx.y, b = t / mtb, mt = t % mtb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;  // <= 64 rows (nz >= 2)
-    float* s_inv = reinterpret_cast<float*>(scratch);       // [64]
-    float* cosv = s_inv + 64;                               // [64]
-    for (int j = threadIdx.x; j < r1 - r0; j += blockDim.x) {
-      const int i = mt * 128 + r0 + j;
-      s_inv[j] = i < N ? inv[(long)b * N + i] : 0.f;
-    }
+    const float* s_inv = reinterpret_cast<const float*>(scratch);  // [64], staged by prefetch
+    float* cosv = reinterpret_cast<float*>(scratch) + 64;          // [64]
     // the summed scores replace this CTA's own rows [r0, r1), which only it reads
     float* own = const_cast<float*>(red);
-    cluster_rows_sum<8>(red, kLd, r0, r1, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
+    cluster_rows_sum<8, 32>(red, kLd, r0, r1, (C + 3) & ~3, nz, [&](int r, int c, float4 v) {
       *reinterpret_cast<float4*>(own + r * kLd + c) = v;
     });
     tc::cluster_arrive();

@@ -44,6 +44,15 @@ constexpr int kGramThreads = 512;
 constexpr int kGramMaxZ = 16;
 constexpr float kGramScale = 1048576.f;  // 2^20 units per unit cosine
 
+// q = 256 hi + lo, sign-extended from 24 bits, assembled by one byte permute:
+// bytes (lo, hi.low, hi.high, sign of hi.high) of the pair {l, h}; sel picks
+// row k of a four-row group (lo byte k of l, int16 k % 2 of h)
+__device__ __forceinline__ int q24(uint32_t l, uint32_t h, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(l), "r"(h), "r"(sel));
+  return static_cast<int>(r);
+}
+
 // q of rows 2l and 2l + 1 from their packed high parts (two int16) and low bytes
 __device__ __forceinline__ int q_lo(uint32_t h, uint32_t l) {
   return static_cast<int>(static_cast<int16_t>(h & 0xffffu)) * 256 + static_cast<int>(l & 0xffu);
@@ -124,6 +133,22 @@ struct GramClusterEpi : TcEpiBase {
     *reinterpret_cast<uint4*>(qhi + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint2*>(qlo + off) = make_uint2(l[0], l[1]);
   }
+  // scratch: 1/||h|| of the tile's 128 rows and 128 columns, then off() of both
+  __device__ void prefetch(uint8_t* scratch, int i, int n) const {
+    int b, mt, nt;
+    tile_of(blockIdx.y, b, mt, nt);
+    float* s_ir = reinterpret_cast<float*>(scratch);
+    float* s_ic = s_ir + 128;
+    long long* s_ro = reinterpret_cast<long long*>(s_ic + 128);
+    long long* s_co = s_ro + 128;
+    for (int k = i; k < 128; k += n) {
+      const int r = mt * 128 + k, c = nt * 128 + k;
+      s_ir[k] = r < N ? inv[(long)b * N + r] : 0.f;
+      s_ic[k] = c < N ? inv[(long)b * N + c] : 0.f;
+      s_ro[k] = slab_off(b, r);
+      s_co[k] = slab_off(b, c);
+    }
+  }
   __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
     const int t = blockIdx.y;
     int b, mt, nt;
@@ -132,18 +157,10 @@ struct GramClusterEpi : TcEpiBase {
     // below take eight rows from a multiple of 8); nz <= 8 leaves nr >= 8
     const int r0 = (z * 128 / nz) & ~7, r1 = z + 1 == nz ? 128 : ((z + 1) * 128 / nz) & ~7;
     const int nr = r1 - r0;
-    float* s_ir = reinterpret_cast<float*>(scratch);  // [128] 1/||h|| of the rows
-    float* s_ic = s_ir + 128;                         // [128] and of the columns
-    long long* s_ro = reinterpret_cast<long long*>(s_ic + 128);  // [128] off(i) of the rows
-    long long* s_co = s_ro + 128;                                // [128] off(j) of the columns
-    for (int k = threadIdx.x; k < 128; k += blockDim.x) {
-      const int i = mt * 128 + k, j = nt * 128 + k;
-      s_ir[k] = i < N ? inv[(long)b * N + i] : 0.f;
-      s_ic[k] = j < N ? inv[(long)b * N + j] : 0.f;
-      s_ro[k] = slab_off(b, i);
-      s_co[k] = slab_off(b, j);
-    }
-    __syncthreads();
+    const float* s_ir = reinterpret_cast<const float*>(scratch);  // staged by prefetch
+    const float* s_ic = s_ir + 128;
+    const long long* s_ro = reinterpret_cast<const long long*>(s_ic + 128);
+    const long long* s_co = s_ro + 128;
     // the quantised sums replace this CTA's own rows [r0, r1), which only it reads
     int* own = reinterpret_cast<int*>(const_cast<float*>(red));
     auto quant = [&](int r, int c, float4 v) {
@@ -154,9 +171,9 @@ struct GramClusterEpi : TcEpiBase {
       *reinterpret_cast<int4*>(own + r * kLd + c) = q;
     };
     if (nz <= 4)
-      cluster_rows_sum<4>(red, kLd, r0, r1, 128, nz, quant);
+      cluster_rows_sum<4, 32>(red, kLd, r0, r1, 128, nz, quant);
     else
-      cluster_rows_sum<8>(red, kLd, r0, r1, 128, nz, quant);
+      cluster_rows_sum<8, 32>(red, kLd, r0, r1, 128, nz, quant);
     tc::cluster_arrive();
     __syncthreads();
     // K(i, j): eight rows of one column per item
@@ -406,44 +423,37 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
       __syncthreads();
 
       // S[r][c] = sum over members j of c of q(row0 + r, j).  Warp w takes
-      // positions [w N / 16, (w+1) N / 16) of the sorted list, lane l rows 2l
-      // and 2l + 1; a segment's sums go to S with one integer atomic per row.
+      // positions [w N / 16, (w+1) N / 16) of the sorted list; lane l rows
+      // 4 (l % 16) .. + 3, the two half-warps alternate positions, and a
+      // segment's sums (halves combined) go to S with one atomic per row.
       const int p0 = warp * N / nwarps, p1 = (warp + 1) * N / nwarps;
-      const int r2 = 2 * lane;
-      const bool act = r2 < R;
+      const int half = lane >> 4, r4 = 4 * (lane & 15);
+      const bool act = r4 < R;
       int pp = p0;
       if (pp < p1) {
         int c = s_lab[s_perm[pp]];
         while (true) {
           const int e = min(s_off[c + 1], p1);
+          int a[4] = {0, 0, 0, 0};
           if (act) {
-            int a0 = 0, a1 = 0;
-            for (; pp + 4 <= e; pp += 4) {
-              uint32_t h[4], l[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = s_perm[pp + u];
-                h[u] = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
-                l[u] = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                a0 += q_lo(h[u], l[u]);
-                a1 += q_hi(h[u], l[u]);
-              }
+            for (int q = pp + half; q < e; q += 2) {
+              const int j = s_perm[q];
+              const uint2 h = *reinterpret_cast<const uint2*>(s_hi + j * R + r4);
+              const uint32_t l = *reinterpret_cast<const uint32_t*>(s_lo + j * R + r4);
+              a[0] += q24(l, h.x, 0xD540u);
+              a[1] += q24(l, h.x, 0xF761u);
+              a[2] += q24(l, h.y, 0xD542u);
+              a[3] += q24(l, h.y, 0xF763u);
             }
-            for (; pp < e; ++pp) {
-              const int j = s_perm[pp];
-              const uint32_t h = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
-              const uint32_t l = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
-              a0 += q_lo(h, l);
-              a1 += q_hi(h, l);
-            }
-            atomicAdd(&s_S[r2 * ldS + c], a0);
-            atomicAdd(&s_S[(r2 + 1) * ldS + c], a1);
-          } else {
-            pp = e;
           }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) a[k] += __shfl_xor_sync(0xffffffffu, a[k], 16);
+          if (act && half == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) atomicAdd(&s_S[(r4 + k) * ldS + c], a[k]);
+          }
+          pp = e;
           if (pp >= p1) break;
           c = s_lab[s_perm[pp]];
         }
@@ -506,7 +516,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
         for (int q = 0; q < Z; ++q) n += s_slot[q * C + c];
         const bool keep = s_hist[c] == 0 || n <= 0;
         s_keep[c] = keep ? 1 : 0;
-        s_invn[c] = keep ? 0.f : 0.0009765625f / sqrtf(static_cast<float>(n));
+        s_invn[c] = keep ? -1.f : 0.0009765625f / sqrtf(static_cast<float>(n));  // < 0: kept
       }
       __syncthreads();
       // a centroid formed in the last pass but kept from this one stays as
@@ -534,17 +544,30 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
       if (r < R) {
         const bool valid = r < nrow;
         float* Lrow = L + ((size_t)b * N + (valid ? row0 + r : 0)) * C;
-        for (int c = sub; c < C; c += 8) {
-          float v;
-          if (s_keep[c]) {
-            v = valid ? Lrow[c] : 0.f;
-          } else {
-            v = static_cast<float>(s_S[r * ldS + c]) * s_invn[c];
-            if (valid && M > 0) Lrow[c] = v;
+        for (int c0 = sub; c0 < C; c0 += 64) {  // eight clusters' loads, then their use
+          int sv[8];
+          float mv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = c0 + 8 * k;
+            sv[k] = c < C ? s_S[r * ldS + c] : 0;
+            mv[k] = c < C ? s_invn[c] : -1.f;
           }
-          if (v > bv) {
-            bv = v;
-            bi = c;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = c0 + 8 * k;
+            if (c >= C) break;
+            float v;
+            if (mv[k] >= 0.f) {
+              v = static_cast<float>(sv[k]) * mv[k];
+              if (valid && M > 0) Lrow[c] = v;
+            } else {
+              v = valid ? Lrow[c] : 0.f;
+            }
+            if (v > bv) {
+              bv = v;
+              bi = c;
+            }
           }
         }
       }

@@ -295,7 +295,7 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
   __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
     const int t = blockIdx.y, n0 = blockIdx.x * BN;
     const int r0 = z * 128 / nz, r1 = min((z + 1) * 128 / nz, this->M - t * 128);
-    cluster_rows_sum<8>(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
+    cluster_rows_sum<8, 32>(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
       const long o = (long)(t * 128 + r) * this->nkv + n0 + c;
       split_store(this->khi + o, this->klo + o, v.x);
       split_store(this->khi + o + 1, this->klo + o + 1, v.y);

@@ -101,6 +101,11 @@ struct TcCfg {
 //        epilogue's own and every CTA takes the whole K range)
 //   bool tile_range(int T, int* begin, int* end, int* step)  optional
 //        override of the CTA's tile walk (returns true when it applies)
+//   void prefetch(uint8_t* scratch, int i, int n)  optional: run by the n
+//        epilogue threads (index i) before they wait for the first
+//        accumulator, to stage data the epilogue reads later into the
+//        scratch (with kClusterReduce, read in reduce(), after the CTA and
+//        cluster barriers)
 // and with kClusterReduce (instead of consume / tile_done):
 //   void consume_red(t, r, n0, z, taddr, State&, float* red_row)
 //        red_row = this row's slot in the CTA's result (kRedLd floats), or
@@ -295,6 +300,8 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     const int quarter = warp & 3, part = (warp - 2) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int r = quarter * 32 + lane;
+    // the epilogue warps stage their per-tile data while the mainloop runs
+    epi.prefetch(epi_scratch, threadIdx.x - 64, 32 * Epi::kEpiWarps);
     typename Epi::State est;
     int tcount = 0;
     for (int t = t_begin; t < t_end; t += t_step, ++tcount) {
@@ -354,6 +361,7 @@ struct TcEpiBase {
   static constexpr bool kClusterReduce = false;
   static constexpr bool kZSplitsK = true;
   __device__ bool tile_range(int, int*, int*, int*) const { return false; }
+  __device__ void prefetch(uint8_t*, int, int) const {}
   __device__ int ahead(int) const { return 0; }
   __device__ int bkoff(int) const { return 0; }
   __device__ int bsel(int, int) const { return 0; }
@@ -369,12 +377,14 @@ __device__ __forceinline__ void epi_bar_sync_n() {
 // Rows [r0, r1) of the cluster's Z (<= ZMAX) results (row stride ld floats,
 // at `red` in every CTA's shared memory), summed in rank order four columns
 // at a time by all threads of the CTA; each thread issues the loads of a
-// batch of items (every rank) before using any.  f(r, c, sum) takes columns
+// batch of items (every rank, LOADS 16-byte loads: 32 where the kernel's
+// registers allow) before using any, since a distributed-shared-memory load
+// is a round trip of about half a microsecond.  f(r, c, sum) takes columns
 // c..c+3 of row r.  ncol: a multiple of 4.
-template <int ZMAX, class F>
+template <int ZMAX, int LOADS = 16, class F>
 __device__ __forceinline__ void cluster_rows_sum(const float* red, uint32_t ld, int r0, int r1,
                                                  int ncol, int Z, F&& f) {
-  constexpr int kBatch = 16 / ZMAX > 1 ? 16 / ZMAX : 1;
+  constexpr int kBatch = LOADS / ZMAX > 1 ? LOADS / ZMAX : 1;
   uint32_t base[ZMAX];
   const uint32_t local = tc::smem_u32(red);
 #pragma unroll

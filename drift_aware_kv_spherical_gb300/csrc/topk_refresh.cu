@@ -315,21 +315,28 @@ struct RefreshClusterEpi : RefreshEpi<BN> {
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   }
+  // scratch: destination rows of this CTA's share of the tile (split regime)
+  __device__ void prefetch(uint8_t* scratch, int k, int n) const {
+    const int Mt = *this->M_total;
+    if (Mt > this->split_max_rows) return;
+    const int t = blockIdx.y, z = blockIdx.z, nz = gridDim.z;
+    const int live = min(128, Mt - t * 128);
+    const int r0 = min(z * 128 / nz, live), r1 = min((z + 1) * 128 / nz, live);
+    int* s_ri = reinterpret_cast<int*>(scratch);
+    for (int j = k; j < r1 - r0; j += n) s_ri[j] = this->rowinfo[t * 128 + r0 + j];
+  }
   __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
     const int Mt = *this->M_total;
     if (Mt <= this->split_max_rows) {
       const int t = blockIdx.y, n0 = blockIdx.x * BN, nkv = this->nkv;
-      const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;  // <= 64 rows (nz >= 2)
+      // rows of this CTA's share that hold selected positions (<= 64, nz >= 2)
+      const int live = min(128, Mt - t * 128);
+      const int r0 = min(z * 128 / nz, live), r1 = min((z + 1) * 128 / nz, live);
       const bool is_v = n0 >= nkv;
-      int* s_ri = reinterpret_cast<int*>(scratch);  // [64] destination rows, one pass
-      for (int j = threadIdx.x; j < r1 - r0; j += blockDim.x) {
-        const int m = t * 128 + r0 + j;
-        s_ri[j] = m < Mt ? this->rowinfo[m] : -1;
-      }
-      __syncthreads();
+      const int* s_ri = reinterpret_cast<const int*>(scratch);  // [64], staged by prefetch
       __nv_bfloat16* cache = is_v ? this->Vc : this->Kc;
       const int coff = is_v ? n0 - nkv : n0;
-      cluster_rows_sum<4>(red, kLd, r0, r1, BN, nz, [&](int r, int c, float4 v) {
+      cluster_rows_sum<4, 32>(red, kLd, r0, r1, BN, nz, [&](int r, int c, float4 v) {
         const int ri = s_ri[r - r0];
         if (ri < 0) return;
         const int b = ri / this->N, p = ri % this->N;
