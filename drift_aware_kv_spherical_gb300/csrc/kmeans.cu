@@ -255,12 +255,13 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
 // Set-up of a call, in one launch: blocks [0, inv_blocks) take 1/||h_i||
 // for 8 rows each (a warp per row, its 16-byte loads unrolled four deep);
 // the rest split mu (fp32) into bf16 hi + lo parts (hi = bf16(mu), lo =
-// bf16(mu - hi)), four values per thread.  Either part may be empty.
+// bf16(mu - hi)), four values per thread, into two [B][C][d] arrays or
+// (cd = C d > 0) one [B][2C][d] array at hi.  Either part may be empty.
 template <typename T>
 __global__ void __launch_bounds__(256)
 k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, int inv_blocks,
           const float* __restrict__ mu, long n_mu, __nv_bfloat16* __restrict__ hi,
-          __nv_bfloat16* __restrict__ lo) {
+          __nv_bfloat16* __restrict__ lo, long cd) {
   pdl_prologue();
   if ((int)blockIdx.x < inv_blocks) {
     constexpr int V = Vec<T>::n;
@@ -284,16 +285,20 @@ k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, in
   const long stride = (long)(gridDim.x - inv_blocks) * blockDim.x;
   for (long i = (long)(blockIdx.x - inv_blocks) * blockDim.x + threadIdx.x; i < n4;
        i += stride) {
+    // cd > 0: one [2C][d] block per window, the C hi rows then the C lo rows
+    const long e = 4 * i;
+    const long eh = cd > 0 ? (e / cd) * 2 * cd + e % cd : e;
+    const long el = cd > 0 ? eh + cd : e;
     const float4 x = reinterpret_cast<const float4*>(mu)[i];
     const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
     const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
     const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
     const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
     const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
-    reinterpret_cast<uint2*>(hi)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
-                                                 *reinterpret_cast<const uint32_t*>(&h1));
-    reinterpret_cast<uint2*>(lo)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
-                                                 *reinterpret_cast<const uint32_t*>(&l1));
+    *reinterpret_cast<uint2*>(hi + eh) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                    *reinterpret_cast<const uint32_t*>(&h1));
+    *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
+                                                    *reinterpret_cast<const uint32_t*>(&l1));
   }
 }
 
@@ -832,6 +837,7 @@ struct KmWs {
   float* part;
   float* L;        // Gram form: [B][N][C] cosines carried for kept centroids
   int32_t* prev;   // Gram form: labels of pass I - 1
+  __nv_bfloat16* mu_split;  // Gram form with pass 0 inside: [B][2C][d] hi, lo rows
   int16_t* qhi;    // Gram form: fixed-point Gram matrices, high and low parts
   uint8_t* qlo;
 };
@@ -854,6 +860,7 @@ KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int 
     const size_t q = (size_t)B * g.Z * N * g.R;
     w.L = cv.take<float>((size_t)BN_ * C);
     w.prev = cv.take<int32_t>((size_t)BN_);
+    if (g.fused0) w.mu_split = cv.take<__nv_bfloat16>((size_t)B * 2 * C * d);
     w.qhi = cv.take<int16_t>(q);
     w.qlo = cv.take<uint8_t>(q);
   }
@@ -900,6 +907,13 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const KmWs w = km_carve(a.ws, p, g, a.B, a.N, a.d, a.C, nullptr);
   const ScanPlan sp = scan_plan<T>(a.B, a.d, a.C);
 
+  const bool gram = p.tc && g.ok && a.iters >= 2 && !kmeans_lloyd_forced() &&
+                    gram_launchable(g);
+  const bool fused0 = gram && g.fused0;  // pass 0 inside the Gram GEMM
+  __nv_bfloat16* split_hi = fused0 ? w.mu_split : w.mu_hi;
+  __nv_bfloat16* split_lo = fused0 ? w.mu_split : w.mu_lo;
+  const long cd = fused0 ? (long)a.C * a.d : 0;
+
   // 1/||h|| and (tensor cores) the split of the given centroids in one
   // launch; with k-means++ seeding the split waits for the seeds
   const int inv_blocks = ceil_div(BN_ * 32, 256);
@@ -907,7 +921,7 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const int split_blocks = n_mu > 0 ? std::min(ceil_div(n_mu / 4, 256), 2 * kSmTarget) : 0;
   const bool seeding = a.init_mode == 1;
   launch_pdl(k_km_prep<T>, inv_blocks + (seeding ? 0 : split_blocks), 256, 0, s, H, BN_, a.d,
-             w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, w.mu_hi, w.mu_lo);
+             w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, split_hi, split_lo, cd);
   if (seeding) {
     for (int r = 0; r < a.C; ++r) {
       launch_pdl(k_kpp_pick<T>, a.B, 1024, 0, s, H, w.inv, a.init_u, a.N, a.d, a.C, r, a.mu,
@@ -918,7 +932,7 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     if (split_blocks > 0)
       launch_pdl(k_km_prep<T>, split_blocks, 256, 0, s, H, 0L, a.d, w.inv, 0, a.mu, n_mu,
-                 w.mu_hi, w.mu_lo);
+                 split_hi, split_lo, cd);
   }
   auto assign_pass = [&](float* scores) {
     switch (p.BN) {
@@ -928,17 +942,20 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
       default: return assign_tc<256>(a, p, w, scores, s);
     }
   };
-  // Gram form: pass 0 against the given centroids (its cosines seed the
-  // carried columns), passes 1..I on the Gram matrices, then one scan that
+  // Gram form: pass 0's cosines against the given centroids (in the Gram
+  // GEMM's launch for C <= 64, else a tensor-core pass) seed the carried
+  // columns; passes 0 (arg-max) or 1..I run on the Gram matrices; one scan
   // forms mu^(I) from the labels of pass I - 1 and C_hat from those of pass I
-  if (p.tc && g.ok && a.iters >= 2 && !kmeans_lloyd_forced() && gram_launchable(g)) {
+  if (gram) {
     const auto* Hb = static_cast<const __nv_bfloat16*>(a.H);
-    cudaError_t e = assign_pass(w.L);
+    cudaError_t e = fused0 ? cudaSuccess : assign_pass(w.L);
     if (e == cudaSuccess)
-      e = gram_build(g, Hb, w.inv, a.B, a.N, a.d, w.qhi, w.qlo, a.status, s);
+      e = gram_build(g, Hb, w.inv, a.B, a.N, a.d, a.C, fused0 ? w.mu_split : nullptr, w.L,
+                     w.qhi, w.qlo, a.status, s);
     if (e == cudaSuccess)
       e = gram_iterate(g, w.qhi, w.qlo, a.B, a.N, a.C, a.iters, Hb, a.d, w.inv, a.mu, a.assign,
-                       w.prev, a.rho, w.L, w.objp, p.ntile, a.obj, a.iters + 1, a.status, s);
+                       w.prev, a.rho, w.L, fused0 ? nullptr : w.objp, p.ntile, a.obj,
+                       a.iters + 1, a.status, s);
     if (e == cudaSuccess)
       e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C, sp.W,
                                 a.mu, nullptr, nullptr, a.counts, a.chat, w.objp, p.ntile,

@@ -66,19 +66,29 @@ __device__ __forceinline__ int gram_quant(float k) {
   return min(max(q, -8388607), 8388607);
 }
 
-// Tile t of the Gram GEMM = (window b, row block mt <= column block nt), the
-// upper triangle of the window's 128 x 128 blocks in row-major order.
+// Tile t of the Gram GEMM = (window b, u = t mod T): u < T0 is a Gram tile,
+// row block mt <= column block nt, the upper triangle of the window's
+// 128 x 128 blocks in row-major order; with pass 0 in the launch, u = T0 + mt
+// is row block mt against the window's [2C][d] block of centroid hi and lo
+// rows (B map 1), whose summed columns are the rows' cosines against the
+// given centroids (nt = -1).
 struct GramClusterEpi : TcEpiBase {
   static constexpr bool kClusterReduce = true;
   static constexpr uint32_t kLd = 128 + 4;
-  int B, N, mtb, T, R, Z;
+  int B, N, mtb, T, T0, R, Z, C;
   const float* inv;
   int16_t* qhi;
   uint8_t* qlo;
+  float* cos0;  // [B][N][C] pass-0 cosines (centroid tiles)
   struct State {};
   __device__ void tile_of(int t, int& b, int& mt, int& nt) const {
     b = t / T;
     int u = t % T;
+    if (u >= T0) {
+      mt = u - T0;
+      nt = -1;
+      return;
+    }
     mt = 0;
     while (u >= mtb - mt) {
       u -= mtb - mt;
@@ -92,10 +102,11 @@ struct GramClusterEpi : TcEpiBase {
     tile_of(t, b, mt, nt);
     return b * N + mt * 128;
   }
+  __device__ int bsel(int t, int) const { return t % T >= T0 ? 1 : 0; }
   __device__ int bcoord(int t, int) const {
     int b, mt, nt;
     tile_of(t, b, mt, nt);
-    return b * N + nt * 128;
+    return nt < 0 ? b * 2 * C : b * N + nt * 128;
   }
   __device__ void consume_red(int, int, int, int, uint32_t taddr, State&,
                               float* red_row) const {
@@ -144,6 +155,7 @@ struct GramClusterEpi : TcEpiBase {
     for (int k = i; k < 128; k += n) {
       const int r = mt * 128 + k, c = nt * 128 + k;
       s_ir[k] = r < N ? inv[(long)b * N + r] : 0.f;
+      if (nt < 0) continue;
       s_ic[k] = c < N ? inv[(long)b * N + c] : 0.f;
       s_ro[k] = slab_off(b, r);
       s_co[k] = slab_off(b, c);
@@ -161,6 +173,25 @@ struct GramClusterEpi : TcEpiBase {
     const float* s_ic = s_ir + 128;
     const long long* s_ro = reinterpret_cast<const long long*>(s_ic + 128);
     const long long* s_co = s_ro + 128;
+    if (nt < 0) {  // centroid tile: cos = (<h, mu_hi> + <h, mu_lo>) / ||h||
+      float* sums = const_cast<float*>(red);  // this CTA's rows, summed in place
+      auto keep = [&](int r, int c, float4 v) {
+        *reinterpret_cast<float4*>(sums + r * kLd + c) = v;
+      };
+      const int ncol = (2 * C + 3) & ~3;
+      if (nz <= 4)
+        cluster_rows_sum<4, 32>(red, kLd, r0, r1, ncol, nz, keep);
+      else
+        cluster_rows_sum<8, 32>(red, kLd, r0, r1, ncol, nz, keep);
+      tc::cluster_arrive();
+      __syncthreads();
+      for (int it = threadIdx.x; it < nr * C; it += blockDim.x) {
+        const int r = r0 + it / C, c = it % C, i = mt * 128 + r;
+        if (i < N)
+          cos0[((long)b * N + i) * C + c] = (sums[r * kLd + c] + sums[r * kLd + C + c]) * s_ir[r];
+      }
+      return;
+    }
     // the quantised sums replace this CTA's own rows [r0, r1), which only it reads
     int* own = reinterpret_cast<int*>(const_cast<float*>(red));
     auto quant = [&](int r, int c, float4 v) {
@@ -316,7 +347,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
           const float* __restrict__ inv, float* __restrict__ mu, int32_t* __restrict__ assign,
           int32_t* __restrict__ prev, float* __restrict__ rho, float* __restrict__ L,
           const float* __restrict__ objp0, int ntile0, float* __restrict__ obj, int obj_ld,
-          int* status) {
+          int pass0, int* status) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int Z = gridDim.x, z = blockIdx.x, b = blockIdx.y;
   const GramSmem o = gram_smem(N, C, R, Z);
@@ -354,6 +385,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
     tc::fence_mbar_init();
   }
   __syncthreads();
+  tc::cluster_arrive();  // this CTA has started (awaited before the first remote access)
   if (tid == 0) {
     const uint8_t* gh = reinterpret_cast<const uint8_t*>(qhi + ((size_t)b * Z + z) * slab);
     const uint8_t* gl = qlo + ((size_t)b * Z + z) * slab;
@@ -365,10 +397,11 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
       tc::bulk_load(sm + o.lo + k, gl + k, static_cast<uint32_t>(min((size_t)32768, slab - k)),
                     bar);
   }
-  for (int j = tid; j < N; j += kGramThreads)
-    s_lab[j] = static_cast<uint8_t>(assign[(size_t)b * N + j]);
+  if (!pass0)
+    for (int j = tid; j < N; j += kGramThreads)
+      s_lab[j] = static_cast<uint8_t>(assign[(size_t)b * N + j]);
   for (int c = tid; c < C; c += kGramThreads) s_formed[c] = 0;  // pass 0 used the given centroids
-  if (obj != nullptr && z == 0) {  // block-uniform: the objective of pass 0
+  if (!pass0 && obj != nullptr && z == 0) {  // block-uniform: the objective of pass 0
     float so = 0.f;
     for (int t = tid; t < ntile0; t += kGramThreads) so += objp0[(size_t)b * ntile0 + t];
     so = block_sum_f32(so, s_red);
@@ -377,6 +410,62 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
   // every thread observes the slab's arrival (a timeout leaves the status set
   // and the passes run on whatever landed; the copies are awaited before exit)
   tc::mbar_wait(bar, 0, status, abort_flag);
+  tc::cluster_wait();  // every CTA of the cluster has started
+
+  if (pass0) {
+    // pass 0 from L, the cosines against the given centroids: arg-max of
+    // this CTA's rows (8 threads per row), then labels and the objective's
+    // partial to the cluster as after every pass
+    const int r = tid >> 3, sub = tid & 7;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (r < nrow) {
+      const float* Lrow = L + ((size_t)b * N + row0 + r) * C;
+      for (int c = sub; c < C; c += 8) {
+        const float v = Lrow[c];
+        if (v > bv) {
+          bv = v;
+          bi = c;
+        }
+      }
+    }
+#pragma unroll
+    for (int d2 = 1; d2 < 8; d2 <<= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d2);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d2);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (sub == 0 && r < R) {
+      if (bi == INT_MAX) {
+        bi = 0;
+        bv = 0.f;
+      }
+      s_newlab[r] = static_cast<uint8_t>(bi);
+      s_best[r] = r < nrow ? bv : 0.f;
+    }
+    __syncthreads();
+    if (obj != nullptr && warp == 0) {
+      float so = 0.f;
+      for (int q = lane; q < R; q += 32) so += s_best[q];
+      so = warp_sum(so);
+      if (lane == 0) tc::st_dsmem_f32(tc::cluster_map(tc::smem_u32(s_objp + z), 0), so);
+    }
+    const int words = R / 4;
+    for (int k = tid; k < Z * words; k += kGramThreads) {
+      const int q = k / words, w = k % words;
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(s_newlab + 4 * w);
+      tc::st_dsmem_u32(tc::cluster_map(tc::smem_u32(s_lab + row0 + 4 * w), q), v);
+    }
+    tc::cluster_sync_all();
+    if (obj != nullptr && z == 0 && tid == 0) {
+      float so = 0.f;
+      for (int q = 0; q < Z; ++q) so += s_objp[q];
+      obj[(size_t)b * obj_ld] = so;
+    }
+  }
 
   float last_obj = 0.f;  // CTA 0, thread 0: the latest pass objective
   for (int p = 1; p <= passes; ++p) {
@@ -678,11 +767,13 @@ GramPlan gram_plan(int dtype, int B, int N, int d, int C) {
   g.smem = gram_smem(N, C, g.R, g.Z).total;
   if (g.smem > 227 * 1024) return g;
   g.mtb = ceil_div(N, 128);
-  g.T = g.mtb * (g.mtb + 1) / 2;
+  g.T0 = g.mtb * (g.mtb + 1) / 2;
+  g.fused0 = 2 * C <= 128;  // the centroids' hi and lo rows fit one 128-row B tile
+  g.T = g.T0 + (g.fused0 ? g.mtb : 0);
   g.KB = ceil_div(d, 64);
   const int tiles = B * g.T;
   g.nz = 1;
-  for (int z = 8; z >= 2; z /= 2)
+  for (int z = 8; z >= 2; --z)
     if (z <= g.KB && (long)tiles * z <= kSmTarget && tiles <= tc_cluster_capacity(z)) {
       g.nz = z;
       break;
@@ -698,16 +789,21 @@ bool gram_launchable(const GramPlan& g) {
 }
 
 cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
-                       int N, int d, int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s) {
+                       int N, int d, int C, const __nv_bfloat16* mu_split, float* cos0,
+                       int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s) {
   TcMaps maps;
   if (!make_tmap_bf16_2d(&maps.a[0], H, d, (uint64_t)B * N, (uint64_t)d * 2, 64, 128))
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   maps.b[0] = maps.a[0];
   maps.b[1] = maps.a[0];
+  if (mu_split != nullptr &&
+      !make_tmap_bf16_2d(&maps.b[1], mu_split, d, (uint64_t)B * 2 * C, (uint64_t)d * 2, 64, 128))
+    return cudaErrorInvalidValue;
+  const int T = mu_split != nullptr ? g.T : g.T0;
   TcShape sh{B * N, nullptr, g.KB, g.kpc, status, INT_MAX};
-  GramClusterEpi epi{{}, B, N, g.mtb, g.T, g.R, g.Z, inv, qhi, qlo};
-  return launch_tc_gemm<128, 1, 1, false>(maps, sh, epi, dim3(1, B * g.T, g.nz), s);
+  GramClusterEpi epi{{}, B, N, g.mtb, T, g.T0, g.R, g.Z, C, inv, qhi, qlo, cos0};
+  return launch_tc_gemm<128, 1, 1, false>(maps, sh, epi, dim3(1, B * T, g.nz), s);
 }
 
 cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,
@@ -729,7 +825,7 @@ cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* q
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return launch_ex(cfg, k_km_gram, qhi, qlo, N, C, g.R, passes, H, d, inv, mu, assign, prev, rho,
-                   L, objp0, ntile0, obj, obj_ld, status);
+                   L, objp0, ntile0, obj, obj_ld, objp0 == nullptr ? 1 : 0, status);
 }
 
 }  // namespace ps

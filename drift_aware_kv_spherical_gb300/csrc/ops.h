@@ -21,15 +21,20 @@ struct GramPlan {
   bool ok;
   int R, Z;      // rows per CTA, CTAs per window of the pass kernel
   size_t smem;   // its shared memory per CTA
-  int mtb, T;    // 128-row blocks, upper-triangle tiles per window
+  int mtb, T0, T;  // 128-row blocks, upper-triangle tiles per window, all tiles
+  bool fused0;     // C <= 64: pass 0's cosines are tiles of the Gram GEMM
   int KB, kpc, nz;  // the Gram GEMM's K blocks and split
 };
 GramPlan gram_plan(int dtype, int B, int N, int d, int C);
 bool gram_launchable(const GramPlan& g);
-// K = X X^T of every window in 24-bit fixed point (qhi/qlo: B * Z * N * R each)
+// K = X X^T of every window in 24-bit fixed point (qhi/qlo: B * Z * N * R
+// each); with mu_split ([B][2C][d] hi then lo rows of the given centroids)
+// also the pass-0 cosines cos0 [B][N][C]
 cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
-                       int N, int d, int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s);
-// passes 1..passes from the labels in assign and the cosines L of pass 0;
+                       int N, int d, int C, const __nv_bfloat16* mu_split, float* cos0,
+                       int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s);
+// passes 1..passes from the labels in assign and the cosines L of pass 0
+// (objp0 == nullptr: pass 0 itself too, from L);
 // leaves the last pass's labels in assign, the pass before's in prev, rho,
 // the objectives, and in mu the centroids that stopped being formed
 cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* qlo, int B, int N,

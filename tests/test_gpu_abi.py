@@ -101,10 +101,10 @@ def test_kernel_trace_records_every_launch(lib):
     rec = ps.ps_trace_records()
     ps.ps_check()
     names = [r[0] for r in rec]
-    assert len(names) == 5
+    assert len(names) == 4
     assert "k_km_prep" in names[0]
-    assert sum("k_tc_gemm" in x for x in names) == 2             # pass 0, the Gram GEMM
-    assert sum("k_km_gram" in x for x in names) == 1             # passes 1 .. I
+    assert sum("k_tc_gemm" in x for x in names) == 1             # Gram GEMM + pass-0 cosines
+    assert sum("k_km_gram" in x for x in names) == 1             # passes 0 .. I
     assert sum("k_cluster_scan" in x for x in names) == 1        # last update + C_hat
     assert all(ms > 0 for _, ms in rec)
     ps.ps_trace_enable(False)

@@ -138,8 +138,9 @@ def test_gram_form_matches_lloyd_form():
 
 
 def test_gram_trace_shape():
-    """The Gram form's launches: set-up, pass 0, the Gram GEMM, one kernel
-    for passes 1..I and one scan for the last update and C_hat."""
+    """The Gram form's launches for C <= 64: set-up, the Gram GEMM (with pass
+    0's cosines as extra tiles), one kernel for passes 0..I and one scan for
+    the last update and C_hat."""
     Ht, _, mu0 = _planted(1, 256, 128, 16, seed=2)
     mu = torch.from_numpy(mu0).cuda()
     ws = ps.workspace(ps.OP_KMEANS, B=1, N=256, d=128, C=16)
@@ -151,7 +152,7 @@ def test_gram_trace_shape():
     names = [r[0] for r in ps.ps_trace_records()]
     ps.ps_trace_enable(False)
     ps.ps_check()
-    assert len(names) == 5, names
+    assert len(names) == 4, names
     assert sum("k_km_gram" in x for x in names) == 1
     assert sum("GramClusterEpi" in x for x in names) == 1
 
