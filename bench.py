@@ -182,7 +182,8 @@ def op_work(w, npos_mean):
 
 # kernel trace names (the library's kernels, as the CUDA runtime names them)
 # -> what they compute
-KERNEL_KEYS = [("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
+KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
+               ("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
                ("k_km_prep", "kmeans_prep"),
                ("k_kpp_", "kmeans_seeding"), ("k_assign", "kmeans_assign"),
                ("k_fp4_amax", "nvfp4_amax"), ("k_fp4_quant", "nvfp4_quant"),
@@ -209,7 +210,16 @@ def kernel_work(key, w, npos_mean):
     nkv = w.Hkv * w.dh
     H = B * N * d * esz
     M = npos_mean * B
+    # Gram form (bf16, N <= 1024): 24-bit Gram slabs of R = 16 ceil(N / 256)
+    # rows per CTA over Z = ceil(N / R) CTAs; pass 0's cosines in the GEMM when
+    # 2C <= 128
+    R = 16 * -(-N // 256)
+    slab = B * -(-N // R) * N * R * 3
+    fused0 = 2 * C <= 128
     return {
+        "gram_gemm": (H + slab + (B * N * C * 4 if fused0 else 0),
+                      B * (float(N) * (N + 1) * d + (2.0 * N * C * d if fused0 else 0.0))),
+        "kmeans_passes": (slab + 2 * B * N * C * 4 + B * N * 12, 0.0),
         "kmeans_assign": (H + B * C * d * 4, 2.0 * B * N * C * d),
         "kmeans_update": (H + B * C * d * 4, 0.0),
         "kmeans_final": (B * N * 4 + 2 * B * C * d * 4, 0.0),
@@ -454,9 +464,7 @@ def main():
         with torch.cuda.graph(g, stream=cap):
             concurrent_step(parity)
         graphs.append(g)
-    launches = graph_kernel_count(graphs[0])
-    if launches is None:                            # runtime not reachable: plan count
-        launches = pipe.kernel_launches_per_step()
+    launches = graph_kernel_count(graphs[0])       # None if the runtime is unreachable
     stream = torch.cuda.current_stream(dev)
     for t in range(args.warmup):                    # graph warm-up
         load(step_no)
@@ -519,6 +527,8 @@ def main():
     trace = ps.ps_trace_records()
     ps.ps_trace_enable(False)
     ps.ps_check()
+    # the library's kernels per step: every launch of its calls is traced
+    lib_launches = round(len(trace) / ntrace)
 
     # end to end through the public API: inputs from pinned host memory every
     # step, the step's results read back
@@ -596,7 +606,8 @@ def main():
         "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
                 for op in ops},
         "clocks": clk,
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": lib_launches * args.steps,
+        "graph_kernel_nodes": launches,
         "eager_ms_per_step": eager_ms,
         "timing": "CUDA-graph replay of the whole step per timed step",
         "parallelism": f"replicas x{world}",

@@ -255,7 +255,7 @@ __host__ __device__ inline GramSmem gram_smem(int N, int C, int R, int Z) {
   uint32_t p = 0;
   o.hi = p;     p = al16(p + (uint32_t)N * R * 2);
   o.lo = p;     p = al16(p + (uint32_t)N * R);
-  o.S = p;      p = al16(p + (uint32_t)R * (C + 1) * 4);
+  o.S = p;      p = al16(p + (uint32_t)C * (R + 4) * 4);
   o.slot = p;   p = al16(p + (uint32_t)Z * C * 8);
   o.npart = p;  p = al16(p + (uint32_t)C * 8);
   o.lab = p;    p = al16(p + (uint32_t)Z * R);
@@ -376,7 +376,9 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = kGramThreads / 32;
   const int row0 = z * R, nrow = min(R, N - row0);
-  const int ldS = C + 1;
+  // S is [C][R + 4]: the arg-max's eight threads of four rows, and the
+  // builds' lanes on consecutive rows, fall on distinct banks (R % 16 == 0)
+  const int ldS = R + 4;
 
   const size_t slab = (size_t)N * R;
   if (tid == 0) {
@@ -472,7 +474,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
     int M = 0;  // labels changed since S was formed (pass 1: all, from scratch)
     if (p == 1) {
       // counting sort of the labels: s_perm lists rows cluster by cluster
-      for (int k = tid; k < R * ldS; k += kGramThreads) s_S[k] = 0;
+      for (int k = tid; k < C * ldS; k += kGramThreads) s_S[k] = 0;
       for (int c = tid; c < C; c += kGramThreads) s_hist[c] = 0;
       __syncthreads();
       for (int j = tid; j < N; j += kGramThreads) atomicAdd(&s_hist[s_lab[j]], 1);
@@ -540,7 +542,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
           for (int k = 0; k < 4; ++k) a[k] += __shfl_xor_sync(0xffffffffu, a[k], 16);
           if (act && half == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) atomicAdd(&s_S[(r4 + k) * ldS + c], a[k]);
+            for (int k = 0; k < 4; ++k) atomicAdd(&s_S[c * ldS + r4 + k], a[k]);
           }
           pp = e;
           if (pp >= p1) break;
@@ -567,10 +569,10 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
           const uint32_t h = *reinterpret_cast<const uint32_t*>(s_hi + j * R + r2);
           const uint32_t l = *reinterpret_cast<const uint16_t*>(s_lo + j * R + r2);
           const int v0 = q_lo(h, l), v1 = q_hi(h, l);
-          atomicAdd(&s_S[r2 * ldS + co], -v0);
-          atomicAdd(&s_S[r2 * ldS + cn], v0);
-          atomicAdd(&s_S[(r2 + 1) * ldS + co], -v1);
-          atomicAdd(&s_S[(r2 + 1) * ldS + cn], v1);
+          atomicAdd(&s_S[co * ldS + r2], -v0);
+          atomicAdd(&s_S[cn * ldS + r2], v0);
+          atomicAdd(&s_S[co * ldS + r2 + 1], -v1);
+          atomicAdd(&s_S[cn * ldS + r2 + 1], v1);
         }
         for (int k = tid; k < M; k += kGramThreads) {
           const int j = s_chg[k];
@@ -589,7 +591,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
       for (int r = tid; r < nrow; r += kGramThreads) {
         const int c = s_lab[row0 + r];
         atomicAdd(reinterpret_cast<unsigned long long*>(&s_npart[c]),
-                  static_cast<unsigned long long>(static_cast<long long>(s_S[r * ldS + c])));
+                  static_cast<unsigned long long>(static_cast<long long>(s_S[c * ldS + r])));
       }
       __syncthreads();
       const uint32_t base = tc::smem_u32(s_slot + (size_t)z * C);
@@ -639,7 +641,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int c = c0 + 8 * k;
-            sv[k] = c < C ? s_S[r * ldS + c] : 0;
+            sv[k] = c < C ? s_S[c * ldS + r] : 0;
             mv[k] = c < C ? s_invn[c] : -1.f;
           }
 #pragma unroll

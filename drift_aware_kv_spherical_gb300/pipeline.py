@@ -144,11 +144,3 @@ class Pipeline:
             self.commit_step(logits, stream)
         self.t += 1
 
-    def kernel_launches_per_step(self):
-        """Approximate kernel count of one step (bf16 tensor-core plans:
-        k-means 2 + (I+1) + I + 1, NVFP4 2, proxy 3, top-k 1, refresh 2,
-        commit 2); the bench counts the captured graph's nodes instead when
-        it can."""
-        w = self.w
-        km = 2 + (w.iters + 1) + w.iters + 1
-        return self.layers * (km + 2 + 3 + 1 + 2) + 2
