@@ -296,11 +296,16 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
     const int t = blockIdx.y, n0 = blockIdx.x * BN;
     const int r0 = z * 128 / nz, r1 = min((z + 1) * 128 / nz, this->M - t * 128);
     cluster_rows_sum<8, 32>(red, kLd, r0, max(r0, r1), BN, nz, [&](int r, int c, float4 v) {
-      const long o = (long)(t * 128 + r) * this->nkv + n0 + c;
-      split_store(this->khi + o, this->klo + o, v.x);
-      split_store(this->khi + o + 1, this->klo + o + 1, v.y);
-      split_store(this->khi + o + 2, this->klo + o + 2, v.z);
-      split_store(this->khi + o + 3, this->klo + o + 3, v.w);
+      const long o = (long)(t * 128 + r) * this->nkv + n0 + c;  // a multiple of 4
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(v.z, v.w);
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+      *reinterpret_cast<uint2*>(this->khi + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      *reinterpret_cast<uint2*>(this->klo + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
     });
     tc::cluster_arrive();
   }
@@ -535,23 +540,45 @@ struct ProxyClusterEpi : ProxyEpi<BN, P> {
     this->head(t, r, part, taddr, reinterpret_cast<float*>(scratch), st);
     stash(part, st, red_row);
   }
-  __device__ void reduce(const float* red, int z, int nz, uint8_t*) const {
+  // with one epilogue warp per TMEM quarter (P == 1) the scratch is free:
+  // the previous distributions of this CTA's rows are staged there while the
+  // mainloop runs, when they fit
+  __device__ bool early_prev(int nrow) const {
+    return P == 1 && this->A_prev != nullptr && nrow * this->C * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch;
+  }
+  __device__ void rows_of(int z, int nz, int mt, int* r0, int* nrow) const {
+    const int a = z * 128 / nz, e = (z + 1) * 128 / nz;
+    *r0 = a;
+    *nrow = max(0, min(e, this->N - mt * 128) - a);
+  }
+  __device__ void prefetch(uint8_t* scratch, int i, int n) const {
+    const int bm = blockIdx.y, b = bm / this->mtb, mt = bm % this->mtb;
+    int r0, nrow;
+    rows_of(blockIdx.z, gridDim.z, mt, &r0, &nrow);
+    if (!early_prev(nrow)) return;
+    const float* src = this->A_prev + ((long)b * this->N + mt * 128 + r0) * this->C;
+    float* dst = reinterpret_cast<float*>(scratch);
+    for (int j = i; j < nrow * this->C; j += n) dst[j] = __ldg(src + j);
+  }
+  __device__ void reduce(const float* red, int z, int nz, uint8_t* scratch) const {
     const int bm = blockIdx.y, b = bm / this->mtb, mt = bm % this->mtb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int r0 = z * 128 / nz, r1 = (z + 1) * 128 / nz;
+    int r0, nrow;
+    rows_of(z, nz, mt, &r0, &nrow);
     const int C = this->C, N = this->N;
-    const int i0 = mt * 128 + r0, nrow = max(0, min(r1, N - mt * 128) - r0);
+    const int i0 = mt * 128 + r0;
     const long row0 = (long)b * N + i0;
     const float hq = (float)this->Hq;
-    // the previous distributions of this CTA's rows (one contiguous block),
-    // staged in one pass with 16-byte loads; the shared memory past the
-    // cluster-read result is this CTA's own
-    float* s_prev = const_cast<float*>(red) + 128 * kLd;
+    // the previous distributions of this CTA's rows (one contiguous block):
+    // staged early in the scratch, or here with 16-byte loads past the
+    // cluster-read result (this CTA's own shared memory)
+    const bool early = early_prev(nrow);
+    float* s_prev = early ? reinterpret_cast<float*>(scratch) : const_cast<float*>(red) + 128 * kLd;
     const bool prev = this->A_prev != nullptr;
     using Cfg = TcCfg<BN, 1, 2, false>;
     // staged when it fits in the ring past the result, else read in place
-    const bool staged = (128 * kLd + nrow * C) * 4 <= Cfg::kStages * Cfg::kStage;
-    if (prev && staged) {
+    const bool staged = early || (128 * kLd + nrow * C) * 4 <= Cfg::kStages * Cfg::kStage;
+    if (prev && staged && !early) {
       const float* src = this->A_prev + row0 * C;
       const int n = nrow * C;
       if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
