@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import glob
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -195,8 +196,9 @@ KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
 
 
 def kernel_key(name):
-    if "k_cluster_scan" in name:
-        return "kmeans_final" if "Lb1E" in name else "kmeans_update"
+    if "k_cluster_scan" in name:  # first template flag: the final pass (C_hat only)
+        m = re.search(r"k_cluster_scanI(?:13__nv_bfloat16|f)Lb([01])E", name)
+        return "kmeans_final" if m and m.group(1) == "1" else "kmeans_update"
     for pat, key in KERNEL_KEYS:
         if pat in name:
             return key

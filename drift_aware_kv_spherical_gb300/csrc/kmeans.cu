@@ -540,7 +540,7 @@ constexpr int kScanRows = 4096;
 constexpr int kMaxColGroups = 2;
 constexpr int kMaxSlices = 8;
 
-template <typename T, bool FINAL, int G>
+template <typename T, bool FINAL, int G, bool FUSED = false>
 __global__ void __launch_bounds__(1024)
 k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
@@ -645,7 +645,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   // count and the mean rho of C_hat
   int n_fin = n;
   float rs_fin = 0.f;
-  if (!FINAL && assign_fin != nullptr) {  // block-uniform
+  if constexpr (FUSED) {  // assign_fin: the final labels
     int cnt = 0;
     for (int i = tid; i < N; i += nthr)
       if (__ldg(assign_fin + (long)b * N + i) == c) {
@@ -691,8 +691,12 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     }
     const float nu = sqrtf(ss);
     const bool formed = n > 0 && nu > 0.f;  // else the centroid is kept
+    if (!FUSED && !formed) {
+      if (S > 1) tc::cluster_wait();
+      return;
+    }
     const long ro = ((long)b * C + c) * d;
-    const float mean = (assign_fin != nullptr && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
+    const float mean = (FUSED && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int col = col0 + (g * nthr + tid) * V;
@@ -723,7 +727,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
               *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
             }
           }
-        } else if (assign_fin != nullptr && n_fin > 0) {
+        } else if (FUSED && n_fin > 0) {
           const float4* mi = reinterpret_cast<const float4*>(mu + ro + col);
 #pragma unroll
           for (int e = 0; e < V; e += 4) {
@@ -731,7 +735,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
             x[e] = m4.x; x[e + 1] = m4.y; x[e + 2] = m4.z; x[e + 3] = m4.w;
           }
         }
-        if (assign_fin != nullptr && n_fin > 0) {
+        if (FUSED && n_fin > 0) {
           float4* co = reinterpret_cast<float4*>(chat + ro + col);
 #pragma unroll
           for (int e = 0; e < V; e += 4)
@@ -765,7 +769,7 @@ ScanPlan scan_plan(int B, int d, int C) {
   return p;
 }
 
-template <typename T, bool FINAL, typename... Args>
+template <typename T, bool FINAL, bool FUSED = false, typename... Args>
 cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, B, p.S);
@@ -780,8 +784,8 @@ cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&.
   attr[1].val.clusterDim.z = p.S;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return p.G == 1 ? launch_ex(cfg, k_cluster_scan<T, FINAL, 1>, std::forward<Args>(args)...)
-                  : launch_ex(cfg, k_cluster_scan<T, FINAL, kMaxColGroups>,
+  return p.G == 1 ? launch_ex(cfg, k_cluster_scan<T, FINAL, 1, FUSED>, std::forward<Args>(args)...)
+                  : launch_ex(cfg, k_cluster_scan<T, FINAL, kMaxColGroups, FUSED>,
                               std::forward<Args>(args)...);
 }
 
@@ -957,9 +961,9 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
                        w.prev, a.rho, w.L, fused0 ? nullptr : w.objp, p.ntile, a.obj,
                        a.iters + 1, a.status, s);
     if (e == cudaSuccess)
-      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C, sp.W,
-                                a.mu, nullptr, nullptr, a.counts, a.chat, w.objp, p.ntile,
-                                nullptr, a.iters + 1, a.iters, a.assign);
+      e = launch_scan<T, false, true>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C,
+                                      sp.W, a.mu, nullptr, nullptr, a.counts, a.chat, w.objp,
+                                      p.ntile, nullptr, a.iters + 1, a.iters, a.assign);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   for (int t = 0; t <= a.iters; ++t) {
