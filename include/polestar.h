@@ -122,6 +122,14 @@ size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
  * counts   [B][C] i32 out  cluster sizes
  * objective[B][I+1] f32 out (nullable)  sum_i cos(h_i, mu_{a_i}) per pass
  * Empty clusters keep their centroid.  Rows of zero norm join cluster 0.
+ *
+ * Two forms compute the same passes.  bf16 windows of N <= 1024 rows with
+ * C <= 256, d <= 16384 and iters >= 2 run them on the window's cosine Gram
+ * matrix (24-bit fixed point, exact integer cluster sums) inside one
+ * thread-block cluster; a row whose two best cosines lie within about 1e-6
+ * may take the other label than an fp64 pass would.  Other shapes, and any
+ * call made while PS_KMEANS_LLOYD is set in the environment (read once per
+ * process), form every centroid and assign on the tensor cores per pass.
  * ------------------------------------------------------------------------- */
 ps_status ps_kmeans_spherical(ps_handle h, const void* H, int dtype, int B,
                               int N, int d, int C, int iters, int init_mode,
