@@ -470,6 +470,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
   }
 
   float last_obj = 0.f;  // CTA 0, thread 0: the latest pass objective
+  bool relabelled = true;  // the last pass took a new arg-max (cluster-uniform)
   for (int p = 1; p <= passes; ++p) {
     int M = 0;  // labels changed since S was formed (pass 1: all, from scratch)
     if (p == 1) {
@@ -550,7 +551,7 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
         }
       }
       M = N;
-    } else {
+    } else if (relabelled) {  // else no label can have changed since the last scan
       // rows whose label changed in the last pass move their column of q
       // from the old cluster's sums to the new one's (integer, so S stays
       // equal to the sums formed from scratch)
@@ -623,12 +624,14 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
         for (int k = tid; k < M; k += kGramThreads) s_prev[s_chg[k]] = s_lab[s_chg[k]];
       __syncthreads();
     }
-    // (M == 0: S, the counts and the norms are those of the last pass)
+    // (M == 0: S, the counts and the norms are those of the last pass, so
+    // are the cosines, and the last pass's arg-max, labels and objective are
+    // this pass's too: they are kept instead of recomputed)
 
     // cosines and arg-max (first maximum): 8 threads per row, thread `sub`
     // taking clusters sub, sub + 8, ...; a kept cluster's column comes from
     // L, the others refresh it
-    {
+    if (M > 0) {
       const int r = tid >> 3, sub = tid & 7;
       float bv = -INFINITY;
       int bi = INT_MAX;
@@ -679,9 +682,10 @@ k_km_gram(const int16_t* __restrict__ qhi, const uint8_t* __restrict__ qlo, int 
         s_newlab[r] = static_cast<uint8_t>(bi);
         s_best[r] = r < nrow ? bv : 0.f;
       }
+      __syncthreads();
     }
-    __syncthreads();
 
+    relabelled = M > 0;
     if (M > 0) {
       // the pass objective's partial to CTA 0, the new labels to every CTA
       if (obj != nullptr && warp == 0) {
