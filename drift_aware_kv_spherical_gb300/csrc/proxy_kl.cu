@@ -654,7 +654,8 @@ TcPlan tc_plan(int dtype, int B, int N, int d, int C, int Hq, int Hkv, int dh) {
       const int cap = z == 1 ? kSmTarget : tc_cluster_capacity(z);
       if (cap <= 0) continue;
       const double waves = ceil_div(groups, cap);
-      const double cost = waves * kpc * (2.0 * 128 * 64 * 2 + (double)bn * 64 * 2);
+      const double arows = B * C <= 64 ? 64.0 : 128.0;
+      const double cost = waves * kpc * (2.0 * arows * 64 * 2 + (double)bn * 64 * 2);
       if (best == 0.0 || cost < best) {
         best = cost;
         p.ck_BN = bn;
@@ -691,14 +692,16 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
                                                                           w.clo);
   {
     TcMaps maps;
+    // with at most 64 centroid rows the tiles bring 64 rows (a quarter less to stream)
+    const int a_rows = a.B * a.C <= 64 ? 64 : 128;
     if (!make_tmap_bf16_2d(&maps.a[0], w.chi, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2,
-                           64, 128) ||
+                           64, a_rows) ||
         !make_tmap_bf16_2d(&maps.a[1], w.clo, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2,
-                           64, 128) ||
+                           64, a_rows) ||
         !make_tmap_bf16_2d(&maps.b[0], a.Wk, nkv, a.d, (uint64_t)nkv * 2, 64, 64))
       return cudaErrorInvalidValue;
     maps.b[1] = maps.b[0];
-    TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status, INT_MAX};
+    TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status, INT_MAX, 0, a_rows};
     const dim3 grid(p.ck_nt, p.ck_mt, p.ck_nz);
     const int M = a.B * a.C;
     cudaError_t e;

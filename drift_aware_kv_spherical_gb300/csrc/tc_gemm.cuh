@@ -52,6 +52,10 @@ struct TcShape {
   int starve_loads;    // test hook: the producer issues no copies, so the
                        // MMA thread's bounded wait must give up (set only
                        // when PS_TEST_STARVE_TMA is in the environment)
+  int a_rows;          // A rows each TMA tile brings (the A maps' box height):
+                       // 64 when M <= 64 (the MMA's rows 64..127 then read
+                       // stale shared memory into accumulator rows nobody
+                       // stores), 0 or 128 otherwise
 };
 
 // KS: 64-wide k-blocks per pipeline stage.  Measured on GB300, one SM's TMA
@@ -191,6 +195,8 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
 
   if (warp == 0) {
     if (lane == 0 && !sh.starve_loads) {
+      const uint32_t a_bytes = (sh.a_rows > 0 ? sh.a_rows : 128) * 128u;
+      const uint32_t stage_bytes = KS * (NA * a_bytes + NB * Cfg::kB);
       int it = 0;
       bool ok = true;
       for (int t = t_begin; ok && t < t_end; t += t_step) {
@@ -203,7 +209,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!tc::mbar_wait(empty + s, ph ^ 1, sh.status, abort_flag)) { ok = false; break; }
-          tc::mbar_expect_tx(full + s, Cfg::kStage);
+          tc::mbar_expect_tx(full + s, stage_bytes);
 #pragma unroll
           for (int sub = 0; sub < KS; ++sub) {
             // a k-block past this chunk (an odd last one) is still loaded,
