@@ -19,6 +19,8 @@ technical summary, written below as ``[Polestar §x, <paragraph>]``:
                                    drifting clusters, sparse K/V refresh
 * §2.B "Current block commitment"  drift delta vs alpha (tau_s - c)^2
 * §2.B "Suffix block commitment"   suffix tokens need c >= tau_s
+* §2.C "CPU offloading"            quantised clusters in host memory, the
+                                   top-k clusters fetched back
 
 Where the page is silent the oracle takes one explicit reading; each reading
 is named in the docstring of the function that takes it.
@@ -39,6 +41,7 @@ from .proxy_kl import centroid_keys, proxy_attn_kl, kl_divergence_rows
 from .topk import topk_drift
 from .refresh import refresh_kv, bf16_round
 from .commit import confidence, commit_rule, CommitParams
+from .offload import record_bytes, pack_clusters, reconstruct_row, fetch_reconstruct
 
 __all__ = [
     "kmeans_spherical", "kmeanspp_init", "normalize_rows",
@@ -47,4 +50,5 @@ __all__ = [
     "centroid_keys", "proxy_attn_kl", "kl_divergence_rows",
     "topk_drift", "refresh_kv", "bf16_round",
     "confidence", "commit_rule", "CommitParams",
+    "record_bytes", "pack_clusters", "reconstruct_row", "fetch_reconstruct",
 ]
