@@ -382,3 +382,77 @@ extern "C" ps_status ps_nvfp4_residual_noalloc(
               scratch, h->num_sms};
   return launch_status(nvfp4_run(a, static_cast<cudaStream_t>(stream)));
 }
+
+// ---- offload of the quantised clusters; see include/polestar.h
+namespace {
+// device memory, or host memory mapped into this device's address space
+bool device_accessible(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged ||
+         (at.type == cudaMemoryTypeHost && at.devicePointer == p);
+}
+}  // namespace
+
+extern "C" size_t ps_store_record_bytes(int d) {
+  return d > 0 && d % 32 == 0 ? ps::store_record_bytes(d) : 0;
+}
+
+extern "C" ps_status ps_host_alloc(size_t bytes, void** ptr) {
+  if (ptr == nullptr || bytes == 0) return PS_ERR_ARG;
+  *ptr = nullptr;
+  void* p = nullptr;
+  cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) return launch_status(e);
+  void* dp = nullptr;
+  e = cudaHostGetDevicePointer(&dp, p, 0);
+  if (e != cudaSuccess || dp != p) {  // one address for host and device (unified addressing)
+    cudaFreeHost(p);
+    return e != cudaSuccess ? launch_status(e) : PS_ERR_CUDA;
+  }
+  *ptr = p;
+  return PS_OK;
+}
+
+extern "C" ps_status ps_host_free(void* ptr) {
+  if (ptr == nullptr) return PS_OK;
+  return launch_status(cudaFreeHost(ptr));
+}
+
+extern "C" ps_status ps_nvfp4_pack_clusters(ps_handle h, const uint8_t* codes,
+                                            const uint8_t* scales, const int32_t* assign, int B,
+                                            int N, int d, int C, void* store, int32_t* order,
+                                            int32_t* cl_off, void* stream) {
+  TraceScope trace_scope(h);
+  PS_REQUIRE(h != nullptr && B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && N <= 16384 && d > 0 && d % 32 == 0 && C >= 1 && C <= 65535 &&
+             B <= 65535);
+  PS_PTR(codes); PS_NN(scales); PS_NN(assign); PS_PTR(store); PS_NN(order); PS_NN(cl_off);
+  PS_REQUIRE(device_accessible(store));
+  return launch_status(pack_clusters_run(codes, scales, assign, B, N, d, C,
+                                         static_cast<uint8_t*>(store), order, cl_off,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ps_status ps_nvfp4_fetch_dequant(ps_handle h, const void* store, const int32_t* order,
+                                            const int32_t* cl_off, const int32_t* sel, int k,
+                                            const float* mu, const float* rho,
+                                            const float* tensor_scale, int B, int N, int d, int C,
+                                            void* Ht, void* stream) {
+  TraceScope trace_scope(h);
+  PS_REQUIRE(h != nullptr && B >= 0);
+  if (B == 0 || k == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && N <= 65535 && d > 0 && d % 32 == 0 && C >= 1 && k >= 1 && k <= C &&
+             B <= 65535);
+  PS_PTR(store); PS_NN(order); PS_NN(cl_off); PS_NN(sel); PS_PTR(mu); PS_NN(rho);
+  PS_NN(tensor_scale); PS_PTR(Ht);
+  PS_REQUIRE(device_accessible(store));
+  return launch_status(fetch_dequant_run(static_cast<const uint8_t*>(store), order, cl_off, sel,
+                                         k, mu, rho, tensor_scale, B, N, d, C,
+                                         static_cast<__nv_bfloat16*>(Ht),
+                                         static_cast<cudaStream_t>(stream)));
+}

@@ -43,6 +43,16 @@ cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* q
                          const float* objp0, int ntile0, float* obj, int obj_ld, int* status,
                          cudaStream_t s);
 
+// offload of the quantised clusters (offload.cu)
+size_t store_record_bytes(int d);
+cudaError_t pack_clusters_run(const uint8_t* codes, const uint8_t* scales, const int32_t* assign,
+                              int B, int N, int d, int C, uint8_t* store, int32_t* order,
+                              int32_t* cl_off, cudaStream_t s);
+cudaError_t fetch_dequant_run(const uint8_t* store, const int32_t* order, const int32_t* cl_off,
+                              const int32_t* sel, int k, const float* mu, const float* rho,
+                              const float* tensor_scale, int B, int N, int d, int C,
+                              __nv_bfloat16* Ht, cudaStream_t s);
+
 struct Nvfp4Args {
   const void* H; int dtype; const float* mu; const int32_t* assign;
   const float* rho; int B, N, d, C;

@@ -20,7 +20,9 @@ OP_KMEANS, OP_NVFP4, OP_PROXY_KL, OP_TOPK, OP_REFRESH, OP_COMMIT = range(6)
 EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_cuda_error",
             "ps_trace_enable", "ps_trace_count", "ps_trace_get",
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
-            "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit"]
+            "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit",
+            "ps_store_record_bytes", "ps_host_alloc", "ps_host_free",
+            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant"]
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -54,6 +56,12 @@ _SIGS = {
     "ps_trace_get": (_i, [_p, _i, ctypes.POINTER(ctypes.c_char_p),
                           ctypes.POINTER(ctypes.c_float)]),
     "ps_workspace_bytes": (_sz, [_i] * 11),
+    "ps_store_record_bytes": (_sz, [_i]),
+    "ps_host_alloc": (_i, [_sz, ctypes.POINTER(_p)]),
+    "ps_host_free": (_i, [_p]),
+    "ps_nvfp4_pack_clusters": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]),
+    "ps_nvfp4_fetch_dequant": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p,
+                                    _p]),
     "ps_kmeans_spherical": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                                  _p, _p, _p, _p, _p, _sz, _p]),
     "ps_nvfp4_residual": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p,
@@ -272,3 +280,63 @@ def ps_trace_records():
                "ps_trace_get")
         out.append((name.value.decode(), ms.value))
     return out
+
+
+# ---- offload of the quantised clusters (include/polestar.h)
+def ps_store_record_bytes(d):
+    return int(_lib().cdll.ps_store_record_bytes(int(d)))
+
+
+class HostStore:
+    """Pinned host memory mapped into the device (ps_host_alloc): `ptr` is
+    valid on host and device; `view()` is a numpy byte view of it."""
+
+    def __init__(self, nbytes):
+        lib = _lib()
+        p = ctypes.c_void_p()
+        _check(lib.cdll.ps_host_alloc(int(nbytes), ctypes.byref(p)), "ps_host_alloc")
+        self.ptr, self.nbytes = p.value, int(nbytes)
+
+    def view(self):
+        import numpy as np
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        return np.frombuffer(buf, dtype=np.uint8)
+
+    def free(self):
+        if self.ptr:
+            _check(_lib().cdll.ps_host_free(ctypes.c_void_p(self.ptr)), "ps_host_free")
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def _store_ptr(store):
+    return store.ptr if isinstance(store, HostStore) else _ptr(store)
+
+
+def ps_nvfp4_pack_clusters(codes, scales, assign, C, store, order, cl_off, stream=None):
+    """Cluster-grouped records of every window into `store` (a device uint8
+    tensor or a HostStore), with order [B][N] and cl_off [B][C+1] (int32)."""
+    lib = _lib()
+    B, N, half = codes.shape
+    st = lib.cdll.ps_nvfp4_pack_clusters(lib.handle(), _ptr(codes), _ptr(scales), _ptr(assign),
+                                         B, N, 2 * half, int(C), _store_ptr(store), _ptr(order),
+                                         _ptr(cl_off), _stream(stream))
+    _check(st, "ps_nvfp4_pack_clusters")
+
+
+def ps_nvfp4_fetch_dequant(store, order, cl_off, sel, mu, rho, tensor_scale, Ht, stream=None):
+    """Reconstructed rows of the selected clusters, read from `store`, into
+    Ht [B][N][d] (bf16); other rows untouched."""
+    lib = _lib()
+    B, N, d = Ht.shape
+    C = mu.shape[1]
+    st = lib.cdll.ps_nvfp4_fetch_dequant(lib.handle(), _store_ptr(store), _ptr(order),
+                                         _ptr(cl_off), _ptr(sel), sel.shape[1], _ptr(mu),
+                                         _ptr(rho), _ptr(tensor_scale), B, N, d, C, _ptr(Ht),
+                                         _stream(stream))
+    _check(st, "ps_nvfp4_fetch_dequant")

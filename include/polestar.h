@@ -96,6 +96,59 @@ int ps_trace_count(ps_handle h);
  * fails. */
 ps_status ps_trace_get(ps_handle h, int i, const char** name, float* ms);
 
+/* ---------------------------------------------------------------------------
+ * Offload of the quantised clusters (§8(f) next #1).
+ * [Polestar §2.C, CPU offloading] -- "quantised hidden-state clusters are
+ * offloaded to pinned CPU memory while only the centroids stay on the GPU;
+ * the top-k clusters are fetched asynchronously".
+ *
+ * Store of a window: one record per row, grouped by cluster (ascending id)
+ * and by ascending position inside a cluster.  A record holds the row's E2M1
+ * codes (d/2 bytes) then its E4M3 block scales (d/16 bytes), each part
+ * zero-padded to a multiple of 16 bytes: ps_store_record_bytes(d) bytes
+ * (0 unless d is a positive multiple of 32).  Layout [B][N][record].
+ *
+ * ps_host_alloc: `bytes` of pinned host memory mapped into the device's
+ * address space, one pointer valid on host and device (the GPU reaches it
+ * over NVLink-C2C or PCIe).  PS_ERR_ARG for ptr == NULL or bytes == 0;
+ * PS_ERR_CUDA if the allocation fails.  Release with ps_host_free.
+ * ------------------------------------------------------------------------- */
+size_t ps_store_record_bytes(int d);
+ps_status ps_host_alloc(size_t bytes, void** ptr);
+ps_status ps_host_free(void* ptr);
+
+/* Writes the store of every window (the offload: the GPU stores straight
+ * into it when it lies in host memory).
+ * codes [B][N][d/2] u8, scales [B][N][d/16] u8, assign [B][N] i32 in [0, C)
+ * (ps_nvfp4_residual's and ps_kmeans_spherical's outputs)
+ * store [B][N][record] u8 out: device memory or ps_host_alloc memory,
+ *       16-byte aligned
+ * order [B][N] i32 out: position of record r;  cl_off [B][C+1] i32 out:
+ *       first record of cluster c (cl_off[C] = rows with a label in [0, C))
+ * PS_ERR_ARG for NULL or misaligned pointers, a store the device cannot
+ * reach, N > 16384, or d not a multiple of 32. */
+ps_status ps_nvfp4_pack_clusters(ps_handle h, const uint8_t* codes,
+                                 const uint8_t* scales, const int32_t* assign,
+                                 int B, int N, int d, int C, void* store,
+                                 int32_t* order, int32_t* cl_off, void* stream);
+
+/* Reads the records of the selected clusters from the store (the fetch) and
+ * writes each row's reconstruction into Ht:
+ *   g = fl(s_b S), deq = fl(v g), t = fl(rho_i mu_c), h~ = fl(t + deq)
+ * (fp32, one rounding each, no fused multiply-add; v the element's E2M1
+ * value, s_b its block's E4M3 value, S the window's tensor scale), rounded
+ * to bf16 (nearest-even).  Rows of unselected clusters are left untouched,
+ * so ps_refresh_kv can take Ht with the same pos / npos.
+ * sel [B][k] i32 (ps_topk_drift's; entries < 0 ignored), mu [B][C][d] f32,
+ * rho [B][N] f32, tensor_scale [B] f32, Ht [B][N][d] bf16 out.
+ * PS_ERR_ARG as for ps_nvfp4_pack_clusters, or k outside [1, C]. */
+ps_status ps_nvfp4_fetch_dequant(ps_handle h, const void* store,
+                                 const int32_t* order, const int32_t* cl_off,
+                                 const int32_t* sel, int k, const float* mu,
+                                 const float* rho, const float* tensor_scale,
+                                 int B, int N, int d, int C, void* Ht,
+                                 void* stream);
+
 /* Workspace bytes `op` needs for these sizes (arguments an op does not use
  * are ignored).  0 means ws may be NULL. */
 size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
