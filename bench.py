@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--offload", action="store_true",
+                    help="quantised clusters in a pinned host store, refresh from the "
+                         "reconstruction of the selected clusters (Polestar 2.C)")
     return ap.parse_args()
 
 
@@ -192,7 +195,8 @@ KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
                ("k_split_f32", "proxy_split"), ("Proxy", "proxy_attn"),
                ("k_proxy", "proxy_attn"), ("k_topk", "topk"), ("k_gather_rows", "refresh_gather"),
                ("Refresh", "refresh_gemm"), ("k_refresh", "refresh_gemm"),
-               ("k_commit_scan", "commit_scan"), ("k_commit_rule", "commit_rule")]
+               ("k_commit_scan", "commit_scan"), ("k_commit_rule", "commit_rule"),
+               ("k_pack_clusters", "offload_pack"), ("k_fetch_dequant", "offload_fetch")]
 
 
 def kernel_key(name):
@@ -235,6 +239,22 @@ def kernel_work(key, w, npos_mean):
         "refresh_gemm": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
         "commit_scan": (B * w.P * w.V * 4, 0.0),
     }.get(key)
+
+
+def offload_rates(records, nsteps, w, npos_mean):
+    """Host-link traffic of the offload kernels: the store they write (every
+    row's record, by the GPU into pinned host memory) and read (the selected
+    clusters' records), GB/s over each kernel's own duration."""
+    rec = (w.d // 2 + 15) // 16 * 16 + (w.d // 16 + 15) // 16 * 16
+    out = {"record_bytes": rec}
+    for key, nbytes in (("offload_pack", w.B * w.N * rec), ("offload_fetch", npos_mean * w.B * rec)):
+        ms = [m for name, m in records if kernel_key(name) == key]
+        if ms:
+            t = sum(ms) / len(ms)
+            out[key] = {"bytes_per_launch": nbytes, "us_per_launch": 1e3 * t,
+                        "host_link_gbs": nbytes / (t * 1e-3) / 1e9,
+                        "launches_per_step": len(ms) / nsteps}
+    return out
 
 
 def kernel_rooflines(records, nsteps, w, npos_mean, hbm, tf):
@@ -396,7 +416,7 @@ def main():
     Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
     logits = [wl.make_logits(w, t, dev) for t in range(4)]
     u = wl.make_uniforms(w, 0, dev)
-    pipe = Pipeline(w, layers=1, device=dev)
+    pipe = Pipeline(w, layers=1, device=dev, offload=args.offload)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     # the step reads its inputs from fixed buffers (graph replay needs fixed
     # addresses); the next step's inputs are copied in outside the timed events
@@ -423,6 +443,9 @@ def main():
         rec(1)
         ps.ps_nvfp4_residual(dH, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
                              ws=pipe.ws[ps.OP_NVFP4])
+        if pipe.offload:  # the store in host memory
+            ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store, st.order,
+                                      st.cl_off)
         rec(2)
         ps.ps_proxy_attn_kl(dQ, st.chat, L["Wk"], prev, cur, st.D, w.Hkv,
                             ws=pipe.ws[ps.OP_PROXY_KL])
@@ -430,7 +453,12 @@ def main():
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
                          st.npos, st.posmask)
         rec(4)
-        ps.ps_refresh_kv(dH, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh,
+        src = dH
+        if pipe.offload:  # the selected clusters' rows from the host store
+            ps.ps_nvfp4_fetch_dequant(st.store, st.order, st.cl_off, st.sel, st.mu, st.rho, st.S,
+                                      st.Ht)
+            src = st.Ht
+        ps.ps_refresh_kv(src, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh,
                          ws=pipe.ws[ps.OP_REFRESH])
         rec(5)
         pipe.commit_step(dL)
@@ -614,6 +642,9 @@ def main():
         "timing": "CUDA-graph replay of the whole step per timed step",
         "parallelism": f"replicas x{world}",
     }
+    if args.offload:
+        line["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
+        line["offload"] = offload_rates(trace, ntrace, w, npos_seen[-1] / w.B)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:

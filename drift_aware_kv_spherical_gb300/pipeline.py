@@ -7,6 +7,12 @@ distribution, top-k drifting clusters and the sparse K/V refresh; then one
 commit over the current block with the last layer's drift.  All buffers are
 allocated once here (caller-side), so a step allocates nothing and can be
 captured in a CUDA graph.
+
+With offload=True (bf16 workloads) each layer's NVFP4 residuals are also
+written, grouped by cluster, into a store in pinned host memory mapped into
+the GPU, and the refresh takes the rows of the selected clusters as
+reconstructed from that store (h~ = rho mu + deq(r)) instead of H
+[Polestar §2.C, CPU offloading].
 """
 
 import torch
@@ -45,8 +51,11 @@ class LayerState:
 class Pipeline:
     """Buffers and the per-step call sequence for workload `w`."""
 
-    def __init__(self, w, layers=None, device="cuda"):
+    def __init__(self, w, layers=None, device="cuda", offload=False):
         self.w = w
+        self.offload = offload
+        if offload and w.dtype != "bf16":
+            raise ValueError("the offload path reconstructs bf16 rows: bf16 workloads only")
         self.layers = w.layers if layers is None else layers
         self.device = device
         B, N, d, C = w.B, w.N, w.d, w.C
@@ -56,6 +65,13 @@ class Pipeline:
                    for op in (ps.OP_KMEANS, ps.OP_NVFP4, ps.OP_PROXY_KL, ps.OP_TOPK,
                               ps.OP_REFRESH, ps.OP_COMMIT)}
         self.state = [LayerState(w, device) for _ in range(self.layers)]
+        if offload:
+            rec = ps.ps_store_record_bytes(d)
+            for st in self.state:
+                st.store = ps.HostStore(B * N * rec)
+                st.order = torch.zeros(B, N, dtype=torch.int32, device=device)
+                st.cl_off = torch.zeros(B, C + 1, dtype=torch.int32, device=device)
+                st.Ht = torch.zeros(B, N, d, dtype=torch.bfloat16, device=device)
         P = w.P
         self.role = wl.make_roles(w).to(device)
         self.undecided = torch.ones(B, P, dtype=torch.uint8, device=device)
@@ -93,23 +109,38 @@ class Pipeline:
                                w.iters, init_mode=1 if first else 0, init_u=init_u,
                                objective=st.obj, ws=self.ws[ps.OP_KMEANS],
                                stream=stream)
+        packed = None
         if concurrent:
             main = stream if stream is not None else torch.cuda.current_stream(self.device)
             side = self.side_streams()[0]
             side.wait_event(main.record_event())
             ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
                                  ws=self.ws[ps.OP_NVFP4], stream=side)
-            joins.append(side.record_event())
+            if self.offload:
+                ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store,
+                                          st.order, st.cl_off, stream=side)
+            packed = side.record_event()
+            joins.append(packed)
         else:
             ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
                                  ws=self.ws[ps.OP_NVFP4], stream=stream)
+            if self.offload:
+                ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store,
+                                          st.order, st.cl_off, stream=stream)
         ps.ps_proxy_attn_kl(Q, st.chat, Wk, None if first else prev, cur, st.D, w.Hkv,
                             ws=self.ws[ps.OP_PROXY_KL], stream=stream)
         if concurrent:  # the drift is final here: the commit may start
             self._after_proxy = main.record_event()
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
                          st.npos, st.posmask, ws=self.ws[ps.OP_TOPK], stream=stream)
-        ps.ps_refresh_kv(H, st.pos, st.npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
+        src = H
+        if self.offload:  # the selected clusters' rows, fetched from the host store
+            if packed is not None:
+                main.wait_event(packed)
+            ps.ps_nvfp4_fetch_dequant(st.store, st.order, st.cl_off, st.sel, st.mu, st.rho,
+                                      st.S, st.Ht, stream=stream)
+            src = st.Ht
+        ps.ps_refresh_kv(src, st.pos, st.npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
                          ws=self.ws[ps.OP_REFRESH], stream=stream)
 
     def commit_step(self, logits, stream=None):

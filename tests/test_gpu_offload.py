@@ -146,3 +146,36 @@ def test_llada_layer_offload_round_trip():
     for i in sorted(want)[:: max(1, len(want) // 12)]:
         assert np.array_equal(got[i], oracle.bf16_round(want[i]))
         assert np.max(np.abs(want[i] - Hn[i])) <= 0.5 * np.max(np.abs(Hn[i]))  # a proxy of h
+
+
+def test_offload_step_matches_oracle_refresh():
+    """A pipeline step in offload mode (store in host memory, side streams as
+    the bench captures them): the refreshed K rows equal the oracle's refresh
+    of the oracle's reconstruction of the selected rows, sampled."""
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+    w = wl.WORKLOADS[1]
+    L = wl.make_layer(w, 0, "cuda")
+    Q = wl.make_queries(w, L["H"], L["Wq"])
+    u = wl.make_uniforms(w, 0, "cuda")
+    logits = wl.make_logits(w, 0, "cuda")
+    pipe = Pipeline(w, layers=1, offload=True)
+    pipe.step([L["H"]], [Q], [L["Wk"]], [L["Wv"]], logits, init_us=[u], first=True,
+              concurrent=True)
+    H1 = wl.drift_rows(w, L["H"], 1)
+    pipe.step([H1], [wl.make_queries(w, H1, L["Wq"])], [L["Wk"]], [L["Wv"]], logits,
+              concurrent=True)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    st = pipe.state[0]
+    rec = ps.ps_store_record_bytes(w.d)
+    store = st.store.view().reshape(w.B, w.N, rec)
+    want = oracle.fetch_reconstruct(store[0], np_(st.order[0]), np_(st.cl_off[0]), np_(st.sel[0]),
+                                    np_(st.mu[0]), np_(st.rho[0]), float(np_(st.S)[0]), w.d)
+    pos = np_(st.pos[0])[: int(np_(st.npos)[0])]
+    assert set(pos.tolist()) == set(want)
+    Wk = np_(L["Wk"]).astype(np.float64)
+    Kc = np_(st.Kc[0]).reshape(w.Ncache, -1)
+    for p in pos[:: max(1, len(pos) // 8)]:
+        ref = oracle.bf16_round(oracle.bf16_round(want[p]).astype(np.float64) @ Wk)
+        rms = np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+        assert np.all(np.abs(Kc[p] - ref) <= 2e-2 * np.abs(ref) + 1e-3 * rms)
