@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time the step on a side stream against a synthetic main "
+                         "forward (bf16 GEMMs of one layer over the window)")
     ap.add_argument("--offload", action="store_true",
                     help="quantised clusters in a pinned host store, refresh from the "
                          "reconstruction of the selected clusters (Polestar 2.C)")
@@ -239,6 +242,87 @@ def kernel_work(key, w, npos_mean):
         "refresh_gemm": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
         "commit_scan": (B * w.P * w.V * 4, 0.0),
     }.get(key)
+
+
+def measure_overlap(w, graphs, dev, reps=20):
+    """Latency hiding (the pages overlap the drift work with the main forward
+    on CUDA streams): the captured drift step on one stream against a
+    synthetic main forward on another, a captured graph of bf16 GEMMs shaped
+    like one transformer layer over the window (x W_qkv, W_o, a gated MLP of
+    width 3.5 d: W_up to 2 widths, W_down back; activations left out).
+    hidden = (t_main + t_drift - t_both) / t_drift, the share of the drift
+    step's time the overlap hides."""
+    import torch
+    M, d = w.B * w.N, w.d
+    ff = int(3.5 * d) // 256 * 256
+    g = torch.Generator(device=dev)
+    g.manual_seed(20260717)
+
+    def rnd(*shape):
+        return (torch.randn(*shape, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+
+    X, Wqkv, Wo, Wup, Wdown = rnd(M, d), rnd(d, 3 * d), rnd(d, d), rnd(d, 2 * ff), rnd(ff, d)
+    sm, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    hi = torch.cuda.Stream(dev, priority=-1)  # the drift step ahead of pending GEMM blocks
+
+    def forward():
+        qkv = X @ Wqkv
+        o = qkv[:, :d] @ Wo
+        up = o @ Wup
+        return up[:, :ff] @ Wdown
+
+    with torch.cuda.stream(sm):
+        for _ in range(3):
+            forward()
+    torch.cuda.synchronize()
+    gm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gm, stream=sm):
+        forward()
+    flops = 2.0 * M * d * (3 * d + d + 2 * ff + ff)
+
+    def timed(run):
+        cur = torch.cuda.current_stream(dev)
+        for i in range(3):
+            run(i, cur)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for i in range(reps):
+            run(i, cur)
+        b.record(cur)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    def on(stream, graph, cur):
+        stream.wait_stream(cur)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        cur.wait_stream(stream)
+
+    t_main = timed(lambda i, cur: on(sm, gm, cur))
+    t_drift = timed(lambda i, cur: on(sd, graphs[i % 2], cur))
+
+    def both(ds):
+        def run(i, cur):
+            sm.wait_stream(cur)
+            ds.wait_stream(cur)
+            with torch.cuda.stream(sm):
+                gm.replay()
+            with torch.cuda.stream(ds):
+                graphs[i % 2].replay()
+            cur.wait_stream(sm)
+            cur.wait_stream(ds)
+        return run
+
+    t_both = timed(both(sd))
+    t_both_hi = timed(both(hi))
+    return {"main_forward": f"bf16 GEMMs of one layer over {M} rows (d {d}, MLP {ff}), "
+                            f"{flops / 1e12:.2f} TFLOP, captured graph",
+            "main_us": t_main, "drift_us": t_drift, "both_us": t_both,
+            "main_tflops": flops / (t_main * 1e-6) / 1e12,
+            "hidden_fraction": (t_main + t_drift - t_both) / t_drift,
+            "both_us_drift_high_priority": t_both_hi,
+            "hidden_fraction_drift_high_priority": (t_main + t_drift - t_both_hi) / t_drift}
 
 
 def offload_rates(records, nsteps, w, npos_mean):
@@ -642,6 +726,8 @@ def main():
         "timing": "CUDA-graph replay of the whole step per timed step",
         "parallelism": f"replicas x{world}",
     }
+    if args.overlap:
+        line["overlap"] = measure_overlap(w, graphs, dev)
     if args.offload:
         line["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
         line["offload"] = offload_rates(trace, ntrace, w, npos_seen[-1] / w.B)
