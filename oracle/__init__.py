@@ -52,3 +52,4 @@ __all__ = [
     "confidence", "commit_rule", "CommitParams",
     "record_bytes", "pack_clusters", "reconstruct_row", "fetch_reconstruct",
 ]
+from .schedule import ScheduleState, schedule_step
