@@ -29,7 +29,7 @@ def nvcc():
 
 
 def _compile(src, extra):
-    obj = os.path.join(OBJ, os.path.basename(src).replace(".cu", ".o"))
+    obj = os.path.join(OBJ, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -38,9 +38,9 @@ def _compile(src, extra):
 
 
 def build(verbose=False, extra=()):
-    """Compile every csrc/*.cu and link libpolestar.so; returns its path."""
+    """Compile every csrc/*.cu and *.cpp and link libpolestar.so; returns its path."""
     os.makedirs(OBJ, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         results = list(ex.map(lambda s: _compile(s, list(extra)), srcs))
     if verbose:

@@ -22,7 +22,7 @@ EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
             "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit",
             "ps_store_record_bytes", "ps_host_alloc", "ps_host_free",
-            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant"]
+            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant", "ps_schedule_step"]
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -45,6 +45,18 @@ class CommitParams(ctypes.Structure):
                 ("ensure_progress", ctypes.c_int)]
 
 
+class ScheduleParams(ctypes.Structure):
+    _fields_ = [("tau_upd", ctypes.c_int), ("full_period", ctypes.c_int),
+                ("block_len", ctypes.c_int)]
+
+
+class ScheduleState(ctypes.Structure):
+    _fields_ = [("since", ctypes.c_int), ("refreshes", ctypes.c_int),
+                ("block_start", ctypes.c_int)]
+
+
+SCHED_REFRESH, SCHED_FULL, SCHED_SLIDE, SCHED_REINIT = 1, 2, 4, 8
+
 _SIGS = {
     "ps_create": (_i, [_i, ctypes.POINTER(_p)]),
     "ps_destroy": (_i, [_p]),
@@ -59,6 +71,8 @@ _SIGS = {
     "ps_store_record_bytes": (_sz, [_i]),
     "ps_host_alloc": (_i, [_sz, ctypes.POINTER(_p)]),
     "ps_host_free": (_i, [_p]),
+    "ps_schedule_step": (_i, [ctypes.POINTER(ScheduleParams), ctypes.POINTER(ScheduleState),
+                              _i, _i]),
     "ps_nvfp4_pack_clusters": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]),
     "ps_nvfp4_fetch_dequant": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p,
                                     _p]),
@@ -340,3 +354,25 @@ def ps_nvfp4_fetch_dequant(store, order, cl_off, sel, mu, rho, tensor_scale, Ht,
                                          _ptr(rho), _ptr(tensor_scale), B, N, d, C, _ptr(Ht),
                                          _stream(stream))
     _check(st, "ps_nvfp4_fetch_dequant")
+
+
+# ---- refresh schedule of the decode loop (include/polestar.h; host only)
+def ps_schedule_step(params, state, committed, block_done):
+    """Actions (SCHED_* flags) of the next step; updates `state` in place."""
+    act = _lib().cdll.ps_schedule_step(ctypes.byref(params), ctypes.byref(state),
+                                       int(committed), int(bool(block_done)))
+    if act < 0:
+        raise PolestarError(-act, "ps_schedule_step")
+    return act
+
+
+class Schedule:
+    """A decode loop's schedule: tau_upd tokens between refreshes, every
+    full_period-th refresh in full, the window sliding by block_len."""
+
+    def __init__(self, tau_upd, full_period, block_len):
+        self.params = ScheduleParams(int(tau_upd), int(full_period), int(block_len))
+        self.state = ScheduleState(0, 0, 0)
+
+    def step(self, committed, block_done):
+        return ps_schedule_step(self.params, self.state, committed, block_done)

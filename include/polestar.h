@@ -354,6 +354,50 @@ ps_status ps_nvfp4_residual_noalloc(ps_handle h, const void* H, int dtype,
                                     int C, uint8_t* codes, uint8_t* scales,
                                     float* tensor_scale, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Refresh schedule of the decode loop (host only; no handle, no GPU work).
+ * [Polestar §2.A, schedule]: the drift refresh is triggered once the decoded
+ * context has moved enough -- after tau_upd tokens were decoded -- and
+ * periodic full passes refresh positions outside the top-k clusters too.
+ *
+ * Called after every decode step with the number of tokens that step
+ * committed and whether the current block is now decided; returns the
+ * actions of the NEXT step (an OR of the flags below, 0 = reuse the cache):
+ *   block_done:        REFRESH | FULL | SLIDE | REINIT -- the window slides
+ *                      by block_len, the next step clusters it from scratch
+ *                      (k-means++), refreshes every position, and the
+ *                      counts restart (since = refreshes = 0);
+ *   else since += committed; if since >= tau_upd (tau_upd = 0: every step):
+ *                      REFRESH, since = 0, refreshes += 1, and FULL too when
+ *                      full_period > 0 and refreshes % full_period == 0.
+ * The state is caller-owned; zero it for the first window (whose first step
+ * the caller runs as block_done would: clustered and refreshed in full).
+ * Errors: NULL pointers, tau_upd < 0, full_period < 0, block_len < 1,
+ * committed < 0 or a negative state field return -PS_ERR_ARG and leave the
+ * state unchanged.  The token count saturates at INT_MAX.
+ * ------------------------------------------------------------------------- */
+enum {
+  PS_SCHED_REFRESH = 1, /* run the drift path and the top-k refresh         */
+  PS_SCHED_FULL = 2,    /* refresh every window position, not only top-k    */
+  PS_SCHED_SLIDE = 4,   /* a new block: reset the commit state              */
+  PS_SCHED_REINIT = 8   /* re-seed k-means (k-means++), no previous A       */
+};
+
+typedef struct {
+  int tau_upd;      /* tokens between refreshes, >= 0                        */
+  int full_period;  /* every full_period-th refresh is full; 0 = never       */
+  int block_len;    /* positions the window slides by, >= 1                  */
+} ps_schedule_params;
+
+typedef struct {
+  int since;        /* tokens committed since the last refresh              */
+  int refreshes;    /* refreshes since the window was built                 */
+  int block_start;  /* sequence position of the current block               */
+} ps_schedule_state;
+
+int ps_schedule_step(const ps_schedule_params* p, ps_schedule_state* s,
+                     int committed, int block_done);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ def cdll():
 
 def _declared():
     src = open(os.path.join(ROOT, "include", "polestar.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:ps_status|size_t|const char\*)\s+(ps_\w+)\(",
+    return sorted(set(re.findall(r"^\s*(?:ps_status|size_t|int|const char\*)\s+(ps_\w+)\(",
                                  src, re.M)))
 
 
