@@ -13,6 +13,14 @@ written, grouped by cluster, into a store in pinned host memory mapped into
 the GPU, and the refresh takes the rows of the selected clusters as
 reconstructed from that store (h~ = rho mu + deq(r)) instead of H
 [Polestar §2.C, CPU offloading].
+
+decode_step()/decode() run the step under the refresh schedule
+(ps_schedule_step, [Polestar §2.A, schedule]): the drift path and the refresh
+run only on steps the schedule marks, a full step refreshes every window
+position from H, a new block resets the commit state and re-seeds k-means;
+the commit runs every step on the last drift computed, and suffix-block
+tokens commit only where the last layer's top-k position mask selects them
+[Polestar §2.B, suffix block commitment].
 """
 
 import torch
@@ -51,7 +59,7 @@ class LayerState:
 class Pipeline:
     """Buffers and the per-step call sequence for workload `w`."""
 
-    def __init__(self, w, layers=None, device="cuda", offload=False):
+    def __init__(self, w, layers=None, device="cuda", offload=False, role=None):
         self.w = w
         self.offload = offload
         if offload and w.dtype != "bf16":
@@ -73,7 +81,10 @@ class Pipeline:
                 st.cl_off = torch.zeros(B, C + 1, dtype=torch.int32, device=device)
                 st.Ht = torch.zeros(B, N, d, dtype=torch.bfloat16, device=device)
         P = w.P
-        self.role = wl.make_roles(w).to(device)
+        self.role = (wl.make_roles(w) if role is None else role).to(device)
+        self.all_pos = torch.arange(N, dtype=torch.int32, device=device).repeat(B, 1)
+        self.all_npos = torch.full((B,), N, dtype=torch.int32, device=device)
+        self._flags = None
         self.undecided = torch.ones(B, P, dtype=torch.uint8, device=device)
         self.d_sum = torch.zeros(B, P, dtype=torch.float32, device=device)
         self.d_cnt = torch.zeros(B, P, dtype=torch.int32, device=device)
@@ -99,10 +110,12 @@ class Pipeline:
         self.d_prev.zero_()
 
     def layer_step(self, l, H, Q, Wk, Wv, init_u=None, first=False, stream=None,
-                   concurrent=False, joins=None):
+                   concurrent=False, joins=None, full=False):
         """One layer.  concurrent: the NVFP4 residuals run on a side stream
         (they depend on k-means only), and the event that ends them is
-        appended to `joins` for the caller to wait on."""
+        appended to `joins` for the caller to wait on.  full: every window
+        position is refreshed, from H (the top-k still sets the position
+        mask)."""
         w, st = self.w, self.state[l]
         cur, prev = st.A[self.t % 2], st.A[(self.t + 1) % 2]
         ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts,
@@ -133,6 +146,12 @@ class Pipeline:
             self._after_proxy = main.record_event()
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
                          st.npos, st.posmask, ws=self.ws[ps.OP_TOPK], stream=stream)
+        if full:
+            if packed is not None:
+                main.wait_event(packed)
+            ps.ps_refresh_kv(H, self.all_pos, self.all_npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
+                             ws=self.ws[ps.OP_REFRESH], stream=stream)
+            return
         src = H
         if self.offload:  # the selected clusters' rows, fetched from the host store
             if packed is not None:
@@ -146,8 +165,9 @@ class Pipeline:
     def commit_step(self, logits, stream=None):
         w, last = self.w, self.state[-1]
         D_blk = last.D[:, w.blk_start:]
+        suffix_sel = last.posmask[:, w.blk_start:]
         ps.ps_commit(logits, self.role, self.undecided, D_blk, w.N, self.d_sum,
-                     self.d_cnt, self.d_prev, None, w.P, self.params, self.token,
+                     self.d_cnt, self.d_prev, suffix_sel, w.N, self.params, self.token,
                      self.conf, self.commit, ws=self.ws[ps.OP_COMMIT], stream=stream)
 
     def step(self, Hs, Qs, Wks, Wvs, logits, init_us=None, first=False, stream=None,
@@ -175,3 +195,60 @@ class Pipeline:
             self.commit_step(logits, stream)
         self.t += 1
 
+
+    def decode_step(self, act, Hs, Qs, Wks, Wvs, logits, init_us=None, stream=None):
+        """One decode step under schedule actions `act` (ps.SCHED_* flags):
+        SLIDE resets the block's commit state; REFRESH runs every layer's
+        drift path (REINIT: k-means++ from init_us and no previous
+        distribution; FULL: every position refreshed); the commit runs every
+        step, on the last layer's most recent drift."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if act & ps.SCHED_SLIDE:
+            with torch.cuda.stream(main):
+                self.reset_block()
+        if act & ps.SCHED_REFRESH:
+            first = bool(act & ps.SCHED_REINIT)
+            for l in range(self.layers):
+                self.layer_step(l, Hs[l], Qs[l], Wks[l], Wvs[l],
+                                None if init_us is None else init_us[l], first, stream,
+                                full=bool(act & ps.SCHED_FULL))
+            self.t += 1
+        self.commit_step(logits, stream)
+
+    def block_progress(self, stream=None):
+        """(tokens committed by the last step, block decided) of the batch,
+        read back to the host (one small copy and a wait on `stream`).  The
+        batch decodes in lockstep: the count is the largest over its windows,
+        and the block is decided when no window has an undecided
+        current-block token."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self._flags is None:
+            self._flags = torch.zeros(2, dtype=torch.int32).pin_memory()
+        cur = (self.role == wl.ROLE_CURRENT)
+        with torch.cuda.stream(main):
+            committed = self.commit.to(torch.int32).sum(dim=1).max()
+            open_ = (self.undecided.bool() & cur).any()
+            self._flags.copy_(torch.stack([committed, open_.to(torch.int32)]),
+                              non_blocking=True)
+        main.synchronize()
+        return int(self._flags[0]), not bool(self._flags[1])
+
+    def decode(self, schedule, inputs, steps, stream=None, on_step=None):
+        """Run `steps` decode steps under `schedule` (a ps.Schedule).
+
+        inputs(t, block_start) returns (Hs, Qs, Wks, Wvs, logits, init_us) of
+        step t, block_start being the schedule's current block; the first
+        step builds the window (k-means++, full refresh).  on_step(t, act) is
+        called after each step's work is enqueued.  Returns the actions
+        taken, one per step."""
+        acts = []
+        act = ps.SCHED_REFRESH | ps.SCHED_FULL | ps.SCHED_REINIT
+        for t in range(steps):
+            Hs, Qs, Wks, Wvs, logits, init_us = inputs(t, schedule.state.block_start)
+            self.decode_step(act, Hs, Qs, Wks, Wvs, logits, init_us, stream)
+            acts.append(act)
+            if on_step is not None:
+                on_step(t, act)
+            committed, done = self.block_progress(stream)
+            act = schedule.step(committed, done)
+        return acts

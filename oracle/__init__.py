@@ -21,6 +21,8 @@ technical summary, written below as ``[Polestar §x, <paragraph>]``:
 * §2.B "Suffix block commitment"   suffix tokens need c >= tau_s
 * §2.C "CPU offloading"            quantised clusters in host memory, the
                                    top-k clusters fetched back
+* §2.A "schedule"                 refresh after tau_upd decoded tokens,
+                                   periodic full passes, window slide
 
 Where the page is silent the oracle takes one explicit reading; each reading
 is named in the docstring of the function that takes it.
