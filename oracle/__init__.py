@@ -23,6 +23,8 @@ technical summary, written below as ``[Polestar §x, <paragraph>]``:
                                    top-k clusters fetched back
 * §2.A "schedule"                 refresh after tau_upd decoded tokens,
                                    periodic full passes, window slide
+* §2.A / §4 "ablation studies"    cosine-dissimilarity and entropy drift
+                                   signals on the proxy distributions
 
 Where the page is silent the oracle takes one explicit reading; each reading
 is named in the docstring of the function that takes it.
@@ -55,3 +57,4 @@ __all__ = [
     "record_bytes", "pack_clusters", "reconstruct_row", "fetch_reconstruct",
 ]
 from .schedule import ScheduleState, schedule_step
+from .scorers import SCORER_KL, SCORER_COSINE, SCORER_ENTROPY, drift_score
