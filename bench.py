@@ -47,6 +47,12 @@ def parse():
     ap.add_argument("--overlap", action="store_true",
                     help="also time the step on a side stream against a synthetic main "
                          "forward (bf16 GEMMs of one layer over the window)")
+    ap.add_argument("--decode", action="store_true",
+                    help="also time the decode loop under the refresh schedule "
+                         "(tau_upd 4, every 4th refresh full) and report it under 'decode'")
+    ap.add_argument("--ablation", action="store_true",
+                    help="also compare the drift signals (KL, cosine, entropy) on the "
+                         "workload's planted drift and time the scoring pass")
     ap.add_argument("--offload", action="store_true",
                     help="quantised clusters in a pinned host store, refresh from the "
                          "reconstruction of the selected clusters (Polestar 2.C)")
@@ -192,7 +198,8 @@ def op_work(w, npos_mean):
 KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
                ("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
                ("k_km_prep", "kmeans_prep"),
-               ("k_kpp_", "kmeans_seeding"), ("k_assign", "kmeans_assign"),
+               ("k_kpp_pick", "kpp_pick"), ("k_kpp_weights", "kpp_weights"),
+               ("k_drift_score", "drift_score"), ("k_assign", "kmeans_assign"),
                ("k_fp4_amax", "nvfp4_amax"), ("k_fp4_quant", "nvfp4_quant"),
                ("Ckeys", "centroid_keys"), ("k_ckeys", "centroid_keys"),
                ("k_split_f32", "proxy_split"), ("Proxy", "proxy_attn"),
@@ -323,6 +330,139 @@ def measure_overlap(w, graphs, dev, reps=20):
             "hidden_fraction": (t_main + t_drift - t_both) / t_drift,
             "both_us_drift_high_priority": t_both_hi,
             "hidden_fraction_drift_high_priority": (t_main + t_drift - t_both_hi) / t_drift}
+
+
+def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, full_period=4):
+    """The decode loop under the refresh schedule, eager, on the workload's
+    layer.  Wall pace: the host reads every step's outcome (tokens
+    committed, block decided) to take the schedule's decision, as a decode
+    loop must.  Device time by step kind: a second run in which a device-side
+    spin before each step lets the host enqueue the whole step first, so the
+    events time the kernels.  The re-init step's kernels: the library trace
+    of one such step."""
+    import torch
+    from drift_aware_kv_spherical_gb300 import polestar as ps
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+    pipe = Pipeline(w, layers=1, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    marks, tokens, timing = [], [0], [False]
+    plain = pipe.block_progress
+
+    def progress(stream=None):
+        c, done = plain(stream)
+        tokens[0] += c
+        return c, done
+
+    pipe.block_progress = progress
+
+    def inputs(t, block_start):
+        if timing[0]:
+            torch.cuda._sleep(2_000_000)
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks.append([ev, None])
+        return [Hs[t % 4]], [Qs[t % 4]], [L["Wk"]], [L["Wv"]], logits[t % 4], [u]
+
+    def on_step(t, act):
+        if timing[0]:
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks[-1][1] = ev
+
+    def run(n):
+        return pipe.decode(ps.Schedule(tau_upd, full_period, w.P), inputs, n, on_step=on_step)
+
+    run(warm)
+    torch.cuda.synchronize()
+    tokens[0] = 0
+    t0 = time.perf_counter()
+    acts = run(steps)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ntok = tokens[0]
+    timing[0] = True
+    acts_t = run(steps)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    kinds = {"reuse": [], "refresh": [], "full": [], "reinit": []}
+    for (a, b), act in zip(marks, acts_t):
+        k = ("reinit" if act & ps.SCHED_REINIT else "full" if act & ps.SCHED_FULL
+             else "refresh" if act & ps.SCHED_REFRESH else "reuse")
+        kinds[k].append(a.elapsed_time(b))
+    # the kernels of one re-init step (k-means++ seeding, full refresh)
+    timing[0] = False
+    Hs0, Qs0, Wk0, Wv0, lg0, us0 = inputs(0, 0)
+    ps.ps_trace_enable(True)
+    torch.cuda._sleep(20_000_000)      # the step's ~140 launches enqueued before it runs
+    pipe.decode_step(ps.SCHED_REFRESH | ps.SCHED_FULL | ps.SCHED_REINIT | ps.SCHED_SLIDE,
+                     Hs0, Qs0, Wk0, Wv0, lg0, us0)
+    torch.cuda.synchronize()
+    rec = ps.ps_trace_records()
+    ps.ps_trace_enable(False)
+    by = {}
+    for name, ms in rec:
+        key = kernel_key(name) or name[:40]
+        n, tot = by.get(key, (0, 0.0))
+        by[key] = (n + 1, tot + ms)
+    return {"tau_upd": tau_upd, "full_period": full_period, "steps": steps,
+            "wall_ms_per_step": wall * 1e3 / steps, "tokens_per_s": ntok / wall,
+            "tokens": ntok, "refresh_frac": sum(bool(a & 1) for a in acts) / steps,
+            "full_frac": sum(bool(a & 2) and not a & 8 for a in acts) / steps,
+            "reinit_frac": sum(bool(a & 8) for a in acts) / steps,
+            "device_ms_by_step_kind": {k: (statistics.mean(v) if v else None)
+                                       for k, v in kinds.items()},
+            "reinit_step_kernels": {k: {"launches": n, "us": round(t * 1e3, 1)}
+                                    for k, (n, t) in sorted(by.items(), key=lambda x: -x[1][1])},
+            "timing": "wall: eager loop with one host read per step; device: CUDA events "
+                      "around each step, enqueued ahead behind a device-side spin"}
+
+
+def measure_ablation(w, L, Hs, Qs, logits, u, dev, steps=3, reps=50):
+    """The drift signals side by side on synthetic data: for each scorer, a
+    window build and `steps` drifted steps of the workload's layer; the rows
+    whose hidden state moved are the truth, and the top-k refresh positions
+    the selection.  Reports precision and recall of the selection (summed
+    over the steps) and the scoring pass's device time on the proxy
+    distributions (ps_drift_score; KL is fused into the proxy on the default
+    path)."""
+    import torch
+    from drift_aware_kv_spherical_gb300 import polestar as ps
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+    names = {ps.SCORER_KL: "kl", ps.SCORER_COSINE: "cosine", ps.SCORER_ENTROPY: "entropy"}
+    out = {}
+    for scorer, name in names.items():
+        pipe = Pipeline(w, layers=1, device=dev, scorer=scorer)
+        pipe.step([Hs[0]], [Qs[0]], [L["Wk"]], [L["Wv"]], logits[0], init_us=[u], first=True)
+        tp = sel = truth = 0
+        for t in range(1, steps + 1):
+            pipe.step([Hs[t]], [Qs[t]], [L["Wk"]], [L["Wv"]], logits[t])
+            moved = (Hs[t] != Hs[t - 1]).any(dim=-1)
+            picked = pipe.state[0].posmask.bool()
+            tp += int((moved & picked).sum())
+            sel += int(picked.sum())
+            truth += int(moved.sum())
+        st = pipe.state[0]
+        cur, prev = st.A[(pipe.t + 1) % 2], st.A[pipe.t % 2]
+        D = torch.empty_like(st.D)
+        for _ in range(5):
+            ps.ps_drift_score(cur, prev, scorer, D)
+        ps.ps_trace_enable(True)
+        torch.cuda._sleep(10_000_000)  # the launches enqueued before they run
+        for _ in range(reps):
+            ps.ps_drift_score(cur, prev, scorer, D)
+        torch.cuda.synchronize()
+        rec = ps.ps_trace_records()
+        ps.ps_trace_enable(False)
+        ps.ps_check()
+        us = statistics.mean(ms for _, ms in rec) * 1e3
+        nbytes = cur.numel() * 4 * (1 if scorer == ps.SCORER_ENTROPY else 2) + D.numel() * 4
+        out[name] = {"precision": tp / max(sel, 1), "recall": tp / max(truth, 1),
+                     "selected_rows": sel, "moved_rows": truth,
+                     "score_pass_us": us, "score_pass_gbs": nbytes / (us * 1e-6) / 1e9}
+    out["note"] = ("truth: rows whose hidden state changed between steps (the current block "
+                   "and a seeded share of the others); selection: the top-k clusters' rows; "
+                   "score pass: the library trace's events around each launch, L2-resident")
+    return out
 
 
 def offload_rates(records, nsteps, w, npos_mean):
@@ -728,6 +868,10 @@ def main():
     }
     if args.overlap:
         line["overlap"] = measure_overlap(w, graphs, dev)
+    if args.ablation:
+        line["ablation"] = measure_ablation(w, L, Hs, Qs, logits, u, dev)
+    if args.decode:
+        line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev)
     if args.offload:
         line["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
         line["offload"] = offload_rates(trace, ntrace, w, npos_seen[-1] / w.B)

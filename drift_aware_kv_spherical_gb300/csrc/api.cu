@@ -307,6 +307,19 @@ ps_status ps_topk_drift(ps_handle h, const float* D, const int32_t* assign,
   return launch_status(topk_run(a, static_cast<cudaStream_t>(stream)));
 }
 
+ps_status ps_drift_score(ps_handle h, const float* A_cur, const float* A_prev, int B, int N,
+                         int C, int scorer, float* D, void* stream) {
+  TraceScope trace_scope(h);
+  PS_REQUIRE(h != nullptr && B >= 0);
+  if (B == 0) return PS_OK;
+  PS_REQUIRE(N >= 1 && C >= 1 && C <= 4096 && (long)B * N <= 2147483647L);
+  PS_REQUIRE(scorer >= PS_SCORER_KL && scorer <= PS_SCORER_ENTROPY);
+  PS_NN(A_cur); PS_NN(D);
+  PS_REQUIRE(D != A_cur && D != A_prev);
+  return launch_status(drift_score_run(A_cur, A_prev, B, N, C, scorer, D,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
                         const int32_t* pos, const int32_t* npos,
                         const void* Wk, const void* Wv, int B, int N, int d,

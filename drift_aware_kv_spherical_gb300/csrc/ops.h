@@ -73,6 +73,10 @@ struct ProxyArgs {
 size_t proxy_ws(int B, int N, int d, int C, int Hq, int Hkv, int dh);
 cudaError_t proxy_run(const ProxyArgs& a, cudaStream_t s);
 
+// ablation drift signals over the proxy distributions (PS_SCORER_*)
+cudaError_t drift_score_run(const float* A_cur, const float* A_prev, int B, int N, int C,
+                            int scorer, float* D, cudaStream_t s);
+
 struct TopkArgs {
   const float* D; const int32_t* assign; const int32_t* counts;
   int B, N, C, k;

@@ -21,6 +21,11 @@ position from H, a new block resets the commit state and re-seeds k-means;
 the commit runs every step on the last drift computed, and suffix-block
 tokens commit only where the last layer's top-k position mask selects them
 [Polestar §2.B, suffix block commitment].
+
+scorer selects the drift signal: the proxy's fused KL (default), or one of
+the ablation signals (cosine dissimilarity, entropy) computed by
+ps_drift_score over the same proxy distributions [Polestar §4, ablation
+studies].
 """
 
 import torch
@@ -59,8 +64,10 @@ class LayerState:
 class Pipeline:
     """Buffers and the per-step call sequence for workload `w`."""
 
-    def __init__(self, w, layers=None, device="cuda", offload=False, role=None):
+    def __init__(self, w, layers=None, device="cuda", offload=False, role=None,
+                 scorer=ps.SCORER_KL):
         self.w = w
+        self.scorer = scorer
         self.offload = offload
         if offload and w.dtype != "bf16":
             raise ValueError("the offload path reconstructs bf16 rows: bf16 workloads only")
@@ -140,8 +147,11 @@ class Pipeline:
             if self.offload:
                 ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store,
                                           st.order, st.cl_off, stream=stream)
-        ps.ps_proxy_attn_kl(Q, st.chat, Wk, None if first else prev, cur, st.D, w.Hkv,
-                            ws=self.ws[ps.OP_PROXY_KL], stream=stream)
+        fused = self.scorer == ps.SCORER_KL  # the proxy's own KL epilogue
+        ps.ps_proxy_attn_kl(Q, st.chat, Wk, None if first or not fused else prev, cur, st.D,
+                            w.Hkv, ws=self.ws[ps.OP_PROXY_KL], stream=stream)
+        if not fused:  # an ablation signal over the same distributions
+            ps.ps_drift_score(cur, None if first else prev, self.scorer, st.D, stream=stream)
         if concurrent:  # the drift is final here: the commit may start
             self._after_proxy = main.record_event()
         ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,

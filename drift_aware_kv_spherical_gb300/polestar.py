@@ -22,7 +22,7 @@ EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
             "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit",
             "ps_store_record_bytes", "ps_host_alloc", "ps_host_free",
-            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant", "ps_schedule_step"]
+            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant", "ps_schedule_step", "ps_drift_score"]
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -56,6 +56,7 @@ class ScheduleState(ctypes.Structure):
 
 
 SCHED_REFRESH, SCHED_FULL, SCHED_SLIDE, SCHED_REINIT = 1, 2, 4, 8
+SCORER_KL, SCORER_COSINE, SCORER_ENTROPY = 0, 1, 2
 
 _SIGS = {
     "ps_create": (_i, [_i, ctypes.POINTER(_p)]),
@@ -71,6 +72,7 @@ _SIGS = {
     "ps_store_record_bytes": (_sz, [_i]),
     "ps_host_alloc": (_i, [_sz, ctypes.POINTER(_p)]),
     "ps_host_free": (_i, [_p]),
+    "ps_drift_score": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _p]),
     "ps_schedule_step": (_i, [ctypes.POINTER(ScheduleParams), ctypes.POINTER(ScheduleState),
                               _i, _i]),
     "ps_nvfp4_pack_clusters": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]),
@@ -258,6 +260,16 @@ def ps_commit(logits, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
         d_ld, _ptr(d_sum), _ptr(d_cnt), _ptr(d_prev), _ptr(suffix_sel), sel_ld, params,
         _ptr(token), _ptr(conf), _ptr(commit), w, wn, _stream(stream))
     _check(st, "ps_commit")
+
+
+def ps_drift_score(A_cur, A_prev, scorer, D, stream=None):
+    """Ablation drift signal (SCORER_*) of distributions A_cur [B][N][C]
+    against A_prev (or None) into D [B][N]."""
+    lib = _lib()
+    B, N, C = A_cur.shape
+    st = lib.cdll.ps_drift_score(lib.handle(), _ptr(A_cur), _ptr(A_prev), B, N, C, int(scorer),
+                                 _ptr(D), _stream(stream))
+    _check(st, "ps_drift_score")
 
 
 def ps_nvfp4_residual_noalloc(H, mu, assign, rho, codes, scales, tensor_scale,

@@ -97,7 +97,7 @@ int ps_trace_count(ps_handle h);
 ps_status ps_trace_get(ps_handle h, int i, const char** name, float* ms);
 
 /* ---------------------------------------------------------------------------
- * Offload of the quantised clusters (§8(f) next #1).
+ * Offload of the quantised clusters.
  * [Polestar §2.C, CPU offloading] -- "quantised hidden-state clusters are
  * offloaded to pinned CPU memory while only the centroids stay on the GPU;
  * the top-k clusters are fetched asynchronously".
@@ -353,6 +353,35 @@ ps_status ps_nvfp4_residual_noalloc(ps_handle h, const void* H, int dtype,
                                     const float* rho, int B, int N, int d,
                                     int C, uint8_t* codes, uint8_t* scales,
                                     float* tensor_scale, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Alternative drift signals for the ablation.
+ * [Polestar §2.A, drift measurement]: KL drift tracks contextual shifts more
+ * closely than cosine dissimilarity on subsets; [Polestar §4, ablation
+ * studies]: it beats cosine similarity and uncertainty-based selection.
+ *
+ * One signal per position from the proxy distributions that
+ * ps_proxy_attn_kl wrote (call it with A_prev = NULL to skip its fused KL,
+ * then this on its A_cur and the previous step's distribution):
+ *   PS_SCORER_KL       D = max(0, sum_c a ln(a / max(a', 1e-30))), a > 0
+ *   PS_SCORER_COSINE   D = max(0, 1 - <a, a'> / (|a| |a'|)); 0 if a norm is 0
+ *   PS_SCORER_ENTROPY  D = -sum_c a ln a over a > 0 (uncertainty of the
+ *                      current distribution; A_prev is not read)
+ * With A_prev == NULL, KL and COSINE write D = 0.
+ *
+ * A_cur, A_prev [B][N][C] f32 (rows of any non-negative weights; the proxy
+ * writes distributions); D [B][N] f32 out, must not alias either input.
+ * Sizes: B >= 0 (0: no-op), N >= 1, 1 <= C <= 4096, B * N <= 2^31 - 1.
+ * Errors: a NULL handle, A_cur or D, a bad size or an unknown scorer return
+ * PS_ERR_ARG before anything is enqueued.
+ * ------------------------------------------------------------------------- */
+typedef enum {
+  PS_SCORER_KL = 0, PS_SCORER_COSINE = 1, PS_SCORER_ENTROPY = 2
+} ps_scorer;
+
+ps_status ps_drift_score(ps_handle h, const float* A_cur, const float* A_prev,
+                         int B, int N, int C, int scorer, float* D,
+                         void* stream);
 
 /* ---------------------------------------------------------------------------
  * Refresh schedule of the decode loop (host only; no handle, no GPU work).
