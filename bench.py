@@ -198,7 +198,8 @@ def op_work(w, npos_mean):
 KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
                ("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
                ("k_km_prep", "kmeans_prep"),
-               ("k_kpp_pick", "kpp_pick"), ("k_kpp_weights", "kpp_weights"),
+               ("k_kpp_gram", "kpp_gram"), ("k_kpp_pick", "kpp_pick"),
+               ("k_kpp_weights", "kpp_weights"),
                ("k_drift_score", "drift_score"), ("k_assign", "kmeans_assign"),
                ("k_fp4_amax", "nvfp4_amax"), ("k_fp4_quant", "nvfp4_quant"),
                ("Ckeys", "centroid_keys"), ("k_ckeys", "centroid_keys"),

@@ -10,6 +10,8 @@
 //                   for the tensor cores, one launch
 //   k_kpp_pick      k-means++ centre r, one CTA per window   (init_mode 1)
 //   k_kpp_weights   weights against centre r, warp per row   (C - 1 rounds)
+//                   (the Gram form seeds from K instead: k_kpp_gram, one
+//                   launch for all rounds; see kmeans_gram.cu)
 //   assignment      bf16 windows: tcgen05 tiles of 128 rows x C centroids,
 //                   <h, mu_hi> + <h, mu_lo> accumulated in TMEM, split over
 //                   d when the windows give too few row tiles.  The d-chunks
@@ -924,9 +926,12 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const long n_mu = p.tc ? (long)a.B * a.C * a.d : 0;
   const int split_blocks = n_mu > 0 ? std::min(ceil_div(n_mu / 4, 256), 2 * kSmTarget) : 0;
   const bool seeding = a.init_mode == 1;
+  // Gram form with k-means++: the seeds come from K itself (gram_seed), one
+  // launch instead of 2C - 1, and pass 0's cosines are K's columns
+  const bool gram_seeding = gram && seeding;
   launch_pdl(k_km_prep<T>, inv_blocks + (seeding ? 0 : split_blocks), 256, 0, s, H, BN_, a.d,
              w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, split_hi, split_lo, cd);
-  if (seeding) {
+  if (seeding && !gram_seeding) {
     for (int r = 0; r < a.C; ++r) {
       launch_pdl(k_kpp_pick<T>, a.B, 1024, 0, s, H, w.inv, a.init_u, a.N, a.d, a.C, r, a.mu,
                  w.w, w.chosen);
@@ -952,13 +957,17 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   // forms mu^(I) from the labels of pass I - 1 and C_hat from those of pass I
   if (gram) {
     const auto* Hb = static_cast<const __nv_bfloat16*>(a.H);
-    cudaError_t e = fused0 ? cudaSuccess : assign_pass(w.L);
+    const bool pass0_in_l = fused0 || gram_seeding;  // pass 0's cosines arrive in L
+    cudaError_t e = pass0_in_l ? cudaSuccess : assign_pass(w.L);
     if (e == cudaSuccess)
-      e = gram_build(g, Hb, w.inv, a.B, a.N, a.d, a.C, fused0 ? w.mu_split : nullptr, w.L,
-                     w.qhi, w.qlo, a.status, s);
+      e = gram_build(g, Hb, w.inv, a.B, a.N, a.d, a.C,
+                     fused0 && !gram_seeding ? w.mu_split : nullptr, w.L, w.qhi, w.qlo,
+                     a.status, s);
+    if (e == cudaSuccess && gram_seeding)
+      e = gram_seed(g, Hb, w.inv, a.init_u, a.B, a.N, a.d, a.C, w.qhi, w.qlo, a.mu, w.L, s);
     if (e == cudaSuccess)
       e = gram_iterate(g, w.qhi, w.qlo, a.B, a.N, a.C, a.iters, Hb, a.d, w.inv, a.mu, a.assign,
-                       w.prev, a.rho, w.L, fused0 ? nullptr : w.objp, p.ntile, a.obj,
+                       w.prev, a.rho, w.L, pass0_in_l ? nullptr : w.objp, p.ntile, a.obj,
                        a.iters + 1, a.status, s);
     if (e == cudaSuccess)
       e = launch_scan<T, false, true>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C,

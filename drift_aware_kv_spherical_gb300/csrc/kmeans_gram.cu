@@ -761,6 +761,71 @@ int gram_capacity(int z, size_t smem) {
   return n;
 }
 
+// k-means++ seeding of a window from its Gram matrix, one CTA of 1024
+// threads per window (thread i = row i, N <= 1024).  Round r picks centre r
+// exactly as the row-by-row seeding does (row floor(u_0 N) first; then the
+// first row whose fp64 running weight sum, in row order, exceeds u_r times
+// the total, or the first row not yet chosen when no weight is left) and
+// lowers every weight to min(w_i, max(0, 1 - cos(x_i, x_pick))), 0 for
+// chosen rows, with the cosine read from K's column pick (contiguous over
+// the rows of a slab).  At the end the seeds mu_r = h_pick / ||h_pick|| are
+// written, and pass 0's cosines L[i][r] = K[i][pick_r], which are the rows'
+// cosines against the seeds, so that no assignment pass is needed.
+__global__ void __launch_bounds__(1024)
+k_kpp_gram(const __nv_bfloat16* __restrict__ H, const float* __restrict__ inv_all,
+           const double* __restrict__ U, const int16_t* __restrict__ qhi,
+           const uint8_t* __restrict__ qlo, int N, int d, int C, int R, int Z,
+           float* __restrict__ mu, float* __restrict__ L) {
+  __shared__ double s_scan[32];
+  __shared__ int s_min[32];
+  __shared__ int s_pick[256];
+  pdl_prologue();
+  const int b = blockIdx.x, i = threadIdx.x;
+  const bool live = i < N;
+  const double* u = U + (long)b * C;
+  // element (i, j) of the window's K at base + j R (the slab layout)
+  const long long base = live ? ((long long)b * Z + i / R) * N * R + i % R : 0;
+  auto cosq = [&](int j) {
+    const long long o = base + (long long)j * R;
+    return static_cast<float>(static_cast<int>(qhi[o]) * 256 + static_cast<int>(qlo[o])) *
+           (1.f / kGramScale);
+  };
+  float wgt = 0.f;
+  bool chosen = false;
+  int pick = min(max((int)floor(u[0] * (double)N), 0), N - 1);
+  for (int r = 0; r < C; ++r) {
+    if (r > 0) {
+      const double wv = live ? (double)wgt : 0.0;
+      double total;
+      double run = block_exclusive_scan<double>(wv, s_scan, &total);
+      run += wv;
+      const int cand = (total > 0.0 && live && run > u[r] * total) ? i : INT_MAX;
+      pick = block_min_int(cand, s_min);
+      if (pick == INT_MAX) {  // no weight left: first row not yet chosen
+        pick = block_min_int(live && !chosen ? i : INT_MAX, s_min);
+        if (pick == INT_MAX) pick = 0;
+      }
+    }
+    if (i == pick) chosen = true;
+    if (i == 0) s_pick[r] = pick;
+    if (r + 1 < C && live) {
+      const float cw = chosen ? 0.f : fmaxf(0.f, 1.f - cosq(pick));
+      wgt = r == 0 ? cw : fminf(wgt, cw);
+    }
+  }
+  __syncthreads();
+  const __nv_bfloat16* Hb = H + (long)b * N * d;
+  const float* inv = inv_all + (long)b * N;
+  for (long e = i; e < (long)C * d; e += blockDim.x) {
+    const int r = (int)(e / d), k = (int)(e % d), p = s_pick[r];
+    mu[((long)b * C + r) * d + k] = to_f32(Hb[(long)p * d + k]) * inv[p];
+  }
+  if (live) {
+    float* Li = L + ((long)b * N + i) * C;
+    for (int r = 0; r < C; ++r) Li[r] = cosq(s_pick[r]);
+  }
+}
+
 }  // namespace
 
 GramPlan gram_plan(int dtype, int B, int N, int d, int C) {
@@ -832,6 +897,14 @@ cudaError_t gram_iterate(const GramPlan& g, const int16_t* qhi, const uint8_t* q
   cfg.numAttrs = 1;
   return launch_ex(cfg, k_km_gram, qhi, qlo, N, C, g.R, passes, H, d, inv, mu, assign, prev, rho,
                    L, objp0, ntile0, obj, obj_ld, objp0 == nullptr ? 1 : 0, status);
+}
+
+cudaError_t gram_seed(const GramPlan& g, const __nv_bfloat16* H, const float* inv,
+                      const double* U, int B, int N, int d, int C, const int16_t* qhi,
+                      const uint8_t* qlo, float* mu, float* L, cudaStream_t s) {
+  if (N > 1024 || C > 256) return cudaErrorInvalidValue;
+  launch_pdl(k_kpp_gram, dim3(B), 1024, 0, s, H, inv, U, qhi, qlo, N, d, C, g.R, g.Z, mu, L);
+  return cudaGetLastError();
 }
 
 }  // namespace ps

@@ -33,6 +33,11 @@ bool gram_launchable(const GramPlan& g);
 cudaError_t gram_build(const GramPlan& g, const __nv_bfloat16* H, const float* inv, int B,
                        int N, int d, int C, const __nv_bfloat16* mu_split, float* cos0,
                        int16_t* qhi, uint8_t* qlo, int* status, cudaStream_t s);
+// k-means++ seeds of every window from its K (after gram_build without
+// mu_split): mu [B][C][d] and pass 0's cosines L [B][N][C]; N <= 1024
+cudaError_t gram_seed(const GramPlan& g, const __nv_bfloat16* H, const float* inv,
+                      const double* U, int B, int N, int d, int C, const int16_t* qhi,
+                      const uint8_t* qlo, float* mu, float* L, cudaStream_t s);
 // passes 1..passes from the labels in assign and the cosines L of pass 0
 // (objp0 == nullptr: pass 0 itself too, from L);
 // leaves the last pass's labels in assign, the pass before's in prev, rho,

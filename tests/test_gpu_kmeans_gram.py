@@ -186,3 +186,49 @@ def test_gram_centroid_emptied_mid_run_is_kept():
     assert_close(g["mu"][0], o["mu"], what="mu")          # mu_1 from pass 1, not mu0_1
     assert_close(g["rho"][0], o["rho"], what="rho")
     assert_close(g["obj"][0], o["obj"], what="objective")
+
+
+@pytest.mark.parametrize("B,N,d,C,seed", [(2, 700, 512, 48, 10), (3, 1024, 1024, 64, 8),
+                                          (3, 257, 256, 100, 6), (1, 96, 128, 96, 3)])
+def test_gram_seeding_matches_oracle_kmeanspp(B, N, d, C, seed):
+    """k-means++ seeded from the window's Gram matrix (one launch), then the
+    Gram passes: the seeds of every draw outside the tie band are the
+    oracle's (k-means++ on the unit rows in fp64), so a window whose passes
+    also stay outside the band (one near-tie moves a row, hence a centroid,
+    hence rows far from any tie) matches the oracle's k-means from them in
+    full.  C = N (every row a seed) and C > 64 (no pass-0 tiles) included.
+    The seeds give each case such a window (a 64-round draw over 1024 rows
+    clears 1e-5 about one time in four)."""
+    Ht, Hn, _ = _planted(B, N, d, C, seed)
+    u = torch.from_numpy(np.random.default_rng(seed).random((B, C))).cuda()
+    g = run_kmeans(Ht, torch.zeros(B, C, d, device="cuda"), 3, init_u=u)
+    pinned = 0
+    for b in range(B):
+        mu0, _, m0 = oracle.kmeanspp_init(Hn[b], C, np_(u[b]), return_margin=True)
+        if m0 < 1e-5 or oracle.kmeans_spherical(Hn[b], mu0, 3)["margin"].min() <= KM_MARGIN:
+            continue
+        pinned += 1
+        assert _check({k: v[b:b + 1] for k, v in g.items()}, Hn[b:b + 1], mu0[None], 3) == 1
+    assert pinned >= 1
+
+
+def test_gram_seeding_trace_shape():
+    """With k-means++ the Gram form launches set-up, the Gram GEMM, the
+    seeding, the passes and the scan: five kernels, none per seed."""
+    Ht, _, _ = _planted(1, 256, 128, 16, seed=2)
+    u = torch.rand(1, 16, dtype=torch.float64, device="cuda")
+    ws = ps.workspace(ps.OP_KMEANS, B=1, N=256, d=128, C=16)
+    out = dict(mu=torch.zeros(1, 16, 128, device="cuda"),
+               assign=torch.zeros(1, 256, dtype=torch.int32, device="cuda"),
+               rho=torch.zeros(1, 256, device="cuda"), chat=torch.zeros(1, 16, 128, device="cuda"),
+               counts=torch.zeros(1, 16, dtype=torch.int32, device="cuda"))
+    ps.ps_trace_enable(True)
+    ps.ps_kmeans_spherical(Ht, out["mu"], out["assign"], out["rho"], out["chat"], out["counts"],
+                           4, init_mode=1, init_u=u, ws=ws)
+    torch.cuda.synchronize()
+    names = [n for n, _ in ps.ps_trace_records()]
+    ps.ps_trace_enable(False)
+    ps.ps_check()
+    assert len(names) == 5, names
+    assert sum("k_kpp_gram" in n for n in names) == 1
+    assert not any("k_kpp_pick" in n or "k_kpp_weights" in n for n in names)
