@@ -761,47 +761,57 @@ int gram_capacity(int z, size_t smem) {
   return n;
 }
 
+// q of K's element (i, j), kh / kl pointing at row i's base in the slab
+__device__ __forceinline__ int kq(const int16_t* kh, const uint8_t* kl, int j, int R) {
+  const long long o = (long long)j * R;
+  return static_cast<int>(kh[o]) * 256 + static_cast<int>(kl[o]);
+}
+
 // k-means++ seeding of a window from its Gram matrix, one CTA of 1024
 // threads per window (thread i = row i, N <= 1024).  Round r picks centre r
-// exactly as the row-by-row seeding does (row floor(u_0 N) first; then the
-// first row whose fp64 running weight sum, in row order, exceeds u_r times
-// the total, or the first row not yet chosen when no weight is left) and
-// lowers every weight to min(w_i, max(0, 1 - cos(x_i, x_pick))), 0 for
-// chosen rows, with the cosine read from K's column pick (contiguous over
-// the rows of a slab).  At the end the seeds mu_r = h_pick / ||h_pick|| are
-// written, and pass 0's cosines L[i][r] = K[i][pick_r], which are the rows'
-// cosines against the seeds, so that no assignment pass is needed.
+// as the row-by-row seeding does (row floor(u_0 N) first; then the first row
+// whose running weight sum, in row order, exceeds u_r times the total -- the
+// count of rows at or below it, the sums being non-decreasing -- or the first
+// row not yet chosen when no weight is left) and lowers every
+// weight to min(w_i, max(0, 1 - cos(x_i, x_pick))), 0 for chosen rows, with
+// the cosine q 2^-20 read from K's column pick (contiguous over the rows of
+// a slab).  The weights are then exact multiples of 2^-20, so they are kept
+// as integers 2^20 - q (capped at 2^21, |cos| <= 1) and summed exactly in 32
+// bits (N 2^21 <= 2^31): the same picks as exact fp64 sums, without the
+// fp64 scan.  At the end the seeds mu_r = h_pick / ||h_pick|| are written,
+// and pass 0's cosines L[i][r] = K[i][pick_r], which are the rows' cosines
+// against the seeds, so that no assignment pass is needed.
 __global__ void __launch_bounds__(1024)
 k_kpp_gram(const __nv_bfloat16* __restrict__ H, const float* __restrict__ inv_all,
            const double* __restrict__ U, const int16_t* __restrict__ qhi,
            const uint8_t* __restrict__ qlo, int N, int d, int C, int R, int Z,
            float* __restrict__ mu, float* __restrict__ L) {
-  __shared__ double s_scan[32];
+  __shared__ uint32_t s_scan[32];
   __shared__ int s_min[32];
   __shared__ int s_pick[256];
+  __shared__ double s_u[256];
   pdl_prologue();
   const int b = blockIdx.x, i = threadIdx.x;
   const bool live = i < N;
-  const double* u = U + (long)b * C;
+  for (int r = i; r < C; r += blockDim.x) s_u[r] = U[(long)b * C + r];
+  __syncthreads();
   // element (i, j) of the window's K at base + j R (the slab layout)
   const long long base = live ? ((long long)b * Z + i / R) * N * R + i % R : 0;
-  auto cosq = [&](int j) {
-    const long long o = base + (long long)j * R;
-    return static_cast<float>(static_cast<int>(qhi[o]) * 256 + static_cast<int>(qlo[o])) *
-           (1.f / kGramScale);
-  };
-  float wgt = 0.f;
+  const int16_t* kh = qhi + base;
+  const uint8_t* kl = qlo + base;
+  uint32_t wgt = 0u;  // weight in units of 2^-20
   bool chosen = false;
-  int pick = min(max((int)floor(u[0] * (double)N), 0), N - 1);
+  int pick = min(max((int)floor(s_u[0] * (double)N), 0), N - 1);
   for (int r = 0; r < C; ++r) {
     if (r > 0) {
-      const double wv = live ? (double)wgt : 0.0;
-      double total;
-      double run = block_exclusive_scan<double>(wv, s_scan, &total);
-      run += wv;
-      const int cand = (total > 0.0 && live && run > u[r] * total) ? i : INT_MAX;
-      pick = block_min_int(cand, s_min);
-      if (pick == INT_MAX) {  // no weight left: first row not yet chosen
+      const uint32_t wv = live ? wgt : 0u;
+      uint32_t total;
+      const uint32_t run = block_exclusive_scan<uint32_t>(wv, s_scan, &total) + wv;
+      // the running sums do not decrease, so the first row above the target
+      // is the number of rows at or below it (N when none is above)
+      const double target = s_u[r] * (double)total;
+      pick = __syncthreads_count(live && (double)run <= target);
+      if (total == 0u || pick >= N) {  // no weight left: first row not yet chosen
         pick = block_min_int(live && !chosen ? i : INT_MAX, s_min);
         if (pick == INT_MAX) pick = 0;
       }
@@ -809,8 +819,9 @@ k_kpp_gram(const __nv_bfloat16* __restrict__ H, const float* __restrict__ inv_al
     if (i == pick) chosen = true;
     if (i == 0) s_pick[r] = pick;
     if (r + 1 < C && live) {
-      const float cw = chosen ? 0.f : fmaxf(0.f, 1.f - cosq(pick));
-      wgt = r == 0 ? cw : fminf(wgt, cw);
+      const uint32_t cw =
+          chosen ? 0u : static_cast<uint32_t>(min(max((1 << 20) - kq(kh, kl, pick, R), 0), 1 << 21));
+      wgt = r == 0 ? cw : min(wgt, cw);
     }
   }
   __syncthreads();
@@ -822,7 +833,8 @@ k_kpp_gram(const __nv_bfloat16* __restrict__ H, const float* __restrict__ inv_al
   }
   if (live) {
     float* Li = L + ((long)b * N + i) * C;
-    for (int r = 0; r < C; ++r) Li[r] = cosq(s_pick[r]);
+    for (int r = 0; r < C; ++r)
+      Li[r] = static_cast<float>(kq(kh, kl, s_pick[r], R)) * (1.f / kGramScale);
   }
 }
 
