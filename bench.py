@@ -190,7 +190,7 @@ def op_work(w, npos_mean):
                      2.0 * B * C * d * nkv + 2.0 * B * N * w.Hq * C * w.dh),
         "topk": (B * N * 13, 0.0),
         "refresh": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
-        "commit": (B * w.P * w.V * 4, 0.0),
+        "commit": (B * w.P * w.V * esz, 0.0),
     }
 
 
@@ -249,7 +249,7 @@ def kernel_work(key, w, npos_mean):
         "topk": (B * N * 13, 0.0),
         "refresh_gather": (2 * M * d * esz, 0.0),
         "refresh_gemm": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
-        "commit_scan": (B * w.P * w.V * 4, 0.0),
+        "commit_scan": (B * w.P * w.V * esz, 0.0),
     }.get(key)
 
 
@@ -525,7 +525,8 @@ def run_reference(args):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy() for H in Hs]
     Hn = [H.float().numpy() for H in Hs]
-    logits = [wl.make_logits(w, t).numpy() for t in range(4)]
+    # the LM head's output dtype (bf16 values, exact in the oracle's fp64)
+    logits = [wl.make_logits(w, t).to(wl.torch_dtype(w)).float().numpy() for t in range(4)]
     u = wl.make_uniforms(w).numpy()
     mu = [oracle.kmeanspp_init(Hn[0][b], w.C, u[b])[0] for b in range(w.B)]
     A_prev = [None] * w.B
@@ -589,7 +590,7 @@ def _blas_threads():
 def workload_config(w):
     return {"workload": w.name, "B": w.B, "N": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "dh": w.dh, "C": w.C, "iters": w.iters, "k": w.k, "P": w.P, "V": w.V,
-            "layers": 1, "l2": "flushed between steps (512 MB write)"}
+            "layers": 1, "logits": w.dtype, "l2": "flushed between steps (512 MB write)"}
 
 
 def cpu_baseline(w, budget_s=20.0):
@@ -640,7 +641,8 @@ def main():
     for t in range(1, 4):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
-    logits = [wl.make_logits(w, t, dev) for t in range(4)]
+    # logits in the workload's dtype, as the model's LM head emits them
+    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(4)]
     u = wl.make_uniforms(w, 0, dev)
     pipe = Pipeline(w, layers=1, device=dev, offload=args.offload)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)

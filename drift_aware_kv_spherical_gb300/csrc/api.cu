@@ -345,14 +345,14 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
   return launch_status(refresh_run(a, static_cast<cudaStream_t>(stream)));
 }
 
-ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
+ps_status ps_commit(ps_handle h, const void* logits, int dtype, int B, int P, int V,
                     const uint8_t* role, uint8_t* undecided,
                     const float* D_blk, int d_ld, float* d_sum, int32_t* d_cnt,
                     float* d_prev, const uint8_t* suffix_sel, int sel_ld,
                     ps_commit_params params, int32_t* token, float* conf,
                     uint8_t* commit, void* ws, size_t ws_bytes, void* stream) {
   TraceScope trace_scope(h);
-  PS_REQUIRE(h != nullptr && B >= 0 && P >= 0);
+  PS_REQUIRE(h != nullptr && dtype_ok(dtype) && B >= 0 && P >= 0);
   if (B == 0 || P == 0) return PS_OK;
   PS_REQUIRE(P <= 1024 && V >= 4 && V % 4 == 0 && (long)B * P <= 65535);
   PS_REQUIRE(d_ld >= P && (suffix_sel == nullptr || sel_ld >= P));
@@ -362,7 +362,7 @@ ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
   PS_NN(d_cnt); PS_NN(d_prev); PS_NN(token); PS_NN(conf); PS_NN(commit);
   ps_status st = check_ws(commit_ws(B, P, V), ws, ws_bytes);
   if (st != PS_OK) return st;
-  CommitArgs a{logits, B, P, V, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
+  CommitArgs a{logits, dtype, B, P, V, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
                suffix_sel, sel_ld, params, token, conf, commit, ws};
   return launch_status(commit_run(a, static_cast<cudaStream_t>(stream)));
 }

@@ -8,7 +8,9 @@
 //
 //   k_commit_scan  one CTA per 16384-logit chunk of a row: chunk max, first
 //                  arg-max, sum exp(l - chunk max) (fp32 pairwise per thread,
-//                  fp64 across threads).  128-bit streaming loads.
+//                  fp64 across threads).  Streaming loads of fp32 or bf16
+//                  logits (bf16 values are exact in fp32, so both run the
+//                  same arithmetic on the same values).
 //   k_commit_rule  one CTA per sequence: merges the chunks in fp64
 //                  (c = 1 / sum), applies the rule, updates the state.
 #include <climits>
@@ -23,8 +25,22 @@ constexpr int kCT = 256;          // threads per scan CTA
 constexpr int kPer = 64;          // logits per thread
 constexpr int kChunk = kCT * kPer;
 
+// four consecutive logits from 16 (fp32) or 8 (bf16) aligned bytes,
+// streamed past the caches
+__device__ __forceinline__ float4 load4(const float* p) {
+  return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 w = __ldcs(reinterpret_cast<const uint2*>(p));
+  float4 x;
+  bf16x2_to_f32(w.x, x.x, x.y);
+  bf16x2_to_f32(w.y, x.z, x.w);
+  return x;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(kCT)
-k_commit_scan(const float* __restrict__ logits, int V, int nchunk,
+k_commit_scan(const T* __restrict__ logits, int V, int nchunk,
               float* __restrict__ pm, int* __restrict__ pidx,
               double* __restrict__ ps) {
   pdl_prologue();
@@ -34,14 +50,14 @@ k_commit_scan(const float* __restrict__ logits, int V, int nchunk,
   const long row = blockIdx.y;
   const int chunk = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const float* L = logits + row * V;
+  const T* L = logits + row * V;
   const int c0 = chunk * kChunk;
   float v[kPer];
 #pragma unroll
   for (int it = 0; it < kPer / 4; ++it) {
     const int e = c0 + (it * kCT + tid) * 4;
     float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (e < V) x = __ldcs(reinterpret_cast<const float4*>(L + e));
+    if (e < V) x = load4(L + e);
     v[it * 4 + 0] = x.x; v[it * 4 + 1] = x.y; v[it * 4 + 2] = x.z; v[it * 4 + 3] = x.w;
   }
   // chunk max and its first index (each thread scans its indices in order)
@@ -191,7 +207,12 @@ cudaError_t commit_run(const CommitArgs& a, cudaStream_t s) {
   float* pm = cv.take<float>(rows);
   int* pidx = cv.take<int>(rows);
   double* ps = cv.take<double>(rows);
-  launch_pdl(k_commit_scan, dim3(nc, a.B * a.P), kCT, 0, s, a.logits, a.V, nc, pm, pidx, ps);
+  if (a.dtype == PS_BF16)
+    launch_pdl(k_commit_scan<__nv_bfloat16>, dim3(nc, a.B * a.P), kCT, 0, s,
+               static_cast<const __nv_bfloat16*>(a.logits), a.V, nc, pm, pidx, ps);
+  else
+    launch_pdl(k_commit_scan<float>, dim3(nc, a.B * a.P), kCT, 0, s,
+               static_cast<const float*>(a.logits), a.V, nc, pm, pidx, ps);
   const int threads = ((a.P + 31) / 32) * 32;
   launch_pdl(k_commit_rule, a.B, threads, 0, s, a.P, nc, pm, pidx, ps, a.role, a.undecided,
                                         a.D, a.d_ld, a.d_sum, a.d_cnt, a.d_prev,

@@ -100,7 +100,7 @@ size_t refresh_ws(int B, int N, int d, int Hkv, int dh);
 cudaError_t refresh_run(const RefreshArgs& a, cudaStream_t s);
 
 struct CommitArgs {
-  const float* logits; int B, P, V; const uint8_t* role; uint8_t* undecided;
+  const void* logits; int dtype; int B, P, V; const uint8_t* role; uint8_t* undecided;
   const float* D; int d_ld; float* d_sum; int32_t* d_cnt; float* d_prev;
   const uint8_t* suffix_sel; int sel_ld; ps_commit_params p;
   int32_t* token; float* conf; uint8_t* commit; void* ws;

@@ -88,7 +88,7 @@ _SIGS = {
                            _sz, _p]),
     "ps_refresh_kv": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p,
                            _i, _i, _p, _sz, _p]),
-    "ps_commit": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _i, _p, _p, _p, _p, _i,
+    "ps_commit": (_i, [_p, _p, _i, _i, _i, _i, _p, _p, _p, _i, _p, _p, _p, _p, _i,
                        CommitParams, _p, _p, _p, _p, _sz, _p]),
 }
 
@@ -256,7 +256,7 @@ def ps_commit(logits, role, undecided, D_blk, d_ld, d_sum, d_cnt, d_prev,
     if not isinstance(params, CommitParams):
         params = CommitParams(*params)
     st = lib.cdll.ps_commit(
-        lib.handle(), _ptr(logits), B, P, V, _ptr(role), _ptr(undecided), _ptr(D_blk),
+        lib.handle(), _ptr(logits), _dtype(logits), B, P, V, _ptr(role), _ptr(undecided), _ptr(D_blk),
         d_ld, _ptr(d_sum), _ptr(d_cnt), _ptr(d_prev), _ptr(suffix_sel), sel_ld, params,
         _ptr(token), _ptr(conf), _ptr(commit), w, wn, _stream(stream))
     _check(st, "ps_commit")

@@ -300,7 +300,9 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
  * Then every undecided current token sets d_sum = fl32(d_sum + D),
  *   d_cnt += 1, d_prev = D; committed tokens get undecided = 0.
  *
- * logits [B][P][V] f32; role [P] u8; undecided [B][P] u8 in/out;
+ * logits [B][P][V] of `dtype` (PS_F32, or PS_BF16 as an LM head emits them:
+ *   bf16 values are exact in fp32, so both take the same decisions on the
+ *   same values); role [P] u8; undecided [B][P] u8 in/out;
  * D_blk: element (b, j) at D_blk[b*d_ld + j] (e.g. the last layer's D with
  *   d_ld = N, offset to the block); d_sum/d_prev [B][P] f32 in/out,
  *   d_cnt [B][P] i32 in/out; suffix_sel: element (b, j) at
@@ -315,7 +317,7 @@ typedef struct {
   int ensure_progress; /* 0 or 1 */
 } ps_commit_params;
 
-ps_status ps_commit(ps_handle h, const float* logits, int B, int P, int V,
+ps_status ps_commit(ps_handle h, const void* logits, int dtype, int B, int P, int V,
                     const uint8_t* role, uint8_t* undecided,
                     const float* D_blk, int d_ld, float* d_sum, int32_t* d_cnt,
                     float* d_prev, const uint8_t* suffix_sel, int sel_ld,

@@ -54,7 +54,7 @@ def test_null_handle_and_bad_args_rejected_on_host(cdll):
                                     None, None, None, None, None, 0, None) == ps.PS_ERR_ARG
     assert cdll.ps_topk_drift(None, None, None, None, 1, 8, 2, 1, None, None, None, None,
                               None, None, 0, None) == ps.PS_ERR_ARG
-    assert cdll.ps_commit(None, None, 1, 2, 8, None, None, None, 2, None, None, None,
+    assert cdll.ps_commit(None, None, 0, 1, 2, 8, None, None, None, 2, None, None, None,
                           None, 2, ps.CommitParams(0.9, 1, 0.1, 0, 1), None, None, None,
                           None, 0, None) == ps.PS_ERR_ARG
     h = ctypes.c_void_p()

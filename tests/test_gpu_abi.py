@@ -73,7 +73,7 @@ def test_topk_and_commit_reject_bad_k_and_mode(lib):
     f = torch.zeros(1, 2, device="cuda")
     i32 = torch.zeros(1, 2, dtype=torch.int32, device="cuda")
     bad = ps.CommitParams(0.9, 1.0, 0.1, 3, 1)
-    assert cd.ps_commit(h, L.data_ptr(), 1, 2, 8, u8.data_ptr(), u8.data_ptr(), f.data_ptr(),
+    assert cd.ps_commit(h, L.data_ptr(), 0, 1, 2, 8, u8.data_ptr(), u8.data_ptr(), f.data_ptr(),
                         2, f.data_ptr(), i32.data_ptr(), f.data_ptr(), None, 2, bad,
                         i32.data_ptr(), f.data_ptr(), u8.data_ptr(), None, 0,
                         s) == ps.PS_ERR_ARG                          # unknown mode

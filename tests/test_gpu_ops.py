@@ -596,6 +596,31 @@ def test_commit(widx, mode, suffix):
     assert unpinned <= 1
 
 
+@pytest.mark.parametrize("widx,V", [(1, None), (0, 16384 * 2 + 12)])
+def test_commit_bf16_logits(widx, V):
+    """bf16 logits (as an LM head emits them): the oracle's decisions on the
+    bf16 values, and outputs bit-identical to the fp32 path on the same
+    (bf16-representable) values; V with a ragged last chunk included."""
+    w, logits, role, und, D, s, cnt, prev, ssel, p = _commit_case(widx, 0, True, seed=3)
+    if V is not None:
+        logits = wl.make_logits(w, 0, "cuda", V=V)
+    Lb = logits.to(torch.bfloat16)
+    dev = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    args = (dev(role), dev(und), dev(D), w.P, dev(s), dev(cnt), dev(prev), dev(ssel),
+            ps.CommitParams(p.tau_s, p.alpha, p.ratio, p.mode, p.ensure_progress))
+    g = run_commit(Lb, *args)
+    g32 = run_commit(Lb.float(), *args)
+    for k in g:
+        assert np.array_equal(g[k], g32[k]), k
+    Ln = np_(Lb)
+    for b in range(Ln.shape[0]):
+        o = oracle.commit_rule(Ln[b], role, und[b], D[b], s[b], cnt[b], prev[b], ssel[b], p)
+        assert np.array_equal(g["token"][b], o["token"])
+        assert_close(g["conf"][b], o["conf"], rtol=CONF_RTOL, atol=0, what="conf")
+        if not (o["margin"] <= BAND).any():
+            assert np.array_equal(g["commit"][b], o["commit"])
+
+
 def test_commit_uniform_and_onehot_closed_forms():
     V = 4096
     L = torch.zeros(1, 2, V, device="cuda")
