@@ -371,8 +371,9 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
             ev.record(stream)
             marks[-1][1] = ev
 
-    def run(n):
-        return pipe.decode(ps.Schedule(tau_upd, full_period, w.P), inputs, n, on_step=on_step)
+    def run(n, graphs=False):
+        return pipe.decode(ps.Schedule(tau_upd, full_period, w.P), inputs, n, on_step=on_step,
+                           graphs=graphs)
 
     run(warm)
     torch.cuda.synchronize()
@@ -382,6 +383,15 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ntok = tokens[0]
+    # the same loop through CUDA graphs (captured during the warm-up run)
+    run(warm + 16, graphs=True)
+    torch.cuda.synchronize()
+    tokens[0] = 0
+    t0 = time.perf_counter()
+    acts_g = run(steps, graphs=True)
+    torch.cuda.synchronize()
+    wall_g = time.perf_counter() - t0
+    ntok_g = tokens[0]
     timing[0] = True
     acts_t = run(steps)
     torch.cuda.synchronize()
@@ -408,15 +418,18 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
         by[key] = (n + 1, tot + ms)
     return {"tau_upd": tau_upd, "full_period": full_period, "steps": steps,
             "wall_ms_per_step": wall * 1e3 / steps, "tokens_per_s": ntok / wall,
-            "tokens": ntok, "refresh_frac": sum(bool(a & 1) for a in acts) / steps,
+            "tokens": ntok, "graph_wall_ms_per_step": wall_g * 1e3 / steps,
+            "graph_tokens_per_s": ntok_g / wall_g,
+            "graph_refresh_frac": sum(bool(a & 1) for a in acts_g) / steps, "refresh_frac": sum(bool(a & 1) for a in acts) / steps,
             "full_frac": sum(bool(a & 2) and not a & 8 for a in acts) / steps,
             "reinit_frac": sum(bool(a & 8) for a in acts) / steps,
             "device_ms_by_step_kind": {k: (statistics.mean(v) if v else None)
                                        for k, v in kinds.items()},
             "reinit_step_kernels": {k: {"launches": n, "us": round(t * 1e3, 1)}
                                     for k, (n, t) in sorted(by.items(), key=lambda x: -x[1][1])},
-            "timing": "wall: eager loop with one host read per step; device: CUDA events "
-                      "around each step, enqueued ahead behind a device-side spin"}
+            "timing": "wall: eager loop (graph_*: the loop through CUDA graphs) with one host "
+                      "read per step; device: CUDA events around each eager step, enqueued "
+                      "ahead behind a device-side spin"}
 
 
 def measure_ablation(w, L, Hs, Qs, logits, u, dev, steps=3, reps=50):

@@ -92,6 +92,8 @@ class Pipeline:
         self.all_pos = torch.arange(N, dtype=torch.int32, device=device).repeat(B, 1)
         self.all_npos = torch.full((B,), N, dtype=torch.int32, device=device)
         self._flags = None
+        self._gin = None
+        self._graphs = {}
         self.undecided = torch.ones(B, P, dtype=torch.uint8, device=device)
         self.d_sum = torch.zeros(B, P, dtype=torch.float32, device=device)
         self.d_cnt = torch.zeros(B, P, dtype=torch.int32, device=device)
@@ -243,19 +245,64 @@ class Pipeline:
         main.synchronize()
         return int(self._flags[0]), not bool(self._flags[1])
 
-    def decode(self, schedule, inputs, steps, stream=None, on_step=None):
+    def graph_step(self, act, Hs, Qs, Wks, Wvs, logits, init_us=None, stream=None):
+        """decode_step through CUDA graphs: the step's inputs are copied into
+        fixed buffers, and the graph of (act, distribution parity) is
+        captured on first use and replayed -- the same kernels in the same
+        order as decode_step, without the host launching them one by one.
+        The weights are captured by address and must not move between
+        steps."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self._gin is None:
+            self._gin = dict(H=[h.clone() for h in Hs], Q=[q.clone() for q in Qs],
+                             logits=logits.clone(),
+                             u=None if init_us is None else [u.clone() for u in init_us],
+                             W=[(wk.data_ptr(), wv.data_ptr()) for wk, wv in zip(Wks, Wvs)])
+            self._graphs = {}
+        g = self._gin
+        if [(wk.data_ptr(), wv.data_ptr()) for wk, wv in zip(Wks, Wvs)] != g["W"]:
+            raise ValueError("graph mode: the weights must stay at the same addresses")
+        with torch.cuda.stream(main):
+            for dst, src in zip(g["H"], Hs):
+                dst.copy_(src, non_blocking=True)
+            for dst, src in zip(g["Q"], Qs):
+                dst.copy_(src, non_blocking=True)
+            g["logits"].copy_(logits, non_blocking=True)
+            if act & ps.SCHED_REINIT:
+                for dst, src in zip(g["u"], init_us):
+                    dst.copy_(src, non_blocking=True)
+        key = (act, self.t % 2)
+        if key not in self._graphs:
+            t0 = self.t
+            graph = torch.cuda.CUDAGraph()
+            main.synchronize()
+            with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+                self.decode_step(act, g["H"], g["Q"], Wks, Wvs, g["logits"], g["u"])
+            self.t = t0  # capturing ran no kernel: the step happens at the replay
+            self._graphs[key] = graph
+            main.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(main):
+            self._graphs[key].replay()
+        if act & ps.SCHED_REFRESH:
+            self.t += 1
+
+    def decode(self, schedule, inputs, steps, stream=None, on_step=None, graphs=False):
         """Run `steps` decode steps under `schedule` (a ps.Schedule).
 
         inputs(t, block_start) returns (Hs, Qs, Wks, Wvs, logits, init_us) of
         step t, block_start being the schedule's current block; the first
         step builds the window (k-means++, full refresh).  on_step(t, act) is
-        called after each step's work is enqueued.  Returns the actions
-        taken, one per step."""
+        called after each step's work is enqueued.  graphs: run the steps
+        through graph_step (the first step, which initialises the library's
+        kernels, eagerly).  Returns the actions taken, one per step."""
         acts = []
         act = ps.SCHED_REFRESH | ps.SCHED_FULL | ps.SCHED_REINIT
         for t in range(steps):
             Hs, Qs, Wks, Wvs, logits, init_us = inputs(t, schedule.state.block_start)
-            self.decode_step(act, Hs, Qs, Wks, Wvs, logits, init_us, stream)
+            if graphs and t > 0:
+                self.graph_step(act, Hs, Qs, Wks, Wvs, logits, init_us, stream)
+            else:
+                self.decode_step(act, Hs, Qs, Wks, Wvs, logits, init_us, stream)
             acts.append(act)
             if on_step is not None:
                 on_step(t, act)

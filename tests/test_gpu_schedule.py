@@ -213,3 +213,45 @@ def test_full_step_refreshes_every_row_of_an_offloaded_layer():
     touched[np_(st.pos[0])[: int(np_(st.npos)[0])]] = True
     assert 0 < touched.sum() < w.N
     assert np.array_equal(K2[~touched], K1[~touched])
+
+
+@pytest.mark.parametrize("widx,steps", [(0, 20), (1, 12)])
+def test_graph_decode_matches_eager(widx, steps):
+    """The decode loop through CUDA graphs (one per action kind and
+    distribution parity, captured on first use) gives the eager loop's
+    actions and every output bit for bit: the same kernels in the same order."""
+    w = wl.WORKLOADS[widx]
+    layers = min(2, w.layers) if widx == 0 else 1
+    cache = {}
+
+    def inputs(t, block_start):
+        widx_ = block_start // w.P
+        Hs, Qs, Wks, Wvs, us = [], [], [], [], []
+        for l in range(layers):
+            if (l, widx_) not in cache:
+                cache[(l, widx_)] = (wl.make_layer(w, l + 10 * widx_, "cuda"),
+                                     wl.make_uniforms(w, l + 10 * widx_, "cuda"))
+            L, u = cache[(l, widx_)]
+            H = wl.drift_rows(w, L["H"], t + 1, l)
+            Hs.append(H)
+            Qs.append(wl.make_queries(w, H, L["Wq"]))
+            us.append(u)
+        Ws = [cache[(l, 0)][0] for l in range(layers)]    # one set of weights for every window
+        logits = wl.make_logits(w, t, "cuda").to(wl.torch_dtype(w))
+        return Hs, Qs, [x["Wk"] for x in Ws], [x["Wv"] for x in Ws], logits, us
+
+    outs = []
+    for graphs in (False, True):
+        pipe = Pipeline(w, layers=layers)
+        pipe.params = ps.CommitParams(TAU_S, w.alpha, w.ratio, w.mode, 1)
+        acts = pipe.decode(ps.Schedule(TAU_UPD, FULL_PERIOD, w.P), inputs, steps, graphs=graphs)
+        torch.cuda.synchronize()
+        ps.ps_check()
+        st = [(x.mu, x.assign, x.D, x.A[0], x.A[1], x.Kc, x.Vc, x.posmask) for x in pipe.state]
+        outs.append((acts, [t.clone() for layer in st for t in layer],
+                     [t.clone() for t in (pipe.undecided, pipe.d_sum, pipe.d_cnt, pipe.token)]))
+    (a0, s0, c0), (a1, s1, c1) = outs
+    assert a0 == a1
+    assert len(set(a0)) >= 3                                  # several kinds of step replayed
+    for x, y in zip(s0 + c0, s1 + c1):
+        assert torch.equal(x, y)
