@@ -8,9 +8,9 @@
 //
 //   k_commit_scan  one CTA per 16384-logit chunk of a row: chunk max, first
 //                  arg-max, sum exp(l - chunk max) (fp32 pairwise per thread,
-//                  fp64 across threads).  Streaming loads of fp32 or bf16
-//                  logits (bf16 values are exact in fp32, so both run the
-//                  same arithmetic on the same values).
+//                  fp64 across threads).  Streaming loads of fp32 logits,
+//                  or of bf16 ones (exact in fp32; 8 a load where V % 8 == 0,
+//                  which groups the per-thread partial sums differently).
 //   k_commit_rule  one CTA per sequence: merges the chunks in fp64
 //                  (c = 1 / sum), applies the rule, updates the state.
 #include <climits>
@@ -25,20 +25,29 @@ constexpr int kCT = 256;          // threads per scan CTA
 constexpr int kPer = 64;          // logits per thread
 constexpr int kChunk = kCT * kPer;
 
-// four consecutive logits from 16 (fp32) or 8 (bf16) aligned bytes,
-// streamed past the caches
-__device__ __forceinline__ float4 load4(const float* p) {
-  return __ldcs(reinterpret_cast<const float4*>(p));
+// W consecutive logits from W * sizeof(T) aligned bytes (16 bytes, or 8 for
+// four bf16 when rows are only 8-byte aligned), streamed past the caches
+__device__ __forceinline__ void loadw(const float* p, float* x) {
+  const float4 w = __ldcs(reinterpret_cast<const float4*>(p));
+  x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
 }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-  const uint2 w = __ldcs(reinterpret_cast<const uint2*>(p));
-  float4 x;
-  bf16x2_to_f32(w.x, x.x, x.y);
-  bf16x2_to_f32(w.y, x.z, x.w);
-  return x;
+__device__ __forceinline__ void loadw(const __nv_bfloat16* p, float* x, int w_elems) {
+  if (w_elems == 8) {
+    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(p));
+    bf16x2_to_f32(w.x, x[0], x[1]);
+    bf16x2_to_f32(w.y, x[2], x[3]);
+    bf16x2_to_f32(w.z, x[4], x[5]);
+    bf16x2_to_f32(w.w, x[6], x[7]);
+  } else {
+    const uint2 w = __ldcs(reinterpret_cast<const uint2*>(p));
+    bf16x2_to_f32(w.x, x[0], x[1]);
+    bf16x2_to_f32(w.y, x[2], x[3]);
+  }
 }
+__device__ __forceinline__ void loadw(const float* p, float* x, int) { loadw(p, x); }
 
-template <typename T>
+// W logits per load: 4 (fp32; bf16 with V % 8 != 0) or 8 (bf16, V % 8 == 0)
+template <typename T, int W>
 __global__ void __launch_bounds__(kCT)
 k_commit_scan(const T* __restrict__ logits, int V, int nchunk,
               float* __restrict__ pm, int* __restrict__ pidx,
@@ -54,20 +63,20 @@ k_commit_scan(const T* __restrict__ logits, int V, int nchunk,
   const int c0 = chunk * kChunk;
   float v[kPer];
 #pragma unroll
-  for (int it = 0; it < kPer / 4; ++it) {
-    const int e = c0 + (it * kCT + tid) * 4;
-    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (e < V) x = load4(L + e);
-    v[it * 4 + 0] = x.x; v[it * 4 + 1] = x.y; v[it * 4 + 2] = x.z; v[it * 4 + 3] = x.w;
+  for (int it = 0; it < kPer / W; ++it) {
+    const int e = c0 + (it * kCT + tid) * W;
+#pragma unroll
+    for (int q = 0; q < W; ++q) v[it * W + q] = -INFINITY;
+    if (e < V) loadw(L + e, v + it * W, W);  // V % W == 0: the group is whole
   }
   // chunk max and its first index (each thread scans its indices in order)
   float m = -INFINITY;
   int mi = INT_MAX;
 #pragma unroll
-  for (int it = 0; it < kPer / 4; ++it)
+  for (int it = 0; it < kPer / W; ++it)
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (v[it * 4 + q] > m) { m = v[it * 4 + q]; mi = c0 + (it * kCT + tid) * 4 + q; }
+    for (int q = 0; q < W; ++q)
+      if (v[it * W + q] > m) { m = v[it * W + q]; mi = c0 + (it * kCT + tid) * W + q; }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float om = __shfl_xor_sync(0xffffffffu, m, o);
@@ -207,12 +216,15 @@ cudaError_t commit_run(const CommitArgs& a, cudaStream_t s) {
   float* pm = cv.take<float>(rows);
   int* pidx = cv.take<int>(rows);
   double* ps = cv.take<double>(rows);
-  if (a.dtype == PS_BF16)
-    launch_pdl(k_commit_scan<__nv_bfloat16>, dim3(nc, a.B * a.P), kCT, 0, s,
-               static_cast<const __nv_bfloat16*>(a.logits), a.V, nc, pm, pidx, ps);
+  const dim3 grid(nc, a.B * a.P);
+  const auto* lb = static_cast<const __nv_bfloat16*>(a.logits);
+  if (a.dtype == PS_BF16 && a.V % 8 == 0)
+    launch_pdl(k_commit_scan<__nv_bfloat16, 8>, grid, kCT, 0, s, lb, a.V, nc, pm, pidx, ps);
+  else if (a.dtype == PS_BF16)
+    launch_pdl(k_commit_scan<__nv_bfloat16, 4>, grid, kCT, 0, s, lb, a.V, nc, pm, pidx, ps);
   else
-    launch_pdl(k_commit_scan<float>, dim3(nc, a.B * a.P), kCT, 0, s,
-               static_cast<const float*>(a.logits), a.V, nc, pm, pidx, ps);
+    launch_pdl(k_commit_scan<float, 4>, grid, kCT, 0, s, static_cast<const float*>(a.logits),
+               a.V, nc, pm, pidx, ps);
   const int threads = ((a.P + 31) / 32) * 32;
   launch_pdl(k_commit_rule, a.B, threads, 0, s, a.P, nc, pm, pidx, ps, a.role, a.undecided,
                                         a.D, a.d_ld, a.d_sum, a.d_cnt, a.d_prev,

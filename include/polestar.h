@@ -300,9 +300,11 @@ ps_status ps_refresh_kv(ps_handle h, const void* H, int dtype,
  * Then every undecided current token sets d_sum = fl32(d_sum + D),
  *   d_cnt += 1, d_prev = D; committed tokens get undecided = 0.
  *
- * logits [B][P][V] of `dtype` (PS_F32, or PS_BF16 as an LM head emits them:
- *   bf16 values are exact in fp32, so both take the same decisions on the
- *   same values); role [P] u8; undecided [B][P] u8 in/out;
+ * logits [B][P][V] of `dtype` (PS_F32, or PS_BF16 as an LM head emits them;
+ *   bf16 values are exact in fp32, and the bf16 scan differs from the fp32 one
+ *   only in how its fp32 partial sums are grouped, so on the same values the
+ *   tokens are equal and the confidences agree to rounding);
+ *   role [P] u8; undecided [B][P] u8 in/out;
  * D_blk: element (b, j) at D_blk[b*d_ld + j] (e.g. the last layer's D with
  *   d_ld = N, offset to the block); d_sum/d_prev [B][P] f32 in/out,
  *   d_cnt [B][P] i32 in/out; suffix_sel: element (b, j) at

@@ -599,8 +599,11 @@ def test_commit(widx, mode, suffix):
 @pytest.mark.parametrize("widx,V", [(1, None), (0, 16384 * 2 + 12)])
 def test_commit_bf16_logits(widx, V):
     """bf16 logits (as an LM head emits them): the oracle's decisions on the
-    bf16 values, and outputs bit-identical to the fp32 path on the same
-    (bf16-representable) values; V with a ragged last chunk included."""
+    bf16 values, and against the fp32 path on the same (bf16-representable)
+    values the same tokens and confidences within rounding (the bf16 scan
+    loads 8 logits a thread where V % 8 == 0, the fp32 one 4, so their fp32
+    partial sums group differently); V with a ragged last chunk (V % 8 = 4,
+    4-logit loads) included."""
     w, logits, role, und, D, s, cnt, prev, ssel, p = _commit_case(widx, 0, True, seed=3)
     if V is not None:
         logits = wl.make_logits(w, 0, "cuda", V=V)
@@ -610,8 +613,8 @@ def test_commit_bf16_logits(widx, V):
             ps.CommitParams(p.tau_s, p.alpha, p.ratio, p.mode, p.ensure_progress))
     g = run_commit(Lb, *args)
     g32 = run_commit(Lb.float(), *args)
-    for k in g:
-        assert np.array_equal(g[k], g32[k]), k
+    assert np.array_equal(g["token"], g32["token"])
+    assert_close(g["conf"], g32["conf"], rtol=CONF_RTOL, atol=0, what="conf vs fp32 path")
     Ln = np_(Lb)
     for b in range(Ln.shape[0]):
         o = oracle.commit_rule(Ln[b], role, und[b], D[b], s[b], cnt[b], prev[b], ssel[b], p)
@@ -619,6 +622,8 @@ def test_commit_bf16_logits(widx, V):
         assert_close(g["conf"][b], o["conf"], rtol=CONF_RTOL, atol=0, what="conf")
         if not (o["margin"] <= BAND).any():
             assert np.array_equal(g["commit"][b], o["commit"])
+            assert np.array_equal(g["undecided"][b], o["undecided"])
+            assert np.array_equal(g["d_sum"][b], o["d_sum"])
 
 
 def test_commit_uniform_and_onehot_closed_forms():
