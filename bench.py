@@ -49,8 +49,9 @@ def parse():
                     help="also time the step on a side stream against a synthetic main "
                          "forward (bf16 GEMMs of one layer over the window)")
     ap.add_argument("--decode", action="store_true",
-                    help="also time the decode loop under the refresh schedule "
-                         "(tau_upd 4, every 4th refresh full) and report it under 'decode'")
+                    help="also time the decode loop under the refresh schedule and report it "
+                         "under 'decode' (one layer: tau_upd 4, every 4th refresh full; "
+                         "multi-layer workloads: every layer refreshed at every step)")
     ap.add_argument("--ablation", action="store_true",
                     help="also compare the drift signals (KL, cosine, entropy) on the "
                          "workload's planted drift and time the scoring pass")
@@ -334,7 +335,8 @@ def measure_overlap(w, graphs, dev, reps=20):
             "hidden_fraction_drift_high_priority": (t_main + t_drift - t_both_hi) / t_drift}
 
 
-def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, full_period=4):
+def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, full_period=4,
+                   layers=1):
     """The decode loop under the refresh schedule, eager, on the workload's
     layer.  Wall pace: the host reads every step's outcome (tokens
     committed, block decided) to take the schedule's decision, as a decode
@@ -345,7 +347,7 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
     import torch
     from drift_aware_kv_spherical_gb300 import polestar as ps
     from drift_aware_kv_spherical_gb300.pipeline import Pipeline
-    pipe = Pipeline(w, layers=1, device=dev)
+    pipe = Pipeline(w, layers=layers, device=dev)
     stream = torch.cuda.current_stream(dev)
     marks, tokens, timing = [], [0], [False]
     plain = pipe.block_progress
@@ -358,12 +360,14 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
     pipe.block_progress = progress
 
     def inputs(t, block_start):
-        if timing[0]:
-            torch.cuda._sleep(2_000_000)
+        if timing[0]:  # long enough for the host to enqueue the whole step behind it
+            torch.cuda._sleep(2_000_000 * layers)
             ev = torch.cuda.Event(enable_timing=True)
             ev.record(stream)
             marks.append([ev, None])
-        return [Hs[t % 4]], [Qs[t % 4]], [L["Wk"]], [L["Wv"]], logits[t % 4], [u]
+        n = layers  # every layer takes the workload's layer (one set of weights)
+        return ([Hs[t % 4]] * n, [Qs[t % 4]] * n, [L["Wk"]] * n, [L["Wv"]] * n,
+                logits[t % 4], [u] * n)
 
     def on_step(t, act):
         if timing[0]:
@@ -405,7 +409,7 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
     timing[0] = False
     Hs0, Qs0, Wk0, Wv0, lg0, us0 = inputs(0, 0)
     ps.ps_trace_enable(True)
-    torch.cuda._sleep(20_000_000)      # the step's ~140 launches enqueued before it runs
+    torch.cuda._sleep(20_000_000 * layers)  # the step's launches enqueued before it runs
     pipe.decode_step(ps.SCHED_REFRESH | ps.SCHED_FULL | ps.SCHED_REINIT | ps.SCHED_SLIDE,
                      Hs0, Qs0, Wk0, Wv0, lg0, us0)
     torch.cuda.synchronize()
@@ -416,7 +420,8 @@ def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, fu
         key = kernel_key(name) or name[:40]
         n, tot = by.get(key, (0, 0.0))
         by[key] = (n + 1, tot + ms)
-    return {"tau_upd": tau_upd, "full_period": full_period, "steps": steps,
+    return {"layers": layers, "tau_upd": tau_upd, "full_period": full_period, "steps": steps,
+            "blocks_finished": sum(bool(a & 4) for a in acts),
             "wall_ms_per_step": wall * 1e3 / steps, "tokens_per_s": ntok / wall,
             "tokens": ntok, "graph_wall_ms_per_step": wall_g * 1e3 / steps,
             "graph_tokens_per_s": ntok_g / wall_g,
@@ -959,7 +964,11 @@ def main():
     if args.ablation:
         line["ablation"] = measure_ablation(w, L, Hs, Qs, logits, u, dev)
     if args.decode:
-        line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev)
+        if w.layers > 1:  # the multi-layer loop refreshes every layer at every step
+            line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev, steps=48, warm=4,
+                                            tau_upd=0, full_period=0, layers=w.layers)
+        else:
+            line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev)
     if args.offload:
         line["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
         line["offload"] = offload_rates(trace, ntrace, w, npos_seen[-1] / w.B)
