@@ -76,3 +76,39 @@ def test_native_schedule_rejects_bad_arguments():
     big = ps.ScheduleState(2 ** 31 - 2, 0, 0)
     assert f(ctypes.byref(ps.ScheduleParams(2 ** 31 - 1, 0, 8)), ctypes.byref(big), 5, 0) == \
         ps.SCHED_REFRESH                                               # saturates, then fires
+
+
+def _expected_refresh_steps(tau, counts):
+    """Steps (0-based, the step whose outcome triggers it) after which a
+    refresh is scheduled: the running token count reaches tau, then restarts."""
+    out, run = [], 0
+    for t, c in enumerate(counts):
+        run += c
+        if run >= tau:
+            out.append(t)
+            run = 0
+    return out
+
+
+@pytest.mark.parametrize("impl", ["oracle", "native"])
+def test_refreshes_follow_the_running_count(impl):
+    rng = random.Random(11)
+    if impl == "native":
+        from drift_aware_kv_spherical_gb300 import _build
+        from drift_aware_kv_spherical_gb300 import polestar as ps
+        if not os.path.exists(ps.LIB_PATH):
+            _build.build()
+    for _ in range(100):
+        tau, full = rng.randint(0, 9), rng.randint(0, 5)
+        counts = [rng.randint(0, 4) for _ in range(60)]
+        if impl == "oracle":
+            st = ScheduleState()
+            acts = [schedule_step(tau, full, 32, st, c, False) for c in counts]
+        else:
+            nat = ps.Schedule(tau, full, 32)
+            acts = [nat.step(c, False) for c in counts]
+        got = [t for t, a in enumerate(acts) if a & REFRESH]
+        assert got == _expected_refresh_steps(tau, counts)
+        fulls = [t for t, a in enumerate(acts) if a & FULL]
+        assert fulls == (got[full - 1::full] if full > 0 else [])
+        assert not any(a & (SLIDE | REINIT) for a in acts)
