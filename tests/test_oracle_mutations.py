@@ -172,3 +172,60 @@ def _reconstruct_nibbles_swapped(code_row, scale_row, S, mu_c, rho_i):
 def test_hot_path_pins_catch(monkeypatch, mod, name, mutant):
     monkeypatch.setattr(mod, name, mutant)
     assert _some_pin_fails(_pins(mod)), (mod.__name__, mutant.__name__)
+
+
+# ---- k-means and NVFP4
+from tests import test_oracle_kmeans as kmeans_pins   # noqa: E402
+from tests import test_oracle_nvfp4 as nvfp4_pins     # noqa: E402
+
+_E2M1_ALL = np.arange(16)
+
+
+def _e2m1_toward_zero(x):
+    """E2M1 rounding toward zero instead of to nearest-even."""
+    x = np.asarray(x, np.float32)
+    vals = oracle.e2m1_decode(_E2M1_ALL[:8]).astype(np.float64)       # 0 .. 6
+    mag = np.minimum(np.abs(x.astype(np.float64)), 6.0)
+    idx = np.searchsorted(vals, mag, side="right") - 1
+    return (idx | np.where(np.signbit(x), 8, 0)).astype(np.int64)
+
+
+def _residual_one_rounding(H, mu, assign, rho):
+    """r = fl(h - rho mu) with the product kept in fp64 (one rounding)."""
+    if mu is None:
+        return oracle.nvfp4_residual(H, mu, assign, rho)
+    H = np.asarray(H, np.float64)
+    t = np.asarray(rho, np.float64)[:, None] * np.asarray(mu, np.float64)[np.asarray(assign)]
+    R = (H - t).astype(np.float32)
+    codes, scales, S = oracle.nvfp4_quantize(R)
+    return codes, scales, S, R
+
+
+def _kmeans_ties_high(H, mu0, iters, chat_in=None):
+    """Ties to the higher cluster index: the oracle run on reversed centroids."""
+    C = np.asarray(mu0).shape[0]
+    rev = np.asarray(mu0)[::-1]
+    o = oracle.kmeans_spherical(H, rev, iters, None if chat_in is None else chat_in[::-1])
+    o = dict(o)
+    o["assign"] = C - 1 - np.asarray(o["assign"])
+    for k in ("mu", "chat", "counts"):
+        o[k] = np.asarray(o[k])[::-1]
+    return o
+
+
+def _kmeanspp_first_pick_up(H, C, u, return_margin=False):
+    """The first centre one row later (ceil instead of floor)."""
+    u = np.array(u, np.float64)
+    u[0] = min(u[0] + 1.0 / np.asarray(H).shape[0], 1 - 1e-12)
+    return oracle.kmeanspp_init(H, C, u, return_margin)
+
+
+@pytest.mark.parametrize("mod,name,mutant", [
+    (nvfp4_pins, "e2m1_encode", _e2m1_toward_zero),
+    (nvfp4_pins, "nvfp4_residual", _residual_one_rounding),
+    (kmeans_pins, "kmeans_spherical", _kmeans_ties_high),
+    (kmeans_pins, "kmeanspp_init", _kmeanspp_first_pick_up),
+])
+def test_kmeans_and_nvfp4_pins_catch(monkeypatch, mod, name, mutant):
+    monkeypatch.setattr(mod, name, mutant)
+    assert _some_pin_fails(_pins(mod)), (mod.__name__, mutant.__name__)

@@ -107,5 +107,12 @@ def test_residual_is_two_fp32_roundings():
     _, _, _, R = nvfp4_residual(H, mu, np.array([0]), rho)
     t = np.float32(np.float32(1 / 3) * np.float32(0.5))
     assert np.array_equal(R[0], (H[0] - t).astype(np.float32))
+    # a product that fp32 must round: fl(fl(1/3) * fl(1.3)) = 0.43333333730697632, the exact
+    # product 0.43333333035310060; IEEE fp32 subtraction of the rounded product gives the
+    # values below, which a single rounding of h - rho mu would miss (0.0666666701436042...)
+    H2 = np.array([[0.5, 2.0] * 8], np.float32)
+    _, _, _, R2 = nvfp4_residual(H2, np.array([[1.3] * 16], np.float32), np.array([0]), rho)
+    assert R2[0, 0] == np.float32(0.06666666269302368)
+    assert R2[0, 1] == np.float32(1.566666603088379)
     _, _, _, R0 = nvfp4_residual(H, None, None, None)
     assert np.array_equal(R0, H)
