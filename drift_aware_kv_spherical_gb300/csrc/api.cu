@@ -389,8 +389,16 @@ extern "C" ps_status ps_nvfp4_residual_noalloc(
     C = 1;
   }
   if (!nvfp4_static_fits(B, N, d)) return PS_ERR_WORKSPACE;
+  // the array's address is per device: the kernels must run on the device
+  // whose address is used, so the caller's current device must be the
+  // handle's
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return launch_status(e);
+  if (cur != h->device) return PS_ERR_ARG;
   float* scratch = nullptr;
-  if (nvfp4_static_scratch(h->device, &scratch) != cudaSuccess) return PS_ERR_CUDA;
+  e = nvfp4_static_scratch(h->device, &scratch);
+  if (e != cudaSuccess) return launch_status(e);
   Nvfp4Args a{H, dtype, mu, assign, rho, B, N, d, C, codes, scales, tensor_scale,
               scratch, h->num_sms};
   return launch_status(nvfp4_run(a, static_cast<cudaStream_t>(stream)));

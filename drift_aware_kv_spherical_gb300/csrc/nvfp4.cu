@@ -217,10 +217,11 @@ bool nvfp4_static_fits(int B, int N, int d) {
   return (long)B * grid_x(B, N, d) <= kStaticParts;
 }
 
-// Looks the array's device address up once per device (with that device
-// current, restoring the caller's current device afterwards).  The first
-// call on a device therefore makes runtime calls that must not happen inside
-// a stream capture.
+// Looks the array's device address up once per device; the caller has made
+// `device` current (the entry point checks this).  The first call on a device
+// therefore makes a runtime call that must not happen inside a stream
+// capture.  The cached address belongs to the device's current context: the
+// library must not be used across a reset of that device.
 cudaError_t nvfp4_static_scratch(int device, float** out) {
   std::lock_guard<std::mutex> lock(g_static_mu);
   auto it = g_static_ptr.find(device);
@@ -228,16 +229,8 @@ cudaError_t nvfp4_static_scratch(int device, float** out) {
     *out = it->second;
     return cudaSuccess;
   }
-  int prev = -1;
-  cudaError_t e = cudaGetDevice(&prev);
-  if (e != cudaSuccess) return e;
-  if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
   float* p = nullptr;
-  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_nvfp4_static_parts);
-  if (prev != device) {
-    cudaError_t e2 = cudaSetDevice(prev);
-    if (e == cudaSuccess) e = e2;
-  }
+  const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_nvfp4_static_parts);
   if (e != cudaSuccess) return e;
   g_static_ptr[device] = p;
   *out = p;

@@ -343,9 +343,13 @@ ps_status ps_commit(ps_handle h, const void* logits, int dtype, int B, int P, in
  *
  * Limit: B <= 16384 (the array holds at most max(608, B) partials);
  * larger B returns PS_ERR_WORKSPACE and launches nothing.
+ * Device: the handle's device must be the calling thread's current device
+ * (PS_ERR_ARG otherwise), since the array's address differs per device.
  * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device made current, then the caller's
- * current device restored); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture.  The kept address belongs to the device's context, so the
+ * library must not be used across a reset of that device (cudaDeviceReset).
+ * A failed look-up returns PS_ERR_CUDA with ps_last_cuda_error() set.
  * Sharing: every call on a device uses the same array and leaves the last
  * call's values in it.  Nothing in it has to start at zero (each call writes
  * every slot it later reads), but calls that overlap on the GPU -- on

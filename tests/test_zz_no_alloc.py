@@ -52,3 +52,28 @@ def test_noalloc_rejects_batches_beyond_its_array(lib):
     with pytest.raises(ps.PolestarError) as e:
         ps.ps_nvfp4_residual_noalloc(H, None, None, None, codes, scales, S)
     assert e.value.status == ps.PS_ERR_WORKSPACE
+
+
+def test_noalloc_at_its_largest_batch_matches_and_allocates_nothing(lib):
+    # B = 16384 is the documented maximum: the array's every slot is in use
+    g = torch.Generator(device="cuda").manual_seed(13)
+    B, N, d, C = 16384, 1, 16, 3
+    H = (torch.randn(B, N, d, device="cuda", generator=g) * 3).to(torch.bfloat16)
+    mu = torch.randn(B, C, d, device="cuda", generator=g)
+    mu = mu / mu.norm(dim=2, keepdim=True)
+    assign = torch.randint(0, C, (B, N), device="cuda", generator=g, dtype=torch.int32)
+    rho = torch.randn(B, N, device="cuda", generator=g)
+    ref = _outputs(H)
+    ws = ps.workspace(ps.OP_NVFP4, B=B, N=N, d=d)
+    ps.ps_nvfp4_residual(H, mu, assign, rho, *ref, ws=ws)
+    got = _outputs(H)
+    ps.ps_nvfp4_residual_noalloc(H, mu, assign, rho, *got)     # warm: set-up done
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(2):
+        ps.ps_nvfp4_residual_noalloc(H, mu, assign, rho, *got)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    ps.ps_check()
+    for r, q in zip(ref, got):
+        assert torch.equal(r, q)
