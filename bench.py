@@ -1,19 +1,23 @@
 """Benchmark of the drift-scoring / sparse-refresh step through libpolestar.
 
-A step is one pass of the whole path over one batch of synthetic input:
-spherical k-means (10 warm-started iterations), NVFP4 residuals, centroid
-keys + proxy attention + KL drift, top-k drifting clusters, sparse K/V
-refresh, and the commit over the current block.  Default workload: one
-LLaDA-8B-shaped layer (batch 1, window 1024, d 4096, 32 heads x 128, C 64,
-k 8, commit over 32 x 126464 logits).
+A step is one pass of the whole path over one batch of synthetic input: for
+every layer, spherical k-means (warm-started), NVFP4 residuals, centroid keys
++ proxy attention + KL drift, top-k drifting clusters and the sparse K/V
+refresh; then the commit over the current block.  Default workload: the
+32-layer stress configuration (batch 32, window 4096, d 4096, 32 heads x 128,
+C 256, 15 k-means iterations, top-k 16, commit over 64 x 126464 logits), each
+layer with its own window, queries, weights and state; the LLaDA-8B-shaped
+layer (batch 1, window 1024) follows under "extra".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl polestar|reference]
 
-Timing: device-side CUDA events on the launching stream, L2 flushed (512 MB
-write) between steps outside the timed events, W >= 3 warm-up steps; for N
+Timing: device-side CUDA events on the launching stream around a CUDA-graph
+replay of the whole step; between steps the inputs drift in place and L2 is
+flushed (512 MB write), outside the timed events; W >= 3 warm-up steps; for N
 > 1 (torchrun) every rank runs an independent replica, the timed region is
 bracketed by barriers and the slowest rank's time counts.  `--impl
-reference` times the CPU oracle on the same workload (rank 0 only).
+reference` times the CPU oracle on one (window, layer) slice of the same
+workload per step and extrapolates to the whole step (rank 0 only).
 """
 
 import argparse
@@ -32,7 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "drift-refresh steps/s and window tokens/s; achieved HBM GB/s vs ~8 TB/s peak"
-DEFAULT_WORKLOAD = "llada8b_layer_n1024"
+DEFAULT_WORKLOAD = "stress_b32_n4096_l32"
+EXTRA_WORKLOAD = "llada8b_layer_n1024"
 L2_FLUSH_BYTES = 512 << 20
 COPY_STREAMS = 1        # end-to-end leg: copy streams (2 and 4 measured 6 % and 14 % slower)
 
@@ -44,10 +49,15 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per step (0: the workload's own, 32 for the 32-layer ones)")
+    ap.add_argument("--extra", default=EXTRA_WORKLOAD,
+                    help="a second workload measured after the first and reported under "
+                         "'extra' ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--overlap", action="store_true",
-                    help="also time the step on a side stream against a synthetic main "
-                         "forward (bf16 GEMMs of one layer over the window)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="skip the latency-hiding measurement (the drift step of one layer on "
+                         "a side stream behind a synthetic main forward)")
     ap.add_argument("--decode", action="store_true",
                     help="also time the decode loop under the refresh schedule and report it "
                          "under 'decode' (one layer: tau_upd 4, every 4th refresh full; "
@@ -254,15 +264,19 @@ def kernel_work(key, w, npos_mean):
     }.get(key)
 
 
-def measure_overlap(w, graphs, dev, reps=20):
+def measure_overlap(w, dev, reps=20):
     """Latency hiding (the pages overlap the drift work with the main forward
-    on CUDA streams): the captured drift step on one stream against a
-    synthetic main forward on another, a captured graph of bf16 GEMMs shaped
-    like one transformer layer over the window (x W_qkv, W_o, a gated MLP of
-    width 3.5 d: W_up to 2 widths, W_down back; activations left out).
-    hidden = (t_main + t_drift - t_both) / t_drift, the share of the drift
-    step's time the overlap hides."""
+    on CUDA streams), through Pipeline.step_overlapped on one layer: the
+    main stream runs a synthetic forward of one transformer layer over the
+    window (bf16 GEMMs: x W_qkv, W_o, a gated MLP of width 3.5 d: W_up to 2
+    widths, W_down back; activations left out) and the layer's drift work
+    forks onto a drift stream behind it.  Each arrangement is captured as a
+    CUDA graph: the forward alone, the drift step alone, both through
+    step_overlapped.  hidden = (t_main + t_drift - t_both) / t_drift, the
+    share of the drift step's time the overlap hides."""
     import torch
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+    from drift_aware_kv_spherical_gb300 import workloads as wl
     M, d = w.B * w.N, w.d
     ff = int(3.5 * d) // 256 * 256
     g = torch.Generator(device=dev)
@@ -272,67 +286,69 @@ def measure_overlap(w, graphs, dev, reps=20):
         return (torch.randn(*shape, generator=g, device=dev) * 0.02).to(torch.bfloat16)
 
     X, Wqkv, Wo, Wup, Wdown = rnd(M, d), rnd(d, 3 * d), rnd(d, d), rnd(d, 2 * ff), rnd(ff, d)
+    L = wl.make_layer(w, 0, dev)
+    H, Wq, Wk, Wv = L["H"], L["Wq"], L["Wk"], L["Wv"]
+    del L
+    Q = wl.make_queries(w, H, Wq)
+    u = wl.make_uniforms(w, 0, dev)
+    logits = wl.make_logits(w, 0, dev).to(wl.torch_dtype(w))
+    pipe = Pipeline(w, layers=1, device=dev)
+    pipe.step([H], [Q], [Wk], [Wv], logits, init_us=[u], first=True)
     sm, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    hi = torch.cuda.Stream(dev, priority=-1)  # the drift step ahead of pending GEMM blocks
 
-    def forward():
-        qkv = X @ Wqkv
-        o = qkv[:, :d] @ Wo
-        up = o @ Wup
-        return up[:, :ff] @ Wdown
+    def forward(l, s):
+        if l > 0:  # the LM head's logits are an input of this measurement
+            return
+        with torch.cuda.stream(s):
+            qkv = X @ Wqkv
+            o = qkv[:, :d] @ Wo
+            up = o @ Wup
+            up[:, :ff] @ Wdown
 
-    with torch.cuda.stream(sm):
-        for _ in range(3):
-            forward()
-    torch.cuda.synchronize()
-    gm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gm, stream=sm):
-        forward()
+    def capture(fn):
+        torch.cuda.synchronize()
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=sm):
+            fn()
+        return graph
+
+    def drift_only():
+        sd.wait_stream(sm)
+        pipe.step([H], [Q], [Wk], [Wv], logits, stream=sd)
+        sm.wait_stream(sd)
+
+    def both():
+        pipe.step_overlapped([H], [Q], [Wk], [Wv], logits, sm, sd, forward=forward)
+
+    gm = capture(lambda: forward(0, sm))
+    gd = capture(drift_only)
+    gb = capture(both)
     flops = 2.0 * M * d * (3 * d + d + 2 * ff + ff)
 
-    def timed(run):
-        cur = torch.cuda.current_stream(dev)
-        for i in range(3):
-            run(i, cur)
+    def timed(graph):
+        for _ in range(3):
+            graph.replay()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
         a.record(cur)
-        for i in range(reps):
-            run(i, cur)
+        for _ in range(reps):
+            graph.replay()
         b.record(cur)
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / reps
 
-    def on(stream, graph, cur):
-        stream.wait_stream(cur)
-        with torch.cuda.stream(stream):
-            graph.replay()
-        cur.wait_stream(stream)
-
-    t_main = timed(lambda i, cur: on(sm, gm, cur))
-    t_drift = timed(lambda i, cur: on(sd, graphs[i % 2], cur))
-
-    def both(ds):
-        def run(i, cur):
-            sm.wait_stream(cur)
-            ds.wait_stream(cur)
-            with torch.cuda.stream(sm):
-                gm.replay()
-            with torch.cuda.stream(ds):
-                graphs[i % 2].replay()
-            cur.wait_stream(sm)
-            cur.wait_stream(ds)
-        return run
-
-    t_both = timed(both(sd))
-    t_both_hi = timed(both(hi))
-    return {"main_forward": f"bf16 GEMMs of one layer over {M} rows (d {d}, MLP {ff}), "
+    t_main, t_drift, t_both = timed(gm), timed(gd), timed(gb)
+    return {"api": "Pipeline.step_overlapped (main stream: the forward; drift stream: "
+                   "clustering, quantisation, proxy attention, top-k, refresh, commit)",
+            "main_forward": f"bf16 GEMMs of one layer over {M} rows (d {d}, MLP {ff}), "
                             f"{flops / 1e12:.2f} TFLOP, captured graph",
             "main_us": t_main, "drift_us": t_drift, "both_us": t_both,
             "main_tflops": flops / (t_main * 1e-6) / 1e12,
-            "hidden_fraction": (t_main + t_drift - t_both) / t_drift,
-            "both_us_drift_high_priority": t_both_hi,
-            "hidden_fraction_drift_high_priority": (t_main + t_drift - t_both_hi) / t_drift}
+            "hidden_fraction": (t_main + t_drift - t_both) / t_drift}
 
 
 def measure_decode(w, L, Hs, Qs, logits, u, dev, steps=64, warm=8, tau_upd=4, full_period=4,
@@ -529,68 +545,80 @@ def kernel_rooflines(records, nsteps, w, npos_mean, hbm, tf):
 
 
 def run_reference(args):
-    """The CPU oracle, as it stands, timed on this host on the same workload."""
+    """The CPU oracle, as it stands, on this host's cores: each step is one
+    (window, layer) slice of the workload -- a1-a6 on one window of one
+    layer, warm-started from its previous step -- and the commit of one
+    sequence; the whole-workload step is extrapolated linearly as B x layers
+    slices plus B commits (exact for one window of one layer)."""
     import numpy as np
     import oracle
     from drift_aware_kv_spherical_gb300 import workloads as wl
 
     w = wl.BY_NAME[args.workload]
-    L = wl.make_layer(w, 0, "cpu")
+    layers = getattr(args, "layers", 0) or w.layers
+    L = wl.make_layer(w, 0, "cpu", B=1)
     H0 = L["H"]
     Wk, Wv = L["Wk"].float().numpy(), L["Wv"].float().numpy()
     Hs = [H0]
     for t in range(1, 4):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
-    Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy() for H in Hs]
-    Hn = [H.float().numpy() for H in Hs]
+    Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy()[0] for H in Hs]
+    Hn = [H.float().numpy()[0] for H in Hs]
     # the LM head's output dtype (bf16 values, exact in the oracle's fp64)
-    logits = [wl.make_logits(w, t).to(wl.torch_dtype(w)).float().numpy() for t in range(4)]
-    u = wl.make_uniforms(w).numpy()
-    mu = [oracle.kmeanspp_init(Hn[0][b], w.C, u[b])[0] for b in range(w.B)]
-    A_prev = [None] * w.B
-    chat = [None] * w.B
-    st = dict(s=np.zeros((w.B, w.P), np.float32), n=np.zeros((w.B, w.P), np.int32),
-              p=np.zeros((w.B, w.P), np.float32), u=np.ones((w.B, w.P), np.uint8))
+    logits = [wl.make_logits(w, t, B=1).to(wl.torch_dtype(w)).float().numpy()[0]
+              for t in range(4)]
+    u = wl.make_uniforms(w, B=1).numpy()[0]
+    mu = oracle.kmeanspp_init(Hn[0], w.C, u)[0]
+    st = dict(mu=mu, chat=None, A=None, s=np.zeros(w.P, np.float32),
+              n=np.zeros(w.P, np.int32), p=np.zeros(w.P, np.float32),
+              u=np.ones(w.P, np.uint8))
     role = np.zeros(w.P, np.uint8)
     params = oracle.CommitParams(w.tau_s, w.alpha, w.ratio, w.mode, 1)
     Kc = np.zeros((w.N, w.Hkv * w.dh), np.float32)
 
     def step(t):
         i = t % 4
-        for b in range(w.B):
-            r = oracle.kmeans_spherical(Hn[i][b], mu[b], w.iters, chat[b])
-            mu[b], chat[b] = r["mu"], r["chat"]
-            oracle.nvfp4_residual(Hn[i][b], r["mu"].astype(np.float32), r["assign"],
-                                  r["rho"].astype(np.float32))
-            Kt = oracle.centroid_keys(r["chat"], Wk)
-            A, D = oracle.proxy_attn_kl(Qs[i][b], Kt, w.Hq, w.Hkv, w.dh, A_prev[b])
-            A_prev[b] = A
-            sel = oracle.topk_drift(D.astype(np.float32), r["assign"], r["counts"], w.k)
-            oracle.refresh_kv(Hn[i][b], sel[2], sel[3], Wk, Wv, Kc, Kc, 0, w.dtype == "bf16")
-            if b == w.B - 1:
-                pass
-            c = oracle.commit_rule(logits[i][b], role, st["u"][b],
-                                   D[w.blk_start:w.blk_start + w.P].astype(np.float32),
-                                   st["s"][b], st["n"][b], st["p"][b], None, params)
-            st["s"][b], st["n"][b], st["p"][b], st["u"][b] = (c["d_sum"], c["d_cnt"],
-                                                              c["d_prev"], c["undecided"])
+        t0 = time.perf_counter()
+        r = oracle.kmeans_spherical(Hn[i], st["mu"], w.iters, st["chat"])
+        st["mu"], st["chat"] = r["mu"], r["chat"]
+        oracle.nvfp4_residual(Hn[i], r["mu"].astype(np.float32), r["assign"],
+                              r["rho"].astype(np.float32))
+        Kt = oracle.centroid_keys(r["chat"], Wk)
+        A, D = oracle.proxy_attn_kl(Qs[i], Kt, w.Hq, w.Hkv, w.dh, st["A"])
+        st["A"] = A
+        sel = oracle.topk_drift(D.astype(np.float32), r["assign"], r["counts"], w.k)
+        oracle.refresh_kv(Hn[i], sel[2], sel[3], Wk, Wv, Kc, Kc, 0, w.dtype == "bf16")
+        t1 = time.perf_counter()
+        c = oracle.commit_rule(logits[i], role, st["u"],
+                               D[w.blk_start:w.blk_start + w.P].astype(np.float32),
+                               st["s"], st["n"], st["p"], None, params)
+        st["s"], st["n"], st["p"], st["u"] = c["d_sum"], c["d_cnt"], c["d_prev"], c["undecided"]
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
 
     for t in range(args.warmup):
         step(t)
-    t0 = time.perf_counter()
-    for t in range(args.steps):
-        step(args.warmup + t)
-    el = time.perf_counter() - t0
-    sps = args.steps / el
+    times = [step(args.warmup + t) for t in range(args.steps)]
+    t_slice = statistics.mean(a for a, _ in times)
+    t_commit = statistics.mean(b for _, b in times)
+    sec = w.B * layers * t_slice + w.B * t_commit
+    sps = 1.0 / sec
     cores = _blas_threads()
-    sample = f"full steps of {w.name} (B={w.B}, every stage, fp64 numpy)"
+    scale = w.B * layers
+    sample = (f"one (window, layer) slice of {w.name} per step: a1-a6 on one window of one "
+              f"layer ({t_slice * 1e3:.1f} ms) and a7 on one sequence ({t_commit * 1e3:.1f} ms), "
+              f"fp64 numpy; " +
+              ("exact: one window of one layer" if scale == 1 else
+               f"extrapolated linearly to the step's {w.B} x {layers} slices and {w.B} commits"))
     line = {"impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000 * el / args.steps, "higher_is_better": True,
+            "ms_per_step": 1000 * sec, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, layers),
+            "window_tokens_per_s": sps * w.B * w.N,
             "cpu_baseline": {"value": sps, "unit": "steps/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "extrapolated": scale > 1},
             "e2e": {"value": sps, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -605,31 +633,343 @@ def _blas_threads():
         return os.cpu_count() or 1
 
 
-def workload_config(w):
+def workload_config(w, layers=None):
+    layers = w.layers if layers is None else layers
     return {"workload": w.name, "B": w.B, "N": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "dh": w.dh, "C": w.C, "iters": w.iters, "k": w.k, "P": w.P, "V": w.V,
-            "layers": 1, "logits": w.dtype, "l2": "flushed between steps (512 MB write)"}
+            "layers": layers, "logits": w.dtype,
+            "weights": "per layer (seeded per layer)",
+            "l2": ("flushed between steps (512 MB write)" if layers == 1 else
+                   "inputs larger than L2 (every layer's window and queries are read each "
+                   "step); also flushed between steps (512 MB write)")}
 
 
-def cpu_baseline(w, budget_s=20.0):
-    """One or more full oracle steps of the workload on the host cores."""
-    ns = argparse.Namespace(steps=1, warmup=0, workload=w.name, gpus=1)
+def cpu_baseline(w, layers, budget_s=20.0):
+    """The oracle on one (window, layer) slice of the workload, extrapolated
+    to the whole step (run_reference), a few samples within the budget."""
     import io
     import contextlib
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        buf = io.StringIO()
-        with contextlib.redirect_stdout(buf):
-            run_reference(ns)
-        n += 1
-        if time.perf_counter() - t0 > budget_s / 4 or n >= 3:
-            break
+    samples = 3
+    ns = argparse.Namespace(steps=samples, warmup=0, workload=w.name, gpus=1, layers=layers)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        run_reference(ns)
     line = json.loads(buf.getvalue())
-    v = line["value"]
-    return {"value": v, "unit": "steps/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"one full step of {w.name} per sample, fp64 numpy (BLAS threads), "
-                      f"{n} sample(s)"}
+    cb = line["cpu_baseline"]
+    cb["sample"] += f", {samples} samples"
+    return cb
+
+
+def one_layer_inputs(w, dev):
+    """One layer's inputs for the optional one-layer measurements: the
+    layer, four steps of drifted hidden states and their queries, four sets
+    of logits, the k-means++ draws."""
+    from drift_aware_kv_spherical_gb300 import workloads as wl
+    L = wl.make_layer(w, 0, dev)
+    Hs = [L["H"]]
+    for t in range(1, 4):
+        Hs.append(wl.drift_rows(w, Hs[-1], t))
+    Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
+    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(4)]
+    return L, Hs, Qs, logits, wl.make_uniforms(w, 0, dev)
+
+
+def bench_workload(w, layers, args, dev, world, local, trace_steps=None):
+    """Every measurement of one workload: the device-timed step (CUDA-graph
+    replay, inputs resident), the per-op breakdown, the library trace, the
+    end-to-end run through the public API; returns the JSON line's fields."""
+    import torch
+    import torch.distributed as dist
+    from drift_aware_kv_spherical_gb300 import polestar as ps
+    from drift_aware_kv_spherical_gb300 import workloads as wl
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+
+    # every layer's own inputs in fixed device buffers (graph replay needs
+    # fixed addresses); between steps they drift in place, outside the timed
+    # events
+    ins = []
+    for l in range(layers):
+        L = wl.make_layer(w, l, dev)
+        Q = wl.make_queries(w, L["H"], L["Wq"])
+        ins.append(dict(H=L["H"], Q=Q, Wq=L["Wq"], Wk=L["Wk"], Wv=L["Wv"],
+                        u=wl.make_uniforms(w, l, dev)))
+        del L
+    torch.cuda.empty_cache()
+    Hs, Qs = [x["H"] for x in ins], [x["Q"] for x in ins]
+    Wks, Wvs, us = [x["Wk"] for x in ins], [x["Wv"] for x in ins], [x["u"] for x in ins]
+    # logits in the workload's dtype, as the model's LM head emits them
+    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(2)]
+    dL = torch.empty_like(logits[0])
+    pipe = Pipeline(w, layers=layers, device=dev, offload=args.offload)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step_no = 0
+
+    def advance():
+        """The next step's inputs: every layer drifts, new logits."""
+        nonlocal step_no
+        step_no += 1
+        for l in range(layers):
+            wl.drift_inplace(w, Hs[l], Qs[l], ins[l]["Wq"], step_no, l)
+        dL.copy_(logits[step_no % 2])
+
+    # window build: k-means++ seeding, first distributions
+    dL.copy_(logits[0])
+    pipe.step(Hs, Qs, Wks, Wvs, dL, init_us=us, first=True)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    ops = ["kmeans", "nvfp4", "proxy_kl", "topk", "refresh", "commit"]
+
+    def op_calls(parity, ev=None):
+        """One step, layer by layer, events between the ops (summed per op)."""
+        pipe.t = parity
+        for l in range(layers):
+            st = pipe.state[l]
+            cur, prev = st.A[parity], st.A[1 - parity]
+            rec = (lambda j: ev[l][j].record()) if ev is not None else (lambda j: None)
+            rec(0)
+            ps.ps_kmeans_spherical(Hs[l], st.mu, st.assign, st.rho, st.chat, st.counts,
+                                   w.iters, objective=st.obj, ws=pipe.ws[ps.OP_KMEANS])
+            rec(1)
+            ps.ps_nvfp4_residual(Hs[l], st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                                 ws=pipe.ws[ps.OP_NVFP4])
+            if pipe.offload:  # the store in host memory
+                ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store,
+                                          st.order, st.cl_off)
+            rec(2)
+            ps.ps_proxy_attn_kl(Qs[l], st.chat, Wks[l], prev, cur, st.D, w.Hkv,
+                                ws=pipe.ws[ps.OP_PROXY_KL])
+            rec(3)
+            ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
+                             st.npos, st.posmask)
+            rec(4)
+            src = Hs[l]
+            if pipe.offload:  # the selected clusters' rows from the host store
+                ps.ps_nvfp4_fetch_dequant(st.store, st.order, st.cl_off, st.sel, st.mu, st.rho,
+                                          st.S, st.Ht)
+                src = st.Ht
+            ps.ps_refresh_kv(src, st.pos, st.npos, Wks[l], Wvs[l], st.Kc, st.Vc, w.Hkv, w.dh,
+                             ws=pipe.ws[ps.OP_REFRESH])
+            rec(5)
+        if ev is not None:
+            ev[layers][0].record()
+        pipe.commit_step(dL)
+        if ev is not None:
+            ev[layers][1].record()
+
+    for t in range(args.warmup):                    # eager warm-up
+        advance()
+        op_calls(step_no % 2)
+    torch.cuda.synchronize()
+    ps.ps_check()
+
+    # one graph per A ping-pong parity: the pipeline's step with the ops off
+    # the critical path (NVFP4, commit) on side streams
+    def concurrent_step(parity):
+        pipe.t = parity          # A[parity] is this step's distribution
+        pipe.step(Hs, Qs, Wks, Wvs, dL, concurrent=True)
+
+    for t in range(2):           # side streams warmed up eagerly
+        advance()
+        concurrent_step(step_no % 2)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    for parity in (0, 1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            concurrent_step(parity)
+        graphs.append(g)
+    launches = graph_kernel_count(graphs[0])       # None if the runtime is unreachable
+    for t in range(args.warmup):                    # graph warm-up
+        advance()
+        graphs[step_no % 2].replay()
+    torch.cuda.synchronize()
+    ps.ps_check()
+
+    # timed region: K graph replays; the inputs drift and L2 is flushed
+    # between them, outside the timed events
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for t in range(args.steps):
+        advance()
+        flush.zero_()
+        gev[t][0].record(stream)
+        graphs[step_no % 2].replay()
+        gev[t][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ps.ps_check()
+    total_ms = world_max(sum(a.elapsed_time(b) for a, b in gev), dev)
+    ms_step = total_ms / args.steps
+    steps_per_s = aggregate_steps_per_s(world, args.steps, total_ms)
+    del graphs
+
+    # per-op breakdown: eager steps, events between the calls; a device-side
+    # spin before each step lets the host enqueue the whole step first, so
+    # the events time the kernels and not the host's launch pace
+    nops = min(args.steps, 3)
+    mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    events = [[mk(6) for _ in range(layers)] + [mk(2)] for _ in range(nops)]
+    for t in range(nops):
+        advance()
+        flush.zero_()
+        torch.cuda._sleep(4_000_000 * layers)
+        op_calls(step_no % 2, events[t])
+    torch.cuda.synchronize()
+    ps.ps_check()
+    npos_mean = float(torch.stack([st.npos.float().mean() for st in pipe.state]).mean())
+    per_op = {op: [sum(ev[l][j].elapsed_time(ev[l][j + 1]) for l in range(layers))
+                   for ev in events] for j, op in enumerate(ops[:5])}
+    per_op["commit"] = [ev[layers][0].elapsed_time(ev[layers][1]) for ev in events]
+    eager_ms = statistics.mean(ev[0][0].elapsed_time(ev[layers][1]) for ev in events)
+
+    # per kernel: the library's own trace (CUDA events around each of its
+    # launches, on the launching stream) over eager steps
+    ntrace = trace_steps or (3 if layers == 1 else 1)
+    ps.ps_trace_enable(True)
+    for t in range(ntrace):
+        advance()
+        flush.zero_()
+        torch.cuda._sleep(4_000_000 * layers)
+        op_calls(step_no % 2)
+    torch.cuda.synchronize()
+    trace = ps.ps_trace_records()
+    ps.ps_trace_enable(False)
+    ps.ps_check()
+    lib_launches = round(len(trace) / ntrace)       # every launch of its calls is traced
+
+    # end to end through the public API (the pipeline's layer and commit
+    # calls, eager): every step copies every layer's window and queries and
+    # the block's logits from pinned host memory and reads its results
+    # back.  Layer l's copy for a step runs on a copy stream as soon as the
+    # previous step's layer l has finished reading its buffers, so copies
+    # overlap the compute of the layers before; every copy and kernel lies
+    # inside the timed interval.
+    hH = [Hs[0].cpu().pin_memory(), None]
+    hQ = [Qs[0].cpu().pin_memory(), None]
+    wl.drift_inplace(w, Hs[0], Qs[0], ins[0]["Wq"], step_no + 1, 0)
+    hH[1], hQ[1] = Hs[0].cpu().pin_memory(), Qs[0].cpu().pin_memory()
+    hL = [x.cpu().pin_memory() for x in logits]
+    last = pipe.state[-1]
+    out = [torch.empty(pipe.token.shape, dtype=torch.int32).pin_memory(),
+           torch.empty(pipe.conf.shape).pin_memory(),
+           torch.empty(pipe.commit.shape, dtype=torch.uint8).pin_memory(),
+           torch.empty(last.D.shape).pin_memory()]
+    cs = torch.cuda.Stream(dev)
+    done = [None] * (layers + 1)
+
+    def e2e_run(n):
+        ev = torch.cuda.Event
+        t0 = ev(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            for l in range(layers):
+                cs.wait_event(done[l] if done[l] is not None else t0)
+                with torch.cuda.stream(cs):
+                    Hs[l].copy_(hH[(i + l) % 2], non_blocking=True)
+                    Qs[l].copy_(hQ[(i + l) % 2], non_blocking=True)
+                stream.wait_event(cs.record_event())
+                joins = []
+                pipe.layer_step(l, Hs[l], Qs[l], Wks[l], Wvs[l], stream=stream,
+                                concurrent=True, joins=joins)
+                for e in joins:
+                    stream.wait_event(e)
+                done[l] = stream.record_event()
+            cs.wait_event(done[layers] if done[layers] is not None else t0)
+            with torch.cuda.stream(cs):
+                dL.copy_(hL[i % 2], non_blocking=True)
+            stream.wait_event(cs.record_event())
+            pipe.commit_step(dL, stream)
+            done[layers] = stream.record_event()
+            pipe.t += 1
+            out[0].copy_(pipe.token, non_blocking=True)
+            out[1].copy_(pipe.conf, non_blocking=True)
+            out[2].copy_(pipe.commit, non_blocking=True)
+            out[3].copy_(last.D, non_blocking=True)
+        t1 = ev(enable_timing=True)
+        t1.record(stream)
+        return t0, t1
+
+    e2e_run(max(1, args.warmup // 2))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a, b = e2e_run(args.steps)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    e2e_ms = world_max(a.elapsed_time(b), dev)
+    h2d = layers * (hH[0].numel() * hH[0].element_size() + hQ[0].numel() * hQ[0].element_size()) \
+        + hL[0].numel() * hL[0].element_size()
+    d2h = sum(x.numel() * x.element_size() for x in out)
+
+    # rooflines: each op's algorithmic work against its measured time, and
+    # every kernel's from the trace
+    hbm, tf, src = peaks()
+    work = op_work(w, npos_mean)
+    rows = {}
+    for op in ops:
+        ms = statistics.mean(per_op[op])
+        by, fl = work[op]
+        if op != "commit":
+            by, fl = by * layers, fl * layers
+        bound = "tensor" if fl / (tf * 1e12) > by / (hbm * 1e9) else "hbm"
+        ach = (fl / (ms * 1e-3) / 1e12) if bound == "tensor" else (by / (ms * 1e-3) / 1e9)
+        peak = tf if bound == "tensor" else hbm
+        rows[op] = {"ms": ms, "bound": bound, "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": ach / peak,
+                    "alg_bytes": by, "alg_flops": fl}
+    kernels = kernel_rooflines(trace, ntrace, w, npos_mean, hbm, tf)
+    # the dominant kernel: most device time per step among those with a
+    # stated algorithmic workload
+    top = max((k for k in kernels if "frac" in kernels[k]),
+              key=lambda k: kernels[k]["us_per_step"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        per = tj.get("per_launch_bytes", {}).get(w.name, {})
+        if tj.get("source_hash") == source_hash() and top in per:
+            traffic = per[top]
+    r = kernels[top]
+    res = {
+        "value": steps_per_s, "ms_per_step": ms_step, "dtype": w.dtype,
+        "config": workload_config(w, layers),
+        "window_tokens_per_s": steps_per_s * w.B * w.N,
+        "e2e": {"value": aggregate_steps_per_s(world, args.steps, e2e_ms), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "timing": "eager calls of the public pipeline API; every layer's window and "
+                          "queries and the logits copied from pinned host memory each step "
+                          "(layer l's copy on a copy stream once the previous step's layer l "
+                          "is done), results read back; one interval over the steps"},
+        "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
+                     "unit": r["unit"], "frac": r["frac"], "traffic": traffic,
+                     "kernel": top, "us_per_launch": r["us_per_launch"],
+                     "launches_per_step": r["launches_per_step"],
+                     "alg_bytes_per_launch": r["alg_bytes"],
+                     "alg_flops_per_launch": r["alg_flops"], "peak_source": src},
+        "kernels": kernels,
+        "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
+                for op in ops},
+        "clocks": clk,
+        "gpu_launches": lib_launches * args.steps,
+        "graph_kernel_nodes": launches,
+        "eager_ms_per_step": eager_ms,
+        "timing": "CUDA-graph replay of the whole step (every layer, then the commit) per "
+                  "timed step",
+    }
+    if args.offload:
+        res["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
+        res["offload"] = offload_rates(trace, ntrace, w, npos_mean)
+    return res
 
 
 def main():
@@ -645,335 +985,51 @@ def main():
 
     import torch
     import torch.distributed as dist
-    from drift_aware_kv_spherical_gb300 import polestar as ps
     from drift_aware_kv_spherical_gb300 import workloads as wl
-    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl")
     w = wl.BY_NAME[args.workload]
-    L = wl.make_layer(w, 0, dev)
-    Hs = [L["H"]]
-    for t in range(1, 4):
-        Hs.append(wl.drift_rows(w, Hs[-1], t))
-    Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
-    # logits in the workload's dtype, as the model's LM head emits them
-    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(4)]
-    u = wl.make_uniforms(w, 0, dev)
-    pipe = Pipeline(w, layers=1, device=dev, offload=args.offload)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # the step reads its inputs from fixed buffers (graph replay needs fixed
-    # addresses); the next step's inputs are copied in outside the timed events
-    dH, dQ, dL = torch.empty_like(Hs[0]), torch.empty_like(Qs[0]), torch.empty_like(logits[0])
-
-    def load(i):
-        dH.copy_(Hs[i % 4])
-        dQ.copy_(Qs[i % 4])
-        dL.copy_(logits[i % 4])
-
-    # window build: k-means++ seeding, first distributions
-    load(0)
-    pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL, init_us=[u], first=True)
-    ops = ["kmeans", "nvfp4", "proxy_kl", "topk", "refresh", "commit"]
-
-    def op_calls(parity, ev=None):
-        """One step's six calls, A ping-pong selected by parity."""
-        st = pipe.state[0]
-        cur, prev = st.A[parity], st.A[1 - parity]
-        rec = (lambda j: ev[j].record()) if ev is not None else (lambda j: None)
-        rec(0)
-        ps.ps_kmeans_spherical(dH, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
-                               objective=st.obj, ws=pipe.ws[ps.OP_KMEANS])
-        rec(1)
-        ps.ps_nvfp4_residual(dH, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
-                             ws=pipe.ws[ps.OP_NVFP4])
-        if pipe.offload:  # the store in host memory
-            ps.ps_nvfp4_pack_clusters(st.codes, st.scales, st.assign, w.C, st.store, st.order,
-                                      st.cl_off)
-        rec(2)
-        ps.ps_proxy_attn_kl(dQ, st.chat, L["Wk"], prev, cur, st.D, w.Hkv,
-                            ws=pipe.ws[ps.OP_PROXY_KL])
-        rec(3)
-        ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
-                         st.npos, st.posmask)
-        rec(4)
-        src = dH
-        if pipe.offload:  # the selected clusters' rows from the host store
-            ps.ps_nvfp4_fetch_dequant(st.store, st.order, st.cl_off, st.sel, st.mu, st.rho, st.S,
-                                      st.Ht)
-            src = st.Ht
-        ps.ps_refresh_kv(src, st.pos, st.npos, L["Wk"], L["Wv"], st.Kc, st.Vc, w.Hkv, w.dh,
-                         ws=pipe.ws[ps.OP_REFRESH])
-        rec(5)
-        pipe.commit_step(dL)
-        rec(6)
-
-    def mk():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-
-    step_no = 1
-    for t in range(args.warmup):                    # eager warm-up
-        load(step_no)
-        op_calls(step_no % 2)
-        step_no += 1
-    torch.cuda.synchronize()
-    ps.ps_check()
-
-    # capture one graph per A ping-pong parity: the pipeline's step with the
-    # ops off the critical path (NVFP4, commit) on side streams
-    def concurrent_step(parity):
-        pipe.t = parity          # A[parity] is this step's distribution
-        pipe.step([dH], [dQ], [L["Wk"]], [L["Wv"]], dL, concurrent=True)
-
-    for t in range(2):           # side streams warmed up eagerly
-        load(step_no)
-        concurrent_step(step_no % 2)
-        step_no += 1
-    torch.cuda.synchronize()
-    ps.ps_check()
-    graphs = []
-    cap = torch.cuda.Stream(dev)
-    for parity in (0, 1):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            concurrent_step(parity)
-        graphs.append(g)
-    launches = graph_kernel_count(graphs[0])       # None if the runtime is unreachable
-    stream = torch.cuda.current_stream(dev)
-    for t in range(args.warmup):                    # graph warm-up
-        load(step_no)
-        graphs[step_no % 2].replay()
-        step_no += 1
-    torch.cuda.synchronize()
-    ps.ps_check()
-
-    # timed region: K graph replays, L2 flushed and inputs staged between them
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    for t in range(args.steps):
-        load(step_no)
-        flush.zero_()
-        gev[t][0].record(stream)
-        graphs[step_no % 2].replay()
-        gev[t][1].record(stream)
-        step_no += 1
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    ps.ps_check()
-    total_ms = world_max(sum(a.elapsed_time(b) for a, b in gev), dev)
-    ms_step = total_ms / args.steps
-    steps_per_s = aggregate_steps_per_s(world, args.steps, total_ms)
-
-    # per-op breakdown: the same steps eagerly, events between the calls; a
-    # device-side spin before each step lets the host enqueue the whole step
-    # first, so the events time the kernels and not the host's launch pace
-    events = [mk() for _ in range(args.steps)]
-    for t in range(args.steps):
-        load(step_no)
-        flush.zero_()
-        torch.cuda._sleep(4_000_000)
-        op_calls(step_no % 2, events[t])
-        step_no += 1
-    torch.cuda.synchronize()
-    ps.ps_check()
-    npos_seen = [int(pipe.state[0].npos.sum())]
-    per_op = {op: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, op in enumerate(ops)}
-    eager_ms = statistics.mean(ev[0].elapsed_time(ev[6]) for ev in events)
-
-    # per kernel: the library's own trace (CUDA events around each of its
-    # launches, on the launching stream) over a few more eager steps
-    ntrace = min(3, args.steps)
-    ps.ps_trace_enable(True)
-    for t in range(ntrace):
-        load(step_no)
-        flush.zero_()
-        torch.cuda._sleep(4_000_000)
-        op_calls(step_no % 2)
-        step_no += 1
-    torch.cuda.synchronize()
-    trace = ps.ps_trace_records()
-    ps.ps_trace_enable(False)
-    ps.ps_check()
-    # the library's kernels per step: every launch of its calls is traced
-    lib_launches = round(len(trace) / ntrace)
-
-    # end to end through the public API: every step's inputs copied from
-    # pinned host memory and its results read back, pipelined as a serving
-    # loop would: the device inputs are double-buffered (a captured graph per
-    # buffer set and A parity), and step i + 1's copies run on a copy stream
-    # while step i computes.  Step i is timed from its start to the end of
-    # both its read-back and step i + 1's copies, and a copy may begin only
-    # inside the interval of the step it overlaps, so every copy and every
-    # kernel lies inside a timed interval; the L2 flush between steps lies
-    # outside them, as for the device-timed value.
-    hH = [H.cpu().pin_memory() for H in Hs]
-    hQ = [Q.cpu().pin_memory() for Q in Qs]
-    hL = [x.cpu().pin_memory() for x in logits]
-    out = [torch.empty(pipe.token.shape, dtype=torch.int32).pin_memory(),
-           torch.empty(pipe.conf.shape).pin_memory(),
-           torch.empty(pipe.commit.shape, dtype=torch.uint8).pin_memory(),
-           torch.empty(pipe.state[0].D.shape).pin_memory()]
-    sets = [(dH, dQ, dL), (torch.empty_like(dH), torch.empty_like(dQ), torch.empty_like(dL))]
-
-    def set_step(k, parity):
-        h, q, lg = sets[k]
-        pipe.t = parity
-        pipe.step([h], [q], [L["Wk"]], [L["Wv"]], lg, concurrent=True)
-
-    sets[1][0].copy_(dH)
-    sets[1][1].copy_(dQ)
-    sets[1][2].copy_(dL)
-    set_step(1, step_no % 2)                        # the second set's side streams warmed up
-    step_no += 1
-    torch.cuda.synchronize()
-    egraphs = [graphs]
-    eg = []
-    for parity in (0, 1):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            set_step(1, parity)
-        eg.append(g)
-    egraphs.append(eg)
-    css = [torch.cuda.Stream(dev) for _ in range(COPY_STREAMS)]
-
-    def copy_in(i, k, after):
-        """After event `after`: step i's inputs into set k, each tensor cut in
-        COPY_STREAMS parts copied on as many streams (copy engines run them
-        side by side); returns an event on the main stream's side that covers
-        them all."""
-        parts = []
-        for src, dst in zip((hH[i % 4], hQ[i % 4], hL[i % 4]), sets[k]):
-            a, b = src.view(-1), dst.view(-1)
-            step = -(-a.numel() // COPY_STREAMS)
-            parts += [(a[j:j + step], b[j:j + step]) for j in range(0, a.numel(), step)]
-        evs = []
-        for n, c in enumerate(css):
-            c.wait_event(after)
-            with torch.cuda.stream(c):
-                for src, dst in parts[n::COPY_STREAMS]:
-                    dst.copy_(src, non_blocking=True)
-            evs.append(c.record_event())
-        for e in evs[1:]:
-            css[0].wait_event(e)
-        return css[0].record_event()
-
-    def e2e_run(n, timed):
-        nonlocal step_no
-        ev = torch.cuda.Event
-        spans = []
-        t0 = ev(enable_timing=True)
-        t0.record(stream)
-        copied = copy_in(0, 0, t0)
-        stream.wait_event(copied)
-        t1 = ev(enable_timing=True)
-        t1.record(stream)
-        spans.append((t0, t1))
-        for i in range(n):
-            k = i % 2
-            if timed:
-                flush.zero_()
-            a = ev(enable_timing=True)
-            a.record(stream)
-            nxt = None
-            if i + 1 < n:  # after `a`: step i - 1, the other set's reader, has finished
-                nxt = copy_in(i + 1, 1 - k, a)
-            egraphs[k][step_no % 2].replay()
-            out[0].copy_(pipe.token, non_blocking=True)
-            out[1].copy_(pipe.conf, non_blocking=True)
-            out[2].copy_(pipe.commit, non_blocking=True)
-            out[3].copy_(pipe.state[0].D, non_blocking=True)
-            if nxt is not None:
-                stream.wait_event(nxt)
-            b = ev(enable_timing=True)
-            b.record(stream)
-            spans.append((a, b))
-            step_no += 1
-        return spans
-
-    e2e_run(args.warmup, False)
-    torch.cuda.synchronize()
-    spans = e2e_run(args.steps, True)
-    torch.cuda.synchronize()
-    ps.ps_check()
-    e2e_ms = world_max(sum(a.elapsed_time(b) for a, b in spans), dev)
-    h2d = sum(x.numel() * x.element_size() for x in (hH[0], hQ[0], hL[0]))
-    d2h = sum(x.numel() * x.element_size() for x in out)
-
-    # roofline of the dominant op
-    hbm, tf, src = peaks()
-    work = op_work(w, npos_seen[-1] / w.B)
-    rows = {}
-    for op in ops:
-        ms = statistics.mean(per_op[op])
-        by, fl = work[op]
-        bound = "tensor" if fl / (tf * 1e12) > by / (hbm * 1e9) else "hbm"
-        ach = (fl / (ms * 1e-3) / 1e12) if bound == "tensor" else (by / (ms * 1e-3) / 1e9)
-        peak = tf if bound == "tensor" else hbm
-        rows[op] = {"ms": ms, "bound": bound, "achieved": ach, "peak": peak,
-                    "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": ach / peak,
-                    "alg_bytes": by, "alg_flops": fl}
-    kernels = kernel_rooflines(trace, ntrace, w, npos_seen[-1] / w.B, hbm, tf)
-    # the dominant kernel: most device time per step among those with a
-    # stated algorithmic workload
-    top = max((k for k in kernels if "frac" in kernels[k]),
-              key=lambda k: kernels[k]["us_per_step"])
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        tj = json.load(open(tpath))
-        if tj.get("source_hash") == source_hash() and top in tj.get("per_launch_bytes", {}):
-            traffic = tj["per_launch_bytes"][top]
-    r = kernels[top]
-    line = {
-        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic", "config": workload_config(w),
-        "window_tokens_per_s": steps_per_s * w.B * w.N,
-        "e2e": {"value": aggregate_steps_per_s(world, args.steps, e2e_ms), "unit": "steps/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "timing": "double-buffered inputs; step i + 1's host-to-device copies on a "
-                          "copy stream under step i; every copy inside a timed interval"},
-        "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
-                     "unit": r["unit"], "frac": r["frac"], "traffic": traffic,
-                     "kernel": top, "us_per_launch": r["us_per_launch"],
-                     "launches_per_step": r["launches_per_step"],
-                     "alg_bytes_per_launch": r["alg_bytes"],
-                     "alg_flops_per_launch": r["alg_flops"], "peak_source": src},
-        "kernels": kernels,
-        "ops": {op: {k: (round(v, 6) if isinstance(v, float) else v) for k, v in rows[op].items()}
-                for op in ops},
-        "clocks": clk,
-        "gpu_launches": lib_launches * args.steps,
-        "graph_kernel_nodes": launches,
-        "eager_ms_per_step": eager_ms,
-        "timing": "CUDA-graph replay of the whole step per timed step",
-        "parallelism": f"replicas x{world}",
-    }
-    if args.overlap:
-        line["overlap"] = measure_overlap(w, graphs, dev)
-    if args.ablation:
-        line["ablation"] = measure_ablation(w, L, Hs, Qs, logits, u, dev)
-    if args.decode:
-        if w.layers > 1:  # the multi-layer loop refreshes every layer at every step
-            line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev, steps=48, warm=4,
-                                            tau_upd=0, full_period=0, layers=w.layers)
-        else:
-            line["decode"] = measure_decode(w, L, Hs, Qs, logits, u, dev)
-    if args.offload:
-        line["config"]["offload"] = "NVFP4 clusters in pinned host memory, fetched per step"
-        line["offload"] = offload_rates(trace, ntrace, w, npos_seen[-1] / w.B)
+    layers = args.layers or w.layers
+    res = bench_workload(w, layers, args, dev, world, local)
+    torch.cuda.empty_cache()
+    line = {"metric": METRIC, "value": res.pop("value"), "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": res.pop("dtype"), "data": "synthetic", "config": res.pop("config")}
+    line.update(res)
+    line["parallelism"] = f"replicas x{world}"
+    if not args.no_overlap:
+        line["overlap"] = measure_overlap(w, dev, reps=20 if layers == 1 else 5)
+        torch.cuda.empty_cache()
+    if args.ablation or args.decode:
+        L, Hs1, Qs1, logits1, u1 = one_layer_inputs(w, dev)
+        if args.ablation:
+            line["ablation"] = measure_ablation(w, L, Hs1, Qs1, logits1, u1, dev)
+        if args.decode:
+            if w.layers > 1:  # the multi-layer loop refreshes every layer at every step
+                line["decode"] = measure_decode(w, L, Hs1, Qs1, logits1, u1, dev, steps=48,
+                                                warm=4, tau_upd=0, full_period=0,
+                                                layers=w.layers)
+            else:
+                line["decode"] = measure_decode(w, L, Hs1, Qs1, logits1, u1, dev)
+        del L, Hs1, Qs1, logits1
+        torch.cuda.empty_cache()
+    if args.extra and args.extra != "none" and args.extra != w.name:
+        xw = wl.BY_NAME[args.extra]
+        xr = bench_workload(xw, xw.layers, args, dev, world, local)
+        line["extra"] = {xw.name: {
+            "value": xr["value"], "unit": "steps/s", "ms_per_step": xr["ms_per_step"],
+            "window_tokens_per_s": xr["window_tokens_per_s"], "config": xr["config"],
+            "e2e": xr["e2e"], "roofline": xr["roofline"], "kernels": xr["kernels"],
+            "clocks": xr["clocks"], "gpu_launches": xr["gpu_launches"]}}
+        if not args.no_overlap:
+            line["extra"][xw.name]["overlap"] = measure_overlap(xw, dev)
+        torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, layers)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -418,6 +418,22 @@ bool device_accessible(const void* p) {
 }
 }  // namespace
 
+extern "C" ps_status ps_block_progress(ps_handle h, const uint8_t* commit,
+                                       const uint8_t* undecided, const uint8_t* role, int B,
+                                       int P, int32_t* out, void* stream) {
+  TraceScope trace_scope(h);
+  PS_REQUIRE(h != nullptr && B >= 0 && P >= 0);
+  PS_NN(out);
+  PS_REQUIRE((reinterpret_cast<uintptr_t>(out) & 7u) == 0);
+  PS_REQUIRE(device_accessible(out));
+  if (B > 0 && P > 0) {
+    PS_REQUIRE((long)B * P <= INT32_MAX);
+    PS_NN(commit); PS_NN(undecided); PS_NN(role);
+  }
+  return launch_status(block_progress_run(commit, undecided, role, B, P, out,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" size_t ps_store_record_bytes(int d) {
   return d > 0 && d % 32 == 0 ? ps::store_record_bytes(d) : 0;
 }

@@ -198,7 +198,45 @@ k_commit_rule(int P, int nchunk, const float* __restrict__ pm,
 
 int nchunks(int V) { return ceil_div(V, kChunk); }
 
+// The decode loop's outcome of a step, one CTA: out[0] = the largest number
+// of positions any sequence committed, out[1] = 1 when no sequence has an
+// undecided current-block position left.  A warp per sequence.
+__global__ void __launch_bounds__(256)
+k_block_progress(const uint8_t* __restrict__ commit, const uint8_t* __restrict__ undecided,
+                 const uint8_t* __restrict__ role, int B, int P, int32_t* __restrict__ out) {
+  pdl_prologue();
+  __shared__ int s_max, s_open;
+  if (threadIdx.x == 0) { s_max = 0; s_open = 0; }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int open = 0;
+  for (int b = warp; b < B; b += nw) {
+    int n = 0;
+    for (int j = lane; j < P; j += 32) {
+      const long row = (long)b * P + j;
+      n += commit[row] != 0;
+      open |= undecided[row] != 0 && role[j] == 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) atomicMax(&s_max, n);
+  }
+  if (__syncthreads_or(open) && threadIdx.x == 0) s_open = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    out[0] = s_max;
+    out[1] = s_open ? 0 : 1;
+  }
+}
+
 }  // namespace
+
+cudaError_t block_progress_run(const uint8_t* commit, const uint8_t* undecided,
+                               const uint8_t* role, int B, int P, int32_t* out,
+                               cudaStream_t s) {
+  launch_pdl(k_block_progress, 1, 256, 0, s, commit, undecided, role, B, P, out);
+  return cudaGetLastError();
+}
 
 size_t commit_ws(int B, int P, int V) {
   const size_t rows = (size_t)B * P * nchunks(V);

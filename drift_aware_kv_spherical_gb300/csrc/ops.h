@@ -107,5 +107,8 @@ struct CommitArgs {
 };
 size_t commit_ws(int B, int P, int V);
 cudaError_t commit_run(const CommitArgs& a, cudaStream_t s);
+cudaError_t block_progress_run(const uint8_t* commit, const uint8_t* undecided,
+                               const uint8_t* role, int B, int P, int32_t* out,
+                               cudaStream_t s);
 
 }  // namespace ps

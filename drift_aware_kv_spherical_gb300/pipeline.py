@@ -105,6 +105,7 @@ class Pipeline:
         self.t = 0
         self._side = None
         self._after_proxy = None
+        self.layer_done = []
 
     def side_streams(self):
         """Two streams for the ops off the critical path (NVFP4, commit)."""
@@ -208,6 +209,40 @@ class Pipeline:
         self.t += 1
 
 
+    def step_overlapped(self, Hs, Qs, Wks, Wvs, logits, main_stream, drift_stream,
+                        forward=None, init_us=None, first=False):
+        """The drift step hidden behind the caller's main forward on CUDA
+        streams [Polestar §2.C, latency hiding]: clustering, quantisation,
+        proxy attention and the update of the KV cache run on `drift_stream`
+        while `main_stream` goes on with the model.
+
+        forward(l, main_stream), if given, enqueues the caller's work that
+        produces layer l's H and Q (l < layers) and, for l == layers, the
+        block's logits.  Layer l's drift work forks from `main_stream` right
+        after forward(l) -- it sees everything enqueued there up to that
+        point -- and runs on `drift_stream` while forward(l + 1) runs on the
+        main stream.  The commit forks after forward(layers).  At the end
+        `main_stream` waits for `drift_stream`: the caches, the drift, the
+        commit outputs and the state for the next step are ready for what
+        the caller enqueues on `main_stream` next.  The event that ends
+        layer l's drift work is kept in `self.layer_done[l]` for a caller
+        that joins earlier, e.g. before a layer reads its cache.  The
+        results are those of step() with the same inputs."""
+        self.layer_done = []
+        for l in range(self.layers):
+            if forward is not None:
+                forward(l, main_stream)
+            drift_stream.wait_event(main_stream.record_event())
+            self.layer_step(l, Hs[l], Qs[l], Wks[l], Wvs[l],
+                            None if init_us is None else init_us[l], first, drift_stream)
+            self.layer_done.append(drift_stream.record_event())
+        if forward is not None:
+            forward(self.layers, main_stream)
+        drift_stream.wait_event(main_stream.record_event())
+        self.commit_step(logits, drift_stream)
+        self.t += 1
+        main_stream.wait_event(drift_stream.record_event())
+
     def decode_step(self, act, Hs, Qs, Wks, Wvs, logits, init_us=None, stream=None):
         """One decode step under schedule actions `act` (ps.SCHED_* flags):
         SLIDE resets the block's commit state; REFRESH runs every layer's
@@ -234,16 +269,12 @@ class Pipeline:
         and the block is decided when no window has an undecided
         current-block token."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
-        if self._flags is None:
-            self._flags = torch.zeros(2, dtype=torch.int32).pin_memory()
-        cur = (self.role == wl.ROLE_CURRENT)
-        with torch.cuda.stream(main):
-            committed = self.commit.to(torch.int32).sum(dim=1).max()
-            open_ = (self.undecided.bool() & cur).any()
-            self._flags.copy_(torch.stack([committed, open_.to(torch.int32)]),
-                              non_blocking=True)
+        if self._flags is None:  # pinned host memory the kernel writes straight into
+            self._flags = ps.HostStore(16)
+            self._flags_view = self._flags.view()[:8].view("int32")
+        ps.ps_block_progress(self.commit, self.undecided, self.role, self._flags, stream=main)
         main.synchronize()
-        return int(self._flags[0]), not bool(self._flags[1])
+        return int(self._flags_view[0]), bool(self._flags_view[1])
 
     def graph_step(self, act, Hs, Qs, Wks, Wvs, logits, init_us=None, stream=None):
         """decode_step through CUDA graphs: the step's inputs are copied into

@@ -22,7 +22,8 @@ EXPORTED = ["ps_create", "ps_destroy", "ps_check", "ps_status_string", "ps_last_
             "ps_workspace_bytes", "ps_kmeans_spherical", "ps_nvfp4_residual",
             "ps_proxy_attn_kl", "ps_topk_drift", "ps_refresh_kv", "ps_commit",
             "ps_store_record_bytes", "ps_host_alloc", "ps_host_free",
-            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant", "ps_schedule_step", "ps_drift_score"]
+            "ps_nvfp4_pack_clusters", "ps_nvfp4_fetch_dequant", "ps_schedule_step", "ps_drift_score",
+            "ps_block_progress"]
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -73,6 +74,7 @@ _SIGS = {
     "ps_host_alloc": (_i, [_sz, ctypes.POINTER(_p)]),
     "ps_host_free": (_i, [_p]),
     "ps_drift_score": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _p]),
+    "ps_block_progress": (_i, [_p, _p, _p, _p, _i, _i, _p, _p]),
     "ps_schedule_step": (_i, [ctypes.POINTER(ScheduleParams), ctypes.POINTER(ScheduleState),
                               _i, _i]),
     "ps_nvfp4_pack_clusters": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]),
@@ -366,6 +368,17 @@ def ps_nvfp4_fetch_dequant(store, order, cl_off, sel, mu, rho, tensor_scale, Ht,
                                          _ptr(rho), _ptr(tensor_scale), B, N, d, C, _ptr(Ht),
                                          _stream(stream))
     _check(st, "ps_nvfp4_fetch_dequant")
+
+
+def ps_block_progress(commit, undecided, role, out, stream=None):
+    """(tokens committed, block decided) of a decode step into `out`: a
+    HostStore of >= 8 bytes (readable on the host once `stream` has reached
+    it) or an int32 device tensor of 2 elements."""
+    lib = _lib()
+    B, P = commit.shape
+    st = lib.cdll.ps_block_progress(lib.handle(), _ptr(commit), _ptr(undecided), _ptr(role),
+                                    B, P, _store_ptr(out), _stream(stream))
+    _check(st, "ps_block_progress")
 
 
 # ---- refresh schedule of the decode loop (include/polestar.h; host only)

@@ -155,6 +155,30 @@ def drift_rows(w, H, step, layer=0):
     return Hf.to(H.dtype)
 
 
+def drift_inplace(w, H, Q, Wq, step, layer=0):
+    """Step `step` >= 1 of the drift, applied in place to H [B][N][d] and to
+    the rows of Q = H Wq that moved: the same recipe as drift_rows (a seeded
+    share of the rows plus the current block move by N(0, drift_std); the
+    32-layer loop's random walk moves every row), drawn only for the rows
+    that move, so a large window drifts without a second copy of it."""
+    device = H.device
+    g = _gen(w.seed + 1000 * layer + 7919 * step + 3, device)
+    B, N, d = H.shape
+    if w.walk:
+        H.copy_((H.float() + _randn((B, N, d), g, device, w.drift_std * 0.9 ** step))
+                .to(H.dtype))
+        Q.copy_(make_queries(w, H, Wq))
+        return
+    mask = torch.rand((B, N), generator=g, device=device) < w.drift_frac
+    mask[:, w.blk_start:w.blk_start + w.P] = True
+    rows = mask.reshape(-1).nonzero().squeeze(1)
+    Hf = H.view(B * N, d)
+    moved = (Hf[rows].float() + _randn((rows.numel(), d), g, device, w.drift_std)).to(H.dtype)
+    Hf[rows] = moved
+    q = (moved @ Wq) if H.is_cuda else (moved.float() @ Wq.float())
+    Q.view(B * N, -1)[rows] = q.to(Q.dtype)
+
+
 def make_queries(w, H, Wq):
     """Q = H Wq laid out [B][N][Hq][dh] in the workload dtype (input
     synthesis; the drift path takes Q as given)."""

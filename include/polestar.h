@@ -392,6 +392,27 @@ ps_status ps_drift_score(ps_handle h, const float* A_cur, const float* A_prev,
                          void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The outcome of a decode step that the refresh schedule below consumes.
+ * [Polestar §2.A, schedule]: refreshes are triggered by the number of
+ * decoded tokens; the window moves on when the current block is decided.
+ *
+ * One small kernel writes out[0] = the largest number of positions any of
+ * the B sequences committed in this step (commit [B][P] u8, every role) and
+ * out[1] = 1 when no sequence has an undecided current-block position left
+ * (undecided [B][P] u8, role [P] u8 with 0 = current block), else 0 -- the
+ * (committed, block_done) pair of ps_schedule_step, computed where the
+ * flags are, so the host reads one 8-byte pair.
+ * out: int32[2], 8-byte aligned, in device memory or in ps_host_alloc
+ * memory (then readable on the host once the stream has reached it).
+ * B == 0 or P == 0 writes (0, 1).  Errors: a NULL handle or out, an
+ * unreachable or misaligned out, or NULL flags with B, P > 0 return
+ * PS_ERR_ARG before anything is enqueued.
+ * ------------------------------------------------------------------------- */
+ps_status ps_block_progress(ps_handle h, const uint8_t* commit,
+                            const uint8_t* undecided, const uint8_t* role,
+                            int B, int P, int32_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Refresh schedule of the decode loop (host only; no handle, no GPU work).
  * [Polestar §2.A, schedule]: the drift refresh is triggered once the decoded
  * context has moved enough -- after tau_upd tokens were decoded -- and

@@ -56,5 +56,5 @@ __all__ = [
     "confidence", "commit_rule", "CommitParams",
     "record_bytes", "pack_clusters", "reconstruct_row", "fetch_reconstruct",
 ]
-from .schedule import ScheduleState, schedule_step
+from .schedule import ScheduleState, schedule_step, block_progress
 from .scorers import SCORER_KL, SCORER_COSINE, SCORER_ENTROPY, drift_score

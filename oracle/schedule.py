@@ -48,3 +48,24 @@ def schedule_step(tau_upd, full_period, block_len, state, committed, block_done)
     if full_period > 0 and state.refreshes % full_period == 0:
         act |= FULL
     return act
+
+
+def block_progress(commit, undecided, role, current_role=0):
+    """The decode loop's outcome of one step, which the schedule above
+    consumes: (tokens committed, block decided).  A batch decodes in
+    lockstep, so the count is the largest over the batch's sequences of the
+    number of positions that committed in this step (every role), and the
+    block is decided when no sequence has an undecided position of the
+    current block.  commit, undecided: [B][P] flags; role: [P]."""
+    B = len(commit)
+    committed = 0
+    still_open = False
+    for b in range(B):
+        n = 0
+        for j in range(len(role)):
+            if commit[b][j]:
+                n += 1
+            if undecided[b][j] and role[j] == current_role:
+                still_open = True
+        committed = max(committed, n)
+    return committed, not still_open

@@ -255,3 +255,23 @@ def test_graph_decode_matches_eager(widx, steps):
     assert len(set(a0)) >= 3                                  # several kinds of step replayed
     for x, y in zip(s0 + c0, s1 + c1):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("B,P", [(1, 16), (4, 32), (32, 64), (3, 1000)])
+def test_block_progress_matches_oracle(B, P):
+    g = torch.Generator(device="cuda").manual_seed(B * 1000 + P)
+    role = torch.randint(0, 3, (P,), device="cuda", generator=g, dtype=torch.uint8)
+    out = ps.HostStore(16)
+    view = out.view()[:8].view("int32")
+    dev_out = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    for density in (0.0, 0.02, 0.5):
+        commit = (torch.rand(B, P, device="cuda", generator=g) < density).to(torch.uint8)
+        undecided = (torch.rand(B, P, device="cuda", generator=g) < density).to(torch.uint8)
+        ps.ps_block_progress(commit, undecided, role, out)
+        ps.ps_block_progress(commit, undecided, role, dev_out)
+        torch.cuda.synchronize()
+        ps.ps_check()
+        want = oracle.block_progress(np_(commit).tolist(), np_(undecided).tolist(),
+                                     np_(role).tolist())
+        assert (int(view[0]), bool(view[1])) == want
+        assert (int(dev_out[0]), bool(dev_out[1])) == want

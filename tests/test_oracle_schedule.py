@@ -112,3 +112,15 @@ def test_refreshes_follow_the_running_count(impl):
         fulls = [t for t, a in enumerate(acts) if a & FULL]
         assert fulls == (got[full - 1::full] if full > 0 else [])
         assert not any(a & (SLIDE | REINIT) for a in acts)
+
+
+def test_block_progress_hand_worked():
+    from oracle.schedule import block_progress
+    role = [0, 0, 1, 2]
+    # sequence 0 commits two tokens (one of them suffix), sequence 1 one
+    commit = [[1, 0, 1, 0], [0, 1, 0, 0]]
+    undecided = [[0, 1, 0, 1], [0, 0, 1, 1]]       # seq 0 still has current token 1 open
+    assert block_progress(commit, undecided, role) == (2, False)
+    undecided = [[0, 0, 1, 1], [0, 0, 0, 1]]       # only suffix / inactive left: decided
+    assert block_progress(commit, undecided, role) == (2, True)
+    assert block_progress([[0] * 4], [[0] * 4], role) == (0, True)
