@@ -267,13 +267,16 @@ def kernel_work(key, w, npos_mean):
 def measure_overlap(w, dev, reps=20):
     """Latency hiding (the pages overlap the drift work with the main forward
     on CUDA streams), through Pipeline.step_overlapped on one layer: the
-    main stream runs a synthetic forward of one transformer layer over the
+    main stream runs a synthetic forward of a transformer layer over the
     window (bf16 GEMMs: x W_qkv, W_o, a gated MLP of width 3.5 d: W_up to 2
-    widths, W_down back; activations left out) and the layer's drift work
-    forks onto a drift stream behind it.  Each arrangement is captured as a
-    CUDA graph: the forward alone, the drift step alone, both through
-    step_overlapped.  hidden = (t_main + t_drift - t_both) / t_drift, the
-    share of the drift step's time the overlap hides."""
+    widths, W_down back; activations left out) that produces the layer's
+    inputs, the layer's drift work forks onto a drift stream behind it, and
+    the main stream goes on with the next layer's forward (the same GEMMs,
+    in the slot step_overlapped gives the rest of the model).  Each
+    arrangement is captured as a CUDA graph: the two forwards alone, the
+    drift step alone, both through step_overlapped.  hidden = (t_main +
+    t_drift - t_both) / t_drift, the share of the drift step's time the
+    overlap hides."""
     import torch
     from drift_aware_kv_spherical_gb300.pipeline import Pipeline
     from drift_aware_kv_spherical_gb300 import workloads as wl
@@ -297,8 +300,6 @@ def measure_overlap(w, dev, reps=20):
     sm, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def forward(l, s):
-        if l > 0:  # the LM head's logits are an input of this measurement
-            return
         with torch.cuda.stream(s):
             qkv = X @ Wqkv
             o = qkv[:, :d] @ Wo
@@ -323,10 +324,10 @@ def measure_overlap(w, dev, reps=20):
     def both():
         pipe.step_overlapped([H], [Q], [Wk], [Wv], logits, sm, sd, forward=forward)
 
-    gm = capture(lambda: forward(0, sm))
+    gm = capture(lambda: (forward(0, sm), forward(1, sm)))
     gd = capture(drift_only)
     gb = capture(both)
-    flops = 2.0 * M * d * (3 * d + d + 2 * ff + ff)
+    flops = 2 * 2.0 * M * d * (3 * d + d + 2 * ff + ff)
 
     def timed(graph):
         for _ in range(3):
@@ -344,7 +345,8 @@ def measure_overlap(w, dev, reps=20):
     t_main, t_drift, t_both = timed(gm), timed(gd), timed(gb)
     return {"api": "Pipeline.step_overlapped (main stream: the forward; drift stream: "
                    "clustering, quantisation, proxy attention, top-k, refresh, commit)",
-            "main_forward": f"bf16 GEMMs of one layer over {M} rows (d {d}, MLP {ff}), "
+            "main_forward": f"bf16 GEMMs of two layers over {M} rows (d {d}, MLP {ff}): the "
+                            f"layer whose drift is computed and the next, "
                             f"{flops / 1e12:.2f} TFLOP, captured graph",
             "main_us": t_main, "drift_us": t_drift, "both_us": t_both,
             "main_tflops": flops / (t_main * 1e-6) / 1e12,

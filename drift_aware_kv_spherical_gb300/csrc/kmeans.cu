@@ -25,8 +25,30 @@
 //                   ascending row order, centroid = normalise(sum of unit
 //                   rows) (+ bf16 split), or on the last pass C_hat =
 //                   mean(rho) * mu; counts; objective
+//
+// Large batches (one d-chunk per tile) take the passes in a faster form with
+// the same results:
+//   * bf16 centroids only.  A pass scores every row against bf16(mu) alone
+//     (one MMA instead of the hi + lo pair).  Rounding a centroid to bf16
+//     moves every cosine by at most e = max_c ||mu_c - bf16(mu_c)|| (Cauchy-
+//     Schwarz), so a row whose best score leads the runner-up by more than
+//     ||h|| (2 e + 2^-13) -- the last term for the tensor cores' fp32
+//     accumulation over d -- has the same arg-max as exact arithmetic.  Rows
+//     within that band are listed with every centroid inside it, and
+//     k_km_recheck decides them with fp32 dot products against the fp32
+//     centroids.
+//   * Early exit.  Once a pass t >= 1 leaves every label of a window as the
+//     pass before did, the next update gives back the same centroids bit for
+//     bit (the update is a fixed function of H and the labels) and so every
+//     later pass the same labels and cosines: those passes and updates are
+//     skipped for that window (the CTAs see the window's flags and take no
+//     tile), and their objectives repeat the last one computed.  The outputs
+//     equal those of computing every pass.
+//   * rho exact.  k_km_rho takes rho_i = <h_i, mu_{a_i}> in fp32 after the
+//     last pass (the passes' best scores use bf16(mu)).
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "ops.h"
 #include "tc_gemm.cuh"
@@ -38,6 +60,30 @@ namespace {
 constexpr int kTileRows = 64;    // rows per assignment tile
 constexpr int kTileC = 128;      // centroids per chunk of an assignment tile
 constexpr int kTileK = 32;       // d per shared-memory stage
+
+// Early exit of the passes: changed[b * kMaxPasses + t] = 1 once pass t >= 1
+// gave some row of window b another label than pass t - 1.  Pass t of window
+// b runs while every pass 1 .. t - 1 changed a label; the update after pass
+// t runs while every pass 1 .. t did.
+constexpr int kMaxPasses = 64;
+__device__ __forceinline__ bool km_pass_active(const int32_t* changed, int b, int t) {
+  const int32_t* f = changed + (long)b * kMaxPasses;
+  for (int q = 1; q < t; ++q)
+    if (__ldcg(f + q) == 0) return false;
+  return true;
+}
+
+// Allowance for the tensor cores' fp32 accumulation of a bf16 score over d
+// (relative to ||h||), on top of the centroids' bf16 rounding.
+constexpr float kAccAllowance = 1.0f / 8192.0f;
+
+// A row whose bf16-centroid arg-max is not certain: its candidates (every
+// centroid whose score lies within the band of the best), in ascending
+// order, or n = -1 when there are more than kRcMax of them (then all C).
+constexpr int kRcMax = 10;
+struct RcEntry {
+  int32_t row, n, c[kRcMax];
+};
 
 
 // k-means++ on the sphere, one round r at a time: k_kpp_pick chooses centre
@@ -257,18 +303,22 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
 // Set-up of a call, in one launch: blocks [0, inv_blocks) take 1/||h_i||
 // for 8 rows each (a warp per row, its 16-byte loads unrolled four deep);
 // the rest split mu (fp32) into bf16 hi + lo parts (hi = bf16(mu), lo =
-// bf16(mu - hi)), four values per thread, into two [B][C][d] arrays or
-// (cd = C d > 0) one [B][2C][d] array at hi.  Either part may be empty.
+// bf16(mu - hi)), a warp per centroid row, four values per lane at a time,
+// into two [B][C][d] arrays or (cd = C d > 0) one [B][2C][d] array at hi.
+// Either part may be empty.  emax (nullable, [B], zeroed by the caller):
+// raised to ||mu_c - hi_c|| of every centroid of window b (fp32 bits
+// compared as integers, which orders non-negative floats, so the result does
+// not depend on the order of the updates).
 template <typename T>
 __global__ void __launch_bounds__(256)
 k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, int inv_blocks,
           const float* __restrict__ mu, long n_mu, __nv_bfloat16* __restrict__ hi,
-          __nv_bfloat16* __restrict__ lo, long cd) {
+          __nv_bfloat16* __restrict__ lo, long cd, int C, float* __restrict__ emax) {
   pdl_prologue();
+  const int lane = threadIdx.x & 31;
   if ((int)blockIdx.x < inv_blocks) {
     constexpr int V = Vec<T>::n;
     const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const T* h = H + row * d;
     float ss = 0.f;
@@ -283,24 +333,35 @@ k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, in
     if (lane == 0) inv[row] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
     return;
   }
-  const long n4 = n_mu >> 2;  // n_mu = B * C * d, a multiple of 16
-  const long stride = (long)(gridDim.x - inv_blocks) * blockDim.x;
-  for (long i = (long)(blockIdx.x - inv_blocks) * blockDim.x + threadIdx.x; i < n4;
-       i += stride) {
-    // cd > 0: one [2C][d] block per window, the C hi rows then the C lo rows
-    const long e = 4 * i;
-    const long eh = cd > 0 ? (e / cd) * 2 * cd + e % cd : e;
-    const long el = cd > 0 ? eh + cd : e;
-    const float4 x = reinterpret_cast<const float4*>(mu)[i];
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
-    const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
-    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-    const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
-    const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
-    *reinterpret_cast<uint2*>(hi + eh) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
-                                                    *reinterpret_cast<const uint32_t*>(&h1));
-    *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
-                                                    *reinterpret_cast<const uint32_t*>(&l1));
+  const long nrow = n_mu / d;  // n_mu = B * C * d, d a multiple of 16
+  const long nwarps = ((long)(gridDim.x - inv_blocks) * blockDim.x) >> 5;
+  for (long r = ((long)(blockIdx.x - inv_blocks) * blockDim.x + threadIdx.x) >> 5; r < nrow;
+       r += nwarps) {
+    float e2 = 0.f;
+    for (int k = lane * 4; k < d; k += 128) {
+      // cd > 0: one [2C][d] block per window, the C hi rows then the C lo rows
+      const long e = r * d + k;
+      const long eh = cd > 0 ? (e / cd) * 2 * cd + e % cd : e;
+      const long el = cd > 0 ? eh + cd : e;
+      const float4 x = *reinterpret_cast<const float4*>(mu + e);
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
+      *reinterpret_cast<uint2*>(hi + eh) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                      *reinterpret_cast<const uint32_t*>(&h1));
+      *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
+                                                      *reinterpret_cast<const uint32_t*>(&l1));
+      e2 = fmaf(x.x - f0.x, x.x - f0.x, e2);
+      e2 = fmaf(x.y - f0.y, x.y - f0.y, e2);
+      e2 = fmaf(x.z - f1.x, x.z - f1.x, e2);
+      e2 = fmaf(x.w - f1.y, x.w - f1.y, e2);
+    }
+    if (emax != nullptr) {
+      e2 = warp_sum(e2);
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(emax) + r / C, __float_as_int(sqrtf(e2)));
+    }
   }
 }
 
@@ -377,6 +438,181 @@ struct KmAssignEpi : TcEpiBase {
     epi_bar_sync();
   }
 };
+
+// Epilogue of the faster passes (one d-chunk per tile, scores against
+// bf16(mu) only; see the file comment).  Per row: the best score (first
+// maximum) and the runner-up.  A row whose lead exceeds the band
+// ||h|| (2 e_b + kAccAllowance) gets its label and best score here, and
+// raises the window's `changed` flag of this pass when the label moved;
+// any other row is listed for k_km_recheck with the centroids inside the
+// band.  Tiles of windows whose passes have settled are skipped.
+template <int BN>
+struct KmFastEpi : TcEpiBase {
+  int B, N, C, mtb, pass;
+  const float* inv;
+  const float* emax;   // [B] max_c ||mu_c - bf16(mu_c)||
+  int32_t* assign;
+  float* best;
+  int32_t* changed;    // [B][kMaxPasses]
+  int* rc_count;       // entries listed in this pass
+  RcEntry* rc_list;    // [B * N]
+  struct State {};
+  __device__ int tiles(int) const { return B * mtb; }
+  __device__ int arow(int t) const { return (t / mtb) * N + (t % mtb) * 128; }
+  __device__ int bcoord(int t, int n0) const { return (t / mtb) * C + n0; }
+  __device__ bool active(int t) const { return km_pass_active(changed, t / mtb, pass); }
+  __device__ void consume(int t, int r, int, int, uint32_t taddr, State&) const {
+    const int b = t / mtb, i = (t % mtb) * 128 + r;
+    const bool valid = i < N;
+    const long row = (long)b * N + i;
+    float bv = -INFINITY, sv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(taddr + c0, v);  // warp-collective
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (c0 + j < C) {
+          if (v[j] > bv) {
+            sv = bv;
+            bv = v[j];
+            bi = c0 + j;
+          } else if (v[j] > sv) {
+            sv = v[j];
+          }
+        }
+      }
+    }
+    float band = 0.f;
+    bool certain = true;
+    if (valid) {
+      const float iv = inv[row];
+      band = (iv > 0.f ? 1.0f / iv : 0.f) * (2.0f * emax[b] + kAccAllowance);
+      certain = bi == INT_MAX || !(bv - sv <= band);  // ties and near-ties are rechecked
+    }
+    const bool listed = valid && !certain;
+    if (__any_sync(0xffffffffu, listed)) {
+      RcEntry en;
+      en.row = (int32_t)row;
+      en.n = 0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(taddr + c0, v);
+        if (listed) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < C && v[j] >= bv - band) {
+              if (en.n < kRcMax) en.c[en.n] = c0 + j;
+              ++en.n;
+            }
+          }
+        }
+      }
+      if (listed) {
+        if (en.n > kRcMax) en.n = -1;
+        rc_list[atomicAdd(rc_count, 1)] = en;
+      }
+    }
+    if (valid && certain) {
+      if (bi == INT_MAX) { bi = 0; bv = 0.f; }
+      if (pass >= 1 && assign[row] != bi) changed[(long)b * kMaxPasses + pass] = 1;
+      assign[row] = bi;
+      best[row] = bv;
+    }
+  }
+  __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
+};
+
+// The listed rows of a pass, a warp per row: fp32 dot products of h_i with
+// the fp32 centroids of its candidates (lanes over d, summed in a fixed
+// order), the first maximum in ascending centroid order; label, best score
+// and the window's `changed` flag as in the epilogue.  Runs on a fixed grid
+// and reads the number of rows from the device.
+__global__ void __launch_bounds__(256)
+k_km_recheck(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, int N, int d,
+             int C, int pass, const int* __restrict__ count, const RcEntry* __restrict__ list,
+             int32_t* __restrict__ assign, float* __restrict__ best,
+             int32_t* __restrict__ changed) {
+  pdl_prologue();
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int n = *count;
+  for (int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; e < n; e += nw) {
+    const RcEntry en = list[e];
+    const long row = en.row;
+    const int b = (int)(row / N);
+    const __nv_bfloat16* h = H + row * d;
+    const int nc = en.n < 0 ? C : en.n;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int q = 0; q < nc; ++q) {
+      const int c = en.n < 0 ? q : en.c[q];
+      const float* m = mu + ((long)b * C + c) * d;
+      float dot = 0.f;
+#pragma unroll 4
+      for (int k = lane * 8; k < d; k += 256) {
+        float hv[8];
+        load16(h + k, hv);
+        const float4 m0 = *reinterpret_cast<const float4*>(m + k);
+        const float4 m1 = *reinterpret_cast<const float4*>(m + k + 4);
+        dot = fmaf(hv[0], m0.x, dot);
+        dot = fmaf(hv[1], m0.y, dot);
+        dot = fmaf(hv[2], m0.z, dot);
+        dot = fmaf(hv[3], m0.w, dot);
+        dot = fmaf(hv[4], m1.x, dot);
+        dot = fmaf(hv[5], m1.y, dot);
+        dot = fmaf(hv[6], m1.z, dot);
+        dot = fmaf(hv[7], m1.w, dot);
+      }
+      dot = warp_sum(dot);
+      if (dot > bv) { bv = dot; bi = c; }  // ascending c: the first maximum
+    }
+    if (lane == 0) {
+      if (bi == INT_MAX) { bi = 0; bv = 0.f; }
+      if (pass >= 1 && assign[row] != bi) changed[(long)b * kMaxPasses + pass] = 1;
+      assign[row] = bi;
+      best[row] = bv;
+    }
+  }
+}
+
+// rho_i = <h_i, mu_{a_i}> in fp32 after the last pass, a warp per row (lanes
+// over d, summed in a fixed order).
+__global__ void __launch_bounds__(256)
+k_km_rho(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, long rows, int N,
+         int d, int C, const int32_t* __restrict__ assign, float* __restrict__ rho) {
+  pdl_prologue();
+  const int lane = threadIdx.x & 31;
+  const long nw = ((long)gridDim.x * blockDim.x) >> 5;
+  for (long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows; row += nw) {
+    const int b = (int)(row / N);
+    const __nv_bfloat16* h = H + row * d;
+    // a label is in [0, C) unless a pass gave up (then the status word says
+    // so); clamped so that no read leaves the centroids
+    const int c = min(max(assign[row], 0), C - 1);
+    const float* m = mu + ((long)b * C + c) * d;
+    float dot = 0.f;
+#pragma unroll 4
+    for (int k = lane * 8; k < d; k += 256) {
+      float hv[8];
+      load16(h + k, hv);
+      const float4 m0 = *reinterpret_cast<const float4*>(m + k);
+      const float4 m1 = *reinterpret_cast<const float4*>(m + k + 4);
+      dot = fmaf(hv[0], m0.x, dot);
+      dot = fmaf(hv[1], m0.y, dot);
+      dot = fmaf(hv[2], m0.z, dot);
+      dot = fmaf(hv[3], m0.w, dot);
+      dot = fmaf(hv[4], m1.x, dot);
+      dot = fmaf(hv[5], m1.y, dot);
+      dot = fmaf(hv[6], m1.z, dot);
+      dot = fmaf(hv[7], m1.w, dot);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) rho[row] = dot;
+  }
+}
 
 // Split assignment inside one thread-block cluster (nz <= 8 d-chunks, C <=
 // 128): each CTA leaves its chunk's 128 x C scores in shared memory; CTA z
@@ -550,7 +786,8 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
                float* __restrict__ chat, const float* __restrict__ objp, int ntile,
                float* __restrict__ obj, int obj_ld, int pass,
-               const int32_t* __restrict__ assign_fin) {
+               const int32_t* __restrict__ assign_fin, const int32_t* __restrict__ changed,
+               float* __restrict__ emax) {
   pdl_prologue();
   constexpr int V = Vec<T>::n;
   constexpr int kMemb = 16 / G;
@@ -560,6 +797,27 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
   __shared__ float s_ss;
   const int c = blockIdx.x, b = blockIdx.y, z = blockIdx.z, S = gridDim.z;
   const int tid = threadIdx.x, nthr = blockDim.x;
+  // The pass objective, CTA (0, b, 0): with `changed` (the faster passes)
+  // from the rows' best scores, sum_i best_i / ||h_i|| in a fixed order
+  // (rho holds the best scores of the latest pass of this window); else from
+  // the assignment tiles' partials.
+  auto fold_objective = [&]() {
+    if (c != 0 || z != 0 || obj == nullptr) return;  // block-uniform
+    float so = 0.f;
+    if (changed != nullptr) {
+      for (int i = tid; i < N; i += nthr) so = fmaf(rho[(long)b * N + i], inv[(long)b * N + i], so);
+    } else {
+      for (int t = tid; t < ntile; t += nthr) so += objp[(long)b * ntile + t];
+    }
+    so = block_sum_f32(so, s_red);
+    if (tid == 0) obj[(long)b * obj_ld + pass] = so;
+  };
+  // a window whose passes have settled keeps its centroids: only the
+  // objective of this pass is written (the same as the last one computed)
+  if (!FINAL && changed != nullptr && !km_pass_active(changed, b, pass + 1)) {
+    fold_objective();
+    return;
+  }
   const int col0 = z * W, col1 = min(d, col0 + W);
   float u[G][V];
 #pragma unroll
@@ -637,12 +895,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     __syncthreads();
   }
   pdl_trigger();
-  if (c == 0 && z == 0 && obj != nullptr) {  // block-uniform: folds the pass objective
-    float so = 0.f;
-    for (int t = tid; t < ntile; t += nthr) so += objp[(long)b * ntile + t];
-    so = block_sum_f32(so, s_red);
-    if (tid == 0) obj[(long)b * obj_ld + pass] = so;
-  }
+  fold_objective();
   // fused last update + final pass: the final labels' members give the
   // count and the mean rho of C_hat
   int n_fin = n;
@@ -699,6 +952,7 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     }
     const long ro = ((long)b * C + c) * d;
     const float mean = (FUSED && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
+    float e2 = 0.f;  // ||mu_c - bf16(mu_c)||^2 over this slice's columns
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int col = col0 + (g * nthr + tid) * V;
@@ -707,6 +961,13 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
         if (formed) {
 #pragma unroll
           for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
+          if (emax != nullptr) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+              const float dv = x[e] - __bfloat162float(__float2bfloat16_rn(x[e]));
+              e2 = fmaf(dv, dv, e2);
+            }
+          }
           float4* mo = reinterpret_cast<float4*>(mu + ro + col);
 #pragma unroll
           for (int e = 0; e < V; e += 4)
@@ -744,6 +1005,13 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
             co[e / 4] = make_float4(mean * x[e], mean * x[e + 1], mean * x[e + 2], mean * x[e + 3]);
         }
       }
+    }
+    // the bf16 rounding bound of the window's centroids: this slice's share
+    // of ||mu_c - bf16(mu_c)|| times sqrt(S) bounds the whole row's (its
+    // square is at most S times the largest slice's)
+    if (emax != nullptr && formed) {  // block-uniform
+      e2 = block_sum_f32(e2, s_red);
+      if (tid == 0) atomicMax(reinterpret_cast<int*>(emax) + b, __float_as_int(sqrtf(e2 * S)));
     }
     // no CTA leaves while another still reads its s_ss
     if (S > 1) tc::cluster_wait();
@@ -846,6 +1114,13 @@ struct KmWs {
   __nv_bfloat16* mu_split;  // Gram form with pass 0 inside: [B][2C][d] hi, lo rows
   int16_t* qhi;    // Gram form: fixed-point Gram matrices, high and low parts
   uint8_t* qlo;
+  // faster passes: per-window flags, rounding bound and recheck list; the
+  // first three are one contiguous block (zeroed per call)
+  int32_t* changed;  // [B][kMaxPasses]
+  float* emax;       // [B]
+  int* rc_count;     // [kMaxPasses]
+  size_t flag_bytes;
+  RcEntry* rc_list;  // [B * N]
 };
 
 KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int d, int C,
@@ -861,6 +1136,14 @@ KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int 
     w.mu_hi = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.mu_lo = cv.take<__nv_bfloat16>((size_t)B * C * d);
     w.part = p.nz > 1 && !p.cluster ? cv.take<float>((size_t)p.nz * C * BN_) : nullptr;
+    if (p.nz == 1) {
+      const size_t nflag = (size_t)B * kMaxPasses + B + kMaxPasses;
+      w.changed = cv.take<int32_t>(nflag);
+      w.emax = reinterpret_cast<float*>(w.changed ? w.changed + (size_t)B * kMaxPasses : nullptr);
+      w.rc_count = w.changed ? w.changed + (size_t)B * kMaxPasses + B : nullptr;
+      w.flag_bytes = nflag * sizeof(int32_t);
+      w.rc_list = cv.take<RcEntry>((size_t)BN_);
+    }
   }
   if (g.ok) {
     const size_t q = (size_t)B * g.Z * N * g.R;
@@ -904,6 +1187,41 @@ cudaError_t assign_tc(const KmeansArgs& a, const KmPlan& p, const KmWs& w, float
   return cudaGetLastError();
 }
 
+// One faster pass (see the file comment): bf16(mu) scores on the tensor
+// cores over a persistent grid of at most one CTA per SM walking the row
+// tiles, tiles of settled windows skipped; then the recheck of the listed
+// rows.
+template <int BN>
+cudaError_t assign_fast(const KmeansArgs& a, const KmPlan& p, const KmWs& w, int pass,
+                        cudaStream_t s) {
+  TcMaps maps;
+  const long rows = (long)a.B * a.N;
+  if (!make_tmap_bf16_2d(&maps.a[0], a.H, a.d, rows, (uint64_t)a.d * 2, 64, 128) ||
+      !make_tmap_bf16_2d(&maps.b[0], w.mu_hi, a.d, (uint64_t)a.B * a.C, (uint64_t)a.d * 2, 64,
+                         BN))
+    return cudaErrorInvalidValue;
+  maps.a[1] = maps.a[0];
+  maps.b[1] = maps.b[0];
+  TcShape sh{(int)rows, nullptr, p.KB, p.KB, a.status, INT_MAX};
+  KmFastEpi<BN> epi{{}, a.B, a.N, a.C, p.mtb, pass, w.inv, w.emax, a.assign, a.rho,
+                    w.changed, w.rc_count + pass, w.rc_list};
+  const int tiles = a.B * p.mtb;
+  const int gy = std::min(tiles, a.num_sms > 0 ? a.num_sms : kSmTarget);
+  cudaError_t e = launch_tc_gemm<BN, 1, 1, false>(maps, sh, epi, dim3(1, gy, 1), s);
+  if (e != cudaSuccess) return e;
+  launch_pdl(k_km_recheck, 2 * kSmTarget, 256, 0, s,
+             static_cast<const __nv_bfloat16*>(a.H), a.mu, a.N, a.d, a.C, pass,
+             w.rc_count + pass, w.rc_list, a.assign, a.rho, w.changed);
+  return cudaGetLastError();
+}
+
+// PS_KMEANS_SLOW set in the environment keeps the hi + lo passes without
+// early exit, for comparing the two.
+bool kmeans_fast_disabled() {
+  static const bool off = std::getenv("PS_KMEANS_SLOW") != nullptr;
+  return off;
+}
+
 template <typename T>
 cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const T* H = static_cast<const T*>(a.H);
@@ -929,8 +1247,16 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   // Gram form with k-means++: the seeds come from K itself (gram_seed), one
   // launch instead of 2C - 1, and pass 0's cosines are K's columns
   const bool gram_seeding = gram && seeding;
+  // the faster passes (one d-chunk per tile, bf16 windows, no Gram form)
+  const bool fast = p.tc && p.nz == 1 && !gram && a.iters + 1 <= kMaxPasses &&
+                    !kmeans_fast_disabled() && std::is_same<T, __nv_bfloat16>::value;
+  if (fast) {
+    cudaError_t e = cudaMemsetAsync(w.changed, 0, w.flag_bytes, s);
+    if (e != cudaSuccess) return e;
+  }
+  float* emax = fast ? w.emax : nullptr;
   launch_pdl(k_km_prep<T>, inv_blocks + (seeding ? 0 : split_blocks), 256, 0, s, H, BN_, a.d,
-             w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, split_hi, split_lo, cd);
+             w.inv, inv_blocks, a.mu, seeding ? 0L : n_mu, split_hi, split_lo, cd, a.C, emax);
   if (seeding && !gram_seeding) {
     for (int r = 0; r < a.C; ++r) {
       launch_pdl(k_kpp_pick<T>, a.B, 1024, 0, s, H, w.inv, a.init_u, a.N, a.d, a.C, r, a.mu,
@@ -941,7 +1267,7 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     if (split_blocks > 0)
       launch_pdl(k_km_prep<T>, split_blocks, 256, 0, s, H, 0L, a.d, w.inv, 0, a.mu, n_mu,
-                 split_hi, split_lo, cd);
+                 split_hi, split_lo, cd, a.C, emax);
   }
   auto assign_pass = [&](float* scores) {
     switch (p.BN) {
@@ -972,7 +1298,39 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     if (e == cudaSuccess)
       e = launch_scan<T, false, true>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C,
                                       sp.W, a.mu, nullptr, nullptr, a.counts, a.chat, w.objp,
-                                      p.ntile, nullptr, a.iters + 1, a.iters, a.assign);
+                                      p.ntile, nullptr, a.iters + 1, a.iters, a.assign,
+                                      static_cast<const int32_t*>(nullptr),
+                                      static_cast<float*>(nullptr));
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  if (fast) {
+    const auto* Hb = static_cast<const __nv_bfloat16*>(a.H);
+    auto pass_fast = [&](int t) {
+      switch (p.BN) {
+        case 32: return assign_fast<32>(a, p, w, t, s);
+        case 64: return assign_fast<64>(a, p, w, t, s);
+        case 128: return assign_fast<128>(a, p, w, t, s);
+        default: return assign_fast<256>(a, p, w, t, s);
+      }
+    };
+    for (int t = 0; t <= a.iters; ++t) {
+      cudaError_t e = pass_fast(t);
+      if (e == cudaSuccess && t < a.iters)
+        e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
+                                  sp.W, a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp,
+                                  p.ntile, a.obj, a.iters + 1, t,
+                                  static_cast<const int32_t*>(nullptr),
+                                  static_cast<const int32_t*>(w.changed), w.emax);
+      if (e != cudaSuccess) return e;
+    }
+    launch_pdl(k_km_rho, std::min(ceil_div(BN_ * 32, 256), 8 * kSmTarget), 256, 0, s, Hb,
+               a.mu, BN_, a.N, a.d, a.C, a.assign, a.rho);
+    cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
+                                         a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
+                                         w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
+                                         static_cast<const int32_t*>(nullptr),
+                                         static_cast<const int32_t*>(w.changed),
+                                         static_cast<float*>(nullptr));
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   for (int t = 0; t <= a.iters; ++t) {
@@ -988,13 +1346,16 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
       e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
                                 sp.W, a.mu, p.tc ? w.mu_hi : nullptr, w.mu_lo, a.counts,
                                 a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t,
-                                static_cast<const int32_t*>(nullptr));
+                                static_cast<const int32_t*>(nullptr),
+                                static_cast<const int32_t*>(nullptr), static_cast<float*>(nullptr));
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
                                        a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
                                        w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
-                                       static_cast<const int32_t*>(nullptr));
+                                       static_cast<const int32_t*>(nullptr),
+                                       static_cast<const int32_t*>(nullptr),
+                                       static_cast<float*>(nullptr));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -105,6 +105,10 @@ struct TcCfg {
 //        epilogue's own and every CTA takes the whole K range)
 //   bool tile_range(int T, int* begin, int* end, int* step)  optional
 //        override of the CTA's tile walk (returns true when it applies)
+//   bool active(int t)             optional (not with kClusterReduce): false
+//        skips tile t in all three roles -- no copies, no MMAs, no
+//        epilogue call; read at the tile from memory that earlier kernels
+//        wrote, so every role sees the same answer
 //   void prefetch(uint8_t* scratch, int i, int n)  optional: run by the n
 //        epilogue threads (index i) before they wait for the first
 //        accumulator, to stage data the epilogue reads later into the
@@ -200,6 +204,9 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
       int it = 0;
       bool ok = true;
       for (int t = t_begin; ok && t < t_end; t += t_step) {
+        if constexpr (!Epi::kClusterReduce) {
+          if (!epi.active(t)) continue;
+        }
         const int arow = epi.arow(t);
         const int ahead = epi.ahead(t);
         const int bkoff = epi.bkoff(t);
@@ -253,7 +260,10 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     if (lane == 0) {
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int t = t_begin; ok && t < t_end; t += t_step, ++tcount) {
+      for (int t = t_begin; ok && t < t_end; t += t_step) {
+        if constexpr (!Epi::kClusterReduce) {
+          if (!epi.active(t)) continue;
+        }
         const int buf = tcount & 1;
         const uint32_t dacc = tmem + buf * BN;
         if (!tc::mbar_wait(acc_empty + buf, ((tcount >> 1) & 1) ^ 1, sh.status, abort_flag)) {
@@ -294,6 +304,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
         }
         if (!ok) break;
         tc::mma_commit(acc_full + buf);
+        ++tcount;
       }
       if (!ok) {  // wait for the MMAs already issued before TMEM is freed
         tc::mma_commit(drain);
@@ -310,7 +321,10 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
     epi.prefetch(epi_scratch, threadIdx.x - 64, 32 * Epi::kEpiWarps);
     typename Epi::State est;
     int tcount = 0;
-    for (int t = t_begin; t < t_end; t += t_step, ++tcount) {
+    for (int t = t_begin; t < t_end; t += t_step) {
+      if constexpr (!Epi::kClusterReduce) {
+        if (!epi.active(t)) continue;
+      }
       const int buf = tcount & 1;
       if (!tc::mbar_wait(acc_full + buf, (tcount >> 1) & 1, sh.status, abort_flag)) break;
       tc::fence_after_sync();
@@ -339,6 +353,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
         else
           epi.tile_done(t, r, n0, blockIdx.z, epi_scratch, est);
       }
+      ++tcount;
     }
   }
   // lanes 1..31 of the TMA and MMA warps wait for their lane 0 here, so each
@@ -367,6 +382,7 @@ struct TcEpiBase {
   static constexpr bool kClusterReduce = false;
   static constexpr bool kZSplitsK = true;
   __device__ bool tile_range(int, int*, int*, int*) const { return false; }
+  __device__ bool active(int) const { return true; }
   __device__ void prefetch(uint8_t*, int, int) const {}
   __device__ int ahead(int) const { return 0; }
   __device__ int bkoff(int) const { return 0; }

@@ -1,0 +1,123 @@
+"""The faster Lloyd passes (bf16 windows with at least one row tile per SM):
+scores against bf16 centroids with the rows near a tie decided again in fp32,
+and the early exit of windows whose labels have settled.  Both must leave
+every output equal to the oracle's run of all passes: labels and counts
+exact, centroids, rho, C_hat and every pass objective within 1e-4 / 1e-6.
+
+The windows here are many and small, so the oracle runs in seconds while the
+batch has more row tiles than the GPU has SMs (the condition for this form).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._parity import KM_MARGIN, assert_close, np_, run_kmeans
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(lib, monkeypatch):
+    monkeypatch.delenv("PS_KMEANS_LLOYD", raising=False)
+    return lib
+
+
+def _planted(B, N, d, planted, seed, spread=1.0):
+    g = torch.Generator().manual_seed(seed)
+    U = torch.randn(planted, d, generator=g)
+    U = U / U.norm(dim=1, keepdim=True)
+    z = torch.randint(0, planted, (B, N), generator=g)
+    eps = torch.randn(B, N, d, generator=g) * spread
+    H = (eps + (d ** 0.5) * U[z]) / (2.0 ** 0.5)
+    return H.to(torch.bfloat16)
+
+
+def _seeds(Hn, C, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([oracle.kmeanspp_init(Hn[b], C, rng.random(C))[0]
+                     for b in range(Hn.shape[0])]).astype(np.float32)
+
+
+def _check(g, Hn, mu0, iters, min_pinned=0.9, exact_ties=False):
+    """Every window whose passes are all clear of the tie band (or, with
+    exact_ties, every window: its only near-ties are exact ones, which both
+    sides give to the lower index) against the oracle's full run."""
+    pinned = 0
+    B = Hn.shape[0]
+    for b in range(B):
+        o = oracle.kmeans_spherical(Hn[b], mu0[b].astype(np.float64), iters)
+        if not exact_ties and o["margin"].min() <= KM_MARGIN:
+            continue
+        pinned += 1
+        assert np.array_equal(g["assign"][b], o["assign"]), b
+        assert np.array_equal(g["counts"][b], o["counts"]), b
+        assert_close(g["mu"][b], o["mu"], what=f"mu {b}")
+        assert_close(g["rho"][b], o["rho"], what=f"rho {b}")
+        assert_close(g["chat"][b], o["chat"], what=f"chat {b}")
+        assert_close(g["obj"][b], o["obj"], what=f"objective {b}")
+    assert pinned >= min_pinned * B, (pinned, B)
+    return pinned
+
+
+@pytest.mark.parametrize("B,N,d,C,iters,spread", [
+    (160, 128, 128, 16, 6, 1.0),     # one full tile per window
+    (80, 300, 96, 40, 5, 1.5),       # ragged last tile (300 = 2 x 128 + 44)
+    (64, 512, 256, 128, 8, 2.0),     # 128 centroids, noisier: later settling
+    (40, 640, 64, 200, 3, 1.0),      # C = 200 (256-wide score tile), few passes
+])
+def test_fast_passes_match_oracle(B, N, d, C, iters, spread):
+    H = _planted(B, N, d, C, seed=B * 7 + C, spread=spread)
+    Hn = H.float().numpy()
+    mu0 = _seeds(Hn, C, seed=C)
+    g = run_kmeans(H.cuda(), torch.from_numpy(mu0).cuda(), iters)
+    _check(g, Hn, mu0, iters)
+
+
+def test_fast_passes_warm_start_settles_early():
+    """A warm start from the previous step's centroids on slightly drifted
+    rows: the labels settle after a pass or two, every later pass is the
+    carried one, and the outputs equal the oracle's full run."""
+    B, N, d, C, iters = 160, 256, 128, 32, 15
+    H0 = _planted(B, N, d, C, seed=3)
+    Hn0 = H0.float().numpy()
+    mu0 = _seeds(Hn0, C, seed=4)
+    g0 = run_kmeans(H0.cuda(), torch.from_numpy(mu0).cuda(), iters)
+    gen = torch.Generator().manual_seed(5)
+    H1 = (H0.float() + 0.3 * torch.randn(H0.shape, generator=gen) *
+          (torch.rand(B, N, 1, generator=gen) < 0.05)).to(torch.bfloat16)
+    g1 = run_kmeans(H1.cuda(), torch.from_numpy(g0["mu"]).cuda(), iters)
+    pinned = _check(g1, H1.float().numpy(), g0["mu"], iters)
+    # settled: the objective stops moving well before the last pass
+    flat = (np.diff(g1["obj"], axis=1) == 0).sum(axis=1)
+    assert np.median(flat) >= iters - 5, flat
+    assert pinned == B
+
+
+def test_fast_passes_exact_ties_take_the_lower_cluster():
+    """Centroid 1 duplicates centroid 0 and centroids 20..31 are twelve
+    copies of one row: their members score exactly alike against the copies
+    (a tie in bf16 and in fp32), so the recheck decides them -- with more
+    than ten candidates for the twelve copies -- and, as the oracle, gives
+    the lowest index.  Every pass must match the oracle, ties included."""
+    B, N, d, C, iters = 160, 128, 64, 32, 2
+    H = _planted(B, N, d, 24, seed=11)
+    Hn = H.float().numpy()
+    mu0 = _seeds(Hn, C, seed=12)
+    mu0[:, 1] = mu0[:, 0]
+    mu0[:, 20:] = mu0[:, 20:21]
+    g = run_kmeans(H.cuda(), torch.from_numpy(mu0).cuda(), iters)
+    _check(g, Hn, mu0, iters, exact_ties=True)
+    # the copies never win: the lowest index takes every tie
+    assert not np.isin(g["assign"], [1] + list(range(21, 32))).any()
+
+
+def test_fast_passes_zero_rows():
+    B, N, d, C = 160, 128, 64, 8
+    H = _planted(B, N, d, C, seed=21)
+    H[:, 5] = 0
+    Hn = H.float().numpy()
+    mu0 = _seeds(Hn, C, seed=22)
+    g = run_kmeans(H.cuda(), torch.from_numpy(mu0).cuda(), 3)
+    assert np.all(g["assign"][:, 5] == 0) and np.all(g["rho"][:, 5] == 0)
+    _check(g, Hn, mu0, 3, exact_ties=True)
