@@ -54,6 +54,12 @@ def parse():
     ap.add_argument("--extra", default=EXTRA_WORKLOAD,
                     help="a second workload measured after the first and reported under "
                          "'extra' ('none' to skip)")
+    ap.add_argument("--op", choices=["kmeans", "nvfp4", "proxy", "topk", "refresh", "commit"],
+                    help="profiling mode: build one layer of the workload (--batch windows), "
+                         "then run this op --reps times on it and exit, printing nothing but a "
+                         "one-line summary (for a profiler to capture the op's kernels)")
+    ap.add_argument("--batch", type=int, default=0, help="windows per layer in --op mode")
+    ap.add_argument("--reps", type=int, default=3, help="calls of the op in --op mode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
                     help="skip the latency-hiding measurement (the drift step of one layer on "
@@ -208,7 +214,9 @@ def op_work(w, npos_mean):
 # kernel trace names (the library's kernels, as the CUDA runtime names them)
 # -> what they compute
 KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
-               ("KmAssign", "kmeans_assign"), ("k_km_argmax", "kmeans_argmax"),
+               ("KmAssign", "kmeans_assign"), ("KmFastEpi", "kmeans_assign"),
+               ("k_km_recheck", "kmeans_recheck"), ("k_km_rho", "kmeans_rho"),
+               ("k_km_argmax", "kmeans_argmax"),
                ("k_km_prep", "kmeans_prep"),
                ("k_kpp_gram", "kpp_gram"), ("k_kpp_pick", "kpp_pick"),
                ("k_kpp_weights", "kpp_weights"),
@@ -249,7 +257,8 @@ def kernel_work(key, w, npos_mean):
         "gram_gemm": (H + slab + (B * N * C * 4 if fused0 else 0),
                       B * (float(N) * (N + 1) * d + (2.0 * N * C * d if fused0 else 0.0))),
         "kmeans_passes": (slab + 2 * B * N * C * 4 + B * N * 12, 0.0),
-        "kmeans_assign": (H + B * C * d * 4, 2.0 * B * N * C * d),
+        "kmeans_assign": (H + B * C * d * 2, 2.0 * B * N * C * d),
+        "kmeans_rho": (H + B * N * 8, 2.0 * B * N * d),
         "kmeans_update": (H + B * C * d * 4, 0.0),
         "kmeans_final": (B * N * 4 + 2 * B * C * d * 4, 0.0),
         "nvfp4_amax": (H, 0.0),
@@ -519,19 +528,34 @@ def offload_rates(records, nsteps, w, npos_mean):
     return out
 
 
+# kernels whose launches take no work for windows whose k-means passes have
+# settled (the faster Lloyd passes skip them)
+EARLY_EXIT = ("kmeans_assign", "kmeans_update", "kmeans_recheck")
+
+
 def kernel_rooflines(records, nsteps, w, npos_mean, hbm, tf):
     """Per kernel: launches and time per step, average launch time and its
-    algorithmic roofline fraction."""
+    algorithmic roofline fraction.  For the k-means kernels with an early
+    exit, the per-launch work and time are those of the launches that did
+    work: a launch under a tenth of the kernel's longest one in the trace took
+    no tile (its windows had settled) and is counted apart; a launch whose
+    windows had partly settled counts as whole, so the fraction errs low."""
     agg = {}
     for name, ms in records:
         k = kernel_key(name)
-        a = agg.setdefault(k, [0, 0.0])
+        a = agg.setdefault(k, [0, 0.0, []])
         a[0] += 1
         a[1] += ms
+        a[2].append(ms)
     out = {}
-    for k, (n, ms) in agg.items():
+    for k, (n, ms, each) in agg.items():
         row = {"launches_per_step": n / nsteps, "us_per_step": 1e3 * ms / nsteps,
                "us_per_launch": 1e3 * ms / n}
+        if k in EARLY_EXIT:
+            busy = [x for x in each if x >= 0.1 * max(each)]
+            row["working_launches_per_step"] = len(busy) / nsteps
+            row["us_per_working_launch"] = 1e3 * sum(busy) / len(busy)
+            n, ms = len(busy), sum(busy)
         work = kernel_work(k, w, npos_mean)
         if work is not None:
             by, fl = work
@@ -974,8 +998,71 @@ def bench_workload(w, layers, args, dev, world, local, trace_steps=None):
     return res
 
 
+def run_op(args):
+    """--op mode: one layer of the workload with `--batch` windows; the
+    window is clustered from centroids drawn from its own rows (no k-means++
+    rounds, so few launches precede the captured ones), one whole step runs,
+    then the chosen op runs --reps times on the layer's state, each call
+    doing the work of a drifted step (k-means restarts from the same warm
+    centroids each time)."""
+    import dataclasses
+    import torch
+    from drift_aware_kv_spherical_gb300 import polestar as ps
+    from drift_aware_kv_spherical_gb300 import workloads as wl
+    from drift_aware_kv_spherical_gb300.pipeline import Pipeline
+    w = wl.BY_NAME[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
+    dev = torch.device("cuda", 0)
+    L = wl.make_layer(w, 0, dev)
+    H, Wk, Wv = L["H"], L["Wk"], L["Wv"]
+    Q = wl.make_queries(w, H, L["Wq"])
+    logits = wl.make_logits(w, 0, dev).to(wl.torch_dtype(w))
+    pipe = Pipeline(w, layers=1, device=dev)
+    st = pipe.state[0]
+    g = torch.Generator(device=dev).manual_seed(7)
+    rows = torch.randint(0, w.N, (w.B, w.C), generator=g, device=dev)
+    seed = torch.gather(H.float(), 1, rows[..., None].expand(-1, -1, w.d))
+    st.mu.copy_(seed / seed.norm(dim=2, keepdim=True))
+    pipe.t = 1
+    pipe.step([H], [Q], [Wk], [Wv], logits)       # A[1] and the clustering
+    wl.drift_inplace(w, H, Q, L["Wq"], 1)
+    pipe.t = 0
+    pipe.step([H], [Q], [Wk], [Wv], logits)       # A[0]: a previous distribution exists
+    torch.cuda.synchronize()
+    ps.ps_check()
+    mu0 = st.mu.clone()
+    cur, prev = st.A[1], st.A[0]
+    for _ in range(args.reps):
+        if args.op == "kmeans":
+            st.mu.copy_(mu0)
+            ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
+                                   objective=st.obj, ws=pipe.ws[ps.OP_KMEANS])
+        elif args.op == "nvfp4":
+            ps.ps_nvfp4_residual(H, st.mu, st.assign, st.rho, st.codes, st.scales, st.S,
+                                 ws=pipe.ws[ps.OP_NVFP4])
+        elif args.op == "proxy":
+            ps.ps_proxy_attn_kl(Q, st.chat, Wk, prev, cur, st.D, w.Hkv,
+                                ws=pipe.ws[ps.OP_PROXY_KL])
+        elif args.op == "topk":
+            ps.ps_topk_drift(st.D, st.assign, st.counts, w.k, st.sel, st.sel_score, st.pos,
+                             st.npos, st.posmask)
+        elif args.op == "refresh":
+            ps.ps_refresh_kv(H, st.pos, st.npos, Wk, Wv, st.Kc, st.Vc, w.Hkv, w.dh,
+                             ws=pipe.ws[ps.OP_REFRESH])
+        else:
+            pipe.commit_step(logits)
+    torch.cuda.synchronize()
+    ps.ps_check()
+    print(json.dumps({"op": args.op, "workload": w.name, "B": w.B, "reps": args.reps,
+                      "npos": int(st.npos.sum())}))
+
+
 def main():
     args = parse()
+    if args.op:
+        run_op(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -359,13 +359,21 @@ struct ProxyEpi : TcEpiBase {
     const int c0 = part * W;
     const uint32_t ta = taddr + c0;
     if constexpr (kReread) {  // scores re-read from TMEM in K-column chunks
-      constexpr int K = W > 64 ? 64 : 32;
+      // 16 columns a load while the head sum A[W] fills most registers
+      constexpr int K = W > 64 ? 64 : 16;
+      auto ld = [&](uint32_t at, uint32_t* raw) {
+        if constexpr (K == 16) {
+          tc::tmem_ld16_nowait(at, raw);
+        } else {
+#pragma unroll
+          for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(at + k, raw + k);
+        }
+      };
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int k0 = 0; k0 < W; k0 += K) {
         uint32_t raw[K];
-#pragma unroll
-        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
+        ld(ta + k0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < K; ++j)
@@ -380,17 +388,28 @@ struct ProxyEpi : TcEpiBase {
 #pragma unroll
         for (int q = 1; q < P; ++q) m = fmaxf(m, mx[r * P + q]);
       }
+      // each term's exp2 once: kept in the accumulator's own TMEM columns
+      // (this tile's scores are not read again) for the pass below
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k0 = 0; k0 < W; k0 += K) {
         uint32_t raw[K];
-#pragma unroll
-        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
+        ld(ta + k0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < K; ++j)
-          if (c0 + k0 + j < C) s4[j & 3] += exp2f(fmaf(__uint_as_float(raw[j]), sl, -m));
+        for (int j = 0; j < K; ++j) {
+          const float e = c0 + k0 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
+          s4[j & 3] += e;
+          raw[j] = __float_as_uint(e);
+        }
+        if constexpr (K == 16) {
+          tc::tmem_st16(ta + k0, raw);
+        } else {
+#pragma unroll
+          for (int k = 0; k < K; k += 32) tc::tmem_st32(ta + k0 + k, raw + k);
+        }
       }
+      tc::tmem_wait_st();
       float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       if constexpr (P > 1) {
         float* sm = mx + 128 * P;
@@ -404,14 +423,10 @@ struct ProxyEpi : TcEpiBase {
 #pragma unroll
       for (int k0 = 0; k0 < W; k0 += K) {
         uint32_t raw[K];
-#pragma unroll
-        for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(ta + k0 + k, raw + k);
+        ld(ta + k0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < K; ++j)
-          if (c0 + k0 + j < C)
-            st.A[k0 + j] =
-                fmaf(exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)), rs, st.A[k0 + j]);
+        for (int j = 0; j < K; ++j) st.A[k0 + j] = fmaf(__uint_as_float(raw[j]), rs, st.A[k0 + j]);
       }
     } else {
       uint32_t raw[W];
