@@ -8,8 +8,14 @@
 // is an IEEE fp32 operation with an explicit rounding (no contraction), so
 // the outputs are bit-exact functions of the inputs.
 //
-//   k_fp4_amax   per-CTA partial max |r| of each window (r recomputed)
+//   k_fp4_amax   partial max |r| of each unit of a window (r recomputed)
 //   k_fp4_quant  tensor scale, block scales and packed codes
+// Work units: a window's N d / 16 blocks of 16 elements in gx slots of
+// consecutive blocks, unit u = b gx + slot.  Both kernels run a persistent
+// grid that takes the units in order (CTA g: units g, g + G, ...), so the
+// CTAs work on one or two windows at a time and those windows' fp32
+// centroids, read once per element, stay in L2; each thread keeps two
+// blocks' loads in flight.
 // The residual r = fl(h - fl(rho * mu_a)) is recomputed in the second kernel
 // instead of being stored: re-reading h costs 2 B/element (bf16), storing r
 // would cost 8.
@@ -94,78 +100,123 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
   return r;
 }
 
+// Partials the scratch holds at most (the workspace-free entry point's
+// fixed array); a window gets gx <= kMaxParts / B of them.
+constexpr int kMaxParts = 16384;
+
+__device__ __forceinline__ void unit_blocks(long nblk, int gx, int slot, long* k0, long* k1) {
+  const long per = (nblk + gx - 1) / gx;
+  *k0 = min(nblk, (long)slot * per);
+  *k1 = min(nblk, *k0 + per);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
            const int32_t* __restrict__ assign, const float* __restrict__ rho,
-           int N, int d, int C, float* __restrict__ part) {
+           int B, int N, int d, int C, int gx, float* __restrict__ part) {
   pdl_prologue();
   __shared__ float s_red[kThreads / 32];
-  const int b = blockIdx.y;
   const int bpr = d / 16;
   const long nblk = (long)N * bpr;
-  float m = 0.f;
-  for (long blk = (long)blockIdx.x * kThreads + threadIdx.x; blk < nblk;
-       blk += (long)gridDim.x * kThreads) {
-    const int row = (int)(blk / bpr), col = (int)(blk % bpr) * 16;
-    float r[16];
-    residual16(H, mu, assign, rho, b, N, d, C, row, col, r);
+  const long units = (long)B * gx;
+  for (long u = blockIdx.x; u < units; u += gridDim.x) {  // CTA-uniform
+    const int b = (int)(u / gx);
+    long k0, k1;
+    unit_blocks(nblk, gx, (int)(u % gx), &k0, &k1);
+    float m = 0.f;
+    long blk = k0 + threadIdx.x;
+    for (; blk + kThreads < k1; blk += 2 * kThreads) {
+      float r0[16], r1[16];
+      residual16(H, mu, assign, rho, b, N, d, C, (int)(blk / bpr), (int)(blk % bpr) * 16, r0);
+      const long b2 = blk + kThreads;
+      residual16(H, mu, assign, rho, b, N, d, C, (int)(b2 / bpr), (int)(b2 % bpr) * 16, r1);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r[e]));
+      for (int e = 0; e < 16; ++e) m = fmaxf(m, fmaxf(fabsf(r0[e]), fabsf(r1[e])));
+    }
+    if (blk < k1) {
+      float r0[16];
+      residual16(H, mu, assign, rho, b, N, d, C, (int)(blk / bpr), (int)(blk % bpr) * 16, r0);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r0[e]));
+    }
+    m = block_max(m, s_red);
+    if (threadIdx.x == 0) part[u] = m;
   }
-  m = block_max(m, s_red);
-  if (threadIdx.x == 0) part[(long)b * gridDim.x + blockIdx.x] = m;
+}
+
+// One 16-element block: its E4M3 scale and eight bytes of E2M1 codes.
+__device__ __forceinline__ void quant_block(const float* r, float S, float six_s,
+                                            uint8_t* __restrict__ codes,
+                                            uint8_t* __restrict__ scales, long rowbase, int d,
+                                            int col) {
+  float bm = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) bm = fmaxf(bm, fabsf(r[e]));
+  const uint32_t sc = e4m3_code(__fdiv_rn(bm, six_s));
+  const float sb = e4m3_value(sc);
+  uint2 q = make_uint2(0u, 0u);
+  if (sb != 0.f) {
+    const float den = __fmul_rn(sb, S);
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __fdiv_rn(r[e], den);
+    q.x = e2m1x8(v);
+    q.y = e2m1x8(v + 8);
+  }
+  *reinterpret_cast<uint2*>(codes + rowbase * (d / 2) + col / 2) = q;
+  scales[rowbase * (d / 16) + col / 16] = (uint8_t)sc;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_fp4_quant(const T* __restrict__ H, const float* __restrict__ mu,
             const int32_t* __restrict__ assign, const float* __restrict__ rho,
-            int N, int d, int C, const float* __restrict__ part, int nparts,
+            int B, int N, int d, int C, int gx, const float* __restrict__ part,
             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
             float* __restrict__ S_out) {
   pdl_prologue();
   __shared__ float s_red[kThreads / 32];
-  const int b = blockIdx.y;
-  float amax = 0.f;
-  for (int p = threadIdx.x; p < nparts; p += kThreads)
-    amax = fmaxf(amax, part[(long)b * nparts + p]);
-  amax = block_max(amax, s_red);
-  const float S = (amax > 0.f && amax <= FLT_MAX)
-                      ? fmaxf(__fdiv_rn(amax, 2688.0f), FLT_MIN) : 1.0f;
-  if (blockIdx.x == 0 && threadIdx.x == 0) S_out[b] = S;
-  const float six_s = __fmul_rn(6.0f, S);
   const int bpr = d / 16;
   const long nblk = (long)N * bpr;
-  for (long blk = (long)blockIdx.x * kThreads + threadIdx.x; blk < nblk;
-       blk += (long)gridDim.x * kThreads) {
-    const int row = (int)(blk / bpr), col = (int)(blk % bpr) * 16;
-    float r[16];
-    residual16(H, mu, assign, rho, b, N, d, C, row, col, r);
-    float bm = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) bm = fmaxf(bm, fabsf(r[e]));
-    const uint32_t sc = e4m3_code(__fdiv_rn(bm, six_s));
-    const float sb = e4m3_value(sc);
-    uint2 q = make_uint2(0u, 0u);
-    if (sb != 0.f) {
-      const float den = __fmul_rn(sb, S);
-      float v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __fdiv_rn(r[e], den);
-      q.x = e2m1x8(v);
-      q.y = e2m1x8(v + 8);
+  const long units = (long)B * gx;
+  for (long u = blockIdx.x; u < units; u += gridDim.x) {  // CTA-uniform
+    const int b = (int)(u / gx), slot = (int)(u % gx);
+    float amax = 0.f;
+    for (int p = threadIdx.x; p < gx; p += kThreads) amax = fmaxf(amax, part[(long)b * gx + p]);
+    amax = block_max(amax, s_red);
+    const float S = (amax > 0.f && amax <= FLT_MAX)
+                        ? fmaxf(__fdiv_rn(amax, 2688.0f), FLT_MIN) : 1.0f;
+    if (slot == 0 && threadIdx.x == 0) S_out[b] = S;
+    const float six_s = __fmul_rn(6.0f, S);
+    long k0, k1;
+    unit_blocks(nblk, gx, slot, &k0, &k1);
+    long blk = k0 + threadIdx.x;
+    for (; blk + kThreads < k1; blk += 2 * kThreads) {
+      float r0[16], r1[16];
+      const int row0 = (int)(blk / bpr), col0 = (int)(blk % bpr) * 16;
+      const long b2 = blk + kThreads;
+      const int row1 = (int)(b2 / bpr), col1 = (int)(b2 % bpr) * 16;
+      residual16(H, mu, assign, rho, b, N, d, C, row0, col0, r0);
+      residual16(H, mu, assign, rho, b, N, d, C, row1, col1, r1);
+      quant_block(r0, S, six_s, codes, scales, (long)b * N + row0, d, col0);
+      quant_block(r1, S, six_s, codes, scales, (long)b * N + row1, d, col1);
     }
-    const long rowbase = (long)b * N + row;
-    *reinterpret_cast<uint2*>(codes + rowbase * (d / 2) + col / 2) = q;
-    scales[rowbase * bpr + col / 16] = (uint8_t)sc;
+    if (blk < k1) {
+      float r0[16];
+      const int row0 = (int)(blk / bpr), col0 = (int)(blk % bpr) * 16;
+      residual16(H, mu, assign, rho, b, N, d, C, row0, col0, r0);
+      quant_block(r0, S, six_s, codes, scales, (long)b * N + row0, d, col0);
+    }
   }
 }
 
+// Slots per window: enough for one block per thread, at most kMaxParts / B
+// (so B gx partials fit the fixed array for every B <= kMaxParts).
 int grid_x(int B, int N, int d) {
   const long nblk = (long)N * (d / 16);
   const int want = ceil_div(nblk, kThreads);
-  const int cap = std::max(1, 4 * kSmTarget / std::max(B, 1));
+  const int cap = std::max(1, kMaxParts / std::max(B, 1));
   return std::max(1, std::min(want, cap));
 }
 
@@ -174,11 +225,12 @@ cudaError_t run_typed(const Nvfp4Args& a, cudaStream_t s) {
   const T* H = static_cast<const T*>(a.H);
   const int gx = grid_x(a.B, a.N, a.d);
   float* part = Carver(a.ws).take<float>((size_t)a.B * gx);
-  const dim3 grid(gx, a.B);
-  launch_pdl(k_fp4_amax<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.N, a.d,
-                                          a.C, part);
-  launch_pdl(k_fp4_quant<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.N, a.d,
-                                           a.C, part, gx, a.codes, a.scales, a.S);
+  const long units = (long)a.B * gx;
+  const int grid = (int)std::min<long>(units, 4L * (a.num_sms > 0 ? a.num_sms : kSmTarget));
+  launch_pdl(k_fp4_amax<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
+             a.C, gx, part);
+  launch_pdl(k_fp4_quant<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
+             a.C, gx, part, a.codes, a.scales, a.S);
   return cudaGetLastError();
 }
 
@@ -205,7 +257,7 @@ cudaError_t nvfp4_run(const Nvfp4Args& a, cudaStream_t s) {
 // keeps this array until the process exits.
 namespace {
 
-constexpr int kStaticParts = 16384;  // floats = 64 KiB; fits B <= 16384
+constexpr int kStaticParts = kMaxParts;  // floats = 64 KiB; fits B <= 16384
 static __device__ __align__(256) float g_nvfp4_static_parts[kStaticParts];
 
 std::mutex g_static_mu;

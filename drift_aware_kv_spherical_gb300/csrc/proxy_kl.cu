@@ -322,9 +322,10 @@ template <int BN, int P>
 struct ProxyEpi : TcEpiBase {
   static constexpr int kEpiWarps = 4 * P;
   static constexpr int W = BN / P;  // columns per thread
-  // scores kept in registers only while they fit: above 64 columns, or with
-  // 16 epilogue warps (576 threads, <= 113 registers each), TMEM is re-read
-  static constexpr bool kReread = W > 64 || P >= 4;
+  // scores kept in registers only while they fit next to the head sum A[W]:
+  // with more than one epilogue warp per lane quarter (W = 64 columns of
+  // scores, exponentials and sums at once would not), TMEM is re-read
+  static constexpr bool kReread = W > 64 || P >= 2;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   int B, N, C, Hq, G, dh, mtb, hps, nslice;
@@ -359,17 +360,17 @@ struct ProxyEpi : TcEpiBase {
     const int c0 = part * W;
     const uint32_t ta = taddr + c0;
     if constexpr (kReread) {  // scores re-read from TMEM in K-column chunks
-      // 16 columns a load while the head sum A[W] fills most registers
-      constexpr int K = W > 64 ? 64 : 16;
+      // 8 columns a load while the head sum A[W] fills most registers
+      constexpr int K = W > 64 ? 64 : 8;
       auto ld = [&](uint32_t at, uint32_t* raw) {
-        if constexpr (K == 16) {
-          tc::tmem_ld16_nowait(at, raw);
+        if constexpr (K == 8) {
+          tc::tmem_ld8_nowait(at, raw);
         } else {
 #pragma unroll
           for (int k = 0; k < K; k += 32) tc::tmem_ld32_nowait(at + k, raw + k);
         }
       };
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int k0 = 0; k0 < W; k0 += K) {
         uint32_t raw[K];
@@ -377,9 +378,9 @@ struct ProxyEpi : TcEpiBase {
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < K; ++j)
-          if (c0 + k0 + j < C) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(raw[j]) * sl);
+          if (c0 + k0 + j < C) m2[j & 1] = fmaxf(m2[j & 1], __uint_as_float(raw[j]) * sl);
       }
-      float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float m = fmaxf(m2[0], m2[1]);
       float* mx = xs + (h & 1) * (2 * 128 * P);
       if constexpr (P > 1) {
         mx[r * P + part] = m;
@@ -390,7 +391,7 @@ struct ProxyEpi : TcEpiBase {
       }
       // each term's exp2 once: kept in the accumulator's own TMEM columns
       // (this tile's scores are not read again) for the pass below
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      float s2[2] = {0.f, 0.f};
 #pragma unroll
       for (int k0 = 0; k0 < W; k0 += K) {
         uint32_t raw[K];
@@ -399,18 +400,18 @@ struct ProxyEpi : TcEpiBase {
 #pragma unroll
         for (int j = 0; j < K; ++j) {
           const float e = c0 + k0 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
-          s4[j & 3] += e;
+          s2[j & 1] += e;
           raw[j] = __float_as_uint(e);
         }
-        if constexpr (K == 16) {
-          tc::tmem_st16(ta + k0, raw);
+        if constexpr (K == 8) {
+          tc::tmem_st8(ta + k0, raw);
         } else {
 #pragma unroll
           for (int k = 0; k < K; k += 32) tc::tmem_st32(ta + k0 + k, raw + k);
         }
       }
       tc::tmem_wait_st();
-      float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      float sum = s2[0] + s2[1];
       if constexpr (P > 1) {
         float* sm = mx + 128 * P;
         sm[r * P + part] = sum;

@@ -123,8 +123,8 @@ struct TcCfg {
 //        tc::cluster_arrive() exactly once, uniformly, after its last read
 //        of another CTA's shared memory (the CTA waits before leaving)
 template <int BN, int NA, int NB, bool B_MN, class Epi>
-__global__ void __launch_bounds__(64 + 32 * Epi::kEpiWarps, 1)
-k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
+__device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& sh,
+                                             const Epi& epi) {
   // k-blocks go through the ring KS at a time; a chunk with an odd count
   // loads one k-block past its end (out of range, or the next chunk's) into
   // its last stage and issues no MMA for it
@@ -152,8 +152,13 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   const int M = sh.M_dev != nullptr ? min(*sh.M_dev, sh.M) : sh.M;
   const bool ksplit = Epi::kZSplitsK && M <= sh.split_max_rows;
   const int T_all = epi.tiles(M);
-  const int T = (ksplit || blockIdx.z == 0 || !Epi::kZSplitsK) ? T_all : 0;
-  int t_begin = blockIdx.y, t_end = T, t_step = gridDim.y;
+  // K not split although the grid has K chunks (the rows outgrew
+  // split_max_rows, known only on the device): the gridDim.z CTAs of a
+  // column tile take turns on the row tiles instead of idling
+  const bool zrows = Epi::kZSplitsK && !ksplit && gridDim.z > 1;
+  const int T = T_all;
+  int t_begin = zrows ? (int)(blockIdx.y + blockIdx.z * gridDim.y) : (int)blockIdx.y;
+  int t_end = T, t_step = zrows ? (int)(gridDim.y * gridDim.z) : (int)gridDim.y;
   if constexpr (Epi::kBlocked) {
     const int per = (T + gridDim.y - 1) / gridDim.y;
     t_begin = blockIdx.y * per;
@@ -374,6 +379,22 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   if constexpr (Epi::kClusterReduce) tc::cluster_wait();
 }
 
+template <int BN, int NA, int NB, bool B_MN, class Epi>
+__global__ void __launch_bounds__(64 + 32 * Epi::kEpiWarps, 1)
+k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
+  tc_gemm_body<BN, NA, NB, B_MN, Epi>(maps, sh, epi);
+}
+
+// The same kernel for 16 epilogue warps (576 threads): a register limit of
+// 112 a thread (18 warps x 112 x 32 fills 64512 of the SM's 65536) in place
+// of the launch bound, under which the compiler settles for 96 and spills
+// the epilogue's per-row state.
+template <int BN, int NA, int NB, bool B_MN, class Epi>
+__global__ void __maxnreg__(112)
+k_tc_gemm_w16(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
+  tc_gemm_body<BN, NA, NB, B_MN, Epi>(maps, sh, epi);
+}
+
 // Plain epilogue base: 2-D maps, strided tiles, no B offset, one b map.
 struct TcEpiBase {
   static constexpr int kEpiWarps = 4;
@@ -448,7 +469,13 @@ template <int BN, int NA, int NB, bool B_MN, class Epi>
 cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi, dim3 grid,
                            cudaStream_t s) {
   using Cfg = TcCfg<BN, NA, NB, B_MN>;
-  auto kern = k_tc_gemm<BN, NA, NB, B_MN, Epi>;
+  static_assert(Epi::kEpiWarps <= 16, "at most 16 epilogue warps");
+  auto kern = [] {
+    if constexpr (Epi::kEpiWarps == 16)
+      return k_tc_gemm_w16<BN, NA, NB, B_MN, Epi>;
+    else
+      return k_tc_gemm<BN, NA, NB, B_MN, Epi>;
+  }();
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

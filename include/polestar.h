@@ -341,7 +341,8 @@ ps_status ps_commit(ps_handle h, const void* logits, int dtype, int B, int P, in
  * which every GPU that loads the library keeps until the process exits.
  * It calls no cudaMalloc, cudaFree or allocating library routine.
  *
- * Limit: B <= 16384 (the array holds at most max(608, B) partials);
+ * Limit: B <= 16384 (the array holds 16384 partials; a window takes at
+ * most 16384 / B of them);
  * larger B returns PS_ERR_WORKSPACE and launches nothing.
  * Device: the handle's device must be the calling thread's current device
  * (PS_ERR_ARG otherwise), since the array's address differs per device.
