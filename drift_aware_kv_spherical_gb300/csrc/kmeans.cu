@@ -303,10 +303,10 @@ k_assign(const T* __restrict__ H, const float* __restrict__ mu,
 // Set-up of a call, in one launch: blocks [0, inv_blocks) take 1/||h_i||
 // for 8 rows each (a warp per row, its 16-byte loads unrolled four deep);
 // the rest split mu (fp32) into bf16 hi + lo parts (hi = bf16(mu), lo =
-// bf16(mu - hi)), a warp per centroid row, four values per lane at a time,
-// into two [B][C][d] arrays or (cd = C d > 0) one [B][2C][d] array at hi.
-// Either part may be empty.  emax (nullable, [B], zeroed by the caller):
-// raised to ||mu_c - hi_c|| of every centroid of window b (fp32 bits
+// bf16(mu - hi)), four values per thread (a warp per centroid row when emax
+// is wanted), into two [B][C][d] arrays or (cd = C d > 0) one [B][2C][d]
+// array at hi.  Either part may be empty.  emax (nullable, [B], zeroed by the
+// caller): raised to ||mu_c - hi_c|| of every centroid of window b (fp32 bits
 // compared as integers, which orders non-negative floats, so the result does
 // not depend on the order of the updates).
 template <typename T>
@@ -331,6 +331,27 @@ k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, in
     }
     ss = warp_sum(ss);
     if (lane == 0) inv[row] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    return;
+  }
+  if (emax == nullptr) {  // no bound wanted: element-wise, four values a thread
+    const long n4 = n_mu >> 2;  // n_mu = B * C * d, a multiple of 16
+    const long stride = (long)(gridDim.x - inv_blocks) * blockDim.x;
+    for (long i = (long)(blockIdx.x - inv_blocks) * blockDim.x + threadIdx.x; i < n4;
+         i += stride) {
+      const long e = 4 * i;
+      const long eh = cd > 0 ? (e / cd) * 2 * cd + e % cd : e;
+      const long el = cd > 0 ? eh + cd : e;
+      const float4 x = reinterpret_cast<const float4*>(mu)[i];
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
+      *reinterpret_cast<uint2*>(hi + eh) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                      *reinterpret_cast<const uint32_t*>(&h1));
+      *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
+                                                      *reinterpret_cast<const uint32_t*>(&l1));
+    }
     return;
   }
   const long nrow = n_mu / d;  // n_mu = B * C * d, d a multiple of 16

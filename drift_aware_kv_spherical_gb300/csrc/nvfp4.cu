@@ -10,12 +10,13 @@
 //
 //   k_fp4_amax   partial max |r| of each unit of a window (r recomputed)
 //   k_fp4_quant  tensor scale, block scales and packed codes
-// Work units: a window's N d / 16 blocks of 16 elements in gx slots of
-// consecutive blocks, unit u = b gx + slot.  Both kernels run a persistent
-// grid that takes the units in order (CTA g: units g, g + G, ...), so the
-// CTAs work on one or two windows at a time and those windows' fp32
-// centroids, read once per element, stay in L2; each thread keeps two
-// blocks' loads in flight.
+// Work units: a window's rows in gx slots of consecutive rows, unit u =
+// b gx + slot.  Both kernels run a persistent grid that takes the units in
+// order (CTA g: units g, g + G, ...), so the CTAs work on one or two windows
+// at a time and those windows' fp32 centroids, read once per element, stay
+// in L2.  A warp takes a row: its label, rho and centroid row are looked up
+// once, and lane j takes the row's 16-element blocks j, j + 32, ..., so every
+// block's loads are independent of the others.
 // The residual r = fl(h - fl(rho * mu_a)) is recomputed in the second kernel
 // instead of being stored: re-reading h costs 2 B/element (bf16), storing r
 // would cost 8.
@@ -64,29 +65,36 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// r[0..15] for block `col` of row `row` of window b.
+// r[0..15] of the block at h (16 elements of a row) against the matching 16
+// centroid values at m (nullptr: r = h) and the row's rho.
 template <typename T>
-__device__ __forceinline__ void residual16(const T* __restrict__ H,
-                                           const float* __restrict__ mu,
-                                           const int32_t* __restrict__ assign,
-                                           const float* __restrict__ rho,
-                                           int b, int N, int d, int C, int row,
-                                           int col, float* r) {
-  const T* h = H + ((long)b * N + row) * d + col;
+__device__ __forceinline__ void residual16(const T* __restrict__ h, const float* __restrict__ m,
+                                           float rh, float* r) {
   constexpr int V = Vec<T>::n;
 #pragma unroll
   for (int q = 0; q < 16 / V; ++q) load16(h + q * V, r + q * V);
-  if (mu != nullptr) {
-    int a = assign[(long)b * N + row];
-    a = min(max(a, 0), C - 1);
-    const float rh = rho[(long)b * N + row];
-    const float* m = mu + ((long)b * C + a) * d + col;
+  if (m != nullptr) {
     float mv[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) load16(m + 4 * q, mv + 4 * q);
 #pragma unroll
     for (int e = 0; e < 16; ++e) r[e] = __fsub_rn(r[e], __fmul_rn(rh, mv[e]));
   }
+}
+
+// The row's centroid (nullptr when H itself is quantised) and rho.
+__device__ __forceinline__ const float* row_centroid(const float* __restrict__ mu,
+                                                     const int32_t* __restrict__ assign,
+                                                     const float* __restrict__ rho, int b,
+                                                     int N, int d, int C, int row, float* rh) {
+  if (mu == nullptr) {
+    *rh = 0.f;
+    return nullptr;
+  }
+  const long i = (long)b * N + row;
+  const int a = min(max(assign[i], 0), C - 1);
+  *rh = rho[i];
+  return mu + ((long)b * C + a) * d;
 }
 
 __device__ __forceinline__ float block_max(float v, float* scratch) {
@@ -104,10 +112,10 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
 // fixed array); a window gets gx <= kMaxParts / B of them.
 constexpr int kMaxParts = 16384;
 
-__device__ __forceinline__ void unit_blocks(long nblk, int gx, int slot, long* k0, long* k1) {
-  const long per = (nblk + gx - 1) / gx;
-  *k0 = min(nblk, (long)slot * per);
-  *k1 = min(nblk, *k0 + per);
+__device__ __forceinline__ void unit_rows(int N, int gx, int slot, int* r0, int* r1) {
+  const int per = (N + gx - 1) / gx;
+  *r0 = min(N, slot * per);
+  *r1 = min(N, *r0 + per);
 }
 
 template <typename T>
@@ -117,28 +125,25 @@ k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
            int B, int N, int d, int C, int gx, float* __restrict__ part) {
   pdl_prologue();
   __shared__ float s_red[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int bpr = d / 16;
-  const long nblk = (long)N * bpr;
   const long units = (long)B * gx;
   for (long u = blockIdx.x; u < units; u += gridDim.x) {  // CTA-uniform
     const int b = (int)(u / gx);
-    long k0, k1;
-    unit_blocks(nblk, gx, (int)(u % gx), &k0, &k1);
+    int r0, r1;
+    unit_rows(N, gx, (int)(u % gx), &r0, &r1);
     float m = 0.f;
-    long blk = k0 + threadIdx.x;
-    for (; blk + kThreads < k1; blk += 2 * kThreads) {
-      float r0[16], r1[16];
-      residual16(H, mu, assign, rho, b, N, d, C, (int)(blk / bpr), (int)(blk % bpr) * 16, r0);
-      const long b2 = blk + kThreads;
-      residual16(H, mu, assign, rho, b, N, d, C, (int)(b2 / bpr), (int)(b2 % bpr) * 16, r1);
+    for (int row = r0 + warp; row < r1; row += kThreads / 32) {
+      float rh;
+      const float* mrow = row_centroid(mu, assign, rho, b, N, d, C, row, &rh);
+      const T* hrow = H + ((long)b * N + row) * d;
+#pragma unroll 2
+      for (int k = lane; k < bpr; k += 32) {
+        float r[16];
+        residual16(hrow + k * 16, mrow != nullptr ? mrow + k * 16 : nullptr, rh, r);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) m = fmaxf(m, fmaxf(fabsf(r0[e]), fabsf(r1[e])));
-    }
-    if (blk < k1) {
-      float r0[16];
-      residual16(H, mu, assign, rho, b, N, d, C, (int)(blk / bpr), (int)(blk % bpr) * 16, r0);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r0[e]));
+        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r[e]));
+      }
     }
     m = block_max(m, s_red);
     if (threadIdx.x == 0) part[u] = m;
@@ -147,9 +152,8 @@ k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
 
 // One 16-element block: its E4M3 scale and eight bytes of E2M1 codes.
 __device__ __forceinline__ void quant_block(const float* r, float S, float six_s,
-                                            uint8_t* __restrict__ codes,
-                                            uint8_t* __restrict__ scales, long rowbase, int d,
-                                            int col) {
+                                            uint8_t* __restrict__ codes_at,
+                                            uint8_t* __restrict__ scale_at) {
   float bm = 0.f;
 #pragma unroll
   for (int e = 0; e < 16; ++e) bm = fmaxf(bm, fabsf(r[e]));
@@ -164,8 +168,8 @@ __device__ __forceinline__ void quant_block(const float* r, float S, float six_s
     q.x = e2m1x8(v);
     q.y = e2m1x8(v + 8);
   }
-  *reinterpret_cast<uint2*>(codes + rowbase * (d / 2) + col / 2) = q;
-  scales[rowbase * (d / 16) + col / 16] = (uint8_t)sc;
+  *reinterpret_cast<uint2*>(codes_at) = q;
+  *scale_at = (uint8_t)sc;
 }
 
 template <typename T>
@@ -177,8 +181,8 @@ k_fp4_quant(const T* __restrict__ H, const float* __restrict__ mu,
             float* __restrict__ S_out) {
   pdl_prologue();
   __shared__ float s_red[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int bpr = d / 16;
-  const long nblk = (long)N * bpr;
   const long units = (long)B * gx;
   for (long u = blockIdx.x; u < units; u += gridDim.x) {  // CTA-uniform
     const int b = (int)(u / gx), slot = (int)(u % gx);
@@ -189,33 +193,43 @@ k_fp4_quant(const T* __restrict__ H, const float* __restrict__ mu,
                         ? fmaxf(__fdiv_rn(amax, 2688.0f), FLT_MIN) : 1.0f;
     if (slot == 0 && threadIdx.x == 0) S_out[b] = S;
     const float six_s = __fmul_rn(6.0f, S);
-    long k0, k1;
-    unit_blocks(nblk, gx, slot, &k0, &k1);
-    long blk = k0 + threadIdx.x;
-    for (; blk + kThreads < k1; blk += 2 * kThreads) {
-      float r0[16], r1[16];
-      const int row0 = (int)(blk / bpr), col0 = (int)(blk % bpr) * 16;
-      const long b2 = blk + kThreads;
-      const int row1 = (int)(b2 / bpr), col1 = (int)(b2 % bpr) * 16;
-      residual16(H, mu, assign, rho, b, N, d, C, row0, col0, r0);
-      residual16(H, mu, assign, rho, b, N, d, C, row1, col1, r1);
-      quant_block(r0, S, six_s, codes, scales, (long)b * N + row0, d, col0);
-      quant_block(r1, S, six_s, codes, scales, (long)b * N + row1, d, col1);
-    }
-    if (blk < k1) {
-      float r0[16];
-      const int row0 = (int)(blk / bpr), col0 = (int)(blk % bpr) * 16;
-      residual16(H, mu, assign, rho, b, N, d, C, row0, col0, r0);
-      quant_block(r0, S, six_s, codes, scales, (long)b * N + row0, d, col0);
+    int r0, r1;
+    unit_rows(N, gx, slot, &r0, &r1);
+    for (int row = r0 + warp; row < r1; row += kThreads / 32) {
+      float rh;
+      const float* mrow = row_centroid(mu, assign, rho, b, N, d, C, row, &rh);
+      const long rowbase = (long)b * N + row;
+      const T* hrow = H + rowbase * d;
+      for (int k = lane; k < bpr; k += 32) {
+        float r[16];
+        residual16(hrow + k * 16, mrow != nullptr ? mrow + k * 16 : nullptr, rh, r);
+        quant_block(r, S, six_s, codes + rowbase * (d / 2) + k * 8, scales + rowbase * bpr + k);
+      }
     }
   }
 }
 
-// Slots per window: enough for one block per thread, at most kMaxParts / B
-// (so B gx partials fit the fixed array for every B <= kMaxParts).
+// CTAs of `threads` threads an SM holds at once: the occupancy query, made
+// once per kernel type (each kernel here has a type of its own); 1 if it
+// fails.
+template <typename K>
+int resident_ctas(K kern, int threads) {
+  static const int n = [&] {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, 0) != cudaSuccess) {
+      cudaGetLastError();
+      v = 1;
+    }
+    return std::max(1, v);
+  }();
+  return n;
+}
+
+// Slots per window: one row per warp of a CTA, at most kMaxParts / B (so
+// B gx partials fit the fixed array for every B <= kMaxParts).
 int grid_x(int B, int N, int d) {
-  const long nblk = (long)N * (d / 16);
-  const int want = ceil_div(nblk, kThreads);
+  (void)d;
+  const int want = ceil_div(N, kThreads / 32);
   const int cap = std::max(1, kMaxParts / std::max(B, 1));
   return std::max(1, std::min(want, cap));
 }
@@ -226,10 +240,13 @@ cudaError_t run_typed(const Nvfp4Args& a, cudaStream_t s) {
   const int gx = grid_x(a.B, a.N, a.d);
   float* part = Carver(a.ws).take<float>((size_t)a.B * gx);
   const long units = (long)a.B * gx;
-  const int grid = (int)std::min<long>(units, 4L * (a.num_sms > 0 ? a.num_sms : kSmTarget));
-  launch_pdl(k_fp4_amax<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
+  // persistent grids: as many CTAs as the SMs hold at once, no second wave
+  const int sms = a.num_sms > 0 ? a.num_sms : kSmTarget;
+  const int g1 = (int)std::min<long>(units, (long)resident_ctas(k_fp4_amax<T>, kThreads) * sms);
+  const int g2 = (int)std::min<long>(units, (long)resident_ctas(k_fp4_quant<T>, kThreads) * sms);
+  launch_pdl(k_fp4_amax<T>, g1, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
              a.C, gx, part);
-  launch_pdl(k_fp4_quant<T>, grid, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
+  launch_pdl(k_fp4_quant<T>, g2, kThreads, 0, s, H, a.mu, a.assign, a.rho, a.B, a.N, a.d,
              a.C, gx, part, a.codes, a.scales, a.S);
   return cudaGetLastError();
 }

@@ -263,9 +263,22 @@ struct CkeysEpi : TcEpiBase {
       float v[32];
       tc::tmem_ld32(taddr + c0, v);
       if (m >= M) continue;
-      const long o = (long)m * nkv + n0 + c0;
+      const long o = (long)m * nkv + n0 + c0;  // a multiple of 32 elements
 #pragma unroll
-      for (int j = 0; j < 32; ++j) split_store(khi + o + j, klo + o + j, v[j]);
+      for (int j = 0; j < 32; j += 8) {  // 8 values: one 16-byte store each for hi and lo
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __nv_bfloat162 hb = __floats2bfloat162_rn(v[j + 2 * q], v[j + 2 * q + 1]);
+          const float2 hf = __bfloat1622float2(hb);
+          const __nv_bfloat162 lb =
+              __floats2bfloat162_rn(v[j + 2 * q] - hf.x, v[j + 2 * q + 1] - hf.y);
+          h[q] = *reinterpret_cast<const uint32_t*>(&hb);
+          l[q] = *reinterpret_cast<const uint32_t*>(&lb);
+        }
+        *reinterpret_cast<uint4*>(khi + o + j) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(klo + o + j) = make_uint4(l[0], l[1], l[2], l[3]);
+      }
     }
   }
 };
@@ -361,7 +374,7 @@ struct ProxyEpi : TcEpiBase {
     const uint32_t ta = taddr + c0;
     if constexpr (kReread) {  // scores re-read from TMEM in K-column chunks
       // 8 columns a load while the head sum A[W] fills most registers
-      constexpr int K = W > 64 ? 64 : 8;
+      constexpr int K = 8;
       auto ld = [&](uint32_t at, uint32_t* raw) {
         if constexpr (K == 8) {
           tc::tmem_ld8_nowait(at, raw);
@@ -519,6 +532,170 @@ struct ProxyEpi : TcEpiBase {
                                  State& st) const {
     finish(t, r, part, reinterpret_cast<float*>(scratch), st);
   }
+};
+
+// Proxy epilogue with the head sum in TMEM, for one CTA per row tile taking
+// all its heads (enough row tiles to fill the GPU).  A head's BN score
+// columns come in NP parts of BN_T = BN / NP columns (NP = 2 when BN = 256),
+// each its own tile, so the two accumulator buffers (2 BN_T columns) and
+// the head sum A (BN columns, fp32) fit the 512 TMEM columns.  One epilogue
+// thread per row (4 warps), with no exchange between warps:
+//   part 0: its scores, their max m0, e0 = 2^(s' - m0) kept in registers,
+//           s0 = sum e0 (s' = score / sqrt(dh) in base 2);
+//   part 1: its max m1, m = max(m0, m1); e1 = 2^(s' - m) written back over
+//           its scores, s = s0 2^(m0 - m) + sum e1; then
+//           A += e0 2^(m0 - m) / s and A += e1 / s in TMEM.
+// (NP = 1: part 0 alone, A += e0 / s0.)  After the row tile's last head:
+// A / Hq, KL against A_prev, stores.  The softmax terms are those of one
+// pass over all C columns up to rounding (the rescale 2^(m0 - m) is exact
+// when m = m0 and within an ulp otherwise).
+template <int BN_T, int NP>
+struct ProxyTmemEpi : TcEpiBase {
+  static constexpr int BN = BN_T * NP;
+  static constexpr int kExtraCols = BN;
+  static constexpr bool kA3D = true;
+  static constexpr bool kBlocked = true;
+  int B, N, C, Hq, G, dh, mtb;
+  float scale;
+  const float* A_prev;
+  float* A_cur;
+  float* D;
+  struct State {
+    float e0[BN_T];
+    float m0, s0;
+    uint32_t extra;
+  };
+  __device__ int tiles(int) const { return B * mtb * Hq * NP; }
+  __device__ int arow(int t) const {
+    const int bm = t / (Hq * NP);
+    return (bm / mtb) * N + (bm % mtb) * 128;
+  }
+  __device__ int ahead(int t) const { return (t / NP) % Hq; }
+  __device__ int bcoord(int t, int) const {
+    return (t / (Hq * NP) / mtb) * C + (t % NP) * BN_T;
+  }
+  __device__ int bkoff(int t) const { return (((t / NP) % Hq) / G) * dh; }
+
+  // A[c .. c + 16) (+)= f * x[0 .. 16), in TMEM; `first`: A = f * x
+  __device__ __forceinline__ void add_a(uint32_t at, const float* x, float f, bool first) const {
+    uint32_t a[16];
+    if (first) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(x[j] * f);
+    } else {
+      tc::tmem_ld16_nowait(at, a);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(fmaf(x[j], f, __uint_as_float(a[j])));
+    }
+    tc::tmem_st16(at, a);
+  }
+
+  __device__ void consume(int t, int r, int, int, uint32_t taddr, State& st) const {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float sl = scale * kLog2e;
+    const int h = (t / NP) % Hq, part = t % NP;
+    const bool first = h == 0;
+    const int c0 = part * BN_T;
+    if (part == 0) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k0 = 0; k0 < BN_T; k0 += 16) {
+        uint32_t raw[16];
+        tc::tmem_ld16_nowait(taddr + k0, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float v = k0 + j < C ? __uint_as_float(raw[j]) * sl : -INFINITY;
+          st.e0[k0 + j] = v;
+          m = fmaxf(m, v);
+        }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN_T; ++c) {
+        st.e0[c] = exp2f(st.e0[c] - m);
+        s += st.e0[c];
+      }
+      st.m0 = m;
+      st.s0 = s;
+      if constexpr (NP == 1) {
+        const float rs = 1.0f / s;
+#pragma unroll
+        for (int k0 = 0; k0 < BN_T; k0 += 16) add_a(st.extra + k0, st.e0 + k0, rs, first);
+        tc::tmem_wait_st();
+      }
+    } else {
+      float m1 = -INFINITY;
+#pragma unroll
+      for (int k0 = 0; k0 < BN_T; k0 += 16) {
+        uint32_t raw[16];
+        tc::tmem_ld16_nowait(taddr + k0, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + k0 + j < C) m1 = fmaxf(m1, __uint_as_float(raw[j]) * sl);
+      }
+      const float m = fmaxf(st.m0, m1);
+      const float f0 = exp2f(st.m0 - m);
+      float s1 = 0.f;
+#pragma unroll
+      for (int k0 = 0; k0 < BN_T; k0 += 16) {
+        uint32_t raw[16];
+        tc::tmem_ld16_nowait(taddr + k0, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float e =
+              c0 + k0 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
+          s1 += e;
+          raw[j] = __float_as_uint(e);
+        }
+        tc::tmem_st16(taddr + k0, raw);
+      }
+      tc::tmem_wait_st();
+      const float rs = 1.0f / fmaf(st.s0, f0, s1);
+      const float r0 = f0 * rs;
+#pragma unroll
+      for (int k0 = 0; k0 < BN_T; k0 += 16) add_a(st.extra + k0, st.e0 + k0, r0, first);
+#pragma unroll
+      for (int k0 = 0; k0 < BN_T; k0 += 16) {
+        uint32_t raw[16];
+        tc::tmem_ld16_nowait(taddr + k0, raw);
+        tc::tmem_wait_ld();
+        add_a(st.extra + BN_T + k0, reinterpret_cast<const float*>(raw), rs, first);
+      }
+      tc::tmem_wait_st();
+    }
+    if (part == NP - 1 && h == Hq - 1) finish(t, r, st);
+  }
+
+  // A / Hq and the KL of the row, from TMEM
+  __device__ void finish(int t, int r, const State& st) const {
+    const int bm = t / (Hq * NP), b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const bool live = i < N, prev = A_prev != nullptr;
+    const long row = (long)b * N + i;
+    const float hq = (float)Hq;
+    float kl = 0.f;
+#pragma unroll 1
+    for (int k0 = 0; k0 < BN; k0 += 32) {
+      uint32_t raw[32];
+      tc::tmem_ld32_nowait(st.extra + k0, raw);  // warp-collective
+      tc::tmem_wait_ld();
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = k0 + j;
+        if (c < C) {
+          const float a = __uint_as_float(raw[j]) / hq;
+          A_cur[row * C + c] = a;
+          if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
+        }
+      }
+    }
+    if (live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+  }
+  __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
 };
 
 // Head slices of one row tile inside one thread-block cluster: CTA z runs
@@ -718,7 +895,13 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
       return cudaErrorInvalidValue;
     maps.b[1] = maps.b[0];
     TcShape sh{a.B * a.C, nullptr, p.KB, p.ck_kpc, a.status, INT_MAX, 0, a_rows};
-    const dim3 grid(p.ck_nt, p.ck_mt, p.ck_nz);
+    // without a d split, at most one CTA per SM walks the row tiles of its
+    // column tile (the epilogue of one tile under the MMAs of the next)
+    const int gy = p.ck_nz > 1 ? p.ck_mt
+                               : std::max(1, std::min(p.ck_mt, (a.num_sms > 0 ? a.num_sms
+                                                                               : kSmTarget) /
+                                                                   p.ck_nt));
+    const dim3 grid(p.ck_nt, gy, p.ck_nz);
     const int M = a.B * a.C;
     cudaError_t e;
     if (p.ck_nz > 1) {  // d-chunks summed inside a thread-block cluster
@@ -746,12 +929,28 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   maps.a[1] = maps.a[0];
   TcShape sh{a.B * a.N, nullptr, a.dh / 64, a.dh / 64, a.status, INT_MAX};
-  // columns of a row split over P epilogue warps per lane quarter (BN / P <= 64)
-  constexpr int P = BN > 64 ? BN / 64 : 1;
+  // columns of a row split over P epilogue warps per lane quarter: two for
+  // BN >= 128 (2 + 8 warps: the register file is allotted in 4-warp steps,
+  // so 12 warps' worth, 168 registers a thread, room for a 128-column head
+  // sum; 16 epilogue warps would get 96 and spill it)
+  constexpr int P = BN > 64 ? 2 : 1;
+  const float scale = (float)(1.0 / std::sqrt((double)a.dh));
+  if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
+    constexpr int NPp = BN > 128 ? 2 : 1;
+    constexpr int BNT = BN / NPp;
+    TcMaps m2 = maps;
+    if (NPp > 1 &&
+        (!make_tmap_bf16_2d(&m2.b[0], w.khi, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                            BNT) ||
+         !make_tmap_bf16_2d(&m2.b[1], w.klo, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                            BNT)))
+      return cudaErrorInvalidValue;
+    ProxyTmemEpi<BNT, NPp> te{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale,
+                              a.A_prev, a.A_cur, a.D};
+    return launch_tc_gemm<BNT, 1, 2, false>(m2, sh, te, dim3(1, a.B * p.mtb, 1), s);
+  }
   ProxyEpi<BN, P> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
-                      (float)(1.0 / std::sqrt((double)a.dh)), a.A_prev, a.A_cur, a.D};
-  if (p.nslice == 1)
-    return launch_tc_gemm<BN, 1, 2, false>(maps, sh, epi, dim3(1, a.B * p.mtb, 1), s);
+                      scale, a.A_prev, a.A_cur, a.D};
   ProxyClusterEpi<BN, P> cepi{epi};
   return launch_tc_gemm<BN, 1, 2, false>(maps, sh, cepi, dim3(1, a.B * p.mtb, p.nslice), s);
 }

@@ -109,6 +109,10 @@ struct TcCfg {
 //        skips tile t in all three roles -- no copies, no MMAs, no
 //        epilogue call; read at the tile from memory that earlier kernels
 //        wrote, so every role sees the same answer
+//   static constexpr int kExtraCols  TMEM columns the epilogue keeps for
+//        itself past the two accumulators (default 0); with it, State has a
+//        uint32_t `extra` that the engine sets to their address in the
+//        thread's lane quarter before the first tile
 //   void prefetch(uint8_t* scratch, int i, int n)  optional: run by the n
 //        epilogue threads (index i) before they wait for the first
 //        accumulator, to stage data the epilogue reads later into the
@@ -122,6 +126,15 @@ struct TcCfg {
 //        called by every thread of the CTA after a cluster barrier; must call
 //        tc::cluster_arrive() exactly once, uniformly, after its last read
 //        of another CTA's shared memory (the CTA waits before leaving)
+// TMEM columns a CTA allocates: the two accumulators and the epilogue's
+// own, rounded up to a power of two (>= 32, <= 512).
+template <int BN, class Epi>
+__host__ __device__ constexpr uint32_t tc_tmem_cols() {
+  constexpr int need = 2 * BN + Epi::kExtraCols;
+  static_assert(need <= 512, "TMEM holds 512 columns");
+  return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+}
+
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& sh,
                                              const Epi& epi) {
@@ -154,10 +167,11 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
   const int T_all = epi.tiles(M);
   // K not split although the grid has K chunks (the rows outgrew
   // split_max_rows, known only on the device): the gridDim.z CTAs of a
-  // column tile take turns on the row tiles instead of idling
+  // column tile take turns on the row tiles instead of idling, z fastest,
+  // so the clusters whose first tile lies past the end hold no work at all
   const bool zrows = Epi::kZSplitsK && !ksplit && gridDim.z > 1;
   const int T = T_all;
-  int t_begin = zrows ? (int)(blockIdx.y + blockIdx.z * gridDim.y) : (int)blockIdx.y;
+  int t_begin = zrows ? (int)(blockIdx.y * gridDim.z + blockIdx.z) : (int)blockIdx.y;
   int t_end = T, t_step = zrows ? (int)(gridDim.y * gridDim.z) : (int)gridDim.y;
   if constexpr (Epi::kBlocked) {
     const int per = (T + gridDim.y - 1) / gridDim.y;
@@ -169,6 +183,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
   if constexpr (Epi::kClusterReduce) {
     int b0 = blockIdx.y, e0 = T_all, s0 = gridDim.y;
     epi.tile_range(T_all, &b0, &e0, &s0);
+    if (zrows) b0 = blockIdx.y * gridDim.z;  // the cluster's first tile (z = 0)
     if (b0 >= e0) return;
   } else {
     if (t_begin >= t_end) return;
@@ -192,7 +207,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
     tc::tma_prefetch(&maps.a[0]);
     tc::tma_prefetch(&maps.b[0]);
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * BN);
+  if (warp == 1) tc::tmem_alloc(tmem_slot, tc_tmem_cols<BN, Epi>());
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
@@ -325,6 +340,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
     // the epilogue warps stage their per-tile data while the mainloop runs
     epi.prefetch(epi_scratch, threadIdx.x - 64, 32 * Epi::kEpiWarps);
     typename Epi::State est;
+    if constexpr (Epi::kExtraCols > 0) est.extra = tmem + 2 * BN + lane_base;
     int tcount = 0;
     for (int t = t_begin; t < t_end; t += t_step) {
       if constexpr (!Epi::kClusterReduce) {
@@ -373,7 +389,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
   }
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 2 * BN);
+    tc::tmem_dealloc(tmem, tc_tmem_cols<BN, Epi>());
   }
   // no CTA leaves while another still reads its result
   if constexpr (Epi::kClusterReduce) tc::cluster_wait();
@@ -385,19 +401,10 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
   tc_gemm_body<BN, NA, NB, B_MN, Epi>(maps, sh, epi);
 }
 
-// The same kernel for 16 epilogue warps (576 threads): a register limit of
-// 112 a thread (18 warps x 112 x 32 fills 64512 of the SM's 65536) in place
-// of the launch bound, under which the compiler settles for 96 and spills
-// the epilogue's per-row state.
-template <int BN, int NA, int NB, bool B_MN, class Epi>
-__global__ void __maxnreg__(112)
-k_tc_gemm_w16(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) {
-  tc_gemm_body<BN, NA, NB, B_MN, Epi>(maps, sh, epi);
-}
-
 // Plain epilogue base: 2-D maps, strided tiles, no B offset, one b map.
 struct TcEpiBase {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kExtraCols = 0;
   static constexpr bool kA3D = false;
   static constexpr bool kBlocked = false;
   static constexpr bool kClusterReduce = false;
@@ -469,13 +476,7 @@ template <int BN, int NA, int NB, bool B_MN, class Epi>
 cudaError_t launch_tc_gemm(const TcMaps& maps, const TcShape& sh, const Epi& epi, dim3 grid,
                            cudaStream_t s) {
   using Cfg = TcCfg<BN, NA, NB, B_MN>;
-  static_assert(Epi::kEpiWarps <= 16, "at most 16 epilogue warps");
-  auto kern = [] {
-    if constexpr (Epi::kEpiWarps == 16)
-      return k_tc_gemm_w16<BN, NA, NB, B_MN, Epi>;
-    else
-      return k_tc_gemm<BN, NA, NB, B_MN, Epi>;
-  }();
+  auto kern = k_tc_gemm<BN, NA, NB, B_MN, Epi>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -639,3 +639,31 @@ def test_commit_uniform_and_onehot_closed_forms():
     assert abs(g["conf"][0][0] - 1 / V) <= 1e-6 / V
     want = 1 / (1 + (V - 1) * math.exp(-6.0))
     assert abs(g["conf"][0][1] - want) <= 1e-6 * want
+
+
+@pytest.mark.parametrize("C,Hq,Hkv", [(256, 4, 2), (200, 6, 3), (100, 2, 2), (256, 8, 8)])
+def test_proxy_row_tile_path_head_sum_in_tmem(C, Hq, Hkv):
+    """160 windows (160 row tiles: one CTA per tile takes all its heads, the
+    head sum kept in TMEM); C above 128 splits a head's columns in two
+    halves joined by the softmax's rescale (C = 200: a ragged second half).
+    With and without a previous distribution, and KL of an identical step
+    exactly 0."""
+    rng = np.random.default_rng(C + Hq)
+    B, N, dh, d = 160, 70, 64, 128
+    Q = torch.from_numpy(rng.standard_normal((B, N, Hq, dh)).astype(np.float32) * 2)
+    Q = Q.to(torch.bfloat16).cuda()
+    chat = torch.from_numpy(rng.standard_normal((B, C, d)).astype(np.float32)).cuda()
+    Wk = torch.from_numpy((rng.standard_normal((d, Hkv * dh)) * 0.1).astype(np.float32))
+    Wk = Wk.to(torch.bfloat16).cuda()
+    w = dataclasses.replace(wl.WORKLOADS[0], Hq=Hq, Hkv=Hkv, dh=dh)
+    A0, D0 = run_proxy(Q, chat, Wk, Hkv)
+    oA0, _ = _oracle_proxy(w, np_(Q), np_(chat), np_(Wk))
+    assert_close(np_(A0), oA0, what="A (no prev)")
+    assert np.all(np_(D0) == 0.0)
+    prev = torch.softmax(torch.randn(B, N, C, device="cuda"), dim=2)
+    A, D = run_proxy(Q, chat, Wk, Hkv, A_prev=prev)
+    oA, oD = _oracle_proxy(w, np_(Q), np_(chat), np_(Wk), np_(prev))
+    assert_close(np_(A), oA, what="A")
+    assert_close(np_(D), oD, what="D")
+    _, D2 = run_proxy(Q, chat, Wk, Hkv, A_prev=A0)
+    assert bool((D2 == 0).all())
