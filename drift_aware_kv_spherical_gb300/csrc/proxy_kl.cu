@@ -538,31 +538,36 @@ struct ProxyEpi : TcEpiBase {
 // all its heads (enough row tiles to fill the GPU).  A head's BN score
 // columns come in NP parts of BN_T = BN / NP columns (NP = 2 when BN = 256),
 // each its own tile, so the two accumulator buffers (2 BN_T columns) and
-// the head sum A (BN columns, fp32) fit the 512 TMEM columns.  One epilogue
-// thread per row (4 warps), with no exchange between warps:
-//   part 0: its scores, their max m0, e0 = 2^(s' - m0) kept in registers,
-//           s0 = sum e0 (s' = score / sqrt(dh) in base 2);
-//   part 1: its max m1, m = max(m0, m1); e1 = 2^(s' - m) written back over
-//           its scores, s = s0 2^(m0 - m) + sum e1; then
-//           A += e0 2^(m0 - m) / s and A += e1 / s in TMEM.
-// (NP = 1: part 0 alone, A += e0 / s0.)  After the row tile's last head:
-// A / Hq, KL against A_prev, stores.  The softmax terms are those of one
-// pass over all C columns up to rounding (the rescale 2^(m0 - m) is exact
-// when m = m0 and within an ulp otherwise).
+// the head sum A (BN columns, fp32) fit the 512 TMEM columns.  Sixteen
+// epilogue warps: the four of a TMEM lane quarter take W = BN_T / 4 columns
+// of each part of their 32 rows and meet through shared memory for a row's
+// max and sum (fixed order).  consume(): a part's scores, its row max m_p,
+// e = 2^(s' - m_p) kept in registers, its row sum s_p (s' = score / sqrt(dh)
+// in base 2).  After the last part, with m = max over the parts, each part's
+// weight is 2^(m_p - m) / sum_p s_p 2^(m_p - m).  tile_done(), which the
+// engine calls once the accumulator is handed back to the MMA, adds the
+// weighted terms of both parts into A in TMEM, so the next tile's MMAs run
+// under it; after the row tile's last head: A / Hq, KL against A_prev,
+// stores.  The softmax terms are those of one pass over all C columns up to
+// rounding.
 template <int BN_T, int NP>
 struct ProxyTmemEpi : TcEpiBase {
+  static constexpr int kEpiWarps = 16;
+  static constexpr int P = 4;            // epilogue warps per lane quarter
+  static constexpr int W = BN_T / P;     // columns a thread takes of each part
   static constexpr int BN = BN_T * NP;
   static constexpr int kExtraCols = BN;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
+  static_assert(W % 8 == 0 && W <= 32, "part width");
   int B, N, C, Hq, G, dh, mtb;
   float scale;
   const float* A_prev;
   float* A_cur;
   float* D;
   struct State {
-    float e0[BN_T];
-    float m0, s0;
+    float e[NP][W];  // this head's exponentials, against each part's own max
+    float m[NP], s[NP];
     uint32_t extra;
   };
   __device__ int tiles(int) const { return B * mtb * Hq * NP; }
@@ -576,116 +581,119 @@ struct ProxyTmemEpi : TcEpiBase {
   }
   __device__ int bkoff(int t) const { return (((t / NP) % Hq) / G) * dh; }
 
-  // A[c .. c + 16) (+)= f * x[0 .. 16), in TMEM; `first`: A = f * x
-  __device__ __forceinline__ void add_a(uint32_t at, const float* x, float f, bool first) const {
-    uint32_t a[16];
-    if (first) {
+  // the row's value from the four warps of a lane quarter (slot: 128 x 4
+  // floats of the scratch), combined in warp order
+  template <bool MAX>
+  __device__ __forceinline__ float row_combine(float v, float* slot, int r, int q) const {
+    slot[r * P + q] = v;
+    epi_bar_sync_n<32 * kEpiWarps>();
+    float x = slot[r * P];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(x[j] * f);
-    } else {
-      tc::tmem_ld16_nowait(at, a);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(fmaf(x[j], f, __uint_as_float(a[j])));
-    }
-    tc::tmem_st16(at, a);
+    for (int k = 1; k < P; ++k) x = MAX ? fmaxf(x, slot[r * P + k]) : x + slot[r * P + k];
+    return x;
   }
 
-  __device__ void consume(int t, int r, int, int, uint32_t taddr, State& st) const {
+  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
+                               State& st) const {
+    // the part as a constant, so that the State arrays stay in registers
+    if (NP == 1 || t % NP == 0)
+      consume_p<0>(r, q, taddr, scratch, st);
+    else
+      consume_p<NP - 1>(r, q, taddr, scratch, st);
+  }
+  template <int p>
+  __device__ __forceinline__ void consume_p(int r, int q, uint32_t taddr, uint8_t* scratch,
+                                            State& st) const {
     constexpr float kLog2e = 1.4426950408889634f;
     const float sl = scale * kLog2e;
-    const int h = (t / NP) % Hq, part = t % NP;
-    const bool first = h == 0;
-    const int c0 = part * BN_T;
-    if (part == 0) {
-      float m = -INFINITY;
+    const int cq = p * BN_T + q * W;  // this thread's first score column of the head
+    float* xs = reinterpret_cast<float*>(scratch) + p * 2 * 128 * P;
+    float m = -INFINITY;
 #pragma unroll
-      for (int k0 = 0; k0 < BN_T; k0 += 16) {
-        uint32_t raw[16];
-        tc::tmem_ld16_nowait(taddr + k0, raw);
-        tc::tmem_wait_ld();
+    for (int k = 0; k < W; k += 8) {  // 8 columns a load: both parts' terms fill the registers
+      uint32_t raw[8];
+      tc::tmem_ld8_nowait(taddr + q * W + k, raw);
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float v = k0 + j < C ? __uint_as_float(raw[j]) * sl : -INFINITY;
-          st.e0[k0 + j] = v;
-          m = fmaxf(m, v);
-        }
+      for (int j = 0; j < 8; ++j) {
+        const float v = cq + k + j < C ? __uint_as_float(raw[j]) * sl : -INFINITY;
+        st.e[p][k + j] = v;
+        m = fmaxf(m, v);
       }
-      float s = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN_T; ++c) {
-        st.e0[c] = exp2f(st.e0[c] - m);
-        s += st.e0[c];
-      }
-      st.m0 = m;
-      st.s0 = s;
-      if constexpr (NP == 1) {
-        const float rs = 1.0f / s;
-#pragma unroll
-        for (int k0 = 0; k0 < BN_T; k0 += 16) add_a(st.extra + k0, st.e0 + k0, rs, first);
-        tc::tmem_wait_st();
-      }
-    } else {
-      float m1 = -INFINITY;
-#pragma unroll
-      for (int k0 = 0; k0 < BN_T; k0 += 16) {
-        uint32_t raw[16];
-        tc::tmem_ld16_nowait(taddr + k0, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + k0 + j < C) m1 = fmaxf(m1, __uint_as_float(raw[j]) * sl);
-      }
-      const float m = fmaxf(st.m0, m1);
-      const float f0 = exp2f(st.m0 - m);
-      float s1 = 0.f;
-#pragma unroll
-      for (int k0 = 0; k0 < BN_T; k0 += 16) {
-        uint32_t raw[16];
-        tc::tmem_ld16_nowait(taddr + k0, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float e =
-              c0 + k0 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
-          s1 += e;
-          raw[j] = __float_as_uint(e);
-        }
-        tc::tmem_st16(taddr + k0, raw);
-      }
-      tc::tmem_wait_st();
-      const float rs = 1.0f / fmaf(st.s0, f0, s1);
-      const float r0 = f0 * rs;
-#pragma unroll
-      for (int k0 = 0; k0 < BN_T; k0 += 16) add_a(st.extra + k0, st.e0 + k0, r0, first);
-#pragma unroll
-      for (int k0 = 0; k0 < BN_T; k0 += 16) {
-        uint32_t raw[16];
-        tc::tmem_ld16_nowait(taddr + k0, raw);
-        tc::tmem_wait_ld();
-        add_a(st.extra + BN_T + k0, reinterpret_cast<const float*>(raw), rs, first);
-      }
-      tc::tmem_wait_st();
     }
-    if (part == NP - 1 && h == Hq - 1) finish(t, r, st);
+    m = row_combine<true>(m, xs, r, q);
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      st.e[p][j] = exp2f(st.e[p][j] - m);
+      s += st.e[p][j];
+    }
+    st.m[p] = m;
+    st.s[p] = row_combine<false>(s, xs + 128 * P, r, q);
   }
 
-  // A / Hq and the KL of the row, from TMEM
-  __device__ void finish(int t, int r, const State& st) const {
+  // A[cols] (+)= f * x, 8 columns at a time, in TMEM; `first`: A = f * x
+  __device__ __forceinline__ void add_a(uint32_t at, const float* x, float f, bool first) const {
+#pragma unroll
+    for (int k = 0; k < W; k += 8) {
+      uint32_t a[8];
+      if (first) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = __float_as_uint(x[k + j] * f);
+      } else {
+        tc::tmem_ld8_nowait(at + k, a);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          a[j] = __float_as_uint(fmaf(x[k + j], f, __uint_as_float(a[j])));
+      }
+      tc::tmem_st8(at + k, a);
+    }
+  }
+
+  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t* scratch,
+                                 State& st) const {
+    if (t % NP != NP - 1) return;  // tile-uniform: after a head's last part
+    const int h = (t / NP) % Hq;
+    float m = st.m[0];
+#pragma unroll
+    for (int p = 1; p < NP; ++p) m = fmaxf(m, st.m[p]);
+    float f[NP], s = 0.f;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      f[p] = exp2f(st.m[p] - m);
+      s = fmaf(st.s[p], f[p], s);
+    }
+    const float rs = 1.0f / s;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) add_a(st.extra + p * BN_T + q * W, st.e[p], f[p] * rs, h == 0);
+    tc::tmem_wait_st();
+    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
+  }
+
+  // A / Hq and the KL of the row: each thread its W columns of each part,
+  // the four warps' KL partials summed in warp order
+  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
     const int bm = t / (Hq * NP), b = bm / mtb, i = (bm % mtb) * 128 + r;
     const bool live = i < N, prev = A_prev != nullptr;
     const long row = (long)b * N + i;
     const float hq = (float)Hq;
     float kl = 0.f;
-#pragma unroll 1
-    for (int k0 = 0; k0 < BN; k0 += 32) {
-      uint32_t raw[32];
-      tc::tmem_ld32_nowait(st.extra + k0, raw);  // warp-collective
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      uint32_t raw[W];
+      if constexpr (W == 32) {
+        tc::tmem_ld32_nowait(st.extra + p * BN_T + q * W, raw);
+      } else if constexpr (W == 16) {
+        tc::tmem_ld16_nowait(st.extra + p * BN_T + q * W, raw);
+      } else {
+        tc::tmem_ld8_nowait(st.extra + p * BN_T + q * W, raw);
+      }
       tc::tmem_wait_ld();
       if (!live) continue;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = k0 + j;
+      for (int j = 0; j < W; ++j) {
+        const int c = p * BN_T + q * W + j;
         if (c < C) {
           const float a = __uint_as_float(raw[j]) / hq;
           A_cur[row * C + c] = a;
@@ -693,9 +701,141 @@ struct ProxyTmemEpi : TcEpiBase {
         }
       }
     }
-    if (live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+    kl = row_combine<false>(kl, xs + 4 * 128 * P, r, q);
+    if (q == 0 && live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
   }
-  __device__ void tile_done(int, int, int, int, uint8_t*, State&) const {}
+};
+
+// Proxy epilogue for C in (128, 256] with one CTA per row tile taking all
+// its heads: a head's 256 score columns in one tile (the two accumulator
+// buffers fill the 512 TMEM columns) and the head sum in registers.  Twelve
+// epilogue warps, three per TMEM lane quarter: with 2 + 12 warps the
+// register file is allotted as for 16, 128 registers a thread, where 2 + 16
+// warps get 96 and spill the head sum.  The three warps of a quarter take
+// 11, 11 and 10 eight-column chunks of their 32 rows (88 sums at most in
+// registers) and meet through shared memory for a row's max and sum, in
+// warp order.  Per head: the max of the scores (TMEM read); exp2 and the
+// sum, the exponentials written back over the scores (one exp2 a score);
+// A += e / sum (TMEM read).  After the row tile's last head: A / Hq, KL.
+struct ProxyRegEpi : TcEpiBase {
+  static constexpr int kEpiWarps = 12;
+  static constexpr int P = 3;
+  static constexpr int BN = 256;
+  static constexpr int kCh = 11;  // eight-column chunks a thread takes (the third warp: 10)
+  static constexpr bool kA3D = true;
+  static constexpr bool kBlocked = true;
+  int B, N, C, Hq, G, dh, mtb;
+  float scale;
+  const float* A_prev;
+  float* A_cur;
+  float* D;
+  struct State {
+    float A[kCh][8];
+  };
+  __device__ int tiles(int) const { return B * mtb * Hq; }
+  __device__ int arow(int t) const {
+    const int bm = t / Hq;
+    return (bm / mtb) * N + (bm % mtb) * 128;
+  }
+  __device__ int ahead(int t) const { return t % Hq; }
+  __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
+  __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
+
+  template <bool MAX>
+  __device__ __forceinline__ float row_combine(float v, float* slot, int r, int q) const {
+    slot[r * P + q] = v;
+    epi_bar_sync_n<32 * kEpiWarps>();
+    float x = slot[r * P];
+#pragma unroll
+    for (int k = 1; k < P; ++k) x = MAX ? fmaxf(x, slot[r * P + k]) : x + slot[r * P + k];
+    return x;
+  }
+
+  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
+                               State& st) const {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float sl = scale * kLog2e;
+    const int h = t % Hq;
+    float* mx = reinterpret_cast<float*>(scratch) + (h & 1) * (2 * 128 * P);
+    if (h == 0) {
+#pragma unroll
+      for (int k = 0; k < kCh; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st.A[k][j] = 0.f;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kCh; ++k) {
+      const int ch = q * kCh + k;  // warp-uniform
+      if (ch < BN / 8) {
+        uint32_t raw[8];
+        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (ch * 8 + j < C) m = fmaxf(m, __uint_as_float(raw[j]) * sl);
+      }
+    }
+    m = row_combine<true>(m, mx, r, q);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kCh; ++k) {
+      const int ch = q * kCh + k;
+      if (ch < BN / 8) {
+        uint32_t raw[8];
+        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float e = ch * 8 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
+          s += e;
+          raw[j] = __float_as_uint(e);
+        }
+        tc::tmem_st8(taddr + ch * 8, raw);
+      }
+    }
+    tc::tmem_wait_st();
+    s = row_combine<false>(s, mx + 128 * P, r, q);
+    const float rs = 1.0f / s;
+#pragma unroll
+    for (int k = 0; k < kCh; ++k) {
+      const int ch = q * kCh + k;
+      if (ch < BN / 8) {
+        uint32_t raw[8];
+        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st.A[k][j] = fmaf(__uint_as_float(raw[j]), rs, st.A[k][j]);
+      }
+    }
+    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
+  }
+
+  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
+    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const bool live = i < N, prev = A_prev != nullptr;
+    const long row = (long)b * N + i;
+    const float hq = (float)Hq;
+    float kl = 0.f;
+    if (live) {
+#pragma unroll
+      for (int k = 0; k < kCh; ++k) {
+        const int ch = q * kCh + k;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = ch * 8 + j;
+          if (ch < BN / 8 && c < C) {
+            const float a = st.A[k][j] / hq;
+            A_cur[row * C + c] = a;
+            if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
+          }
+        }
+      }
+    }
+    kl = row_combine<false>(kl, xs + 4 * 128 * P, r, q);
+    if (q == 0 && live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+  }
+  __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
 };
 
 // Head slices of one row tile inside one thread-block cluster: CTA z runs
@@ -935,6 +1075,13 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   // sum; 16 epilogue warps would get 96 and spill it)
   constexpr int P = BN > 64 ? 2 : 1;
   const float scale = (float)(1.0 / std::sqrt((double)a.dh));
+  if constexpr (BN == 256) {
+    if (p.nslice == 1) {  // a CTA per row tile, the head sum in registers
+      ProxyRegEpi re{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+                     a.A_cur, a.D};
+      return launch_tc_gemm<256, 1, 2, false>(maps, sh, re, dim3(1, a.B * p.mtb, 1), s);
+    }
+  }
   if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
     constexpr int NPp = BN > 128 ? 2 : 1;
     constexpr int BNT = BN / NPp;

@@ -3,8 +3,8 @@
 // CTA = 2 + E warps: warp 0 issues TMA loads into an S-stage shared-memory
 // ring, warp 1 issues tcgen05.mma (one thread) into one of two 128 x BN fp32
 // accumulators in TMEM (double-buffered, so the MMAs of the next tile run
-// while the epilogue drains this one), and the E = Epi::kEpiWarps (4, 8 or
-// 16) warps from 2 on drain the accumulator and hand rows to an op-specific
+// while the epilogue drains this one), and the E = Epi::kEpiWarps (4, 8, 12
+// or 16) warps from 2 on drain the accumulator and hand rows to an op-specific
 // epilogue: warp w reads the TMEM lane quarter w % 4 it may access, and with
 // E > 4 the E / 4 warps of a quarter split the BN columns between them.  The CTA owns
 // one BN-column tile (blockIdx.x) and walks row tiles t < epi.tiles(M)
@@ -96,7 +96,7 @@ struct TcCfg {
 //   void tile_done(int t, int r, int n0, int z, uint8_t* scratch, State&)
 //        called by the 128 epilogue threads together after consume; may
 //        synchronise with epi_bar_sync(); scratch = 16 KB of shared memory
-//   static constexpr int kEpiWarps  4 (default), 8 or 16; above 4 the
+//   static constexpr int kEpiWarps  4 (default), 8, 12 or 16; above 4 the
 //        engine calls consume_part / tile_done_part / consume_red_part, which
 //        also take the thread's column part (0 .. kEpiWarps / 4 - 1) and the
 //        scratch, and may synchronise the epilogue warps with
@@ -187,6 +187,10 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
     if (b0 >= e0) return;
   } else {
     if (t_begin >= t_end) return;
+    // every tile of this CTA skipped (active() false): leave before set-up
+    bool any = false;
+    for (int t = t_begin; t < t_end && !any; t += t_step) any = epi.active(t);
+    if (!any) return;
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
