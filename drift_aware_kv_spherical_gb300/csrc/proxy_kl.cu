@@ -39,6 +39,15 @@ namespace {
 constexpr int kRows = 16;   // window rows per proxy CTA
 constexpr int kKc = 32;     // head-dim stage of the centroid keys
 
+// 2^x by the special-function unit's approximation (PTX ex2.approx.ftz.f32:
+// a relative error of a few ulp, subnormal results flushed to zero, and
+// 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename TW>
 __global__ void __launch_bounds__(256)
 k_ckeys(const float* __restrict__ chat, const TW* __restrict__ Wk, int M,
@@ -341,6 +350,8 @@ struct ProxyEpi : TcEpiBase {
   static constexpr bool kReread = W > 64 || P >= 2;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
+  // two (max, sum) exchange slots of 2 x 128 x P floats, then 128 x P for KL
+  static_assert(5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb, hps, nslice;
   float scale;
   const float* A_prev;
@@ -412,7 +423,8 @@ struct ProxyEpi : TcEpiBase {
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-          const float e = c0 + k0 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
+          const float e =
+              c0 + k0 + j < C ? ex2_approx(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
           s2[j & 1] += e;
           raw[j] = __float_as_uint(e);
         }
@@ -466,7 +478,7 @@ struct ProxyEpi : TcEpiBase {
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < W; ++c) {
-        e[c] = c0 + c < C ? exp2f(e[c] - m) : 0.f;
+        e[c] = c0 + c < C ? ex2_approx(e[c] - m) : 0.f;
         s4[c & 3] += e[c];
       }
       float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
@@ -560,6 +572,8 @@ struct ProxyTmemEpi : TcEpiBase {
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   static_assert(W % 8 == 0 && W <= 32, "part width");
+  // per part a (max, sum) exchange of 2 x 128 x P floats; KL at 4 x 128 x P
+  static_assert(NP <= 2 && 5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb;
   float scale;
   const float* A_prev;
@@ -625,7 +639,7 @@ struct ProxyTmemEpi : TcEpiBase {
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      st.e[p][j] = exp2f(st.e[p][j] - m);
+      st.e[p][j] = ex2_approx(st.e[p][j] - m);
       s += st.e[p][j];
     }
     st.m[p] = m;
@@ -661,7 +675,7 @@ struct ProxyTmemEpi : TcEpiBase {
     float f[NP], s = 0.f;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-      f[p] = exp2f(st.m[p] - m);
+      f[p] = ex2_approx(st.m[p] - m);
       s = fmaf(st.s[p], f[p], s);
     }
     const float rs = 1.0f / s;
@@ -707,30 +721,39 @@ struct ProxyTmemEpi : TcEpiBase {
 };
 
 // Proxy epilogue for C in (128, 256] with one CTA per row tile taking all
-// its heads: a head's 256 score columns in one tile (the two accumulator
-// buffers fill the 512 TMEM columns) and the head sum in registers.  Twelve
-// epilogue warps, three per TMEM lane quarter: with 2 + 12 warps the
-// register file is allotted as for 16, 128 registers a thread, where 2 + 16
-// warps get 96 and spill the head sum.  The three warps of a quarter take
-// 11, 11 and 10 eight-column chunks of their 32 rows (88 sums at most in
-// registers) and meet through shared memory for a row's max and sum, in
-// warp order.  Per head: the max of the scores (TMEM read); exp2 and the
-// sum, the exponentials written back over the scores (one exp2 a score);
-// A += e / sum (TMEM read).  After the row tile's last head: A / Hq, KL.
-struct ProxyRegEpi : TcEpiBase {
-  static constexpr int kEpiWarps = 12;
-  static constexpr int P = 3;
+// its heads: a head's 256 score columns in one accumulator and the head sum
+// A (256 columns, fp32) in the other half of TMEM, so the accumulator is
+// single-buffered (the next head's MMAs wait for this epilogue; the TMA
+// copies run ahead).  Sixteen epilogue warps, four per TMEM lane quarter,
+// each taking 64 columns of its 32 rows in few TMEM round trips:
+//   pass 1: the scores (two 32-column loads, one wait), their max m_q over
+//           the thread's columns, e = 2^(s' - m_q) written back over them,
+//           and their sum s_q (s' = score / sqrt(dh) in base 2);
+//   the four warps of a row exchange (m_q, s_q) through shared memory once
+//   (fixed order): m = max m_q, s = sum s_q 2^(m_q - m);
+//   pass 2: A += e 2^(m_q - m) / s, 32 columns at a time (e and A read
+//           together, one wait).
+// After the row tile's last head: A / Hq, KL against A_prev, stores.  The
+// softmax terms are those of one pass over the row up to rounding (the
+// rescale 2^(m_q - m) is 1 for the warp holding the max).
+struct ProxySoloEpi : TcEpiBase {
+  static constexpr int kEpiWarps = 16;
+  static constexpr int P = 4;
   static constexpr int BN = 256;
-  static constexpr int kCh = 11;  // eight-column chunks a thread takes (the third warp: 10)
+  static constexpr int W = BN / P;  // 64 columns a thread
+  static constexpr int kAccBufs = 1;
+  static constexpr int kExtraCols = BN;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
+  // two (max, sum) exchange slots of 128 x P float4
+  static_assert(2 * 128 * P * 16 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb;
   float scale;
   const float* A_prev;
   float* A_cur;
   float* D;
   struct State {
-    float A[kCh][8];
+    uint32_t extra;
   };
   __device__ int tiles(int) const { return B * mtb * Hq; }
   __device__ int arow(int t) const {
@@ -741,73 +764,99 @@ struct ProxyRegEpi : TcEpiBase {
   __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
   __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
 
-  template <bool MAX>
-  __device__ __forceinline__ float row_combine(float v, float* slot, int r, int q) const {
-    slot[r * P + q] = v;
-    epi_bar_sync_n<32 * kEpiWarps>();
-    float x = slot[r * P];
+  // the max and the sum of 2^(v sl - m) over 32 scores v (raw TMEM words),
+  // e = 2^(v sl - m) written back over them; n < 32: only the first n count
+  // (n >= 1), the others take e = 0.  m = sl * max v, as sl > 0.
+  template <bool kFull>
+  __device__ __forceinline__ void half_exp(uint32_t addr, int n, float sl, float& m,
+                                           float& sum) const {
+    uint32_t v[32];
+    tc::tmem_ld32_nowait(addr, v);
+    tc::tmem_wait_ld();
+    if constexpr (!kFull) {
 #pragma unroll
-    for (int k = 1; k < P; ++k) x = MAX ? fmaxf(x, slot[r * P + k]) : x + slot[r * P + k];
-    return x;
+      for (int j = 0; j < 32; ++j)
+        if (j >= n) v[j] = __float_as_uint(-INFINITY);
+    }
+    float mx[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mx[j] = fmaxf(fmaxf(__uint_as_float(v[j]), __uint_as_float(v[j + 8])),
+                    fmaxf(__uint_as_float(v[j + 16]), __uint_as_float(v[j + 24])));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
+    m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
+    float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float e = ex2_approx(fmaf(__uint_as_float(v[j]), sl, -m));
+      sp[j & 3] += e;
+      v[j] = __float_as_uint(e);
+    }
+    sum = (sp[0] + sp[1]) + (sp[2] + sp[3]);
+    tc::tmem_st32(addr, v);
   }
 
   __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
                                State& st) const {
     constexpr float kLog2e = 1.4426950408889634f;
     const float sl = scale * kLog2e;
-    const int h = t % Hq;
-    float* mx = reinterpret_cast<float*>(scratch) + (h & 1) * (2 * 128 * P);
-    if (h == 0) {
+    const int h = t % Hq, c0 = q * W;
+    // pass 1, in two halves of 32 columns, each against its own max; a half
+    // past column C is left out (its max -inf, its weight 0)
+    float mh[2], sh[2];
 #pragma unroll
-      for (int k = 0; k < kCh; ++k)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) st.A[k][j] = 0.f;
+    for (int g = 0; g < 2; ++g) {
+      const int n = C - (c0 + 32 * g);
+      mh[g] = -INFINITY;
+      sh[g] = 0.f;
+      if (n >= 32)
+        half_exp<true>(taddr + c0 + 32 * g, 32, sl, mh[g], sh[g]);
+      else if (n > 0)
+        half_exp<false>(taddr + c0 + 32 * g, n, sl, mh[g], sh[g]);
     }
-    float m = -INFINITY;
+    // the row's max and sum from the eight halves of the quarter, in order
+    float4* xs = reinterpret_cast<float4*>(scratch) + (h & 1) * 128 * P;
+    xs[r * P + q] = make_float4(mh[0], sh[0], mh[1], sh[1]);
+    epi_bar_sync_n<32 * kEpiWarps>();
+    float4 x[P];
 #pragma unroll
-    for (int k = 0; k < kCh; ++k) {
-      const int ch = q * kCh + k;  // warp-uniform
-      if (ch < BN / 8) {
-        uint32_t raw[8];
-        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
-        tc::tmem_wait_ld();
+    for (int k = 0; k < P; ++k) x[k] = xs[r * P + k];
+    float mr = fmaxf(fmaxf(x[0].x, x[0].z), fmaxf(x[1].x, x[1].z));
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (ch * 8 + j < C) m = fmaxf(m, __uint_as_float(raw[j]) * sl);
-      }
+    for (int k = 2; k < P; ++k) mr = fmaxf(mr, fmaxf(x[k].x, x[k].z));
+    float sr = 0.f;
+#pragma unroll
+    for (int k = 0; k < P; ++k) {  // a left-out half adds 0 x 2^-inf = 0
+      sr = fmaf(x[k].y, ex2_approx(x[k].x - mr), sr);
+      sr = fmaf(x[k].w, ex2_approx(x[k].z - mr), sr);
     }
-    m = row_combine<true>(m, mx, r, q);
-    float s = 0.f;
+    const float rs = 1.0f / sr;
+    // columns at or past C of A are never read, so a left-out half's weight
+    // only has to be finite
+    float f[2];
 #pragma unroll
-    for (int k = 0; k < kCh; ++k) {
-      const int ch = q * kCh + k;
-      if (ch < BN / 8) {
-        uint32_t raw[8];
-        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
-        tc::tmem_wait_ld();
+    for (int g = 0; g < 2; ++g) f[g] = mh[g] == -INFINITY ? 0.f : ex2_approx(mh[g] - mr) * rs;
+    tc::tmem_wait_st();
+    // pass 2: A += e f, 32 columns at a time (e and A read together)
+    const bool first = h == 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float e = ch * 8 + j < C ? exp2f(fmaf(__uint_as_float(raw[j]), sl, -m)) : 0.f;
-          s += e;
-          raw[j] = __float_as_uint(e);
-        }
-        tc::tmem_st8(taddr + ch * 8, raw);
+    for (int g = 0; g < 2; ++g) {
+      uint32_t e[32], a[32];
+      tc::tmem_ld32_nowait(taddr + c0 + 32 * g, e);
+      if (!first) tc::tmem_ld32_nowait(st.extra + c0 + 32 * g, a);
+      tc::tmem_wait_ld();
+      if (first) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(__uint_as_float(e[j]) * f[g]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a[j] = __float_as_uint(fmaf(__uint_as_float(e[j]), f[g], __uint_as_float(a[j])));
       }
+      tc::tmem_st32(st.extra + c0 + 32 * g, a);
     }
     tc::tmem_wait_st();
-    s = row_combine<false>(s, mx + 128 * P, r, q);
-    const float rs = 1.0f / s;
-#pragma unroll
-    for (int k = 0; k < kCh; ++k) {
-      const int ch = q * kCh + k;
-      if (ch < BN / 8) {
-        uint32_t raw[8];
-        tc::tmem_ld8_nowait(taddr + ch * 8, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) st.A[k][j] = fmaf(__uint_as_float(raw[j]), rs, st.A[k][j]);
-      }
-    }
     if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
   }
 
@@ -816,24 +865,36 @@ struct ProxyRegEpi : TcEpiBase {
     const bool live = i < N, prev = A_prev != nullptr;
     const long row = (long)b * N + i;
     const float hq = (float)Hq;
+    const int c0 = q * W;
     float kl = 0.f;
-    if (live) {
+#pragma unroll 1
+    for (int k = 0; k < W; k += 8) {  // once per row tile: 8 columns at a time
+      uint32_t a[8];
+      tc::tmem_ld8_nowait(st.extra + c0 + k, a);  // warp-collective
+      tc::tmem_wait_ld();
+      if (!live) continue;
 #pragma unroll
-      for (int k = 0; k < kCh; ++k) {
-        const int ch = q * kCh + k;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = ch * 8 + j;
-          if (ch < BN / 8 && c < C) {
-            const float a = st.A[k][j] / hq;
-            A_cur[row * C + c] = a;
-            if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
-          }
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + k + j;
+        if (c < C) {
+          const float av = __uint_as_float(a[j]) / hq;
+          A_cur[row * C + c] = av;
+          if (prev && av > 0.f) kl += av * logf(av / fmaxf(A_prev[row * C + c], 1e-30f));
         }
       }
     }
-    kl = row_combine<false>(kl, xs + 4 * 128 * P, r, q);
-    if (q == 0 && live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+    // the exchange slot the previous head used: every thread has read it
+    // before this head's exchange barrier, and the next row tile's first
+    // exchange waits for this epilogue (single-buffered accumulator)
+    float* zs = xs + (Hq & 1) * 4 * 128 * P;
+    zs[r * P + q] = kl;
+    epi_bar_sync_n<32 * kEpiWarps>();
+    if (q == 0 && live) {
+      float sum = zs[r * P];
+#pragma unroll
+      for (int k = 1; k < P; ++k) sum += zs[r * P + k];
+      D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
+    }
   }
   __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
 };
@@ -1076,10 +1137,10 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   constexpr int P = BN > 64 ? 2 : 1;
   const float scale = (float)(1.0 / std::sqrt((double)a.dh));
   if constexpr (BN == 256) {
-    if (p.nslice == 1) {  // a CTA per row tile, the head sum in registers
-      ProxyRegEpi re{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
-                     a.A_cur, a.D};
-      return launch_tc_gemm<256, 1, 2, false>(maps, sh, re, dim3(1, a.B * p.mtb, 1), s);
+    if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
+      ProxySoloEpi pe{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+                      a.A_cur, a.D};
+      return launch_tc_gemm<256, 1, 2, false>(maps, sh, pe, dim3(1, a.B * p.mtb, 1), s);
     }
   }
   if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM

@@ -109,6 +109,10 @@ struct TcCfg {
 //        skips tile t in all three roles -- no copies, no MMAs, no
 //        epilogue call; read at the tile from memory that earlier kernels
 //        wrote, so every role sees the same answer
+//   static constexpr int kAccBufs   accumulators in TMEM (default 2, double
+//        buffered: the MMAs of the next tile run under this tile's epilogue;
+//        1: the next tile's MMAs wait for the epilogue, for epilogues that
+//        need the TMEM columns of the second for themselves)
 //   static constexpr int kExtraCols  TMEM columns the epilogue keeps for
 //        itself past the two accumulators (default 0); with it, State has a
 //        uint32_t `extra` that the engine sets to their address in the
@@ -130,7 +134,7 @@ struct TcCfg {
 // own, rounded up to a power of two (>= 32, <= 512).
 template <int BN, class Epi>
 __host__ __device__ constexpr uint32_t tc_tmem_cols() {
-  constexpr int need = 2 * BN + Epi::kExtraCols;
+  constexpr int need = Epi::kAccBufs * BN + Epi::kExtraCols;
   static_assert(need <= 512, "TMEM holds 512 columns");
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
@@ -288,9 +292,10 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
         if constexpr (!Epi::kClusterReduce) {
           if (!epi.active(t)) continue;
         }
-        const int buf = tcount & 1;
+        const int buf = tcount % Epi::kAccBufs;
         const uint32_t dacc = tmem + buf * BN;
-        if (!tc::mbar_wait(acc_empty + buf, ((tcount >> 1) & 1) ^ 1, sh.status, abort_flag)) {
+        if (!tc::mbar_wait(acc_empty + buf, ((tcount / Epi::kAccBufs) & 1) ^ 1, sh.status,
+                           abort_flag)) {
           ok = false;
           break;
         }
@@ -344,14 +349,15 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
     // the epilogue warps stage their per-tile data while the mainloop runs
     epi.prefetch(epi_scratch, threadIdx.x - 64, 32 * Epi::kEpiWarps);
     typename Epi::State est;
-    if constexpr (Epi::kExtraCols > 0) est.extra = tmem + 2 * BN + lane_base;
+    if constexpr (Epi::kExtraCols > 0) est.extra = tmem + Epi::kAccBufs * BN + lane_base;
     int tcount = 0;
     for (int t = t_begin; t < t_end; t += t_step) {
       if constexpr (!Epi::kClusterReduce) {
         if (!epi.active(t)) continue;
       }
-      const int buf = tcount & 1;
-      if (!tc::mbar_wait(acc_full + buf, (tcount >> 1) & 1, sh.status, abort_flag)) break;
+      const int buf = tcount % Epi::kAccBufs;
+      if (!tc::mbar_wait(acc_full + buf, (tcount / Epi::kAccBufs) & 1, sh.status, abort_flag))
+        break;
       tc::fence_after_sync();
       if constexpr (Epi::kClusterReduce) {
         // the stage ring is idle once the CTA's last accumulator is full
@@ -409,6 +415,7 @@ k_tc_gemm(const __grid_constant__ TcMaps maps, const TcShape sh, const Epi epi) 
 struct TcEpiBase {
   static constexpr int kEpiWarps = 4;
   static constexpr int kExtraCols = 0;
+  static constexpr int kAccBufs = 2;
   static constexpr bool kA3D = false;
   static constexpr bool kBlocked = false;
   static constexpr bool kClusterReduce = false;
