@@ -302,7 +302,7 @@ def measure_overlap(w, dev, reps=20):
     del L
     Q = wl.make_queries(w, H, Wq)
     u = wl.make_uniforms(w, 0, dev)
-    logits = wl.make_logits(w, 0, dev).to(wl.torch_dtype(w))
+    logits = wl.make_logits(w, 0, dev)
     pipe = Pipeline(w, layers=1, device=dev)
     pipe.step([H], [Q], [Wk], [Wv], logits, init_us=[u], first=True)
     sm, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -589,9 +589,7 @@ def run_reference(args):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy()[0] for H in Hs]
     Hn = [H.float().numpy()[0] for H in Hs]
-    # the LM head's output dtype (bf16 values, exact in the oracle's fp64)
-    logits = [wl.make_logits(w, t, B=1).to(wl.torch_dtype(w)).float().numpy()[0]
-              for t in range(4)]
+    logits = [wl.make_logits(w, t, B=1).numpy()[0] for t in range(4)]
     u = wl.make_uniforms(w, B=1).numpy()[0]
     mu = oracle.kmeanspp_init(Hn[0], w.C, u)[0]
     st = dict(mu=mu, chat=None, A=None, s=np.zeros(w.P, np.float32),
@@ -662,7 +660,7 @@ def workload_config(w, layers=None):
     layers = w.layers if layers is None else layers
     return {"workload": w.name, "B": w.B, "N": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "dh": w.dh, "C": w.C, "iters": w.iters, "k": w.k, "P": w.P, "V": w.V,
-            "layers": layers, "logits": w.dtype,
+            "layers": layers, "logits": "f32",
             "weights": "per layer (seeded per layer)",
             "l2": ("flushed between steps (512 MB write)" if layers == 1 else
                    "inputs larger than L2 (every layer's window and queries are read each "
@@ -695,7 +693,7 @@ def one_layer_inputs(w, dev):
     for t in range(1, 4):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
-    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(4)]
+    logits = [wl.make_logits(w, t, dev) for t in range(4)]
     return L, Hs, Qs, logits, wl.make_uniforms(w, 0, dev)
 
 
@@ -722,8 +720,8 @@ def bench_workload(w, layers, args, dev, world, local, trace_steps=None):
     torch.cuda.empty_cache()
     Hs, Qs = [x["H"] for x in ins], [x["Q"] for x in ins]
     Wks, Wvs, us = [x["Wk"] for x in ins], [x["Wv"] for x in ins], [x["u"] for x in ins]
-    # logits in the workload's dtype, as the model's LM head emits them
-    logits = [wl.make_logits(w, t, dev).to(wl.torch_dtype(w)) for t in range(2)]
+    # fp32 logits, as the workloads state them
+    logits = [wl.make_logits(w, t, dev) for t in range(2)]
     dL = torch.empty_like(logits[0])
     pipe = Pipeline(w, layers=layers, device=dev, offload=args.offload)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -1022,7 +1020,7 @@ def run_op(args):
     L = wl.make_layer(w, 0, dev)
     H, Wk, Wv = L["H"], L["Wk"], L["Wv"]
     Q = wl.make_queries(w, H, L["Wq"])
-    logits = wl.make_logits(w, 0, dev).to(wl.torch_dtype(w))
+    logits = wl.make_logits(w, 0, dev)
     pipe = Pipeline(w, layers=1, device=dev)
     st = pipe.state[0]
     g = torch.Generator(device=dev).manual_seed(7)
@@ -1038,7 +1036,11 @@ def run_op(args):
     ps.ps_check()
     mu0 = st.mu.clone()
     cur, prev = st.A[1], st.A[0]
-    for _ in range(args.reps):
+    # each call timed with CUDA events on the current stream (the first is
+    # a warm-up when there are several)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.reps + 1)]
+    ev[0].record()
+    for rep in range(args.reps):
         if args.op == "kmeans":
             st.mu.copy_(mu0)
             ps.ps_kmeans_spherical(H, st.mu, st.assign, st.rho, st.chat, st.counts, w.iters,
@@ -1057,10 +1059,13 @@ def run_op(args):
                              ws=pipe.ws[ps.OP_REFRESH])
         else:
             pipe.commit_step(logits)
+        ev[rep + 1].record()
     torch.cuda.synchronize()
     ps.ps_check()
+    us = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(args.reps)]
     print(json.dumps({"op": args.op, "workload": w.name, "B": w.B, "reps": args.reps,
-                      "npos": int(st.npos.sum())}))
+                      "npos": int(st.npos.sum()),
+                      "us_per_call": statistics.median(us[1:] if len(us) > 1 else us)}))
 
 
 def main():

@@ -64,13 +64,12 @@ constexpr int kTileK = 32;       // d per shared-memory stage
 // Early exit of the passes: changed[b * kMaxPasses + t] = 1 once pass t >= 1
 // gave some row of window b another label than pass t - 1.  Pass t of window
 // b runs while every pass 1 .. t - 1 changed a label; the update after pass
-// t runs while every pass 1 .. t did.
+// t runs while every pass 1 .. t did.  A pass raises its flag only if it ran,
+// and it ran only if every pass before it changed a label, so "every pass
+// 1 .. t - 1 changed" is the one flag of pass t - 1 (t >= 2).
 constexpr int kMaxPasses = 64;
 __device__ __forceinline__ bool km_pass_active(const int32_t* changed, int b, int t) {
-  const int32_t* f = changed + (long)b * kMaxPasses;
-  for (int q = 1; q < t; ++q)
-    if (__ldcg(f + q) == 0) return false;
-  return true;
+  return t <= 1 || __ldcg(changed + (long)b * kMaxPasses + t - 1) != 0;
 }
 
 // Allowance for the tensor cores' fp32 accumulation of a bf16 score over d
@@ -778,30 +777,31 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
 }
 
 // Per (cluster c, window b, column slice z): members in ascending row order.
-// The d columns are cut into S slices of W columns (a multiple of 16); the S
-// CTAs of one (c, b) form a thread-block cluster along z.  Each thread owns
-// V consecutive columns (V = 16 bytes of H) of its slice, times G (1 or 2)
-// groups, so a member row costs one 16-byte load per thread, and up to
-// 16 / G member rows are loaded together.  Rows are scanned in blocks of
-// 4096: the block's assignments are staged in shared memory with 16-byte
-// loads, every thread counts the members in its contiguous run of rows, one
-// block scan places them, and the member list sits in shared memory (over the
-// staged assignments, which are all read before the scan); 1/||h|| of a
-// member is loaded with its row.
+// A CTA takes clusters [U x, U x + U) of window y in turn (U from
+// scan_units).  The d columns are cut into S slices of W columns (a
+// multiple of 16); the S CTAs of one (x, b) form a thread-block cluster along
+// z.  Each thread owns V consecutive columns (V = 16 bytes of H) of its
+// slice, times G (1 or 2) groups, so a member row costs one 16-byte load per
+// thread, and up to 16 (G = 1) or 4 (G = 2) member rows are loaded together.
+// Rows are scanned in blocks of 4096: the block's assignments are staged in
+// shared memory with 16-byte loads, every thread counts the members in its
+// contiguous run of rows, one block scan places them, and the member list
+// sits in shared memory (over the staged assignments, which are all read
+// before the scan); 1/||h|| of a member is loaded with its row.
 // Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
 // is empty or its sum is zero), plus its bf16 split; the squared norm is the
 // sum of the slices' partials, read from each CTA's shared memory across the
 // cluster in rank order, so every slice divides by the same number.  Final
 // pass: C_hat_c = mean(rho over members) * mu_c (kept when empty).  Slice 0
-// writes the cluster size; CTA (0, b, 0) folds the pass objective from the
-// tile partials.
+// writes the cluster size; the CTA of cluster 0 and slice 0 folds the pass
+// objective from the tile partials.
 constexpr int kScanRows = 4096;
 constexpr int kMaxColGroups = 2;
 constexpr int kMaxSlices = 8;
 
 template <typename T, bool FINAL, int G, bool FUSED = false>
 __global__ void __launch_bounds__(1024)
-k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
+k_cluster_scan(int U, const T* __restrict__ H, const float* __restrict__ inv,
                const int32_t* __restrict__ assign, const float* __restrict__ rho, int N,
                int d, int C, int W, float* __restrict__ mu, __nv_bfloat16* __restrict__ mu_hi,
                __nv_bfloat16* __restrict__ mu_lo, int32_t* __restrict__ counts,
@@ -811,19 +811,20 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
                float* __restrict__ emax) {
   pdl_prologue();
   constexpr int V = Vec<T>::n;
-  constexpr int kMemb = 16 / G;
+  constexpr int kMemb = G == 1 ? 16 : 4;  // rows loaded together, within 64 registers
   __shared__ __align__(16) int list[kScanRows];  // staged assignments, then members
   __shared__ int s_scan[32];
   __shared__ float s_red[32];
   __shared__ float s_ss;
-  const int c = blockIdx.x, b = blockIdx.y, z = blockIdx.z, S = gridDim.z;
+  const int b = blockIdx.y, z = blockIdx.z, S = gridDim.z;
+  const int c_lo = blockIdx.x * U, c_hi = min(C, c_lo + U);  // this CTA's clusters
   const int tid = threadIdx.x, nthr = blockDim.x;
-  // The pass objective, CTA (0, b, 0): with `changed` (the faster passes)
-  // from the rows' best scores, sum_i best_i / ||h_i|| in a fixed order
+  // The pass objective, by the CTA of cluster 0 and slice 0: with `changed`
+  // (the faster passes) from the rows' best scores, sum_i best_i / ||h_i|| in a fixed order
   // (rho holds the best scores of the latest pass of this window); else from
   // the assignment tiles' partials.
   auto fold_objective = [&]() {
-    if (c != 0 || z != 0 || obj == nullptr) return;  // block-uniform
+    if (c_lo != 0 || z != 0 || obj == nullptr) return;  // block-uniform
     float so = 0.f;
     if (changed != nullptr) {
       for (int i = tid; i < N; i += nthr) so = fmaf(rho[(long)b * N + i], inv[(long)b * N + i], so);
@@ -839,204 +840,214 @@ k_cluster_scan(const T* __restrict__ H, const float* __restrict__ inv,
     fold_objective();
     return;
   }
-  const int col0 = z * W, col1 = min(d, col0 + W);
-  float u[G][V];
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; ++c) {
+    {
+      const int col0 = z * W, col1 = min(d, col0 + W);
+      float u[G][V];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < V; ++e) u[g][e] = 0.f;
-  float rs = 0.f;
-  int n = 0;
-  for (int base = 0; base < N; base += kScanRows) {
-    const int len = min(kScanRows, N - base);
-    const int32_t* ab = assign + (long)b * N + base;
-    if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
-      const int n4 = len >> 2;
-      for (int j = tid; j < n4; j += nthr)
-        reinterpret_cast<int4*>(list)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
-      for (int j = (n4 << 2) + tid; j < len; j += nthr) list[j] = __ldg(ab + j);
-    } else {
-      for (int j = tid; j < len; j += nthr) list[j] = __ldg(ab + j);
-    }
-    __syncthreads();
-    const int R = (len + nthr - 1) / nthr;  // <= 64
-    const int q0 = tid * R;
-    unsigned long long hit = 0ull;
-    int cnt = 0;
-    for (int q = 0; q < R; ++q) {
-      if (q0 + q < len && list[q0 + q] == c) {
-        hit |= 1ull << q;
-        ++cnt;
-      }
-    }
-    const int r0 = base + q0;
-    int tot;
-    int w = block_exclusive_scan<int>(cnt, s_scan, &tot);
-    while (hit) {
-      const int q = __ffsll(hit) - 1;
-      hit &= hit - 1;
-      const int i = r0 + q;
-      list[w] = i;
-      ++w;
-    }
-    __syncthreads();
-    if constexpr (FINAL) {
-      for (int m = tid; m < tot; m += nthr) rs += rho[(long)b * N + list[m]];
-    } else {
-      for (int m = 0; m < tot; m += kMemb) {
-        const int cnt_m = min(kMemb, tot - m);
-        uint4 raw[kMemb][G];
-        float sc[kMemb];
-#pragma unroll
-        for (int q = 0; q < kMemb; ++q) {
-          const long row = (long)b * N + list[m + (q < cnt_m ? q : 0)];
-          sc[q] = q < cnt_m ? __ldg(inv + row) : 0.f;
-          const T* h = H + row * d;
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const int col = col0 + (g * nthr + tid) * V;
-            raw[q][g] = (q < cnt_m && col < col1)
-                            ? __ldg(reinterpret_cast<const uint4*>(h + col))
-                            : make_uint4(0u, 0u, 0u, 0u);
+        for (int e = 0; e < V; ++e) u[g][e] = 0.f;
+      float rs = 0.f;
+      int n = 0;
+      for (int base = 0; base < N; base += kScanRows) {
+        const int len = min(kScanRows, N - base);
+        const int32_t* ab = assign + (long)b * N + base;
+        if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
+          const int n4 = len >> 2;
+          for (int j = tid; j < n4; j += nthr)
+            reinterpret_cast<int4*>(list)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
+          for (int j = (n4 << 2) + tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+        } else {
+          for (int j = tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+        }
+        __syncthreads();
+        const int R = (len + nthr - 1) / nthr;  // <= 64
+        const int q0 = tid * R;
+        unsigned long long hit = 0ull;
+        int cnt = 0;
+        for (int q = 0; q < R; ++q) {
+          if (q0 + q < len && list[q0 + q] == c) {
+            hit |= 1ull << q;
+            ++cnt;
           }
         }
+        const int r0 = base + q0;
+        int tot;
+        int w = block_exclusive_scan<int>(cnt, s_scan, &tot);
+        while (hit) {
+          const int q = __ffsll(hit) - 1;
+          hit &= hit - 1;
+          const int i = r0 + q;
+          list[w] = i;
+          ++w;
+        }
+        __syncthreads();
+        if constexpr (FINAL) {
+          for (int m = tid; m < tot; m += nthr) rs += rho[(long)b * N + list[m]];
+        } else {
+          for (int m = 0; m < tot; m += kMemb) {
+            const int cnt_m = min(kMemb, tot - m);
+            uint4 raw[kMemb][G];
+            float sc[kMemb];
 #pragma unroll
-        for (int q = 0; q < kMemb; ++q) {
+            for (int q = 0; q < kMemb; ++q) {
+              const long row = (long)b * N + list[m + (q < cnt_m ? q : 0)];
+              sc[q] = q < cnt_m ? __ldg(inv + row) : 0.f;
+              const T* h = H + row * d;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float v[V];
-            unpack16(raw[q][g], v, T{});
+              for (int g = 0; g < G; ++g) {
+                const int col = col0 + (g * nthr + tid) * V;
+                raw[q][g] = (q < cnt_m && col < col1)
+                                ? __ldg(reinterpret_cast<const uint4*>(h + col))
+                                : make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
 #pragma unroll
-            for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc[q], u[g][e]);
+            for (int q = 0; q < kMemb; ++q) {
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                float v[V];
+                unpack16(raw[q][g], v, T{});
+#pragma unroll
+                for (int e = 0; e < V; ++e) u[g][e] = fmaf(v[e], sc[q], u[g][e]);
+              }
+            }
           }
         }
+        n += tot;
+        __syncthreads();
+      }
+      if (c == c_lo) fold_objective();
+      // fused last update + final pass: the final labels' members give the
+      // count and the mean rho of C_hat
+      int n_fin = n;
+      float rs_fin = 0.f;
+      if constexpr (FUSED) {  // assign_fin: the final labels
+        int cnt = 0;
+        for (int i = tid; i < N; i += nthr)
+          if (__ldg(assign_fin + (long)b * N + i) == c) {
+            rs_fin += rho[(long)b * N + i];
+            ++cnt;
+          }
+        block_exclusive_scan<int>(cnt, s_scan, &n_fin);
+        rs_fin = block_sum_f32(rs_fin, s_red);
+      }
+      if (z == 0 && tid == 0) counts[(long)b * C + c] = n_fin;
+      if constexpr (FINAL) {
+        const float tot = block_sum_f32(rs, s_red);
+        if (n == 0) goto next_cluster;  // block-uniform
+        const float mean = tot / (float)n;
+        const float* mc = mu + ((long)b * C + c) * d;
+        float* o = chat + ((long)b * C + c) * d;
+        for (int k = col0 + tid; k < col1; k += nthr) o[k] = mean * mc[k];
+      } else {
+        float ss = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
+        ss = block_sum_f32(ss, s_red);
+        if (S > 1) {  // every CTA of the cluster reaches the barrier and the wait below
+          if (tid == 0) s_ss = ss;
+          tc::cluster_sync_all();
+          if (tid == 0) {
+            const uint32_t a = tc::smem_u32(&s_ss);
+            float part[kMaxSlices];
+#pragma unroll
+            for (int r = 0; r < kMaxSlices; ++r)
+              part[r] = r < S ? tc::ld_dsmem_f32(tc::cluster_map(a, r)) : 0.f;
+            float t = 0.f;
+#pragma unroll
+            for (int r = 0; r < kMaxSlices; ++r)
+              if (r < S) t += part[r];
+            s_red[0] = t;
+          }
+          tc::cluster_arrive();
+          __syncthreads();
+          ss = s_red[0];
+        }
+        const float nu = sqrtf(ss);
+        const bool formed = n > 0 && nu > 0.f;  // else the centroid is kept
+        if (!FUSED && !formed) {
+          if (S > 1) tc::cluster_wait();
+          goto next_cluster;
+        }
+        const long ro = ((long)b * C + c) * d;
+        const float mean = (FUSED && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
+        float e2 = 0.f;  // ||mu_c - bf16(mu_c)||^2 over this slice's columns
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int col = col0 + (g * nthr + tid) * V;
+          if (col < col1) {  // V consecutive columns: 16-byte fp32 stores, 8- or 16-byte bf16
+            float x[V];
+            if (formed) {
+#pragma unroll
+              for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
+              if (emax != nullptr) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                  const float dv = x[e] - __bfloat162float(__float2bfloat16_rn(x[e]));
+                  e2 = fmaf(dv, dv, e2);
+                }
+              }
+              float4* mo = reinterpret_cast<float4*>(mu + ro + col);
+#pragma unroll
+              for (int e = 0; e < V; e += 4)
+                mo[e / 4] = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+              if (mu_hi != nullptr) {
+                uint32_t hi[V / 2], lo[V / 2];
+#pragma unroll
+                for (int e = 0; e < V; e += 2) {
+                  const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
+                  const float2 hf = __bfloat1622float2(h);
+                  const __nv_bfloat162 l = __floats2bfloat162_rn(x[e] - hf.x, x[e + 1] - hf.y);
+                  hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                  lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
+                }
+                if constexpr (V == 8) {
+                  *reinterpret_cast<uint4*>(mu_hi + ro + col) =
+                      make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                  *reinterpret_cast<uint4*>(mu_lo + ro + col) =
+                      make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                } else {
+                  *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
+                  *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
+                }
+              }
+            } else if (FUSED && n_fin > 0) {
+              const float4* mi = reinterpret_cast<const float4*>(mu + ro + col);
+#pragma unroll
+              for (int e = 0; e < V; e += 4) {
+                const float4 m4 = mi[e / 4];
+                x[e] = m4.x; x[e + 1] = m4.y; x[e + 2] = m4.z; x[e + 3] = m4.w;
+              }
+            }
+            if (FUSED && n_fin > 0) {
+              float4* co = reinterpret_cast<float4*>(chat + ro + col);
+#pragma unroll
+              for (int e = 0; e < V; e += 4)
+                co[e / 4] =
+                    make_float4(mean * x[e], mean * x[e + 1], mean * x[e + 2], mean * x[e + 3]);
+            }
+          }
+        }
+        // the bf16 rounding bound of the window's centroids: this slice's share
+        // of ||mu_c - bf16(mu_c)|| times sqrt(S) bounds the whole row's (its
+        // square is at most S times the largest slice's)
+        if (emax != nullptr && formed) {  // block-uniform
+          e2 = block_sum_f32(e2, s_red);
+          if (tid == 0) atomicMax(reinterpret_cast<int*>(emax) + b, __float_as_int(sqrtf(e2 * S)));
+        }
+        // no CTA leaves while another still reads its s_ss
+        if (S > 1) tc::cluster_wait();
       }
     }
-    n += tot;
-    __syncthreads();
+  next_cluster:
+    __syncthreads();  // the shared arrays serve the next cluster
   }
   pdl_trigger();
-  fold_objective();
-  // fused last update + final pass: the final labels' members give the
-  // count and the mean rho of C_hat
-  int n_fin = n;
-  float rs_fin = 0.f;
-  if constexpr (FUSED) {  // assign_fin: the final labels
-    int cnt = 0;
-    for (int i = tid; i < N; i += nthr)
-      if (__ldg(assign_fin + (long)b * N + i) == c) {
-        rs_fin += rho[(long)b * N + i];
-        ++cnt;
-      }
-    block_exclusive_scan<int>(cnt, s_scan, &n_fin);
-    rs_fin = block_sum_f32(rs_fin, s_red);
-  }
-  if (z == 0 && tid == 0) counts[(long)b * C + c] = n_fin;
-  if constexpr (FINAL) {
-    const float tot = block_sum_f32(rs, s_red);
-    if (n == 0) return;
-    const float mean = tot / (float)n;
-    const float* mc = mu + ((long)b * C + c) * d;
-    float* o = chat + ((long)b * C + c) * d;
-    for (int k = col0 + tid; k < col1; k += nthr) o[k] = mean * mc[k];
-  } else {
-    float ss = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < V; ++e) ss = fmaf(u[g][e], u[g][e], ss);
-    ss = block_sum_f32(ss, s_red);
-    if (S > 1) {  // every CTA of the cluster reaches the barrier and the wait below
-      if (tid == 0) s_ss = ss;
-      tc::cluster_sync_all();
-      if (tid == 0) {
-        const uint32_t a = tc::smem_u32(&s_ss);
-        float part[kMaxSlices];
-#pragma unroll
-        for (int r = 0; r < kMaxSlices; ++r)
-          part[r] = r < S ? tc::ld_dsmem_f32(tc::cluster_map(a, r)) : 0.f;
-        float t = 0.f;
-#pragma unroll
-        for (int r = 0; r < kMaxSlices; ++r)
-          if (r < S) t += part[r];
-        s_red[0] = t;
-      }
-      tc::cluster_arrive();
-      __syncthreads();
-      ss = s_red[0];
-    }
-    const float nu = sqrtf(ss);
-    const bool formed = n > 0 && nu > 0.f;  // else the centroid is kept
-    if (!FUSED && !formed) {
-      if (S > 1) tc::cluster_wait();
-      return;
-    }
-    const long ro = ((long)b * C + c) * d;
-    const float mean = (FUSED && n_fin > 0) ? rs_fin / (float)n_fin : 0.f;
-    float e2 = 0.f;  // ||mu_c - bf16(mu_c)||^2 over this slice's columns
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const int col = col0 + (g * nthr + tid) * V;
-      if (col < col1) {  // V consecutive columns: 16-byte fp32 stores, 8- or 16-byte bf16
-        float x[V];
-        if (formed) {
-#pragma unroll
-          for (int e = 0; e < V; ++e) x[e] = u[g][e] / nu;
-          if (emax != nullptr) {
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-              const float dv = x[e] - __bfloat162float(__float2bfloat16_rn(x[e]));
-              e2 = fmaf(dv, dv, e2);
-            }
-          }
-          float4* mo = reinterpret_cast<float4*>(mu + ro + col);
-#pragma unroll
-          for (int e = 0; e < V; e += 4)
-            mo[e / 4] = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-          if (mu_hi != nullptr) {
-            uint32_t hi[V / 2], lo[V / 2];
-#pragma unroll
-            for (int e = 0; e < V; e += 2) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
-              const float2 hf = __bfloat1622float2(h);
-              const __nv_bfloat162 l = __floats2bfloat162_rn(x[e] - hf.x, x[e + 1] - hf.y);
-              hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
-              lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
-            }
-            if constexpr (V == 8) {
-              *reinterpret_cast<uint4*>(mu_hi + ro + col) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4*>(mu_lo + ro + col) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            } else {
-              *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
-              *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
-            }
-          }
-        } else if (FUSED && n_fin > 0) {
-          const float4* mi = reinterpret_cast<const float4*>(mu + ro + col);
-#pragma unroll
-          for (int e = 0; e < V; e += 4) {
-            const float4 m4 = mi[e / 4];
-            x[e] = m4.x; x[e + 1] = m4.y; x[e + 2] = m4.z; x[e + 3] = m4.w;
-          }
-        }
-        if (FUSED && n_fin > 0) {
-          float4* co = reinterpret_cast<float4*>(chat + ro + col);
-#pragma unroll
-          for (int e = 0; e < V; e += 4)
-            co[e / 4] = make_float4(mean * x[e], mean * x[e + 1], mean * x[e + 2], mean * x[e + 3]);
-        }
-      }
-    }
-    // the bf16 rounding bound of the window's centroids: this slice's share
-    // of ||mu_c - bf16(mu_c)|| times sqrt(S) bounds the whole row's (its
-    // square is at most S times the largest slice's)
-    if (emax != nullptr && formed) {  // block-uniform
-      e2 = block_sum_f32(e2, s_red);
-      if (tid == 0) atomicMax(reinterpret_cast<int*>(emax) + b, __float_as_int(sqrtf(e2 * S)));
-    }
-    // no CTA leaves while another still reads its s_ss
-    if (S > 1) tc::cluster_wait();
-  }
 }
 
 // Column slices of the cluster scan: enough (<= 8, a power of two) that the
@@ -1060,10 +1071,20 @@ ScanPlan scan_plan(int B, int d, int C) {
   return p;
 }
 
+// Clusters a scan CTA takes in turn (U): 1 while the C x B x S CTAs are
+// about a wave, up to 8 when there are many more, so that a pass whose
+// windows have all settled launches few CTAs (each checks its window's flag
+// once and leaves) while a working pass keeps several waves of CTAs.
+int scan_units(int B, int C, int S) {
+  const long ctas = (long)C * B * S;
+  return (int)std::max(1L, std::min(8L, ctas / (8L * kSmTarget)));
+}
+
 template <typename T, bool FINAL, bool FUSED = false, typename... Args>
 cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&... args) {
+  const int U = scan_units(B, C, p.S);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, B, p.S);
+  cfg.gridDim = dim3(ceil_div(C, U), B, p.S);
   cfg.blockDim = dim3(p.threads);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1075,9 +1096,10 @@ cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&.
   attr[1].val.clusterDim.z = p.S;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return p.G == 1 ? launch_ex(cfg, k_cluster_scan<T, FINAL, 1, FUSED>, std::forward<Args>(args)...)
-                  : launch_ex(cfg, k_cluster_scan<T, FINAL, kMaxColGroups, FUSED>,
-                              std::forward<Args>(args)...);
+  return p.G == 1
+             ? launch_ex(cfg, k_cluster_scan<T, FINAL, 1, FUSED>, U, std::forward<Args>(args)...)
+             : launch_ex(cfg, k_cluster_scan<T, FINAL, kMaxColGroups, FUSED>, U,
+                         std::forward<Args>(args)...);
 }
 
 // PS_KMEANS_LLOYD set in the environment keeps every pass in the Lloyd form

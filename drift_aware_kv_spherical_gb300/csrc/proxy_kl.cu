@@ -899,6 +899,234 @@ struct ProxySoloEpi : TcEpiBase {
   __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
 };
 
+// Proxy epilogue for C in (128, 256] with one CTA per row tile taking all
+// its heads, a head's scores in two 128-column parts (two MMA tiles, each in
+// its own accumulator, double-buffered) and the head sum A (256 columns,
+// fp32) in the rest of TMEM.  P epilogue warps per TMEM lane quarter (4 P in
+// all), each taking W = 128 / P columns of each part of its 32 rows, in
+// chunks of 32 columns:
+//   part 0: per chunk the max m of its scores and e = 2^(s' - m), kept in
+//           registers, with their sum s, so the part's accumulator goes back
+//           to the MMA at once (the next head's part 0 is computed under the
+//           rest of this epilogue);
+//   part 1: the same, e written back over the scores;
+//   the P warps of a row exchange their chunks' (m, s) through shared
+//   memory once (fixed order): M = max m, S = sum s 2^(m - M); then
+//   A += e 2^(m - M) / S for every chunk (s' = score / sqrt(dh) in base 2).
+// After the row tile's last head: A / Hq, KL against A_prev, stores.  The
+// softmax terms are those of one pass over the row up to rounding.  With
+// P = 2 (8 epilogue warps, 10 in all) a thread has 168 registers, room for
+// part 0's terms next to one chunk of part 1's scores; with P = 4 it has 96.
+template <int P>
+struct ProxyHalvesEpi : TcEpiBase {
+  static constexpr int kEpiWarps = 4 * P;
+  static constexpr int BN_T = 128;     // columns of a part (one MMA tile)
+  static constexpr int W = BN_T / P;   // columns a thread takes of each part
+  static constexpr int NCH = W / 32;   // 32-column chunks of a thread's part
+  static constexpr int kExtraCols = 2 * BN_T;
+  static constexpr bool kA3D = true;
+  static constexpr bool kBlocked = true;
+  static_assert(W % 32 == 0, "32-column chunks");
+  // two exchange slots of 128 x P threads x 2 NCH (m, s) pairs
+  static constexpr int kSlot = 128 * P * 4 * NCH;  // floats
+  static_assert(2 * kSlot * 4 <= (int)TcCfg<BN_T, 1, 2, false>::kScratch, "scratch");
+  int B, N, C, Hq, G, dh, mtb;
+  float scale;
+  const float* A_prev;
+  float* A_cur;
+  float* D;
+  struct State {
+    float e0[W];  // part 0's exponentials, each chunk against its own max
+    float m0[NCH], s0[NCH];
+    uint32_t extra;
+  };
+  __device__ int tiles(int) const { return B * mtb * Hq * 2; }
+  __device__ int arow(int t) const {
+    const int bm = t / (Hq * 2);
+    return (bm / mtb) * N + (bm % mtb) * 128;
+  }
+  __device__ int ahead(int t) const { return (t / 2) % Hq; }
+  __device__ int bcoord(int t, int) const { return (t / (Hq * 2) / mtb) * C + (t % 2) * BN_T; }
+  __device__ int bkoff(int t) const { return (((t / 2) % Hq) / G) * dh; }
+
+  // 32 scores v (raw TMEM words; n < 32: only the first n count, n >= 1):
+  // m = sl * max v, e = 2^(v sl - m) in place, their sum
+  template <bool kFull>
+  __device__ __forceinline__ void exp_chunk(uint32_t* v, int n, float sl, float& m,
+                                            float& sum) const {
+    if constexpr (!kFull) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j >= n) v[j] = __float_as_uint(-INFINITY);
+    }
+    float mx[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mx[j] = fmaxf(fmaxf(__uint_as_float(v[j]), __uint_as_float(v[j + 8])),
+                    fmaxf(__uint_as_float(v[j + 16]), __uint_as_float(v[j + 24])));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
+    m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
+    float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float e = ex2_approx(fmaf(__uint_as_float(v[j]), sl, -m));
+      sp[j & 3] += e;
+      v[j] = __float_as_uint(e);
+    }
+    sum = (sp[0] + sp[1]) + (sp[2] + sp[3]);
+  }
+
+  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
+                               State& st) const {
+    // the part as a constant, so that e0 stays in registers
+    if (t % 2 == 0)
+      part0(q, taddr, st);
+    else
+      part1(t, r, q, taddr, scratch, st);
+  }
+
+  __device__ __forceinline__ void part0(int q, uint32_t taddr, State& st) const {
+    constexpr float kLog2e = 1.4426950408889634f;
+    uint32_t v[W];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) tc::tmem_ld32_nowait(taddr + q * W + 32 * k, v + 32 * k);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < NCH; ++k)  // C > 128: part 0 is whole
+      exp_chunk<true>(v + 32 * k, 32, scale * kLog2e, st.m0[k], st.s0[k]);
+#pragma unroll
+    for (int j = 0; j < W; ++j) st.e0[j] = __uint_as_float(v[j]);
+  }
+
+  __device__ __forceinline__ void part1(int t, int r, int q, uint32_t taddr, uint8_t* scratch,
+                                        State& st) const {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const int h = (t / 2) % Hq;
+    // part 1, a chunk at a time: columns 128 + q W + 32 k ..; a chunk past
+    // column C is left out (max -inf, weight 0)
+    float m1[NCH], s1[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      const int n = C - BN_T - q * W - 32 * k;
+      m1[k] = -INFINITY;
+      s1[k] = 0.f;
+      if (n > 0) {
+        uint32_t v[32];
+        tc::tmem_ld32_nowait(taddr + q * W + 32 * k, v);
+        tc::tmem_wait_ld();
+        if (n >= 32)
+          exp_chunk<true>(v, 32, scale * kLog2e, m1[k], s1[k]);
+        else
+          exp_chunk<false>(v, n, scale * kLog2e, m1[k], s1[k]);
+        tc::tmem_st32(taddr + q * W + 32 * k, v);
+      }
+    }
+    // the row's max and sum from the chunks of its P threads, in order
+    float4* xs = reinterpret_cast<float4*>(reinterpret_cast<float*>(scratch) + (h & 1) * kSlot);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k)
+      xs[(r * P + q) * NCH + k] = make_float4(st.m0[k], st.s0[k], m1[k], s1[k]);
+    epi_bar_sync_n<32 * kEpiWarps>();
+    float4 x[P * NCH];
+#pragma unroll
+    for (int k = 0; k < P * NCH; ++k) x[k] = xs[r * P * NCH + k];
+    float mr = fmaxf(x[0].x, x[0].z);
+#pragma unroll
+    for (int k = 1; k < P * NCH; ++k) mr = fmaxf(mr, fmaxf(x[k].x, x[k].z));
+    float sr = 0.f;
+#pragma unroll
+    for (int k = 0; k < P * NCH; ++k) {  // a left-out chunk adds 0 x 2^-inf = 0
+      sr = fmaf(x[k].y, ex2_approx(x[k].x - mr), sr);
+      sr = fmaf(x[k].w, ex2_approx(x[k].z - mr), sr);
+    }
+    const float rs = 1.0f / sr;
+    const bool first = h == 0;
+    const uint32_t a0 = st.extra + q * W, a1 = st.extra + BN_T + q * W;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      const float f0 = ex2_approx(st.m0[k] - mr) * rs;
+      uint32_t a[32];
+      if (first) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(st.e0[32 * k + j] * f0);
+      } else {
+        tc::tmem_ld32_nowait(a0 + 32 * k, a);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a[j] = __float_as_uint(fmaf(st.e0[32 * k + j], f0, __uint_as_float(a[j])));
+      }
+      tc::tmem_st32(a0 + 32 * k, a);
+    }
+    // e0 is dead until the next part 0 writes it: constants need no registers
+#pragma unroll
+    for (int j = 0; j < W; ++j) st.e0[j] = 0.f;
+    tc::tmem_wait_st();  // part 1's terms written back before they are read
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      // columns at or past C of A are never read: a left-out chunk's weight
+      // only has to be finite
+      const float f1 = m1[k] == -INFINITY ? 0.f : ex2_approx(m1[k] - mr) * rs;
+      uint32_t e[32], a[32];
+      tc::tmem_ld32_nowait(taddr + q * W + 32 * k, e);
+      if (!first) tc::tmem_ld32_nowait(a1 + 32 * k, a);
+      tc::tmem_wait_ld();
+      if (first) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(__uint_as_float(e[j]) * f1);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a[j] = __float_as_uint(fmaf(__uint_as_float(e[j]), f1, __uint_as_float(a[j])));
+      }
+      tc::tmem_st32(a1 + 32 * k, a);
+    }
+    tc::tmem_wait_st();
+    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
+  }
+
+  // A / Hq and the KL of the row: each thread its W columns of each part,
+  // 8 at a time; the P warps' KL partials summed in warp order
+  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
+    const int bm = t / (Hq * 2), b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const bool live = i < N, prev = A_prev != nullptr;
+    const long row = (long)b * N + i;
+    const float hq = (float)Hq;
+    float kl = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < 2 * W; k += 8) {  // once per row tile
+      const int c0 = (k / W) * BN_T + q * W + k % W;
+      uint32_t a[8];
+      tc::tmem_ld8_nowait(st.extra + c0, a);  // warp-collective
+      tc::tmem_wait_ld();
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + j;
+        if (c < C) {
+          const float av = __uint_as_float(a[j]) / hq;
+          A_cur[row * C + c] = av;
+          if (prev && av > 0.f) kl += av * logf(av / fmaxf(A_prev[row * C + c], 1e-30f));
+        }
+      }
+    }
+    // the exchange slot the previous head used: every thread has read it
+    // before this head's exchange barrier, and the next row tile's first
+    // exchange waits for this epilogue's part-1 accumulator
+    float* zs = xs + (Hq & 1) * kSlot;
+    zs[r * P + q] = kl;
+    epi_bar_sync_n<32 * kEpiWarps>();
+    if (q == 0 && live) {
+      float sum = zs[r * P];
+#pragma unroll
+      for (int k = 1; k < P; ++k) sum += zs[r * P + k];
+      D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
+    }
+  }
+  __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
+};
+
 // Head slices of one row tile inside one thread-block cluster: CTA z runs
 // heads [z hps, (z+1) hps) of row tile blockIdx.y and leaves its head sum in
 // shared memory; then CTA z finishes rows [128 z / Z, 128 (z+1) / Z), one
@@ -1137,10 +1365,26 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   constexpr int P = BN > 64 ? 2 : 1;
   const float scale = (float)(1.0 / std::sqrt((double)a.dh));
   if constexpr (BN == 256) {
-    if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
-      ProxySoloEpi pe{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
-                      a.A_cur, a.D};
-      return launch_tc_gemm<256, 1, 2, false>(maps, sh, pe, dim3(1, a.B * p.mtb, 1), s);
+    if (p.nslice == 1) {  // a CTA per row tile, two 128-column parts, the head sum in TMEM
+      TcMaps m2 = maps;
+      if (!make_tmap_bf16_2d(&m2.b[0], w.khi, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                             128) ||
+          !make_tmap_bf16_2d(&m2.b[1], w.klo, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
+                             128))
+        return cudaErrorInvalidValue;
+      if (std::getenv("PS_PROXY_SOLO") != nullptr) {
+        ProxySoloEpi pe{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+                        a.A_cur, a.D};
+        return launch_tc_gemm<256, 1, 2, false>(maps, sh, pe, dim3(1, a.B * p.mtb, 1), s);
+      }
+      if (std::getenv("PS_PROXY_H4") != nullptr) {
+        ProxyHalvesEpi<4> he{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale,
+                             a.A_prev, a.A_cur, a.D};
+        return launch_tc_gemm<128, 1, 2, false>(m2, sh, he, dim3(1, a.B * p.mtb, 1), s);
+      }
+      ProxyHalvesEpi<2> he{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+                           a.A_cur, a.D};
+      return launch_tc_gemm<128, 1, 2, false>(m2, sh, he, dim3(1, a.B * p.mtb, 1), s);
     }
   }
   if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
