@@ -23,7 +23,10 @@
 //                   sum in registers; the head slices of a row tile
 //                   (<= 8) form a thread-block cluster that sums them in
 //                   slice order through distributed shared memory, divides
-//                   by Hq and takes KL
+//                   by Hq and takes KL.  With at least one row tile per SM,
+//                   one CTA takes all heads of a row tile and keeps the head
+//                   sum in TMEM (ProxyTmemEpi for C <= 128; ProxyHalvesEpi,
+//                   a head's scores in two 128-column tiles, for C > 128)
 // Every reduction has a fixed order, so identical inputs give identical
 // bits and KL(A || A) is exactly 0.
 #include <algorithm>
@@ -546,54 +549,46 @@ struct ProxyEpi : TcEpiBase {
   }
 };
 
-// Proxy epilogue with the head sum in TMEM, for one CTA per row tile taking
-// all its heads (enough row tiles to fill the GPU).  A head's BN score
-// columns come in NP parts of BN_T = BN / NP columns (NP = 2 when BN = 256),
-// each its own tile, so the two accumulator buffers (2 BN_T columns) and
-// the head sum A (BN columns, fp32) fit the 512 TMEM columns.  Sixteen
-// epilogue warps: the four of a TMEM lane quarter take W = BN_T / 4 columns
-// of each part of their 32 rows and meet through shared memory for a row's
-// max and sum (fixed order).  consume(): a part's scores, its row max m_p,
-// e = 2^(s' - m_p) kept in registers, its row sum s_p (s' = score / sqrt(dh)
-// in base 2).  After the last part, with m = max over the parts, each part's
-// weight is 2^(m_p - m) / sum_p s_p 2^(m_p - m).  tile_done(), which the
-// engine calls once the accumulator is handed back to the MMA, adds the
-// weighted terms of both parts into A in TMEM, so the next tile's MMAs run
-// under it; after the row tile's last head: A / Hq, KL against A_prev,
-// stores.  The softmax terms are those of one pass over all C columns up to
-// rounding.
-template <int BN_T, int NP>
+// Proxy epilogue with the head sum in TMEM, for C <= 128 and one CTA per
+// row tile taking all its heads (enough row tiles to fill the GPU): the two
+// accumulator buffers (2 BN columns) and the head sum A (BN columns, fp32)
+// in TMEM.  Sixteen epilogue warps: the four of a TMEM lane quarter take
+// W = BN / 4 columns of their 32 rows and meet through shared memory for a
+// row's max and sum (fixed order).  consume(): the scores, the row max m,
+// e = 2^(s' - m) kept in registers, the row sum (s' = score / sqrt(dh) in
+// base 2).  tile_done(), which the engine calls once the accumulator is
+// handed back to the MMA, adds e / sum into A in TMEM, so the next head's
+// MMAs run under it; after the row tile's last head: A / Hq, KL against
+// A_prev, stores.
+template <int BN>
 struct ProxyTmemEpi : TcEpiBase {
   static constexpr int kEpiWarps = 16;
   static constexpr int P = 4;            // epilogue warps per lane quarter
-  static constexpr int W = BN_T / P;     // columns a thread takes of each part
-  static constexpr int BN = BN_T * NP;
+  static constexpr int W = BN / P;       // columns a thread takes
   static constexpr int kExtraCols = BN;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   static_assert(W % 8 == 0 && W <= 32, "part width");
-  // per part a (max, sum) exchange of 2 x 128 x P floats; KL at 4 x 128 x P
-  static_assert(NP <= 2 && 5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
+  // a (max, sum) exchange of 2 x 128 x P floats; KL at 4 x 128 x P
+  static_assert(5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb;
   float scale;
   const float* A_prev;
   float* A_cur;
   float* D;
   struct State {
-    float e[NP][W];  // this head's exponentials, against each part's own max
-    float m[NP], s[NP];
+    float e[W];  // this head's exponentials
+    float s;
     uint32_t extra;
   };
-  __device__ int tiles(int) const { return B * mtb * Hq * NP; }
+  __device__ int tiles(int) const { return B * mtb * Hq; }
   __device__ int arow(int t) const {
-    const int bm = t / (Hq * NP);
+    const int bm = t / Hq;
     return (bm / mtb) * N + (bm % mtb) * 128;
   }
-  __device__ int ahead(int t) const { return (t / NP) % Hq; }
-  __device__ int bcoord(int t, int) const {
-    return (t / (Hq * NP) / mtb) * C + (t % NP) * BN_T;
-  }
-  __device__ int bkoff(int t) const { return (((t / NP) % Hq) / G) * dh; }
+  __device__ int ahead(int t) const { return t % Hq; }
+  __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
+  __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
 
   // the row's value from the four warps of a lane quarter (slot: 128 x 4
   // floats of the scratch), combined in warp order
@@ -607,31 +602,22 @@ struct ProxyTmemEpi : TcEpiBase {
     return x;
   }
 
-  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
+  __device__ void consume_part(int, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
                                State& st) const {
-    // the part as a constant, so that the State arrays stay in registers
-    if (NP == 1 || t % NP == 0)
-      consume_p<0>(r, q, taddr, scratch, st);
-    else
-      consume_p<NP - 1>(r, q, taddr, scratch, st);
-  }
-  template <int p>
-  __device__ __forceinline__ void consume_p(int r, int q, uint32_t taddr, uint8_t* scratch,
-                                            State& st) const {
     constexpr float kLog2e = 1.4426950408889634f;
     const float sl = scale * kLog2e;
-    const int cq = p * BN_T + q * W;  // this thread's first score column of the head
-    float* xs = reinterpret_cast<float*>(scratch) + p * 2 * 128 * P;
+    const int cq = q * W;  // this thread's first score column
+    float* xs = reinterpret_cast<float*>(scratch);
     float m = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < W; k += 8) {  // 8 columns a load: both parts' terms fill the registers
+    for (int k = 0; k < W; k += 8) {
       uint32_t raw[8];
-      tc::tmem_ld8_nowait(taddr + q * W + k, raw);
+      tc::tmem_ld8_nowait(taddr + cq + k, raw);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float v = cq + k + j < C ? __uint_as_float(raw[j]) * sl : -INFINITY;
-        st.e[p][k + j] = v;
+        st.e[k + j] = v;
         m = fmaxf(m, v);
       }
     }
@@ -639,75 +625,57 @@ struct ProxyTmemEpi : TcEpiBase {
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      st.e[p][j] = ex2_approx(st.e[p][j] - m);
-      s += st.e[p][j];
+      st.e[j] = ex2_approx(st.e[j] - m);
+      s += st.e[j];
     }
-    st.m[p] = m;
-    st.s[p] = row_combine<false>(s, xs + 128 * P, r, q);
+    st.s = row_combine<false>(s, xs + 128 * P, r, q);
   }
 
-  // A[cols] (+)= f * x, 8 columns at a time, in TMEM; `first`: A = f * x
-  __device__ __forceinline__ void add_a(uint32_t at, const float* x, float f, bool first) const {
+  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t* scratch,
+                                 State& st) const {
+    const int h = t % Hq;
+    const float f = 1.0f / st.s;
+    const uint32_t at = st.extra + q * W;
 #pragma unroll
     for (int k = 0; k < W; k += 8) {
       uint32_t a[8];
-      if (first) {
+      if (h == 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = __float_as_uint(x[k + j] * f);
+        for (int j = 0; j < 8; ++j) a[j] = __float_as_uint(st.e[k + j] * f);
       } else {
         tc::tmem_ld8_nowait(at + k, a);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          a[j] = __float_as_uint(fmaf(x[k + j], f, __uint_as_float(a[j])));
+          a[j] = __float_as_uint(fmaf(st.e[k + j], f, __uint_as_float(a[j])));
       }
       tc::tmem_st8(at + k, a);
     }
-  }
-
-  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t* scratch,
-                                 State& st) const {
-    if (t % NP != NP - 1) return;  // tile-uniform: after a head's last part
-    const int h = (t / NP) % Hq;
-    float m = st.m[0];
-#pragma unroll
-    for (int p = 1; p < NP; ++p) m = fmaxf(m, st.m[p]);
-    float f[NP], s = 0.f;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      f[p] = ex2_approx(st.m[p] - m);
-      s = fmaf(st.s[p], f[p], s);
-    }
-    const float rs = 1.0f / s;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) add_a(st.extra + p * BN_T + q * W, st.e[p], f[p] * rs, h == 0);
     tc::tmem_wait_st();
     if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
   }
 
-  // A / Hq and the KL of the row: each thread its W columns of each part,
-  // the four warps' KL partials summed in warp order
+  // A / Hq and the KL of the row: each thread its W columns, the four
+  // warps' KL partials summed in warp order
   __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
-    const int bm = t / (Hq * NP), b = bm / mtb, i = (bm % mtb) * 128 + r;
+    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
     const bool live = i < N, prev = A_prev != nullptr;
     const long row = (long)b * N + i;
     const float hq = (float)Hq;
     float kl = 0.f;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      uint32_t raw[W];
-      if constexpr (W == 32) {
-        tc::tmem_ld32_nowait(st.extra + p * BN_T + q * W, raw);
-      } else if constexpr (W == 16) {
-        tc::tmem_ld16_nowait(st.extra + p * BN_T + q * W, raw);
-      } else {
-        tc::tmem_ld8_nowait(st.extra + p * BN_T + q * W, raw);
-      }
-      tc::tmem_wait_ld();
-      if (!live) continue;
+    uint32_t raw[W];
+    if constexpr (W == 32) {
+      tc::tmem_ld32_nowait(st.extra + q * W, raw);
+    } else if constexpr (W == 16) {
+      tc::tmem_ld16_nowait(st.extra + q * W, raw);
+    } else {
+      tc::tmem_ld8_nowait(st.extra + q * W, raw);
+    }
+    tc::tmem_wait_ld();
+    if (live) {
 #pragma unroll
       for (int j = 0; j < W; ++j) {
-        const int c = p * BN_T + q * W + j;
+        const int c = q * W + j;
         if (c < C) {
           const float a = __uint_as_float(raw[j]) / hq;
           A_cur[row * C + c] = a;
@@ -721,204 +689,23 @@ struct ProxyTmemEpi : TcEpiBase {
 };
 
 // Proxy epilogue for C in (128, 256] with one CTA per row tile taking all
-// its heads: a head's 256 score columns in one accumulator and the head sum
-// A (256 columns, fp32) in the other half of TMEM, so the accumulator is
-// single-buffered (the next head's MMAs wait for this epilogue; the TMA
-// copies run ahead).  Sixteen epilogue warps, four per TMEM lane quarter,
-// each taking 64 columns of its 32 rows in few TMEM round trips:
-//   pass 1: the scores (two 32-column loads, one wait), their max m_q over
-//           the thread's columns, e = 2^(s' - m_q) written back over them,
-//           and their sum s_q (s' = score / sqrt(dh) in base 2);
-//   the four warps of a row exchange (m_q, s_q) through shared memory once
-//   (fixed order): m = max m_q, s = sum s_q 2^(m_q - m);
-//   pass 2: A += e 2^(m_q - m) / s, 32 columns at a time (e and A read
-//           together, one wait).
-// After the row tile's last head: A / Hq, KL against A_prev, stores.  The
-// softmax terms are those of one pass over the row up to rounding (the
-// rescale 2^(m_q - m) is 1 for the warp holding the max).
-struct ProxySoloEpi : TcEpiBase {
-  static constexpr int kEpiWarps = 16;
-  static constexpr int P = 4;
-  static constexpr int BN = 256;
-  static constexpr int W = BN / P;  // 64 columns a thread
-  static constexpr int kAccBufs = 1;
-  static constexpr int kExtraCols = BN;
-  static constexpr bool kA3D = true;
-  static constexpr bool kBlocked = true;
-  // two (max, sum) exchange slots of 128 x P float4
-  static_assert(2 * 128 * P * 16 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
-  int B, N, C, Hq, G, dh, mtb;
-  float scale;
-  const float* A_prev;
-  float* A_cur;
-  float* D;
-  struct State {
-    uint32_t extra;
-  };
-  __device__ int tiles(int) const { return B * mtb * Hq; }
-  __device__ int arow(int t) const {
-    const int bm = t / Hq;
-    return (bm / mtb) * N + (bm % mtb) * 128;
-  }
-  __device__ int ahead(int t) const { return t % Hq; }
-  __device__ int bcoord(int t, int) const { return (t / Hq / mtb) * C; }
-  __device__ int bkoff(int t) const { return ((t % Hq) / G) * dh; }
-
-  // the max and the sum of 2^(v sl - m) over 32 scores v (raw TMEM words),
-  // e = 2^(v sl - m) written back over them; n < 32: only the first n count
-  // (n >= 1), the others take e = 0.  m = sl * max v, as sl > 0.
-  template <bool kFull>
-  __device__ __forceinline__ void half_exp(uint32_t addr, int n, float sl, float& m,
-                                           float& sum) const {
-    uint32_t v[32];
-    tc::tmem_ld32_nowait(addr, v);
-    tc::tmem_wait_ld();
-    if constexpr (!kFull) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j >= n) v[j] = __float_as_uint(-INFINITY);
-    }
-    float mx[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      mx[j] = fmaxf(fmaxf(__uint_as_float(v[j]), __uint_as_float(v[j + 8])),
-                    fmaxf(__uint_as_float(v[j + 16]), __uint_as_float(v[j + 24])));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
-    m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
-    float sp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float e = ex2_approx(fmaf(__uint_as_float(v[j]), sl, -m));
-      sp[j & 3] += e;
-      v[j] = __float_as_uint(e);
-    }
-    sum = (sp[0] + sp[1]) + (sp[2] + sp[3]);
-    tc::tmem_st32(addr, v);
-  }
-
-  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
-                               State& st) const {
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float sl = scale * kLog2e;
-    const int h = t % Hq, c0 = q * W;
-    // pass 1, in two halves of 32 columns, each against its own max; a half
-    // past column C is left out (its max -inf, its weight 0)
-    float mh[2], sh[2];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const int n = C - (c0 + 32 * g);
-      mh[g] = -INFINITY;
-      sh[g] = 0.f;
-      if (n >= 32)
-        half_exp<true>(taddr + c0 + 32 * g, 32, sl, mh[g], sh[g]);
-      else if (n > 0)
-        half_exp<false>(taddr + c0 + 32 * g, n, sl, mh[g], sh[g]);
-    }
-    // the row's max and sum from the eight halves of the quarter, in order
-    float4* xs = reinterpret_cast<float4*>(scratch) + (h & 1) * 128 * P;
-    xs[r * P + q] = make_float4(mh[0], sh[0], mh[1], sh[1]);
-    epi_bar_sync_n<32 * kEpiWarps>();
-    float4 x[P];
-#pragma unroll
-    for (int k = 0; k < P; ++k) x[k] = xs[r * P + k];
-    float mr = fmaxf(fmaxf(x[0].x, x[0].z), fmaxf(x[1].x, x[1].z));
-#pragma unroll
-    for (int k = 2; k < P; ++k) mr = fmaxf(mr, fmaxf(x[k].x, x[k].z));
-    float sr = 0.f;
-#pragma unroll
-    for (int k = 0; k < P; ++k) {  // a left-out half adds 0 x 2^-inf = 0
-      sr = fmaf(x[k].y, ex2_approx(x[k].x - mr), sr);
-      sr = fmaf(x[k].w, ex2_approx(x[k].z - mr), sr);
-    }
-    const float rs = 1.0f / sr;
-    // columns at or past C of A are never read, so a left-out half's weight
-    // only has to be finite
-    float f[2];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) f[g] = mh[g] == -INFINITY ? 0.f : ex2_approx(mh[g] - mr) * rs;
-    tc::tmem_wait_st();
-    // pass 2: A += e f, 32 columns at a time (e and A read together)
-    const bool first = h == 0;
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      uint32_t e[32], a[32];
-      tc::tmem_ld32_nowait(taddr + c0 + 32 * g, e);
-      if (!first) tc::tmem_ld32_nowait(st.extra + c0 + 32 * g, a);
-      tc::tmem_wait_ld();
-      if (first) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(__uint_as_float(e[j]) * f[g]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          a[j] = __float_as_uint(fmaf(__uint_as_float(e[j]), f[g], __uint_as_float(a[j])));
-      }
-      tc::tmem_st32(st.extra + c0 + 32 * g, a);
-    }
-    tc::tmem_wait_st();
-    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
-  }
-
-  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
-    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
-    const bool live = i < N, prev = A_prev != nullptr;
-    const long row = (long)b * N + i;
-    const float hq = (float)Hq;
-    const int c0 = q * W;
-    float kl = 0.f;
-#pragma unroll 1
-    for (int k = 0; k < W; k += 8) {  // once per row tile: 8 columns at a time
-      uint32_t a[8];
-      tc::tmem_ld8_nowait(st.extra + c0 + k, a);  // warp-collective
-      tc::tmem_wait_ld();
-      if (!live) continue;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c0 + k + j;
-        if (c < C) {
-          const float av = __uint_as_float(a[j]) / hq;
-          A_cur[row * C + c] = av;
-          if (prev && av > 0.f) kl += av * logf(av / fmaxf(A_prev[row * C + c], 1e-30f));
-        }
-      }
-    }
-    // the exchange slot the previous head used: every thread has read it
-    // before this head's exchange barrier, and the next row tile's first
-    // exchange waits for this epilogue (single-buffered accumulator)
-    float* zs = xs + (Hq & 1) * 4 * 128 * P;
-    zs[r * P + q] = kl;
-    epi_bar_sync_n<32 * kEpiWarps>();
-    if (q == 0 && live) {
-      float sum = zs[r * P];
-#pragma unroll
-      for (int k = 1; k < P; ++k) sum += zs[r * P + k];
-      D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
-    }
-  }
-  __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
-};
-
-// Proxy epilogue for C in (128, 256] with one CTA per row tile taking all
 // its heads, a head's scores in two 128-column parts (two MMA tiles, each in
 // its own accumulator, double-buffered) and the head sum A (256 columns,
-// fp32) in the rest of TMEM.  P epilogue warps per TMEM lane quarter (4 P in
-// all), each taking W = 128 / P columns of each part of its 32 rows, in
-// chunks of 32 columns:
-//   part 0: per chunk the max m of its scores and e = 2^(s' - m), kept in
-//           registers, with their sum s, so the part's accumulator goes back
-//           to the MMA at once (the next head's part 0 is computed under the
-//           rest of this epilogue);
-//   part 1: the same, e written back over the scores;
-//   the P warps of a row exchange their chunks' (m, s) through shared
-//   memory once (fixed order): M = max m, S = sum s 2^(m - M); then
-//   A += e 2^(m - M) / S for every chunk (s' = score / sqrt(dh) in base 2).
+// fp32) in the rest of TMEM.  Eight epilogue warps, two per TMEM lane
+// quarter (so 168 registers a thread), each taking W = 64 columns of each
+// part of its 32 rows in two 32-column chunks:
+//   consume (either part): per chunk the max m of its scores and
+//           e = 2^(s' - m), kept in registers, with their sum s; the part's
+//           accumulator goes back to the MMA as soon as it returns, so the
+//           next head's MMAs run under the rest of this head's epilogue;
+//   tile_done after part 1: the two warps of a row exchange their chunks'
+//           (m, s) through shared memory once (fixed order): M = max m,
+//           S = sum s 2^(m - M); then A += e 2^(m - M) / S for every chunk
+//           (s' = score / sqrt(dh) in base 2).
 // After the row tile's last head: A / Hq, KL against A_prev, stores.  The
-// softmax terms are those of one pass over the row up to rounding.  With
-// P = 2 (8 epilogue warps, 10 in all) a thread has 168 registers, room for
-// part 0's terms next to one chunk of part 1's scores; with P = 4 it has 96.
-template <int P>
+// softmax terms are those of one pass over the row up to rounding.
 struct ProxyHalvesEpi : TcEpiBase {
+  static constexpr int P = 2;          // epilogue warps per lane quarter
   static constexpr int kEpiWarps = 4 * P;
   static constexpr int BN_T = 128;     // columns of a part (one MMA tile)
   static constexpr int W = BN_T / P;   // columns a thread takes of each part
@@ -927,7 +714,7 @@ struct ProxyHalvesEpi : TcEpiBase {
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   static_assert(W % 32 == 0, "32-column chunks");
-  // two exchange slots of 128 x P threads x 2 NCH (m, s) pairs
+  // two exchange slots of 128 x P threads x NCH float4 (m0, s0, m1, s1)
   static constexpr int kSlot = 128 * P * 4 * NCH;  // floats
   static_assert(2 * kSlot * 4 <= (int)TcCfg<BN_T, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb;
@@ -936,8 +723,8 @@ struct ProxyHalvesEpi : TcEpiBase {
   float* A_cur;
   float* D;
   struct State {
-    float e0[W];  // part 0's exponentials, each chunk against its own max
-    float m0[NCH], s0[NCH];
+    float e[2][W];  // each part's exponentials, each chunk against its own max
+    float m[2][NCH], s[2][NCH];
     uint32_t extra;
   };
   __device__ int tiles(int) const { return B * mtb * Hq * 2; }
@@ -977,110 +764,88 @@ struct ProxyHalvesEpi : TcEpiBase {
     sum = (sp[0] + sp[1]) + (sp[2] + sp[3]);
   }
 
-  __device__ void consume_part(int t, int r, int q, int, int, uint32_t taddr, uint8_t* scratch,
+  __device__ void consume_part(int t, int, int q, int, int, uint32_t taddr, uint8_t*,
                                State& st) const {
-    // the part as a constant, so that e0 stays in registers
+    // the part as a constant, so that State stays in registers
     if (t % 2 == 0)
-      part0(q, taddr, st);
+      part<0>(q, taddr, st);
     else
-      part1(t, r, q, taddr, scratch, st);
+      part<1>(q, taddr, st);
   }
 
-  __device__ __forceinline__ void part0(int q, uint32_t taddr, State& st) const {
+  template <int p>
+  __device__ __forceinline__ void part(int q, uint32_t taddr, State& st) const {
     constexpr float kLog2e = 1.4426950408889634f;
+    const float sl = scale * kLog2e;
     uint32_t v[W];
 #pragma unroll
     for (int k = 0; k < NCH; ++k) tc::tmem_ld32_nowait(taddr + q * W + 32 * k, v + 32 * k);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < NCH; ++k)  // C > 128: part 0 is whole
-      exp_chunk<true>(v + 32 * k, 32, scale * kLog2e, st.m0[k], st.s0[k]);
+    for (int k = 0; k < NCH; ++k) {
+      // columns p 128 + q W + 32 k ..; a chunk past column C is left out
+      // (max -inf, sum 0); part 0 is whole (C > 128)
+      const int n = p == 0 ? 32 : C - BN_T - q * W - 32 * k;
+      st.m[p][k] = -INFINITY;
+      st.s[p][k] = 0.f;
+      if (n >= 32)
+        exp_chunk<true>(v + 32 * k, 32, sl, st.m[p][k], st.s[p][k]);
+      else if (n > 0)
+        exp_chunk<false>(v + 32 * k, n, sl, st.m[p][k], st.s[p][k]);
+    }
 #pragma unroll
-    for (int j = 0; j < W; ++j) st.e0[j] = __uint_as_float(v[j]);
+    for (int j = 0; j < W; ++j) st.e[p][j] = __uint_as_float(v[j]);
   }
 
-  __device__ __forceinline__ void part1(int t, int r, int q, uint32_t taddr, uint8_t* scratch,
-                                        State& st) const {
-    constexpr float kLog2e = 1.4426950408889634f;
+  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t* scratch,
+                                 State& st) const {
+    if (t % 2 == 0) return;  // tile-uniform: after a head's part 1
     const int h = (t / 2) % Hq;
-    // part 1, a chunk at a time: columns 128 + q W + 32 k ..; a chunk past
-    // column C is left out (max -inf, weight 0)
-    float m1[NCH], s1[NCH];
-#pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-      const int n = C - BN_T - q * W - 32 * k;
-      m1[k] = -INFINITY;
-      s1[k] = 0.f;
-      if (n > 0) {
-        uint32_t v[32];
-        tc::tmem_ld32_nowait(taddr + q * W + 32 * k, v);
-        tc::tmem_wait_ld();
-        if (n >= 32)
-          exp_chunk<true>(v, 32, scale * kLog2e, m1[k], s1[k]);
-        else
-          exp_chunk<false>(v, n, scale * kLog2e, m1[k], s1[k]);
-        tc::tmem_st32(taddr + q * W + 32 * k, v);
-      }
-    }
     // the row's max and sum from the chunks of its P threads, in order
     float4* xs = reinterpret_cast<float4*>(reinterpret_cast<float*>(scratch) + (h & 1) * kSlot);
 #pragma unroll
     for (int k = 0; k < NCH; ++k)
-      xs[(r * P + q) * NCH + k] = make_float4(st.m0[k], st.s0[k], m1[k], s1[k]);
+      xs[(r * P + q) * NCH + k] = make_float4(st.m[0][k], st.s[0][k], st.m[1][k], st.s[1][k]);
     epi_bar_sync_n<32 * kEpiWarps>();
-    float4 x[P * NCH];
+    float mr = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < P * NCH; ++k) x[k] = xs[r * P * NCH + k];
-    float mr = fmaxf(x[0].x, x[0].z);
-#pragma unroll
-    for (int k = 1; k < P * NCH; ++k) mr = fmaxf(mr, fmaxf(x[k].x, x[k].z));
+    for (int k = 0; k < P * NCH; ++k) {
+      const float4 x = xs[r * P * NCH + k];
+      mr = fmaxf(mr, fmaxf(x.x, x.z));
+    }
     float sr = 0.f;
 #pragma unroll
     for (int k = 0; k < P * NCH; ++k) {  // a left-out chunk adds 0 x 2^-inf = 0
-      sr = fmaf(x[k].y, ex2_approx(x[k].x - mr), sr);
-      sr = fmaf(x[k].w, ex2_approx(x[k].z - mr), sr);
+      const float4 x = xs[r * P * NCH + k];
+      sr = fmaf(x.y, ex2_approx(x.x - mr), sr);
+      sr = fmaf(x.w, ex2_approx(x.z - mr), sr);
     }
     const float rs = 1.0f / sr;
     const bool first = h == 0;
-    const uint32_t a0 = st.extra + q * W, a1 = st.extra + BN_T + q * W;
 #pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-      const float f0 = ex2_approx(st.m0[k] - mr) * rs;
-      uint32_t a[32];
-      if (first) {
+    for (int p = 0; p < 2; ++p) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(st.e0[32 * k + j] * f0);
-      } else {
-        tc::tmem_ld32_nowait(a0 + 32 * k, a);
-        tc::tmem_wait_ld();
+      for (int k = 0; k < NCH; ++k) {
+        // columns at or past C of A are never read: a left-out chunk's
+        // weight only has to be finite
+        const float f = st.m[p][k] == -INFINITY ? 0.f : ex2_approx(st.m[p][k] - mr) * rs;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          a[j] = __float_as_uint(fmaf(st.e0[32 * k + j], f0, __uint_as_float(a[j])));
+        for (int hh = 0; hh < 32; hh += 16) {
+          const uint32_t at = st.extra + p * BN_T + q * W + 32 * k + hh;
+          uint32_t a[16];
+          if (first) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(st.e[p][32 * k + hh + j] * f);
+          } else {
+            tc::tmem_ld16_nowait(at, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              a[j] = __float_as_uint(fmaf(st.e[p][32 * k + hh + j], f, __uint_as_float(a[j])));
+          }
+          tc::tmem_st16(at, a);
+        }
       }
-      tc::tmem_st32(a0 + 32 * k, a);
-    }
-    // e0 is dead until the next part 0 writes it: constants need no registers
-#pragma unroll
-    for (int j = 0; j < W; ++j) st.e0[j] = 0.f;
-    tc::tmem_wait_st();  // part 1's terms written back before they are read
-#pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-      // columns at or past C of A are never read: a left-out chunk's weight
-      // only has to be finite
-      const float f1 = m1[k] == -INFINITY ? 0.f : ex2_approx(m1[k] - mr) * rs;
-      uint32_t e[32], a[32];
-      tc::tmem_ld32_nowait(taddr + q * W + 32 * k, e);
-      if (!first) tc::tmem_ld32_nowait(a1 + 32 * k, a);
-      tc::tmem_wait_ld();
-      if (first) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(__uint_as_float(e[j]) * f1);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          a[j] = __float_as_uint(fmaf(__uint_as_float(e[j]), f1, __uint_as_float(a[j])));
-      }
-      tc::tmem_st32(a1 + 32 * k, a);
     }
     tc::tmem_wait_st();
     if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
@@ -1113,7 +878,9 @@ struct ProxyHalvesEpi : TcEpiBase {
     }
     // the exchange slot the previous head used: every thread has read it
     // before this head's exchange barrier, and the next row tile's first
-    // exchange waits for this epilogue's part-1 accumulator
+    // exchange comes after every thread's part 1 of its first head, which
+    // the MMA computes only once this epilogue has handed back the part-1
+    // accumulator of this head
     float* zs = xs + (Hq & 1) * kSlot;
     zs[r * P + q] = kl;
     epi_bar_sync_n<32 * kEpiWarps>();
@@ -1124,7 +891,6 @@ struct ProxyHalvesEpi : TcEpiBase {
       D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
     }
   }
-  __device__ void tile_done_part(int, int, int, int, int, uint8_t*, State&) const {}
 };
 
 // Head slices of one row tile inside one thread-block cluster: CTA z runs
@@ -1364,42 +1130,22 @@ cudaError_t proxy_tc(const ProxyArgs& a, const TcPlan& p, cudaStream_t s) {
   // sum; 16 epilogue warps would get 96 and spill it)
   constexpr int P = BN > 64 ? 2 : 1;
   const float scale = (float)(1.0 / std::sqrt((double)a.dh));
-  if constexpr (BN == 256) {
-    if (p.nslice == 1) {  // a CTA per row tile, two 128-column parts, the head sum in TMEM
+  if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
+    if constexpr (BN == 256) {  // two 128-column parts
       TcMaps m2 = maps;
       if (!make_tmap_bf16_2d(&m2.b[0], w.khi, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
                              128) ||
           !make_tmap_bf16_2d(&m2.b[1], w.klo, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
                              128))
         return cudaErrorInvalidValue;
-      if (std::getenv("PS_PROXY_SOLO") != nullptr) {
-        ProxySoloEpi pe{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+      ProxyHalvesEpi he{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
                         a.A_cur, a.D};
-        return launch_tc_gemm<256, 1, 2, false>(maps, sh, pe, dim3(1, a.B * p.mtb, 1), s);
-      }
-      if (std::getenv("PS_PROXY_H4") != nullptr) {
-        ProxyHalvesEpi<4> he{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale,
-                             a.A_prev, a.A_cur, a.D};
-        return launch_tc_gemm<128, 1, 2, false>(m2, sh, he, dim3(1, a.B * p.mtb, 1), s);
-      }
-      ProxyHalvesEpi<2> he{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
-                           a.A_cur, a.D};
       return launch_tc_gemm<128, 1, 2, false>(m2, sh, he, dim3(1, a.B * p.mtb, 1), s);
+    } else {
+      ProxyTmemEpi<BN> te{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale, a.A_prev,
+                          a.A_cur, a.D};
+      return launch_tc_gemm<BN, 1, 2, false>(maps, sh, te, dim3(1, a.B * p.mtb, 1), s);
     }
-  }
-  if (p.nslice == 1) {  // a CTA per row tile, the head sum in TMEM
-    constexpr int NPp = BN > 128 ? 2 : 1;
-    constexpr int BNT = BN / NPp;
-    TcMaps m2 = maps;
-    if (NPp > 1 &&
-        (!make_tmap_bf16_2d(&m2.b[0], w.khi, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
-                            BNT) ||
-         !make_tmap_bf16_2d(&m2.b[1], w.klo, nkv, (uint64_t)a.B * a.C, (uint64_t)nkv * 2, 64,
-                            BNT)))
-      return cudaErrorInvalidValue;
-    ProxyTmemEpi<BNT, NPp> te{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, scale,
-                              a.A_prev, a.A_cur, a.D};
-    return launch_tc_gemm<BNT, 1, 2, false>(m2, sh, te, dim3(1, a.B * p.mtb, 1), s);
   }
   ProxyEpi<BN, P> epi{{}, a.B, a.N, a.C, a.Hq, a.Hq / a.Hkv, a.dh, p.mtb, p.hps, p.nslice,
                       scale, a.A_prev, a.A_cur, a.D};
