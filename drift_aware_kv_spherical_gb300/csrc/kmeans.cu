@@ -1080,9 +1080,12 @@ int scan_units(int B, int C, int S) {
   return (int)std::max(1L, std::min(8L, ctas / (8L * kSmTarget)));
 }
 
+// gated: an update pass of the faster Lloyd form, whose settled windows'
+// CTAs leave at once (the other scans give each CTA one cluster)
 template <typename T, bool FINAL, bool FUSED = false, typename... Args>
-cudaError_t launch_scan(const ScanPlan& p, int B, int C, cudaStream_t s, Args&&... args) {
-  const int U = scan_units(B, C, p.S);
+cudaError_t launch_scan(const ScanPlan& p, int B, int C, bool gated, cudaStream_t s,
+                        Args&&... args) {
+  const int U = gated && !FINAL ? scan_units(B, C, p.S) : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ceil_div(C, U), B, p.S);
   cfg.blockDim = dim3(p.threads);
@@ -1339,7 +1342,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
                        w.prev, a.rho, w.L, pass0_in_l ? nullptr : w.objp, p.ntile, a.obj,
                        a.iters + 1, a.status, s);
     if (e == cudaSuccess)
-      e = launch_scan<T, false, true>(sp, a.B, a.C, s, H, w.inv, w.prev, a.rho, a.N, a.d, a.C,
+      e = launch_scan<T, false, true>(sp, a.B, a.C, false, s,
+                                      H, w.inv, w.prev, a.rho, a.N, a.d, a.C,
                                       sp.W, a.mu, nullptr, nullptr, a.counts, a.chat, w.objp,
                                       p.ntile, nullptr, a.iters + 1, a.iters, a.assign,
                                       static_cast<const int32_t*>(nullptr),
@@ -1359,7 +1363,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     for (int t = 0; t <= a.iters; ++t) {
       cudaError_t e = pass_fast(t);
       if (e == cudaSuccess && t < a.iters)
-        e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
+        e = launch_scan<T, false>(sp, a.B, a.C, true, s,
+                                  H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
                                   sp.W, a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp,
                                   p.ntile, a.obj, a.iters + 1, t,
                                   static_cast<const int32_t*>(nullptr),
@@ -1368,7 +1373,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     launch_pdl(k_km_rho, std::min(ceil_div(BN_ * 32, 256), 8 * kSmTarget), 256, 0, s, Hb,
                a.mu, BN_, a.N, a.d, a.C, a.assign, a.rho);
-    cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
+    cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, false, s,
+                                         H, w.inv, a.assign, a.rho, a.N, a.d,
                                          a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
                                          w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
                                          static_cast<const int32_t*>(nullptr),
@@ -1386,14 +1392,16 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     if (e != cudaSuccess) return e;
     if (t < a.iters)
-      e = launch_scan<T, false>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
+      e = launch_scan<T, false>(sp, a.B, a.C, false, s,
+                                H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
                                 sp.W, a.mu, p.tc ? w.mu_hi : nullptr, w.mu_lo, a.counts,
                                 a.chat, w.objp, p.ntile, a.obj, a.iters + 1, t,
                                 static_cast<const int32_t*>(nullptr),
                                 static_cast<const int32_t*>(nullptr), static_cast<float*>(nullptr));
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, s, H, w.inv, a.assign, a.rho, a.N, a.d,
+  cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, false, s,
+                                       H, w.inv, a.assign, a.rho, a.N, a.d,
                                        a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
                                        w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
                                        static_cast<const int32_t*>(nullptr),
