@@ -302,7 +302,7 @@ def measure_overlap(w, dev, reps=20):
     del L
     Q = wl.make_queries(w, H, Wq)
     u = wl.make_uniforms(w, 0, dev)
-    logits = wl.make_logits(w, 0, dev)
+    logits = wl.make_logits(w, 0, dev).to(wl.logits_dtype(w))
     pipe = Pipeline(w, layers=1, device=dev)
     pipe.step([H], [Q], [Wk], [Wv], logits, init_us=[u], first=True)
     sm, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -589,7 +589,9 @@ def run_reference(args):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]).float().numpy()[0] for H in Hs]
     Hn = [H.float().numpy()[0] for H in Hs]
-    logits = [wl.make_logits(w, t, B=1).numpy()[0] for t in range(4)]
+    # the logits as they arrive (bf16 values are exact in the oracle's fp64)
+    logits = [wl.make_logits(w, t, B=1).to(wl.logits_dtype(w)).float().numpy()[0]
+              for t in range(4)]
     u = wl.make_uniforms(w, B=1).numpy()[0]
     mu = oracle.kmeanspp_init(Hn[0], w.C, u)[0]
     st = dict(mu=mu, chat=None, A=None, s=np.zeros(w.P, np.float32),
@@ -660,7 +662,7 @@ def workload_config(w, layers=None):
     layers = w.layers if layers is None else layers
     return {"workload": w.name, "B": w.B, "N": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "dh": w.dh, "C": w.C, "iters": w.iters, "k": w.k, "P": w.P, "V": w.V,
-            "layers": layers, "logits": "f32",
+            "layers": layers, "logits": w.logits,
             "weights": "per layer (seeded per layer)",
             "l2": ("flushed between steps (512 MB write)" if layers == 1 else
                    "inputs larger than L2 (every layer's window and queries are read each "
@@ -693,7 +695,7 @@ def one_layer_inputs(w, dev):
     for t in range(1, 4):
         Hs.append(wl.drift_rows(w, Hs[-1], t))
     Qs = [wl.make_queries(w, H, L["Wq"]) for H in Hs]
-    logits = [wl.make_logits(w, t, dev) for t in range(4)]
+    logits = [wl.make_logits(w, t, dev).to(wl.logits_dtype(w)) for t in range(4)]
     return L, Hs, Qs, logits, wl.make_uniforms(w, 0, dev)
 
 
@@ -720,8 +722,8 @@ def bench_workload(w, layers, args, dev, world, local, trace_steps=None):
     torch.cuda.empty_cache()
     Hs, Qs = [x["H"] for x in ins], [x["Q"] for x in ins]
     Wks, Wvs, us = [x["Wk"] for x in ins], [x["Wv"] for x in ins], [x["u"] for x in ins]
-    # fp32 logits, as the workloads state them
-    logits = [wl.make_logits(w, t, dev) for t in range(2)]
+    # the logits in the dtype the workload states (else the model's own)
+    logits = [wl.make_logits(w, t, dev).to(wl.logits_dtype(w)) for t in range(2)]
     dL = torch.empty_like(logits[0])
     pipe = Pipeline(w, layers=layers, device=dev, offload=args.offload)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -1020,7 +1022,7 @@ def run_op(args):
     L = wl.make_layer(w, 0, dev)
     H, Wk, Wv = L["H"], L["Wk"], L["Wv"]
     Q = wl.make_queries(w, H, L["Wq"])
-    logits = wl.make_logits(w, 0, dev)
+    logits = wl.make_logits(w, 0, dev).to(wl.logits_dtype(w))
     pipe = Pipeline(w, layers=1, device=dev)
     st = pipe.state[0]
     g = torch.Generator(device=dev).manual_seed(7)

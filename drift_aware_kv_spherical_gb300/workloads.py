@@ -52,6 +52,8 @@ class Workload:
     alpha: float = 1.0
     ratio: float = 0.1
     walk: bool = False      # 32-layer loop: decaying random walk on all rows
+    logits: str = "f32"     # dtype the block's logits arrive in: "f32" where the
+                            # workload states it, else the model's own ("bf16")
     desc: str = field(default="", compare=False)
 
     @property
@@ -76,7 +78,7 @@ WORKLOADS = [
     Workload("llada8b_layer_n1024", 1, B=1, N=1024, d=4096, Hq=32, Hkv=32,
              dh=128, C=64, iters=10, k=8, P=32, V=126464, dtype="bf16",
              planted=64, noise=1.0, drift_frac=0.05, drift_std=0.5,
-             blk_start=512, logit_std=2.0, wq_std=0.02,
+             blk_start=512, logit_std=2.0, wq_std=0.02, logits="bf16",
              desc="LLaDA-8B-shaped layer, batch 1, window 1024"),
     Workload("dream7b_gqa_b8_n2048", 2, B=8, N=2048, d=3584, Hq=28, Hkv=4,
              dh=128, C=128, iters=10, k=12, P=32, V=152064, dtype="bf16",
@@ -87,7 +89,7 @@ WORKLOADS = [
              dh=128, C=64, iters=10, k=8, P=32, V=126464, dtype="bf16",
              planted=64, noise=1.0, drift_frac=1.0, drift_std=0.3,
              blk_start=512, logit_std=2.0, wq_std=0.02, layers=32,
-             mode=MODE_RATIO, ratio=0.1, walk=True,
+             mode=MODE_RATIO, ratio=0.1, walk=True, logits="bf16",
              desc="32-layer LLaDA-8B-shaped step loop, batch 4"),
     Workload("stress_b32_n4096_l32", 4, B=32, N=4096, d=4096, Hq=32, Hkv=32,
              dh=128, C=256, iters=15, k=16, P=64, V=126464, dtype="bf16",
@@ -188,6 +190,11 @@ def make_queries(w, H, Wq):
     else:
         Q = H.reshape(B * N, d).float() @ Wq.float()
     return Q.reshape(B, N, w.Hq, w.dh).to(H.dtype).contiguous()
+
+
+def logits_dtype(w):
+    """The dtype a workload's block logits arrive in."""
+    return torch.float32 if w.logits == "f32" else torch.bfloat16
 
 
 def make_uniforms(w, layer=0, device="cpu", B=None):

@@ -45,6 +45,6 @@ def test_refresh_and_commit_work_closed_forms():
 
 def test_workload_config_names_logits_and_flush():
     cfg = bench.workload_config(wl.BY_NAME["llada8b_layer_n1024"])
-    assert cfg["workload"] == "llada8b_layer_n1024" and cfg["logits"] == "f32"
+    assert cfg["workload"] == "llada8b_layer_n1024" and cfg["logits"] == "bf16"
     assert "flushed" in cfg["l2"]
     assert bench.L2_FLUSH_BYTES > 129 * 10**6      # larger than the GPU's L2
