@@ -599,7 +599,9 @@ k_km_recheck(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, 
 }
 
 // rho_i = <h_i, mu_{a_i}> in fp32 after the last pass, a warp per row (lanes
-// over d, summed in a fixed order).
+// over d, summed in a fixed order): steps of 128 elements, lane j taking
+// elements 4j .. 4j+3 of a step, so each warp load of h (8 bytes a lane)
+// and of mu (16 bytes a lane) is one contiguous run.
 __global__ void __launch_bounds__(256)
 k_km_rho(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, long rows, int N,
          int d, int C, const int32_t* __restrict__ assign, float* __restrict__ rho) {
@@ -614,20 +616,17 @@ k_km_rho(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, long
     const int c = min(max(assign[row], 0), C - 1);
     const float* m = mu + ((long)b * C + c) * d;
     float dot = 0.f;
-#pragma unroll 4
-    for (int k = lane * 8; k < d; k += 256) {
-      float hv[8];
-      load16(h + k, hv);
+#pragma unroll 8
+    for (int k = lane * 4; k < d; k += 128) {
+      const uint2 hw = __ldg(reinterpret_cast<const uint2*>(h + k));
+      float hv[4];
+      bf16x2_to_f32(hw.x, hv[0], hv[1]);
+      bf16x2_to_f32(hw.y, hv[2], hv[3]);
       const float4 m0 = *reinterpret_cast<const float4*>(m + k);
-      const float4 m1 = *reinterpret_cast<const float4*>(m + k + 4);
       dot = fmaf(hv[0], m0.x, dot);
       dot = fmaf(hv[1], m0.y, dot);
       dot = fmaf(hv[2], m0.z, dot);
       dot = fmaf(hv[3], m0.w, dot);
-      dot = fmaf(hv[4], m1.x, dot);
-      dot = fmaf(hv[5], m1.y, dot);
-      dot = fmaf(hv[6], m1.z, dot);
-      dot = fmaf(hv[7], m1.w, dot);
     }
     dot = warp_sum(dot);
     if (lane == 0) rho[row] = dot;

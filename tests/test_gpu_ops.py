@@ -264,6 +264,47 @@ def test_nvfp4_e4m3_scale_sweep():
     assert np.array_equal(codes[0], oc)
 
 
+def test_nvfp4_codes_at_boundaries_after_division():
+    """Blocks with scale s (E4M3 values that are not powers of two, S = 1)
+    whose elements are fl(m s) for m within a few ulp of every E2M1 midpoint
+    and grid point: the quotient r / s lands on or next to a rounding
+    boundary, where the kernel's reciprocal product must give way to the
+    IEEE division; every code against the oracle."""
+    marks = [0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.5, 3.0, 3.5, 4.0, 5.0]
+    ms = []
+    for mk in marks:
+        x = np.float32(mk)
+        for k in range(-2, 3):
+            v = x
+            for _ in range(abs(k)):
+                v = np.nextafter(v, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+            ms.append(v)
+    ms = np.array(ms, np.float32)               # 65 multipliers, 15 a block
+    scales_e4 = oracle.e4m3_decode(np.arange(1, 127)).astype(np.float32)
+    blocks = []
+    for sv in scales_e4:
+        for j in range(0, len(ms), 15):
+            blk = np.zeros(16, np.float32)
+            blk[0] = np.float32(6.0) * sv           # block max: scale code E4M3(s) = s
+            part = (ms[j:j + 15] * sv).astype(np.float32)
+            part[1::2] *= -1
+            blk[1:1 + len(part)] = part
+            blocks.append(blk)
+    body = np.stack(blocks)
+    per_row = 256 // 16
+    rows = math.ceil(len(body) / per_row)
+    H = np.zeros((rows * per_row, 16), np.float32)
+    H[:len(body)] = body
+    H = H.reshape(rows, 256)
+    H = np.concatenate([np.zeros((1, 256), np.float32), H])
+    H[0, 0] = 2688.0                            # the window amax: S = 1
+    codes, scales, S = run_nvfp4(torch.from_numpy(H[None]).cuda(), None, None, None)
+    oc, os_, oS, _ = oracle.nvfp4_residual(H, None, None, None)
+    assert S[0] == oS == 1.0
+    assert np.array_equal(scales[0], os_)
+    assert np.array_equal(codes[0], oc)
+
+
 def test_nvfp4_zero_and_bf16_input():
     z = torch.zeros(2, 3, 32, device="cuda", dtype=torch.bfloat16)
     codes, scales, S = run_nvfp4(z, None, None, None)
@@ -641,15 +682,18 @@ def test_commit_uniform_and_onehot_closed_forms():
     assert abs(g["conf"][0][1] - want) <= 1e-6 * want
 
 
-@pytest.mark.parametrize("C,Hq,Hkv", [(256, 4, 2), (200, 6, 3), (100, 2, 2), (256, 8, 8)])
-def test_proxy_row_tile_path_head_sum_in_tmem(C, Hq, Hkv):
-    """160 windows (160 row tiles: one CTA per tile takes all its heads, the
-    head sum kept in TMEM); C above 128 splits a head's columns in two
-    halves joined by the softmax's rescale (C = 200: a ragged second half).
-    With and without a previous distribution, and KL of an identical step
-    exactly 0."""
-    rng = np.random.default_rng(C + Hq)
-    B, N, dh, d = 160, 70, 64, 128
+@pytest.mark.parametrize("C,Hq,Hkv,B,N", [(256, 4, 2, 160, 70), (200, 6, 3, 160, 70),
+                                           (100, 2, 2, 160, 70), (256, 8, 8, 160, 70),
+                                           (200, 4, 2, 80, 250), (256, 2, 1, 78, 256)])
+def test_proxy_row_tile_path_head_sum_in_tmem(C, Hq, Hkv, B, N):
+    """At least 152 row tiles (one CTA per tile takes all its heads, the head
+    sum kept in TMEM); C above 128 splits a head's columns in two halves
+    joined by the softmax's rescale (C = 200: a ragged second half); two row
+    tiles per window (N = 250: the second ragged) and a shared KV head
+    (Hkv = 1).  With and without a previous distribution, and KL of an
+    identical step exactly 0."""
+    rng = np.random.default_rng(C + Hq + N)
+    dh, d = 64, 128
     Q = torch.from_numpy(rng.standard_normal((B, N, Hq, dh)).astype(np.float32) * 2)
     Q = Q.to(torch.bfloat16).cuda()
     chat = torch.from_numpy(rng.standard_normal((B, C, d)).astype(np.float32)).cuda()
