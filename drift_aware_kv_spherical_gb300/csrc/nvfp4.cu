@@ -15,8 +15,17 @@
 // order (CTA g: units g, g + G, ...), so the CTAs work on one or two windows
 // at a time and those windows' fp32 centroids, read once per element, stay
 // in L2.  A warp takes a row: its label, rho and centroid row are looked up
-// once, and lane j takes the row's 16-element blocks j, j + 32, ..., so every
-// block's loads are independent of the others.
+// once.  k_fp4_amax takes the row in steps of 128 elements, lane j taking
+// elements 4j .. 4j+3 of a step, so every warp load is one contiguous run
+// (256 bytes of bf16 h, 512 of fp32 mu); k_fp4_quant gives lane j the row's
+// 16-element blocks j, j + 32, ..., so a block's scale and its eight code
+// bytes come from one lane (the quad layout measured slower there: its
+// 2-byte code stores and per-quad scale work).
+// The quantiser divides r by the block's d = s_blk * S as r * RN(1/d), and
+// falls back to the IEEE division where that could change the code: the
+// product lies within 3 * 2^-24 relative of RN(r / d) (two roundings and
+// the reciprocal's), so when the E2M1 conversion takes the same code at
+// q (1 - 2^-20) and q (1 + 2^-20) that is the code of RN(r / d) too.
 // The residual r = fl(h - fl(rho * mu_a)) is recomputed in the second kernel
 // instead of being stored: re-reading h costs 2 B/element (bf16), storing r
 // would cost 8.
@@ -63,6 +72,50 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   const uint32_t e = (c >> 3) & 15u, m = c & 7u;
   if (e == 0) return (float)m * 0.001953125f;
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Four consecutive elements of a row (8- or 16-byte aligned) as fp32.
+__device__ __forceinline__ void load4(const float* p, float* out) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  bf16x2_to_f32(v.x, out[0], out[1]);
+  bf16x2_to_f32(v.y, out[2], out[3]);
+}
+
+// r[0..3] = fl(h - fl(rho * mu)) of four elements (m == nullptr: r = h).
+template <typename T>
+__device__ __forceinline__ void residual4(const T* __restrict__ h, const float* __restrict__ m,
+                                          float rh, float* r) {
+  load4(h, r);
+  if (m != nullptr) {
+    float mv[4];
+    load4(m, mv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) r[e] = __fsub_rn(r[e], __fmul_rn(rh, mv[e]));
+  }
+}
+
+// The codes of x[0..7] / den (four bytes, element 2j in the low nibble of
+// byte j), with rinv = RN(1 / den) finite: the product path where both
+// ends of its error band convert alike, else the IEEE division.
+__device__ __forceinline__ uint32_t e2m1_div8(const float* x, float den, float rinv) {
+  constexpr float kLo = 1.0f - 0x1p-20f, kHi = 1.0f + 0x1p-20f;
+  float lo[8], hi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float q = __fmul_rn(x[e], rinv);
+    lo[e] = __fmul_rn(q, kLo);
+    hi[e] = __fmul_rn(q, kHi);
+  }
+  const uint32_t a = e2m1x8(lo), b = e2m1x8(hi);
+  if (a == b) return a;
+  float v[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(x[e], den);
+  return e2m1x8(v);
 }
 
 // r[0..15] of the block at h (16 elements of a row) against the matching 16
@@ -126,7 +179,6 @@ k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
   pdl_prologue();
   __shared__ float s_red[kThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int bpr = d / 16;
   const long units = (long)B * gx;
   for (long u = blockIdx.x; u < units; u += gridDim.x) {  // CTA-uniform
     const int b = (int)(u / gx);
@@ -137,12 +189,12 @@ k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
       float rh;
       const float* mrow = row_centroid(mu, assign, rho, b, N, d, C, row, &rh);
       const T* hrow = H + ((long)b * N + row) * d;
-#pragma unroll 2
-      for (int k = lane; k < bpr; k += 32) {
-        float r[16];
-        residual16(hrow + k * 16, mrow != nullptr ? mrow + k * 16 : nullptr, rh, r);
+#pragma unroll 8
+      for (int c = 4 * lane; c < d; c += 128) {
+        float r[4];
+        residual4(hrow + c, mrow != nullptr ? mrow + c : nullptr, rh, r);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(r[e]));
+        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(r[e]));
       }
     }
     m = block_max(m, s_red);
@@ -150,7 +202,9 @@ k_fp4_amax(const T* __restrict__ H, const float* __restrict__ mu,
   }
 }
 
-// One 16-element block: its E4M3 scale and eight bytes of E2M1 codes.
+// One 16-element block: its E4M3 scale and eight bytes of E2M1 codes.  The
+// codes of r / den come from r * RN(1 / den) wherever that cannot change
+// them (e2m1_div8), else from the IEEE division.
 __device__ __forceinline__ void quant_block(const float* r, float S, float six_s,
                                             uint8_t* __restrict__ codes_at,
                                             uint8_t* __restrict__ scale_at) {
@@ -162,11 +216,17 @@ __device__ __forceinline__ void quant_block(const float* r, float S, float six_s
   uint2 q = make_uint2(0u, 0u);
   if (sb != 0.f) {
     const float den = __fmul_rn(sb, S);
-    float v[16];
+    if (den >= FLT_MIN) {
+      const float rinv = __frcp_rn(den);
+      q.x = e2m1_div8(r, den, rinv);
+      q.y = e2m1_div8(r + 8, den, rinv);
+    } else {
+      float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __fdiv_rn(r[e], den);
-    q.x = e2m1x8(v);
-    q.y = e2m1x8(v + 8);
+      for (int e = 0; e < 16; ++e) v[e] = __fdiv_rn(r[e], den);
+      q.x = e2m1x8(v);
+      q.y = e2m1x8(v + 8);
+    }
   }
   *reinterpret_cast<uint2*>(codes_at) = q;
   *scale_at = (uint8_t)sc;
