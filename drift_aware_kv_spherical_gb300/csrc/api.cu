@@ -120,10 +120,13 @@ ps_status ps_create(int device, ps_handle* out) {
   h->num_sms = prop.multiProcessorCount;
   h->status = nullptr;
   h->trace = nullptr;
+  h->aux = nullptr;
   e = cudaMalloc(&h->status, 16);
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     if (h->status) cudaFree(h->status);
+    if (h->aux) cudaStreamDestroy(h->aux);
     delete h;
     return launch_status(e);
   }
@@ -138,6 +141,7 @@ ps_status ps_destroy(ps_handle h) {
     delete h->trace;
   }
   cudaFree(h->status);
+  if (h->aux) cudaStreamDestroy(h->aux);
   delete h;
   return PS_OK;
 }
@@ -239,7 +243,7 @@ ps_status ps_kmeans_spherical(ps_handle h, const void* H, int dtype, int B,
   ps_status st = check_ws(kmeans_ws(B, N, d, C), ws, ws_bytes);
   if (st != PS_OK) return st;
   KmeansArgs a{H, dtype, B, N, d, C, iters, init_mode, init_u, mu, assign, rho,
-               chat, counts, objective, ws, h->status, h->num_sms};
+               chat, counts, objective, ws, h->status, h->num_sms, h->aux};
   return launch_status(kmeans_run(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -18,6 +18,9 @@ struct ps_handle_s {
   int num_sms;
   int* status;  // device word: 0 ok, else a PS_ERR_* code set by a kernel
   ps::TraceSink* trace;  // non-null while ps_trace_enable is on
+  cudaStream_t aux;      // the library's own stream: captures the bodies of
+                         // conditional graph nodes while the caller's stream
+                         // is being captured
 };
 
 namespace ps {

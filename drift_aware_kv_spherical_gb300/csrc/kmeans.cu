@@ -1267,6 +1267,77 @@ bool kmeans_fast_disabled() {
   return off;
 }
 
+// Inside a stream capture, pass t >= 2 of the faster passes (with its
+// update) becomes the body of a conditional graph node: this kernel, just
+// before it, opens the node only if some window still runs pass t, so a
+// pass after every window has settled costs one small launch instead of
+// three (the assignment, the recheck and the update, all of whose CTAs
+// would only find their windows settled).
+__global__ void __launch_bounds__(256)
+k_km_gate(const int32_t* __restrict__ changed, int B, int t, cudaGraphConditionalHandle h) {
+  bool any = false;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) any = any || km_pass_active(changed, b, t);
+  any = __syncthreads_or(any) != 0;
+  if (threadIdx.x == 0) cudaGraphSetConditional(h, any ? 1u : 0u);
+}
+
+// The objectives of passes 2 .. I-1 that no window ran (their updates were
+// gated off): each repeats the pass before, which is what those updates
+// would have written (the fold of the same best scores).  One CTA, passes
+// in order.
+__global__ void __launch_bounds__(1024)
+k_km_obj_carry(const int32_t* __restrict__ changed, int B, int iters, float* __restrict__ obj,
+               int obj_ld) {
+  for (int t = 2; t < iters; ++t) {
+    bool any = false;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) any = any || km_pass_active(changed, b, t);
+    any = __syncthreads_or(any) != 0;
+    if (!any)
+      for (int b = threadIdx.x; b < B; b += blockDim.x)
+        obj[(long)b * obj_ld + t] = obj[(long)b * obj_ld + t - 1];
+    __syncthreads();
+  }
+}
+
+// While `s` is being captured into a graph: enqueue on `s` the gate for pass
+// t and a conditional node whose body `launch_body(stream)` enqueues (on
+// the handle's own stream `aux`, captured into the node's body graph).
+template <typename F>
+cudaError_t gated_pass(cudaStream_t s, cudaStream_t aux, const int32_t* changed, int B, int t,
+                       F&& launch_body) {
+  cudaStreamCaptureStatus cs;
+  cudaGraph_t g;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t nd = 0;
+  cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, nullptr, &g, &deps, nullptr, &nd);
+  if (e != cudaSuccess) return e;
+  cudaGraphConditionalHandle h;
+  e = cudaGraphConditionalHandleCreate(&h, g, 0u, 0u);
+  if (e != cudaSuccess) return e;
+  k_km_gate<<<1, 256, 0, s>>>(changed, B, t, h);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamGetCaptureInfo(s, &cs, nullptr, &g, &deps, nullptr, &nd);
+  if (e != cudaSuccess) return e;
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = h;
+  np.conditional.type = cudaGraphCondTypeIf;
+  np.conditional.size = 1;
+  cudaGraphNode_t node;
+  e = cudaGraphAddNode(&node, g, deps, nullptr, nd, &np);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamBeginCaptureToGraph(aux, np.conditional.phGraph_out[0], nullptr, nullptr, 0,
+                                    cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) return e;
+  cudaError_t eb = launch_body(aux);
+  cudaGraph_t body;
+  e = cudaStreamEndCapture(aux, &body);
+  if (eb != cudaSuccess) return eb;
+  if (e != cudaSuccess) return e;
+  return cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1,
+                                             cudaStreamSetCaptureDependencies);
+}
+
 template <typename T>
 cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   const T* H = static_cast<const T*>(a.H);
@@ -1351,23 +1422,39 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   }
   if (fast) {
     const auto* Hb = static_cast<const __nv_bfloat16*>(a.H);
-    auto pass_fast = [&](int t) {
+    auto pass_fast = [&](int t, cudaStream_t st) {
       switch (p.BN) {
-        case 32: return assign_fast<32>(a, p, w, t, s);
-        case 64: return assign_fast<64>(a, p, w, t, s);
-        case 128: return assign_fast<128>(a, p, w, t, s);
-        default: return assign_fast<256>(a, p, w, t, s);
+        case 32: return assign_fast<32>(a, p, w, t, st);
+        case 64: return assign_fast<64>(a, p, w, t, st);
+        case 128: return assign_fast<128>(a, p, w, t, st);
+        default: return assign_fast<256>(a, p, w, t, st);
       }
     };
+    // inside a capture, passes 2 .. I become conditional nodes (k_km_gate)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t ec = cudaStreamIsCapturing(s, &cs);
+    if (ec != cudaSuccess) return ec;
+    const bool gate = cs == cudaStreamCaptureStatusActive && a.aux != nullptr;
     for (int t = 0; t <= a.iters; ++t) {
-      cudaError_t e = pass_fast(t);
-      if (e == cudaSuccess && t < a.iters)
-        e = launch_scan<T, false>(sp, a.B, a.C, true, s,
-                                  H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
-                                  sp.W, a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp,
-                                  p.ntile, a.obj, a.iters + 1, t,
-                                  static_cast<const int32_t*>(nullptr),
-                                  static_cast<const int32_t*>(w.changed), w.emax);
+      auto pass_and_update = [&, t](cudaStream_t st) {
+        cudaError_t e = pass_fast(t, st);
+        if (e == cudaSuccess && t < a.iters)
+          e = launch_scan<T, false>(sp, a.B, a.C, true, st,
+                                    H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
+                                    sp.W, a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp,
+                                    p.ntile, a.obj, a.iters + 1, t,
+                                    static_cast<const int32_t*>(nullptr),
+                                    static_cast<const int32_t*>(w.changed), w.emax);
+        return e;
+      };
+      cudaError_t e = gate && t >= 2
+                          ? gated_pass(s, a.aux, w.changed, a.B, t, pass_and_update)
+                          : pass_and_update(s);
+      if (e != cudaSuccess) return e;
+    }
+    if (gate && a.obj != nullptr && a.iters > 2) {
+      k_km_obj_carry<<<1, 1024, 0, s>>>(w.changed, a.B, a.iters, a.obj, a.iters + 1);
+      cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
     launch_pdl(k_km_rho, std::min(ceil_div(BN_ * 32, 256), 8 * kSmTarget), 256, 0, s, Hb,

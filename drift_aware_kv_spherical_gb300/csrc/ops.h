@@ -11,6 +11,7 @@ struct KmeansArgs {
   const double* init_u;
   float* mu; int32_t* assign; float* rho; float* chat; int32_t* counts;
   float* obj; void* ws; int* status; int num_sms;
+  cudaStream_t aux;  // captures conditional-node bodies (the handle's own stream)
 };
 size_t kmeans_ws(int B, int N, int d, int C);
 cudaError_t kmeans_run(const KmeansArgs& a, cudaStream_t s);
