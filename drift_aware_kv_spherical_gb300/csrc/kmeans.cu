@@ -371,8 +371,9 @@ k_km_prep(const T* __restrict__ H, long rows, int d, float* __restrict__ inv, in
       const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
       *reinterpret_cast<uint2*>(hi + eh) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
                                                       *reinterpret_cast<const uint32_t*>(&h1));
-      *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
-                                                      *reinterpret_cast<const uint32_t*>(&l1));
+      if (lo != nullptr)  // the faster passes use the hi part only
+        *reinterpret_cast<uint2*>(lo + el) = make_uint2(*reinterpret_cast<const uint32_t*>(&l0),
+                                                        *reinterpret_cast<const uint32_t*>(&l1));
       e2 = fmaf(x.x - f0.x, x.x - f0.x, e2);
       e2 = fmaf(x.y - f0.y, x.y - f0.y, e2);
       e2 = fmaf(x.z - f1.x, x.z - f1.x, e2);
@@ -1008,11 +1009,13 @@ k_cluster_scan(int U, const T* __restrict__ H, const float* __restrict__ inv,
                 if constexpr (V == 8) {
                   *reinterpret_cast<uint4*>(mu_hi + ro + col) =
                       make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                  *reinterpret_cast<uint4*>(mu_lo + ro + col) =
-                      make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                  if (mu_lo != nullptr)  // the faster passes use the hi part only
+                    *reinterpret_cast<uint4*>(mu_lo + ro + col) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 } else {
                   *reinterpret_cast<uint2*>(mu_hi + ro + col) = make_uint2(hi[0], hi[1]);
-                  *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
+                  if (mu_lo != nullptr)
+                    *reinterpret_cast<uint2*>(mu_lo + ro + col) = make_uint2(lo[0], lo[1]);
                 }
               }
             } else if (FUSED && n_fin > 0) {
@@ -1369,6 +1372,7 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
   if (fast) {
     cudaError_t e = cudaMemsetAsync(w.changed, 0, w.flag_bytes, s);
     if (e != cudaSuccess) return e;
+    split_lo = nullptr;  // the faster passes score against the hi part alone
   }
   float* emax = fast ? w.emax : nullptr;
   launch_pdl(k_km_prep<T>, inv_blocks + (seeding ? 0 : split_blocks), 256, 0, s, H, BN_, a.d,
@@ -1441,7 +1445,8 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
         if (e == cudaSuccess && t < a.iters)
           e = launch_scan<T, false>(sp, a.B, a.C, true, st,
                                     H, w.inv, a.assign, a.rho, a.N, a.d, a.C,
-                                    sp.W, a.mu, w.mu_hi, w.mu_lo, a.counts, a.chat, w.objp,
+                                    sp.W, a.mu, w.mu_hi, static_cast<__nv_bfloat16*>(nullptr),
+                                    a.counts, a.chat, w.objp,
                                     p.ntile, a.obj, a.iters + 1, t,
                                     static_cast<const int32_t*>(nullptr),
                                     static_cast<const int32_t*>(w.changed), w.emax);
