@@ -784,10 +784,12 @@ k_km_argmax(const float* __restrict__ part, int nz, int B, int N, int C,
 // slice, times G (1 or 2) groups, so a member row costs one 16-byte load per
 // thread, and up to 16 (G = 1) or 4 (G = 2) member rows are loaded together.
 // Rows are scanned in blocks of 4096: the block's assignments are staged in
-// shared memory with 16-byte loads, every thread counts the members in its
+// shared memory with 16-byte loads (once for all of the CTA's clusters when
+// the window has at most 4096 rows), every thread counts the members in its
 // contiguous run of rows, one block scan places them, and the member list
 // sits in shared memory (over the staged assignments, which are all read
-// before the scan); 1/||h|| of a member is loaded with its row.
+// before the scan, in a longer window); 1/||h|| of a member is loaded with
+// its row.
 // Update pass: centroid = normalise(sum_i h_i/||h_i||) (kept when the cluster
 // is empty or its sum is zero), plus its bf16 split; the squared norm is the
 // sum of the slices' partials, read from each CTA's shared memory across the
@@ -813,6 +815,9 @@ k_cluster_scan(int U, const T* __restrict__ H, const float* __restrict__ inv,
   constexpr int V = Vec<T>::n;
   constexpr int kMemb = G == 1 ? 16 : 4;  // rows loaded together, within 64 registers
   __shared__ __align__(16) int list[kScanRows];  // staged assignments, then members
+  // a window of at most kScanRows rows: its assignments staged once for all
+  // of this CTA's clusters (the members then go to list)
+  __shared__ __align__(16) int lab[kScanRows];
   __shared__ int s_scan[32];
   __shared__ float s_red[32];
   __shared__ float s_ss;
@@ -840,6 +845,19 @@ k_cluster_scan(int U, const T* __restrict__ H, const float* __restrict__ inv,
     fold_objective();
     return;
   }
+  const bool whole = N <= kScanRows;
+  if (whole) {
+    const int32_t* ab = assign + (long)b * N;
+    if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
+      const int n4 = N >> 2;
+      for (int j = tid; j < n4; j += nthr)
+        reinterpret_cast<int4*>(lab)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
+      for (int j = (n4 << 2) + tid; j < N; j += nthr) lab[j] = __ldg(ab + j);
+    } else {
+      for (int j = tid; j < N; j += nthr) lab[j] = __ldg(ab + j);
+    }
+    __syncthreads();
+  }
 #pragma unroll 1
   for (int c = c_lo; c < c_hi; ++c) {
     {
@@ -853,22 +871,25 @@ k_cluster_scan(int U, const T* __restrict__ H, const float* __restrict__ inv,
       int n = 0;
       for (int base = 0; base < N; base += kScanRows) {
         const int len = min(kScanRows, N - base);
-        const int32_t* ab = assign + (long)b * N + base;
-        if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
-          const int n4 = len >> 2;
-          for (int j = tid; j < n4; j += nthr)
-            reinterpret_cast<int4*>(list)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
-          for (int j = (n4 << 2) + tid; j < len; j += nthr) list[j] = __ldg(ab + j);
-        } else {
-          for (int j = tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+        const int* src = whole ? lab : list;
+        if (!whole) {
+          const int32_t* ab = assign + (long)b * N + base;
+          if (((reinterpret_cast<uintptr_t>(ab)) & 15) == 0) {
+            const int n4 = len >> 2;
+            for (int j = tid; j < n4; j += nthr)
+              reinterpret_cast<int4*>(list)[j] = __ldg(reinterpret_cast<const int4*>(ab) + j);
+            for (int j = (n4 << 2) + tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+          } else {
+            for (int j = tid; j < len; j += nthr) list[j] = __ldg(ab + j);
+          }
+          __syncthreads();
         }
-        __syncthreads();
         const int R = (len + nthr - 1) / nthr;  // <= 64
         const int q0 = tid * R;
         unsigned long long hit = 0ull;
         int cnt = 0;
         for (int q = 0; q < R; ++q) {
-          if (q0 + q < len && list[q0 + q] == c) {
+          if (q0 + q < len && src[q0 + q] == c) {
             hit |= 1ull << q;
             ++cnt;
           }
@@ -1083,11 +1104,12 @@ int scan_units(int B, int C, int S) {
 }
 
 // gated: an update pass of the faster Lloyd form, whose settled windows'
-// CTAs leave at once (the other scans give each CTA one cluster)
+// CTAs leave at once; it and the final scan give a CTA several clusters of
+// one window (their labels staged once), the other updates one
 template <typename T, bool FINAL, bool FUSED = false, typename... Args>
 cudaError_t launch_scan(const ScanPlan& p, int B, int C, bool gated, cudaStream_t s,
                         Args&&... args) {
-  const int U = gated && !FINAL ? scan_units(B, C, p.S) : 1;
+  const int U = gated || FINAL ? scan_units(B, C, p.S) : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ceil_div(C, U), B, p.S);
   cfg.blockDim = dim3(p.threads);
