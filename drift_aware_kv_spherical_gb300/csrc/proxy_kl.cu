@@ -51,6 +51,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// log2(x) by the special-function unit's approximation (PTX
+// lg2.approx.ftz.f32: an absolute error near 2^-22 on [0.5, 2], a relative
+// error of a few ulp elsewhere)
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One KL term a ln(a / p) (a > 0), the log by lg2_approx: its error, at most
+// about 2^-22 a per term, keeps a row's KL within 2^-22 of the exact sum of
+// terms (the terms' weights a sum to 1).  An exact ratio of 1 gives exactly
+// 0, so KL(A || A) = 0.
+__device__ __forceinline__ float kl_term(float a, float p) {
+  constexpr float kLn2 = 0.69314718055994531f;
+  const float q = a / fmaxf(p, 1e-30f);
+  return q == 1.0f ? 0.f : a * (lg2_approx(q) * kLn2);
+}
+
 template <typename TW>
 __global__ void __launch_bounds__(256)
 k_ckeys(const float* __restrict__ chat, const TW* __restrict__ Wk, int M,
@@ -342,7 +361,8 @@ struct CkeysClusterEpi : CkeysEpi<BN> {
 // epilogue warps of a TMEM lane quarter each take W = BN / P columns of the
 // row and combine their partial max and sum through shared memory (scratch:
 // two head slots of [max | sum][128 rows][P], then KL partials [128][P]).
-// After the slice's last head (one slice per tile): A / Hq, KL, store.
+// The thread-block cluster of a row tile's slices then sums A in slice
+// order, divides by Hq and takes KL (ProxyClusterEpi).
 template <int BN, int P>
 struct ProxyEpi : TcEpiBase {
   static constexpr int kEpiWarps = 4 * P;
@@ -353,8 +373,8 @@ struct ProxyEpi : TcEpiBase {
   static constexpr bool kReread = W > 64 || P >= 2;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
-  // two (max, sum) exchange slots of 2 x 128 x P floats, then 128 x P for KL
-  static_assert(5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
+  // two (max, sum) exchange slots of 2 x 128 x P floats
+  static_assert(4 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb, hps, nslice;
   float scale;
   const float* A_prev;
@@ -498,56 +518,92 @@ struct ProxyEpi : TcEpiBase {
       for (int c = 0; c < W; ++c) st.A[c] = fmaf(e[c], rs, st.A[c]);
     }
   }
-  // After the slice's last head: A / Hq, the KL terms of this thread's
-  // columns, the row's KL from the P partials (part order).
-  __device__ void finish(int t, int r, int part, float* xs, const State& st) const {
-    const int h = t % Hq;
-    if ((h + 1) % hps != 0 && h + 1 != Hq) return;  // tile-uniform
-    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
-    const bool live = i < N, prev = A_prev != nullptr;
-    const long row = (long)b * N + i;
-    const float hq = (float)Hq;
-    const int c0 = part * W;
-    float kl = 0.f;
-    if (live) {
+};
+
+// The last step of a row tile whose head sum A / Hq has been staged in
+// shared memory, T[r ldT + c] (nrow rows of C <= 32 kJ columns): warp ew of
+// E writes rows ew, ew + E, ... to A_cur and takes their KL against A_prev,
+// lane j over columns j, j + 32, ... (every warp access one contiguous run
+// of a row), then a fixed shuffle tree; D = max(KL, 0), or 0 without a
+// previous distribution.  kR rows at a time, all of their A_prev loads
+// issued before any is used.
+template <int kJ, int kR = 6>
+__device__ __forceinline__ void proxy_rows_out(const float* T, int ldT, int nrow, int C,
+                                               long row0, int ew, int E,
+                                               const float* __restrict__ A_prev,
+                                               float* __restrict__ A_cur,
+                                               float* __restrict__ D) {
+  const int lane = threadIdx.x & 31;
+  const bool prev = A_prev != nullptr;
+  for (int r = ew; r < nrow; r += kR * E) {
+    float pv[kR][kJ];
 #pragma unroll
-      for (int c = 0; c < W; ++c) {
-        if (c0 + c < C) {
-          const float a = st.A[c] / hq;
-          A_cur[row * C + c0 + c] = a;
-          if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c0 + c], 1e-30f));
+    for (int u = 0; u < kR; ++u)
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int c = lane + 32 * j, ru = r + u * E;
+        pv[u][j] = prev && ru < nrow && c < C ? __ldg(A_prev + (row0 + ru) * C + c) : 1.f;
+      }
+#pragma unroll
+    for (int u = 0; u < kR; ++u) {
+      const int ru = r + u * E;
+      if (ru >= nrow) break;  // warp-uniform
+      const long g = (row0 + ru) * C;
+      float kl = 0.f;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int c = lane + 32 * j;
+        if (c < C) {
+          const float av = T[ru * ldT + c];
+          A_cur[g + c] = av;
+          if (prev && av > 0.f) kl += kl_term(av, pv[u][j]);
         }
       }
+      kl = warp_sum(kl);
+      if (lane == 0) D[row0 + ru] = prev ? fmaxf(kl, 0.f) : 0.f;
     }
-    if constexpr (P > 1) {
-      float* zs = xs + 4 * 128 * P;
-      zs[r * P + part] = kl;
-      epi_bar_sync_n<128 * P>();
-      if (part == 0 && live) {
-        float sum = zs[r * P];
+  }
+}
+
+// Row stride (floats) of the staged A: C rounded up to 8, plus 4, so that the
+// 16-byte stores of 8 consecutive rows at one column fall in distinct banks.
+__host__ __device__ constexpr int proxy_stage_ld(int C) { return ((C + 7) & ~7) + 4; }
+
+// The previous distributions of a row tile (nrow rows of C floats from row
+// row0, one contiguous block) into L2 ahead of their use: the 16-byte
+// aligned part of the block, by one thread.
+__device__ __forceinline__ void proxy_prefetch_prev(const float* A_prev, long row0, int nrow,
+                                                    int C) {
+  if (A_prev == nullptr || nrow <= 0) return;
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(A_prev + row0 * C);
+  const uintptr_t b1 = reinterpret_cast<uintptr_t>(A_prev + (row0 + nrow) * C);
+  const uintptr_t a0 = (b0 + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t a1 = b1 & ~static_cast<uintptr_t>(15);
+  if (a1 > a0) tc::bulk_prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+}
+
+// A thread's n (a multiple of 4) consecutive head-sum columns from c0 on,
+// times inv = RN(1 / Hq) (A / Hq exactly when Hq is a power of two, else
+// within an ulp), into row r of the staged tile; columns at or past C are
+// left out.
+template <int n>
+__device__ __forceinline__ void proxy_stage_cols(float* T, int ldT, int r, int c0, int C,
+                                                 const uint32_t* a, float inv) {
+  static_assert(n % 4 == 0, "whole float4s");
 #pragma unroll
-        for (int q = 1; q < P; ++q) sum += zs[r * P + q];
-        D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
-      }
-    } else if (live) {
-      D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+  for (int j = 0; j < n; j += 4) {
+    const int c = c0 + j;
+    const float4 v = make_float4(__uint_as_float(a[j]) * inv, __uint_as_float(a[j + 1]) * inv,
+                                 __uint_as_float(a[j + 2]) * inv, __uint_as_float(a[j + 3]) * inv);
+    if (c + 4 <= C) {
+      *reinterpret_cast<float4*>(T + r * ldT + c) = v;
+    } else {
+      if (c < C) T[r * ldT + c] = v.x;
+      if (c + 1 < C) T[r * ldT + c + 1] = v.y;
+      if (c + 2 < C) T[r * ldT + c + 2] = v.z;
     }
   }
-  __device__ void consume(int t, int r, int, int, uint32_t taddr, State& st) const {
-    head(t, r, 0, taddr, nullptr, st);
-  }
-  __device__ void consume_part(int t, int r, int part, int, int, uint32_t taddr,
-                               uint8_t* scratch, State& st) const {
-    head(t, r, part, taddr, reinterpret_cast<float*>(scratch), st);
-  }
-  __device__ void tile_done(int t, int r, int, int, uint8_t*, State& st) const {
-    finish(t, r, 0, nullptr, st);
-  }
-  __device__ void tile_done_part(int t, int r, int part, int, int, uint8_t* scratch,
-                                 State& st) const {
-    finish(t, r, part, reinterpret_cast<float*>(scratch), st);
-  }
-};
+}
 
 // Proxy epilogue with the head sum in TMEM, for C <= 128 and one CTA per
 // row tile taking all its heads (enough row tiles to fill the GPU): the two
@@ -558,19 +614,22 @@ struct ProxyEpi : TcEpiBase {
 // e = 2^(s' - m) kept in registers, the row sum (s' = score / sqrt(dh) in
 // base 2).  tile_done(), which the engine calls once the accumulator is
 // handed back to the MMA, adds e / sum into A in TMEM, so the next head's
-// MMAs run under it; after the row tile's last head: A / Hq, KL against
-// A_prev, stores.
+// MMAs run under it; after the row tile's last head (after_tiles, every
+// warp of the CTA): A / Hq staged row-major in the idle stage ring, A_cur
+// stored and KL taken against A_prev (prefetched into L2 three heads
+// before) a row per warp.
 template <int BN>
 struct ProxyTmemEpi : TcEpiBase {
   static constexpr int kEpiWarps = 16;
   static constexpr int P = 4;            // epilogue warps per lane quarter
   static constexpr int W = BN / P;       // columns a thread takes
   static constexpr int kExtraCols = BN;
+  static constexpr bool kAfterTiles = true;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   static_assert(W % 8 == 0 && W <= 32, "part width");
-  // a (max, sum) exchange of 2 x 128 x P floats; KL at 4 x 128 x P
-  static_assert(5 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
+  // a (max, sum) exchange of 2 x 128 x P floats
+  static_assert(2 * 128 * P * 4 <= (int)TcCfg<BN, 1, 2, false>::kScratch, "scratch");
   int B, N, C, Hq, G, dh, mtb;
   float scale;
   const float* A_prev;
@@ -631,9 +690,12 @@ struct ProxyTmemEpi : TcEpiBase {
     st.s = row_combine<false>(s, xs + 128 * P, r, q);
   }
 
-  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t* scratch,
-                                 State& st) const {
+  __device__ void tile_done_part(int t, int r, int q, int, int, uint8_t*, State& st) const {
     const int h = t % Hq;
+    if (h == max(Hq - 3, 0) && r == 0 && q == 0) {  // A_prev needed three heads on
+      const int bm = t / Hq, i0 = (bm % mtb) * 128;
+      proxy_prefetch_prev(A_prev, (long)(bm / mtb) * N + i0, min(128, N - i0), C);
+    }
     const float f = 1.0f / st.s;
     const uint32_t at = st.extra + q * W;
 #pragma unroll
@@ -652,39 +714,39 @@ struct ProxyTmemEpi : TcEpiBase {
       tc::tmem_st8(at + k, a);
     }
     tc::tmem_wait_st();
-    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
   }
 
-  // A / Hq and the KL of the row: each thread its W columns, the four
-  // warps' KL partials summed in warp order
-  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
-    const int bm = t / Hq, b = bm / mtb, i = (bm % mtb) * 128 + r;
-    const bool live = i < N, prev = A_prev != nullptr;
-    const long row = (long)b * N + i;
-    const float hq = (float)Hq;
-    float kl = 0.f;
-    uint32_t raw[W];
-    if constexpr (W == 32) {
-      tc::tmem_ld32_nowait(st.extra + q * W, raw);
-    } else if constexpr (W == 16) {
-      tc::tmem_ld16_nowait(st.extra + q * W, raw);
-    } else {
-      tc::tmem_ld8_nowait(st.extra + q * W, raw);
-    }
-    tc::tmem_wait_ld();
-    if (live) {
-#pragma unroll
-      for (int j = 0; j < W; ++j) {
-        const int c = q * W + j;
-        if (c < C) {
-          const float a = __uint_as_float(raw[j]) / hq;
-          A_cur[row * C + c] = a;
-          if (prev && a > 0.f) kl += a * logf(a / fmaxf(A_prev[row * C + c], 1e-30f));
-        }
+  // After the CTA's tiles, every warp: the epilogue warps stage A / Hq from
+  // TMEM in the idle stage ring (row-major), then all warps store it and
+  // take the KL a row per warp (proxy_rows_out)
+  __device__ void after_tiles(int t_begin, uint32_t tmem) const {
+    constexpr int ldT = proxy_stage_ld(BN);
+    static_assert(128 * ldT * 4 <= (int)(TcCfg<BN, 1, 2, false>::kStages *
+                                          TcCfg<BN, 1, 2, false>::kStage), "staged A > ring");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bm = t_begin / Hq, b = bm / mtb, i0 = (bm % mtb) * 128;
+    float* T = reinterpret_cast<float*>(tc_ring_base());
+    if (warp >= 2) {
+      const int quarter = warp & 3, q = (warp - 2) >> 2;
+      const uint32_t at =
+          tmem + kAccBufs * BN + (static_cast<uint32_t>(quarter * 32) << 16) + q * W;
+      tc::fence_after_sync();
+      uint32_t raw[W];
+      if constexpr (W == 32) {
+        tc::tmem_ld32_nowait(at, raw);
+      } else if constexpr (W == 16) {
+        tc::tmem_ld16_nowait(at, raw);
+      } else {
+        tc::tmem_ld8_nowait(at, raw);
       }
+      tc::tmem_wait_ld();
+      proxy_stage_cols<W>(T, proxy_stage_ld(C), quarter * 32 + lane, q * W, C, raw,
+                          1.0f / (float)Hq);
     }
-    kl = row_combine<false>(kl, xs + 4 * 128 * P, r, q);
-    if (q == 0 && live) D[row] = prev ? fmaxf(kl, 0.f) : 0.f;
+    __syncthreads();
+    static_assert(BN % 32 == 0, "whole 32-column runs");
+    proxy_rows_out<BN / 32>(T, proxy_stage_ld(C), min(128, N - i0), C, (long)b * N + i0, warp,
+                            (int)(blockDim.x >> 5), A_prev, A_cur, D);
   }
 };
 
@@ -702,8 +764,11 @@ struct ProxyTmemEpi : TcEpiBase {
 //           (m, s) through shared memory once (fixed order): M = max m,
 //           S = sum s 2^(m - M); then A += e 2^(m - M) / S for every chunk
 //           (s' = score / sqrt(dh) in base 2).
-// After the row tile's last head: A / Hq, KL against A_prev, stores.  The
-// softmax terms are those of one pass over the row up to rounding.
+// After the row tile's last head (after_tiles, every warp of the CTA): A / Hq
+// staged row-major in the idle stage ring, then A_cur stored and KL taken
+// against A_prev a row per warp, both with contiguous warp accesses; A_prev
+// is prefetched into L2 three heads before.  The softmax terms are those of
+// one pass over the row up to rounding.
 struct ProxyHalvesEpi : TcEpiBase {
   static constexpr int P = 2;          // epilogue warps per lane quarter
   static constexpr int kEpiWarps = 4 * P;
@@ -711,6 +776,7 @@ struct ProxyHalvesEpi : TcEpiBase {
   static constexpr int W = BN_T / P;   // columns a thread takes of each part
   static constexpr int NCH = W / 32;   // 32-column chunks of a thread's part
   static constexpr int kExtraCols = 2 * BN_T;
+  static constexpr bool kAfterTiles = true;
   static constexpr bool kA3D = true;
   static constexpr bool kBlocked = true;
   static_assert(W % 32 == 0, "32-column chunks");
@@ -801,6 +867,10 @@ struct ProxyHalvesEpi : TcEpiBase {
                                  State& st) const {
     if (t % 2 == 0) return;  // tile-uniform: after a head's part 1
     const int h = (t / 2) % Hq;
+    if (h == max(Hq - 3, 0) && r == 0 && q == 0) {  // A_prev needed three heads on
+      const int bm = t / (Hq * 2), i0 = (bm % mtb) * 128;
+      proxy_prefetch_prev(A_prev, (long)(bm / mtb) * N + i0, min(128, N - i0), C);
+    }
     // the row's max and sum from the chunks of its P threads, in order
     float4* xs = reinterpret_cast<float4*>(reinterpret_cast<float*>(scratch) + (h & 1) * kSlot);
 #pragma unroll
@@ -848,48 +918,36 @@ struct ProxyHalvesEpi : TcEpiBase {
       }
     }
     tc::tmem_wait_st();
-    if (h == Hq - 1) finish(t, r, q, reinterpret_cast<float*>(scratch), st);
   }
 
-  // A / Hq and the KL of the row: each thread its W columns of each part,
-  // 8 at a time; the P warps' KL partials summed in warp order
-  __device__ void finish(int t, int r, int q, float* xs, const State& st) const {
-    const int bm = t / (Hq * 2), b = bm / mtb, i = (bm % mtb) * 128 + r;
-    const bool live = i < N, prev = A_prev != nullptr;
-    const long row = (long)b * N + i;
-    const float hq = (float)Hq;
-    float kl = 0.f;
+  // After the CTA's tiles, every warp: the epilogue warps stage A / Hq from
+  // TMEM in the idle stage ring (row-major), then all warps store it and
+  // take the KL a row per warp (proxy_rows_out)
+  __device__ void after_tiles(int t_begin, uint32_t tmem) const {
+    constexpr int ldT = proxy_stage_ld(2 * BN_T);
+    static_assert(128 * ldT * 4 <= (int)(TcCfg<BN_T, 1, 2, false>::kStages *
+                                          TcCfg<BN_T, 1, 2, false>::kStage), "staged A > ring");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bm = t_begin / (Hq * 2), b = bm / mtb, i0 = (bm % mtb) * 128;
+    float* T = reinterpret_cast<float*>(tc_ring_base());
+    const int ld = proxy_stage_ld(C);
+    if (warp >= 2) {
+      const int quarter = warp & 3, q = (warp - 2) >> 2;
+      const uint32_t extra = tmem + kAccBufs * BN_T + (static_cast<uint32_t>(quarter * 32) << 16);
+      tc::fence_after_sync();
 #pragma unroll 1
-    for (int k = 0; k < 2 * W; k += 8) {  // once per row tile
-      const int c0 = (k / W) * BN_T + q * W + k % W;
-      uint32_t a[8];
-      tc::tmem_ld8_nowait(st.extra + c0, a);  // warp-collective
-      tc::tmem_wait_ld();
-      if (!live) continue;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c0 + j;
-        if (c < C) {
-          const float av = __uint_as_float(a[j]) / hq;
-          A_cur[row * C + c] = av;
-          if (prev && av > 0.f) kl += av * logf(av / fmaxf(A_prev[row * C + c], 1e-30f));
-        }
+      for (int k = 0; k < 2 * W; k += 64) {  // 64 columns of one part at a time
+        const int c0 = (k / W) * BN_T + q * W + k % W;
+        uint32_t a[64];
+        tc::tmem_ld32_nowait(extra + c0, a);
+        tc::tmem_ld32_nowait(extra + c0 + 32, a + 32);
+        tc::tmem_wait_ld();
+        proxy_stage_cols<64>(T, ld, quarter * 32 + lane, c0, C, a, 1.0f / (float)Hq);
       }
     }
-    // the exchange slot the previous head used: every thread has read it
-    // before this head's exchange barrier, and the next row tile's first
-    // exchange comes after every thread's part 1 of its first head, which
-    // the MMA computes only once this epilogue has handed back the part-1
-    // accumulator of this head
-    float* zs = xs + (Hq & 1) * kSlot;
-    zs[r * P + q] = kl;
-    epi_bar_sync_n<32 * kEpiWarps>();
-    if (q == 0 && live) {
-      float sum = zs[r * P];
-#pragma unroll
-      for (int k = 1; k < P; ++k) sum += zs[r * P + k];
-      D[row] = prev ? fmaxf(sum, 0.f) : 0.f;
-    }
+    __syncthreads();
+    proxy_rows_out<2 * BN_T / 32>(T, ld, min(128, N - i0), C, (long)b * N + i0, warp,
+                                  (int)(blockDim.x >> 5), A_prev, A_cur, D);
   }
 };
 

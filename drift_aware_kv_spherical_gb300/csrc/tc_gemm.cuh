@@ -117,6 +117,11 @@ struct TcCfg {
 //        itself past the two accumulators (default 0); with it, State has a
 //        uint32_t `extra` that the engine sets to their address in the
 //        thread's lane quarter before the first tile
+//   static constexpr bool kAfterTiles, void after_tiles(int t_begin,
+//        uint32_t tmem)  optional: with kAfterTiles, every thread of the CTA
+//        calls after_tiles once all its tiles are done (after a CTA barrier,
+//        with the stage ring idle and TMEM, at address tmem, still
+//        allocated; warp w may read TMEM lane quarter w % 4)
 //   void prefetch(uint8_t* scratch, int i, int n)  optional: run by the n
 //        epilogue threads (index i) before they wait for the first
 //        accumulator, to stage data the epilogue reads later into the
@@ -139,6 +144,17 @@ __host__ __device__ constexpr uint32_t tc_tmem_cols() {
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 
+// The CTA's stage ring: the start of its dynamic shared memory, 1024-byte
+// aligned.  Once the accumulator of the CTA's last tile is full, every copy
+// into the ring has landed and every MMA that read it has completed, so the
+// epilogue may use the ring's Cfg::kStages * Cfg::kStage bytes from then on
+// (the last tile's consume / tile_done).
+__device__ __forceinline__ uint8_t* tc_ring_base() {
+  extern __shared__ uint8_t smem_raw[];
+  return reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
 template <int BN, int NA, int NB, bool B_MN, class Epi>
 __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& sh,
                                              const Epi& epi) {
@@ -148,9 +164,7 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
   constexpr int KS = tc_ks<BN, NA, NB, B_MN>();
   using Cfg = TcCfg<BN, NA, NB, B_MN, KS>;
   constexpr int S = Cfg::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = tc_ring_base();
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;      // [2]
@@ -391,6 +405,11 @@ __device__ __forceinline__ void tc_gemm_body(const TcMaps& maps, const TcShape& 
   // warp reaches the CTA barrier converged (the barrier is warp-aligned)
   __syncwarp();
   __syncthreads();
+  if constexpr (Epi::kAfterTiles) {
+    // skipped after a timed-out wait (the status word is set already)
+    if (t_begin < t_end && *abort_flag == 0) epi.after_tiles(t_begin, tmem);
+    __syncthreads();
+  }
   pdl_trigger();
   if constexpr (Epi::kClusterReduce) {
     static_assert(128 * Cfg::kRedLd * 4 <= Cfg::kStages * Cfg::kStage, "cluster result > ring");
@@ -416,6 +435,7 @@ struct TcEpiBase {
   static constexpr int kEpiWarps = 4;
   static constexpr int kExtraCols = 0;
   static constexpr int kAccBufs = 2;
+  static constexpr bool kAfterTiles = false;
   static constexpr bool kA3D = false;
   static constexpr bool kBlocked = false;
   static constexpr bool kClusterReduce = false;
@@ -423,6 +443,7 @@ struct TcEpiBase {
   __device__ bool tile_range(int, int*, int*, int*) const { return false; }
   __device__ bool active(int) const { return true; }
   __device__ void prefetch(uint8_t*, int, int) const {}
+  __device__ void after_tiles(int, uint32_t) const {}
   __device__ int ahead(int) const { return 0; }
   __device__ int bkoff(int) const { return 0; }
   __device__ int bsel(int, int) const { return 0; }
