@@ -215,6 +215,7 @@ def op_work(w, npos_mean):
 KERNEL_KEYS = [("GramClusterEpi", "gram_gemm"), ("k_km_gram", "kmeans_passes"),
                ("KmAssign", "kmeans_assign"), ("KmFastEpi", "kmeans_assign"),
                ("k_km_recheck", "kmeans_recheck"), ("k_km_rho", "kmeans_rho"),
+               ("k_km_fin_stats", "kmeans_fin_stats"), ("k_km_fin_chat", "kmeans_final"),
                ("k_km_argmax", "kmeans_argmax"),
                ("k_km_prep", "kmeans_prep"),
                ("k_kpp_gram", "kpp_gram"), ("k_kpp_pick", "kpp_pick"),
@@ -259,6 +260,7 @@ def kernel_work(key, w, npos_mean):
         "kmeans_assign": (H + B * C * d * 2, 2.0 * B * N * C * d),
         "kmeans_rho": (H + B * N * 8, 2.0 * B * N * d),
         "kmeans_update": (H + B * C * d * 4, 0.0),
+        "kmeans_fin_stats": (B * N * 12, 0.0),
         "kmeans_final": (B * N * 4 + 2 * B * C * d * 4, 0.0),
         "nvfp4_amax": (H, 0.0),
         "nvfp4_quant": (H + B * N * d // 2 + B * N * d // 16, 0.0),

@@ -46,6 +46,8 @@
 //     equal those of computing every pass.
 //   * rho exact.  k_km_rho takes rho_i = <h_i, mu_{a_i}> in fp32 after the
 //     last pass (the passes' best scores use bf16(mu)).
+//   * The last step (C_hat, counts, the last objective) from per-slice
+//     cluster statistics (k_km_fin_stats, k_km_fin_chat), no member lists.
 #include <algorithm>
 #include <climits>
 #include <type_traits>
@@ -634,6 +636,82 @@ k_km_rho(const __nv_bfloat16* __restrict__ H, const float* __restrict__ mu, long
   }
 }
 
+constexpr int kFinRows = 512;  // rows a CTA of k_km_fin_stats takes
+
+// The faster passes' last step, in two kernels instead of a member list per
+// (cluster, window).  k_km_fin_stats, CTA (slice, b): the labels and rho of
+// rows [slice kFinRows, ...) of window b staged in shared memory; thread c
+// counts the rows labelled c and sums their rho in ascending row order (a
+// label outside [0, C) counts for no cluster); the slice's objective terms
+// sum rho_i / ||h_i|| in a fixed order.
+__global__ void __launch_bounds__(256)
+k_km_fin_stats(const int32_t* __restrict__ assign, const float* __restrict__ rho,
+               const float* __restrict__ inv, int N, int C, int32_t* __restrict__ cnt_part,
+               float* __restrict__ rs_part, float* __restrict__ obj_part) {
+  pdl_prologue();
+  __shared__ int lab[kFinRows];
+  __shared__ float rr[kFinRows];
+  __shared__ float s_red[32];
+  const int b = blockIdx.y, sl = blockIdx.x, S = gridDim.x, t = threadIdx.x;
+  const int r0 = sl * kFinRows, len = min(kFinRows, N - r0);
+  const long base = (long)b * N + r0;
+  float so = 0.f;
+  for (int i = t; i < len; i += blockDim.x) {
+    lab[i] = assign[base + i];
+    const float rv = rho[base + i];
+    rr[i] = rv;
+    so = fmaf(rv, inv[base + i], so);
+  }
+  so = block_sum_f32(so, s_red);  // its barriers also publish lab and rr
+  if (t == 0) obj_part[(long)b * S + sl] = so;
+  for (int c = t; c < C; c += blockDim.x) {
+    int n = 0;
+    float rs = 0.f;
+    for (int i = 0; i < len; ++i)  // every thread reads the same word: a broadcast
+      if (lab[i] == c) {
+        rs += rr[i];
+        ++n;
+      }
+    cnt_part[((long)b * S + sl) * C + c] = n;
+    rs_part[((long)b * S + sl) * C + c] = rs;
+  }
+}
+
+// k_km_fin_chat, CTA (c, b): the count and the rho sum of cluster c over the
+// slices in slice order; C_hat_c = (sum / n) mu_c, a cluster left empty
+// keeping the caller's row; CTA (0, b) writes the pass objective, the
+// slices' terms in slice order.
+__global__ void __launch_bounds__(256)
+k_km_fin_chat(const int32_t* __restrict__ cnt_part, const float* __restrict__ rs_part,
+              const float* __restrict__ obj_part, int S, const float* __restrict__ mu, int d,
+              int C, int32_t* __restrict__ counts, float* __restrict__ chat,
+              float* __restrict__ obj, int obj_ld, int pass) {
+  pdl_prologue();
+  const int c = blockIdx.x, b = blockIdx.y;
+  int n = 0;
+  float rs = 0.f;
+  for (int sl = 0; sl < S; ++sl) {
+    n += cnt_part[((long)b * S + sl) * C + c];
+    rs += rs_part[((long)b * S + sl) * C + c];
+  }
+  if (threadIdx.x == 0) {
+    counts[(long)b * C + c] = n;
+    if (c == 0 && obj != nullptr) {
+      float o = 0.f;
+      for (int sl = 0; sl < S; ++sl) o += obj_part[(long)b * S + sl];
+      obj[(long)b * obj_ld + pass] = o;
+    }
+  }
+  if (n == 0) return;
+  const float mean = rs / (float)n;
+  const float4* m4 = reinterpret_cast<const float4*>(mu + ((long)b * C + c) * d);
+  float4* o4 = reinterpret_cast<float4*>(chat + ((long)b * C + c) * d);
+  for (int k = threadIdx.x; k < d / 4; k += blockDim.x) {
+    const float4 v = __ldg(m4 + k);
+    o4[k] = make_float4(mean * v.x, mean * v.y, mean * v.z, mean * v.w);
+  }
+}
+
 // Split assignment inside one thread-block cluster (nz <= 8 d-chunks, C <=
 // 128): each CTA leaves its chunk's 128 x C scores in shared memory; CTA z
 // then takes rows [128 z / nz, 128 (z+1) / nz) of the tile, one warp per row:
@@ -1191,7 +1269,13 @@ struct KmWs {
   int* rc_count;     // [kMaxPasses]
   size_t flag_bytes;
   RcEntry* rc_list;  // [B * N]
+  // faster passes' last step: per (window, slice) cluster statistics
+  int32_t* fin_cnt;  // [B][S][C]
+  float* fin_rs;     // [B][S][C]
+  float* fin_obj;    // [B][S]
 };
+
+inline int fin_slices(int N) { return (N + kFinRows - 1) / kFinRows; }
 
 KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int d, int C,
               size_t* bytes) {
@@ -1213,6 +1297,10 @@ KmWs km_carve(void* base, const KmPlan& p, const GramPlan& g, int B, int N, int 
       w.rc_count = w.changed ? w.changed + (size_t)B * kMaxPasses + B : nullptr;
       w.flag_bytes = nflag * sizeof(int32_t);
       w.rc_list = cv.take<RcEntry>((size_t)BN_);
+      const size_t nfs = (size_t)B * fin_slices(N);
+      w.fin_cnt = cv.take<int32_t>(nfs * C);
+      w.fin_rs = cv.take<float>(nfs * C);
+      w.fin_obj = cv.take<float>(nfs);
     }
   }
   if (g.ok) {
@@ -1486,14 +1574,15 @@ cudaError_t run_typed(const KmeansArgs& a, cudaStream_t s) {
     }
     launch_pdl(k_km_rho, std::min(ceil_div(BN_ * 32, 256), 8 * kSmTarget), 256, 0, s, Hb,
                a.mu, BN_, a.N, a.d, a.C, a.assign, a.rho);
-    cudaError_t e = launch_scan<T, true>(sp, a.B, a.C, false, s,
-                                         H, w.inv, a.assign, a.rho, a.N, a.d,
-                                         a.C, sp.W, a.mu, nullptr, nullptr, a.counts, a.chat,
-                                         w.objp, p.ntile, a.obj, a.iters + 1, a.iters,
-                                         static_cast<const int32_t*>(nullptr),
-                                         static_cast<const int32_t*>(w.changed),
-                                         static_cast<float*>(nullptr));
-    return e != cudaSuccess ? e : cudaGetLastError();
+    const int S = fin_slices(a.N);
+    launch_pdl(k_km_fin_stats, dim3(S, a.B), 256, 0, s, static_cast<const int32_t*>(a.assign),
+               static_cast<const float*>(a.rho), static_cast<const float*>(w.inv), a.N, a.C,
+               w.fin_cnt, w.fin_rs, w.fin_obj);
+    launch_pdl(k_km_fin_chat, dim3(a.C, a.B), 256, 0, s,
+               static_cast<const int32_t*>(w.fin_cnt), static_cast<const float*>(w.fin_rs),
+               static_cast<const float*>(w.fin_obj), S, static_cast<const float*>(a.mu), a.d,
+               a.C, a.counts, a.chat, a.obj, a.iters + 1, a.iters);
+    return cudaGetLastError();
   }
   for (int t = 0; t <= a.iters; ++t) {
     cudaError_t e = cudaSuccess;
