@@ -212,8 +212,11 @@ k_refresh(const T* __restrict__ H, const int32_t* __restrict__ pos,
 // [K | V] = X . [W_k | W_v] on tcgen05 with the weights streamed through TMA
 // as MN-major tiles, and a scatter epilogue into the cache rows.
 
-// One warp per selected row; block (x, b) covers rows 8x .. 8x+7 of window b.
-__global__ void __launch_bounds__(256)
+// One warp per selected row; block (x, b) takes rows 8x .. 8x+7 of window b,
+// then 8 gridDim.x further on, and so on (the grid is sized to about what
+// the GPU holds at once, as the selection's size is known only here).  A
+// lane copies 16 bytes of the row per step, eight steps' loads in flight.
+__global__ void __launch_bounds__(256, 4)
 k_gather_rows(const __nv_bfloat16* __restrict__ H, const int32_t* __restrict__ pos,
               const int32_t* __restrict__ npos, int B, int N, int d,
               __nv_bfloat16* __restrict__ X, int32_t* __restrict__ rowinfo,
@@ -228,15 +231,16 @@ k_gather_rows(const __nv_bfloat16* __restrict__ H, const int32_t* __restrict__ p
   }
   if (b == 0 && blockIdx.x == 0 && threadIdx.x == 0) *M_total = total;
   const int Mb = min(max(npos[b], 0), N);
-  const int j = blockIdx.x * 8 + warp;
-  if (j >= Mb) return;
-  const int p = pos[(long)b * N + j];
-  const bool valid = p >= 0 && p < N;
-  const uint4* src = reinterpret_cast<const uint4*>(H + ((long)b * N + (valid ? p : 0)) * d);
-  uint4* dst = reinterpret_cast<uint4*>(X + (long)(off + j) * d);
-  for (int c = lane; c < d / 8; c += 32)
-    dst[c] = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-  if (lane == 0) rowinfo[off + j] = valid ? b * N + p : -1;
+  for (int j = blockIdx.x * 8 + warp; j < Mb; j += gridDim.x * 8) {
+    const int p = pos[(long)b * N + j];
+    const bool valid = p >= 0 && p < N;
+    const uint4* src = reinterpret_cast<const uint4*>(H + ((long)b * N + (valid ? p : 0)) * d);
+    uint4* dst = reinterpret_cast<uint4*>(X + (long)(off + j) * d);
+#pragma unroll 8
+    for (int c = lane; c < d / 8; c += 32)
+      dst[c] = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) rowinfo[off + j] = valid ? b * N + p : -1;
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -375,7 +379,8 @@ cudaError_t refresh_tc(const RefreshArgs& a, const RefreshPlan& pl, cudaStream_t
   __nv_bfloat16* X = cv.take<__nv_bfloat16>((size_t)rows * a.d);
   int32_t* rowinfo = cv.take<int32_t>((size_t)rows);
   int32_t* M_total = cv.take<int32_t>(4);
-  launch_pdl(k_gather_rows, dim3(ceil_div(a.N, 8), a.B), 256, 0, s, 
+  const int gx = std::max(1, std::min(ceil_div(a.N, 8), ceil_div(8 * kSmTarget, a.B)));
+  launch_pdl(k_gather_rows, dim3(gx, a.B), 256, 0, s,
       static_cast<const __nv_bfloat16*>(a.H), a.pos, a.npos, a.B, a.N, a.d, X, rowinfo,
       M_total);
   TcMaps maps;
