@@ -206,7 +206,7 @@ def op_work(w, npos_mean):
                      2.0 * B * C * d * nkv + 2.0 * B * N * w.Hq * C * w.dh),
         "topk": (B * N * 13, 0.0),
         "refresh": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
-        "commit": (B * w.P * w.V * esz, 0.0),
+        "commit": (B * w.P * w.V * (2 if w.logits == "bf16" else 4), 0.0),
     }
 
 
@@ -270,7 +270,7 @@ def kernel_work(key, w, npos_mean):
         "topk": (B * N * 13, 0.0),
         "refresh_gather": (2 * M * d * esz, 0.0),
         "refresh_gemm": (2 * d * nkv * esz + M * d * esz + 2 * M * nkv * esz, 4.0 * M * d * nkv),
-        "commit_scan": (B * w.P * w.V * esz, 0.0),
+        "commit_scan": (B * w.P * w.V * (2 if w.logits == "bf16" else 4), 0.0),
     }.get(key)
 
 
