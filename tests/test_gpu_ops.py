@@ -684,14 +684,15 @@ def test_commit_uniform_and_onehot_closed_forms():
 
 @pytest.mark.parametrize("C,Hq,Hkv,B,N", [(256, 4, 2, 160, 70), (200, 6, 3, 160, 70),
                                            (100, 2, 2, 160, 70), (256, 8, 8, 160, 70),
-                                           (200, 4, 2, 80, 250), (256, 2, 1, 78, 256)])
+                                           (200, 4, 2, 80, 250), (256, 2, 1, 78, 256),
+                                           (64, 4, 4, 160, 70), (20, 2, 2, 80, 130)])
 def test_proxy_row_tile_path_head_sum_in_tmem(C, Hq, Hkv, B, N):
     """At least 152 row tiles (one CTA per tile takes all its heads, the head
     sum kept in TMEM); C above 128 splits a head's columns in two halves
     joined by the softmax's rescale (C = 200: a ragged second half); two row
-    tiles per window (N = 250: the second ragged) and a shared KV head
-    (Hkv = 1).  With and without a previous distribution, and KL of an
-    identical step exactly 0."""
+    tiles per window (N = 250 and 130: the second ragged) and a shared KV head
+    (Hkv = 1); 64- and 32-column score tiles (C = 64, 20).  With and without a
+    previous distribution, and KL of an identical step exactly 0."""
     rng = np.random.default_rng(C + Hq + N)
     dh, d = 64, 128
     Q = torch.from_numpy(rng.standard_normal((B, N, Hq, dh)).astype(np.float32) * 2)
