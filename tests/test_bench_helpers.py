@@ -25,6 +25,10 @@ def test_kernel_names_map_to_report_keys():
         "void ps::<unnamed>::k_fetch_dequant(...)": "offload_fetch",
         "_ZN2ps12_GLOBAL__N_114k_cluster_scanI13__nv_bfloat16Lb0ELb1ELb1EEEvv": "kmeans_update",
         "_ZN2ps12_GLOBAL__N_114k_cluster_scanI13__nv_bfloat16Lb1ELb0ELb0EEEvv": "kmeans_final",
+        "ps::<unnamed>::k_km_fin_stats(const int *, ...)": "kmeans_fin_stats",
+        "ps::<unnamed>::k_km_fin_chat(const int *, ...)": "kmeans_final",
+        "ps::<unnamed>::k_km_rho(const __nv_bfloat16 *, ...)": "kmeans_rho",
+        "ps::<unnamed>::k_gather_rows(const __nv_bfloat16 *, ...)": "refresh_gather",
     }
     for name, key in cases.items():
         assert bench.kernel_key(name) == key, name
@@ -40,6 +44,11 @@ def test_refresh_and_commit_work_closed_forms():
     assert bench.kernel_work("commit_scan", w, M)[0] == w.B * w.P * w.V * 2   # bf16 logits
     tiny = wl.BY_NAME["tiny_d256_n128"]
     assert bench.kernel_work("commit_scan", tiny, 1)[0] == tiny.B * tiny.P * tiny.V * 4
+    # bf16 windows with fp32 logits: the scan's bytes are the logits' own
+    st = wl.BY_NAME["stress_b32_n4096_l32"]
+    assert st.dtype == "bf16" and st.logits == "f32"
+    assert bench.kernel_work("commit_scan", st, 1)[0] == st.B * st.P * st.V * 4
+    assert bench.op_work(st, 1)["commit"][0] == st.B * st.P * st.V * 4
     assert bench.kernel_work("no_such_kernel", w, M) is None
 
 
