@@ -173,7 +173,11 @@ size_t ps_workspace_bytes(int op, int B, int N, int d, int C, int Hq, int Hkv,
  * chat     [B][C][d] f32 in/out  mean(rho of members) * mu_c; clusters left
  *          empty keep the caller's values
  * counts   [B][C] i32 out  cluster sizes
- * objective[B][I+1] f32 out (nullable)  sum_i cos(h_i, mu_{a_i}) per pass
+ * objective[B][I+1] f32 out (nullable)  sum_i cos(h_i, mu_{a_i}) per pass;
+ *          with the faster passes (bf16 windows, at least one 128-row tile per
+ *          SM) the passes before the last sum their bf16-centroid scores, each
+ *          within 2^-9 * N of the exact sum; the last pass's is exact up to
+ *          fp32 rounding
  * Empty clusters keep their centroid.  Rows of zero norm join cluster 0.
  *
  * Two forms compute the same passes.  bf16 windows of N <= 1024 rows with

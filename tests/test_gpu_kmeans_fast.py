@@ -57,7 +57,11 @@ def _check(g, Hn, mu0, iters, min_pinned=0.75, exact_ties=False):
         assert_close(g["mu"][b], o["mu"], what=f"mu {b}")
         assert_close(g["rho"][b], o["rho"], what=f"rho {b}")
         assert_close(g["chat"][b], o["chat"], what=f"chat {b}")
-        assert_close(g["obj"][b], o["obj"], what=f"objective {b}")
+        # the last pass's objective from the exact rho; the earlier ones from
+        # the passes' bf16-centroid scores, within 2^-9 N of the exact sums
+        assert_close(g["obj"][b][-1:], o["obj"][-1:], what=f"last objective {b}")
+        assert_close(g["obj"][b][:-1], o["obj"][:-1], atol=2.0 ** -9 * Hn.shape[1],
+                     what=f"objective {b}")
     assert pinned >= min_pinned * B, (pinned, B)
     return pinned
 
@@ -74,6 +78,21 @@ def test_fast_passes_match_oracle(B, N, d, C, iters, spread):
     mu0 = _seeds(Hn, C, seed=C)
     g = run_kmeans(H.cuda(), torch.from_numpy(mu0).cuda(), iters)
     _check(g, Hn, mu0, iters)
+
+
+@pytest.mark.parametrize("B,N,C", [(8, 4200, 16), (10, 4200, 256)])
+def test_fast_passes_long_windows(B, N, C):
+    """Windows past 4096 rows: the labels are not staged whole in the
+    updates, and the last step's statistics take nine 512-row slices.  C = 16
+    makes clusters of about 260 rows, C = 256 those of the stress workload.
+    At 4200 rows a window often holds a row within 1e-5 of a tie in some pass;
+    such windows are left out, and at least 40 % remain."""
+    d, iters = 64, 3
+    H = _planted(B, N, d, C, seed=B * 7 + C, spread=1.0)
+    Hn = H.float().numpy()
+    mu0 = _seeds(Hn, C, seed=C)
+    g = run_kmeans(H.cuda(), torch.from_numpy(mu0).cuda(), iters)
+    _check(g, Hn, mu0, iters, min_pinned=0.4)
 
 
 def test_fast_passes_warm_start_settles_early():
